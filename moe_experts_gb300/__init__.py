@@ -1,0 +1,10 @@
+"""epq: block-quantized decode kernels for GB300 (sm_103a).
+
+The compute lives in libepq.so (hand-written CUDA, C ABI in include/epq.h);
+this package only marshals torch tensors into that ABI.
+"""
+from ._lib import (  # noqa: F401
+    EPQ_Q8_0, EPQ_Q4_0, EPQ_Q4_1, EPQ_Q4_K, FORMATS, EpqError, declared_symbols, load,
+    epq_row_bytes, epq_block_weights, epq_block_bytes, epq_status_string, epq_device_error,
+    epq_quantize, epq_dequantize, epq_gemv, epq_gemv_ex,
+)

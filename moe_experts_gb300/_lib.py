@@ -1,0 +1,161 @@
+"""ctypes binding of libepq.so (include/epq.h): argument marshalling only.
+
+Every function here forwards to the C ABI of the same name.  Tensors are
+torch CUDA tensors; their device pointers and torch's current CUDA stream are
+passed through.  Output tensors that the caller does not supply are
+allocated with torch (device memory is torch's business; the library itself
+never allocates).  There is no fallback: if the shared library is missing or
+a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libepq.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "epq.h")
+
+EPQ_Q8_0, EPQ_Q4_0, EPQ_Q4_1, EPQ_Q4_K = 0, 1, 2, 3
+FORMATS = {"Q8_0": EPQ_Q8_0, "Q4_0": EPQ_Q4_0, "Q4_1": EPQ_Q4_1, "Q4_K": EPQ_Q4_K}
+
+_lib = None
+
+
+class EpqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _lib.epq_status_string(status).decode() if _lib else str(status)
+        extra = f" (cudaError {_lib.epq_last_cuda_error()})" if _lib and status == 6 else ""
+        super().__init__(f"{fn} failed: {msg}{extra}")
+        self.status = status
+
+
+class GemvOpts(ctypes.Structure):
+    _fields_ = [("residual", ctypes.c_void_p), ("rms_prenorm", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("swiglu", ctypes.c_int), ("x_group", ctypes.c_int), ("x_head_dim", ctypes.c_int)]
+
+
+def declared_symbols() -> list[str]:
+    """Every function the public header declares."""
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(epq_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(path: str | None = None):
+    """Load libepq.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with moe_experts_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    i64, vp, i32, f32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sig = {
+        "epq_status_string": (ctypes.c_char_p, [i32]),
+        "epq_last_cuda_error": (i32, []),
+        "epq_device_error": (i32, []),
+        "epq_block_weights": (i64, [i32]),
+        "epq_block_bytes": (i64, [i32]),
+        "epq_row_bytes": (i64, [i32, i64]),
+        "epq_quantize": (i32, [i32, vp, i64, i64, vp, vp]),
+        "epq_dequantize": (i32, [i32, vp, i64, i64, vp, vp]),
+        "epq_gemv": (i32, [i32, vp, vp, vp, i64, i64, i32, vp]),
+        "epq_gemv_ex": (i32, [i32, vp, vp, vp, i64, i64, i32, ctypes.POINTER(GemvOpts), vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise EpqError(fn, st)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+# ------------------------------------------------------------------ host-only queries
+def epq_row_bytes(fmt: int, cols: int) -> int:
+    return int(load().epq_row_bytes(fmt, cols))
+
+
+def epq_block_weights(fmt: int) -> int:
+    return int(load().epq_block_weights(fmt))
+
+
+def epq_block_bytes(fmt: int) -> int:
+    return int(load().epq_block_bytes(fmt))
+
+
+def epq_status_string(st: int) -> str:
+    return load().epq_status_string(st).decode()
+
+
+def epq_device_error() -> int:
+    return int(load().epq_device_error())
+
+
+# ------------------------------------------------------------------ packing
+def epq_quantize(fmt: int, W: torch.Tensor, blocks: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """W float32 [rows, cols] (CUDA) -> packed uint8 [rows, row_bytes]."""
+    lib = load()
+    rows, cols = W.shape
+    rb = lib.epq_row_bytes(fmt, cols)
+    if blocks is None:
+        blocks = torch.empty((rows, max(rb, 0)), dtype=torch.uint8, device=W.device)
+    _check("epq_quantize", lib.epq_quantize(fmt, _ptr(W), rows, cols, _ptr(blocks), _stream(stream)))
+    return blocks
+
+
+def epq_dequantize(fmt: int, blocks: torch.Tensor, rows: int, cols: int, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    lib = load()
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=blocks.device)
+    _check("epq_dequantize", lib.epq_dequantize(fmt, _ptr(blocks), rows, cols, _ptr(out), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ GEMV
+def epq_gemv(fmt: int, blocks: torch.Tensor, x: torch.Tensor, rows: int, cols: int, y: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """x float32 [nvec, cols] (or [cols]) -> y float32 [nvec, rows]."""
+    lib = load()
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    nvec = x2.shape[0]
+    if y is None:
+        y = torch.empty((nvec, rows), dtype=torch.float32, device=x.device)
+    _check("epq_gemv", lib.epq_gemv(fmt, _ptr(blocks), _ptr(x2), _ptr(y), rows, cols, nvec, _stream(stream)))
+    return y
+
+
+def epq_gemv_ex(fmt: int, blocks: torch.Tensor, x: torch.Tensor, rows: int, cols: int, y: torch.Tensor | None = None,
+                residual: torch.Tensor | None = None, rms_prenorm: bool = False, rms_eps: float = 0.0,
+                swiglu: bool = False, x_group: int = 0, x_head_dim: int = 0, stream=None) -> torch.Tensor:
+    lib = load()
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    nvec = x2.shape[0]
+    rows_out = rows // 2 if swiglu else rows
+    if y is None:
+        y = torch.empty((nvec, rows_out), dtype=torch.float32, device=x.device)
+    o = GemvOpts(residual.data_ptr() if residual is not None else None, int(rms_prenorm), float(rms_eps),
+                 int(swiglu), int(x_group), int(x_head_dim))
+    _check("epq_gemv_ex", lib.epq_gemv_ex(fmt, _ptr(blocks), _ptr(x2), _ptr(y), rows, cols, nvec,
+                                          ctypes.byref(o), _stream(stream)))
+    return y

@@ -1,0 +1,127 @@
+// Host-side plumbing of the C ABI: status strings, format sizes, the
+// per-device attribute cache and the device error word.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace epq {
+
+// One error word per device (a separate instance lives on every device that
+// loads the library).
+__device__ unsigned g_device_error = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+unsigned *g_err_slot[kMaxDevices] = {};
+thread_local int g_last_cuda_error = 0;
+}  // namespace
+
+bool current_device(DeviceInfo *out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_info[dev];
+  if (d.device != dev) {
+    DeviceInfo t;
+    t.device = dev;
+    if (cudaDeviceGetAttribute(&t.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&t.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    d = t;
+  }
+  *out = d;
+  return true;
+}
+
+unsigned *device_error_slot() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_slot[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_err_slot[dev] = static_cast<unsigned *>(p);
+  }
+  return g_err_slot[dev];
+}
+
+epq_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return EPQ_ERR_CUDA;
+}
+
+}  // namespace epq
+
+extern "C" {
+
+const char *epq_status_string(epq_status s) {
+  switch (s) {
+    case EPQ_OK: return "ok";
+    case EPQ_ERR_ARG: return "invalid argument";
+    case EPQ_ERR_FORMAT: return "unknown block format";
+    case EPQ_ERR_SHAPE: return "unsupported shape";
+    case EPQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case EPQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case EPQ_ERR_CUDA: return "CUDA runtime error";
+    case EPQ_ERR_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+int epq_last_cuda_error(void) { return epq::g_last_cuda_error; }
+
+int epq_device_error(void) {
+  unsigned *slot = epq::device_error_slot();
+  if (!slot) return -1;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(&v, epq::g_device_error, sizeof(v)) != cudaSuccess) return -1;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(epq::g_device_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+  return static_cast<int>(v);
+}
+
+int64_t epq_block_weights(epq_fmt fmt) {
+  switch (fmt) {
+    case EPQ_Q8_0:
+    case EPQ_Q4_0:
+    case EPQ_Q4_1: return 32;
+    case EPQ_Q4_K: return 256;
+  }
+  return -1;
+}
+
+int64_t epq_block_bytes(epq_fmt fmt) {
+  switch (fmt) {
+    case EPQ_Q8_0: return 34;
+    case EPQ_Q4_0: return 18;
+    case EPQ_Q4_1: return 20;
+    case EPQ_Q4_K: return 144;
+  }
+  return -1;
+}
+
+int64_t epq_row_bytes(epq_fmt fmt, int64_t cols) {
+  const int64_t bw = epq_block_weights(fmt);
+  if (bw < 0 || cols <= 0 || cols % bw) return -1;
+  return cols / bw * epq_block_bytes(fmt);
+}
+
+}  // extern "C"

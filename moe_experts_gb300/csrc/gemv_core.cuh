@@ -1,0 +1,191 @@
+// Dequant-GEMV engine: per-thread block-column arithmetic shared by the dense
+// GEMV and the expert kernels.
+//
+// Work split.  A row of `cols` weights is a run of nblk = cols/32 "columns"
+// of 32 weights (a Q8_0/Q4_0/Q4_1 block, or one Q4_K sub-block).  Thread c of
+// a row group owns column c for the whole kernel: it keeps the 32 activations
+// of that column in registers, pre-scaled, and only ever reads the packed
+// bytes of column c of each row from shared memory.
+//
+// Nibble -> float in one instruction.  The 32-bit pattern (n << 4p) read as
+// an IEEE float is the exact value n * 2^(4p - 149) (a subnormal or the
+// smallest normals, where the encoding is linear) for any bit position up to
+// 23.  So masking the packed word with 0xF << 4p yields the weight code as a
+// float that carries a known power of two; the activation it multiplies is
+// stored pre-multiplied by the inverse power, chosen so that every product
+// n * x * 2^(A - 149) is a normal float.  The two nibbles above bit 23 are
+// first shifted down by 16.  Codes of Q8_0 use the same trick on bytes after
+// an XOR with 0x80 (q + 128).  Products are accumulated with the packed
+// fma.rn.f32x2 (two IEEE fp32 FMAs per instruction, subnormals kept).
+//
+// Per-block scales and minima enter once per column:
+//   Q4_K  part = d*c * sum(n x) - dmin*k * sum(x)
+//   Q4_0  part = d * (sum(n x) - 8 sum(x))
+//   Q4_1  part = d * sum(n x) + m * sum(x)
+//   Q8_0  part = d * (sum((q+128) x) - 128 sum(x))
+// with sum(x) of the column precomputed once (in the same scaled units).
+#pragma once
+
+#include "common.cuh"
+
+namespace epq {
+
+template <int FMT>
+struct Fmt;
+
+// Shift (in bits) that each weight position of a 32-weight column carries
+// in its float pattern; x is stored as x * 2^(A - shift).
+template <>
+struct Fmt<EPQ_Q4_K> {
+  static constexpr int kBlockBytes = 144;
+  __device__ static constexpr int shift(int j) { return (j & 7) < 6 ? 4 * (j & 7) : 4 * ((j & 7) - 4); }
+};
+template <>
+struct Fmt<EPQ_Q4_0> {
+  static constexpr int kBlockBytes = 18;
+  __device__ static constexpr int shift(int j) { return (j & 7) < 6 ? 4 * (j & 7) : 4 * ((j & 7) - 4); }
+};
+template <>
+struct Fmt<EPQ_Q4_1> {
+  static constexpr int kBlockBytes = 20;
+  __device__ static constexpr int shift(int j) { return (j & 7) < 6 ? 4 * (j & 7) : 4 * ((j & 7) - 4); }
+};
+template <>
+struct Fmt<EPQ_Q8_0> {
+  static constexpr int kBlockBytes = 34;
+  __device__ static constexpr int shift(int j) { return (j & 3) == 3 ? 8 : 8 * (j & 3); }
+};
+
+__device__ __forceinline__ float fbits(uint32_t u) { return __uint_as_float(u); }
+
+// sum over one 32-bit word of 8 nibbles (weights 8i..8i+7) for NV vectors.
+template <int NV>
+__device__ __forceinline__ void nib_word(uint32_t w, const float (&xr)[NV][32], int i, float (&a)[NV][2]) {
+  const float f0 = fbits(w & 0x0000000Fu), f1 = fbits(w & 0x000000F0u);
+  const float f2 = fbits(w & 0x00000F00u), f3 = fbits(w & 0x0000F000u);
+  const float f4 = fbits(w & 0x000F0000u), f5 = fbits(w & 0x00F00000u);
+  const uint32_t h = w >> 16;
+  const float f6 = fbits(h & 0x00000F00u), f7 = fbits(h & 0x0000F000u);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    ffma2(a[v][0], a[v][1], f0, f1, xr[v][8 * i + 0], xr[v][8 * i + 1]);
+    ffma2(a[v][0], a[v][1], f2, f3, xr[v][8 * i + 2], xr[v][8 * i + 3]);
+    ffma2(a[v][0], a[v][1], f4, f5, xr[v][8 * i + 4], xr[v][8 * i + 5]);
+    ffma2(a[v][0], a[v][1], f6, f7, xr[v][8 * i + 6], xr[v][8 * i + 7]);
+  }
+}
+
+// sum over one 32-bit word of 4 int8 codes (weights 4i..4i+3), biased by 128.
+template <int NV>
+__device__ __forceinline__ void byte_word(uint32_t w, const float (&xr)[NV][32], int i, float (&a)[NV][2]) {
+  const uint32_t u = w ^ 0x80808080u;
+  const float f0 = fbits(u & 0x000000FFu), f1 = fbits(u & 0x0000FF00u);
+  const float f2 = fbits(u & 0x00FF0000u), f3 = fbits((u >> 16) & 0x0000FF00u);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    ffma2(a[v][0], a[v][1], f0, f1, xr[v][4 * i + 0], xr[v][4 * i + 1]);
+    ffma2(a[v][0], a[v][1], f2, f3, xr[v][4 * i + 2], xr[v][4 * i + 3]);
+  }
+}
+
+// Per-thread constants of one block column (independent of the row).
+template <int FMT>
+struct ColConst {
+  int off;        // byte offset of the column's block (or superblock header) in a row
+  int qoff;       // byte offset of the aligned word run holding the codes
+  int qsh;        // funnel shift (0 or 16) that realigns the code words
+  int csel, csh;  // Q4_K: scale-code word pair selector and shift
+  int ksel, ksh;  // Q4_K: min-code word pair selector and shift
+  __device__ void init(int c) {
+    if (FMT == EPQ_Q4_K) {
+      const int sb = c >> 3, s = c & 7;
+      off = sb * 144;
+      qoff = off + 16 + 16 * s;
+      qsh = 0;
+      const int pc = 6 * s;        // scale code bits in the 96-bit stream
+      csel = pc >= 32;
+      csh = pc & 31;
+      const int pk = 48 + 6 * s;   // min code bits
+      ksel = pk >= 64;
+      ksh = pk & 31;
+    } else {
+      const int bb = Fmt<FMT>::kBlockBytes;
+      off = c * bb;
+      const int q0 = off + (FMT == EPQ_Q4_1 ? 4 : 2);
+      qoff = q0 & ~3;
+      qsh = (q0 & 3) * 8;
+      csel = csh = ksel = ksh = 0;
+    }
+  }
+};
+
+// Partial dot product of one row's column for NV vectors, in scaled units.
+// `row` points at the row's packed bytes in shared memory; xs[v] is the
+// column's scaled activation sum sum(x) * 2^(A_v - 149).
+template <int FMT, int NV>
+__device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FMT> &cc, const float (&xr)[NV][32],
+                                           const float (&xs)[NV], float (&part)[NV]) {
+  float a[NV][2];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) a[v][0] = a[v][1] = 0.0f;
+  if (FMT == EPQ_Q4_K) {
+    const uint4 h = *reinterpret_cast<const uint4 *>(row + cc.off);
+    const uint4 q = *reinterpret_cast<const uint4 *>(row + cc.qoff);
+    nib_word<NV>(q.x, xr, 0, a);
+    nib_word<NV>(q.y, xr, 1, a);
+    nib_word<NV>(q.z, xr, 2, a);
+    nib_word<NV>(q.w, xr, 3, a);
+    const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+    const uint32_t c6 = __funnelshift_r(cc.csel ? h.z : h.y, cc.csel ? h.w : h.z, cc.csh) & 63u;
+    const uint32_t k6 = __funnelshift_r(cc.ksel ? h.w : h.z, cc.ksel ? 0u : h.w, cc.ksh) & 63u;
+    const float S = d * static_cast<float>(c6);
+    const float M = dmin * static_cast<float>(k6);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) part[v] = fmaf(S, a[v][0] + a[v][1], -M * xs[v]);
+  } else if (FMT == EPQ_Q4_1) {
+    const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
+    const uint32_t dm = *reinterpret_cast<const uint32_t *>(row + cc.off);
+    nib_word<NV>(wq[0], xr, 0, a);
+    nib_word<NV>(wq[1], xr, 1, a);
+    nib_word<NV>(wq[2], xr, 2, a);
+    nib_word<NV>(wq[3], xr, 3, a);
+    const float d = half_bits_to_float(dm), m = half_bits_to_float(dm >> 16);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) part[v] = fmaf(d, a[v][0] + a[v][1], m * xs[v]);
+  } else if (FMT == EPQ_Q4_0) {
+    const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
+    const uint32_t w0 = wq[0], w1 = wq[1], w2 = wq[2], w3 = wq[3], w4 = wq[4];
+    const float d = half_bits_to_float(*reinterpret_cast<const unsigned short *>(row + cc.off));
+    nib_word<NV>(__funnelshift_r(w0, w1, cc.qsh), xr, 0, a);
+    nib_word<NV>(__funnelshift_r(w1, w2, cc.qsh), xr, 1, a);
+    nib_word<NV>(__funnelshift_r(w2, w3, cc.qsh), xr, 2, a);
+    nib_word<NV>(__funnelshift_r(w3, w4, cc.qsh), xr, 3, a);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) part[v] = d * ((a[v][0] + a[v][1]) - 8.0f * xs[v]);
+  } else {  // Q8_0
+    const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
+    const float d = half_bits_to_float(*reinterpret_cast<const unsigned short *>(row + cc.off));
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = wq[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) byte_word<NV>(__funnelshift_r(w[i], w[i + 1], cc.qsh), xr, i, a);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) part[v] = d * ((a[v][0] + a[v][1]) - 128.0f * xs[v]);
+  }
+}
+
+// Load and pre-scale one column of activations for NV vectors.
+// Returns per-vector local max |x|, sum x^2 and sum x (unscaled) through
+// the output arrays; the scaled registers are filled by scale_column().
+struct XGather {
+  int group;     // > 1: heads of x are repeated `group` times
+  int head_dim;  // floats per head
+  __device__ __forceinline__ int src(int j) const {
+    if (group <= 1) return j;
+    const int span = head_dim * group;
+    return (j / span) * head_dim + (j % head_dim);
+  }
+};
+
+}  // namespace epq

@@ -32,3 +32,22 @@ def read_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return read_golden
+
+
+@pytest.fixture(scope="session")
+def epq_lib():
+    """Build (if stale) and load libepq.so; the C ABI under test."""
+    from moe_experts_gb300 import build as _build
+    _build.build()
+    import moe_experts_gb300 as epq
+    epq.load()
+    return epq
+
+
+@pytest.fixture(scope="session")
+def cuda_dev(epq_lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test selected but CUDA is not available")
+    torch.cuda.init()
+    return torch.device("cuda:0")
