@@ -1,0 +1,538 @@
+"""Benchmark of the block-quantized decode path on GB300.
+
+Default workload (the headline): full MoE decode step with Q4_K weights --
+40 layers, hidden 2048, 256 experts (gate/up 512x2048, down 2048x512), top-8
+routed + 1 shared expert, q/k/v/o 2048x2048 Q4_K per layer, router 256x2048
+fp32 with Zipf(1.1) popularity, a 64-token decode run at batch 1.  One
+"step" = the 64-token run (64 x 40 layers of GEMVs + router/top-K + expert
+gate/up+SwiGLU + down + combine), replayed from one CUDA graph.  18.7 GB of
+packed weights stay resident; every step streams 1.1 GB per token, far
+beyond the 129 MB L2, so no flush is needed.
+
+Other workloads (--workload): gemv4096, layer8b (per --fmt), dense8b
+(--nvec 1/2/4/8), moe_layer (--ntok 1/8).
+
+The JSON line carries: value (tok/s for decode workloads, GB/s otherwise),
+roofline of the dominant kernel (live CUDA-event pairs inside the graph),
+e2e (host buffers, H2D + D2H inside the timed region), clocks sampled
+during the timed region, gpu_launches, and the CPU baseline (the oracle on
+a bounded sample).  --impl reference times the oracle itself.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective weight GB/s and % of HBM peak for Q4_K dequant-GEMV; decode tok/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        try:
+            for line in open(self.path):
+                f = [v.strip() for v in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax.append(float(f[2]))
+                except ValueError:
+                    continue
+                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except Exception:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ workloads
+class Workload:
+    name = ""
+    unit = "tok/s"
+    units_per_step = 1.0       # tokens (or bytes) per step
+    dtype = "f32"
+
+    def config(self):
+        return {}
+
+
+def quantize_into(epq, fmt, W, out=None):
+    return epq.epq_quantize(fmt, W, blocks=out)
+
+
+class MoEDecodeWorkload(Workload):
+    name = "moe_decode"
+    unit = "tok/s"
+
+    def __init__(self, epq, dev, fmt, layers=None):
+        from synthetic import workloads as wl
+        self.cfg = c = wl.MoEDecode() if layers is None else wl.MoEDecode(layers=layers)
+        self.fmt, self.dev, self.epq = fmt, dev, epq
+        H, I, E = c.hidden, c.inter, c.n_experts
+        rbH, rbI = epq.epq_row_bytes(fmt, H), epq.epq_row_bytes(fmt, I)
+        import torch
+        self.layers = []
+        for l in range(c.layers):
+            wqkv = torch.empty((3 * H, rbH), dtype=torch.uint8, device=dev)
+            for t in range(3):
+                epq.epq_quantize(fmt, wl.weight("moe_decode", l, t, H, H, dev), blocks=wqkv[t * H:(t + 1) * H])
+            wo = epq.epq_quantize(fmt, wl.weight("moe_decode", l, 3, H, H, dev))
+            R, bias = wl.moe_router("moe_decode", l, E, H, dev, c.zipf_s)
+            gu = torch.empty((E, 2 * I, rbH), dtype=torch.uint8, device=dev)
+            dn = torch.empty((E, H, rbI), dtype=torch.uint8, device=dev)
+            for e0 in range(0, E, 64):
+                n = min(64, E - e0)
+                Wg = wl.weight("moe_decode", l, 10, n * 2 * I, H, dev, expert=e0)
+                epq.epq_quantize(fmt, Wg, blocks=gu[e0:e0 + n].view(n * 2 * I, rbH))
+                Wd = wl.weight("moe_decode", l, 11, n * H, I, dev, expert=e0)
+                epq.epq_quantize(fmt, Wd, blocks=dn[e0:e0 + n].view(n * H, rbI))
+                del Wg, Wd
+            sgu = epq.epq_quantize(fmt, wl.weight("moe_decode", l, 12, 2 * I, H, dev))
+            sdn = epq.epq_quantize(fmt, wl.weight("moe_decode", l, 13, H, I, dev))
+            layer = epq.MoELayer(fmt, R, gu, dn, router_bias=bias, shared_gate_up=sgu, shared_down=sdn)
+            self.layers.append((wqkv, wo, layer))
+        torch.cuda.synchronize()
+        from moe_experts_gb300.decode import MoEDecoder
+        self.model = MoEDecoder(c, fmt, self.layers, dev)
+        self.T = c.tokens
+        self.x = wl.activations("moe_decode", self.T, H, dev)
+        self.out = torch.empty((self.T, H), dtype=torch.float32, device=dev)
+        self.units_per_step = float(self.T)
+        self.bytes_per_token = c.layers * (4 * H * rbH + E * H * 4 + (c.topk + 1) * (2 * I * rbH + H * rbI))
+        self.kernels_per_step = self.T * c.layers * 5
+        # dominant-kernel candidates: name -> (algorithmic bytes per launch, launches per step)
+        self.kernel_bytes = {
+            "gemv_qkv": 3 * H * rbH + 4 * (H + 3 * H),
+            "gemv_o": H * rbH + 4 * (H + 2 * H),
+            "moe_router": E * H * 4 + 4 * H,
+            "moe_gateup": (c.topk + 1) * 2 * I * rbH + 4 * (H + (c.topk + 1) * I),
+            "moe_down": (c.topk + 1) * H * rbI + 4 * ((c.topk + 1) * I + 2 * H),
+        }
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "moe_decode_q4k", "layers": c.layers, "hidden": c.hidden, "experts": c.n_experts,
+                "inter": c.inter, "topk": c.topk, "shared_experts": 1, "tokens_per_step": c.tokens, "batch": 1,
+                "router": "fp32 zipf(1.1)", "weights_resident_gb": round(self.resident_gb(), 2),
+                "bytes_per_token": self.bytes_per_token, "l2": "inputs larger than L2 (1.1 GB/token)"}
+
+    def resident_gb(self):
+        tot = 0
+        for wqkv, wo, layer in self.layers:
+            tot += wqkv.numel() + wo.numel() + layer.gate_up.numel() + layer.down.numel()
+            tot += layer.router.numel() * 4 + layer.shared_gate_up.numel() + layer.shared_down.numel()
+        return tot / 1e9
+
+    def step(self, stream, x=None, out=None, timers=None):
+        x = self.x if x is None else x
+        out = self.out if out is None else out
+        for t in range(self.T):
+            self.model.token(x[t:t + 1], out[t:t + 1], stream=stream, timers=timers if t < 64 else None)
+
+    # ---- oracle on a bounded sample (a few layers of one token)
+    def oracle_sample(self, budget_s=20.0):
+        import numpy as np
+        import oracle
+        from oracle.moe import MoEWeights
+        c = self.cfg
+        H, I = c.hidden, c.inter
+        x = self.x[0:1].cpu().numpy().astype(np.float32)
+        h = x.astype(np.float64)
+        t0 = time.perf_counter()
+        done = 0
+        for l, (wqkv, wo, layer) in enumerate(self.layers):
+            pq = wqkv.cpu().numpy()
+            po = wo.cpu().numpy()
+            mw = MoEWeights(fmt=self.fmt, hidden=H, inter=I, router=layer.router.cpu().numpy(),
+                            gate_up=None, down=None, router_bias=layer.router_bias.cpu().numpy(),
+                            shared_gate_up=layer.shared_gate_up.cpu().numpy(),
+                            shared_down=layer.shared_down.cpu().numpy())
+            ts = time.perf_counter()
+            xn = oracle.rmsnorm_f64(h, c.rms_eps)
+            qkv = oracle.gemv_f64(self.fmt, pq, xn, H)
+            h = h + oracle.gemv_f64(self.fmt, po, qkv[:, 2 * H:], H)
+            xin = oracle.rmsnorm_f64(h, c.rms_eps)
+            logits = oracle.router_logits_f64(mw.router, xin, mw.router_bias)
+            idx = oracle.topk_select(logits, c.topk)
+            w = oracle.combine_weights(logits, idx, True)
+            y = h.copy()
+            gu_all, dn_all = layer.gate_up, layer.down
+            for k, e in enumerate(idx[0]):
+                o = oracle.expert_forward_f64(self.fmt, gu_all[int(e)].cpu().numpy(), dn_all[int(e)].cpu().numpy(),
+                                              H, I, xin[0])[0]
+                y += w[0, k] * o
+            o = oracle.expert_forward_f64(self.fmt, mw.shared_gate_up, mw.shared_down, H, I, xin[0])[0]
+            h = y + o
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        per_token = dt / done * c.layers
+        return 1.0 / per_token, f"1 token through {done} of {c.layers} layers (oracle, float64), scaled to 40 layers"
+
+
+class DenseDecodeWorkload(Workload):
+    name = "dense8b"
+    unit = "tok/s"
+
+    def __init__(self, epq, dev, fmt, nvec=1, layers=None):
+        import torch
+        from synthetic import workloads as wl
+        self.cfg = c = wl.DenseDecode() if layers is None else wl.DenseDecode(layers=layers)
+        self.fmt, self.dev, self.epq, self.nvec = fmt, dev, epq, nvec
+        H = c.hidden
+        rbH, rbI = epq.epq_row_bytes(fmt, H), epq.epq_row_bytes(fmt, c.inter)
+        nq, nkv = c.q_rows, c.kv_rows
+        self.layers = []
+        for l in range(c.layers):
+            wqkv = torch.empty((nq + 2 * nkv, rbH), dtype=torch.uint8, device=dev)
+            epq.epq_quantize(fmt, wl.weight("dense8b", l, 0, nq, H, dev), blocks=wqkv[:nq])
+            epq.epq_quantize(fmt, wl.weight("dense8b", l, 1, nkv, H, dev), blocks=wqkv[nq:nq + nkv])
+            epq.epq_quantize(fmt, wl.weight("dense8b", l, 2, nkv, H, dev), blocks=wqkv[nq + nkv:])
+            wo = epq.epq_quantize(fmt, wl.weight("dense8b", l, 3, H, nq, dev))
+            wgu = torch.empty((2 * c.inter, rbH), dtype=torch.uint8, device=dev)
+            epq.epq_quantize(fmt, wl.weight("dense8b", l, 4, c.inter, H, dev), blocks=wgu[:c.inter])
+            epq.epq_quantize(fmt, wl.weight("dense8b", l, 5, c.inter, H, dev), blocks=wgu[c.inter:])
+            wd = epq.epq_quantize(fmt, wl.weight("dense8b", l, 6, H, c.inter, dev))
+            self.layers.append((wqkv, wo, wgu, wd))
+        head = torch.empty((c.vocab, rbH), dtype=torch.uint8, device=dev)
+        for r0 in range(0, c.vocab, 16384):
+            n = min(16384, c.vocab - r0)
+            epq.epq_quantize(fmt, wl.weight("dense8b", 0, 7, n, H, dev, expert=r0), blocks=head[r0:r0 + n])
+        self.head = head
+        torch.cuda.synchronize()
+        from moe_experts_gb300.decode import DenseDecoder
+        self.model = DenseDecoder(c, fmt, self.layers, head, dev, nvec=nvec)
+        self.x = wl.activations("dense8b", nvec, H, dev)
+        self.units_per_step = float(nvec)
+        wbytes = c.layers * ((nq + 2 * nkv) * rbH + H * epq.epq_row_bytes(fmt, nq) + 2 * c.inter * rbH
+                             + H * rbI) + c.vocab * rbH
+        self.bytes_per_token = wbytes
+        self.kernels_per_step = c.layers * 4 + 1
+        self.kernel_bytes = {
+            "gemv_qkv": (nq + 2 * nkv) * rbH + 4 * nvec * (H + nq + 2 * nkv),
+            "gemv_o": H * epq.epq_row_bytes(fmt, nq) + 4 * nvec * (nkv + 2 * H),
+            "gemv_gateup": 2 * c.inter * rbH + 4 * nvec * (H + c.inter),
+            "gemv_down": H * rbI + 4 * nvec * (c.inter + 2 * H),
+        }
+
+    def config(self):
+        c = self.cfg
+        return {"workload": f"dense8b_decode_{'q4k' if self.fmt == 3 else self.fmt}", "layers": c.layers,
+                "hidden": c.hidden, "inter": c.inter, "heads": c.heads, "kv_heads": c.kv_heads, "vocab": c.vocab,
+                "nvec": self.nvec, "batch": 1, "weight_bytes_per_step": self.bytes_per_token,
+                "l2": "inputs larger than L2 (4.2 GB/step)"}
+
+    def step(self, stream, x=None, out=None, timers=None):
+        self.model.step(self.x if x is None else x, stream=stream, timers=timers)
+
+    def oracle_sample(self, budget_s=20.0):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        H = c.hidden
+        x = self.x.cpu().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        done = 0
+        nbytes = 0
+        for wqkv, wo, wgu, wd in self.layers:
+            for w, cols in ((wqkv, H), (wgu, H)):
+                p = w.cpu().numpy()
+                oracle.gemv_f64(self.fmt, p, x, cols)
+                nbytes += p.size
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        # scale by bytes: the sample covered qkv + gate/up of `done` layers
+        rate = nbytes / dt
+        return self.nvec * rate / self.bytes_per_token, \
+            f"{done} layers' qkv+gate/up GEMVs (oracle, float64), scaled by bytes to the full step"
+
+
+# ------------------------------------------------------------------ timing
+def run_epq(args):
+    import torch
+    import moe_experts_gb300 as epq
+    from moe_experts_gb300 import build as _build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    _build.build()
+    epq.load()
+    fmt = epq.FORMATS[args.fmt]
+    if args.workload == "moe_decode":
+        W = MoEDecodeWorkload(epq, dev, fmt, layers=args.layers)
+    elif args.workload == "dense8b":
+        W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers)
+    else:
+        raise SystemExit(f"unknown workload {args.workload}")
+
+    stream = torch.cuda.Stream(device=dev)
+    # warm the kernels (sets smem attributes) outside capture
+    with torch.cuda.stream(stream):
+        W.step(stream)
+    stream.synchronize()
+    assert epq.epq_device_error() == 0, "device-side wait timed out during warm-up"
+
+    # timers: CUDA event pairs around each kernel of layer 0, for every token
+    timers = Timers(torch, W)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        W.step(stream, timers=timers)
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    kernel_ms = timers.averages()
+    clocks = clk.summary()
+    err = epq.epq_device_error()
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: host (pinned) inputs in, results back to host, per step
+    x_host = W.x.cpu().pin_memory()
+    out_dev = torch.empty_like(W.out if hasattr(W, "out") else W.model.logits)
+    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    x_dev = torch.empty_like(W.x)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        W.step(stream, x=x_dev, out=out_dev if hasattr(W, "out") else None)
+    res_src = out_dev if hasattr(W, "out") else W.model.logits
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        g2.replay()
+        out_host.copy_(res_src, non_blocking=True)
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, min(args.steps, 5))
+    barrier()
+    e2.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(n_e2e):
+            x_dev.copy_(x_host, non_blocking=True)
+            g2.replay()
+            out_host.copy_(res_src, non_blocking=True)
+    e3.record(stream)
+    e3.synchronize()
+    e2e_ms = e2.elapsed_time(e3) / n_e2e
+
+    units = W.units_per_step * ws
+    value = units / (ms * 1e-3)
+    peak, peak_kind = measured_peaks()
+    # dominant kernel: largest total time per step
+    launches = {k: W.kernels_per_step // len(W.kernel_bytes) for k in W.kernel_bytes}
+    dom = max(kernel_ms, key=lambda k: kernel_ms[k] * launches[k]) if kernel_ms else None
+    roof = None
+    if dom:
+        ach = W.kernel_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_kind": peak_kind + " copy bandwidth",
+                "traffic": None, "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
+                "bytes_per_launch": W.kernel_bytes[dom],
+                "all_kernels_us": {k: round(v * 1e3, 3) for k, v in kernel_ms.items()}}
+    eff_gbs = W.bytes_per_token * (value / ws) / 1e9 if W.unit == "tok/s" else None
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": W.unit, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "q4k weights / f32 activations / f32 accumulate", "data": "synthetic",
+        "config": {**W.config(), "parallelism": f"replicas{ws}" if ws > 1 else "single"},
+        "effective_weight_gbs": round(eff_gbs, 1) if eff_gbs else None,
+        "pct_of_measured_hbm": round(100 * eff_gbs / peak, 2) if eff_gbs else None,
+        "pct_of_nominal_8tbs": round(100 * eff_gbs / NOMINAL_HBM_GBS, 2) if eff_gbs else None,
+        "roofline": roof, "clocks": clocks, "gpu_launches": W.kernels_per_step * args.steps,
+        "e2e": {"value": round(W.units_per_step * ws / (e2e_ms * 1e-3), 3), "unit": W.unit,
+                "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4},
+        "device_error": err,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, sample = W.oracle_sample(budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": W.unit, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+class Timers:
+    """CUDA event pairs recorded (as graph nodes) around each kernel of
+    layer 0 for every token of the step; averaged after the timed region."""
+
+    def __init__(self, torch, W):
+        self.torch = torch
+        self.pairs = {}
+        self.names = list(W.kernel_bytes)
+
+    def pair(self, name):
+        t = self.torch
+        a = t.cuda.Event(enable_timing=True, external=True)
+        b = t.cuda.Event(enable_timing=True, external=True)
+        self.pairs.setdefault(name, []).append((a, b))
+        return a, b
+
+    def averages(self):
+        out = {}
+        for k, ps in self.pairs.items():
+            v = [a.elapsed_time(b) for a, b in ps]
+            out[k] = sum(v) / len(v)
+        return out
+
+
+def run_reference(args):
+    """The oracle, timed on the host cores, on a bounded sample of the same
+    workload (the other ranks of a multi-GPU launch exit without work)."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+    import moe_experts_gb300 as epq
+    from moe_experts_gb300 import build as _build
+    _build.build()
+    epq.load()
+    dev = torch.device(f"cuda:{local}")
+    fmt = epq.FORMATS[args.fmt]
+    # the reference arm only needs the packed weights of the sampled layers
+    if args.workload == "moe_decode":
+        W = MoEDecodeWorkload(epq, dev, fmt, layers=max(1, args.ref_layers))
+        W.cfg = __import__("synthetic.workloads", fromlist=["MoEDecode"]).MoEDecode()
+    else:
+        W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=max(1, args.ref_layers))
+    per_step = args.cpu_budget / max(1, args.steps + args.warmup)
+    vals = []
+    t_all = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        v, sample = W.oracle_sample(budget_s=per_step)
+        if i >= args.warmup:
+            vals.append(v)
+    dt = time.perf_counter() - t_all
+    value = statistics.mean(vals)
+    ms = 1e3 * W.units_per_step / value if W.unit == "tok/s" else None
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": W.unit, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3) if ms else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": W.config(),
+            "cpu_baseline": {"value": round(value, 6), "unit": W.unit, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": W.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(dt, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="epq", choices=["epq", "reference"])
+    ap.add_argument("--workload", default="moe_decode", choices=["moe_decode", "dense8b"])
+    ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K"])
+    ap.add_argument("--nvec", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (smaller cases)")
+    ap.add_argument("--ref-layers", type=int, default=2)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_epq(args)
+
+
+if __name__ == "__main__":
+    main()

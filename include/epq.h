@@ -76,6 +76,11 @@ int epq_last_cuda_error(void);
  * Synchronizes the device. */
 int epq_device_error(void);
 
+/* Same, and where the first timeout happened: the CTA index, the pipeline
+ * step (tile or work-unit index) and the thread index (any pointer may be
+ * NULL). */
+int epq_device_error_detail(int *block, int *where, int *thread);
+
 /* Weights per block (32 or 256), bytes per block, and packed bytes per row:
  * cols/block_weights*block_bytes, or -1 when cols is not a positive multiple
  * of the block size or fmt is unknown.  Host-only, no device needed. */
@@ -112,7 +117,7 @@ epq_status epq_dequantize(epq_fmt fmt, const void *blocks, int64_t rows, int64_t
  * The entries of x must be finite with max|x| < 2^100; entries more than
  * about 2^100 below max|x| count as zero.
  * Requirements: 1 <= nvec <= 8, rows >= 1, cols % 256 == 0 and
- * 256 <= cols <= 32768 (EPQ_ERR_SHAPE), blocks/x/y 16-byte aligned.
+ * 256 <= cols <= 16384 (EPQ_ERR_SHAPE), blocks/x/y 16-byte aligned.
  * y must not overlap x or blocks. */
 epq_status epq_gemv(epq_fmt fmt, const void *blocks, const float *x, float *y,
                     int64_t rows, int64_t cols, int nvec, epq_stream_t stream);
@@ -131,7 +136,15 @@ epq_status epq_gemv(epq_fmt fmt, const void *blocks, const float *x, float *y,
  *                x[(j / (x_head_dim*x_group)) * x_head_dim + j % x_head_dim]
  *                (each head of x repeated x_group times, as a grouped-query
  *                attention output over a one-token context).  x then holds
- *                cols / x_group floats per vector; x_head_dim % 32 == 0. */
+ *                cols / x_group floats per vector; x_head_dim % 32 == 0.
+ *   x_ld         floats between consecutive x vectors (0 = the vector length);
+ *                a multiple of 4, so that a slice of a wider buffer can be
+ *                read in place.
+ *   weights_ready  1: the packed weights were not written by work that may
+ *                still be running on the stream, so the kernel may start
+ *                streaming them into shared memory before the preceding
+ *                kernel has finished (programmatic dependent launch).  x and
+ *                residual are always read only after it has finished. */
 typedef struct {
   const float *residual;
   int rms_prenorm;
@@ -139,11 +152,82 @@ typedef struct {
   int swiglu;
   int x_group;
   int x_head_dim;
+  int64_t x_ld;
+  int weights_ready;
 } epq_gemv_opts;
 
 epq_status epq_gemv_ex(epq_fmt fmt, const void *blocks, const float *x, float *y,
                        int64_t rows, int64_t cols, int nvec, const epq_gemv_opts *opts,
                        epq_stream_t stream);
+
+/* ---------------------------------------------------------------- MoE layer
+ * [F] "每层流水线" and "3. Metal 计算着色器"; shapes from [F] "模型架构" and
+ * [E] "記憶體怎麼配置的".  For every token t (x_t = row t of x):
+ *   xin_t  = x_t, or x_t / sqrt(mean(x_t^2) + rms_eps) with rms_prenorm
+ *   l_t    = R xin_t + bias                       (router logits, float32)
+ *   S_t    = the topk experts of largest l_t (ties -> lower expert index)
+ *   p_t    = softmax(l_t) over all experts; w_tk = p_t[e_k], divided by
+ *            sum_k p_t[e_k] when norm_topk
+ *   E_e(v) = down_e( silu(gate_e v) * (up_e v) )  (silu(g) = g/(1+exp(-g)))
+ *   y_t    = x_t + sum_k w_tk E_{e_k}(xin_t) + g_t E_shared(xin_t)
+ *            g_t = 1, or sigmoid(shared_gate_vec . xin_t) when given.
+ * Tokens that pick the same expert share one pass over its weights. */
+typedef struct {
+  const float *weight; /* [n_experts][hidden] float32, 16-byte aligned */
+  const float *bias;   /* [n_experts] or NULL */
+  int n_experts;       /* 1..1024 */
+  int norm_topk;       /* 1: renormalize the selected probabilities */
+} epq_router;
+
+typedef struct {
+  epq_fmt fmt;
+  int n_experts; /* must equal the router's */
+  int hidden;    /* H: multiple of 256, 256..16384 */
+  int inter;     /* I: multiple of 256, 256..16384 */
+  /* expert e: gate_up + e*gate_up_stride holds 2*I packed rows of H weights
+   * (the I gate rows, then the I up rows); down + e*down_stride holds H
+   * packed rows of I weights.  A stride of 0 means the packed size.  Strides
+   * must be multiples of 16 bytes. */
+  const void *gate_up;
+  int64_t gate_up_stride;
+  const void *down;
+  int64_t down_stride;
+  const void *shared_gate_up;    /* NULL: no shared expert */
+  const void *shared_down;
+  const float *shared_gate_vec;  /* NULL: shared weight 1; else [H] */
+} epq_experts;
+
+typedef struct {
+  int rms_prenorm;
+  float rms_eps;
+  float *logits_out; /* NULL or [ntok][n_experts]: the router logits */
+  float *h_out;      /* NULL or [ntok][topk+1][I]: silu(g)*u per token and
+                        slot (slot k = k-th choice, slot topk = shared) */
+  int stages;        /* 0 = all; else a mask of EPQ_MOE_ROUTE, EPQ_MOE_GATE_UP,
+                        EPQ_MOE_DOWN: the selected kernels only.  Stages of
+                        one layer may be issued by separate calls in order
+                        with the same arguments and workspace (the workspace
+                        carries the routing and h between them). */
+} epq_moe_opts;
+
+enum { EPQ_MOE_ROUTE = 1, EPQ_MOE_GATE_UP = 2, EPQ_MOE_DOWN = 4 };
+
+/* Workspace bytes epq_moe_forward needs for these shapes (0 on bad input).
+ * Host-only. */
+size_t epq_moe_workspace_bytes(const epq_router *router, const epq_experts *experts, int ntok, int topk);
+
+/* One MoE layer for ntok tokens (1..16) and topk (1..16, <= n_experts).
+ *   x          float32 [ntok][H]            y  float32 [ntok][H] (may equal x)
+ *   topk_idx   NULL or int32 [ntok][topk]   (selected experts, best first)
+ *   topk_w     NULL or float32 [ntok][topk] (their combine weights)
+ *   workspace  device scratch of epq_moe_workspace_bytes(); contents need no
+ *              initialisation and are reused by the next call (calls that
+ *              share a workspace must be ordered on one stream).
+ * Three kernels are queued: router + top-K + grouping, gate/up + SwiGLU,
+ * down + combine + residual.  No host synchronisation. */
+epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts, const float *x, int ntok,
+                           int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w,
+                           void *workspace, size_t workspace_bytes, epq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,28 @@ class EpqError(RuntimeError):
 
 class GemvOpts(ctypes.Structure):
     _fields_ = [("residual", ctypes.c_void_p), ("rms_prenorm", ctypes.c_int), ("rms_eps", ctypes.c_float),
-                ("swiglu", ctypes.c_int), ("x_group", ctypes.c_int), ("x_head_dim", ctypes.c_int)]
+                ("swiglu", ctypes.c_int), ("x_group", ctypes.c_int), ("x_head_dim", ctypes.c_int),
+                ("x_ld", ctypes.c_int64), ("weights_ready", ctypes.c_int)]
+
+
+class Router(ctypes.Structure):
+    _fields_ = [("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("n_experts", ctypes.c_int),
+                ("norm_topk", ctypes.c_int)]
+
+
+class Experts(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("n_experts", ctypes.c_int), ("hidden", ctypes.c_int),
+                ("inter", ctypes.c_int), ("gate_up", ctypes.c_void_p), ("gate_up_stride", ctypes.c_int64),
+                ("down", ctypes.c_void_p), ("down_stride", ctypes.c_int64), ("shared_gate_up", ctypes.c_void_p),
+                ("shared_down", ctypes.c_void_p), ("shared_gate_vec", ctypes.c_void_p)]
+
+
+class MoeOpts(ctypes.Structure):
+    _fields_ = [("rms_prenorm", ctypes.c_int), ("rms_eps", ctypes.c_float), ("logits_out", ctypes.c_void_p),
+                ("h_out", ctypes.c_void_p), ("stages", ctypes.c_int)]
+
+
+EPQ_MOE_ROUTE, EPQ_MOE_GATE_UP, EPQ_MOE_DOWN = 1, 2, 4
 
 
 def declared_symbols() -> list[str]:
@@ -59,6 +80,7 @@ def load(path: str | None = None):
         "epq_status_string": (ctypes.c_char_p, [i32]),
         "epq_last_cuda_error": (i32, []),
         "epq_device_error": (i32, []),
+        "epq_device_error_detail": (i32, [ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]),
         "epq_block_weights": (i64, [i32]),
         "epq_block_bytes": (i64, [i32]),
         "epq_row_bytes": (i64, [i32, i64]),
@@ -66,6 +88,9 @@ def load(path: str | None = None):
         "epq_dequantize": (i32, [i32, vp, i64, i64, vp, vp]),
         "epq_gemv": (i32, [i32, vp, vp, vp, i64, i64, i32, vp]),
         "epq_gemv_ex": (i32, [i32, vp, vp, vp, i64, i64, i32, ctypes.POINTER(GemvOpts), vp]),
+        "epq_moe_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Router), ctypes.POINTER(Experts), i32, i32]),
+        "epq_moe_forward": (i32, [ctypes.POINTER(Router), ctypes.POINTER(Experts), vp, i32, i32,
+                                  ctypes.POINTER(MoeOpts), vp, vp, vp, vp, ctypes.c_size_t, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -111,6 +136,13 @@ def epq_device_error() -> int:
     return int(load().epq_device_error())
 
 
+def epq_device_error_detail() -> tuple[int, int, int, int]:
+    """(code, block, pipeline step, thread) of the first wait timeout; clears it."""
+    b, w, t = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = load().epq_device_error_detail(ctypes.byref(b), ctypes.byref(w), ctypes.byref(t))
+    return int(code), b.value, w.value, t.value
+
+
 # ------------------------------------------------------------------ packing
 def epq_quantize(fmt: int, W: torch.Tensor, blocks: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """W float32 [rows, cols] (CUDA) -> packed uint8 [rows, row_bytes]."""
@@ -147,15 +179,72 @@ def epq_gemv(fmt: int, blocks: torch.Tensor, x: torch.Tensor, rows: int, cols: i
 
 def epq_gemv_ex(fmt: int, blocks: torch.Tensor, x: torch.Tensor, rows: int, cols: int, y: torch.Tensor | None = None,
                 residual: torch.Tensor | None = None, rms_prenorm: bool = False, rms_eps: float = 0.0,
-                swiglu: bool = False, x_group: int = 0, x_head_dim: int = 0, stream=None) -> torch.Tensor:
+                swiglu: bool = False, x_group: int = 0, x_head_dim: int = 0, weights_ready: bool = False,
+                stream=None) -> torch.Tensor:
     lib = load()
     x2 = x if x.dim() == 2 else x.view(1, -1)
     nvec = x2.shape[0]
+    if x2.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    x_ld = x2.stride(0) if nvec > 1 else 0
     rows_out = rows // 2 if swiglu else rows
     if y is None:
         y = torch.empty((nvec, rows_out), dtype=torch.float32, device=x.device)
     o = GemvOpts(residual.data_ptr() if residual is not None else None, int(rms_prenorm), float(rms_eps),
-                 int(swiglu), int(x_group), int(x_head_dim))
+                 int(swiglu), int(x_group), int(x_head_dim), int(x_ld), int(weights_ready))
     _check("epq_gemv_ex", lib.epq_gemv_ex(fmt, _ptr(blocks), _ptr(x2), _ptr(y), rows, cols, nvec,
                                           ctypes.byref(o), _stream(stream)))
     return y
+
+
+# ------------------------------------------------------------------ MoE layer
+def _addr(t):
+    return None if t is None else t.data_ptr()
+
+
+class MoELayer:
+    """Device-resident MoE weights in the layout epq_moe_forward expects.
+
+    router [E, H] float32; gate_up uint8 [E, 2*I, row_bytes(H)] (gate rows
+    then up rows); down uint8 [E, H, row_bytes(I)]; optional shared expert
+    (same shapes without E) and shared gate vector [H].
+    """
+
+    def __init__(self, fmt, router, gate_up, down, router_bias=None, shared_gate_up=None, shared_down=None,
+                 shared_gate_vec=None, norm_topk=True):
+        self.fmt = int(fmt)
+        self.router, self.router_bias = router, router_bias
+        self.gate_up, self.down = gate_up, down
+        self.shared_gate_up, self.shared_down, self.shared_gate_vec = shared_gate_up, shared_down, shared_gate_vec
+        self.E, self.H = router.shape
+        self.I = down.shape[2] * epq_block_weights(self.fmt) // epq_block_bytes(self.fmt)
+        self.norm_topk = bool(norm_topk)
+        self._r = Router(_addr(router), _addr(router_bias), self.E, int(self.norm_topk))
+        self._x = Experts(self.fmt, self.E, self.H, self.I, _addr(gate_up), gate_up[0].numel(), _addr(down),
+                          down[0].numel(), _addr(shared_gate_up), _addr(shared_down), _addr(shared_gate_vec))
+
+    def workspace_bytes(self, ntok: int, topk: int) -> int:
+        return int(load().epq_moe_workspace_bytes(ctypes.byref(self._r), ctypes.byref(self._x), ntok, topk))
+
+
+def epq_moe_workspace_bytes(layer: MoELayer, ntok: int, topk: int) -> int:
+    return layer.workspace_bytes(ntok, topk)
+
+
+def epq_moe_forward(layer: MoELayer, x: torch.Tensor, topk: int, y: torch.Tensor | None = None,
+                    topk_idx: torch.Tensor | None = None, topk_w: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, rms_prenorm: bool = False, rms_eps: float = 0.0,
+                    logits_out: torch.Tensor | None = None, h_out: torch.Tensor | None = None, stages: int = 0,
+                    stream=None):
+    """x float32 [ntok, H] -> y float32 [ntok, H]; returns (y, topk_idx, topk_w)."""
+    lib = load()
+    ntok = x.shape[0]
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.empty(layer.workspace_bytes(ntok, topk), dtype=torch.uint8, device=x.device)
+    o = MoeOpts(int(rms_prenorm), float(rms_eps), _addr(logits_out), _addr(h_out), int(stages))
+    _check("epq_moe_forward", lib.epq_moe_forward(
+        ctypes.byref(layer._r), ctypes.byref(layer._x), _ptr(x), ntok, topk, ctypes.byref(o), _ptr(y),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return y, topk_idx, topk_w

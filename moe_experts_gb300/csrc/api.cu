@@ -8,7 +8,7 @@ namespace epq {
 
 // One error word per device (a separate instance lives on every device that
 // loads the library).
-__device__ unsigned g_device_error = 0;
+__device__ unsigned g_device_error[4] = {0, 0, 0, 0};
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -87,16 +87,21 @@ const char *epq_status_string(epq_status s) {
 
 int epq_last_cuda_error(void) { return epq::g_last_cuda_error; }
 
-int epq_device_error(void) {
+int epq_device_error_detail(int *block, int *where, int *thread) {
   unsigned *slot = epq::device_error_slot();
   if (!slot) return -1;
-  unsigned v = 0;
+  unsigned v[4] = {0, 0, 0, 0};
   if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-  if (cudaMemcpyFromSymbol(&v, epq::g_device_error, sizeof(v)) != cudaSuccess) return -1;
-  const unsigned zero = 0;
-  if (cudaMemcpyToSymbol(epq::g_device_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
-  return static_cast<int>(v);
+  if (cudaMemcpyFromSymbol(v, epq::g_device_error, sizeof(v)) != cudaSuccess) return -1;
+  const unsigned zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(epq::g_device_error, zero, sizeof(zero)) != cudaSuccess) return -1;
+  if (block) *block = static_cast<int>(v[1]);
+  if (where) *where = static_cast<int>(v[2]);
+  if (thread) *thread = static_cast<int>(v[3]);
+  return static_cast<int>(v[0]);
 }
+
+int epq_device_error(void) { return epq_device_error_detail(nullptr, nullptr, nullptr); }
 
 int64_t epq_block_weights(epq_fmt fmt) {
   switch (fmt) {

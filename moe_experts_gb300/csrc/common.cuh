@@ -25,6 +25,7 @@ enum DeviceError : unsigned {
   DEVERR_FULL_WAIT = 1,    // consumer waited too long for a tile
   DEVERR_EMPTY_WAIT = 2,   // producer waited too long for a free stage
   DEVERR_DRAIN_WAIT = 3,   // copies still in flight at exit
+  DEVERR_RED_WAIT = 4,     // waited too long for the cross-warp reduction
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -72,15 +73,27 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // the longest legitimate wait is one tile copy behind a busy HBM.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Record the first timeout of the device: err[0] = code, err[1] = block,
+// err[2] = `where` (the pipeline step, e.g. tile index), err[3] = thread.
+__device__ __forceinline__ void record_error(unsigned *err, unsigned code, unsigned where) {
+  if (atomicCAS(err, 0u, code) == 0u) {
+    err[1] = blockIdx.x;
+    err[2] = where;
+    err[3] = threadIdx.x;
+    __threadfence();
+  }
+}
+
 // Bounded parity wait.  Returns false (after recording `code`) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code,
+                                          unsigned where = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicCAS(err, 0u, code);
+      record_error(err, code, where);
       return false;
     }
   }
@@ -89,11 +102,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
 // Warp-uniform bounded wait: lane 0 spins (bounded), the verdict is broadcast,
 // and on success every lane performs its own acquire of the completed phase
 // (which returns at once).  All lanes of the warp must call it.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code) {
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code,
+                                          unsigned where = 0) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, code) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, code, where) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) ok = mbar_wait(bar, parity, err, code) ? 1 : 0;
+  if (ok) ok = mbar_wait(bar, parity, err, code, where) ? 1 : 0;
   return __all_sync(0xffffffffu, ok) != 0;
 }
 

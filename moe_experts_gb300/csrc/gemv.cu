@@ -24,9 +24,9 @@ namespace epq {
 namespace {
 
 constexpr int kMaxConsumers = 512;
-constexpr int kProducerThreads = 32;
-constexpr int kTileTarget = 40 * 1024;   // bytes of packed weights per stage
-constexpr int kSmemTarget = 160 * 1024;  // ring budget per CTA
+constexpr int kTileTarget = 80 * 1024;   // bytes of packed weights per stage
+constexpr int kSmemTarget = 170 * 1024;  // ring budget per CTA
+constexpr int kRedRing = 4;              // reduction buffers in flight
 
 struct GemvParams {
   const uint8_t *W;
@@ -55,111 +55,92 @@ struct GemvParams {
 };
 
 struct SmemLayout {
-  uint32_t stage_off, full_off, empty_off, redbar_off, red_off, scratch_off, total;
+  uint32_t full_off, empty_off, rfull_off, rempty_off, red_off, scratch_off, total;
 };
+
+__host__ __device__ inline int wpg_of(int tpr) { return tpr > 32 ? tpr / 32 : 1; }
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, uint32_t stage_bytes, int nv, int red_rows, int tpr,
                                                   int nthreads) {
   SmemLayout L;
-  L.stage_off = 0;
   uint32_t o = static_cast<uint32_t>(stages) * stage_bytes + 16;  // +16: code-word over-read pad
   o = (o + 15u) & ~15u;
   L.full_off = o;
   o += 8u * stages;
   L.empty_off = o;
   o += 8u * stages;
-  L.redbar_off = o;
-  o += 16;
+  L.rfull_off = o;
+  o += 8u * kRedRing;
+  L.rempty_off = o;
+  o += 8u * kRedRing;
   L.red_off = o;
-  const int wpg = tpr > 32 ? tpr / 32 : 1;
-  o += 4u * 2 * nv * red_rows * wpg;
+  o += 4u * kRedRing * nv * red_rows * wpg_of(tpr);
   o = (o + 15u) & ~15u;
   L.scratch_off = o;
-  o += 4u * 3 * nv * (nthreads / 32);
+  o += 4u * 2 * nv * (nthreads / 32);
   L.total = (o + 15u) & ~15u;
   return L;
 }
 
-// Butterfly reduce-scatter of RPG partials over W lanes (W = segment width,
-// a power of two >= RPG).  The first log2(RPG) levels (offsets W/2, W/4, ...)
-// halve the set of rows a lane carries; the remaining levels are plain
-// butterflies.  On return v[.][0] holds the full sum of row `base` (the
-// returned index); the W/RPG lanes of each run share a row.
-template <int RPG, int NV>
-__device__ __forceinline__ int reduce_scatter(float (&v)[NV][RPG], int W, int lane) {
-  int base = 0;
-  int o = W >> 1;
-#pragma unroll
-  for (int n = RPG; n > 1; n >>= 1) {
-    const int h = n / 2;
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < h; ++i) {
-#pragma unroll
-      for (int q = 0; q < NV; ++q) {
-        const float send = upper ? v[q][i] : v[q][i + h];
-        const float keep = upper ? v[q][i + h] : v[q][i];
-        v[q][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-      }
-    }
-    if (upper) base += h;
-    o >>= 1;
-  }
-  for (; o >= 1; o >>= 1) {
-#pragma unroll
-    for (int q = 0; q < NV; ++q) v[q][0] += __shfl_xor_sync(0xffffffffu, v[q][0], o);
-  }
-  return base;
+// Output epilogue for one row of one vector.
+__device__ __forceinline__ void store_row(const GemvParams &p, int v, int64_t orow, float val) {
+  if (p.residual) val += p.residual[v * p.y_stride + orow];
+  p.y[v * p.y_stride + orow] = val;
 }
 
-__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
-
 template <int FMT, int NV, int RPG, bool SWIGLU>
-__global__ void __launch_bounds__(kMaxConsumers + kProducerThreads, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int nthreads = p.groups * p.tpr;
+  const int nwarps = nthreads / 32;
+  const bool has_fin = p.tpr > 32;   // cross-warp rows go through the finisher warp
+  const int wpg = wpg_of(p.tpr);
   const SmemLayout L = smem_layout(p.stages, p.stage_bytes, NV, p.red_rows, p.tpr, nthreads);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full_off);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty_off);
-  uint64_t *redbar = reinterpret_cast<uint64_t *>(smem + L.redbar_off);
+  uint64_t *rfull = reinterpret_cast<uint64_t *>(smem + L.rfull_off);
+  uint64_t *rempty = reinterpret_cast<uint64_t *>(smem + L.rempty_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   float *scratch = reinterpret_cast<float *>(smem + L.scratch_off);
   const int tid = threadIdx.x;
-  const int nwarps = nthreads / 32;
+  const int lane = tid & 31;
 
   // rows of this CTA
   const int64_t rb = (static_cast<int64_t>(blockIdx.x) * p.rows_out) / gridDim.x;
   const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * p.rows_out) / gridDim.x;
   const int ntiles = static_cast<int>((re - rb + p.tile_rows - 1) / p.tile_rows);
+  const int red_stride = NV * p.red_rows * wpg;   // floats per reduction buffer
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nwarps);
     }
-    mbar_init(&redbar[0], nwarps);
-    mbar_init(&redbar[1], nwarps);
+    for (int b = 0; b < kRedRing; ++b) {
+      mbar_init(&rfull[b], nwarps);
+      mbar_init(&rempty[b], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
   pdl_launch_dependents();
 
-  if (tid >= nthreads) {
-    // ------------------------------------------------------------ producer
+  // ------------------------------------------------------------------ producer
+  if (tid >= nthreads && tid < nthreads + 32) {
     if (tid != nthreads) return;
     if (!p.early_weights) pdl_wait();
     int issued = 0;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % p.stages;
-      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, p.err, DEVERR_EMPTY_WAIT)) {
+      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, p.err, DEVERR_EMPTY_WAIT, t)) {
         ok = false;
         break;
       }
       const int64_t r0 = rb + static_cast<int64_t>(t) * p.tile_rows;
       const int64_t nr = min(static_cast<int64_t>(p.tile_rows), re - r0);
       const uint32_t bytes = static_cast<uint32_t>(nr * p.row_bytes);
-      uint8_t *dst = smem + L.stage_off + static_cast<uint32_t>(s) * p.stage_bytes;
+      uint8_t *dst = smem + static_cast<uint32_t>(s) * p.stage_bytes;
       if (SWIGLU) {
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
         bulk_g2s(dst, p.W + r0 * p.row_bytes, bytes, &full[s]);
@@ -173,32 +154,28 @@ __global__ void __launch_bounds__(kMaxConsumers + kProducerThreads, 1) gemv_kern
     if (!ok) {
       // drain: wait (bounded) for every copy still in flight before leaving
       for (int t = max(0, issued - p.stages); t < issued; ++t)
-        mbar_wait(&full[t % p.stages], (t / p.stages) & 1, p.err, DEVERR_DRAIN_WAIT);
+        mbar_wait(&full[t % p.stages], (t / p.stages) & 1, p.err, DEVERR_DRAIN_WAIT, t);
     }
     return;
   }
 
-  // -------------------------------------------------------------- consumers
+  // ------------------------------------------------------------------ prologue
+  // consumers load their activation column; everyone (consumers + finisher)
+  // learns the per-vector exponent and RMS factor.
+  const bool is_fin = tid >= nthreads + 32;
   const int g = tid / p.tpr;
   const int c = tid % p.tpr;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const bool active = c < p.nblk;
-  const int W = p.tpr < 32 ? p.tpr : 32;
-
+  const bool active = !is_fin && c < p.nblk;
   ColConst<FMT> cc;
   cc.init(active ? c : 0);
   const XGather xg{p.x_group, p.x_head_dim};
+  pdl_wait();  // x and the residual are produced upstream
 
-  pdl_wait();  // x is produced upstream
-
-  // load the column's activations
   float xr[NV][32];
-  float amax[NV], ssq[NV], xsum[NV];
+  float xsum[NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    amax[v] = 0.0f;
-    ssq[v] = 0.0f;
+    float amax = 0.0f, ssq = 0.0f;
     xsum[v] = 0.0f;
     const bool vv = v < p.nv && active;
 #pragma unroll
@@ -212,22 +189,20 @@ __global__ void __launch_bounds__(kMaxConsumers + kProducerThreads, 1) gemv_kern
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      amax[v] = fmaxf(amax[v], fabsf(xr[v][j]));
-      if (g == 0) ssq[v] = fmaf(xr[v][j], xr[v][j], ssq[v]);
+      amax = fmaxf(amax, fabsf(xr[v][j]));
+      if (g == 0) ssq = fmaf(xr[v][j], xr[v][j], ssq);
       xsum[v] += xr[v][j];
     }
-  }
-  // CTA-wide max |x| and sum x^2 per vector (consumer threads only)
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    float a = warp_max_all(amax[v]);
-    float q = warp_sum_xor<32>(ssq[v]);
-    if (lane == 0) {
-      scratch[(2 * v) * nwarps + warp] = a;
-      scratch[(2 * v + 1) * nwarps + warp] = q;
+    if (!is_fin) {
+      amax = warp_max_all(amax);
+      ssq = warp_sum_xor<32>(ssq);
+      if (lane == 0) {
+        scratch[(2 * v) * nwarps + (tid >> 5)] = amax;
+        scratch[(2 * v + 1) * nwarps + (tid >> 5)] = ssq;
+      }
     }
   }
-  named_sync(1, nthreads);
+  named_sync(1, nthreads + (has_fin ? 32 : 0));
   int expo[NV];
   float outscale[NV];
 #pragma unroll
@@ -239,9 +214,7 @@ __global__ void __launch_bounds__(kMaxConsumers + kProducerThreads, 1) gemv_kern
     }
     // |x| < 2^E; activations are stored as x * 2^(126 - E - shift) so that
     // every product lands at scale 2^(-23 - E).
-    int eb = (__float_as_int(a) >> 23) & 0xFF;
-    if (eb == 0) eb = 1;
-    const int E = eb - 126;
+    const int E = bound_exponent(a);
     expo[v] = E;
 #pragma unroll
     for (int j = 0; j < 32; ++j) xr[v][j] = scale_pow2(xr[v][j], 126 - E - Fmt<FMT>::shift(j));
@@ -250,13 +223,45 @@ __global__ void __launch_bounds__(kMaxConsumers + kProducerThreads, 1) gemv_kern
     if (p.rms) r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.cols)), p.rms_eps)));
     outscale[v] = r;
   }
-
-  // per-tile loop
   constexpr int RH = SWIGLU ? RPG / 2 : RPG;  // gate rows per group (swiglu)
+
+  // ------------------------------------------------------------------ finisher
+  if (is_fin) {
+    for (int t = 0; t < ntiles; ++t) {
+      const int b = t % kRedRing;
+      if (!warp_wait(&rfull[b], (t / kRedRing) & 1, p.err, DEVERR_RED_WAIT, t)) return;
+      const float *rbuf = red + b * red_stride;
+      const int64_t r0 = rb + static_cast<int64_t>(t) * p.tile_rows;
+      const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
+      for (int o = lane; o < nr; o += 32) {
+        const int gg = o / RH, k = o % RH;
+        for (int v = 0; v < p.nv && v < NV; ++v) {
+          const float *slot = rbuf + (v * p.red_rows + gg * RPG + k) * wpg;
+          float acc = 0.0f;
+          for (int w = 0; w < wpg; ++w) acc += slot[w];
+          float val = unscale(acc, expo[v]) * outscale[v];
+          if (SWIGLU) {
+            const float *us = slot + RH * wpg;
+            float ua = 0.0f;
+            for (int w = 0; w < wpg; ++w) ua += us[w];
+            val = silu(val) * (unscale(ua, expo[v]) * outscale[v]);
+          }
+          store_row(p, v, r0 + o, val);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[b]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int W = p.tpr < 32 ? p.tpr : 32;
+  const int wg = c >> 5;
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % p.stages;
-    if (!warp_wait(&full[s], (t / p.stages) & 1, p.err, DEVERR_FULL_WAIT)) return;
-    const uint8_t *base = smem + L.stage_off + static_cast<uint32_t>(s) * p.stage_bytes;
+    if (!warp_wait(&full[s], (t / p.stages) & 1, p.err, DEVERR_FULL_WAIT, t)) return;
+    const uint8_t *base = smem + static_cast<uint32_t>(s) * p.stage_bytes;
     const int64_t r0 = rb + static_cast<int64_t>(t) * p.tile_rows;
     const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
     float part[NV][RPG];
@@ -278,73 +283,32 @@ __global__ void __launch_bounds__(kMaxConsumers + kProducerThreads, 1) gemv_kern
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 
-    // reduce over the group
-    int ri = reduce_scatter<RPG, NV>(part, W, lane % W);
-    float res[NV];
-#pragma unroll
-    for (int v = 0; v < NV; ++v) res[v] = 0.0f;
-    int row_k = -1;  // which of the group's RPG rows this thread finalizes
-    if (p.tpr > 32) {
-      const int wpg = p.tpr / 32;
-      const int wg = c >> 5;
-      float *rbuf = red + (t & 1) * NV * p.red_rows * wpg;
-      const int per_row = 32 / RPG;
-      if ((lane % per_row) == 0) {
+    const int ri = reduce_scatter<RPG, NV>(part, W, lane % W);
+    if (has_fin) {
+      // hand the warp's row partials to the finisher through the ring
+      const int b = t % kRedRing;
+      if (t >= kRedRing && !warp_wait(&rempty[b], ((t / kRedRing) - 1) & 1, p.err, DEVERR_RED_WAIT, t)) return;
+      float *rbuf = red + b * red_stride;
+      if ((lane % (32 / RPG)) == 0) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) rbuf[(v * p.red_rows + g * RPG + ri) * wpg + wg] = part[v][0];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&redbar[t & 1]);
-      if (wg == 0) {
-        if (!warp_wait(&redbar[t & 1], (t >> 1) & 1, p.err, DEVERR_FULL_WAIT)) return;
-        if (c < RPG) {
-#pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            float acc = 0.0f;
-            for (int w = 0; w < wpg; ++w) acc += rbuf[(v * p.red_rows + g * RPG + c) * wpg + w];
-            res[v] = acc;
-          }
-          row_k = c;
-        }
-      }
+      if (lane == 0) mbar_arrive(&rfull[b]);
     } else {
-#pragma unroll
-      for (int v = 0; v < NV; ++v) res[v] = part[v][0];
-      if (((lane % W) % (W / RPG)) == 0) row_k = ri;
-    }
-
-    // epilogue
-    if (SWIGLU) {
-      // gate row k (< RH) pairs with up row k + RH
+      // the whole row lives in this warp: the first lane of each run finishes it
       float up[NV];
-      if (p.tpr > 32) {
 #pragma unroll
-        for (int v = 0; v < NV; ++v) up[v] = __shfl_down_sync(0xffffffffu, res[v], RH);
-      } else {
-#pragma unroll
-        for (int v = 0; v < NV; ++v) up[v] = __shfl_xor_sync(0xffffffffu, res[v], W / 2);
-      }
-      if (row_k >= 0 && row_k < RH) {
-        const int lr = g * RH + row_k;
+      for (int v = 0; v < NV; ++v) up[v] = SWIGLU ? __shfl_xor_sync(0xffffffffu, part[v][0], W / 2) : 0.0f;
+      const bool holder = ((lane % W) % (W / RPG)) == 0;
+      if (holder && (!SWIGLU || ri < RH)) {
+        const int lr = SWIGLU ? g * RH + ri : g * RPG + ri;
         if (lr < nr) {
-          const int64_t orow = r0 + lr;
           for (int v = 0; v < p.nv && v < NV; ++v) {
-            const float gv = scale_pow2(res[v], 23 + expo[v]) * outscale[v];
-            const float uv = scale_pow2(up[v], 23 + expo[v]) * outscale[v];
-            float o = silu(gv) * uv;
-            if (p.residual) o += p.residual[v * p.y_stride + orow];
-            p.y[v * p.y_stride + orow] = o;
+            float val = unscale(part[v][0], expo[v]) * outscale[v];
+            if (SWIGLU) val = silu(val) * (unscale(up[v], expo[v]) * outscale[v]);
+            store_row(p, v, r0 + lr, val);
           }
-        }
-      }
-    } else if (row_k >= 0) {
-      const int lr = g * RPG + row_k;
-      if (lr < nr) {
-        const int64_t orow = r0 + lr;
-        for (int v = 0; v < p.nv && v < NV; ++v) {
-          float o = scale_pow2(res[v], 23 + expo[v]) * outscale[v];
-          if (p.residual) o += p.residual[v * p.y_stride + orow];
-          p.y[v * p.y_stride + orow] = o;
         }
       }
     }
@@ -370,26 +334,28 @@ bool make_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, int n
   pl->tpr = nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32;
   if (pl->tpr > kMaxConsumers) return false;
   pl->groups = std::max(1, kMaxConsumers / pl->tpr);
-  const int wcap = std::min(pl->tpr, 32);
-  const int rmax = std::min(8, wcap);
-  const int64_t per_row = row_bytes * (swiglu ? 2 : 1);
-  int rpg = swiglu ? 2 : 1;
-  while (rpg * 2 <= rmax && static_cast<int64_t>(pl->groups) * rpg * 2 * per_row <= kTileTarget) rpg *= 2;
-  pl->rpg = rpg;
-  const int rows_per_tile = pl->groups * (swiglu ? rpg / 2 : rpg);
-  pl->tile_rows = rows_per_tile;
-  pl->stage_bytes = static_cast<uint32_t>(((rows_per_tile * per_row) + 15) & ~int64_t(15));
-  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, kSmemTarget / pl->stage_bytes)));
-  const int red_rows = pl->groups * rpg;
-  while (pl->stages > 2 &&
-         smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, pl->groups * pl->tpr).total >
-             static_cast<uint32_t>(dev.max_smem_optin))
-    --pl->stages;
-  pl->smem = smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, pl->groups * pl->tpr).total;
-  if (pl->smem > static_cast<uint32_t>(dev.max_smem_optin)) return false;
   int64_t g = std::min<int64_t>(dev.sm_count, (rows_out + 7) / 8);
   pl->grid = static_cast<unsigned>(std::max<int64_t>(1, g));
-  return true;
+  const int64_t rows_per_cta = (rows_out + pl->grid - 1) / pl->grid;
+  const int rmax = std::min(8, std::min(pl->tpr, 32));
+  const int64_t per_row = row_bytes * (swiglu ? 2 : 1);
+  auto tile_rows_of = [&](int r) { return static_cast<int64_t>(pl->groups) * (swiglu ? r / 2 : r); };
+  int rpg = swiglu ? 2 : 1;
+  // grow the tile while it fits the stage target and the CTA keeps >= 2 tiles
+  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= kTileTarget &&
+         tile_rows_of(rpg * 2) * 2 <= rows_per_cta)
+    rpg *= 2;
+  pl->rpg = rpg;
+  pl->tile_rows = static_cast<int>(tile_rows_of(rpg));
+  pl->stage_bytes = static_cast<uint32_t>(((pl->tile_rows * per_row) + 15) & ~int64_t(15));
+  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, kSmemTarget / pl->stage_bytes)));
+  const int red_rows = pl->groups * rpg;
+  const int nthreads = pl->groups * pl->tpr;
+  while (pl->stages > 2 && smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total >
+                               static_cast<uint32_t>(dev.max_smem_optin))
+    --pl->stages;
+  pl->smem = smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total;
+  return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
 }
 
 template <int FMT, int NV, int RPG, bool SW>
@@ -397,7 +363,7 @@ cudaError_t launch_one(const GemvParams &p, const Plan &pl, cudaStream_t s, bool
   auto k = gemv_kernel<FMT, NV, RPG, SW>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(pl.grid), block(pl.groups * pl.tpr + kProducerThreads);
+  const dim3 grid(pl.grid), block(pl.groups * pl.tpr + 32 + (pl.tpr > 32 ? 32 : 0));
   if (pdl) return launch_pdl(k, grid, block, pl.smem, s, p);
   k<<<grid, block, pl.smem, s>>>(p);
   return cudaGetLastError();
@@ -440,6 +406,7 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   if (!aligned16(blocks) || !aligned16(x) || !aligned16(y) || (opts.residual && !aligned16(opts.residual)))
     return EPQ_ERR_ALIGN;
   if (opts.rms_prenorm && !(opts.rms_eps >= 0.0f)) return EPQ_ERR_ARG;
+  if (opts.x_ld < 0 || (opts.x_ld && (opts.x_ld % 4 || opts.x_ld < cols / xg))) return EPQ_ERR_ARG;
   DeviceInfo dev;
   if (!current_device(&dev) || dev.major * 10 + dev.minor < 100) return EPQ_ERR_DEVICE;
   unsigned *err = device_error_slot();
@@ -465,13 +432,13 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   p.red_rows = pl.groups * pl.rpg;
   p.stages = pl.stages;
   p.stage_bytes = pl.stage_bytes;
-  p.x_stride = cols / xg;
+  p.x_stride = opts.x_ld ? opts.x_ld : cols / xg;
   p.y_stride = rows_out;
   p.rms = opts.rms_prenorm;
   p.rms_eps = opts.rms_eps;
   p.x_group = xg;
   p.x_head_dim = opts.x_head_dim;
-  p.early_weights = 0;
+  p.early_weights = opts.weights_ready ? 1 : 0;
   p.err = err;
   for (int v0 = 0; v0 < nvec; v0 += 2) {
     p.nv = std::min(2, nvec - v0);
@@ -480,10 +447,10 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
     p.residual = opts.residual ? opts.residual + v0 * p.y_stride : nullptr;
     cudaError_t e = cudaErrorInvalidValue;
     switch (fmt) {
-      case EPQ_Q8_0: e = dispatch_fmt<EPQ_Q8_0>(p, pl, s, false, sw); break;
-      case EPQ_Q4_0: e = dispatch_fmt<EPQ_Q4_0>(p, pl, s, false, sw); break;
-      case EPQ_Q4_1: e = dispatch_fmt<EPQ_Q4_1>(p, pl, s, false, sw); break;
-      case EPQ_Q4_K: e = dispatch_fmt<EPQ_Q4_K>(p, pl, s, false, sw); break;
+      case EPQ_Q8_0: e = dispatch_fmt<EPQ_Q8_0>(p, pl, s, true, sw); break;
+      case EPQ_Q4_0: e = dispatch_fmt<EPQ_Q4_0>(p, pl, s, true, sw); break;
+      case EPQ_Q4_1: e = dispatch_fmt<EPQ_Q4_1>(p, pl, s, true, sw); break;
+      case EPQ_Q4_K: e = dispatch_fmt<EPQ_Q4_K>(p, pl, s, true, sw); break;
     }
     if (e != cudaSuccess) return cuda_fail(e);
   }

@@ -188,4 +188,74 @@ struct XGather {
   }
 };
 
+// Butterfly reduce-scatter of RPG partials over W lanes (W = segment width,
+// a power of two >= RPG).  The first log2(RPG) levels (offsets W/2, W/4, ...)
+// halve the set of rows a lane carries; the remaining levels are plain
+// butterflies.  On return v[.][0] holds the full sum of row `base` (the
+// returned index); the W/RPG lanes of each run share a row.
+template <int RPG, int NV>
+__device__ __forceinline__ int reduce_scatter(float (&v)[NV][RPG], int W, int lane) {
+  int base = 0;
+  int o = W >> 1;
+#pragma unroll
+  for (int n = RPG; n > 1; n >>= 1) {
+    const int h = n / 2;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+#pragma unroll
+      for (int q = 0; q < NV; ++q) {
+        const float send = upper ? v[q][i] : v[q][i + h];
+        const float keep = upper ? v[q][i + h] : v[q][i];
+        v[q][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    if (upper) base += h;
+    o >>= 1;
+  }
+  for (; o >= 1; o >>= 1) {
+#pragma unroll
+    for (int q = 0; q < NV; ++q) v[q][0] += __shfl_xor_sync(0xffffffffu, v[q][0], o);
+  }
+  return base;
+}
+
+
+// Activation column loader: 32 consecutive floats of x (16-byte aligned).
+__device__ __forceinline__ void load_column(const float *src, float (&xr)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 q = *reinterpret_cast<const float4 *>(src + j);
+    xr[j] = q.x;
+    xr[j + 1] = q.y;
+    xr[j + 2] = q.z;
+    xr[j + 3] = q.w;
+  }
+}
+
+// Exponent E with |v| < 2^E for every |v| <= amax (amax >= 0, finite).
+__device__ __forceinline__ int bound_exponent(float amax) {
+  int eb = (__float_as_int(amax) >> 23) & 0xFF;
+  if (eb == 0) eb = 1;
+  return eb - 126;
+}
+
+// Turn a loaded column into the scaled form column_dot() expects:
+// x_j * 2^(126 - E - shift_j), and return sum(x) * 2^(-23 - E).
+template <int FMT>
+__device__ __forceinline__ float scale_column(float (&xr)[32], int E) {
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) s += xr[j];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) xr[j] = scale_pow2(xr[j], 126 - E - Fmt<FMT>::shift(j));
+  return scale_pow2(s, -23 - E);
+}
+
+// Undo the scaling of a finished row sum.
+__device__ __forceinline__ float unscale(float v, int E) { return scale_pow2(v, 23 + E); }
+
+// silu(g) = g / (1 + exp(-g))
+__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+
 }  // namespace epq

@@ -1,0 +1,817 @@
+// Mixture-of-experts layer (epq_moe_forward).
+//
+// "Flash-MoE：在笔记本上运行 397B 参数大模型", section "每层流水线": router
+// matvec, softmax + top-K, then the selected experts' forward and the
+// combine.  Here all of it stays on the GPU in three kernels on one stream:
+//
+//   1. router_kernel   logits = R xin (+bias) for every token (warp per
+//                      expert row); the last CTA to finish (an atomic ticket,
+//                      no spinning) runs softmax + top-K per token and groups
+//                      tokens by expert: the distinct experts in ascending
+//                      order become "slots", each with its list of
+//                      (token, choice) entries; the shared expert is the last
+//                      slot and serves every token.
+//   2. gateup_kernel   persistent TMA-staged dequant-GEMV over the virtual
+//                      rows slot*I + i: each tile stages the gate rows and the
+//                      matching up rows of one expert; every token entry of
+//                      the slot reuses the staged bytes; the epilogue writes
+//                      h = silu(g) * u and records max|h| per (token, slot).
+//   3. down_kernel     persistent over hidden rows: for each tile of rows the
+//                      down rows of every slot are staged in turn, applied to
+//                      each entry's h, weighted and accumulated per token in
+//                      shared memory; then y = x + accumulated sum.
+//
+// Each expert's weights are read once per layer however many tokens use it.
+#include <algorithm>
+
+#include "gemv_core.cuh"
+
+namespace epq {
+namespace {
+
+constexpr int kMaxTok = 16;
+constexpr int kMaxTopk = 16;
+constexpr int kMaxExperts = 1024;
+constexpr int kRouterThreads = 256;
+constexpr int kMaxConsumers = 512;
+constexpr int kTileTarget = 40 * 1024;
+constexpr int kSmemTarget = 160 * 1024;
+
+// ------------------------------------------------------------------ workspace
+struct WsLayout {
+  size_t counter, logits, xstat, gshared, idx, w, meta, active, cnt, list, hmax, h, total;
+};
+
+inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int ntok, int topk, int E, int I) {
+  WsLayout L;
+  size_t o = 0;
+  const size_t slots = static_cast<size_t>(ntok) * topk + 1;
+  L.counter = o; o = al256(o + 16);
+  L.logits = o; o = al256(o + 4ull * ntok * E);
+  L.xstat = o; o = al256(o + 8ull * ntok);
+  L.gshared = o; o = al256(o + 4ull * ntok);
+  L.idx = o; o = al256(o + 4ull * ntok * topk);
+  L.w = o; o = al256(o + 4ull * ntok * topk);
+  L.meta = o; o = al256(o + 16);
+  L.active = o; o = al256(o + 4ull * slots);
+  L.cnt = o; o = al256(o + 4ull * slots);
+  L.list = o; o = al256(o + 4ull * slots * ntok);
+  L.hmax = o; o = al256(o + 4ull * ntok * (topk + 1));
+  L.h = o; o = al256(o + 4ull * ntok * (topk + 1) * I);
+  L.total = o;
+  return L;
+}
+
+struct MoeArgs {
+  // router
+  const float *R;
+  const float *bias;
+  const float *gvec;
+  int E, H, I, ntok, topk, norm_topk, rms;
+  float eps;
+  int has_shared;
+  // experts
+  const uint8_t *gate_up;
+  int64_t gu_stride;
+  const uint8_t *down;
+  int64_t dn_stride;
+  const uint8_t *sh_gate_up;
+  const uint8_t *sh_down;
+  int64_t gu_row_bytes, dn_row_bytes;
+  // io
+  const float *x;
+  float *y;
+  int32_t *out_idx;
+  float *out_w;
+  // workspace views
+  uint32_t *counter;
+  float *logits;
+  float *xstat;      // [ntok][2]: max|x| (as float), rms factor
+  float *gshared;    // [ntok]
+  int32_t *idx;      // [ntok][topk]
+  float *w;          // [ntok][topk]
+  int32_t *meta;     // [0] = n_active, [1] = n_slots
+  int32_t *active;   // [slots] expert id
+  int32_t *cnt;      // [slots] entries
+  int32_t *list;     // [slots][ntok] entry = t*32 + k (k == topk: shared)
+  uint32_t *hmax;    // [ntok][topk+1] bits of max|h|
+  float *h;          // [ntok][topk+1][I]
+  unsigned *err;
+};
+
+// ------------------------------------------------------------------ 1. router
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a) {
+  __shared__ float s_rms[kMaxTok];
+  __shared__ float s_red[kRouterThreads / 32][kMaxTok];
+  __shared__ int s_last;
+  __shared__ int s_slot_of[kMaxExperts];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();
+
+  // per-token sum of squares and max |x| (every CTA: it needs the rms factor)
+  for (int t = 0; t < a.ntok; ++t) {
+    float ss = 0.0f, mx = 0.0f;
+    for (int j = tid; j < a.H; j += kRouterThreads) {
+      const float v = a.x[static_cast<int64_t>(t) * a.H + j];
+      ss = fmaf(v, v, ss);
+      mx = fmaxf(mx, fabsf(v));
+    }
+    ss = warp_sum_xor<32>(ss);
+    mx = warp_max_all(mx);
+    if (lane == 0) s_red[warp][t] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float tot = 0.0f;
+      for (int w = 0; w < kRouterThreads / 32; ++w) tot += s_red[w][t];
+      s_rms[t] = a.rms ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(a.H)), a.eps))) : 1.0f;
+    }
+    __syncthreads();
+    if (lane == 0) s_red[warp][t] = mx;
+    __syncthreads();
+    if (tid == 0 && blockIdx.x == 0) {
+      float m = 0.0f;
+      for (int w = 0; w < kRouterThreads / 32; ++w) m = fmaxf(m, s_red[w][t]);
+      a.xstat[2 * t] = m;
+      a.xstat[2 * t + 1] = s_rms[t];
+    }
+    __syncthreads();
+  }
+
+  // logits: warp per row; rows E .. (shared gate vector) as one extra row
+  const int nrows = a.E + (a.gvec ? 1 : 0);
+  const int r_begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * nrows) / gridDim.x);
+  const int r_end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * nrows) / gridDim.x);
+  for (int r = r_begin + warp; r < r_end; r += kRouterThreads / 32) {
+    const float *wrow = r < a.E ? a.R + static_cast<int64_t>(r) * a.H : a.gvec;
+    float acc[kMaxTok];
+#pragma unroll
+    for (int t = 0; t < kMaxTok; ++t) acc[t] = 0.0f;
+    for (int j = lane * 4; j < a.H; j += 128) {
+      const float4 wv = *reinterpret_cast<const float4 *>(wrow + j);
+#pragma unroll
+      for (int t = 0; t < kMaxTok; ++t) {
+        if (t < a.ntok) {
+          const float4 xv = *reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(t) * a.H + j);
+          acc[t] = fmaf(wv.x, xv.x, fmaf(wv.y, xv.y, fmaf(wv.z, xv.z, fmaf(wv.w, xv.w, acc[t]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxTok; ++t) {
+      if (t < a.ntok) {
+        const float v = warp_sum_xor<32>(acc[t]) * s_rms[t];
+        if (lane == 0) {
+          if (r < a.E) {
+            a.logits[static_cast<int64_t>(t) * a.E + r] = v + (a.bias ? a.bias[r] : 0.0f);
+          } else {
+            a.gshared[t] = __fdiv_rn(1.0f, 1.0f + expf(-v));
+          }
+        }
+      }
+    }
+  }
+
+  // ticket: the last CTA to arrive finishes the routing
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned ticket = atomicAdd(a.counter, 1u);
+    s_last = ticket == gridDim.x - 1;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  // softmax + top-K: warp per token
+  for (int t = warp; t < a.ntok; t += kRouterThreads / 32) {
+    const float *lt = a.logits + static_cast<int64_t>(t) * a.E;
+    float lmax = -INFINITY;
+    for (int e = lane; e < a.E; e += 32) lmax = fmaxf(lmax, __ldcg(lt + e));
+    lmax = warp_max_all(lmax);
+    float den = 0.0f;
+    for (int e = lane; e < a.E; e += 32) den += expf(__ldcg(lt + e) - lmax);
+    den = warp_sum_xor<32>(den);
+    float lv[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) lv[i] = (lane + 32 * i < a.E) ? __ldcg(lt + lane + 32 * i) : -INFINITY;
+    float sel_sum = 0.0f;
+    int prev_e = -1;
+    float prev_v = INFINITY;
+    float pk[kMaxTopk];
+    int ek[kMaxTopk];
+    for (int k = 0; k < a.topk; ++k) {
+      // best remaining: largest value, then lowest index, strictly after (prev_v, prev_e)
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        const float v = lv[i];
+        const bool after = v < prev_v || (v == prev_v && e > prev_e);
+        if (e < a.E && after && (v > bv || (v == bv && e < be))) {
+          bv = v;
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int e2 = __shfl_xor_sync(0xffffffffu, be, o);
+        if (v2 > bv || (v2 == bv && e2 < be)) {
+          bv = v2;
+          be = e2;
+        }
+      }
+      prev_v = bv;
+      prev_e = be;
+      const float p = __fdiv_rn(expf(bv - lmax), den);
+      if (k < kMaxTopk) {
+        pk[k] = p;
+        ek[k] = be;
+      }
+      sel_sum += p;
+    }
+    if (lane == 0) {
+      for (int k = 0; k < a.topk; ++k) {
+        const float wk = a.norm_topk ? __fdiv_rn(pk[k], sel_sum) : pk[k];
+        a.idx[t * a.topk + k] = ek[k];
+        a.w[t * a.topk + k] = wk;
+        if (a.out_idx) a.out_idx[t * a.topk + k] = ek[k];
+        if (a.out_w) a.out_w[t * a.topk + k] = wk;
+      }
+    }
+  }
+  __syncthreads();
+
+  // group tokens by expert: slots in ascending expert order (block scan)
+  __shared__ int s_idx[kMaxTok * kMaxTopk];
+  __shared__ int s_wsum[kRouterThreads / 32];
+  const int nsel = a.ntok * a.topk;
+  for (int e = tid; e < a.E; e += kRouterThreads) s_slot_of[e] = 0;
+  for (int i = tid; i < nsel; i += kRouterThreads) s_idx[i] = __ldcg(a.idx + i);
+  __syncthreads();
+  for (int i = tid; i < nsel; i += kRouterThreads) s_slot_of[s_idx[i]] = 1;
+  __syncthreads();
+  constexpr int EPT = kMaxExperts / kRouterThreads;  // experts per thread
+  int flags = 0, cntl = 0;
+#pragma unroll
+  for (int q = 0; q < EPT; ++q) {
+    const int e = tid * EPT + q;
+    if (e < a.E && s_slot_of[e]) {
+      flags |= 1 << q;
+      ++cntl;
+    }
+  }
+  int incl = cntl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int woff = 0, total = 0;
+  for (int w = 0; w < kRouterThreads / 32; ++w) {
+    if (w < warp) woff += s_wsum[w];
+    total += s_wsum[w];
+  }
+  __syncthreads();
+  int pos = woff + incl - cntl;
+#pragma unroll
+  for (int q = 0; q < EPT; ++q) {
+    const int e = tid * EPT + q;
+    if (e < a.E) {
+      if (flags & (1 << q)) {
+        a.active[pos] = e;
+        s_slot_of[e] = pos++;
+      } else {
+        s_slot_of[e] = -1;
+      }
+    }
+  }
+  if (tid == 0) {
+    a.meta[0] = total;
+    a.meta[1] = total + (a.has_shared ? 1 : 0);
+  }
+  __syncthreads();
+  const int nact = total;
+  for (int s = tid; s < nact + (a.has_shared ? 1 : 0); s += kRouterThreads) {
+    int c = 0;
+    for (int t = 0; t < a.ntok; ++t) {
+      for (int k = 0; k < a.topk; ++k) {
+        if (s < nact ? s_slot_of[s_idx[t * a.topk + k]] == s : k == 0) {
+          a.list[s * a.ntok + c++] = t * 32 + (s < nact ? k : a.topk);
+        }
+      }
+    }
+    a.cnt[s] = c;
+  }
+  for (int i = tid; i < a.ntok * (a.topk + 1); i += kRouterThreads) a.hmax[i] = 0u;
+  if (tid == 0) *a.counter = 0u;
+}
+
+// ------------------------------------------------------------------ engine plan
+struct EnginePlan {
+  int tpr, groups, rpg, tile_rows, stages;
+  uint32_t stage_bytes, smem, red_off, bar_off, acc_off;
+};
+
+int next_pow2(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// cols: weights per row; per_row: staged bytes per output row; extra: smem
+// after the ring (reduction buffers and accumulators).
+bool engine_plan(int cols, int64_t per_row, bool swiglu, int acc_floats_per_row, const DeviceInfo &dev,
+                 EnginePlan *pl) {
+  const int nblk = cols / 32;
+  pl->tpr = nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32;
+  if (pl->tpr > kMaxConsumers) return false;
+  pl->groups = std::max(1, kMaxConsumers / pl->tpr);
+  const int rmax = std::min(8, std::min(pl->tpr, 32));
+  int rpg = swiglu ? 2 : 1;
+  while (rpg * 2 <= rmax && static_cast<int64_t>(pl->groups) * (swiglu ? rpg : rpg * 2) * per_row <= kTileTarget)
+    rpg *= 2;
+  pl->rpg = rpg;
+  pl->tile_rows = pl->groups * (swiglu ? rpg / 2 : rpg);
+  pl->stage_bytes = static_cast<uint32_t>((pl->tile_rows * per_row + 15) & ~int64_t(15));
+  const int wpg = pl->tpr > 32 ? pl->tpr / 32 : 1;
+  const uint32_t red_bytes = 4u * 2 * pl->groups * rpg * wpg;
+  const uint32_t acc_bytes = 4u * kMaxTok * pl->tile_rows * acc_floats_per_row;
+  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, kSmemTarget / pl->stage_bytes)));
+  for (;;) {
+    uint32_t o = pl->stages * pl->stage_bytes + 16;
+    o = (o + 15) & ~15u;
+    pl->bar_off = o;
+    o += 16u * pl->stages + 16;
+    pl->red_off = o;
+    o += red_bytes;
+    pl->acc_off = o;
+    o += acc_bytes;
+    pl->smem = (o + 15) & ~15u;
+    if (pl->smem <= static_cast<uint32_t>(dev.max_smem_optin) || pl->stages <= 2) break;
+    --pl->stages;
+  }
+  return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
+}
+
+struct EngineArgs {
+  MoeArgs a;
+  int tpr, groups, tile_rows, stages;
+  uint32_t stage_bytes, red_off, bar_off, acc_off;
+};
+
+// Cross-thread reduction of RPG partials of a tile (see gemv.cu).  Returns
+// the row (0..RPG-1 within the group) this thread finalizes, or -1; `res`
+// holds that row's sum.  `rbuf` is this tile's half of the shared buffer.
+template <int RPG>
+__device__ __forceinline__ int reduce_rows(float (&part)[1][RPG], float &res, const EngineArgs &p, int g, int c,
+                                           int lane, float *rbuf, uint64_t *redbar, int phase, bool &ok) {
+  const int W = p.tpr < 32 ? p.tpr : 32;
+  const int ri = reduce_scatter<RPG, 1>(part, W, lane % W);
+  res = 0.0f;
+  if (p.tpr > 32) {
+    const int wpg = p.tpr / 32;
+    const int wg = c >> 5;
+    if ((lane % (32 / RPG)) == 0) rbuf[(g * RPG + ri) * wpg + wg] = part[0][0];
+    __syncwarp();
+    // all consumer warps wait (double buffer: see the dense kernel)
+    if (lane == 0) mbar_arrive(redbar);
+    if (!warp_wait(redbar, phase, p.a.err, DEVERR_RED_WAIT)) {
+      ok = false;
+      return -1;
+    }
+    if (wg == 0 && c < RPG) {
+      float acc = 0.0f;
+      for (int w = 0; w < wpg; ++w) acc += rbuf[(g * RPG + c) * wpg + w];
+      res = acc;
+      return c;
+    }
+    return -1;
+  }
+  res = part[0][0];
+  return (((lane % W) % (W / RPG)) == 0) ? ri : -1;
+}
+
+// ------------------------------------------------------------------ 2. gate/up
+template <int FMT, int RPG>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const EngineArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const MoeArgs &a = p.a;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+  uint64_t *empty = full + p.stages;
+  uint64_t *redbar = empty + p.stages;
+  float *red = reinterpret_cast<float *>(smem + p.red_off);
+  const int nthreads = p.groups * p.tpr;
+  const int nwarps = nthreads / 32;
+  const int tid = threadIdx.x;
+  constexpr int RH = RPG / 2;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nwarps);
+    }
+    mbar_init(&redbar[0], nwarps);
+    mbar_init(&redbar[1], nwarps);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // routing is produced by the router kernel
+
+  const int I = a.I;
+  const int64_t total = static_cast<int64_t>(__ldcg(a.meta + 1)) * I;
+  const int nact = __ldcg(a.meta);
+  const int64_t rb = (static_cast<int64_t>(blockIdx.x) * total) / gridDim.x;
+  const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * total) / gridDim.x;
+  auto tile_len = [&](int64_t r0) {
+    const int64_t lim = min(re, (r0 / I + 1) * I);
+    return static_cast<int>(min(static_cast<int64_t>(p.tile_rows), lim - r0));
+  };
+
+  if (tid >= nthreads) {
+    if (tid != nthreads) return;
+    int t = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
+      const int s = t % p.stages;
+      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT)) {
+        ok = false;
+        break;
+      }
+      const int nr = tile_len(r0);
+      const int slot = static_cast<int>(r0 / I);
+      const int i0 = static_cast<int>(r0 % I);
+      const uint8_t *base = slot < nact ? a.gate_up + static_cast<int64_t>(__ldcg(a.active + slot)) * a.gu_stride
+                                        : a.sh_gate_up;
+      const uint32_t bytes = static_cast<uint32_t>(nr * a.gu_row_bytes);
+      uint8_t *dst = smem + static_cast<uint32_t>(s) * p.stage_bytes;
+      mbar_arrive_expect_tx(&full[s], 2 * bytes);
+      bulk_g2s(dst, base + static_cast<int64_t>(i0) * a.gu_row_bytes, bytes, &full[s]);
+      bulk_g2s(dst + p.tile_rows * a.gu_row_bytes, base + static_cast<int64_t>(I + i0) * a.gu_row_bytes, bytes,
+               &full[s]);
+      ++issued;
+    }
+    if (!ok)
+      for (int u = max(0, issued - p.stages); u < issued; ++u)
+        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT);
+    return;
+  }
+
+  const int g = tid / p.tpr, c = tid % p.tpr, lane = tid & 31;
+  const int nblk = a.H / 32;
+  const bool active = c < nblk;
+  ColConst<FMT> cc;
+  cc.init(active ? c : 0);
+  float xr[1][32];
+  float xs[1] = {0.0f};
+  int cur_t = -1, cur_E = 0;
+  float cur_rms = 1.0f;
+  int t = 0, rphase = 0;
+  for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
+    const int s = t % p.stages;
+    if (!warp_wait(&full[s], (t / p.stages) & 1, a.err, DEVERR_FULL_WAIT)) return;
+    const int nr = tile_len(r0);
+    const int slot = static_cast<int>(r0 / I);
+    const int i0 = static_cast<int>(r0 % I);
+    const uint8_t *stage = smem + static_cast<uint32_t>(s) * p.stage_bytes;
+    const int ne = __ldcg(a.cnt + slot);
+    bool ok = true;
+    for (int j = 0; j < ne; ++j) {
+      const int ent = __ldcg(a.list + slot * a.ntok + j);
+      const int tok = ent >> 5, k = ent & 31;
+      if (tok != cur_t) {
+        cur_t = tok;
+        cur_E = bound_exponent(__ldcg(a.xstat + 2 * tok));
+        cur_rms = __ldcg(a.xstat + 2 * tok + 1);
+        if (active) {
+          load_column(a.x + static_cast<int64_t>(tok) * a.H + 32 * c, xr[0]);
+          xs[0] = scale_column<FMT>(xr[0], cur_E);
+        }
+      }
+      float part[1][RPG];
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) {
+        const int lr = g * RH + (q % RH);
+        float pr[1] = {0.0f};
+        if (active && lr < nr) {
+          const uint8_t *row = stage + static_cast<uint32_t>(lr) * a.gu_row_bytes;
+          if (q >= RH) row += p.tile_rows * a.gu_row_bytes;
+          column_dot<FMT, 1>(row, cc, xr, xs, pr);
+        }
+        part[0][q] = pr[0];
+      }
+      float res;
+      float *rbuf = red + (rphase & 1) * p.groups * RPG * (p.tpr > 32 ? p.tpr / 32 : 1);
+      const int row_k = reduce_rows<RPG>(part, res, p, g, c, lane, rbuf, &redbar[rphase & 1], (rphase >> 1) & 1, ok);
+      ++rphase;
+      float up;
+      if (p.tpr > 32)
+        up = __shfl_down_sync(0xffffffffu, res, RH);
+      else
+        up = __shfl_xor_sync(0xffffffffu, res, (p.tpr < 32 ? p.tpr : 32) / 2);
+      if (__any_sync(0xffffffffu, !ok)) return;
+      if (row_k >= 0 && row_k < RH) {
+        const int lr = g * RH + row_k;
+        if (lr < nr) {
+          const float gv = unscale(res, cur_E) * cur_rms;
+          const float uv = unscale(up, cur_E) * cur_rms;
+          const float hv = silu(gv) * uv;
+          const int hs = tok * (a.topk + 1) + k;
+          a.h[static_cast<int64_t>(hs) * I + i0 + lr] = hv;
+          atomicMax(a.hmax + hs, __float_as_uint(fabsf(hv)));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+// ------------------------------------------------------------------ 3. down + combine
+template <int FMT, int RPG>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_kernel(const EngineArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const MoeArgs &a = p.a;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+  uint64_t *empty = full + p.stages;
+  uint64_t *redbar = empty + p.stages;
+  float *red = reinterpret_cast<float *>(smem + p.red_off);
+  float *acc = reinterpret_cast<float *>(smem + p.acc_off);  // [kMaxTok][tile_rows]
+  const int nthreads = p.groups * p.tpr;
+  const int nwarps = nthreads / 32;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nwarps);
+    }
+    mbar_init(&redbar[0], nwarps);
+    mbar_init(&redbar[1], nwarps);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < kMaxTok * p.tile_rows; i += blockDim.x) acc[i] = 0.0f;
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // h, routing and hmax come from the previous kernels
+
+  const int H = a.H, I = a.I;
+  const int nslots = __ldcg(a.meta + 1);
+  const int nact = __ldcg(a.meta);
+  const int64_t rb = (static_cast<int64_t>(blockIdx.x) * H) / gridDim.x;
+  const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * H) / gridDim.x;
+  const int ntiles = static_cast<int>((re - rb + p.tile_rows - 1) / p.tile_rows);
+  const int nunits = ntiles * nslots;
+
+  if (tid >= nthreads) {
+    if (tid != nthreads) return;
+    int issued = 0;
+    bool ok = true;
+    for (int u = 0; u < nunits; ++u) {
+      const int s = u % p.stages;
+      if (u >= p.stages && !mbar_wait(&empty[s], ((u / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT)) {
+        ok = false;
+        break;
+      }
+      const int tile = u / nslots, slot = u % nslots;
+      const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
+      const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
+      const uint8_t *base = slot < nact ? a.down + static_cast<int64_t>(__ldcg(a.active + slot)) * a.dn_stride
+                                        : a.sh_down;
+      const uint32_t bytes = static_cast<uint32_t>(nr * a.dn_row_bytes);
+      mbar_arrive_expect_tx(&full[s], bytes);
+      bulk_g2s(smem + static_cast<uint32_t>(s) * p.stage_bytes, base + r0 * a.dn_row_bytes, bytes, &full[s]);
+      ++issued;
+    }
+    if (!ok)
+      for (int u = max(0, issued - p.stages); u < issued; ++u)
+        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT);
+    return;
+  }
+
+  const int g = tid / p.tpr, c = tid % p.tpr, lane = tid & 31;
+  const int nblk = I / 32;
+  const bool active = c < nblk;
+  ColConst<FMT> cc;
+  cc.init(active ? c : 0);
+  float xr[1][32];
+  float xs[1] = {0.0f};
+  int rphase = 0;
+  int my_row = -1;  // tile row this thread finalizes (same for every unit)
+  for (int u = 0; u < nunits; ++u) {
+    const int s = u % p.stages;
+    if (!warp_wait(&full[s], (u / p.stages) & 1, a.err, DEVERR_FULL_WAIT)) return;
+    const int tile = u / nslots, slot = u % nslots;
+    const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
+    const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
+    const uint8_t *stage = smem + static_cast<uint32_t>(s) * p.stage_bytes;
+    const int ne = __ldcg(a.cnt + slot);
+    bool ok = true;
+    for (int j = 0; j < ne; ++j) {
+      const int ent = __ldcg(a.list + slot * a.ntok + j);
+      const int tok = ent >> 5, k = ent & 31;
+      const int hs = tok * (a.topk + 1) + k;
+      const int E = bound_exponent(__uint_as_float(__ldcg(a.hmax + hs)));
+      if (active) {
+        load_column(a.h + static_cast<int64_t>(hs) * I + 32 * c, xr[0]);
+        xs[0] = scale_column<FMT>(xr[0], E);
+      }
+      float part[1][RPG];
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) {
+        const int lr = g * RPG + q;
+        float pr[1] = {0.0f};
+        if (active && lr < nr) column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes, cc, xr, xs, pr);
+        part[0][q] = pr[0];
+      }
+      float res;
+      float *rbuf = red + (rphase & 1) * p.groups * RPG * (p.tpr > 32 ? p.tpr / 32 : 1);
+      const int row_k = reduce_rows<RPG>(part, res, p, g, c, lane, rbuf, &redbar[rphase & 1], (rphase >> 1) & 1, ok);
+      ++rphase;
+      if (__any_sync(0xffffffffu, !ok)) return;
+      if (row_k >= 0) {
+        my_row = g * RPG + row_k;
+        const float wk = k < a.topk ? __ldcg(a.w + tok * a.topk + k) : (a.gvec ? __ldcg(a.gshared + tok) : 1.0f);
+        acc[tok * p.tile_rows + my_row] += wk * unscale(res, E);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (slot == nslots - 1 && my_row >= 0 && my_row < nr) {
+      // all slots of this tile are in: y = x + weighted expert sum
+      for (int tk = 0; tk < a.ntok; ++tk) {
+        const int64_t o = static_cast<int64_t>(tk) * H + r0 + my_row;
+        a.y[o] = a.x[o] + acc[tk * p.tile_rows + my_row];
+        acc[tk * p.tile_rows + my_row] = 0.0f;
+      }
+    }
+  }
+}
+
+template <typename K>
+cudaError_t launch_engine(K kernel, const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, p.groups * p.tpr + 32, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_gateup(const EngineArgs &p, int rpg, unsigned grid, uint32_t smem, cudaStream_t s) {
+  switch (rpg) {
+    case 2: return launch_engine(gateup_kernel<FMT, 2>, p, grid, smem, s);
+    case 4: return launch_engine(gateup_kernel<FMT, 4>, p, grid, smem, s);
+    case 8: return launch_engine(gateup_kernel<FMT, 8>, p, grid, smem, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int FMT>
+cudaError_t launch_down(const EngineArgs &p, int rpg, unsigned grid, uint32_t smem, cudaStream_t s) {
+  switch (rpg) {
+    case 1: return launch_engine(down_kernel<FMT, 1>, p, grid, smem, s);
+    case 2: return launch_engine(down_kernel<FMT, 2>, p, grid, smem, s);
+    case 4: return launch_engine(down_kernel<FMT, 4>, p, grid, smem, s);
+    case 8: return launch_engine(down_kernel<FMT, 8>, p, grid, smem, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+epq_status check_moe(const epq_router *r, const epq_experts *x, int ntok, int topk) {
+  if (!r || !x) return EPQ_ERR_ARG;
+  if (epq_block_weights(x->fmt) < 0) return EPQ_ERR_FORMAT;
+  if (!r->weight || !x->gate_up || !x->down) return EPQ_ERR_ARG;
+  if (r->n_experts < 1 || r->n_experts > kMaxExperts || x->n_experts != r->n_experts) return EPQ_ERR_ARG;
+  if (ntok < 1 || ntok > kMaxTok || topk < 1 || topk > kMaxTopk || topk > r->n_experts) return EPQ_ERR_ARG;
+  if (x->hidden < 256 || x->hidden > 16384 || x->hidden % 256) return EPQ_ERR_SHAPE;
+  if (x->inter < 256 || x->inter > 16384 || x->inter % 256) return EPQ_ERR_SHAPE;
+  if ((x->shared_gate_up == nullptr) != (x->shared_down == nullptr)) return EPQ_ERR_ARG;
+  if (x->gate_up_stride < 0 || x->down_stride < 0 || x->gate_up_stride % 16 || x->down_stride % 16)
+    return EPQ_ERR_ALIGN;
+  const int64_t gu = 2ll * x->inter * epq_row_bytes(x->fmt, x->hidden);
+  const int64_t dn = static_cast<int64_t>(x->hidden) * epq_row_bytes(x->fmt, x->inter);
+  if ((x->gate_up_stride && x->gate_up_stride < gu) || (x->down_stride && x->down_stride < dn)) return EPQ_ERR_ARG;
+  if (!aligned16(r->weight) || !aligned16(x->gate_up) || !aligned16(x->down) ||
+      (x->shared_gate_up && (!aligned16(x->shared_gate_up) || !aligned16(x->shared_down))) ||
+      (x->shared_gate_vec && !aligned16(x->shared_gate_vec)))
+    return EPQ_ERR_ALIGN;
+  return EPQ_OK;
+}
+
+}  // namespace
+}  // namespace epq
+
+using namespace epq;
+
+extern "C" size_t epq_moe_workspace_bytes(const epq_router *router, const epq_experts *experts, int ntok, int topk) {
+  if (check_moe(router, experts, ntok, topk) != EPQ_OK) return 0;
+  return ws_layout(ntok, topk, router->n_experts, experts->inter).total;
+}
+
+extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts, const float *x, int ntok,
+                                      int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w,
+                                      void *workspace, size_t workspace_bytes, epq_stream_t stream) {
+  epq_status st = check_moe(router, experts, ntok, topk);
+  if (st != EPQ_OK) return st;
+  if (!x || !y) return EPQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y)) return EPQ_ERR_ALIGN;
+  epq_moe_opts o = {};
+  if (opts) o = *opts;
+  if (o.rms_prenorm && !(o.rms_eps >= 0.0f)) return EPQ_ERR_ARG;
+  if (o.h_out && !aligned16(o.h_out)) return EPQ_ERR_ALIGN;
+  const int E = router->n_experts, H = experts->hidden, I = experts->inter;
+  const WsLayout L = ws_layout(ntok, topk, E, I);
+  if (!workspace || workspace_bytes < L.total) return EPQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EPQ_ERR_ALIGN;
+  DeviceInfo dev;
+  if (!current_device(&dev) || dev.major * 10 + dev.minor < 100) return EPQ_ERR_DEVICE;
+  unsigned *err = device_error_slot();
+  if (!err) return EPQ_ERR_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+
+  MoeArgs a = {};
+  a.R = router->weight;
+  a.bias = router->bias;
+  a.gvec = experts->shared_gate_up ? experts->shared_gate_vec : nullptr;
+  a.E = E;
+  a.H = H;
+  a.I = I;
+  a.ntok = ntok;
+  a.topk = topk;
+  a.norm_topk = router->norm_topk;
+  a.rms = o.rms_prenorm;
+  a.eps = o.rms_eps;
+  a.has_shared = experts->shared_gate_up != nullptr;
+  a.gu_row_bytes = epq_row_bytes(experts->fmt, H);
+  a.dn_row_bytes = epq_row_bytes(experts->fmt, I);
+  a.gate_up = static_cast<const uint8_t *>(experts->gate_up);
+  a.gu_stride = experts->gate_up_stride ? experts->gate_up_stride : 2ll * I * a.gu_row_bytes;
+  a.down = static_cast<const uint8_t *>(experts->down);
+  a.dn_stride = experts->down_stride ? experts->down_stride : static_cast<int64_t>(H) * a.dn_row_bytes;
+  a.sh_gate_up = static_cast<const uint8_t *>(experts->shared_gate_up);
+  a.sh_down = static_cast<const uint8_t *>(experts->shared_down);
+  a.x = x;
+  a.y = y;
+  a.out_idx = topk_idx;
+  a.out_w = topk_w;
+  a.counter = reinterpret_cast<uint32_t *>(ws + L.counter);
+  a.logits = o.logits_out ? o.logits_out : reinterpret_cast<float *>(ws + L.logits);
+  a.xstat = reinterpret_cast<float *>(ws + L.xstat);
+  a.gshared = reinterpret_cast<float *>(ws + L.gshared);
+  a.idx = reinterpret_cast<int32_t *>(ws + L.idx);
+  a.w = reinterpret_cast<float *>(ws + L.w);
+  a.meta = reinterpret_cast<int32_t *>(ws + L.meta);
+  a.active = reinterpret_cast<int32_t *>(ws + L.active);
+  a.cnt = reinterpret_cast<int32_t *>(ws + L.cnt);
+  a.list = reinterpret_cast<int32_t *>(ws + L.list);
+  a.hmax = reinterpret_cast<uint32_t *>(ws + L.hmax);
+  a.h = o.h_out ? o.h_out : reinterpret_cast<float *>(ws + L.h);
+  a.err = err;
+
+  const int stages = (o.stages & 7) ? (o.stages & 7) : 7;
+  cudaError_t e = cudaSuccess;
+  if (stages & EPQ_MOE_ROUTE) {
+    // The ticket counter must start at zero: the router's last CTA resets it
+    // after each call; a fresh workspace is cleared here once per call (tiny).
+    e = cudaMemsetAsync(a.counter, 0, 16, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int nrows = E + (a.gvec ? 1 : 0);
+    const unsigned rgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (nrows + 7) / 8)));
+    router_kernel<<<rgrid, kRouterThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  }
+
+  EnginePlan gp, dp;
+  if (!engine_plan(H, 2 * a.gu_row_bytes, true, 0, dev, &gp)) return EPQ_ERR_SHAPE;
+  if (!engine_plan(I, a.dn_row_bytes, false, 1, dev, &dp)) return EPQ_ERR_SHAPE;
+
+  EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_bytes, gp.red_off, gp.bar_off, gp.acc_off};
+  const unsigned ggrid = static_cast<unsigned>(dev.sm_count);
+  if (stages & EPQ_MOE_GATE_UP) switch (experts->fmt) {
+    case EPQ_Q8_0: e = launch_gateup<EPQ_Q8_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
+    case EPQ_Q4_0: e = launch_gateup<EPQ_Q4_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
+    case EPQ_Q4_1: e = launch_gateup<EPQ_Q4_1>(ga, gp.rpg, ggrid, gp.smem, s); break;
+    case EPQ_Q4_K: e = launch_gateup<EPQ_Q4_K>(ga, gp.rpg, ggrid, gp.smem, s); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  EngineArgs da{a, dp.tpr, dp.groups, dp.tile_rows, dp.stages, dp.stage_bytes, dp.red_off, dp.bar_off, dp.acc_off};
+  const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
+  if (stages & EPQ_MOE_DOWN) switch (experts->fmt) {
+    case EPQ_Q8_0: e = launch_down<EPQ_Q8_0>(da, dp.rpg, dgrid, dp.smem, s); break;
+    case EPQ_Q4_0: e = launch_down<EPQ_Q4_0>(da, dp.rpg, dgrid, dp.smem, s); break;
+    case EPQ_Q4_1: e = launch_down<EPQ_Q4_1>(da, dp.rpg, dgrid, dp.smem, s); break;
+    case EPQ_Q4_K: e = launch_down<EPQ_Q4_K>(da, dp.rpg, dgrid, dp.smem, s); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return EPQ_OK;
+}

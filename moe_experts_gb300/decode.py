@@ -1,0 +1,117 @@
+"""Decode-step composition: the per-token sequence of library calls for a
+dense 8B-class decoder and for a MoE decoder, ready to be captured in one
+CUDA graph.
+
+Each layer is pre-norm with a weightless RMS norm (folded into the GEMVs'
+prologue), and attention over a one-token context: softmax over a single
+key is 1, so each query head's output is the value head it reads (grouped
+heads share one value head).  q and k are still computed, so the weight
+traffic is that of a real decode step.  Every step below is one C-ABI call;
+this module holds device buffers and the order of the calls, nothing else.
+
+`timers` (optional) brackets each call of the first layer with a pair of
+CUDA events, so that per-kernel durations can be read after a graph replay.
+"""
+from __future__ import annotations
+
+import contextlib
+
+import torch
+
+from . import _lib as L
+
+
+@contextlib.contextmanager
+def _timed(timers, name, stream, on):
+    if timers is None or not on:
+        yield
+        return
+    a, b = timers.pair(name)
+    a.record(stream)
+    yield
+    b.record(stream)
+
+
+class DenseDecoder:
+    """32-layer dense decoder + LM head, Q-format weights, nvec columns.
+
+    Per layer (h: [nvec, H] residual stream):
+      qkv = Wqkv rms(h)                 (q, k, v rows concatenated)
+      h   = h + Wo v                    (v heads repeated heads/kv_heads times)
+      m   = silu(Wg rms(h)) * (Wu rms(h))
+      h   = h + Wd m
+    then logits = Whead rms(h).
+    """
+
+    def __init__(self, cfg, fmt, layers, head, device, nvec=1):
+        self.cfg, self.fmt, self.layers, self.head, self.nvec = cfg, fmt, layers, head, nvec
+        H = cfg.hidden
+        self.qkv = torch.empty((nvec, cfg.q_rows + 2 * cfg.kv_rows), dtype=torch.float32, device=device)
+        self.m = torch.empty((nvec, cfg.inter), dtype=torch.float32, device=device)
+        self.h = torch.empty((nvec, H), dtype=torch.float32, device=device)
+        self.logits = torch.empty((nvec, cfg.vocab), dtype=torch.float32, device=device)
+
+    def step(self, x, stream=None, timers=None):
+        """x [nvec, H] (read only) -> self.logits."""
+        c, f, H = self.cfg, self.fmt, self.cfg.hidden
+        nq, nkv = c.q_rows, c.kv_rows
+        h = self.h
+        for li, (wqkv, wo, wgu, wd) in enumerate(self.layers):
+            src = x if li == 0 else h
+            on = li == 0
+            with _timed(timers, "gemv_qkv", stream, on):
+                L.epq_gemv_ex(f, wqkv, src, nq + 2 * nkv, H, y=self.qkv, rms_prenorm=True, rms_eps=c.rms_eps,
+                              weights_ready=True, stream=stream)
+            v = self.qkv[:, nq + nkv:]
+            with _timed(timers, "gemv_o", stream, on):
+                L.epq_gemv_ex(f, wo, v, H, nq, y=h, residual=src, x_group=c.heads // c.kv_heads,
+                              x_head_dim=c.head_dim, weights_ready=True, stream=stream)
+            with _timed(timers, "gemv_gateup", stream, on):
+                L.epq_gemv_ex(f, wgu, h, 2 * c.inter, H, y=self.m, rms_prenorm=True, rms_eps=c.rms_eps,
+                              swiglu=True, weights_ready=True, stream=stream)
+            with _timed(timers, "gemv_down", stream, on):
+                L.epq_gemv_ex(f, wd, self.m, H, c.inter, y=h, residual=h, weights_ready=True, stream=stream)
+        L.epq_gemv_ex(f, self.head, h, c.vocab, H, y=self.logits, rms_prenorm=True, rms_eps=c.rms_eps,
+                      weights_ready=True, stream=stream)
+        return self.logits
+
+
+class MoEDecoder:
+    """MoE decoder, batch 1.
+
+    Per layer: qkv = Wqkv rms(h); h = h + Wo v; h = h + MoE(rms(h)).
+    """
+
+    def __init__(self, cfg, fmt, layers, device):
+        self.cfg, self.fmt, self.layers = cfg, fmt, layers
+        H = cfg.hidden
+        self.qkv = torch.empty((1, 3 * H), dtype=torch.float32, device=device)
+        self.h = torch.empty((1, H), dtype=torch.float32, device=device)
+        ws = max(layer.workspace_bytes(1, cfg.topk) for (_, _, layer) in layers)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+
+    def token(self, x, out, stream=None, timers=None):
+        """x [1, H] (read only) -> out [1, H], the hidden state after the last layer."""
+        c, f, H = self.cfg, self.fmt, self.cfg.hidden
+        h = self.h
+        n = len(self.layers)
+        for li, (wqkv, wo, moe) in enumerate(self.layers):
+            src = x if li == 0 else h
+            on = li == 0
+            with _timed(timers, "gemv_qkv", stream, on):
+                L.epq_gemv_ex(f, wqkv, src, 3 * H, H, y=self.qkv, rms_prenorm=True, rms_eps=c.rms_eps,
+                              weights_ready=True, stream=stream)
+            with _timed(timers, "gemv_o", stream, on):
+                L.epq_gemv_ex(f, wo, self.qkv[:, 2 * H:], H, H, y=h, residual=src, weights_ready=True,
+                              stream=stream)
+            y = out if li == n - 1 else h
+            if timers is not None and on:
+                for name, st in (("moe_router", L.EPQ_MOE_ROUTE), ("moe_gateup", L.EPQ_MOE_GATE_UP),
+                                 ("moe_down", L.EPQ_MOE_DOWN)):
+                    with _timed(timers, name, stream, True):
+                        L.epq_moe_forward(moe, h, c.topk, y=y, workspace=self.ws, rms_prenorm=True,
+                                          rms_eps=c.rms_eps, stages=st, stream=stream)
+            else:
+                L.epq_moe_forward(moe, h, c.topk, y=y, workspace=self.ws, rms_prenorm=True, rms_eps=c.rms_eps,
+                                  stream=stream)
+        return out

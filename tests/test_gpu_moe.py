@@ -1,0 +1,205 @@
+"""GPU parity of the MoE layer (router + top-K + grouping, gate/up + SwiGLU,
+down + weighted combine + residual) against the float64 oracle.
+
+Acceptance (per token):
+* top-K indices identical to the oracle's; when the oracle's margin between
+  the K-th and (K+1)-th logit is below the router GEMV's error bound the
+  case is "tie-ambiguous" and the GPU's set must merely be valid (every
+  chosen logit within the bound of every unchosen one);
+* stage-wise, as in the EPM page's three-level verification: the SwiGLU
+  outputs h (returned through h_out) against the oracle's on the same
+  selection; then y against the oracle's down + combine fed with the GPU's
+  own h and weights;
+* end to end: |y - y_ref| <= 1e-3 (|x| + sum_k w_k A_k + g A_s).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from oracle.moe import MoEWeights
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+def _make(fmt, E, H, I, seed, shared=True, gate_vec=False, bias=False, norm=True):
+    R = synthetic.student_t((E, H), seed=seed).numpy()
+    gu = np.stack([oracle.quantize(fmt, synthetic.student_t((2 * I, H), seed=seed + 1 + e).numpy()) for e in range(E)])
+    dn = np.stack([oracle.quantize(fmt, synthetic.student_t((H, I), seed=seed + 1000 + e).numpy()) for e in range(E)])
+    mw = MoEWeights(fmt=fmt, hidden=H, inter=I, router=R, gate_up=gu, down=dn, norm_topk=norm)
+    if bias:
+        mw.router_bias = synthetic.normal((E,), seed=seed + 5).numpy()
+    if shared:
+        mw.shared_gate_up = oracle.quantize(fmt, synthetic.student_t((2 * I, H), seed=seed + 7).numpy())
+        mw.shared_down = oracle.quantize(fmt, synthetic.student_t((H, I), seed=seed + 8).numpy())
+        if gate_vec:
+            mw.shared_gate_vec = synthetic.normal((H,), seed=seed + 9, scale=0.05).numpy()
+    return mw
+
+
+def _to_gpu(epq, mw, dev):
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    return epq.MoELayer(mw.fmt, t(mw.router), t(mw.gate_up), t(mw.down), router_bias=t(mw.router_bias),
+                        shared_gate_up=t(mw.shared_gate_up), shared_down=t(mw.shared_down),
+                        shared_gate_vec=t(mw.shared_gate_vec), norm_topk=mw.norm_topk)
+
+
+def _run(epq, layer, x, topk, dev, rms_eps=None):
+    ntok, H = x.shape
+    xs = torch.from_numpy(x).to(dev)
+    idx = torch.empty((ntok, topk), dtype=torch.int32, device=dev)
+    w = torch.empty((ntok, topk), dtype=torch.float32, device=dev)
+    h = torch.empty((ntok, topk + 1, layer.I), dtype=torch.float32, device=dev)
+    logits = torch.empty((ntok, layer.E), dtype=torch.float32, device=dev)
+    y, _, _ = epq.epq_moe_forward(layer, xs, topk, topk_idx=idx, topk_w=w, rms_prenorm=rms_eps is not None,
+                                  rms_eps=rms_eps or 0.0, logits_out=logits, h_out=h)
+    torch.cuda.synchronize()
+    return (y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), h.cpu().numpy(), logits.cpu().numpy())
+
+
+def _check_topk(ref, idx_gpu, topk, router, xin):
+    """Identical top-K unless tie-ambiguous; ambiguous cases must be valid."""
+    Abound = np.abs(xin) @ np.abs(router.astype(np.float64)).T      # router GEMV error scale
+    for t in range(idx_gpu.shape[0]):
+        l = ref.logits[t]
+        order = np.argsort(-l, kind="stable")
+        margin = l[order[topk - 1]] - (l[order[topk]] if topk < l.size else -np.inf)
+        eps = 1e-4 * Abound[t].max()
+        if margin > eps:
+            assert idx_gpu[t].tolist() == ref.idx[t].tolist(), (t, idx_gpu[t], ref.idx[t])
+        else:
+            chosen = set(idx_gpu[t].tolist())
+            others = [e for e in range(l.size) if e not in chosen]
+            assert min(l[list(chosen)]) >= (max(l[others]) if others else -np.inf) - eps
+
+
+def _stagewise(mw, x, topk, idx, wts, h_gpu, y_gpu, xin, rms=False):
+    """h vs oracle on the GPU's selection; y vs down+combine fed with h_gpu."""
+    fmt, H, I = mw.fmt, mw.hidden, mw.inter
+    ntok = x.shape[0]
+    y_ref = x.astype(np.float64).copy()
+    y_bound = 1e-6 * np.abs(x.astype(np.float64))
+    for t in range(ntok):
+        slots = [(k, int(idx[t, k])) for k in range(topk)]
+        if mw.shared_gate_up is not None:
+            slots.append((topk, -1))
+        for k, e in slots:
+            GU = mw.gate_up[e] if e >= 0 else mw.shared_gate_up
+            D = mw.down[e] if e >= 0 else mw.shared_down
+            gu = oracle.gemv_f64(fmt, GU, xin[t], H)[0]
+            Agu = oracle.gemv_bound(fmt, GU, xin[t], H)[0]
+            g, u, Ag, Au = gu[:I], gu[I:], Agu[:I], Agu[I:]
+            silu = g / (1 + np.exp(-g))
+            h_ref = silu * u
+            hb = TOL * (1.1 * Ag * np.abs(u) + np.abs(silu) * Au) + 1e-6 * np.abs(h_ref) + 1e-30
+            err = np.abs(h_gpu[t, k] - h_ref)
+            assert (err <= hb).all(), f"h token {t} slot {k}: worst {(err / hb).max():.3g}"
+            o = oracle.gemv_f64(fmt, D, h_gpu[t, k], I)[0]
+            Ao = oracle.gemv_bound(fmt, D, h_gpu[t, k], I)[0]
+            if e >= 0:
+                wk = float(wts[t, k])
+            elif mw.shared_gate_vec is not None:
+                wk = 1 / (1 + np.exp(-(xin[t] @ mw.shared_gate_vec.astype(np.float64))))
+            else:
+                wk = 1.0
+            y_ref[t] += wk * o
+            y_bound[t] += abs(wk) * (TOL * Ao + 1e-6 * np.abs(o))
+    err = np.abs(y_gpu - y_ref)
+    assert (err <= y_bound + 1e-30).all(), f"combine: worst {(err / (y_bound + 1e-30)).max():.3g}"
+
+
+def _end_to_end(mw, x, ref, y_gpu):
+    fmt, H, I = mw.fmt, mw.hidden, mw.inter
+    bound = np.abs(x.astype(np.float64)).copy()
+    for t in range(x.shape[0]):
+        slots = [(ref.w[t, k], mw.gate_up[e], mw.down[e]) for k, e in enumerate(ref.idx[t])]
+        if mw.shared_gate_up is not None:
+            gs = ref.shared_gate[t] if ref.shared_gate is not None else 1.0
+            slots.append((gs, mw.shared_gate_up, mw.shared_down))
+        for wk, GU, D in slots:
+            _, g, u, h = oracle.expert_forward_f64(fmt, GU, D, H, I, ref.xin[t])
+            bound[t] += abs(wk) * oracle.gemv_bound(fmt, D, h[0], I)[0]
+    err = np.abs(y_gpu - ref.y)
+    assert (err <= 1e-3 * bound).all(), f"end to end: worst {(err / (1e-3 * bound)).max():.3g}"
+
+
+CASES = [
+    # fmt, E, H, I, topk, ntok, shared, gate_vec, bias, norm, rms
+    (oracle.Q4_K, 8, 512, 256, 2, 1, True, False, False, True, None),
+    (oracle.Q4_K, 8, 512, 256, 2, 3, True, True, True, True, 1e-6),
+    (oracle.Q8_0, 6, 256, 512, 3, 2, False, False, True, False, None),
+    (oracle.Q4_0, 16, 1024, 256, 4, 8, True, False, False, True, 1e-5),
+    (oracle.Q4_1, 5, 768, 256, 5, 4, True, True, False, True, None),
+    (oracle.Q4_K, 32, 2048, 512, 8, 1, True, False, True, True, 1e-6),
+    (oracle.Q4_K, 3, 256, 256, 1, 16, False, False, False, True, None),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_moe_parity(epq_lib, cuda_dev, case):
+    fmt, E, H, I, topk, ntok, shared, gvec, bias, norm, rms = case
+    mw = _make(fmt, E, H, I, seed=E * 100 + H + I + fmt, shared=shared, gate_vec=gvec, bias=bias, norm=norm)
+    x = synthetic.normal((ntok, H), seed=H + ntok, scale=2.0).numpy()
+    layer = _to_gpu(epq_lib, mw, cuda_dev)
+    y, idx, w, h, logits = _run(epq_lib, layer, x, topk, cuda_dev, rms_eps=rms)
+    ref = oracle.moe_forward_f64(mw, x, topk, rms_eps=rms)
+    # router logits within the GEMV bound
+    Al = np.abs(ref.xin) @ np.abs(mw.router.astype(np.float64)).T
+    assert (np.abs(logits - ref.logits) <= TOL * Al + 1e-6).all()
+    _check_topk(ref, idx, topk, mw.router, ref.xin)
+    same = (idx == ref.idx).all()
+    if same:
+        assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
+    _stagewise(mw, x, topk, idx, w, h, y, ref.xin)
+    if same:
+        _end_to_end(mw, x, ref, y)
+    assert epq_lib.epq_device_error() == 0
+
+
+def test_moe_all_tokens_one_expert_and_inplace(epq_lib, cuda_dev):
+    """A dominant router bias sends every token to expert 2 first; y may alias x."""
+    fmt, E, H, I, topk, ntok = oracle.Q4_K, 8, 512, 256, 2, 5
+    mw = _make(fmt, E, H, I, seed=77, shared=True)
+    mw.router_bias = np.zeros(E, np.float32)
+    mw.router_bias[2] = 1000.0
+    x = synthetic.normal((ntok, H), seed=78).numpy()
+    layer = _to_gpu(epq_lib, mw, cuda_dev)
+    xs = torch.from_numpy(x).to(cuda_dev)
+    idx = torch.empty((ntok, topk), dtype=torch.int32, device=cuda_dev)
+    epq_lib.epq_moe_forward(layer, xs, topk, y=xs, topk_idx=idx)       # in place
+    ref = oracle.moe_forward_f64(mw, x, topk)
+    assert (idx.cpu().numpy()[:, 0] == 2).all()
+    _end_to_end(mw, x, ref, xs.cpu().numpy())
+
+
+def test_moe_zero_experts_identity_and_determinism(epq_lib, cuda_dev):
+    fmt, E, H, I, topk, ntok = oracle.Q4_0, 4, 256, 256, 2, 3
+    mw = _make(fmt, E, H, I, seed=5, shared=False)
+    mw.gate_up = np.stack([oracle.quantize(fmt, np.zeros((2 * I, H), np.float32))] * E)
+    mw.down = np.stack([oracle.quantize(fmt, np.zeros((H, I), np.float32))] * E)
+    x = synthetic.normal((ntok, H), seed=6).numpy()
+    layer = _to_gpu(epq_lib, mw, cuda_dev)
+    y = _run(epq_lib, layer, x, topk, cuda_dev)[0]
+    assert np.array_equal(y, x)
+    mw2 = _make(oracle.Q4_K, 16, 512, 256, seed=9)
+    layer2 = _to_gpu(epq_lib, mw2, cuda_dev)
+    x2 = synthetic.normal((4, 512), seed=10).numpy()
+    r1 = _run(epq_lib, layer2, x2, 4, cuda_dev)
+    r2 = _run(epq_lib, layer2, x2, 4, cuda_dev)
+    for a, b in zip(r1, r2):
+        assert np.array_equal(a, b)
+
+
+def test_moe_argument_errors(epq_lib, cuda_dev):
+    mw = _make(oracle.Q4_K, 4, 256, 256, seed=3, shared=False)
+    layer = _to_gpu(epq_lib, mw, cuda_dev)
+    x = torch.zeros((1, 256), device=cuda_dev)
+    with pytest.raises(epq_lib.EpqError):
+        epq_lib.epq_moe_forward(layer, x, 5)                             # topk > n_experts
+    with pytest.raises(epq_lib.EpqError) as e:
+        epq_lib.epq_moe_forward(layer, x, 2, workspace=torch.empty(16, dtype=torch.uint8, device=cuda_dev))
+    assert e.value.status == 5
+    with pytest.raises(epq_lib.EpqError):
+        epq_lib.epq_moe_forward(layer, torch.zeros((17, 256), device=cuda_dev), 2)   # ntok > 16
