@@ -88,6 +88,15 @@ int64_t epq_block_weights(epq_fmt fmt);
 int64_t epq_block_bytes(epq_fmt fmt);
 int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
 
+/* Tuning hooks (host-only, process-wide; the defaults suit GB300).
+ *   EPQ_TUNE_TILE_BYTES  target packed bytes per pipeline stage of the GEMV
+ *                        engines (4096 .. 131072)
+ *   EPQ_TUNE_RING_BYTES  shared-memory ring budget per CTA (32768 .. 200704)
+ * Returns the previous value, or -1 for an unknown key or a value out of
+ * range (nothing changes then).  Affects launches issued afterwards. */
+enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2 };
+int epq_set_tuning(int key, int value);
+
 /* ---------------------------------------------------------------- packing
  * epq_quantize: [H] "GGUF 的量化格式" (the four quantizers).
  *   W       float32 [rows][cols], row-major, finite values.
@@ -220,9 +229,12 @@ size_t epq_moe_workspace_bytes(const epq_router *router, const epq_experts *expe
  *   x          float32 [ntok][H]            y  float32 [ntok][H] (may equal x)
  *   topk_idx   NULL or int32 [ntok][topk]   (selected experts, best first)
  *   topk_w     NULL or float32 [ntok][topk] (their combine weights)
- *   workspace  device scratch of epq_moe_workspace_bytes(); contents need no
- *              initialisation and are reused by the next call (calls that
- *              share a workspace must be ordered on one stream).
+ *   workspace  device scratch of epq_moe_workspace_bytes(), zero-filled
+ *              before its first use (e.g. one cudaMemsetAsync).  Each call
+ *              leaves its first 16 bytes (a ticket counter) at zero again, so
+ *              the same workspace serves any number of later calls; calls that
+ *              share a workspace must be ordered on one stream.  After a
+ *              device-side error (epq_device_error) zero it again.
  * Three kernels are queued: router + top-K + grouping, gate/up + SwiGLU,
  * down + combine + residual.  No host synchronisation. */
 epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts, const float *x, int ntok,

@@ -84,6 +84,7 @@ def load(path: str | None = None):
         "epq_block_weights": (i64, [i32]),
         "epq_block_bytes": (i64, [i32]),
         "epq_row_bytes": (i64, [i32, i64]),
+        "epq_set_tuning": (i32, [i32, i32]),
         "epq_quantize": (i32, [i32, vp, i64, i64, vp, vp]),
         "epq_dequantize": (i32, [i32, vp, i64, i64, vp, vp]),
         "epq_gemv": (i32, [i32, vp, vp, vp, i64, i64, i32, vp]),
@@ -126,6 +127,13 @@ def epq_block_weights(fmt: int) -> int:
 
 def epq_block_bytes(fmt: int) -> int:
     return int(load().epq_block_bytes(fmt))
+
+
+EPQ_TUNE_TILE_BYTES, EPQ_TUNE_RING_BYTES = 1, 2
+
+
+def epq_set_tuning(key: int, value: int) -> int:
+    return int(load().epq_set_tuning(key, value))
 
 
 def epq_status_string(st: int) -> str:
@@ -242,7 +250,7 @@ def epq_moe_forward(layer: MoELayer, x: torch.Tensor, topk: int, y: torch.Tensor
     if y is None:
         y = torch.empty_like(x)
     if workspace is None:
-        workspace = torch.empty(layer.workspace_bytes(ntok, topk), dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(layer.workspace_bytes(ntok, topk), dtype=torch.uint8, device=x.device)
     o = MoeOpts(int(rms_prenorm), float(rms_eps), _addr(logits_out), _addr(h_out), int(stages))
     _check("epq_moe_forward", lib.epq_moe_forward(
         ctypes.byref(layer._r), ctypes.byref(layer._x), _ptr(x), ntok, topk, ctypes.byref(o), _ptr(y),

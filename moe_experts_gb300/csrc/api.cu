@@ -1,5 +1,6 @@
 // Host-side plumbing of the C ABI: status strings, format sizes, the
 // per-device attribute cache and the device error word.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -62,6 +63,14 @@ unsigned *device_error_slot() {
   return g_err_slot[dev];
 }
 
+namespace {
+std::atomic<int> g_tile_bytes{32 * 1024};
+std::atomic<int> g_ring_bytes{170 * 1024};
+}  // namespace
+
+int tune_tile_bytes() { return g_tile_bytes.load(std::memory_order_relaxed); }
+int tune_ring_bytes() { return g_ring_bytes.load(std::memory_order_relaxed); }
+
 epq_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
   return EPQ_ERR_CUDA;
@@ -86,6 +95,18 @@ const char *epq_status_string(epq_status s) {
 }
 
 int epq_last_cuda_error(void) { return epq::g_last_cuda_error; }
+
+int epq_set_tuning(int key, int value) {
+  switch (key) {
+    case EPQ_TUNE_TILE_BYTES:
+      if (value < 4096 || value > 131072) return -1;
+      return epq::g_tile_bytes.exchange(value);
+    case EPQ_TUNE_RING_BYTES:
+      if (value < 32768 || value > 200704) return -1;
+      return epq::g_ring_bytes.exchange(value);
+  }
+  return -1;
+}
 
 int epq_device_error_detail(int *block, int *where, int *thread) {
   unsigned *slot = epq::device_error_slot();

@@ -12,7 +12,7 @@
 
 #include <utility>
 
-#include "../../include/epq.h"
+#include "epq.h"
 
 namespace epq {
 
@@ -197,6 +197,10 @@ bool current_device(DeviceInfo *out);
 // Device address of the error word of the current device (looked up once
 // per device with cudaGetSymbolAddress), or nullptr on failure.
 unsigned *device_error_slot();
+
+// Current tuning values (see epq_set_tuning).
+int tune_tile_bytes();
+int tune_ring_bytes();
 
 // Record a CUDA error for epq_last_cuda_error() and return EPQ_ERR_CUDA.
 epq_status cuda_fail(cudaError_t e);

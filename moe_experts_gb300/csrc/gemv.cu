@@ -24,9 +24,7 @@ namespace epq {
 namespace {
 
 constexpr int kMaxConsumers = 512;
-constexpr int kTileTarget = 80 * 1024;   // bytes of packed weights per stage
-constexpr int kSmemTarget = 170 * 1024;  // ring budget per CTA
-constexpr int kRedRing = 4;              // reduction buffers in flight
+constexpr int kRedRing = 8;              // reduction buffers in flight
 
 struct GemvParams {
   const uint8_t *W;
@@ -40,8 +38,10 @@ struct GemvParams {
   int nblk;            // cols / 32
   int tpr;             // threads per row group (>= nblk)
   int groups;          // row groups per CTA
-  int tile_rows;       // output rows per tile (= groups * RPG, or groups * RPG/2 with swiglu)
-  int red_rows;        // partial rows per tile (= groups * RPG)
+  int teams;           // independent consumer teams (each takes every teams-th tile)
+  int gpt;             // row groups per team (1 when tpr >= 32, else 32 / tpr)
+  int tile_rows;       // output rows per tile (= gpt * RPG, or gpt * RPG/2 with swiglu)
+  int red_rows;        // partial rows per tile (= gpt * RPG)
   int stages;
   uint32_t stage_bytes;
   int nv;              // vectors in this launch (<= NV template)
@@ -111,13 +111,14 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
   const int ntiles = static_cast<int>((re - rb + p.tile_rows - 1) / p.tile_rows);
   const int red_stride = NV * p.red_rows * wpg;   // floats per reduction buffer
 
+  const int team_warps = nwarps / p.teams;
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], nwarps);
+      mbar_init(&empty[s], team_warps);
     }
     for (int b = 0; b < kRedRing; ++b) {
-      mbar_init(&rfull[b], nwarps);
+      mbar_init(&rfull[b], team_warps);
       mbar_init(&rempty[b], 1);
     }
     fence_mbar_init();
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
 
   float xr[NV][32];
   float xsum[NV];
+  XCol<NV> xc;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     float amax = 0.0f, ssq = 0.0f;
@@ -191,7 +193,6 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
     for (int j = 0; j < 32; ++j) {
       amax = fmaxf(amax, fabsf(xr[v][j]));
       if (g == 0) ssq = fmaf(xr[v][j], xr[v][j], ssq);
-      xsum[v] += xr[v][j];
     }
     if (!is_fin) {
       amax = warp_max_all(amax);
@@ -216,9 +217,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
     // every product lands at scale 2^(-23 - E).
     const int E = bound_exponent(a);
     expo[v] = E;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) xr[v][j] = scale_pow2(xr[v][j], 126 - E - Fmt<FMT>::shift(j));
-    xsum[v] = scale_pow2(xsum[v], -23 - E);
+    xsum[v] = scale_column<FMT>(xr[v], E, xc.p[v]);
     float r = 1.0f;
     if (p.rms) r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.cols)), p.rms_eps)));
     outscale[v] = r;
@@ -258,7 +257,11 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
   // ------------------------------------------------------------------ consumers
   const int W = p.tpr < 32 ? p.tpr : 32;
   const int wg = c >> 5;
-  for (int t = 0; t < ntiles; ++t) {
+  const int team_size = nthreads / p.teams;
+  const int team = tid / team_size;
+  const int gt = g % p.gpt;  // group index within the team (row block of the tile)
+  // stages % teams == 0 (see make_plan): the stages this team waits on are its own
+  for (int t = team; t < ntiles; t += p.teams) {
     const int s = t % p.stages;
     if (!warp_wait(&full[s], (t / p.stages) & 1, p.err, DEVERR_FULL_WAIT, t)) return;
     const uint8_t *base = smem + static_cast<uint32_t>(s) * p.stage_bytes;
@@ -267,12 +270,12 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
     float part[NV][RPG];
 #pragma unroll
     for (int k = 0; k < RPG; ++k) {
-      const int lr = SWIGLU ? (g * RH + (k % RH)) : (g * RPG + k);
+      const int lr = SWIGLU ? (gt * RH + (k % RH)) : (gt * RPG + k);
       float pr[NV];
       if (active && lr < nr) {
         const uint8_t *row = base + static_cast<uint32_t>(lr) * p.row_bytes;
         if (SWIGLU && k >= RH) row += p.tile_rows * p.row_bytes;
-        column_dot<FMT, NV>(row, cc, xr, xsum, pr);
+        column_dot<FMT, NV>(row, cc, xc, xsum, pr);
       } else {
 #pragma unroll
         for (int v = 0; v < NV; ++v) pr[v] = 0.0f;
@@ -285,13 +288,14 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
 
     const int ri = reduce_scatter<RPG, NV>(part, W, lane % W);
     if (has_fin) {
-      // hand the warp's row partials to the finisher through the ring
+      // hand the warp's row partials to the finisher through the ring (one
+      // buffer per tile, in tile order)
       const int b = t % kRedRing;
       if (t >= kRedRing && !warp_wait(&rempty[b], ((t / kRedRing) - 1) & 1, p.err, DEVERR_RED_WAIT, t)) return;
       float *rbuf = red + b * red_stride;
       if ((lane % (32 / RPG)) == 0) {
 #pragma unroll
-        for (int v = 0; v < NV; ++v) rbuf[(v * p.red_rows + g * RPG + ri) * wpg + wg] = part[v][0];
+        for (int v = 0; v < NV; ++v) rbuf[(v * p.red_rows + gt * RPG + ri) * wpg + wg] = part[v][0];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rfull[b]);
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
       for (int v = 0; v < NV; ++v) up[v] = SWIGLU ? __shfl_xor_sync(0xffffffffu, part[v][0], W / 2) : 0.0f;
       const bool holder = ((lane % W) % (W / RPG)) == 0;
       if (holder && (!SWIGLU || ri < RH)) {
-        const int lr = SWIGLU ? g * RH + ri : g * RPG + ri;
+        const int lr = SWIGLU ? gt * RH + ri : gt * RPG + ri;
         if (lr < nr) {
           for (int v = 0; v < p.nv && v < NV; ++v) {
             float val = unscale(part[v][0], expo[v]) * outscale[v];
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
 
 // ------------------------------------------------------------------ host
 struct Plan {
-  int tpr, groups, rpg, tile_rows, stages;
+  int tpr, groups, gpt, teams, rpg, tile_rows, stages;
   uint32_t stage_bytes, smem;
   unsigned grid;
 };
@@ -334,28 +338,42 @@ bool make_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, int n
   pl->tpr = nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32;
   if (pl->tpr > kMaxConsumers) return false;
   pl->groups = std::max(1, kMaxConsumers / pl->tpr);
+  // a team is one row group, or one warp holding several narrow groups
+  pl->gpt = pl->tpr >= 32 ? 1 : 32 / pl->tpr;
+  pl->teams = pl->groups / pl->gpt;
   int64_t g = std::min<int64_t>(dev.sm_count, (rows_out + 7) / 8);
   pl->grid = static_cast<unsigned>(std::max<int64_t>(1, g));
   const int64_t rows_per_cta = (rows_out + pl->grid - 1) / pl->grid;
   const int rmax = std::min(8, std::min(pl->tpr, 32));
   const int64_t per_row = row_bytes * (swiglu ? 2 : 1);
-  auto tile_rows_of = [&](int r) { return static_cast<int64_t>(pl->groups) * (swiglu ? r / 2 : r); };
+  auto tile_rows_of = [&](int r) { return static_cast<int64_t>(pl->gpt) * (swiglu ? r / 2 : r); };
+  const int64_t tile_target = tune_tile_bytes(), ring_target = tune_ring_bytes();
   int rpg = swiglu ? 2 : 1;
-  // grow the tile while it fits the stage target and the CTA keeps >= 2 tiles
-  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= kTileTarget &&
-         tile_rows_of(rpg * 2) * 2 <= rows_per_cta)
+  // grow the tile while it fits the stage target and every team keeps >= 2 tiles
+  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= tile_target &&
+         tile_rows_of(rpg * 2) * 2 * pl->teams <= rows_per_cta)
     rpg *= 2;
   pl->rpg = rpg;
   pl->tile_rows = static_cast<int>(tile_rows_of(rpg));
   pl->stage_bytes = static_cast<uint32_t>(((pl->tile_rows * per_row) + 15) & ~int64_t(15));
-  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, kSmemTarget / pl->stage_bytes)));
-  const int red_rows = pl->groups * rpg;
+  // Every stage must belong to one team: with stages a multiple of teams,
+  // tile t and tile t + stages are consumed by the same team, so each team
+  // waits on its stages strictly in order and a parity wait can never see a
+  // phase that is two uses old.
+  const int red_rows = pl->gpt * rpg;
   const int nthreads = pl->groups * pl->tpr;
-  while (pl->stages > 2 && smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total >
-                               static_cast<uint32_t>(dev.max_smem_optin))
-    --pl->stages;
+  auto fits = [&](int st) {
+    return smem_layout(st, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total <=
+           static_cast<uint32_t>(dev.max_smem_optin);
+  };
+  int per_team = static_cast<int>(std::min<int64_t>(16, ring_target / pl->stage_bytes)) / pl->teams;
+  per_team = std::max(1, std::min(per_team, 16 / pl->teams));
+  while (per_team > 1 && !fits(per_team * pl->teams)) --per_team;
+  if (pl->teams == 1 && per_team < 2 && fits(2)) per_team = 2;
+  pl->stages = per_team * pl->teams;
+  if (!fits(pl->stages)) return false;
   pl->smem = smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total;
-  return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
+  return true;
 }
 
 template <int FMT, int NV, int RPG, bool SW>
@@ -429,7 +447,9 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   p.tpr = pl.tpr;
   p.groups = pl.groups;
   p.tile_rows = pl.tile_rows;
-  p.red_rows = pl.groups * pl.rpg;
+  p.red_rows = pl.gpt * pl.rpg;
+  p.teams = pl.teams;
+  p.gpt = pl.gpt;
   p.stages = pl.stages;
   p.stage_bytes = pl.stage_bytes;
   p.x_stride = opts.x_ld ? opts.x_ld : cols / xg;

@@ -58,33 +58,63 @@ struct Fmt<EPQ_Q8_0> {
 
 __device__ __forceinline__ float fbits(uint32_t u) { return __uint_as_float(u); }
 
+// A pair of floats held in one 64-bit register pair, the operand form of
+// fma.rn.f32x2.  Keeping activations and accumulators in this form avoids
+// re-pairing registers around every packed FMA.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f2_t f2_bits(uint32_t lo, uint32_t hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_sum(f2_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ void f2_fma(f2_t &acc, f2_t a, f2_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// Activations of one 32-weight column for NV vectors, as 16 pairs each.
+template <int NV>
+struct XCol {
+  f2_t p[NV][16];
+};
+
 // sum over one 32-bit word of 8 nibbles (weights 8i..8i+7) for NV vectors.
 template <int NV>
-__device__ __forceinline__ void nib_word(uint32_t w, const float (&xr)[NV][32], int i, float (&a)[NV][2]) {
-  const float f0 = fbits(w & 0x0000000Fu), f1 = fbits(w & 0x000000F0u);
-  const float f2 = fbits(w & 0x00000F00u), f3 = fbits(w & 0x0000F000u);
-  const float f4 = fbits(w & 0x000F0000u), f5 = fbits(w & 0x00F00000u);
+__device__ __forceinline__ void nib_word(uint32_t w, const XCol<NV> &x, int i, f2_t (&acc)[NV]) {
+  const f2_t p01 = f2_bits(w & 0x0000000Fu, w & 0x000000F0u);
+  const f2_t p23 = f2_bits(w & 0x00000F00u, w & 0x0000F000u);
+  const f2_t p45 = f2_bits(w & 0x000F0000u, w & 0x00F00000u);
   const uint32_t h = w >> 16;
-  const float f6 = fbits(h & 0x00000F00u), f7 = fbits(h & 0x0000F000u);
+  const f2_t p67 = f2_bits(h & 0x00000F00u, h & 0x0000F000u);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    ffma2(a[v][0], a[v][1], f0, f1, xr[v][8 * i + 0], xr[v][8 * i + 1]);
-    ffma2(a[v][0], a[v][1], f2, f3, xr[v][8 * i + 2], xr[v][8 * i + 3]);
-    ffma2(a[v][0], a[v][1], f4, f5, xr[v][8 * i + 4], xr[v][8 * i + 5]);
-    ffma2(a[v][0], a[v][1], f6, f7, xr[v][8 * i + 6], xr[v][8 * i + 7]);
+    f2_fma(acc[v], p01, x.p[v][4 * i + 0]);
+    f2_fma(acc[v], p23, x.p[v][4 * i + 1]);
+    f2_fma(acc[v], p45, x.p[v][4 * i + 2]);
+    f2_fma(acc[v], p67, x.p[v][4 * i + 3]);
   }
 }
 
 // sum over one 32-bit word of 4 int8 codes (weights 4i..4i+3), biased by 128.
 template <int NV>
-__device__ __forceinline__ void byte_word(uint32_t w, const float (&xr)[NV][32], int i, float (&a)[NV][2]) {
+__device__ __forceinline__ void byte_word(uint32_t w, const XCol<NV> &x, int i, f2_t (&acc)[NV]) {
   const uint32_t u = w ^ 0x80808080u;
-  const float f0 = fbits(u & 0x000000FFu), f1 = fbits(u & 0x0000FF00u);
-  const float f2 = fbits(u & 0x00FF0000u), f3 = fbits((u >> 16) & 0x0000FF00u);
+  const f2_t p01 = f2_bits(u & 0x000000FFu, u & 0x0000FF00u);
+  const f2_t p23 = f2_bits(u & 0x00FF0000u, (u >> 16) & 0x0000FF00u);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    ffma2(a[v][0], a[v][1], f0, f1, xr[v][4 * i + 0], xr[v][4 * i + 1]);
-    ffma2(a[v][0], a[v][1], f2, f3, xr[v][4 * i + 2], xr[v][4 * i + 3]);
+    f2_fma(acc[v], p01, x.p[v][2 * i + 0]);
+    f2_fma(acc[v], p23, x.p[v][2 * i + 1]);
   }
 }
 
@@ -123,45 +153,45 @@ struct ColConst {
 // `row` points at the row's packed bytes in shared memory; xs[v] is the
 // column's scaled activation sum sum(x) * 2^(A_v - 149).
 template <int FMT, int NV>
-__device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FMT> &cc, const float (&xr)[NV][32],
+__device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FMT> &cc, const XCol<NV> &x,
                                            const float (&xs)[NV], float (&part)[NV]) {
-  float a[NV][2];
+  f2_t acc[NV];
 #pragma unroll
-  for (int v = 0; v < NV; ++v) a[v][0] = a[v][1] = 0.0f;
+  for (int v = 0; v < NV; ++v) acc[v] = 0ull;
   if (FMT == EPQ_Q4_K) {
     const uint4 h = *reinterpret_cast<const uint4 *>(row + cc.off);
     const uint4 q = *reinterpret_cast<const uint4 *>(row + cc.qoff);
-    nib_word<NV>(q.x, xr, 0, a);
-    nib_word<NV>(q.y, xr, 1, a);
-    nib_word<NV>(q.z, xr, 2, a);
-    nib_word<NV>(q.w, xr, 3, a);
+    nib_word<NV>(q.x, x, 0, acc);
+    nib_word<NV>(q.y, x, 1, acc);
+    nib_word<NV>(q.z, x, 2, acc);
+    nib_word<NV>(q.w, x, 3, acc);
     const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
     const uint32_t c6 = __funnelshift_r(cc.csel ? h.z : h.y, cc.csel ? h.w : h.z, cc.csh) & 63u;
     const uint32_t k6 = __funnelshift_r(cc.ksel ? h.w : h.z, cc.ksel ? 0u : h.w, cc.ksh) & 63u;
     const float S = d * static_cast<float>(c6);
     const float M = dmin * static_cast<float>(k6);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) part[v] = fmaf(S, a[v][0] + a[v][1], -M * xs[v]);
+    for (int v = 0; v < NV; ++v) part[v] = fmaf(S, f2_sum(acc[v]), -M * xs[v]);
   } else if (FMT == EPQ_Q4_1) {
     const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
     const uint32_t dm = *reinterpret_cast<const uint32_t *>(row + cc.off);
-    nib_word<NV>(wq[0], xr, 0, a);
-    nib_word<NV>(wq[1], xr, 1, a);
-    nib_word<NV>(wq[2], xr, 2, a);
-    nib_word<NV>(wq[3], xr, 3, a);
+    nib_word<NV>(wq[0], x, 0, acc);
+    nib_word<NV>(wq[1], x, 1, acc);
+    nib_word<NV>(wq[2], x, 2, acc);
+    nib_word<NV>(wq[3], x, 3, acc);
     const float d = half_bits_to_float(dm), m = half_bits_to_float(dm >> 16);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) part[v] = fmaf(d, a[v][0] + a[v][1], m * xs[v]);
+    for (int v = 0; v < NV; ++v) part[v] = fmaf(d, f2_sum(acc[v]), m * xs[v]);
   } else if (FMT == EPQ_Q4_0) {
     const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
     const uint32_t w0 = wq[0], w1 = wq[1], w2 = wq[2], w3 = wq[3], w4 = wq[4];
     const float d = half_bits_to_float(*reinterpret_cast<const unsigned short *>(row + cc.off));
-    nib_word<NV>(__funnelshift_r(w0, w1, cc.qsh), xr, 0, a);
-    nib_word<NV>(__funnelshift_r(w1, w2, cc.qsh), xr, 1, a);
-    nib_word<NV>(__funnelshift_r(w2, w3, cc.qsh), xr, 2, a);
-    nib_word<NV>(__funnelshift_r(w3, w4, cc.qsh), xr, 3, a);
+    nib_word<NV>(__funnelshift_r(w0, w1, cc.qsh), x, 0, acc);
+    nib_word<NV>(__funnelshift_r(w1, w2, cc.qsh), x, 1, acc);
+    nib_word<NV>(__funnelshift_r(w2, w3, cc.qsh), x, 2, acc);
+    nib_word<NV>(__funnelshift_r(w3, w4, cc.qsh), x, 3, acc);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) part[v] = d * ((a[v][0] + a[v][1]) - 8.0f * xs[v]);
+    for (int v = 0; v < NV; ++v) part[v] = d * (f2_sum(acc[v]) - 8.0f * xs[v]);
   } else {  // Q8_0
     const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
     const float d = half_bits_to_float(*reinterpret_cast<const unsigned short *>(row + cc.off));
@@ -169,9 +199,9 @@ __device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FM
 #pragma unroll
     for (int i = 0; i < 9; ++i) w[i] = wq[i];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) byte_word<NV>(__funnelshift_r(w[i], w[i + 1], cc.qsh), xr, i, a);
+    for (int i = 0; i < 8; ++i) byte_word<NV>(__funnelshift_r(w[i], w[i + 1], cc.qsh), x, i, acc);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) part[v] = d * ((a[v][0] + a[v][1]) - 128.0f * xs[v]);
+    for (int v = 0; v < NV; ++v) part[v] = d * (f2_sum(acc[v]) - 128.0f * xs[v]);
   }
 }
 
@@ -241,14 +271,16 @@ __device__ __forceinline__ int bound_exponent(float amax) {
 }
 
 // Turn a loaded column into the scaled form column_dot() expects:
-// x_j * 2^(126 - E - shift_j), and return sum(x) * 2^(-23 - E).
+// x_j * 2^(126 - E - shift_j) packed in pairs, and return sum(x) * 2^(-23 - E).
 template <int FMT>
-__device__ __forceinline__ float scale_column(float (&xr)[32], int E) {
+__device__ __forceinline__ float scale_column(const float (&xr)[32], int E, f2_t (&out)[16]) {
   float s = 0.0f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) s += xr[j];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) xr[j] = scale_pow2(xr[j], 126 - E - Fmt<FMT>::shift(j));
+  for (int j = 0; j < 32; j += 2)
+    out[j / 2] = f2_pack(scale_pow2(xr[j], 126 - E - Fmt<FMT>::shift(j)),
+                         scale_pow2(xr[j + 1], 126 - E - Fmt<FMT>::shift(j + 1)));
   return scale_pow2(s, -23 - E);
 }
 

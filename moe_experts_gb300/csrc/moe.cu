@@ -34,8 +34,6 @@ constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kRouterThreads = 256;
 constexpr int kMaxConsumers = 512;
-constexpr int kTileTarget = 40 * 1024;
-constexpr int kSmemTarget = 160 * 1024;
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
@@ -314,9 +312,13 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
 }
 
 // ------------------------------------------------------------------ engine plan
+constexpr int kRedRing = 4;
+constexpr int kHSmemMax = 64 * 1024;  // stage all SwiGLU outputs in smem up to this size
+
 struct EnginePlan {
   int tpr, groups, rpg, tile_rows, stages;
-  uint32_t stage_bytes, smem, red_off, bar_off, acc_off;
+  uint32_t stage_bytes, smem, bar_off, red_off, meta_off, hs_off, acc_off;
+  int stage_h;  // down: all of h staged in shared memory
 };
 
 int next_pow2(int v) {
@@ -325,32 +327,50 @@ int next_pow2(int v) {
   return p;
 }
 
-// cols: weights per row; per_row: staged bytes per output row; extra: smem
-// after the ring (reduction buffers and accumulators).
-bool engine_plan(int cols, int64_t per_row, bool swiglu, int acc_floats_per_row, const DeviceInfo &dev,
-                 EnginePlan *pl) {
+// ints/floats of the routing metadata copy in shared memory
+inline int meta_words(int ntok, int topk) {
+  const int slots = ntok * topk + 1;
+  return 2 + 2 * slots + slots * ntok + ntok * topk + ntok + ntok * (topk + 1) + ntok;
+}
+
+// cols: weights per row; per_row: staged bytes per output row;
+// rows_hint: output rows a CTA is expected to own (keeps >= 2 tiles).
+bool engine_plan(int cols, int64_t per_row, bool swiglu, int64_t rows_hint, int ntok, int topk, int I_for_h,
+                 bool down, const DeviceInfo &dev, EnginePlan *pl) {
   const int nblk = cols / 32;
   pl->tpr = nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32;
   if (pl->tpr > kMaxConsumers) return false;
   pl->groups = std::max(1, kMaxConsumers / pl->tpr);
   const int rmax = std::min(8, std::min(pl->tpr, 32));
+  auto tile_rows_of = [&](int r) { return static_cast<int64_t>(pl->groups) * (swiglu ? r / 2 : r); };
   int rpg = swiglu ? 2 : 1;
-  while (rpg * 2 <= rmax && static_cast<int64_t>(pl->groups) * (swiglu ? rpg : rpg * 2) * per_row <= kTileTarget)
+  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= tune_tile_bytes() &&
+         tile_rows_of(rpg * 2) <= std::max<int64_t>(rows_hint, tile_rows_of(rpg)))
     rpg *= 2;
   pl->rpg = rpg;
-  pl->tile_rows = pl->groups * (swiglu ? rpg / 2 : rpg);
+  pl->tile_rows = static_cast<int>(tile_rows_of(rpg));
   pl->stage_bytes = static_cast<uint32_t>((pl->tile_rows * per_row + 15) & ~int64_t(15));
   const int wpg = pl->tpr > 32 ? pl->tpr / 32 : 1;
-  const uint32_t red_bytes = 4u * 2 * pl->groups * rpg * wpg;
-  const uint32_t acc_bytes = 4u * kMaxTok * pl->tile_rows * acc_floats_per_row;
-  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, kSmemTarget / pl->stage_bytes)));
+  const uint32_t red_bytes = 4u * kRedRing * pl->groups * rpg * wpg;
+  const uint32_t meta_bytes = 4u * meta_words(ntok, topk);
+  const int64_t hbytes = 4ll * ntok * (topk + 1) * I_for_h;
+  pl->stage_h = down && hbytes <= kHSmemMax;
+  const uint32_t hs_bytes = pl->stage_h ? static_cast<uint32_t>(hbytes) : 0u;
+  const uint32_t acc_bytes = down ? 4u * ntok * pl->tile_rows : 0u;
+  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, tune_ring_bytes() / pl->stage_bytes)));
   for (;;) {
     uint32_t o = pl->stages * pl->stage_bytes + 16;
     o = (o + 15) & ~15u;
     pl->bar_off = o;
-    o += 16u * pl->stages + 16;
+    o += 16u * pl->stages + 16u * kRedRing;
     pl->red_off = o;
     o += red_bytes;
+    o = (o + 15) & ~15u;
+    pl->meta_off = o;
+    o += meta_bytes;
+    o = (o + 15) & ~15u;
+    pl->hs_off = o;
+    o += hs_bytes;
     pl->acc_off = o;
     o += acc_bytes;
     pl->smem = (o + 15) & ~15u;
@@ -362,54 +382,103 @@ bool engine_plan(int cols, int64_t per_row, bool swiglu, int acc_floats_per_row,
 
 struct EngineArgs {
   MoeArgs a;
-  int tpr, groups, tile_rows, stages;
-  uint32_t stage_bytes, red_off, bar_off, acc_off;
+  int tpr, groups, tile_rows, stages, stage_h;
+  uint32_t stage_bytes, bar_off, red_off, meta_off, hs_off, acc_off;
 };
 
-// Cross-thread reduction of RPG partials of a tile (see gemv.cu).  Returns
-// the row (0..RPG-1 within the group) this thread finalizes, or -1; `res`
-// holds that row's sum.  `rbuf` is this tile's half of the shared buffer.
+// Shared-memory copy of the routing results (see router_kernel).
+struct Meta {
+  int *nact, *nslots, *active, *cnt, *list, *expo;
+  float *w, *gs, *rms;
+  __device__ Meta(uint8_t *base, int ntok, int topk) {
+    const int slots = ntok * topk + 1;
+    int *i = reinterpret_cast<int *>(base);
+    nact = i;
+    nslots = i + 1;
+    active = i + 2;
+    cnt = active + slots;
+    list = cnt + slots;
+    w = reinterpret_cast<float *>(list + slots * ntok);
+    gs = w + ntok * topk;
+    expo = reinterpret_cast<int *>(gs + ntok);
+    rms = reinterpret_cast<float *>(expo + ntok * (topk + 1));
+  }
+};
+
+// Fill the metadata copy (threads [0, nthr) of the CTA); `down` selects the
+// h exponents, otherwise the x exponents and RMS factors.
+__device__ void load_meta(const MoeArgs &a, Meta &m, int tid, int nthr, bool down) {
+  const int slots = a.ntok * a.topk + 1;
+  if (tid == 0) {
+    *m.nact = __ldcg(a.meta);
+    *m.nslots = __ldcg(a.meta + 1);
+  }
+  for (int i = tid; i < slots; i += nthr) {
+    m.active[i] = __ldcg(a.active + i);
+    m.cnt[i] = __ldcg(a.cnt + i);
+  }
+  for (int i = tid; i < slots * a.ntok; i += nthr) m.list[i] = __ldcg(a.list + i);
+  for (int i = tid; i < a.ntok * a.topk; i += nthr) m.w[i] = __ldcg(a.w + i);
+  for (int i = tid; i < a.ntok; i += nthr) {
+    m.gs[i] = a.gvec ? __ldcg(a.gshared + i) : 1.0f;
+    m.rms[i] = __ldcg(a.xstat + 2 * i + 1);
+  }
+  if (down) {
+    for (int i = tid; i < a.ntok * (a.topk + 1); i += nthr)
+      m.expo[i] = bound_exponent(__uint_as_float(__ldcg(a.hmax + i)));
+  } else {
+    for (int i = tid; i < a.ntok; i += nthr) m.expo[i] = bound_exponent(__ldcg(a.xstat + 2 * i));
+  }
+}
+
+// Row reduction of one (unit, entry) for RPG partials: in-warp reduce-scatter,
+// then either the row holder (groups within a warp) returns its row, or the
+// warp hands its partials to the finisher through ring buffer `b`.
 template <int RPG>
-__device__ __forceinline__ int reduce_rows(float (&part)[1][RPG], float &res, const EngineArgs &p, int g, int c,
-                                           int lane, float *rbuf, uint64_t *redbar, int phase, bool &ok) {
+__device__ __forceinline__ int reduce_or_hand_off(float (&part)[1][RPG], const EngineArgs &p, int g, int c,
+                                                  int lane, float *red, uint64_t *rfull, uint64_t *rempty, int use,
+                                                  bool &ok) {
   const int W = p.tpr < 32 ? p.tpr : 32;
   const int ri = reduce_scatter<RPG, 1>(part, W, lane % W);
-  res = 0.0f;
   if (p.tpr > 32) {
     const int wpg = p.tpr / 32;
-    const int wg = c >> 5;
-    if ((lane % (32 / RPG)) == 0) rbuf[(g * RPG + ri) * wpg + wg] = part[0][0];
-    __syncwarp();
-    // all consumer warps wait (double buffer: see the dense kernel)
-    if (lane == 0) mbar_arrive(redbar);
-    if (!warp_wait(redbar, phase, p.a.err, DEVERR_RED_WAIT)) {
+    const int b = use % kRedRing;
+    if (use >= kRedRing && !warp_wait(&rempty[b], ((use / kRedRing) - 1) & 1, p.a.err, DEVERR_RED_WAIT, use)) {
       ok = false;
       return -1;
     }
-    if (wg == 0 && c < RPG) {
-      float acc = 0.0f;
-      for (int w = 0; w < wpg; ++w) acc += rbuf[(g * RPG + c) * wpg + w];
-      res = acc;
-      return c;
-    }
+    float *rbuf = red + b * p.groups * RPG * wpg;
+    if ((lane % (32 / RPG)) == 0) rbuf[(g * RPG + ri) * wpg + (c >> 5)] = part[0][0];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rfull[b]);
     return -1;
   }
-  res = part[0][0];
   return (((lane % W) % (W / RPG)) == 0) ? ri : -1;
+}
+
+// Finisher side of the hand-off: wait for ring buffer of `use`, sum the
+// warp partials of slot row `r` (0..groups*RPG-1).
+__device__ __forceinline__ float fin_row(const float *rbuf, int r, int wpg) {
+  float acc = 0.0f;
+  for (int w = 0; w < wpg; ++w) acc += rbuf[r * wpg + w];
+  return acc;
 }
 
 // ------------------------------------------------------------------ 2. gate/up
 template <int FMT, int RPG>
-__global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const EngineArgs p) {
+__global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const EngineArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const MoeArgs &a = p.a;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
   uint64_t *empty = full + p.stages;
-  uint64_t *redbar = empty + p.stages;
+  uint64_t *rfull = empty + p.stages;
+  uint64_t *rempty = rfull + kRedRing;
   float *red = reinterpret_cast<float *>(smem + p.red_off);
   const int nthreads = p.groups * p.tpr;
   const int nwarps = nthreads / 32;
-  const int tid = threadIdx.x;
+  const bool has_fin = p.tpr > 32;
+  const int wpg = has_fin ? p.tpr / 32 : 1;
+  const int tid = threadIdx.x, lane = tid & 31;
   constexpr int RH = RPG / 2;
 
   if (tid == 0) {
@@ -417,8 +486,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const Eng
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nwarps);
     }
-    mbar_init(&redbar[0], nwarps);
-    mbar_init(&redbar[1], nwarps);
+    for (int b = 0; b < kRedRing; ++b) {
+      mbar_init(&rfull[b], nwarps);
+      mbar_init(&rempty[b], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -427,7 +498,6 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const Eng
 
   const int I = a.I;
   const int64_t total = static_cast<int64_t>(__ldcg(a.meta + 1)) * I;
-  const int nact = __ldcg(a.meta);
   const int64_t rb = (static_cast<int64_t>(blockIdx.x) * total) / gridDim.x;
   const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * total) / gridDim.x;
   auto tile_len = [&](int64_t r0) {
@@ -435,14 +505,15 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const Eng
     return static_cast<int>(min(static_cast<int64_t>(p.tile_rows), lim - r0));
   };
 
-  if (tid >= nthreads) {
+  if (tid >= nthreads && tid < nthreads + 32) {
+    // producer
     if (tid != nthreads) return;
-    int t = 0;
-    int issued = 0;
+    const int nact = __ldcg(a.meta);
+    int t = 0, issued = 0;
     bool ok = true;
     for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
       const int s = t % p.stages;
-      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT)) {
+      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, t)) {
         ok = false;
         break;
       }
@@ -461,39 +532,75 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const Eng
     }
     if (!ok)
       for (int u = max(0, issued - p.stages); u < issued; ++u)
-        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT);
+        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT, u);
     return;
   }
 
-  const int g = tid / p.tpr, c = tid % p.tpr, lane = tid & 31;
+  // consumers and finisher: routing metadata into shared memory
+  Meta m(smem + p.meta_off, a.ntok, a.topk);
+  const bool is_fin = tid >= nthreads + 32;
+  const int ctid = is_fin ? nthreads + lane : tid;
+  load_meta(a, m, ctid, nthreads + (has_fin ? 32 : 0), false);
+  named_sync(1, nthreads + (has_fin ? 32 : 0));
+
+  if (is_fin) {
+    int use = 0, t = 0;
+    for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
+      const int nr = tile_len(r0);
+      const int slot = static_cast<int>(r0 / I);
+      const int i0 = static_cast<int>(r0 % I);
+      const int ne = m.cnt[slot];
+      for (int j = 0; j < ne; ++j, ++use) {
+        const int b = use % kRedRing;
+        if (!warp_wait(&rfull[b], (use / kRedRing) & 1, a.err, DEVERR_RED_WAIT, use)) return;
+        const float *rbuf = red + b * p.groups * RPG * wpg;
+        const int ent = m.list[slot * a.ntok + j];
+        const int tok = ent >> 5, k = ent & 31;
+        const int E = m.expo[tok];
+        const float r = m.rms[tok];
+        const int hs = tok * (a.topk + 1) + k;
+        for (int o = lane; o < nr; o += 32) {
+          const int gg = o / RH, kk = o % RH;
+          const float gv = unscale(fin_row(rbuf, gg * RPG + kk, wpg), E) * r;
+          const float uv = unscale(fin_row(rbuf, gg * RPG + RH + kk, wpg), E) * r;
+          const float hv = silu(gv) * uv;
+          a.h[static_cast<int64_t>(hs) * I + i0 + o] = hv;
+          atomicMax(a.hmax + hs, __float_as_uint(fabsf(hv)));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[b]);
+      }
+    }
+    return;
+  }
+
+  const int g = tid / p.tpr, c = tid % p.tpr;
   const int nblk = a.H / 32;
   const bool active = c < nblk;
   ColConst<FMT> cc;
   cc.init(active ? c : 0);
-  float xr[1][32];
+  float xr[32];
+  XCol<1> xc;
   float xs[1] = {0.0f};
-  int cur_t = -1, cur_E = 0;
-  float cur_rms = 1.0f;
-  int t = 0, rphase = 0;
+  int cur_t = -1;
+  int use = 0, t = 0;
   for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
     const int s = t % p.stages;
-    if (!warp_wait(&full[s], (t / p.stages) & 1, a.err, DEVERR_FULL_WAIT)) return;
+    if (!warp_wait(&full[s], (t / p.stages) & 1, a.err, DEVERR_FULL_WAIT, t)) return;
     const int nr = tile_len(r0);
     const int slot = static_cast<int>(r0 / I);
     const int i0 = static_cast<int>(r0 % I);
     const uint8_t *stage = smem + static_cast<uint32_t>(s) * p.stage_bytes;
-    const int ne = __ldcg(a.cnt + slot);
+    const int ne = m.cnt[slot];
     bool ok = true;
-    for (int j = 0; j < ne; ++j) {
-      const int ent = __ldcg(a.list + slot * a.ntok + j);
+    for (int j = 0; j < ne; ++j, ++use) {
+      const int ent = m.list[slot * a.ntok + j];
       const int tok = ent >> 5, k = ent & 31;
       if (tok != cur_t) {
         cur_t = tok;
-        cur_E = bound_exponent(__ldcg(a.xstat + 2 * tok));
-        cur_rms = __ldcg(a.xstat + 2 * tok + 1);
         if (active) {
-          load_column(a.x + static_cast<int64_t>(tok) * a.H + 32 * c, xr[0]);
-          xs[0] = scale_column<FMT>(xr[0], cur_E);
+          load_column(a.x + static_cast<int64_t>(tok) * a.H + 32 * c, xr);
+          xs[0] = scale_column<FMT>(xr, m.expo[tok], xc.p[0]);
         }
       }
       float part[1][RPG];
@@ -504,80 +611,84 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_kernel(const Eng
         if (active && lr < nr) {
           const uint8_t *row = stage + static_cast<uint32_t>(lr) * a.gu_row_bytes;
           if (q >= RH) row += p.tile_rows * a.gu_row_bytes;
-          column_dot<FMT, 1>(row, cc, xr, xs, pr);
+          column_dot<FMT, 1>(row, cc, xc, xs, pr);
         }
         part[0][q] = pr[0];
       }
-      float res;
-      float *rbuf = red + (rphase & 1) * p.groups * RPG * (p.tpr > 32 ? p.tpr / 32 : 1);
-      const int row_k = reduce_rows<RPG>(part, res, p, g, c, lane, rbuf, &redbar[rphase & 1], (rphase >> 1) & 1, ok);
-      ++rphase;
-      float up;
-      if (p.tpr > 32)
-        up = __shfl_down_sync(0xffffffffu, res, RH);
-      else
-        up = __shfl_xor_sync(0xffffffffu, res, (p.tpr < 32 ? p.tpr : 32) / 2);
+      if (j == ne - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage is no longer read
+      }
+      const int row_k = reduce_or_hand_off<RPG>(part, p, g, c, lane, red, rfull, rempty, use, ok);
       if (__any_sync(0xffffffffu, !ok)) return;
-      if (row_k >= 0 && row_k < RH) {
-        const int lr = g * RH + row_k;
-        if (lr < nr) {
-          const float gv = unscale(res, cur_E) * cur_rms;
-          const float uv = unscale(up, cur_E) * cur_rms;
-          const float hv = silu(gv) * uv;
-          const int hs = tok * (a.topk + 1) + k;
-          a.h[static_cast<int64_t>(hs) * I + i0 + lr] = hv;
-          atomicMax(a.hmax + hs, __float_as_uint(fabsf(hv)));
+      if (!has_fin) {
+        const int W = p.tpr < 32 ? p.tpr : 32;
+        const float up = __shfl_xor_sync(0xffffffffu, part[0][0], W / 2);
+        if (row_k >= 0 && row_k < RH) {
+          const int lr = g * RH + row_k;
+          if (lr < nr) {
+            const int E = m.expo[tok];
+            const float r = m.rms[tok];
+            const float hv = silu(unscale(part[0][0], E) * r) * (unscale(up, E) * r);
+            const int hs = tok * (a.topk + 1) + k;
+            a.h[static_cast<int64_t>(hs) * I + i0 + lr] = hv;
+            atomicMax(a.hmax + hs, __float_as_uint(fabsf(hv)));
+          }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 
 // ------------------------------------------------------------------ 3. down + combine
 template <int FMT, int RPG>
-__global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_kernel(const EngineArgs p) {
+__global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const EngineArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const MoeArgs &a = p.a;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
   uint64_t *empty = full + p.stages;
-  uint64_t *redbar = empty + p.stages;
+  uint64_t *rfull = empty + p.stages;
+  uint64_t *rempty = rfull + kRedRing;
   float *red = reinterpret_cast<float *>(smem + p.red_off);
-  float *acc = reinterpret_cast<float *>(smem + p.acc_off);  // [kMaxTok][tile_rows]
+  float *hs_smem = reinterpret_cast<float *>(smem + p.hs_off);
+  float *acc = reinterpret_cast<float *>(smem + p.acc_off);  // [ntok][tile_rows]
   const int nthreads = p.groups * p.tpr;
   const int nwarps = nthreads / 32;
-  const int tid = threadIdx.x;
+  const bool has_fin = p.tpr > 32;
+  const int wpg = has_fin ? p.tpr / 32 : 1;
+  const int tid = threadIdx.x, lane = tid & 31;
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nwarps);
     }
-    mbar_init(&redbar[0], nwarps);
-    mbar_init(&redbar[1], nwarps);
+    for (int b = 0; b < kRedRing; ++b) {
+      mbar_init(&rfull[b], nwarps);
+      mbar_init(&rempty[b], 1);
+    }
     fence_mbar_init();
   }
-  for (int i = tid; i < kMaxTok * p.tile_rows; i += blockDim.x) acc[i] = 0.0f;
+  for (int i = tid; i < a.ntok * p.tile_rows; i += blockDim.x) acc[i] = 0.0f;
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();  // h, routing and hmax come from the previous kernels
 
   const int H = a.H, I = a.I;
-  const int nslots = __ldcg(a.meta + 1);
-  const int nact = __ldcg(a.meta);
   const int64_t rb = (static_cast<int64_t>(blockIdx.x) * H) / gridDim.x;
   const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * H) / gridDim.x;
   const int ntiles = static_cast<int>((re - rb + p.tile_rows - 1) / p.tile_rows);
-  const int nunits = ntiles * nslots;
 
-  if (tid >= nthreads) {
+  if (tid >= nthreads && tid < nthreads + 32) {
     if (tid != nthreads) return;
+    const int nslots = __ldcg(a.meta + 1);
+    const int nact = __ldcg(a.meta);
+    const int nunits = ntiles * nslots;
     int issued = 0;
     bool ok = true;
     for (int u = 0; u < nunits; ++u) {
       const int s = u % p.stages;
-      if (u >= p.stages && !mbar_wait(&empty[s], ((u / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT)) {
+      if (u >= p.stages && !mbar_wait(&empty[s], ((u / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, u)) {
         ok = false;
         break;
       }
@@ -593,59 +704,109 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_kernel(const Engin
     }
     if (!ok)
       for (int u = max(0, issued - p.stages); u < issued; ++u)
-        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT);
+        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT, u);
     return;
   }
 
-  const int g = tid / p.tpr, c = tid % p.tpr, lane = tid & 31;
+  // consumers and finisher: routing metadata (and all of h) into shared memory
+  Meta m(smem + p.meta_off, a.ntok, a.topk);
+  const bool is_fin = tid >= nthreads + 32;
+  const int ctid = is_fin ? nthreads + lane : tid;
+  const int nthr = nthreads + (has_fin ? 32 : 0);
+  load_meta(a, m, ctid, nthr, true);
+  if (p.stage_h) {
+    const int n4 = a.ntok * (a.topk + 1) * I / 4;
+    const float4 *src = reinterpret_cast<const float4 *>(a.h);
+    float4 *dst = reinterpret_cast<float4 *>(hs_smem);
+    for (int i = ctid; i < n4; i += nthr) dst[i] = __ldcg(src + i);
+  }
+  named_sync(1, nthr);
+  const int nslots = *m.nslots;
+  const int nunits = ntiles * nslots;
+
+  if (is_fin) {
+    int use = 0;
+    for (int u = 0; u < nunits; ++u) {
+      const int tile = u / nslots, slot = u % nslots;
+      const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
+      const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
+      const int ne = m.cnt[slot];
+      for (int j = 0; j < ne; ++j, ++use) {
+        const int b = use % kRedRing;
+        if (!warp_wait(&rfull[b], (use / kRedRing) & 1, a.err, DEVERR_RED_WAIT, use)) return;
+        const float *rbuf = red + b * p.groups * RPG * wpg;
+        const int ent = m.list[slot * a.ntok + j];
+        const int tok = ent >> 5, k = ent & 31;
+        const int E = m.expo[tok * (a.topk + 1) + k];
+        const float wk = k < a.topk ? m.w[tok * a.topk + k] : m.gs[tok];
+        for (int o = lane; o < nr; o += 32) acc[tok * p.tile_rows + o] += wk * unscale(fin_row(rbuf, o, wpg), E);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[b]);
+      }
+      if (slot == nslots - 1) {
+        for (int o = lane; o < nr; o += 32) {
+          for (int tk = 0; tk < a.ntok; ++tk) {
+            const int64_t oi = static_cast<int64_t>(tk) * H + r0 + o;
+            a.y[oi] = a.x[oi] + acc[tk * p.tile_rows + o];
+            acc[tk * p.tile_rows + o] = 0.0f;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  const int g = tid / p.tpr, c = tid % p.tpr;
   const int nblk = I / 32;
   const bool active = c < nblk;
   ColConst<FMT> cc;
   cc.init(active ? c : 0);
-  float xr[1][32];
+  float xr[32];
+  XCol<1> xc;
   float xs[1] = {0.0f};
-  int rphase = 0;
-  int my_row = -1;  // tile row this thread finalizes (same for every unit)
+  int use = 0;
+  int my_row = -1;  // tile row this thread finalizes (holder path; same for every unit)
   for (int u = 0; u < nunits; ++u) {
     const int s = u % p.stages;
-    if (!warp_wait(&full[s], (u / p.stages) & 1, a.err, DEVERR_FULL_WAIT)) return;
+    if (!warp_wait(&full[s], (u / p.stages) & 1, a.err, DEVERR_FULL_WAIT, u)) return;
     const int tile = u / nslots, slot = u % nslots;
     const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
     const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
     const uint8_t *stage = smem + static_cast<uint32_t>(s) * p.stage_bytes;
-    const int ne = __ldcg(a.cnt + slot);
+    const int ne = m.cnt[slot];
     bool ok = true;
-    for (int j = 0; j < ne; ++j) {
-      const int ent = __ldcg(a.list + slot * a.ntok + j);
+    for (int j = 0; j < ne; ++j, ++use) {
+      const int ent = m.list[slot * a.ntok + j];
       const int tok = ent >> 5, k = ent & 31;
-      const int hs = tok * (a.topk + 1) + k;
-      const int E = bound_exponent(__uint_as_float(__ldcg(a.hmax + hs)));
+      const int hsi = tok * (a.topk + 1) + k;
+      const int E = m.expo[hsi];
       if (active) {
-        load_column(a.h + static_cast<int64_t>(hs) * I + 32 * c, xr[0]);
-        xs[0] = scale_column<FMT>(xr[0], E);
+        const float *src = p.stage_h ? hs_smem + static_cast<int64_t>(hsi) * I + 32 * c
+                                     : a.h + static_cast<int64_t>(hsi) * I + 32 * c;
+        load_column(src, xr);
+        xs[0] = scale_column<FMT>(xr, E, xc.p[0]);
       }
       float part[1][RPG];
 #pragma unroll
       for (int q = 0; q < RPG; ++q) {
         const int lr = g * RPG + q;
         float pr[1] = {0.0f};
-        if (active && lr < nr) column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes, cc, xr, xs, pr);
+        if (active && lr < nr) column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes, cc, xc, xs, pr);
         part[0][q] = pr[0];
       }
-      float res;
-      float *rbuf = red + (rphase & 1) * p.groups * RPG * (p.tpr > 32 ? p.tpr / 32 : 1);
-      const int row_k = reduce_rows<RPG>(part, res, p, g, c, lane, rbuf, &redbar[rphase & 1], (rphase >> 1) & 1, ok);
-      ++rphase;
+      if (j == ne - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      const int row_k = reduce_or_hand_off<RPG>(part, p, g, c, lane, red, rfull, rempty, use, ok);
       if (__any_sync(0xffffffffu, !ok)) return;
-      if (row_k >= 0) {
+      if (!has_fin && row_k >= 0) {
         my_row = g * RPG + row_k;
-        const float wk = k < a.topk ? __ldcg(a.w + tok * a.topk + k) : (a.gvec ? __ldcg(a.gshared + tok) : 1.0f);
-        acc[tok * p.tile_rows + my_row] += wk * unscale(res, E);
+        const float wk = k < a.topk ? m.w[tok * a.topk + k] : m.gs[tok];
+        acc[tok * p.tile_rows + my_row] += wk * unscale(part[0][0], E);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (slot == nslots - 1 && my_row >= 0 && my_row < nr) {
+    if (!has_fin && slot == nslots - 1 && my_row >= 0 && my_row < nr) {
       // all slots of this tile are in: y = x + weighted expert sum
       for (int tk = 0; tk < a.ntok; ++tk) {
         const int64_t o = static_cast<int64_t>(tk) * H + r0 + my_row;
@@ -660,8 +821,8 @@ template <typename K>
 cudaError_t launch_engine(K kernel, const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, p.groups * p.tpr + 32, smem, s>>>(p);
-  return cudaGetLastError();
+  const dim3 block(p.groups * p.tpr + 32 + (p.tpr > 32 ? 32 : 0));
+  return launch_pdl(kernel, dim3(grid), block, smem, s, p);
 }
 
 template <int FMT>
@@ -780,10 +941,8 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const int stages = (o.stages & 7) ? (o.stages & 7) : 7;
   cudaError_t e = cudaSuccess;
   if (stages & EPQ_MOE_ROUTE) {
-    // The ticket counter must start at zero: the router's last CTA resets it
-    // after each call; a fresh workspace is cleared here once per call (tiny).
-    e = cudaMemsetAsync(a.counter, 0, 16, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    // The ticket counter starts at zero in a fresh (zero-filled) workspace and
+    // the router's last CTA puts it back to zero for the next call.
     const int nrows = E + (a.gvec ? 1 : 0);
     const unsigned rgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (nrows + 7) / 8)));
     router_kernel<<<rgrid, kRouterThreads, 0, s>>>(a);
@@ -791,11 +950,16 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   }
 
   EnginePlan gp, dp;
-  if (!engine_plan(H, 2 * a.gu_row_bytes, true, 0, dev, &gp)) return EPQ_ERR_SHAPE;
-  if (!engine_plan(I, a.dn_row_bytes, false, 1, dev, &dp)) return EPQ_ERR_SHAPE;
-
-  EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_bytes, gp.red_off, gp.bar_off, gp.acc_off};
+  const int max_slots = std::min(E, ntok * topk) + (a.has_shared ? 1 : 0);
   const unsigned ggrid = static_cast<unsigned>(dev.sm_count);
+  const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
+  const int64_t g_hint = (static_cast<int64_t>(max_slots) * I + ggrid - 1) / ggrid / 2;
+  const int64_t d_hint = (H + dgrid - 1) / dgrid;
+  if (!engine_plan(H, 2 * a.gu_row_bytes, true, g_hint, ntok, topk, I, false, dev, &gp)) return EPQ_ERR_SHAPE;
+  if (!engine_plan(I, a.dn_row_bytes, false, d_hint, ntok, topk, I, true, dev, &dp)) return EPQ_ERR_SHAPE;
+
+  EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_h, gp.stage_bytes, gp.bar_off,
+                gp.red_off, gp.meta_off, gp.hs_off, gp.acc_off};
   if (stages & EPQ_MOE_GATE_UP) switch (experts->fmt) {
     case EPQ_Q8_0: e = launch_gateup<EPQ_Q8_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
     case EPQ_Q4_0: e = launch_gateup<EPQ_Q4_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
@@ -804,8 +968,8 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   }
   if (e != cudaSuccess) return cuda_fail(e);
 
-  EngineArgs da{a, dp.tpr, dp.groups, dp.tile_rows, dp.stages, dp.stage_bytes, dp.red_off, dp.bar_off, dp.acc_off};
-  const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
+  EngineArgs da{a, dp.tpr, dp.groups, dp.tile_rows, dp.stages, dp.stage_h, dp.stage_bytes, dp.bar_off,
+                dp.red_off, dp.meta_off, dp.hs_off, dp.acc_off};
   if (stages & EPQ_MOE_DOWN) switch (experts->fmt) {
     case EPQ_Q8_0: e = launch_down<EPQ_Q8_0>(da, dp.rpg, dgrid, dp.smem, s); break;
     case EPQ_Q4_0: e = launch_down<EPQ_Q4_0>(da, dp.rpg, dgrid, dp.smem, s); break;
