@@ -65,7 +65,7 @@ unsigned *device_error_slot() {
 
 namespace {
 std::atomic<int> g_tile_bytes{32 * 1024};
-std::atomic<int> g_ring_bytes{170 * 1024};
+std::atomic<int> g_ring_bytes{180 * 1024};
 }  // namespace
 
 int tune_tile_bytes() { return g_tile_bytes.load(std::memory_order_relaxed); }

@@ -338,30 +338,48 @@ bool make_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, int n
   pl->tpr = nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32;
   if (pl->tpr > kMaxConsumers) return false;
   pl->groups = std::max(1, kMaxConsumers / pl->tpr);
-  // a team is one row group, or one warp holding several narrow groups
-  pl->gpt = pl->tpr >= 32 ? 1 : 32 / pl->tpr;
-  pl->teams = pl->groups / pl->gpt;
   int64_t g = std::min<int64_t>(dev.sm_count, (rows_out + 7) / 8);
   pl->grid = static_cast<unsigned>(std::max<int64_t>(1, g));
   const int64_t rows_per_cta = (rows_out + pl->grid - 1) / pl->grid;
   const int rmax = std::min(8, std::min(pl->tpr, 32));
   const int64_t per_row = row_bytes * (swiglu ? 2 : 1);
-  auto tile_rows_of = [&](int r) { return static_cast<int64_t>(pl->gpt) * (swiglu ? r / 2 : r); };
   const int64_t tile_target = tune_tile_bytes(), ring_target = tune_ring_bytes();
-  int rpg = swiglu ? 2 : 1;
-  // grow the tile while it fits the stage target and every team keeps >= 2 tiles
-  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= tile_target &&
-         tile_rows_of(rpg * 2) * 2 * pl->teams <= rows_per_cta)
-    rpg *= 2;
-  pl->rpg = rpg;
-  pl->tile_rows = static_cast<int>(tile_rows_of(rpg));
+  const int min_gpt = pl->tpr >= 32 ? 1 : 32 / pl->tpr;  // a team is whole warps
+  const int nthreads = pl->groups * pl->tpr;
+  // Pick (groups per team, rows per group): the bulk copy of one tile must be
+  // large (the TMA engine has a per-copy cost: below ~32 KB it cannot keep
+  // HBM busy), every team should get >= 2 tiles, and more teams are better
+  // (they overlap each other's latency).  Score = copy size capped at the
+  // target, then teams.
+  int best_gpt = pl->groups, best_rpg = swiglu ? 2 : 1;
+  int64_t best_score = -1;
+  for (int gpt = min_gpt; gpt <= pl->groups; gpt *= 2) {
+    if (pl->groups % gpt) continue;
+    const int teams = pl->groups / gpt;
+    for (int rpg = swiglu ? 2 : 1; rpg <= rmax; rpg *= 2) {
+      const int64_t tile_rows = static_cast<int64_t>(gpt) * (swiglu ? rpg / 2 : rpg);
+      const int64_t bytes = tile_rows * per_row;
+      if (bytes > 2 * tile_target && rpg > (swiglu ? 2 : 1)) continue;
+      const bool two_each = tile_rows * 2 * teams <= rows_per_cta;
+      const int64_t eff = std::min(bytes, tile_target);
+      const int64_t score = (two_each ? (int64_t(1) << 40) : 0) + eff * 64 + teams;
+      if (score > best_score) {
+        best_score = score;
+        best_gpt = gpt;
+        best_rpg = rpg;
+      }
+    }
+  }
+  pl->gpt = best_gpt;
+  pl->teams = pl->groups / best_gpt;
+  pl->rpg = best_rpg;
+  pl->tile_rows = static_cast<int>(static_cast<int64_t>(best_gpt) * (swiglu ? best_rpg / 2 : best_rpg));
   pl->stage_bytes = static_cast<uint32_t>(((pl->tile_rows * per_row) + 15) & ~int64_t(15));
   // Every stage must belong to one team: with stages a multiple of teams,
   // tile t and tile t + stages are consumed by the same team, so each team
   // waits on its stages strictly in order and a parity wait can never see a
   // phase that is two uses old.
-  const int red_rows = pl->gpt * rpg;
-  const int nthreads = pl->groups * pl->tpr;
+  const int red_rows = pl->gpt * pl->rpg;
   auto fits = [&](int st) {
     return smem_layout(st, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total <=
            static_cast<uint32_t>(dev.max_smem_optin);
