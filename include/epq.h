@@ -241,6 +241,30 @@ epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts,
                            int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w,
                            void *workspace, size_t workspace_bytes, epq_stream_t stream);
 
+/* epq_moe_forward_noalloc: the same MoE layer, for callers that cannot
+ * allocate device memory -- for instance a runtime that plans all of its
+ * device memory up front and hands out no scratch, or code that must not
+ * call the CUDA allocator from its decode loop.  (The source pages have no
+ * counterpart; this is an interface convenience.)
+ *
+ * Instead of a caller workspace it uses one fixed 1 MiB array compiled into
+ * the library (a file-scope __device__ array; every GPU that loads the
+ * library holds it until the process exits).  Inputs and outputs are still
+ * passed by the caller, exactly as for epq_moe_forward.
+ *   - Shapes whose workspace (epq_moe_workspace_bytes) exceeds 1 MiB are
+ *     rejected with EPQ_ERR_WORKSPACE before anything is queued.
+ *   - No cudaMalloc / cudaFree or other allocating call is made.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the previous call's
+ *     contents; each call clears the part that must start at zero.  Calls
+ *     that may overlap on the GPU (different streams without ordering) race
+ *     on the array and must not be issued. */
+epq_status epq_moe_forward_noalloc(const epq_router *router, const epq_experts *experts, const float *x,
+                                   int ntok, int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx,
+                                   float *topk_w, epq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -92,6 +92,8 @@ def load(path: str | None = None):
         "epq_moe_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Router), ctypes.POINTER(Experts), i32, i32]),
         "epq_moe_forward": (i32, [ctypes.POINTER(Router), ctypes.POINTER(Experts), vp, i32, i32,
                                   ctypes.POINTER(MoeOpts), vp, vp, vp, vp, ctypes.c_size_t, vp]),
+        "epq_moe_forward_noalloc": (i32, [ctypes.POINTER(Router), ctypes.POINTER(Experts), vp, i32, i32,
+                                          ctypes.POINTER(MoeOpts), vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -256,3 +258,19 @@ def epq_moe_forward(layer: MoELayer, x: torch.Tensor, topk: int, y: torch.Tensor
         ctypes.byref(layer._r), ctypes.byref(layer._x), _ptr(x), ntok, topk, ctypes.byref(o), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(), _stream(stream)))
     return y, topk_idx, topk_w
+
+
+def epq_moe_forward_noalloc(layer: MoELayer, x: torch.Tensor, topk: int, y: torch.Tensor,
+                            topk_idx: torch.Tensor | None = None, topk_w: torch.Tensor | None = None,
+                            rms_prenorm: bool = False, rms_eps: float = 0.0, stream=None):
+    """The MoE layer with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot allocate device memory: nothing is allocated
+    here either, so y (and the optional top-K outputs) must be supplied.
+    """
+    lib = load()
+    o = MoeOpts(int(rms_prenorm), float(rms_eps), None, None, 0)
+    _check("epq_moe_forward_noalloc", lib.epq_moe_forward_noalloc(
+        ctypes.byref(layer._r), ctypes.byref(layer._x), _ptr(x), x.shape[0], topk, ctypes.byref(o), _ptr(y),
+        _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+    return y

@@ -23,6 +23,7 @@
 //
 // Each expert's weights are read once per layer however many tokens use it.
 #include <algorithm>
+#include <mutex>
 
 #include "gemv_core.cuh"
 
@@ -978,4 +979,53 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return EPQ_OK;
+}
+
+// ------------------------------------------------------------------ fixed-scratch variant
+// A copy of the MoE workspace that lives in a file-scope device array instead
+// of caller memory, for callers that cannot allocate device memory.  Every
+// GPU that loads the library holds these bytes until the process exits.
+namespace {
+constexpr size_t kFixedScratchBytes = size_t(1) << 20;  // 1 MiB
+__device__ __align__(256) uint8_t g_moe_fixed_scratch[kFixedScratchBytes];
+
+std::mutex g_fixed_mu;
+void *g_fixed_ptr[64] = {};
+
+// Device address of the fixed scratch on the current device.  The host-side
+// name of the array is only a stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+epq_status fixed_scratch_ptr(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return EPQ_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_fixed_mu);
+  if (!g_fixed_ptr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_fixed_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    g_fixed_ptr[dev] = p;
+  }
+  *out = g_fixed_ptr[dev];
+  return EPQ_OK;
+}
+}  // namespace
+
+extern "C" epq_status epq_moe_forward_noalloc(const epq_router *router, const epq_experts *experts, const float *x,
+                                              int ntok, int topk, const epq_moe_opts *opts, float *y,
+                                              int32_t *topk_idx, float *topk_w, epq_stream_t stream) {
+  const epq_status st = check_moe(router, experts, ntok, topk);
+  if (st != EPQ_OK) return st;
+  const size_t need = ws_layout(ntok, topk, router->n_experts, experts->inter).total;
+  if (need > kFixedScratchBytes) return EPQ_ERR_WORKSPACE;
+  void *ws = nullptr;
+  const epq_status sp = fixed_scratch_ptr(&ws);
+  if (sp != EPQ_OK) return sp;
+  // The array keeps whatever the previous call left; the ticket counter at
+  // its start must read zero when the router starts, so clear it here.
+  const cudaError_t e = cudaMemsetAsync(ws, 0, 16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return epq_moe_forward(router, experts, x, ntok, topk, opts, y, topk_idx, topk_w, ws, kFixedScratchBytes, stream);
 }
