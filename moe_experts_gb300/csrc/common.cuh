@@ -121,6 +121,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
       : "memory");
 }
 
+// Warp-wide asynchronous copy of `bytes` (a multiple of 16) from global to
+// shared memory in 16-byte pieces, all lanes in parallel; each lane then
+// arms one arrival on `bar` that fires when its own pieces have landed (the
+// barrier must expect 32 arrivals per phase).  For small, scattered tiles
+// this keeps many requests in flight without a single copy engine.
+__device__ __forceinline__ void warp_copy_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, int lane) {
+  const uint32_t d = smem_addr(dst_smem);
+  const char *sp = static_cast<const char *>(src_gmem);
+  for (uint32_t off = 16u * lane; off < bytes; off += 512u)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + off), "l"(sp + off) : "memory");
+}
+__device__ __forceinline__ void warp_copy_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding kernel's writes /
 // allow the next kernel to begin its prologue.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

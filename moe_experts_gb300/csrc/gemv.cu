@@ -51,17 +51,22 @@ struct GemvParams {
   float rms_eps;
   int x_group, x_head_dim;
   int early_weights;   // weights are ready: stream them before the PDL wait
+  int xstage;          // x is staged once per CTA in shared memory (coalesced)
   unsigned *err;
 };
 
 struct SmemLayout {
-  uint32_t full_off, empty_off, rfull_off, rempty_off, red_off, scratch_off, total;
+  uint32_t full_off, empty_off, rfull_off, rempty_off, red_off, scratch_off, xs_off, total;
 };
+
+// x staging: 32-float columns padded to 36 floats, so that a thread reading
+// its own column with 16-byte loads never shares a bank with its neighbours.
+constexpr int kXPad = 36;
 
 __host__ __device__ inline int wpg_of(int tpr) { return tpr > 32 ? tpr / 32 : 1; }
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, uint32_t stage_bytes, int nv, int red_rows, int tpr,
-                                                  int nthreads) {
+                                                  int nthreads, int xstage_cols = 0) {
   SmemLayout L;
   uint32_t o = static_cast<uint32_t>(stages) * stage_bytes + 16;  // +16: code-word over-read pad
   o = (o + 15u) & ~15u;
@@ -78,6 +83,9 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, uint32_t stage_byt
   o = (o + 15u) & ~15u;
   L.scratch_off = o;
   o += 4u * 2 * nv * (nthreads / 32);
+  o = (o + 15u) & ~15u;
+  L.xs_off = o;
+  o += 4u * nv * (xstage_cols / 32) * kXPad;
   L.total = (o + 15u) & ~15u;
   return L;
 }
@@ -95,7 +103,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
   const int nwarps = nthreads / 32;
   const bool has_fin = p.tpr > 32;   // cross-warp rows go through the finisher warp
   const int wpg = wpg_of(p.tpr);
-  const SmemLayout L = smem_layout(p.stages, p.stage_bytes, NV, p.red_rows, p.tpr, nthreads);
+  const SmemLayout L = smem_layout(p.stages, p.stage_bytes, NV, p.red_rows, p.tpr, nthreads, p.xstage ? p.cols : 0);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full_off);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty_off);
   uint64_t *rfull = reinterpret_cast<uint64_t *>(smem + L.rfull_off);
@@ -175,31 +183,58 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
   float xr[NV][32];
   float xsum[NV];
   XCol<NV> xc;
+  float *xs = reinterpret_cast<float *>(smem + L.xs_off);
+  if (p.xstage) {
+    // coalesced, once per CTA: consumer threads copy (gathered) x into the
+    // padded staging area and take per-vector max |x| and sum x^2 as they go
+    const int c4 = p.cols / 4;
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    float amax = 0.0f, ssq = 0.0f;
-    xsum[v] = 0.0f;
-    const bool vv = v < p.nv && active;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (vv) q4 = *reinterpret_cast<const float4 *>(p.x + v * p.x_stride + xg.src(32 * c + j));
-      xr[v][j] = q4.x;
-      xr[v][j + 1] = q4.y;
-      xr[v][j + 2] = q4.z;
-      xr[v][j + 3] = q4.w;
+    for (int v = 0; v < NV; ++v) {
+      float amax = 0.0f, ssq = 0.0f;
+      if (!is_fin && v < p.nv) {
+        for (int e4 = tid; e4 < c4; e4 += nthreads) {
+          const int j = 4 * e4;
+          const float4 q4 = *reinterpret_cast<const float4 *>(p.x + v * p.x_stride + xg.src(j));
+          *reinterpret_cast<float4 *>(xs + (v * p.nblk + j / 32) * kXPad + (j & 31)) = q4;
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(q4.x), fabsf(q4.y)), fmaxf(fabsf(q4.z), fabsf(q4.w))));
+          ssq = fmaf(q4.x, q4.x, fmaf(q4.y, q4.y, fmaf(q4.z, q4.z, fmaf(q4.w, q4.w, ssq))));
+        }
+      }
+      if (!is_fin) {
+        amax = warp_max_all(amax);
+        ssq = warp_sum_xor<32>(ssq);
+        if (lane == 0) {
+          scratch[(2 * v) * nwarps + (tid >> 5)] = amax;
+          scratch[(2 * v + 1) * nwarps + (tid >> 5)] = ssq;
+        }
+      }
     }
+  } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      amax = fmaxf(amax, fabsf(xr[v][j]));
-      if (g == 0) ssq = fmaf(xr[v][j], xr[v][j], ssq);
-    }
-    if (!is_fin) {
-      amax = warp_max_all(amax);
-      ssq = warp_sum_xor<32>(ssq);
-      if (lane == 0) {
-        scratch[(2 * v) * nwarps + (tid >> 5)] = amax;
-        scratch[(2 * v + 1) * nwarps + (tid >> 5)] = ssq;
+    for (int v = 0; v < NV; ++v) {
+      float amax = 0.0f, ssq = 0.0f;
+      const bool vv = v < p.nv && active;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vv) q4 = *reinterpret_cast<const float4 *>(p.x + v * p.x_stride + xg.src(32 * c + j));
+        xr[v][j] = q4.x;
+        xr[v][j + 1] = q4.y;
+        xr[v][j + 2] = q4.z;
+        xr[v][j + 3] = q4.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        amax = fmaxf(amax, fabsf(xr[v][j]));
+        if (g == 0) ssq = fmaf(xr[v][j], xr[v][j], ssq);
+      }
+      if (!is_fin) {
+        amax = warp_max_all(amax);
+        ssq = warp_sum_xor<32>(ssq);
+        if (lane == 0) {
+          scratch[(2 * v) * nwarps + (tid >> 5)] = amax;
+          scratch[(2 * v + 1) * nwarps + (tid >> 5)] = ssq;
+        }
       }
     }
   }
@@ -217,6 +252,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
     // every product lands at scale 2^(-23 - E).
     const int E = bound_exponent(a);
     expo[v] = E;
+    if (p.xstage) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active && v < p.nv) q4 = *reinterpret_cast<const float4 *>(xs + (v * p.nblk + c) * kXPad + j);
+        xr[v][j] = q4.x;
+        xr[v][j + 1] = q4.y;
+        xr[v][j + 2] = q4.z;
+        xr[v][j + 3] = q4.w;
+      }
+    }
     xsum[v] = scale_column<FMT>(xr[v], E, xc.p[v]);
     float r = 1.0f;
     if (p.rms) r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.cols)), p.rms_eps)));
@@ -321,7 +367,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
 
 // ------------------------------------------------------------------ host
 struct Plan {
-  int tpr, groups, gpt, teams, rpg, tile_rows, stages;
+  int tpr, groups, gpt, teams, rpg, tile_rows, stages, xstage;
   uint32_t stage_bytes, smem;
   unsigned grid;
 };
@@ -390,7 +436,18 @@ bool make_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, int n
   if (pl->teams == 1 && per_team < 2 && fits(2)) per_team = 2;
   pl->stages = per_team * pl->teams;
   if (!fits(pl->stages)) return false;
-  pl->smem = smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads).total;
+  // stage x in shared memory too when it fits beside the ring
+  const int min_stages = pl->teams == 1 ? 2 : pl->teams;
+  pl->xstage = 0;
+  for (int st = pl->stages; st >= min_stages; st -= pl->teams) {
+    if (smem_layout(st, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads, cols).total <=
+        static_cast<uint32_t>(dev.max_smem_optin)) {
+      pl->stages = st;
+      pl->xstage = 1;
+      break;
+    }
+  }
+  pl->smem = smem_layout(pl->stages, pl->stage_bytes, nv, red_rows, pl->tpr, nthreads, pl->xstage ? cols : 0).total;
   return true;
 }
 
@@ -477,6 +534,7 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   p.x_group = xg;
   p.x_head_dim = opts.x_head_dim;
   p.early_weights = opts.weights_ready ? 1 : 0;
+  p.xstage = pl.xstage;
   p.err = err;
   for (int v0 = 0; v0 < nvec; v0 += 2) {
     p.nv = std::min(2, nvec - v0);

@@ -33,7 +33,7 @@ namespace {
 constexpr int kMaxTok = 16;
 constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 1024;
-constexpr int kRouterThreads = 256;
+constexpr int kRouterThreads = 128;
 constexpr int kMaxConsumers = 512;
 
 // ------------------------------------------------------------------ workspace
@@ -101,30 +101,40 @@ struct MoeArgs {
 };
 
 // ------------------------------------------------------------------ 1. router
+constexpr int kRouterWarps = kRouterThreads / 32;
+constexpr int kRouterXSmem = 40 * 1024;  // stage x in shared memory up to this size (static smem stays < 48 KB)
+
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a) {
   __shared__ float s_rms[kMaxTok];
-  __shared__ float s_red[kRouterThreads / 32][kMaxTok];
+  __shared__ float s_red[kRouterWarps][kMaxTok];
   __shared__ int s_last;
   __shared__ int s_slot_of[kMaxExperts];
+  __shared__ __align__(16) float s_x[kRouterXSmem / 4];
+  __shared__ int s_idx[kMaxTok * kMaxTopk];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
   pdl_wait();
 
-  // per-token sum of squares and max |x| (every CTA: it needs the rms factor)
+  // stage x (all tokens) and take per-token sum of squares and max |x|
+  const bool xs = static_cast<int64_t>(a.ntok) * a.H * 4 <= kRouterXSmem;
   for (int t = 0; t < a.ntok; ++t) {
     float ss = 0.0f, mx = 0.0f;
-    for (int j = tid; j < a.H; j += kRouterThreads) {
-      const float v = a.x[static_cast<int64_t>(t) * a.H + j];
-      ss = fmaf(v, v, ss);
-      mx = fmaxf(mx, fabsf(v));
+    const float4 *src = reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(t) * a.H);
+    for (int j = tid; j < a.H / 4; j += kRouterThreads) {
+      const float4 v = src[j];
+      if (xs) reinterpret_cast<float4 *>(s_x + t * a.H)[j] = v;
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
     ss = warp_sum_xor<32>(ss);
     mx = warp_max_all(mx);
-    if (lane == 0) s_red[warp][t] = ss;
+    if (lane == 0) {
+      s_red[warp][t] = ss;
+    }
     __syncthreads();
     if (tid == 0) {
       float tot = 0.0f;
-      for (int w = 0; w < kRouterThreads / 32; ++w) tot += s_red[w][t];
+      for (int w = 0; w < kRouterWarps; ++w) tot += s_red[w][t];
       s_rms[t] = a.rms ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(a.H)), a.eps))) : 1.0f;
     }
     __syncthreads();
@@ -132,29 +142,43 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
     __syncthreads();
     if (tid == 0 && blockIdx.x == 0) {
       float m = 0.0f;
-      for (int w = 0; w < kRouterThreads / 32; ++w) m = fmaxf(m, s_red[w][t]);
+      for (int w = 0; w < kRouterWarps; ++w) m = fmaxf(m, s_red[w][t]);
       a.xstat[2 * t] = m;
       a.xstat[2 * t + 1] = s_rms[t];
     }
     __syncthreads();
   }
+  const float *xbase = xs ? s_x : a.x;
 
-  // logits: warp per row; rows E .. (shared gate vector) as one extra row
+  // logits: warp per row (rows E.. = the shared gate vector as one extra row);
+  // each lane keeps 8 independent 16-byte loads of the row in flight.
   const int nrows = a.E + (a.gvec ? 1 : 0);
   const int r_begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * nrows) / gridDim.x);
   const int r_end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * nrows) / gridDim.x);
-  for (int r = r_begin + warp; r < r_end; r += kRouterThreads / 32) {
-    const float *wrow = r < a.E ? a.R + static_cast<int64_t>(r) * a.H : a.gvec;
+  for (int r = r_begin + warp; r < r_end; r += kRouterWarps) {
+    const float4 *wrow = reinterpret_cast<const float4 *>(r < a.E ? a.R + static_cast<int64_t>(r) * a.H : a.gvec);
     float acc[kMaxTok];
 #pragma unroll
     for (int t = 0; t < kMaxTok; ++t) acc[t] = 0.0f;
-    for (int j = lane * 4; j < a.H; j += 128) {
-      const float4 wv = *reinterpret_cast<const float4 *>(wrow + j);
+    const int n4 = a.H / 4;  // multiple of 64
+    for (int j0 = 0; j0 < n4; j0 += 256) {
+      float4 wv[8];
 #pragma unroll
-      for (int t = 0; t < kMaxTok; ++t) {
-        if (t < a.ntok) {
-          const float4 xv = *reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(t) * a.H + j);
-          acc[t] = fmaf(wv.x, xv.x, fmaf(wv.y, xv.y, fmaf(wv.z, xv.z, fmaf(wv.w, xv.w, acc[t]))));
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * 32 + lane;
+        wv[u] = j < n4 ? __ldcs(wrow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * 32 + lane;
+        if (j < n4) {
+#pragma unroll
+          for (int t = 0; t < kMaxTok; ++t) {
+            if (t < a.ntok) {
+              const float4 xv = reinterpret_cast<const float4 *>(xbase + static_cast<int64_t>(t) * a.H)[j];
+              acc[t] = fmaf(wv[u].x, xv.x, fmaf(wv[u].y, xv.y, fmaf(wv[u].z, xv.z, fmaf(wv[u].w, xv.w, acc[t]))));
+            }
+          }
         }
       }
     }
@@ -187,15 +211,19 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
   // softmax + top-K: warp per token
   for (int t = warp; t < a.ntok; t += kRouterThreads / 32) {
     const float *lt = a.logits + static_cast<int64_t>(t) * a.E;
-    float lmax = -INFINITY;
-    for (int e = lane; e < a.E; e += 32) lmax = fmaxf(lmax, __ldcg(lt + e));
-    lmax = warp_max_all(lmax);
-    float den = 0.0f;
-    for (int e = lane; e < a.E; e += 32) den += expf(__ldcg(lt + e) - lmax);
-    den = warp_sum_xor<32>(den);
+    // one round of independent loads, then everything from registers
     float lv[kMaxExperts / 32];
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) lv[i] = (lane + 32 * i < a.E) ? __ldcg(lt + lane + 32 * i) : -INFINITY;
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) lmax = fmaxf(lmax, lv[i]);
+    lmax = warp_max_all(lmax);
+    float den = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i)
+      if (lane + 32 * i < a.E) den += expf(lv[i] - lmax);
+    den = warp_sum_xor<32>(den);
     float sel_sum = 0.0f;
     int prev_e = -1;
     float prev_v = INFINITY;
@@ -237,6 +265,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
       for (int k = 0; k < a.topk; ++k) {
         const float wk = a.norm_topk ? __fdiv_rn(pk[k], sel_sum) : pk[k];
         a.idx[t * a.topk + k] = ek[k];
+        s_idx[t * a.topk + k] = ek[k];
         a.w[t * a.topk + k] = wk;
         if (a.out_idx) a.out_idx[t * a.topk + k] = ek[k];
         if (a.out_w) a.out_w[t * a.topk + k] = wk;
@@ -246,11 +275,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
   __syncthreads();
 
   // group tokens by expert: slots in ascending expert order (block scan)
-  __shared__ int s_idx[kMaxTok * kMaxTopk];
   __shared__ int s_wsum[kRouterThreads / 32];
   const int nsel = a.ntok * a.topk;
   for (int e = tid; e < a.E; e += kRouterThreads) s_slot_of[e] = 0;
-  for (int i = tid; i < nsel; i += kRouterThreads) s_idx[i] = __ldcg(a.idx + i);
   __syncthreads();
   for (int i = tid; i < nsel; i += kRouterThreads) s_slot_of[s_idx[i]] = 1;
   __syncthreads();
@@ -356,7 +383,8 @@ bool engine_plan(int cols, int64_t per_row, bool swiglu, int64_t rows_hint, int 
   const uint32_t meta_bytes = 4u * meta_words(ntok, topk);
   const int64_t hbytes = 4ll * ntok * (topk + 1) * I_for_h;
   pl->stage_h = down && hbytes <= kHSmemMax;
-  const uint32_t hs_bytes = pl->stage_h ? static_cast<uint32_t>(hbytes) : 0u;
+  // staged h: the scaled values plus one scaled column sum per 32 values
+  const uint32_t hs_bytes = pl->stage_h ? static_cast<uint32_t>(hbytes + hbytes / 32) : 0u;
   const uint32_t acc_bytes = down ? 4u * ntok * pl->tile_rows : 0u;
   pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, tune_ring_bytes() / pl->stage_bytes)));
   for (;;) {
@@ -465,6 +493,31 @@ __device__ __forceinline__ float fin_row(const float *rbuf, int r, int wpg) {
   return acc;
 }
 
+
+// Producer warp: expert id of `slot` (slot >= nact means the shared expert,
+// returned as -1).  The ids are fetched once, 32 per lane-parallel load, so
+// the producer never waits on a global load between bulk copies.
+struct SlotIds {
+  int ids[ (kMaxTok * kMaxTopk + 1 + 31) / 32 ];  // one id per lane per chunk
+  int nact;
+  __device__ void load(const MoeArgs &a, int lane) {
+    nact = __ldcg(a.meta);
+#pragma unroll
+    for (int c = 0; c < (kMaxTok * kMaxTopk + 1 + 31) / 32; ++c) {
+      const int s = c * 32 + lane;
+      ids[c] = s < nact ? __ldcg(a.active + s) : -1;
+    }
+  }
+  // all lanes of the warp must call this
+  __device__ int get(int slot) const {
+    int v = -1;
+#pragma unroll
+    for (int c = 0; c < (kMaxTok * kMaxTopk + 1 + 31) / 32; ++c)
+      if (slot / 32 == c) v = __shfl_sync(0xffffffffu, ids[c], slot & 31);
+    return slot < nact ? v : -1;
+  }
+};
+
 // ------------------------------------------------------------------ 2. gate/up
 template <int FMT, int RPG>
 __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const EngineArgs p) {
@@ -484,7 +537,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 32);  // one arrival per producer lane (warp_copy_arrive)
       mbar_init(&empty[s], nwarps);
     }
     for (int b = 0; b < kRedRing; ++b) {
@@ -507,33 +560,32 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
   };
 
   if (tid >= nthreads && tid < nthreads + 32) {
-    // producer
-    if (tid != nthreads) return;
-    const int nact = __ldcg(a.meta);
-    int t = 0, issued = 0;
-    bool ok = true;
+    // producer warp: the expert ids are held by the warp; every tile is
+    // copied by all 32 lanes with 16-byte asynchronous copies
+    const int plane = tid - nthreads;
+    SlotIds ids;
+    ids.load(a, plane);
+    int t = 0;
     for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
       const int s = t % p.stages;
-      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, t)) {
-        ok = false;
-        break;
+      const int slot = static_cast<int>(r0 / I);
+      const int e = ids.get(slot);
+      if (t >= p.stages && !warp_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, t)) {
+        // drain: every lane waits for its own copies still in flight
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        return;
       }
       const int nr = tile_len(r0);
-      const int slot = static_cast<int>(r0 / I);
       const int i0 = static_cast<int>(r0 % I);
-      const uint8_t *base = slot < nact ? a.gate_up + static_cast<int64_t>(__ldcg(a.active + slot)) * a.gu_stride
-                                        : a.sh_gate_up;
+      const uint8_t *base = e >= 0 ? a.gate_up + static_cast<int64_t>(e) * a.gu_stride : a.sh_gate_up;
       const uint32_t bytes = static_cast<uint32_t>(nr * a.gu_row_bytes);
       uint8_t *dst = smem + static_cast<uint32_t>(s) * p.stage_bytes;
-      mbar_arrive_expect_tx(&full[s], 2 * bytes);
-      bulk_g2s(dst, base + static_cast<int64_t>(i0) * a.gu_row_bytes, bytes, &full[s]);
-      bulk_g2s(dst + p.tile_rows * a.gu_row_bytes, base + static_cast<int64_t>(I + i0) * a.gu_row_bytes, bytes,
-               &full[s]);
-      ++issued;
+      warp_copy_g2s(dst, base + static_cast<int64_t>(i0) * a.gu_row_bytes, bytes, plane);
+      warp_copy_g2s(dst + p.tile_rows * a.gu_row_bytes, base + static_cast<int64_t>(I + i0) * a.gu_row_bytes, bytes,
+                    plane);
+      warp_copy_arrive(&full[s]);
     }
-    if (!ok)
-      for (int u = max(0, issued - p.stages); u < issued; ++u)
-        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT, u);
+    asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
 
@@ -661,7 +713,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 32);  // one arrival per producer lane (warp_copy_arrive)
       mbar_init(&empty[s], nwarps);
     }
     for (int b = 0; b < kRedRing; ++b) {
@@ -681,31 +733,28 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
   const int ntiles = static_cast<int>((re - rb + p.tile_rows - 1) / p.tile_rows);
 
   if (tid >= nthreads && tid < nthreads + 32) {
-    if (tid != nthreads) return;
+    // producer warp: all 32 lanes copy every unit with 16-byte async copies
+    const int plane = tid - nthreads;
     const int nslots = __ldcg(a.meta + 1);
-    const int nact = __ldcg(a.meta);
+    SlotIds ids;
+    ids.load(a, plane);
     const int nunits = ntiles * nslots;
-    int issued = 0;
-    bool ok = true;
     for (int u = 0; u < nunits; ++u) {
       const int s = u % p.stages;
-      if (u >= p.stages && !mbar_wait(&empty[s], ((u / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, u)) {
-        ok = false;
-        break;
-      }
       const int tile = u / nslots, slot = u % nslots;
+      const int e = ids.get(slot);
+      if (u >= p.stages && !warp_wait(&empty[s], ((u / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, u)) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        return;
+      }
       const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
       const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
-      const uint8_t *base = slot < nact ? a.down + static_cast<int64_t>(__ldcg(a.active + slot)) * a.dn_stride
-                                        : a.sh_down;
+      const uint8_t *base = e >= 0 ? a.down + static_cast<int64_t>(e) * a.dn_stride : a.sh_down;
       const uint32_t bytes = static_cast<uint32_t>(nr * a.dn_row_bytes);
-      mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_g2s(smem + static_cast<uint32_t>(s) * p.stage_bytes, base + r0 * a.dn_row_bytes, bytes, &full[s]);
-      ++issued;
+      warp_copy_g2s(smem + static_cast<uint32_t>(s) * p.stage_bytes, base + r0 * a.dn_row_bytes, bytes, plane);
+      warp_copy_arrive(&full[s]);
     }
-    if (!ok)
-      for (int u = max(0, issued - p.stages); u < issued; ++u)
-        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT, u);
+    asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
 
@@ -715,13 +764,43 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
   const int ctid = is_fin ? nthreads + lane : tid;
   const int nthr = nthreads + (has_fin ? 32 : 0);
   load_meta(a, m, ctid, nthr, true);
+  const int nblk = I / 32;
+  const int nh = a.ntok * (a.topk + 1);
+  // staged h: pair i of column c of slot vector hsi at pairs[(hsi*16 + i)*nblk + c]
+  // (neighbouring threads read neighbouring pairs); scaled column sums after.
+  f2_t *pairs = reinterpret_cast<f2_t *>(hs_smem);
+  float *hsum = hs_smem + static_cast<int64_t>(nh) * I;  // [nh][nblk]
+  named_sync(1, nthr);  // the h exponents are in m.expo
   if (p.stage_h) {
-    const int n4 = a.ntok * (a.topk + 1) * I / 4;
-    const float4 *src = reinterpret_cast<const float4 *>(a.h);
-    float4 *dst = reinterpret_cast<float4 *>(hs_smem);
-    for (int i = ctid; i < n4; i += nthr) dst[i] = __ldcg(src + i);
+    // coalesced: thread q takes 4 consecutive floats; 8 consecutive threads
+    // hold one 32-float column and reduce its sum with shuffles
+    const int n4 = nh * I / 4;
+    for (int q0 = ctid - (ctid & 31); q0 < n4; q0 += nthr) {
+      const int q = q0 + (ctid & 31);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      int hsi = 0, col = 0, j = 0;
+      if (q < n4) {
+        v = __ldcg(reinterpret_cast<const float4 *>(a.h) + q);
+        hsi = (4 * q) / I;
+        col = ((4 * q) % I) / 32;
+        j = (4 * q) & 31;
+      }
+      const int E = m.expo[hsi];
+      float sum = (v.x + v.y) + (v.z + v.w);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      if (q < n4) {
+        const int base = (hsi * 16 + j / 2) * nblk + col;
+        pairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
+                              scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
+        pairs[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
+                                     scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
+        if (j == 0) hsum[hsi * nblk + col] = scale_pow2(sum, -23 - E);
+      }
+    }
+    named_sync(1, nthr);
   }
-  named_sync(1, nthr);
   const int nslots = *m.nslots;
   const int nunits = ntiles * nslots;
 
@@ -758,7 +837,6 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
   }
 
   const int g = tid / p.tpr, c = tid % p.tpr;
-  const int nblk = I / 32;
   const bool active = c < nblk;
   ColConst<FMT> cc;
   cc.init(active ? c : 0);
@@ -781,18 +859,24 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
       const int tok = ent >> 5, k = ent & 31;
       const int hsi = tok * (a.topk + 1) + k;
       const int E = m.expo[hsi];
-      if (active) {
-        const float *src = p.stage_h ? hs_smem + static_cast<int64_t>(hsi) * I + 32 * c
-                                     : a.h + static_cast<int64_t>(hsi) * I + 32 * c;
-        load_column(src, xr);
-        xs[0] = scale_column<FMT>(xr, E, xc.p[0]);
+      const bool rows_here = g * RPG < nr;  // this group has rows in the tile
+      if (active && rows_here) {
+        if (p.stage_h) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xc.p[0][i] = pairs[(hsi * 16 + i) * nblk + c];
+          xs[0] = hsum[hsi * nblk + c];
+        } else {
+          load_column(a.h + static_cast<int64_t>(hsi) * I + 32 * c, xr);
+          xs[0] = scale_column<FMT>(xr, E, xc.p[0]);
+        }
       }
       float part[1][RPG];
 #pragma unroll
       for (int q = 0; q < RPG; ++q) {
         const int lr = g * RPG + q;
         float pr[1] = {0.0f};
-        if (active && lr < nr) column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes, cc, xc, xs, pr);
+        if (active && rows_here && lr < nr)
+          column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes, cc, xc, xs, pr);
         part[0][q] = pr[0];
       }
       if (j == ne - 1) {
@@ -945,7 +1029,7 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
     // The ticket counter starts at zero in a fresh (zero-filled) workspace and
     // the router's last CTA puts it back to zero for the next call.
     const int nrows = E + (a.gvec ? 1 : 0);
-    const unsigned rgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (nrows + 7) / 8)));
+    const unsigned rgrid = static_cast<unsigned>(std::max(1, std::min(2 * dev.sm_count, (nrows + kRouterWarps - 1) / kRouterWarps)));
     router_kernel<<<rgrid, kRouterThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   }
