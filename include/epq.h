@@ -216,7 +216,11 @@ typedef struct {
                         EPQ_MOE_DOWN: the selected kernels only.  Stages of
                         one layer may be issued by separate calls in order
                         with the same arguments and workspace (the workspace
-                        carries the routing and h between them). */
+                        carries the logits, routing and h between them).
+                        The gate/up stage computes the routing; a call with
+                        the router stage but not the gate/up stage adds a
+                        one-CTA routing kernel when it returns topk_idx /
+                        topk_w or runs the down stage. */
 } epq_moe_opts;
 
 enum { EPQ_MOE_ROUTE = 1, EPQ_MOE_GATE_UP = 2, EPQ_MOE_DOWN = 4 };
@@ -229,14 +233,14 @@ size_t epq_moe_workspace_bytes(const epq_router *router, const epq_experts *expe
  *   x          float32 [ntok][H]            y  float32 [ntok][H] (may equal x)
  *   topk_idx   NULL or int32 [ntok][topk]   (selected experts, best first)
  *   topk_w     NULL or float32 [ntok][topk] (their combine weights)
- *   workspace  device scratch of epq_moe_workspace_bytes(), zero-filled
- *              before its first use (e.g. one cudaMemsetAsync).  Each call
- *              leaves its first 16 bytes (a ticket counter) at zero again, so
- *              the same workspace serves any number of later calls; calls that
- *              share a workspace must be ordered on one stream.  After a
- *              device-side error (epq_device_error) zero it again.
- * Three kernels are queued: router + top-K + grouping, gate/up + SwiGLU,
- * down + combine + residual.  No host synchronisation. */
+ *   workspace  device scratch of epq_moe_workspace_bytes(); no
+ *              initialisation is needed and nothing carries over between
+ *              calls, except between the stages of one layer (see stages).
+ *              Calls that share a workspace must be ordered on one stream.
+ * Three kernels are queued: router logits; routing (softmax, top-K,
+ * grouping) + gate/up + SwiGLU; down + combine + residual.  No host
+ * synchronisation.  Logits must be finite (a NaN logit ranks above all
+ * others; the selection is then unspecified by the method). */
 epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts, const float *x, int ntok,
                            int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w,
                            void *workspace, size_t workspace_bytes, epq_stream_t stream);
@@ -257,10 +261,9 @@ epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts,
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
- *   - All calls on a device share the array, which keeps the previous call's
- *     contents; each call clears the part that must start at zero.  Calls
- *     that may overlap on the GPU (different streams without ordering) race
- *     on the array and must not be issued. */
+ *   - All calls on a device share the array.  Calls that may overlap on
+ *     the GPU (different streams without ordering) race on the array and
+ *     must not be issued. */
 epq_status epq_moe_forward_noalloc(const epq_router *router, const epq_experts *experts, const float *x,
                                    int ntok, int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx,
                                    float *topk_w, epq_stream_t stream);

@@ -252,7 +252,7 @@ def epq_moe_forward(layer: MoELayer, x: torch.Tensor, topk: int, y: torch.Tensor
     if y is None:
         y = torch.empty_like(x)
     if workspace is None:
-        workspace = torch.zeros(layer.workspace_bytes(ntok, topk), dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(layer.workspace_bytes(ntok, topk), dtype=torch.uint8, device=x.device)
     o = MoeOpts(int(rms_prenorm), float(rms_eps), _addr(logits_out), _addr(h_out), int(stages))
     _check("epq_moe_forward", lib.epq_moe_forward(
         ctypes.byref(layer._r), ctypes.byref(layer._x), _ptr(x), ntok, topk, ctypes.byref(o), _ptr(y),

@@ -5,17 +5,21 @@
 // combine.  Here all of it stays on the GPU in three kernels on one stream:
 //
 //   1. router_kernel   logits = R xin (+bias) for every token (warp per
-//                      expert row); the last CTA to finish (an atomic ticket,
-//                      no spinning) runs softmax + top-K per token and groups
-//                      tokens by expert: the distinct experts in ascending
-//                      order become "slots", each with its list of
-//                      (token, choice) entries; the shared expert is the last
-//                      slot and serves every token.
-//   2. gateup_kernel   persistent TMA-staged dequant-GEMV over the virtual
-//                      rows slot*I + i: each tile stages the gate rows and the
-//                      matching up rows of one expert; every token entry of
-//                      the slot reuses the staged bytes; the epilogue writes
-//                      h = silu(g) * u and records max|h| per (token, slot).
+//                      expert row, the row's first loads issued before the
+//                      grid-dependency wait), plus max|x| and the RMS factor.
+//   2. gateup_kernel   every CTA first routes all tokens on its own from the
+//                      logits (softmax + top-K per token, then grouping: the
+//                      distinct experts in ascending order become "slots",
+//                      each with its list of (token, choice) entries; the
+//                      shared expert is the last slot and serves every
+//                      token), so no grid-wide step sits between the router
+//                      and the expert weights.  Then a persistent staged
+//                      dequant-GEMV over the virtual rows slot*I + i: each
+//                      tile stages the gate rows and the matching up rows of
+//                      one expert; every token entry of the slot reuses the
+//                      staged bytes; the epilogue writes h = silu(g) * u and
+//                      records max|h| per (token, slot).  CTA 0 publishes the
+//                      routing for the down kernel and the caller.
 //   3. down_kernel     persistent over hidden rows: for each tile of rows the
 //                      down rows of every slot are staged in turn, applied to
 //                      each entry's h, weighted and accumulated per token in
@@ -38,7 +42,7 @@ constexpr int kMaxConsumers = 512;
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-  size_t counter, logits, xstat, gshared, idx, w, meta, active, cnt, list, hmax, h, total;
+  size_t logits, xstat, gshared, idx, w, meta, active, cnt, list, hmax, h, total;
 };
 
 inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -47,7 +51,6 @@ WsLayout ws_layout(int ntok, int topk, int E, int I) {
   WsLayout L;
   size_t o = 0;
   const size_t slots = static_cast<size_t>(ntok) * topk + 1;
-  L.counter = o; o = al256(o + 16);
   L.logits = o; o = al256(o + 4ull * ntok * E);
   L.xstat = o; o = al256(o + 8ull * ntok);
   L.gshared = o; o = al256(o + 4ull * ntok);
@@ -85,7 +88,6 @@ struct MoeArgs {
   int32_t *out_idx;
   float *out_w;
   // workspace views
-  uint32_t *counter;
   float *logits;
   float *xstat;      // [ntok][2]: max|x| (as float), rms factor
   float *gshared;    // [ntok]
@@ -103,24 +105,48 @@ struct MoeArgs {
 // ------------------------------------------------------------------ 1. router
 constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kRouterXSmem = 40 * 1024;  // stage x in shared memory up to this size (static smem stays < 48 KB)
+constexpr int kRouterChunk = 16;         // 16-byte loads of a router row in flight per lane
 
+// chunk j0.. of router row r (zeros past the row or for r >= r_end)
+__device__ __forceinline__ void router_chunk(const MoeArgs &a, int r, int r_end, int j0, int lane,
+                                             float4 (&wv)[kRouterChunk]) {
+  const int n4 = a.H / 4;
+  const float4 *wrow = reinterpret_cast<const float4 *>(r < a.E ? a.R + static_cast<int64_t>(r) * a.H : a.gvec);
+#pragma unroll
+  for (int u = 0; u < kRouterChunk; ++u) {
+    const int j = j0 + u * 32 + lane;
+    wv[u] = (r < r_end && j < n4) ? __ldcs(wrow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Router logits of every token (NT >= ntok): warp per row of R; the rows
+// E.. hold the shared-expert gate vector as one extra row.  The first chunk
+// of each warp's first row is requested before the grid-dependency wait (R
+// is a weight: nothing upstream writes it).  CTA 0 publishes max|x| and the
+// RMS factor per token and clears the max|h| accumulators of the gate/up
+// kernel.
+template <int NT>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a) {
-  __shared__ float s_rms[kMaxTok];
-  __shared__ float s_red[kRouterWarps][kMaxTok];
-  __shared__ int s_last;
-  __shared__ int s_slot_of[kMaxExperts];
+  __shared__ float s_part[2][kRouterWarps][NT];
+  __shared__ float s_rms[NT];
   __shared__ __align__(16) float s_x[kRouterXSmem / 4];
-  __shared__ int s_idx[kMaxTok * kMaxTopk];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nrows = a.E + (a.gvec ? 1 : 0);
+  const int r_begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * nrows) / gridDim.x);
+  const int r_end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * nrows) / gridDim.x);
+  const int n4 = a.H / 4;  // multiple of 64
+  float4 wv[kRouterChunk];
+  router_chunk(a, r_begin + warp, r_end, 0, lane, wv);
   pdl_launch_dependents();
   pdl_wait();
 
-  // stage x (all tokens) and take per-token sum of squares and max |x|
+  // x staged in shared memory; per-token sum of squares and max |x|
   const bool xs = static_cast<int64_t>(a.ntok) * a.H * 4 <= kRouterXSmem;
   for (int t = 0; t < a.ntok; ++t) {
     float ss = 0.0f, mx = 0.0f;
     const float4 *src = reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(t) * a.H);
-    for (int j = tid; j < a.H / 4; j += kRouterThreads) {
+#pragma unroll 4
+    for (int j = tid; j < n4; j += kRouterThreads) {
       const float4 v = src[j];
       if (xs) reinterpret_cast<float4 *>(s_x + t * a.H)[j] = v;
       ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
@@ -129,51 +155,44 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
     ss = warp_sum_xor<32>(ss);
     mx = warp_max_all(mx);
     if (lane == 0) {
-      s_red[warp][t] = ss;
+      s_part[0][warp][t] = ss;
+      s_part[1][warp][t] = mx;
     }
-    __syncthreads();
-    if (tid == 0) {
-      float tot = 0.0f;
-      for (int w = 0; w < kRouterWarps; ++w) tot += s_red[w][t];
-      s_rms[t] = a.rms ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(a.H)), a.eps))) : 1.0f;
-    }
-    __syncthreads();
-    if (lane == 0) s_red[warp][t] = mx;
-    __syncthreads();
-    if (tid == 0 && blockIdx.x == 0) {
-      float m = 0.0f;
-      for (int w = 0; w < kRouterWarps; ++w) m = fmaxf(m, s_red[w][t]);
-      a.xstat[2 * t] = m;
-      a.xstat[2 * t + 1] = s_rms[t];
-    }
-    __syncthreads();
   }
+  __syncthreads();
+  if (tid < a.ntok) {
+    float tot = 0.0f, m = 0.0f;
+    for (int w = 0; w < kRouterWarps; ++w) {
+      tot += s_part[0][w][tid];
+      m = fmaxf(m, s_part[1][w][tid]);
+    }
+    const float r = a.rms ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(a.H)), a.eps)))
+                          : 1.0f;
+    s_rms[tid] = r;
+    if (blockIdx.x == 0) {
+      a.xstat[2 * tid] = m;
+      a.xstat[2 * tid + 1] = r;
+    }
+  }
+  if (blockIdx.x == 0)
+    for (int i = tid; i < a.ntok * (a.topk + 1); i += kRouterThreads) a.hmax[i] = 0u;
+  __syncthreads();
   const float *xbase = xs ? s_x : a.x;
 
-  // logits: warp per row (rows E.. = the shared gate vector as one extra row);
-  // each lane keeps 8 independent 16-byte loads of the row in flight.
-  const int nrows = a.E + (a.gvec ? 1 : 0);
-  const int r_begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * nrows) / gridDim.x);
-  const int r_end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * nrows) / gridDim.x);
+  bool preloaded = true;
   for (int r = r_begin + warp; r < r_end; r += kRouterWarps) {
-    const float4 *wrow = reinterpret_cast<const float4 *>(r < a.E ? a.R + static_cast<int64_t>(r) * a.H : a.gvec);
-    float acc[kMaxTok];
+    float acc[NT];
 #pragma unroll
-    for (int t = 0; t < kMaxTok; ++t) acc[t] = 0.0f;
-    const int n4 = a.H / 4;  // multiple of 64
-    for (int j0 = 0; j0 < n4; j0 += 256) {
-      float4 wv[8];
+    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+    for (int j0 = 0; j0 < n4; j0 += 32 * kRouterChunk) {
+      if (!preloaded) router_chunk(a, r, r_end, j0, lane, wv);
+      preloaded = false;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u * 32 + lane;
-        wv[u] = j < n4 ? __ldcs(wrow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRouterChunk; ++u) {
         const int j = j0 + u * 32 + lane;
         if (j < n4) {
 #pragma unroll
-          for (int t = 0; t < kMaxTok; ++t) {
+          for (int t = 0; t < NT; ++t) {
             if (t < a.ntok) {
               const float4 xv = reinterpret_cast<const float4 *>(xbase + static_cast<int64_t>(t) * a.H)[j];
               acc[t] = fmaf(wv[u].x, xv.x, fmaf(wv[u].y, xv.y, fmaf(wv[u].z, xv.z, fmaf(wv[u].w, xv.w, acc[t]))));
@@ -183,7 +202,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
       }
     }
 #pragma unroll
-    for (int t = 0; t < kMaxTok; ++t) {
+    for (int t = 0; t < NT; ++t) {
       if (t < a.ntok) {
         const float v = warp_sum_xor<32>(acc[t]) * s_rms[t];
         if (lane == 0) {
@@ -196,147 +215,217 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
       }
     }
   }
+}
 
-  // ticket: the last CTA to arrive finishes the routing
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned ticket = atomicAdd(a.counter, 1u);
-    s_last = ticket == gridDim.x - 1;
-    if (s_last) __threadfence();
+// ------------------------------------------------------------------ routing
+// Shared-memory copy of the routing results.
+struct Meta {
+  int *nact, *nslots, *active, *cnt, *list, *expo, *idx;
+  float *w, *gs, *rms;
+  unsigned *sel, *base, *tmask;
+  int slots;
+  __device__ Meta(uint8_t *mem, int ntok, int topk) {
+    slots = ntok * topk + 1;
+    int *i = reinterpret_cast<int *>(mem);
+    nact = i;
+    nslots = i + 1;
+    active = i + 2;
+    cnt = active + slots;
+    list = cnt + slots;
+    w = reinterpret_cast<float *>(list + slots * ntok);
+    gs = w + ntok * topk;
+    expo = reinterpret_cast<int *>(gs + ntok);
+    rms = reinterpret_cast<float *>(expo + ntok * (topk + 1));
+    idx = reinterpret_cast<int *>(rms + ntok);
+    sel = reinterpret_cast<unsigned *>(idx + ntok * topk);
+    base = sel + 32;
+    tmask = base + 32;
   }
-  __syncthreads();
-  if (!s_last) return;
+  // the bit sets route_tokens() accumulates into; before a __syncthreads()
+  __device__ void clear(int tid, int nthr) {
+    for (int i = tid; i < 32; i += nthr) sel[i] = 0u;
+    for (int i = tid; i < slots; i += nthr) tmask[i] = 0u;
+  }
+};
 
-  // softmax + top-K: warp per token
-  for (int t = warp; t < a.ntok; t += kRouterThreads / 32) {
-    const float *lt = a.logits + static_cast<int64_t>(t) * a.E;
-    // one round of independent loads, then everything from registers
-    float lv[kMaxExperts / 32];
+// ints/floats of Meta
+inline int meta_words(int ntok, int topk) {
+  const int slots = ntok * topk + 1;
+  return 2 + 2 * slots + slots * ntok + ntok * topk + ntok + ntok * (topk + 1) + ntok + ntok * topk + 64 + slots;
+}
+
+// Integer key with the order of the logits: larger logit, larger key; -0
+// and +0 equal.
+__device__ __forceinline__ unsigned order_key(float f) {
+  const unsigned b = __float_as_uint(__fadd_rn(f, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Softmax + top-K of one token's logits lt[0..E) by one warp (NPL*32 >= E;
+// lane l holds experts l, l+32, ...).  Order: larger logit first, equal
+// logits in ascending expert order.  Each round is one warp max over the
+// lanes' best remaining keys and one warp min over the expert ids holding
+// that key; only the winning lane rescans its entries.  Writes the experts
+// to idx[0..topk) and their softmax probabilities, renormalised over the
+// selection when `norm`, to w[0..topk).
+template <int NPL>
+__device__ __noinline__ void topk_token(const float *lt, int E, int topk, int norm, int lane, int *idx, float *w) {
+  float v[NPL];
+  unsigned key[NPL];
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) lv[i] = (lane + 32 * i < a.E) ? __ldcg(lt + lane + 32 * i) : -INFINITY;
-    float lmax = -INFINITY;
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < E ? __ldcg(lt + e) : 0.0f;
+    key[i] = e < E ? max(order_key(v[i]), 1u) : 0u;  // 0: absent or taken
+  }
+  unsigned bk = 0u;
+  int bi = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) lmax = fmaxf(lmax, lv[i]);
-    lmax = warp_max_all(lmax);
-    float den = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i)
-      if (lane + 32 * i < a.E) den += expf(lv[i] - lmax);
-    den = warp_sum_xor<32>(den);
-    float sel_sum = 0.0f;
-    int prev_e = -1;
-    float prev_v = INFINITY;
-    float pk[kMaxTopk];
-    int ek[kMaxTopk];
-    for (int k = 0; k < a.topk; ++k) {
-      // best remaining: largest value, then lowest index, strictly after (prev_v, prev_e)
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        const float v = lv[i];
-        const bool after = v < prev_v || (v == prev_v && e > prev_e);
-        if (e < a.E && after && (v > bv || (v == bv && e < be))) {
-          bv = v;
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int e2 = __shfl_xor_sync(0xffffffffu, be, o);
-        if (v2 > bv || (v2 == bv && e2 < be)) {
-          bv = v2;
-          be = e2;
-        }
-      }
-      prev_v = bv;
-      prev_e = be;
-      const float p = __fdiv_rn(expf(bv - lmax), den);
-      if (k < kMaxTopk) {
-        pk[k] = p;
-        ek[k] = be;
-      }
-      sel_sum += p;
+  for (int i = 0; i < NPL; ++i)
+    if (key[i] > bk) {
+      bk = key[i];
+      bi = i;
     }
+  float lmax = 0.0f, den = 0.0f, sel_sum = 0.0f;
+  for (int k = 0; k < topk; ++k) {
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
+    const unsigned e = __reduce_min_sync(0xffffffffu, bk == kmax ? static_cast<unsigned>(bi * 32 + lane) : 0xffffffffu);
+    const float lv = key_value(kmax);
+    if (k == 0) {
+      lmax = lv;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (i * 32 + lane < E) den += expf(v[i] - lmax);
+      den = warp_sum_xor<32>(den);
+    }
+    const float p = __fdiv_rn(expf(lv - lmax), den);
+    sel_sum += p;
     if (lane == 0) {
-      for (int k = 0; k < a.topk; ++k) {
-        const float wk = a.norm_topk ? __fdiv_rn(pk[k], sel_sum) : pk[k];
-        a.idx[t * a.topk + k] = ek[k];
-        s_idx[t * a.topk + k] = ek[k];
-        a.w[t * a.topk + k] = wk;
-        if (a.out_idx) a.out_idx[t * a.topk + k] = ek[k];
-        if (a.out_w) a.out_w[t * a.topk + k] = wk;
-      }
+      idx[k] = static_cast<int>(e);
+      w[k] = p;
     }
-  }
-  __syncthreads();
-
-  // group tokens by expert: slots in ascending expert order (block scan)
-  __shared__ int s_wsum[kRouterThreads / 32];
-  const int nsel = a.ntok * a.topk;
-  for (int e = tid; e < a.E; e += kRouterThreads) s_slot_of[e] = 0;
-  __syncthreads();
-  for (int i = tid; i < nsel; i += kRouterThreads) s_slot_of[s_idx[i]] = 1;
-  __syncthreads();
-  constexpr int EPT = kMaxExperts / kRouterThreads;  // experts per thread
-  int flags = 0, cntl = 0;
+    if (lane == static_cast<int>(e & 31u)) {
+      const int taken = bi;
+      bk = 0u;
 #pragma unroll
-  for (int q = 0; q < EPT; ++q) {
-    const int e = tid * EPT + q;
-    if (e < a.E && s_slot_of[e]) {
-      flags |= 1 << q;
-      ++cntl;
-    }
-  }
-  int incl = cntl;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
-  int woff = 0, total = 0;
-  for (int w = 0; w < kRouterThreads / 32; ++w) {
-    if (w < warp) woff += s_wsum[w];
-    total += s_wsum[w];
-  }
-  __syncthreads();
-  int pos = woff + incl - cntl;
-#pragma unroll
-  for (int q = 0; q < EPT; ++q) {
-    const int e = tid * EPT + q;
-    if (e < a.E) {
-      if (flags & (1 << q)) {
-        a.active[pos] = e;
-        s_slot_of[e] = pos++;
-      } else {
-        s_slot_of[e] = -1;
-      }
-    }
-  }
-  if (tid == 0) {
-    a.meta[0] = total;
-    a.meta[1] = total + (a.has_shared ? 1 : 0);
-  }
-  __syncthreads();
-  const int nact = total;
-  for (int s = tid; s < nact + (a.has_shared ? 1 : 0); s += kRouterThreads) {
-    int c = 0;
-    for (int t = 0; t < a.ntok; ++t) {
-      for (int k = 0; k < a.topk; ++k) {
-        if (s < nact ? s_slot_of[s_idx[t * a.topk + k]] == s : k == 0) {
-          a.list[s * a.ntok + c++] = t * 32 + (s < nact ? k : a.topk);
+      for (int i = 0; i < NPL; ++i) {
+        if (i == taken) key[i] = 0u;
+        if (key[i] > bk) {
+          bk = key[i];
+          bi = i;
         }
       }
     }
-    a.cnt[s] = c;
   }
-  for (int i = tid; i < a.ntok * (a.topk + 1); i += kRouterThreads) a.hmax[i] = 0u;
-  if (tid == 0) *a.counter = 0u;
+  __syncwarp();
+  if (norm && lane < topk) w[lane] = __fdiv_rn(w[lane], sel_sum);
+  __syncwarp();
+}
+
+// Routing of all tokens inside one CTA; every thread of the CTA calls it,
+// after Meta::clear() and a __syncthreads().  Softmax + top-K per token
+// (warp per token), then grouping: the distinct selected experts in
+// ascending order become slots 0..nact-1 and the shared expert (if any) slot
+// nact; list[s*ntok + j] holds the entries t*32 + k of slot s in ascending
+// token order.  `publish`: also write the routing to global memory (the
+// caller's top-K outputs and what the down kernel reads).
+__device__ void route_tokens(const MoeArgs &a, Meta &m, bool publish) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthr = blockDim.x, nwarps = nthr >> 5;
+  const int npl = (a.E + 31) / 32;
+  for (int t = warp; t < a.ntok; t += nwarps) {
+    const float *lt = a.logits + static_cast<int64_t>(t) * a.E;
+    int *ix = m.idx + t * a.topk;
+    float *wt = m.w + t * a.topk;
+    if (npl <= 1) topk_token<1>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
+    else if (npl <= 2) topk_token<2>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
+    else if (npl <= 4) topk_token<4>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
+    else if (npl <= 8) topk_token<8>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
+    else if (npl <= 16) topk_token<16>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
+    else topk_token<32>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
+    if (lane < a.topk) {
+      const int e = ix[lane];
+      atomicOr(&m.sel[e >> 5], 1u << (e & 31));
+      if (publish) {
+        const int o = t * a.topk + lane;
+        a.idx[o] = e;
+        a.w[o] = wt[lane];
+        if (a.out_idx) a.out_idx[o] = e;
+        if (a.out_w) a.out_w[o] = wt[lane];
+      }
+    }
+  }
+  for (int t = tid; t < a.ntok; t += nthr) {
+    m.gs[t] = a.gvec ? __ldcg(a.gshared + t) : 1.0f;
+    m.rms[t] = __ldcg(a.xstat + 2 * t + 1);
+    m.expo[t] = bound_exponent(__ldcg(a.xstat + 2 * t));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // slots: exclusive scan of the per-word counts of selected experts
+    const unsigned word = m.sel[lane];
+    const int c = __popc(word);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    m.base[lane] = static_cast<unsigned>(incl - c);
+    int pos = incl - c;
+    for (unsigned b = word; b; b &= b - 1u) m.active[pos++] = lane * 32 + __ffs(static_cast<int>(b)) - 1;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      *m.nact = total;
+      *m.nslots = total + (a.has_shared ? 1 : 0);
+      if (a.has_shared) m.tmask[total] = (1u << a.ntok) - 1u;
+    }
+  }
+  __syncthreads();
+  const int nsel = a.ntok * a.topk;
+  auto slot_of = [&](int e) {
+    return static_cast<int>(m.base[e >> 5]) + __popc(m.sel[e >> 5] & ((1u << (e & 31)) - 1u));
+  };
+  for (int i = tid; i < nsel; i += nthr) atomicOr(&m.tmask[slot_of(m.idx[i])], 1u << (i / a.topk));
+  __syncthreads();
+  const int nact = *m.nact, nslots = *m.nslots;
+  for (int i = tid; i < nsel; i += nthr) {
+    const int t = i / a.topk, k = i - t * a.topk;
+    const int s = slot_of(m.idx[i]);
+    m.list[s * a.ntok + __popc(m.tmask[s] & ((1u << t) - 1u))] = t * 32 + k;
+  }
+  if (a.has_shared)
+    for (int t = tid; t < a.ntok; t += nthr) m.list[nact * a.ntok + t] = t * 32 + a.topk;
+  for (int s = tid; s < nslots; s += nthr) m.cnt[s] = __popc(m.tmask[s]);
+  __syncthreads();
+  if (publish) {
+    if (tid == 0) {
+      a.meta[0] = nact;
+      a.meta[1] = nslots;
+    }
+    for (int s = tid; s < nslots; s += nthr) {
+      a.active[s] = s < nact ? m.active[s] : -1;
+      a.cnt[s] = m.cnt[s];
+    }
+    for (int i = tid; i < nslots * a.ntok; i += nthr)
+      if (i % a.ntok < m.cnt[i / a.ntok]) a.list[i] = m.list[i];
+  }
+}
+
+// Routing alone, for a call that runs the router stage without the gate/up
+// stage: one CTA computes and publishes what the gate/up kernel would.
+constexpr int kSelectThreads = 256;
+__global__ void __launch_bounds__(kSelectThreads) select_kernel(const MoeArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_sel[];
+  Meta m(smem_sel, a.ntok, a.topk);
+  m.clear(threadIdx.x, blockDim.x);
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
+  route_tokens(a, m, true);
 }
 
 // ------------------------------------------------------------------ engine plan
@@ -353,12 +442,6 @@ int next_pow2(int v) {
   int p = 1;
   while (p < v) p <<= 1;
   return p;
-}
-
-// ints/floats of the routing metadata copy in shared memory
-inline int meta_words(int ntok, int topk) {
-  const int slots = ntok * topk + 1;
-  return 2 + 2 * slots + slots * ntok + ntok * topk + ntok + ntok * (topk + 1) + ntok;
 }
 
 // cols: weights per row; per_row: staged bytes per output row;
@@ -415,49 +498,25 @@ struct EngineArgs {
   uint32_t stage_bytes, bar_off, red_off, meta_off, hs_off, acc_off;
 };
 
-// Shared-memory copy of the routing results (see router_kernel).
-struct Meta {
-  int *nact, *nslots, *active, *cnt, *list, *expo;
-  float *w, *gs, *rms;
-  __device__ Meta(uint8_t *base, int ntok, int topk) {
-    const int slots = ntok * topk + 1;
-    int *i = reinterpret_cast<int *>(base);
-    nact = i;
-    nslots = i + 1;
-    active = i + 2;
-    cnt = active + slots;
-    list = cnt + slots;
-    w = reinterpret_cast<float *>(list + slots * ntok);
-    gs = w + ntok * topk;
-    expo = reinterpret_cast<int *>(gs + ntok);
-    rms = reinterpret_cast<float *>(expo + ntok * (topk + 1));
-  }
-};
-
-// Fill the metadata copy (threads [0, nthr) of the CTA); `down` selects the
-// h exponents, otherwise the x exponents and RMS factors.
-__device__ void load_meta(const MoeArgs &a, Meta &m, int tid, int nthr, bool down) {
-  const int slots = a.ntok * a.topk + 1;
+// Fill the metadata copy from the routing the gate/up kernel published, with
+// the h exponents from the max|h| accumulators (threads [0, nthr) of the CTA).
+__device__ void load_meta(const MoeArgs &a, Meta &m, int tid, int nthr) {
   if (tid == 0) {
     *m.nact = __ldcg(a.meta);
     *m.nslots = __ldcg(a.meta + 1);
   }
-  for (int i = tid; i < slots; i += nthr) {
+  for (int i = tid; i < m.slots; i += nthr) {
     m.active[i] = __ldcg(a.active + i);
     m.cnt[i] = __ldcg(a.cnt + i);
   }
-  for (int i = tid; i < slots * a.ntok; i += nthr) m.list[i] = __ldcg(a.list + i);
+  for (int i = tid; i < m.slots * a.ntok; i += nthr) m.list[i] = __ldcg(a.list + i);
   for (int i = tid; i < a.ntok * a.topk; i += nthr) m.w[i] = __ldcg(a.w + i);
   for (int i = tid; i < a.ntok; i += nthr) {
     m.gs[i] = a.gvec ? __ldcg(a.gshared + i) : 1.0f;
     m.rms[i] = __ldcg(a.xstat + 2 * i + 1);
   }
-  if (down) {
-    for (int i = tid; i < a.ntok * (a.topk + 1); i += nthr)
-      m.expo[i] = bound_exponent(__uint_as_float(__ldcg(a.hmax + i)));
-  } else {
-    for (int i = tid; i < a.ntok; i += nthr) m.expo[i] = bound_exponent(__ldcg(a.xstat + 2 * i));
-  }
+  for (int i = tid; i < a.ntok * (a.topk + 1); i += nthr)
+    m.expo[i] = bound_exponent(__uint_as_float(__ldcg(a.hmax + i)));
 }
 
 // Row reduction of one (unit, entry) for RPG partials: in-warp reduce-scatter,
@@ -546,12 +605,16 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
     }
     fence_mbar_init();
   }
+  Meta m(smem + p.meta_off, a.ntok, a.topk);
+  m.clear(tid, blockDim.x);
   __syncthreads();
   pdl_launch_dependents();
-  pdl_wait();  // routing is produced by the router kernel
+  pdl_wait();  // logits and x statistics come from the router kernel
+  route_tokens(a, m, blockIdx.x == 0);
 
   const int I = a.I;
-  const int64_t total = static_cast<int64_t>(__ldcg(a.meta + 1)) * I;
+  const int nact = *m.nact;
+  const int64_t total = static_cast<int64_t>(*m.nslots) * I;
   const int64_t rb = (static_cast<int64_t>(blockIdx.x) * total) / gridDim.x;
   const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * total) / gridDim.x;
   auto tile_len = [&](int64_t r0) {
@@ -560,16 +623,14 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
   };
 
   if (tid >= nthreads && tid < nthreads + 32) {
-    // producer warp: the expert ids are held by the warp; every tile is
-    // copied by all 32 lanes with 16-byte asynchronous copies
+    // producer warp: every tile is copied by all 32 lanes with 16-byte
+    // asynchronous copies
     const int plane = tid - nthreads;
-    SlotIds ids;
-    ids.load(a, plane);
     int t = 0;
     for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
       const int s = t % p.stages;
       const int slot = static_cast<int>(r0 / I);
-      const int e = ids.get(slot);
+      const int e = slot < nact ? m.active[slot] : -1;
       if (t >= p.stages && !warp_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, t)) {
         // drain: every lane waits for its own copies still in flight
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -589,13 +650,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
     return;
   }
 
-  // consumers and finisher: routing metadata into shared memory
-  Meta m(smem + p.meta_off, a.ntok, a.topk);
   const bool is_fin = tid >= nthreads + 32;
-  const int ctid = is_fin ? nthreads + lane : tid;
-  load_meta(a, m, ctid, nthreads + (has_fin ? 32 : 0), false);
-  named_sync(1, nthreads + (has_fin ? 32 : 0));
-
   if (is_fin) {
     int use = 0, t = 0;
     for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
@@ -612,14 +667,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
         const int E = m.expo[tok];
         const float r = m.rms[tok];
         const int hs = tok * (a.topk + 1) + k;
+        unsigned hm = 0u;
         for (int o = lane; o < nr; o += 32) {
           const int gg = o / RH, kk = o % RH;
           const float gv = unscale(fin_row(rbuf, gg * RPG + kk, wpg), E) * r;
           const float uv = unscale(fin_row(rbuf, gg * RPG + RH + kk, wpg), E) * r;
           const float hv = silu(gv) * uv;
           a.h[static_cast<int64_t>(hs) * I + i0 + o] = hv;
-          atomicMax(a.hmax + hs, __float_as_uint(fabsf(hv)));
+          hm = max(hm, __float_as_uint(fabsf(hv)));
         }
+        hm = __reduce_max_sync(0xffffffffu, hm);
+        if (lane == 0 && hm) atomicMax(a.hmax + hs, hm);
         __syncwarp();
         if (lane == 0) mbar_arrive(&rempty[b]);
       }
@@ -677,17 +735,20 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
       if (!has_fin) {
         const int W = p.tpr < 32 ? p.tpr : 32;
         const float up = __shfl_xor_sync(0xffffffffu, part[0][0], W / 2);
+        const int hs = tok * (a.topk + 1) + k;  // the same entry for the whole warp
+        unsigned hm = 0u;
         if (row_k >= 0 && row_k < RH) {
           const int lr = g * RH + row_k;
           if (lr < nr) {
             const int E = m.expo[tok];
             const float r = m.rms[tok];
             const float hv = silu(unscale(part[0][0], E) * r) * (unscale(up, E) * r);
-            const int hs = tok * (a.topk + 1) + k;
             a.h[static_cast<int64_t>(hs) * I + i0 + lr] = hv;
-            atomicMax(a.hmax + hs, __float_as_uint(fabsf(hv)));
+            hm = __float_as_uint(fabsf(hv));
           }
         }
+        hm = __reduce_max_sync(0xffffffffu, hm);
+        if (lane == 0 && hm) atomicMax(a.hmax + hs, hm);
       }
     }
   }
@@ -763,7 +824,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
   const bool is_fin = tid >= nthreads + 32;
   const int ctid = is_fin ? nthreads + lane : tid;
   const int nthr = nthreads + (has_fin ? 32 : 0);
-  load_meta(a, m, ctid, nthr, true);
+  load_meta(a, m, ctid, nthr);
   const int nblk = I / 32;
   const int nh = a.ntok * (a.topk + 1);
   // staged h: pair i of column c of slot vector hsi at pairs[(hsi*16 + i)*nblk + c]
@@ -1009,7 +1070,6 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   a.y = y;
   a.out_idx = topk_idx;
   a.out_w = topk_w;
-  a.counter = reinterpret_cast<uint32_t *>(ws + L.counter);
   a.logits = o.logits_out ? o.logits_out : reinterpret_cast<float *>(ws + L.logits);
   a.xstat = reinterpret_cast<float *>(ws + L.xstat);
   a.gshared = reinterpret_cast<float *>(ws + L.gshared);
@@ -1026,12 +1086,19 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const int stages = (o.stages & 7) ? (o.stages & 7) : 7;
   cudaError_t e = cudaSuccess;
   if (stages & EPQ_MOE_ROUTE) {
-    // The ticket counter starts at zero in a fresh (zero-filled) workspace and
-    // the router's last CTA puts it back to zero for the next call.
     const int nrows = E + (a.gvec ? 1 : 0);
-    const unsigned rgrid = static_cast<unsigned>(std::max(1, std::min(2 * dev.sm_count, (nrows + kRouterWarps - 1) / kRouterWarps)));
-    router_kernel<<<rgrid, kRouterThreads, 0, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    const unsigned rgrid = static_cast<unsigned>(
+        std::max(1, std::min(2 * dev.sm_count, (nrows + kRouterWarps - 1) / kRouterWarps)));
+    if (ntok <= 1) e = launch_pdl(router_kernel<1>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+    else if (ntok <= 4) e = launch_pdl(router_kernel<4>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+    else e = launch_pdl(router_kernel<kMaxTok>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!(stages & EPQ_MOE_GATE_UP) && (topk_idx || topk_w || (stages & EPQ_MOE_DOWN))) {
+      // the gate/up kernel routes for itself; without it, route here when
+      // this call returns the selection or runs the down stage
+      e = launch_pdl(select_kernel, dim3(1), dim3(kSelectThreads), 4u * meta_words(ntok, topk), s, a);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
   }
 
   EnginePlan gp, dp;
@@ -1107,9 +1174,5 @@ extern "C" epq_status epq_moe_forward_noalloc(const epq_router *router, const ep
   void *ws = nullptr;
   const epq_status sp = fixed_scratch_ptr(&ws);
   if (sp != EPQ_OK) return sp;
-  // The array keeps whatever the previous call left; the ticket counter at
-  // its start must read zero when the router starts, so clear it here.
-  const cudaError_t e = cudaMemsetAsync(ws, 0, 16, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e);
   return epq_moe_forward(router, experts, x, ntok, topk, opts, y, topk_idx, topk_w, ws, kFixedScratchBytes, stream);
 }

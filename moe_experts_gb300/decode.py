@@ -88,7 +88,7 @@ class MoEDecoder:
         self.qkv = torch.empty((1, 3 * H), dtype=torch.float32, device=device)
         self.h = torch.empty((1, H), dtype=torch.float32, device=device)
         ws = max(layer.workspace_bytes(1, cfg.topk) for (_, _, layer) in layers)
-        self.ws = torch.zeros(ws, dtype=torch.uint8, device=device)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def token(self, x, out, stream=None, timers=None):
         """x [1, H] (read only) -> out [1, H], the hidden state after the last layer."""
