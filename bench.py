@@ -35,6 +35,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "effective weight GB/s and % of HBM peak for Q4_K dequant-GEMV; decode tok/s"
 NOMINAL_HBM_GBS = 8000.0
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the kernel as it stands; the summary with its command is the
+# named file.  An entry must go when its kernel changes.
+NCU_TRAFFIC = {
+    "moe_gateup": (10_709_888, "profiles/moe_gateup_q4k_full.md"),
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -421,7 +427,9 @@ def run_epq(args):
         ach = W.kernel_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": peak_kind + " copy bandwidth",
-                "traffic": None, "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
+                "traffic": NCU_TRAFFIC[dom][0] if dom in NCU_TRAFFIC else None,
+                "traffic_source": NCU_TRAFFIC[dom][1] if dom in NCU_TRAFFIC else None,
+                "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
                 "bytes_per_launch": W.kernel_bytes[dom],
                 "all_kernels_us": {k: round(v * 1e3, 3) for k, v in kernel_ms.items()}}
     eff_gbs = W.bytes_per_token * (value / ws) / 1e9 if W.unit == "tok/s" else None
