@@ -51,14 +51,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// A waiting thread is suspended until the phase completes or kSuspendNs
+// pass, whichever is first, so waiters do not take issue slots from the
+// warps that work.
+constexpr uint32_t kSuspendNs = 100000;  // 100 us
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -90,8 +95,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       record_error(err, code, where);
       return false;
@@ -121,19 +125,9 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
       : "memory");
 }
 
-// Warp-wide asynchronous copy of `bytes` (a multiple of 16) from global to
-// shared memory in 16-byte pieces, all lanes in parallel; each lane then
-// arms one arrival on `bar` that fires when its own pieces have landed (the
-// barrier must expect 32 arrivals per phase).  For small, scattered tiles
-// this keeps many requests in flight without a single copy engine.
-__device__ __forceinline__ void warp_copy_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, int lane) {
-  const uint32_t d = smem_addr(dst_smem);
-  const char *sp = static_cast<const char *>(src_gmem);
-  for (uint32_t off = 16u * lane; off < bytes; off += 512u)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + off), "l"(sp + off) : "memory");
-}
-__device__ __forceinline__ void warp_copy_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+// Bring the 128-byte line holding `p` into this SM's L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 // Programmatic dependent launch: wait for the preceding kernel's writes /

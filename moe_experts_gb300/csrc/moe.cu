@@ -249,7 +249,7 @@ struct Meta {
 };
 
 // ints/floats of Meta
-inline int meta_words(int ntok, int topk) {
+__host__ __device__ inline int meta_words(int ntok, int topk) {
   const int slots = ntok * topk + 1;
   return 2 + 2 * slots + slots * ntok + ntok * topk + ntok + ntok * (topk + 1) + ntok + ntok * topk + 64 + slots;
 }
@@ -264,104 +264,186 @@ __device__ __forceinline__ float key_value(unsigned k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Softmax + top-K of one token's logits lt[0..E) by one warp (NPL*32 >= E;
-// lane l holds experts l, l+32, ...).  Order: larger logit first, equal
-// logits in ascending expert order.  Each round is one warp max over the
-// lanes' best remaining keys and one warp min over the expert ids holding
-// that key; only the winning lane rescans its entries.  Writes the experts
-// to idx[0..topk) and their softmax probabilities, renormalised over the
-// selection when `norm`, to w[0..topk).
-template <int NPL>
-__device__ __noinline__ void topk_token(const float *lt, int E, int topk, int norm, int lane, int *idx, float *w) {
-  float v[NPL];
-  unsigned key[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = e < E ? __ldcg(lt + e) : 0.0f;
-    key[i] = e < E ? max(order_key(v[i]), 1u) : 0u;  // 0: absent or taken
-  }
-  unsigned bk = 0u;
-  int bi = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (key[i] > bk) {
-      bk = key[i];
-      bi = i;
+// Selection scratch (32-bit words), at least kSelScratchWords: candidates
+// of up to kCandMax (key, expert) pairs, per-chunk softmax statistics and
+// the selected keys.
+constexpr int kCandMax = 2048;
+constexpr int kSelScratchWords = 2 * kCandMax + 2 * kMaxTok * (kMaxExperts / 32) + kMaxTok * kMaxTopk;
+
+// (key, expert) packed so that a larger value comes first: larger key,
+// then lower expert index.
+__device__ __forceinline__ unsigned long long cand_pack(unsigned key, int e) {
+  return (static_cast<unsigned long long>(key) << 32) | (0xffffffffu - static_cast<unsigned>(e));
+}
+
+// Softmax + top-K of every token, by all threads of the CTA (after a
+// __syncthreads), in batches of tokens whose candidates fit kCandMax.
+// Level 1: warp per (token, 32-expert chunk): the chunk's best topk entries
+// in order, by rounds of warp max + ballot (equal keys: lowest lane, i.e.
+// lowest expert, first), and the chunk's softmax statistics (max, sum of
+// exp(l - max)).  Level 2: thread per candidate: its rank among the
+// token's candidates is the count of those that come first; rank < topk
+// places it.  Then warp per token: the softmax denominator from the chunk
+// statistics and the selected probabilities (renormalised when norm_topk).
+// Writes m.idx, m.w (and the caller's outputs when `publish`), m.sel bits.
+__device__ void select_topk(const MoeArgs &a, Meta &m, uint32_t *scratch, bool publish) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthr = blockDim.x, nwarps = nthr >> 5;
+  const int E = a.E, K = a.topk;
+  const int nch = (E + 31) / 32;
+  unsigned long long *cand = reinterpret_cast<unsigned long long *>(scratch);  // [tb][nch][K]
+  float *cmax = reinterpret_cast<float *>(scratch + 2 * kCandMax);             // [tb][nch]
+  float *cden = cmax + kMaxTok * (kMaxExperts / 32);                           // [tb][nch]
+  unsigned *skey = reinterpret_cast<unsigned *>(cden + kMaxTok * (kMaxExperts / 32));  // [tb][K]
+  const int tb = max(1, min(a.ntok, kCandMax / (nch * K)));
+#pragma unroll 1
+  for (int t0 = 0; t0 < a.ntok; t0 += tb) {
+    const int nt = min(tb, a.ntok - t0);
+    // level 1
+#pragma unroll 1
+    for (int job = warp; job < nt * nch; job += nwarps) {
+      const int tl = job / nch, c = job - tl * nch;
+      const int e = c * 32 + lane;
+      const float v = e < E ? __ldcg(a.logits + static_cast<int64_t>(t0 + tl) * E + e) : 0.0f;
+      unsigned key = e < E ? max(order_key(v), 1u) : 0u;  // 0: absent or taken
+      const unsigned k0 = __reduce_max_sync(0xffffffffu, key);
+      const float mc = key_value(k0);
+      float d = e < E ? expf(v - mc) : 0.0f;
+      unsigned long long mine = 0ull;
+#pragma unroll 1
+      for (int k = 0; k < K; ++k) {
+        const unsigned kmax = k == 0 ? k0 : __reduce_max_sync(0xffffffffu, key);
+        const int w = __ffs(__ballot_sync(0xffffffffu, key == kmax && kmax != 0u)) - 1;
+        if (lane == k) mine = w >= 0 ? cand_pack(kmax, c * 32 + w) : 0ull;
+        if (lane == w) key = 0u;
+      }
+      d = warp_sum_xor<32>(d);
+      if (lane < K) cand[job * K + lane] = mine;
+      if (lane == 0) {
+        cmax[job] = mc;
+        cden[job] = d;
+      }
     }
-  float lmax = 0.0f, den = 0.0f, sel_sum = 0.0f;
-  for (int k = 0; k < topk; ++k) {
-    const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
-    const unsigned e = __reduce_min_sync(0xffffffffu, bk == kmax ? static_cast<unsigned>(bi * 32 + lane) : 0xffffffffu);
-    const float lv = key_value(kmax);
-    if (k == 0) {
-      lmax = lv;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (i * 32 + lane < E) den += expf(v[i] - lmax);
+    __syncthreads();
+    // level 2
+    const int C = nch * K;
+#pragma unroll 1
+    for (int i = tid; i < nt * C; i += nthr) {
+      const int tl = i / C;
+      const unsigned long long ci = cand[i];
+      if (ci == 0ull) continue;
+      const unsigned long long *ct = cand + tl * C;  // 16-byte aligned when C is even
+      int r = 0, j = 0;
+      if ((C & 1) == 0) {
+        const ulonglong2 *c2 = reinterpret_cast<const ulonglong2 *>(ct);
+#pragma unroll 4
+        for (; j < C / 2; ++j) {
+          const ulonglong2 v = c2[j];
+          r += (v.x > ci ? 1 : 0) + (v.y > ci ? 1 : 0);
+        }
+        j = C;
+      }
+#pragma unroll 4
+      for (; j < C; ++j) r += ct[j] > ci ? 1 : 0;
+      if (r < K) {
+        m.idx[(t0 + tl) * K + r] = static_cast<int>(0xffffffffu - static_cast<unsigned>(ci));
+        skey[tl * K + r] = static_cast<unsigned>(ci >> 32);
+      }
+    }
+    __syncthreads();
+    // softmax: warp per token
+#pragma unroll 1
+    for (int tl = nwarps - 1 - warp; tl < nt; tl += nwarps) {
+      const int t = t0 + tl;
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = lane; c < nch; c += 32) mx = fmaxf(mx, cmax[tl * nch + c]);
+      mx = warp_max_all(mx);
+      float den = 0.0f;
+#pragma unroll 1
+      for (int c = lane; c < nch; c += 32) den += cden[tl * nch + c] * expf(cmax[tl * nch + c] - mx);
       den = warp_sum_xor<32>(den);
-    }
-    const float p = __fdiv_rn(expf(lv - lmax), den);
-    sel_sum += p;
-    if (lane == 0) {
-      idx[k] = static_cast<int>(e);
-      w[k] = p;
-    }
-    if (lane == static_cast<int>(e & 31u)) {
-      const int taken = bi;
-      bk = 0u;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        if (i == taken) key[i] = 0u;
-        if (key[i] > bk) {
-          bk = key[i];
-          bi = i;
+      const float p = lane < K ? __fdiv_rn(expf(key_value(skey[tl * K + lane]) - mx), den) : 0.0f;
+      const float sel_sum = warp_sum_xor<32>(p);
+      if (lane < K) {
+        const float wk = a.norm_topk ? __fdiv_rn(p, sel_sum) : p;
+        const int e = m.idx[t * K + lane];
+        m.w[t * K + lane] = wk;
+        atomicOr(&m.sel[e >> 5], 1u << (e & 31));
+        if (publish) {
+          const int o = t * K + lane;
+          a.idx[o] = e;
+          a.w[o] = wk;
+          if (a.out_idx) a.out_idx[o] = e;
+          if (a.out_w) a.out_w[o] = wk;
         }
       }
     }
+    if (t0 + tb < a.ntok) __syncthreads();  // the next batch reuses the scratch
   }
-  __syncwarp();
-  if (norm && lane < topk) w[lane] = __fdiv_rn(w[lane], sel_sum);
-  __syncwarp();
+}
+
+// What the down kernel reads of the routing, from the CTA's copy.
+__device__ void publish_routing(const MoeArgs &a, const Meta &m, int tid, int nthr) {
+  const int nact = *m.nact, nslots = *m.nslots;
+  if (tid == 0) {
+    a.meta[0] = nact;
+    a.meta[1] = nslots;
+  }
+#pragma unroll 1
+  for (int s = tid; s < nslots; s += nthr) {
+    a.active[s] = s < nact ? m.active[s] : -1;
+    a.cnt[s] = m.cnt[s];
+  }
+#pragma unroll 1
+  for (int i = tid; i < nslots * a.ntok; i += nthr)
+    if (i % a.ntok < m.cnt[i / a.ntok]) a.list[i] = m.list[i];
 }
 
 // Routing of all tokens inside one CTA; every thread of the CTA calls it,
-// after Meta::clear() and a __syncthreads().  Softmax + top-K per token
-// (warp per token), then grouping: the distinct selected experts in
+// after Meta::clear() and a __syncthreads(); `scratch` holds
+// kSelScratchWords.  Softmax + top-K of every token (select_topk), then
+// grouping: the distinct selected experts in
 // ascending order become slots 0..nact-1 and the shared expert (if any) slot
 // nact; list[s*ntok + j] holds the entries t*32 + k of slot s in ascending
 // token order.  `publish`: also write the routing to global memory (the
 // caller's top-K outputs and what the down kernel reads).
-__device__ void route_tokens(const MoeArgs &a, Meta &m, bool publish) {
+__device__ void route_tokens(const MoeArgs &a, Meta &m, uint32_t *scratch, bool publish) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarps = nthr >> 5;
-  const int npl = (a.E + 31) / 32;
-  for (int t = warp; t < a.ntok; t += nwarps) {
-    const float *lt = a.logits + static_cast<int64_t>(t) * a.E;
-    int *ix = m.idx + t * a.topk;
-    float *wt = m.w + t * a.topk;
-    if (npl <= 1) topk_token<1>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
-    else if (npl <= 2) topk_token<2>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
-    else if (npl <= 4) topk_token<4>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
-    else if (npl <= 8) topk_token<8>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
-    else if (npl <= 16) topk_token<16>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
-    else topk_token<32>(lt, a.E, a.topk, a.norm_topk, lane, ix, wt);
-    if (lane < a.topk) {
-      const int e = ix[lane];
-      atomicOr(&m.sel[e >> 5], 1u << (e & 31));
-      if (publish) {
-        const int o = t * a.topk + lane;
-        a.idx[o] = e;
-        a.w[o] = wt[lane];
-        if (a.out_idx) a.out_idx[o] = e;
-        if (a.out_w) a.out_w[o] = wt[lane];
-      }
-    }
-  }
+  select_topk(a, m, scratch, publish);
+  const int rwarp = nwarps - 1 - warp;  // rwarp 0 ran token 0's softmax
+#pragma unroll 1
   for (int t = tid; t < a.ntok; t += nthr) {
     m.gs[t] = a.gvec ? __ldcg(a.gshared + t) : 1.0f;
     m.rms[t] = __ldcg(a.xstat + 2 * t + 1);
     m.expo[t] = bound_exponent(__ldcg(a.xstat + 2 * t));
+  }
+  if (a.ntok == 1) {
+    // one token: its topk distinct experts are the slots, in ascending
+    // order (rank among the chosen), one entry each
+    if (rwarp == 0) {  // m.w of token 0 is this warp's own write
+      const int e = lane < a.topk ? m.idx[lane] : 0x7fffffff;
+      int rank = 0;
+#pragma unroll 1
+      for (int j = 0; j < a.topk; ++j) rank += __shfl_sync(0xffffffffu, e, j) < e ? 1 : 0;
+      if (lane < a.topk) {
+        m.active[rank] = e;
+        m.list[rank] = lane;
+        m.cnt[rank] = 1;
+      }
+      if (lane == 0) {
+        *m.nact = a.topk;
+        *m.nslots = a.topk + (a.has_shared ? 1 : 0);
+        if (a.has_shared) {
+          m.list[a.topk] = a.topk;
+          m.cnt[a.topk] = 1;
+        }
+      }
+    }
+    __syncthreads();
+    if (publish) publish_routing(a, m, tid, nthr);
+    return;
   }
   __syncthreads();
   if (warp == 0) {
@@ -376,6 +458,7 @@ __device__ void route_tokens(const MoeArgs &a, Meta &m, bool publish) {
     }
     m.base[lane] = static_cast<unsigned>(incl - c);
     int pos = incl - c;
+#pragma unroll 1
     for (unsigned b = word; b; b &= b - 1u) m.active[pos++] = lane * 32 + __ffs(static_cast<int>(b)) - 1;
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
@@ -389,30 +472,23 @@ __device__ void route_tokens(const MoeArgs &a, Meta &m, bool publish) {
   auto slot_of = [&](int e) {
     return static_cast<int>(m.base[e >> 5]) + __popc(m.sel[e >> 5] & ((1u << (e & 31)) - 1u));
   };
+#pragma unroll 1
   for (int i = tid; i < nsel; i += nthr) atomicOr(&m.tmask[slot_of(m.idx[i])], 1u << (i / a.topk));
   __syncthreads();
   const int nact = *m.nact, nslots = *m.nslots;
+#pragma unroll 1
   for (int i = tid; i < nsel; i += nthr) {
     const int t = i / a.topk, k = i - t * a.topk;
     const int s = slot_of(m.idx[i]);
     m.list[s * a.ntok + __popc(m.tmask[s] & ((1u << t) - 1u))] = t * 32 + k;
   }
   if (a.has_shared)
+#pragma unroll 1
     for (int t = tid; t < a.ntok; t += nthr) m.list[nact * a.ntok + t] = t * 32 + a.topk;
+#pragma unroll 1
   for (int s = tid; s < nslots; s += nthr) m.cnt[s] = __popc(m.tmask[s]);
   __syncthreads();
-  if (publish) {
-    if (tid == 0) {
-      a.meta[0] = nact;
-      a.meta[1] = nslots;
-    }
-    for (int s = tid; s < nslots; s += nthr) {
-      a.active[s] = s < nact ? m.active[s] : -1;
-      a.cnt[s] = m.cnt[s];
-    }
-    for (int i = tid; i < nslots * a.ntok; i += nthr)
-      if (i % a.ntok < m.cnt[i / a.ntok]) a.list[i] = m.list[i];
-  }
+  if (publish) publish_routing(a, m, tid, nthr);
 }
 
 // Routing alone, for a call that runs the router stage without the gate/up
@@ -421,11 +497,12 @@ constexpr int kSelectThreads = 256;
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(const MoeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_sel[];
   Meta m(smem_sel, a.ntok, a.topk);
+  uint32_t *scratch = reinterpret_cast<uint32_t *>(smem_sel + ((4u * meta_words(a.ntok, a.topk) + 15u) & ~15u));
   m.clear(threadIdx.x, blockDim.x);
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
-  route_tokens(a, m, true);
+  route_tokens(a, m, scratch, true);
 }
 
 // ------------------------------------------------------------------ engine plan
@@ -444,32 +521,42 @@ int next_pow2(int v) {
   return p;
 }
 
-// cols: weights per row; per_row: staged bytes per output row;
-// rows_hint: output rows a CTA is expected to own (keeps >= 2 tiles).
+// largest down RPG the per-token accumulators allow (RPG * NT <= 32)
+inline int down_max_rpg(int ntok) { return ntok <= 4 ? 8 : 2; }
+
+constexpr int64_t kMoeTileBytes = 96 * 1024;  // a tile may hold all of a CTA's decode-sized share
+
+// cols: weights per row; per_row: staged bytes per output row; rows_hint:
+// output rows a CTA is expected to own (the tile grows until it covers
+// them, within kMoeTileBytes).  Down: a thread takes every tpr-th column
+// block (tpr <= 32) and RPG is bounded by its per-token accumulators.
 bool engine_plan(int cols, int64_t per_row, bool swiglu, int64_t rows_hint, int ntok, int topk, int I_for_h,
                  bool down, const DeviceInfo &dev, EnginePlan *pl) {
   const int nblk = cols / 32;
-  pl->tpr = nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32;
+  pl->tpr = down ? std::min(32, std::max(8, next_pow2(nblk)))
+                 : (nblk <= 32 ? std::max(8, next_pow2(nblk)) : ((nblk + 31) / 32) * 32);
   if (pl->tpr > kMaxConsumers) return false;
   pl->groups = std::max(1, kMaxConsumers / pl->tpr);
-  const int rmax = std::min(8, std::min(pl->tpr, 32));
+  const int rmax = down ? std::min(8, down_max_rpg(ntok)) : std::min(8, std::min(pl->tpr, 32));
   auto tile_rows_of = [&](int r) { return static_cast<int64_t>(pl->groups) * (swiglu ? r / 2 : r); };
+  const int64_t tile_cap = std::max<int64_t>(tune_tile_bytes(), kMoeTileBytes);
   int rpg = swiglu ? 2 : 1;
-  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= tune_tile_bytes() &&
+  while (rpg * 2 <= rmax && tile_rows_of(rpg * 2) * per_row <= tile_cap &&
          tile_rows_of(rpg * 2) <= std::max<int64_t>(rows_hint, tile_rows_of(rpg)))
     rpg *= 2;
   pl->rpg = rpg;
   pl->tile_rows = static_cast<int>(tile_rows_of(rpg));
   pl->stage_bytes = static_cast<uint32_t>((pl->tile_rows * per_row + 15) & ~int64_t(15));
   const int wpg = pl->tpr > 32 ? pl->tpr / 32 : 1;
-  const uint32_t red_bytes = 4u * kRedRing * pl->groups * rpg * wpg;
+  const uint32_t red_bytes = down ? 0u : 4u * kRedRing * pl->groups * rpg * wpg;
   const uint32_t meta_bytes = 4u * meta_words(ntok, topk);
   const int64_t hbytes = 4ll * ntok * (topk + 1) * I_for_h;
   pl->stage_h = down && hbytes <= kHSmemMax;
   // staged h: the scaled values plus one scaled column sum per 32 values
   const uint32_t hs_bytes = pl->stage_h ? static_cast<uint32_t>(hbytes + hbytes / 32) : 0u;
-  const uint32_t acc_bytes = down ? 4u * ntok * pl->tile_rows : 0u;
-  pl->stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(8, tune_ring_bytes() / pl->stage_bytes)));
+  const uint32_t acc_bytes = 0u;
+  pl->stages = static_cast<int>(
+      std::max<int64_t>(2, std::min<int64_t>(down ? 16 : 8, tune_ring_bytes() / pl->stage_bytes)));
   for (;;) {
     uint32_t o = pl->stages * pl->stage_bytes + 16;
     o = (o + 15) & ~15u;
@@ -492,6 +579,39 @@ bool engine_plan(int cols, int64_t per_row, bool swiglu, int64_t rows_hint, int 
   return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
 }
 
+// One-shot down form (down_flat_kernel): every slot's rows of a CTA staged
+// at once.  Returns false when the shapes need the pipelined form.
+bool flat_down_plan(int I, int64_t row_bytes, int H, unsigned grid, int max_slots, int ntok, int topk,
+                    const DeviceInfo &dev, EnginePlan *pl) {
+  if (ntok > 4) return false;
+  const int nblk = I / 32;
+  const int64_t hbytes = 4ll * ntok * (topk + 1) * I;
+  if (hbytes > kHSmemMax) return false;
+  pl->tpr = std::min(32, std::max(8, next_pow2(nblk)));
+  pl->groups = kMaxConsumers / pl->tpr;
+  pl->rpg = 1;
+  pl->tile_rows = static_cast<int>((H + grid - 1) / grid);
+  pl->stage_bytes = static_cast<uint32_t>((pl->tile_rows * row_bytes + 15) & ~int64_t(15));
+  pl->stages = max_slots;
+  pl->stage_h = 1;
+  const int nt = ntok <= 1 ? 1 : 4;
+  uint32_t o = static_cast<uint32_t>(max_slots) * pl->stage_bytes;
+  o = (o + 15) & ~15u;
+  pl->bar_off = o;
+  o += 16;
+  pl->red_off = o;
+  pl->meta_off = o;
+  o += 4u * meta_words(ntok, topk);
+  o = (o + 15) & ~15u;
+  pl->hs_off = o;
+  o += static_cast<uint32_t>(hbytes + hbytes / 32);
+  o = (o + 15) & ~15u;
+  pl->acc_off = o;
+  o += 4u * max_slots * pl->tile_rows * nt;
+  pl->smem = (o + 15) & ~15u;
+  return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
+}
+
 struct EngineArgs {
   MoeArgs a;
   int tpr, groups, tile_rows, stages, stage_h;
@@ -505,16 +625,21 @@ __device__ void load_meta(const MoeArgs &a, Meta &m, int tid, int nthr) {
     *m.nact = __ldcg(a.meta);
     *m.nslots = __ldcg(a.meta + 1);
   }
+#pragma unroll 1
   for (int i = tid; i < m.slots; i += nthr) {
     m.active[i] = __ldcg(a.active + i);
     m.cnt[i] = __ldcg(a.cnt + i);
   }
+#pragma unroll 1
   for (int i = tid; i < m.slots * a.ntok; i += nthr) m.list[i] = __ldcg(a.list + i);
+#pragma unroll 1
   for (int i = tid; i < a.ntok * a.topk; i += nthr) m.w[i] = __ldcg(a.w + i);
+#pragma unroll 1
   for (int i = tid; i < a.ntok; i += nthr) {
     m.gs[i] = a.gvec ? __ldcg(a.gshared + i) : 1.0f;
     m.rms[i] = __ldcg(a.xstat + 2 * i + 1);
   }
+#pragma unroll 1
   for (int i = tid; i < a.ntok * (a.topk + 1); i += nthr)
     m.expo[i] = bound_exponent(__uint_as_float(__ldcg(a.hmax + i)));
 }
@@ -596,7 +721,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 32);  // one arrival per producer lane (warp_copy_arrive)
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], nwarps);
     }
     for (int b = 0; b < kRedRing; ++b) {
@@ -610,7 +735,19 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();  // logits and x statistics come from the router kernel
-  route_tokens(a, m, blockIdx.x == 0);
+
+  // consumer coordinates (the x column is loaded once the routing is done)
+  const int g = tid / p.tpr, c = tid % p.tpr;
+  const int nblk = a.H / 32;
+  const bool active = tid < nthreads && c < nblk;
+  ColConst<FMT> cc;
+  cc.init(active ? c : 0);
+  XCol<1> xc;
+  float xs[1] = {0.0f};
+  int cur_t = -1;
+  if (active && g == 0)  // token 0's x lines, into L1 while the routing runs
+    prefetch_l1(a.x + 32 * c);
+  route_tokens(a, m, reinterpret_cast<uint32_t *>(smem), blockIdx.x == 0);  // the ring is free until routed
 
   const int I = a.I;
   const int nact = *m.nact;
@@ -623,30 +760,35 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
   };
 
   if (tid >= nthreads && tid < nthreads + 32) {
-    // producer warp: every tile is copied by all 32 lanes with 16-byte
-    // asynchronous copies
-    const int plane = tid - nthreads;
+    // producer: one thread issues two bulk copies per tile (gate rows, up rows)
+    if (tid != nthreads) return;
+    int issued = 0;
+    bool ok = true;
     int t = 0;
     for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
       const int s = t % p.stages;
       const int slot = static_cast<int>(r0 / I);
       const int e = slot < nact ? m.active[slot] : -1;
-      if (t >= p.stages && !warp_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, t)) {
-        // drain: every lane waits for its own copies still in flight
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        return;
+      if (t >= p.stages && !mbar_wait(&empty[s], ((t / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, t)) {
+        ok = false;
+        break;
       }
       const int nr = tile_len(r0);
       const int i0 = static_cast<int>(r0 % I);
       const uint8_t *base = e >= 0 ? a.gate_up + static_cast<int64_t>(e) * a.gu_stride : a.sh_gate_up;
       const uint32_t bytes = static_cast<uint32_t>(nr * a.gu_row_bytes);
       uint8_t *dst = smem + static_cast<uint32_t>(s) * p.stage_bytes;
-      warp_copy_g2s(dst, base + static_cast<int64_t>(i0) * a.gu_row_bytes, bytes, plane);
-      warp_copy_g2s(dst + p.tile_rows * a.gu_row_bytes, base + static_cast<int64_t>(I + i0) * a.gu_row_bytes, bytes,
-                    plane);
-      warp_copy_arrive(&full[s]);
+      mbar_arrive_expect_tx(&full[s], 2 * bytes);
+      bulk_g2s(dst, base + static_cast<int64_t>(i0) * a.gu_row_bytes, bytes, &full[s]);
+      bulk_g2s(dst + p.tile_rows * a.gu_row_bytes, base + static_cast<int64_t>(I + i0) * a.gu_row_bytes, bytes,
+               &full[s]);
+      ++issued;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok) {
+      // drain: wait (bounded) for every copy still in flight before leaving
+      for (int u = max(0, issued - p.stages); u < issued; ++u)
+        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT, u);
+    }
     return;
   }
 
@@ -685,15 +827,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
     return;
   }
 
-  const int g = tid / p.tpr, c = tid % p.tpr;
-  const int nblk = a.H / 32;
-  const bool active = c < nblk;
-  ColConst<FMT> cc;
-  cc.init(active ? c : 0);
   float xr[32];
-  XCol<1> xc;
-  float xs[1] = {0.0f};
-  int cur_t = -1;
   int use = 0, t = 0;
   for (int64_t r0 = rb; r0 < re; r0 += tile_len(r0), ++t) {
     const int s = t % p.stages;
@@ -755,93 +889,103 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
 }
 
 // ------------------------------------------------------------------ 3. down + combine
-template <int FMT, int RPG>
-__global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const EngineArgs p) {
+// Rows of y are split over the CTAs.  A unit is the CTA's rows (one tile of
+// them) of one slot's down matrix; the units of a tile are staged slot by
+// slot.  Row group g owns tile rows g*RPG .. g*RPG+RPG-1 for every slot: its
+// threads accumulate w * (partial dot) per token in registers across all
+// slots and entries, and the group reduces once per tile, when the tile's
+// last slot is in, to write y = x + sum.  NT >= ntok.
+template <int FMT, int RPG, int NT>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_kernel(const EngineArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const MoeArgs &a = p.a;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
   uint64_t *empty = full + p.stages;
-  uint64_t *rfull = empty + p.stages;
-  uint64_t *rempty = rfull + kRedRing;
-  float *red = reinterpret_cast<float *>(smem + p.red_off);
   float *hs_smem = reinterpret_cast<float *>(smem + p.hs_off);
-  float *acc = reinterpret_cast<float *>(smem + p.acc_off);  // [ntok][tile_rows]
   const int nthreads = p.groups * p.tpr;
-  const int nwarps = nthreads / 32;
-  const bool has_fin = p.tpr > 32;
-  const int wpg = has_fin ? p.tpr / 32 : 1;
   const int tid = threadIdx.x, lane = tid & 31;
-
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 32);  // one arrival per producer lane (warp_copy_arrive)
-      mbar_init(&empty[s], nwarps);
-    }
-    for (int b = 0; b < kRedRing; ++b) {
-      mbar_init(&rfull[b], nwarps);
-      mbar_init(&rempty[b], 1);
-    }
-    fence_mbar_init();
-  }
-  for (int i = tid; i < a.ntok * p.tile_rows; i += blockDim.x) acc[i] = 0.0f;
-  __syncthreads();
-  pdl_launch_dependents();
-  pdl_wait();  // h, routing and hmax come from the previous kernels
-
   const int H = a.H, I = a.I;
   const int64_t rb = (static_cast<int64_t>(blockIdx.x) * H) / gridDim.x;
   const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * H) / gridDim.x;
   const int ntiles = static_cast<int>((re - rb + p.tile_rows - 1) / p.tile_rows);
+  // warps whose groups own rows of the first (largest) tile do the units;
+  // the others only help stage h
+  const int nr0 = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - rb));
+  const int work_groups = min(p.groups, (nr0 + RPG - 1) / RPG);
+  const int work_warps = (work_groups * p.tpr + 31) / 32;
 
-  if (tid >= nthreads && tid < nthreads + 32) {
-    // producer warp: all 32 lanes copy every unit with 16-byte async copies
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], work_warps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // h, routing and hmax come from the previous kernels
+
+  if (tid >= nthreads) {
+    // producer warp: the expert ids are held by the warp; one lane issues a
+    // bulk copy per unit
     const int plane = tid - nthreads;
     const int nslots = __ldcg(a.meta + 1);
     SlotIds ids;
     ids.load(a, plane);
     const int nunits = ntiles * nslots;
+    int issued = 0;
+    bool ok = true;
     for (int u = 0; u < nunits; ++u) {
       const int s = u % p.stages;
       const int tile = u / nslots, slot = u % nslots;
       const int e = ids.get(slot);
       if (u >= p.stages && !warp_wait(&empty[s], ((u / p.stages) - 1) & 1, a.err, DEVERR_EMPTY_WAIT, u)) {
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        return;
+        ok = false;
+        break;
       }
       const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
       const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
       const uint8_t *base = e >= 0 ? a.down + static_cast<int64_t>(e) * a.dn_stride : a.sh_down;
       const uint32_t bytes = static_cast<uint32_t>(nr * a.dn_row_bytes);
-      warp_copy_g2s(smem + static_cast<uint32_t>(s) * p.stage_bytes, base + r0 * a.dn_row_bytes, bytes, plane);
-      warp_copy_arrive(&full[s]);
+      if (plane == 0) {
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s(smem + static_cast<uint32_t>(s) * p.stage_bytes, base + r0 * a.dn_row_bytes, bytes, &full[s]);
+      }
+      ++issued;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok && plane == 0) {
+      for (int u = max(0, issued - p.stages); u < issued; ++u)
+        mbar_wait(&full[u % p.stages], (u / p.stages) & 1, a.err, DEVERR_DRAIN_WAIT, u);
+    }
     return;
   }
 
-  // consumers and finisher: routing metadata (and all of h) into shared memory
+  // consumers: routing metadata (and all of h) into shared memory
   Meta m(smem + p.meta_off, a.ntok, a.topk);
-  const bool is_fin = tid >= nthreads + 32;
-  const int ctid = is_fin ? nthreads + lane : tid;
-  const int nthr = nthreads + (has_fin ? 32 : 0);
-  load_meta(a, m, ctid, nthr);
   const int nblk = I / 32;
   const int nh = a.ntok * (a.topk + 1);
+  if (p.stage_h) {
+    // the h lines this thread stages below, fetched while the routing loads
+    const int n4 = nh * I / 4;
+    for (int q = tid; q < n4; q += nthreads)
+      if ((q & 7) == 0 || q == tid) prefetch_l1(reinterpret_cast<const float4 *>(a.h) + q);
+  }
+  load_meta(a, m, tid, nthreads);
   // staged h: pair i of column c of slot vector hsi at pairs[(hsi*16 + i)*nblk + c]
   // (neighbouring threads read neighbouring pairs); scaled column sums after.
   f2_t *pairs = reinterpret_cast<f2_t *>(hs_smem);
   float *hsum = hs_smem + static_cast<int64_t>(nh) * I;  // [nh][nblk]
-  named_sync(1, nthr);  // the h exponents are in m.expo
+  named_sync(1, nthreads);  // the h exponents are in m.expo
   if (p.stage_h) {
     // coalesced: thread q takes 4 consecutive floats; 8 consecutive threads
     // hold one 32-float column and reduce its sum with shuffles
     const int n4 = nh * I / 4;
-    for (int q0 = ctid - (ctid & 31); q0 < n4; q0 += nthr) {
-      const int q = q0 + (ctid & 31);
+    for (int q0 = tid - lane; q0 < n4; q0 += nthreads) {
+      const int q = q0 + lane;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       int hsi = 0, col = 0, j = 0;
       if (q < n4) {
-        v = __ldcg(reinterpret_cast<const float4 *>(a.h) + q);
+        v = reinterpret_cast<const float4 *>(a.h)[q];  // L1: prefetched above
         hsi = (4 * q) / I;
         col = ((4 * q) % I) / 32;
         j = (4 * q) & 31;
@@ -860,52 +1004,28 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
         if (j == 0) hsum[hsi * nblk + col] = scale_pow2(sum, -23 - E);
       }
     }
-    named_sync(1, nthr);
+    named_sync(1, nthreads);
   }
   const int nslots = *m.nslots;
   const int nunits = ntiles * nslots;
+  if (tid >= work_warps * 32) return;
 
-  if (is_fin) {
-    int use = 0;
-    for (int u = 0; u < nunits; ++u) {
-      const int tile = u / nslots, slot = u % nslots;
-      const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
-      const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
-      const int ne = m.cnt[slot];
-      for (int j = 0; j < ne; ++j, ++use) {
-        const int b = use % kRedRing;
-        if (!warp_wait(&rfull[b], (use / kRedRing) & 1, a.err, DEVERR_RED_WAIT, use)) return;
-        const float *rbuf = red + b * p.groups * RPG * wpg;
-        const int ent = m.list[slot * a.ntok + j];
-        const int tok = ent >> 5, k = ent & 31;
-        const int E = m.expo[tok * (a.topk + 1) + k];
-        const float wk = k < a.topk ? m.w[tok * a.topk + k] : m.gs[tok];
-        for (int o = lane; o < nr; o += 32) acc[tok * p.tile_rows + o] += wk * unscale(fin_row(rbuf, o, wpg), E);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rempty[b]);
-      }
-      if (slot == nslots - 1) {
-        for (int o = lane; o < nr; o += 32) {
-          for (int tk = 0; tk < a.ntok; ++tk) {
-            const int64_t oi = static_cast<int64_t>(tk) * H + r0 + o;
-            a.y[oi] = a.x[oi] + acc[tk * p.tile_rows + o];
-            acc[tk * p.tile_rows + o] = 0.0f;
-          }
-        }
-      }
-    }
-    return;
-  }
-
+  // thread c of a group takes the column blocks c, c + tpr, ... (tpr <= 32,
+  // so a row's reduction stays inside one warp)
   const int g = tid / p.tpr, c = tid % p.tpr;
   const bool active = c < nblk;
+  // bytes of tpr column blocks (tpr is a multiple of 8: whole Q4_K superblocks)
+  const int cb_bytes = FMT == EPQ_Q4_K ? p.tpr * 144 / 8 : p.tpr * Fmt<FMT>::kBlockBytes;
   ColConst<FMT> cc;
   cc.init(active ? c : 0);
   float xr[32];
   XCol<1> xc;
   float xs[1] = {0.0f};
-  int use = 0;
-  int my_row = -1;  // tile row this thread finalizes (holder path; same for every unit)
+  float acc[RPG][NT];
+#pragma unroll
+  for (int q = 0; q < RPG; ++q)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[q][t] = 0.0f;
   for (int u = 0; u < nunits; ++u) {
     const int s = u % p.stages;
     if (!warp_wait(&full[s], (u / p.stages) & 1, a.err, DEVERR_FULL_WAIT, u)) return;
@@ -913,83 +1033,271 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) down_kernel(const Engin
     const int64_t r0 = rb + static_cast<int64_t>(tile) * p.tile_rows;
     const int nr = static_cast<int>(min(static_cast<int64_t>(p.tile_rows), re - r0));
     const uint8_t *stage = smem + static_cast<uint32_t>(s) * p.stage_bytes;
+    const bool rows_here = active && g * RPG < nr;  // this group has rows in the tile
     const int ne = m.cnt[slot];
-    bool ok = true;
-    for (int j = 0; j < ne; ++j, ++use) {
+    for (int j = 0; j < ne; ++j) {
       const int ent = m.list[slot * a.ntok + j];
       const int tok = ent >> 5, k = ent & 31;
       const int hsi = tok * (a.topk + 1) + k;
+      if (!rows_here) continue;
       const int E = m.expo[hsi];
-      const bool rows_here = g * RPG < nr;  // this group has rows in the tile
-      if (active && rows_here) {
+      const float wk = k < a.topk ? m.w[tok * a.topk + k] : m.gs[tok];
+      float part[RPG];
+#pragma unroll
+      for (int q = 0; q < RPG; ++q) part[q] = 0.0f;
+      for (int cb = c, ib = 0; cb < nblk; cb += p.tpr, ++ib) {
         if (p.stage_h) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) xc.p[0][i] = pairs[(hsi * 16 + i) * nblk + c];
-          xs[0] = hsum[hsi * nblk + c];
+          for (int i = 0; i < 16; ++i) xc.p[0][i] = pairs[(hsi * 16 + i) * nblk + cb];
+          xs[0] = hsum[hsi * nblk + cb];
         } else {
-          load_column(a.h + static_cast<int64_t>(hsi) * I + 32 * c, xr);
+          load_column(a.h + static_cast<int64_t>(hsi) * I + 32 * cb, xr);
           xs[0] = scale_column<FMT>(xr, E, xc.p[0]);
         }
+#pragma unroll
+        for (int q = 0; q < RPG; ++q) {
+          const int lr = g * RPG + q;
+          if (lr < nr) {
+            float pr[1] = {0.0f};
+            column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes + ib * cb_bytes, cc, xc, xs, pr);
+            part[q] += pr[0];
+          }
+        }
       }
-      float part[1][RPG];
 #pragma unroll
       for (int q = 0; q < RPG; ++q) {
-        const int lr = g * RPG + q;
-        float pr[1] = {0.0f};
-        if (active && rows_here && lr < nr)
-          column_dot<FMT, 1>(stage + static_cast<uint32_t>(lr) * a.dn_row_bytes, cc, xc, xs, pr);
-        part[0][q] = pr[0];
-      }
-      if (j == ne - 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-      }
-      const int row_k = reduce_or_hand_off<RPG>(part, p, g, c, lane, red, rfull, rempty, use, ok);
-      if (__any_sync(0xffffffffu, !ok)) return;
-      if (!has_fin && row_k >= 0) {
-        my_row = g * RPG + row_k;
-        const float wk = k < a.topk ? m.w[tok * a.topk + k] : m.gs[tok];
-        acc[tok * p.tile_rows + my_row] += wk * unscale(part[0][0], E);
+        const float v = wk * unscale(part[q], E);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          if (t == tok) acc[q][t] += v;
       }
     }
-    if (!has_fin && slot == nslots - 1 && my_row >= 0 && my_row < nr) {
-      // all slots of this tile are in: y = x + weighted expert sum
-      for (int tk = 0; tk < a.ntok; ++tk) {
-        const int64_t o = static_cast<int64_t>(tk) * H + r0 + my_row;
-        a.y[o] = a.x[o] + acc[tk * p.tile_rows + my_row];
-        acc[tk * p.tile_rows + my_row] = 0.0f;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage is no longer read
+    if (slot != nslots - 1) continue;
+
+    // all slots of this tile are in: reduce each (row, token) over the group
+    // and write y = x + weighted expert sum
+#pragma unroll
+    for (int q = 0; q < RPG; ++q) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float v = acc[q][t];
+        for (int o = p.tpr / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        const int lr = g * RPG + q;
+        if (c == 0 && t < a.ntok && lr < nr) {
+          const int64_t o = static_cast<int64_t>(t) * H + r0 + lr;
+          a.y[o] = a.x[o] + v;
+        }
+        acc[q][t] = 0.0f;
       }
     }
   }
 }
 
+// ------------------------------------------------------------------ 3b. down + combine, one-shot form
+// Used when every slot's rows of a CTA fit shared memory at once (decode:
+// a few KB per slot).  The producer stages them with one bulk copy per slot
+// on a single barrier; the consumers then work on (slot, row) pairs with no
+// per-unit synchronisation: group g takes pairs g, g + groups, ...; a pair's
+// dot per entry is reduced inside the group and its weighted value per
+// token is stored in contrib[(slot * rows + row) * NT + t]; after a bounded
+// CTA barrier one thread per (row, token) adds the slots in order, so the
+// result does not depend on timing.  NT >= ntok.
+template <int FMT, int NT>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_flat_kernel(const EngineArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const MoeArgs &a = p.a;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+  uint64_t *done = full + 1;
+  float *hs_smem = reinterpret_cast<float *>(smem + p.hs_off);
+  float *contrib = reinterpret_cast<float *>(smem + p.acc_off);
+  const int nthreads = p.groups * p.tpr;
+  const int nwarps = nthreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int H = a.H, I = a.I;
+  const int64_t rb = (static_cast<int64_t>(blockIdx.x) * H) / gridDim.x;
+  const int nr = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * H) / gridDim.x - rb);  // <= tile_rows
+
+  if (tid == 0) {
+    mbar_init(full, 1);
+    mbar_init(done, nwarps);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // h, routing and hmax come from the previous kernels
+
+  if (tid >= nthreads) {
+    // producer warp: every slot's rows of this CTA, one bulk copy each
+    const int plane = tid - nthreads;
+    const int nslots = __ldcg(a.meta + 1);
+    SlotIds ids;
+    ids.load(a, plane);
+    const uint32_t bytes = static_cast<uint32_t>(nr * a.dn_row_bytes);
+    if (plane == 0) mbar_arrive_expect_tx(full, bytes * static_cast<uint32_t>(nslots));
+#pragma unroll 1
+    for (int s = 0; s < nslots; ++s) {
+      const int e = ids.get(s);
+      const uint8_t *base = e >= 0 ? a.down + static_cast<int64_t>(e) * a.dn_stride : a.sh_down;
+      if (plane == 0)
+        bulk_g2s(smem + static_cast<uint32_t>(s) * p.stage_bytes, base + rb * a.dn_row_bytes, bytes, full);
+    }
+    return;
+  }
+
+  // consumers: routing metadata and all of h into shared memory
+  Meta m(smem + p.meta_off, a.ntok, a.topk);
+  const int nblk = I / 32;
+  const int nh = a.ntok * (a.topk + 1);
+  const int n4 = nh * I / 4;
+#pragma unroll 1
+  for (int q = tid; q < n4; q += nthreads)
+    if ((q & 7) == 0 || q == tid) prefetch_l1(reinterpret_cast<const float4 *>(a.h) + q);
+  load_meta(a, m, tid, nthreads);
+  f2_t *pairs = reinterpret_cast<f2_t *>(hs_smem);
+  float *hsum = hs_smem + static_cast<int64_t>(nh) * I;  // [nh][nblk]
+  named_sync(1, nthreads);  // the h exponents are in m.expo
+#pragma unroll 1
+  for (int q0 = tid - lane; q0 < n4; q0 += nthreads) {
+    const int q = q0 + lane;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    int hsi = 0, col = 0, j = 0;
+    if (q < n4) {
+      v = reinterpret_cast<const float4 *>(a.h)[q];  // L1: prefetched above
+      hsi = (4 * q) / I;
+      col = ((4 * q) % I) / 32;
+      j = (4 * q) & 31;
+    }
+    const int E = m.expo[hsi];
+    float sum = (v.x + v.y) + (v.z + v.w);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    if (q < n4) {
+      const int base = (hsi * 16 + j / 2) * nblk + col;
+      pairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
+                            scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
+      pairs[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
+                                   scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
+      if (j == 0) hsum[hsi * nblk + col] = scale_pow2(sum, -23 - E);
+    }
+  }
+  named_sync(1, nthreads);
+  const int nslots = *m.nslots;
+
+  const int g = tid / p.tpr, c = tid % p.tpr;
+  const bool active = c < nblk;
+  const int cb_bytes = FMT == EPQ_Q4_K ? p.tpr * 144 / 8 : p.tpr * Fmt<FMT>::kBlockBytes;
+  ColConst<FMT> cc;
+  cc.init(active ? c : 0);
+  XCol<1> xc;
+  float xs[1] = {0.0f};
+  if (!warp_wait(full, 0, a.err, DEVERR_FULL_WAIT, 0)) return;
+  const int npairs = nslots * nr;
+  const int iters = (npairs + p.groups - 1) / p.groups;  // the same for every warp
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    const int pi = g + it * p.groups;
+    const bool have = pi < npairs;
+    const int s = have ? pi / nr : 0, r = have ? pi - s * nr : 0;
+    const int ne = have ? m.cnt[s] : 0;
+    const int ne_max = __reduce_max_sync(0xffffffffu, ne);  // uniform trip count for the shuffles
+    float accp[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) accp[t] = 0.0f;
+    const uint8_t *row = smem + static_cast<uint32_t>(s) * p.stage_bytes + static_cast<uint32_t>(r) * a.dn_row_bytes;
+#pragma unroll 1
+    for (int jj = 0; jj < ne_max; ++jj) {
+      const bool on = jj < ne;
+      const int ent = on ? m.list[s * a.ntok + jj] : 0;
+      const int tok = ent >> 5, k = ent & 31;
+      const int hsi = tok * (a.topk + 1) + k;
+      float part = 0.0f;
+      if (on && active) {
+#pragma unroll 1
+        for (int cb = c, ib = 0; cb < nblk; cb += p.tpr, ++ib) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xc.p[0][i] = pairs[(hsi * 16 + i) * nblk + cb];
+          xs[0] = hsum[hsi * nblk + cb];
+          float pr[1] = {0.0f};
+          column_dot<FMT, 1>(row + ib * cb_bytes, cc, xc, xs, pr);
+          part += pr[0];
+        }
+      }
+      for (int o = p.tpr / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (on) {
+        const float v = (k < a.topk ? m.w[tok * a.topk + k] : m.gs[tok]) * unscale(part, m.expo[hsi]);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          if (t == tok) accp[t] += v;
+      }
+    }
+    if (have && c == 0) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) contrib[(s * p.tile_rows + r) * NT + t] = accp[t];
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(done);
+  // y = x + sum over slots, one thread per (row, token), slots in order
+  if (tid < ((nr * a.ntok + 31) & ~31)) {
+    if (!warp_wait(done, 0, a.err, DEVERR_RED_WAIT, 0)) return;
+    if (tid < nr * a.ntok) {
+      const int r = tid / a.ntok, t = tid - r * a.ntok;
+      float v = 0.0f;
+#pragma unroll 1
+      for (int s = 0; s < nslots; ++s) v += contrib[(s * p.tile_rows + r) * NT + t];
+      const int64_t o = static_cast<int64_t>(t) * H + rb + r;
+      a.y[o] = a.x[o] + v;
+    }
+  }
+}
+
+// block: consumers + the producer warp (+ the finisher warp when `fin`)
 template <typename K>
-cudaError_t launch_engine(K kernel, const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
+cudaError_t launch_engine(K kernel, const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s, bool fin) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 block(p.groups * p.tpr + 32 + (p.tpr > 32 ? 32 : 0));
+  const dim3 block(p.groups * p.tpr + 32 + (fin ? 32 : 0));
   return launch_pdl(kernel, dim3(grid), block, smem, s, p);
 }
 
 template <int FMT>
 cudaError_t launch_gateup(const EngineArgs &p, int rpg, unsigned grid, uint32_t smem, cudaStream_t s) {
+  const bool fin = p.tpr > 32;
   switch (rpg) {
-    case 2: return launch_engine(gateup_kernel<FMT, 2>, p, grid, smem, s);
-    case 4: return launch_engine(gateup_kernel<FMT, 4>, p, grid, smem, s);
-    case 8: return launch_engine(gateup_kernel<FMT, 8>, p, grid, smem, s);
+    case 2: return launch_engine(gateup_kernel<FMT, 2>, p, grid, smem, s, fin);
+    case 4: return launch_engine(gateup_kernel<FMT, 4>, p, grid, smem, s, fin);
+    case 8: return launch_engine(gateup_kernel<FMT, 8>, p, grid, smem, s, fin);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// NT: token accumulators per thread (>= ntok); RPG * NT <= 32 registers
+template <int FMT, int NT>
+cudaError_t launch_down_nt(const EngineArgs &p, int rpg, unsigned grid, uint32_t smem, cudaStream_t s) {
+  switch (rpg) {
+    case 1: return launch_engine(down_kernel<FMT, 1, NT>, p, grid, smem, s, false);
+    case 2: return launch_engine(down_kernel<FMT, 2, NT>, p, grid, smem, s, false);
+    case 4: if (NT <= 8) return launch_engine(down_kernel<FMT, (NT <= 8 ? 4 : 1), NT>, p, grid, smem, s, false); break;
+    case 8: if (NT <= 4) return launch_engine(down_kernel<FMT, (NT <= 4 ? 8 : 1), NT>, p, grid, smem, s, false); break;
   }
   return cudaErrorInvalidValue;
 }
 
 template <int FMT>
+cudaError_t launch_down_flat(const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
+  if (p.a.ntok <= 1) return launch_engine(down_flat_kernel<FMT, 1>, p, grid, smem, s, false);
+  return launch_engine(down_flat_kernel<FMT, 4>, p, grid, smem, s, false);
+}
+
+template <int FMT>
 cudaError_t launch_down(const EngineArgs &p, int rpg, unsigned grid, uint32_t smem, cudaStream_t s) {
-  switch (rpg) {
-    case 1: return launch_engine(down_kernel<FMT, 1>, p, grid, smem, s);
-    case 2: return launch_engine(down_kernel<FMT, 2>, p, grid, smem, s);
-    case 4: return launch_engine(down_kernel<FMT, 4>, p, grid, smem, s);
-    case 8: return launch_engine(down_kernel<FMT, 8>, p, grid, smem, s);
-  }
-  return cudaErrorInvalidValue;
+  const int ntok = p.a.ntok;
+  if (ntok <= 1) return launch_down_nt<FMT, 1>(p, rpg, grid, smem, s);
+  if (ntok <= 4) return launch_down_nt<FMT, 4>(p, rpg, grid, smem, s);
+  return launch_down_nt<FMT, kMaxTok>(p, rpg, grid, smem, s);
 }
 
 epq_status check_moe(const epq_router *r, const epq_experts *x, int ntok, int topk) {
@@ -1096,7 +1404,8 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
     if (!(stages & EPQ_MOE_GATE_UP) && (topk_idx || topk_w || (stages & EPQ_MOE_DOWN))) {
       // the gate/up kernel routes for itself; without it, route here when
       // this call returns the selection or runs the down stage
-      e = launch_pdl(select_kernel, dim3(1), dim3(kSelectThreads), 4u * meta_words(ntok, topk), s, a);
+      const uint32_t sel_smem = ((4u * meta_words(ntok, topk) + 15u) & ~15u) + 4u * kSelScratchWords;
+      e = launch_pdl(select_kernel, dim3(1), dim3(kSelectThreads), sel_smem, s, a);
       if (e != cudaSuccess) return cuda_fail(e);
     }
   }
@@ -1105,10 +1414,13 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const int max_slots = std::min(E, ntok * topk) + (a.has_shared ? 1 : 0);
   const unsigned ggrid = static_cast<unsigned>(dev.sm_count);
   const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
-  const int64_t g_hint = (static_cast<int64_t>(max_slots) * I + ggrid - 1) / ggrid / 2;
+  const int64_t g_hint = (static_cast<int64_t>(max_slots) * I + ggrid - 1) / ggrid;
   const int64_t d_hint = (H + dgrid - 1) / dgrid;
   if (!engine_plan(H, 2 * a.gu_row_bytes, true, g_hint, ntok, topk, I, false, dev, &gp)) return EPQ_ERR_SHAPE;
-  if (!engine_plan(I, a.dn_row_bytes, false, d_hint, ntok, topk, I, true, dev, &dp)) return EPQ_ERR_SHAPE;
+  // the gate/up kernel routes in its stage ring before the first copy
+  if (static_cast<int64_t>(gp.stages) * gp.stage_bytes < 4ll * kSelScratchWords) return EPQ_ERR_SHAPE;
+  const bool flat = flat_down_plan(I, a.dn_row_bytes, H, dgrid, max_slots, ntok, topk, dev, &dp);
+  if (!flat && !engine_plan(I, a.dn_row_bytes, false, d_hint, ntok, topk, I, true, dev, &dp)) return EPQ_ERR_SHAPE;
 
   EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_h, gp.stage_bytes, gp.bar_off,
                 gp.red_off, gp.meta_off, gp.hs_off, gp.acc_off};
@@ -1122,7 +1434,13 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
 
   EngineArgs da{a, dp.tpr, dp.groups, dp.tile_rows, dp.stages, dp.stage_h, dp.stage_bytes, dp.bar_off,
                 dp.red_off, dp.meta_off, dp.hs_off, dp.acc_off};
-  if (stages & EPQ_MOE_DOWN) switch (experts->fmt) {
+  if ((stages & EPQ_MOE_DOWN) && flat) switch (experts->fmt) {
+    case EPQ_Q8_0: e = launch_down_flat<EPQ_Q8_0>(da, dgrid, dp.smem, s); break;
+    case EPQ_Q4_0: e = launch_down_flat<EPQ_Q4_0>(da, dgrid, dp.smem, s); break;
+    case EPQ_Q4_1: e = launch_down_flat<EPQ_Q4_1>(da, dgrid, dp.smem, s); break;
+    case EPQ_Q4_K: e = launch_down_flat<EPQ_Q4_K>(da, dgrid, dp.smem, s); break;
+  }
+  else if (stages & EPQ_MOE_DOWN) switch (experts->fmt) {
     case EPQ_Q8_0: e = launch_down<EPQ_Q8_0>(da, dp.rpg, dgrid, dp.smem, s); break;
     case EPQ_Q4_0: e = launch_down<EPQ_Q4_0>(da, dp.rpg, dgrid, dp.smem, s); break;
     case EPQ_Q4_1: e = launch_down<EPQ_Q4_1>(da, dp.rpg, dgrid, dp.smem, s); break;
