@@ -39,7 +39,6 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture of the kernel as it stands; the summary with its command is the
 # named file.  An entry must go when its kernel changes.
 NCU_TRAFFIC = {
-    "moe_gateup": (10_709_888, "profiles/moe_gateup_q4k_full.md"),
 }
 FALLBACK_HBM_GBS = 6800.0
 

@@ -301,7 +301,7 @@ __device__ void select_topk(const MoeArgs &a, Meta &m, uint32_t *scratch, bool p
     const int nt = min(tb, a.ntok - t0);
     // level 1
 #pragma unroll 1
-    for (int job = warp; job < nt * nch; job += nwarps) {
+    for (int job = nwarps - 1 - warp; job < nt * nch; job += nwarps) {  // the last warps first
       const int tl = job / nch, c = job - tl * nch;
       const int e = c * 32 + lane;
       const float v = e < E ? __ldcg(a.logits + static_cast<int64_t>(t0 + tl) * E + e) : 0.0f;
@@ -612,6 +612,37 @@ bool flat_down_plan(int I, int64_t row_bytes, int H, unsigned grid, int max_slot
   return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
 }
 
+// One-shot gate/up form (gateup_flat_kernel): a CTA's whole share of gate
+// and up rows staged at once.  Returns false when the shapes need the
+// pipelined form.
+bool flat_gateup_plan(int H, int64_t row_bytes, int I, unsigned grid, int max_slots, int ntok, int topk,
+                      const DeviceInfo &dev, EnginePlan *pl) {
+  if (ntok > 4) return false;
+  const int nblk = H / 32;
+  pl->tpr = std::min(32, std::max(8, next_pow2(nblk)));
+  pl->groups = kMaxConsumers / pl->tpr;
+  pl->rpg = 2;
+  pl->tile_rows = static_cast<int>((static_cast<int64_t>(max_slots) * I + grid - 1) / grid);
+  pl->stage_bytes = static_cast<uint32_t>((2 * pl->tile_rows * row_bytes + 15) & ~int64_t(15));
+  if (pl->stage_bytes < 4u * kSelScratchWords) pl->stage_bytes = 4u * kSelScratchWords;  // routing scratch
+  pl->stages = 1;
+  pl->stage_h = 0;
+  uint32_t o = pl->stage_bytes;
+  pl->bar_off = o;
+  o += 16;
+  pl->red_off = o;
+  pl->meta_off = o;
+  o += 4u * meta_words(ntok, topk);
+  o = (o + 15) & ~15u;
+  pl->hs_off = o;  // scaled x pairs and column sums
+  o += static_cast<uint32_t>(4ll * ntok * H + 4ll * ntok * nblk);
+  o = (o + 15) & ~15u;
+  pl->acc_off = o;  // per-CTA max|h|
+  o += 4u * ntok * (topk + 1);
+  pl->smem = (o + 15) & ~15u;
+  return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
+}
+
 struct EngineArgs {
   MoeArgs a;
   int tpr, groups, tile_rows, stages, stage_h;
@@ -885,6 +916,172 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
         if (lane == 0 && hm) atomicMax(a.hmax + hs, hm);
       }
     }
+  }
+}
+
+// ------------------------------------------------------------------ 2b. gate/up, one-shot form
+// Used when a CTA's whole share of gate and up rows fits shared memory at
+// once (decode).  While the last warps select the experts, the other warps
+// stage x of every token in scaled form; after routing the producer copies
+// the CTA's rows (per slot segment: the gate rows, then the matching up
+// rows) on one barrier.  Group g takes virtual rows g, g + groups, ...: for
+// every entry of the row's slot it forms the gate and up dots over its
+// column blocks, reduces them inside the group and writes
+// h = silu(g) * u.  max|h| is reduced per CTA before one global atomic per
+// (token, slot).  NT >= ntok.
+template <int FMT, int NT>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(const EngineArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const MoeArgs &a = p.a;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+  uint64_t *done = full + 1;
+  f2_t *xpairs = reinterpret_cast<f2_t *>(smem + p.hs_off);  // [ntok][16][nblk]
+  const int nthreads = p.groups * p.tpr;
+  const int nwarps_c = nthreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int H = a.H, I = a.I;
+  const int nblk = H / 32;
+  float *xsum = reinterpret_cast<float *>(xpairs + static_cast<int64_t>(a.ntok) * 16 * nblk);  // [ntok][nblk]
+  unsigned *hmax_cta = reinterpret_cast<unsigned *>(smem + p.acc_off);  // [ntok * (topk + 1)]
+
+  if (tid == 0) {
+    mbar_init(full, 1);
+    mbar_init(done, nwarps_c);
+    fence_mbar_init();
+  }
+  Meta m(smem + p.meta_off, a.ntok, a.topk);
+  m.clear(tid, blockDim.x);
+  for (int i = tid; i < a.ntok * (a.topk + 1); i += blockDim.x) hmax_cta[i] = 0u;
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // logits, x statistics and x come from the router kernel and before
+
+  // x of every token, scaled, by the warps that do not start the selection
+  const int nch = (a.E + 31) / 32;
+  const int xwarps = nwarps - min(nwarps - 1, a.ntok * nch);
+  if (warp < xwarps) {
+    const int n4 = a.ntok * H / 4;
+#pragma unroll 1
+    for (int q0 = tid - lane; q0 < n4; q0 += xwarps * 32) {
+      const int q = q0 + lane;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      int t = 0, col = 0, j = 0;
+      if (q < n4) {
+        v = reinterpret_cast<const float4 *>(a.x)[q];
+        t = (4 * q) / H;
+        col = ((4 * q) % H) / 32;
+        j = (4 * q) & 31;
+      }
+      const int E = bound_exponent(__ldcg(a.xstat + 2 * t));
+      float sum = (v.x + v.y) + (v.z + v.w);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      if (q < n4) {
+        const int base = (t * 16 + j / 2) * nblk + col;
+        xpairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
+                               scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
+        xpairs[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
+                                      scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
+        if (j == 0) xsum[t * nblk + col] = scale_pow2(sum, -23 - E);
+      }
+    }
+  }
+  route_tokens(a, m, reinterpret_cast<uint32_t *>(smem), blockIdx.x == 0);  // the stage area is free until routed
+
+  const int nact = *m.nact;
+  const int64_t total = static_cast<int64_t>(*m.nslots) * I;
+  const int64_t rb = (static_cast<int64_t>(blockIdx.x) * total) / gridDim.x;
+  const int nrows = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * total) / gridDim.x - rb);  // <= tile_rows
+  uint8_t *gate_s = smem;
+  uint8_t *up_s = smem + static_cast<uint32_t>(p.tile_rows) * a.gu_row_bytes;
+
+  if (tid >= nthreads) {
+    // producer: per slot segment of this CTA's rows, the gate rows and the up rows
+    if (tid == nthreads && nrows > 0) {
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(2 * nrows * a.gu_row_bytes));
+      int64_t r0 = rb;
+      const int64_t re = rb + nrows;
+#pragma unroll 1
+      while (r0 < re) {
+        const int slot = static_cast<int>(r0 / I);
+        const int64_t r1 = min(re, static_cast<int64_t>(slot + 1) * I);
+        const int e = slot < nact ? m.active[slot] : -1;
+        const uint8_t *base = e >= 0 ? a.gate_up + static_cast<int64_t>(e) * a.gu_stride : a.sh_gate_up;
+        const int64_t i0 = r0 - static_cast<int64_t>(slot) * I;
+        const uint32_t bytes = static_cast<uint32_t>((r1 - r0) * a.gu_row_bytes);
+        const uint32_t off = static_cast<uint32_t>((r0 - rb) * a.gu_row_bytes);
+        bulk_g2s(gate_s + off, base + i0 * a.gu_row_bytes, bytes, full);
+        bulk_g2s(up_s + off, base + (I + i0) * a.gu_row_bytes, bytes, full);
+        r0 = r1;
+      }
+    }
+    return;
+  }
+
+  const int g = tid / p.tpr, c = tid % p.tpr;
+  const bool active = c < nblk;
+  const int cb_bytes = FMT == EPQ_Q4_K ? p.tpr * 144 / 8 : p.tpr * Fmt<FMT>::kBlockBytes;
+  ColConst<FMT> cc;
+  cc.init(active ? c : 0);
+  XCol<1> xc;
+  float xs[1] = {0.0f};
+  if (nrows > 0 && !warp_wait(full, 0, a.err, DEVERR_FULL_WAIT, 0)) return;
+  const int iters = (nrows + p.groups - 1) / p.groups;  // the same for every warp
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    const int v = g + it * p.groups;
+    const bool have = v < nrows;
+    const int64_t rv = rb + (have ? v : 0);
+    const int slot = static_cast<int>(rv / I);
+    const int i = static_cast<int>(rv - static_cast<int64_t>(slot) * I);
+    const int ne = have ? m.cnt[slot] : 0;
+    const int ne_max = __reduce_max_sync(0xffffffffu, ne);
+    const uint8_t *grow = gate_s + static_cast<uint32_t>(have ? v : 0) * a.gu_row_bytes;
+    const uint8_t *urow = up_s + static_cast<uint32_t>(have ? v : 0) * a.gu_row_bytes;
+#pragma unroll 1
+    for (int jj = 0; jj < ne_max; ++jj) {
+      const bool on = jj < ne;
+      const int ent = on ? m.list[slot * a.ntok + jj] : 0;
+      const int tok = ent >> 5, k = ent & 31;
+      float pg = 0.0f, pu = 0.0f;
+      if (on && active) {
+#pragma unroll 1
+        for (int cb = c, ib = 0; cb < nblk; cb += p.tpr, ++ib) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) xc.p[0][q] = xpairs[(tok * 16 + q) * nblk + cb];
+          xs[0] = xsum[tok * nblk + cb];
+          float pr[1] = {0.0f};
+          column_dot<FMT, 1>(grow + ib * cb_bytes, cc, xc, xs, pr);
+          pg += pr[0];
+          pr[0] = 0.0f;
+          column_dot<FMT, 1>(urow + ib * cb_bytes, cc, xc, xs, pr);
+          pu += pr[0];
+        }
+      }
+      for (int o = p.tpr / 2; o > 0; o >>= 1) {
+        pg += __shfl_xor_sync(0xffffffffu, pg, o);
+        pu += __shfl_xor_sync(0xffffffffu, pu, o);
+      }
+      if (on && c == 0) {
+        const int E = m.expo[tok];
+        const float r = m.rms[tok];
+        const float hv = silu(unscale(pg, E) * r) * (unscale(pu, E) * r);
+        const int hs = tok * (a.topk + 1) + k;
+        a.h[static_cast<int64_t>(hs) * I + i] = hv;
+        atomicMax(hmax_cta + hs, __float_as_uint(fabsf(hv)));
+      }
+    }
+  }
+  // one global max|h| update per (token, slot) and CTA
+  __syncwarp();
+  if (lane == 0) mbar_arrive(done);
+  if (warp == 0) {
+    if (!warp_wait(done, 0, a.err, DEVERR_RED_WAIT, 0)) return;
+#pragma unroll 1
+    for (int q = lane; q < a.ntok * (a.topk + 1); q += 32)
+      if (hmax_cta[q]) atomicMax(a.hmax + q, hmax_cta[q]);
   }
 }
 
@@ -1287,6 +1484,12 @@ cudaError_t launch_down_nt(const EngineArgs &p, int rpg, unsigned grid, uint32_t
 }
 
 template <int FMT>
+cudaError_t launch_gateup_flat(const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
+  if (p.a.ntok <= 1) return launch_engine(gateup_flat_kernel<FMT, 1>, p, grid, smem, s, false);
+  return launch_engine(gateup_flat_kernel<FMT, 4>, p, grid, smem, s, false);
+}
+
+template <int FMT>
 cudaError_t launch_down_flat(const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
   if (p.a.ntok <= 1) return launch_engine(down_flat_kernel<FMT, 1>, p, grid, smem, s, false);
   return launch_engine(down_flat_kernel<FMT, 4>, p, grid, smem, s, false);
@@ -1416,15 +1619,23 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
   const int64_t g_hint = (static_cast<int64_t>(max_slots) * I + ggrid - 1) / ggrid;
   const int64_t d_hint = (H + dgrid - 1) / dgrid;
-  if (!engine_plan(H, 2 * a.gu_row_bytes, true, g_hint, ntok, topk, I, false, dev, &gp)) return EPQ_ERR_SHAPE;
-  // the gate/up kernel routes in its stage ring before the first copy
+  const bool gflat = flat_gateup_plan(H, a.gu_row_bytes, I, ggrid, max_slots, ntok, topk, dev, &gp);
+  if (!gflat && !engine_plan(H, 2 * a.gu_row_bytes, true, g_hint, ntok, topk, I, false, dev, &gp))
+    return EPQ_ERR_SHAPE;
+  // the gate/up kernel routes in its stage area before the first copy
   if (static_cast<int64_t>(gp.stages) * gp.stage_bytes < 4ll * kSelScratchWords) return EPQ_ERR_SHAPE;
   const bool flat = flat_down_plan(I, a.dn_row_bytes, H, dgrid, max_slots, ntok, topk, dev, &dp);
   if (!flat && !engine_plan(I, a.dn_row_bytes, false, d_hint, ntok, topk, I, true, dev, &dp)) return EPQ_ERR_SHAPE;
 
   EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_h, gp.stage_bytes, gp.bar_off,
                 gp.red_off, gp.meta_off, gp.hs_off, gp.acc_off};
-  if (stages & EPQ_MOE_GATE_UP) switch (experts->fmt) {
+  if ((stages & EPQ_MOE_GATE_UP) && gflat) switch (experts->fmt) {
+    case EPQ_Q8_0: e = launch_gateup_flat<EPQ_Q8_0>(ga, ggrid, gp.smem, s); break;
+    case EPQ_Q4_0: e = launch_gateup_flat<EPQ_Q4_0>(ga, ggrid, gp.smem, s); break;
+    case EPQ_Q4_1: e = launch_gateup_flat<EPQ_Q4_1>(ga, ggrid, gp.smem, s); break;
+    case EPQ_Q4_K: e = launch_gateup_flat<EPQ_Q4_K>(ga, ggrid, gp.smem, s); break;
+  }
+  else if (stages & EPQ_MOE_GATE_UP) switch (experts->fmt) {
     case EPQ_Q8_0: e = launch_gateup<EPQ_Q8_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
     case EPQ_Q4_0: e = launch_gateup<EPQ_Q4_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
     case EPQ_Q4_1: e = launch_gateup<EPQ_Q4_1>(ga, gp.rpg, ggrid, gp.smem, s); break;
