@@ -39,6 +39,7 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture of the kernel as it stands; the summary with its command is the
 # named file.  An entry must go when its kernel changes.
 NCU_TRAFFIC = {
+    "moe_gateup": (10_700_672, "profiles/moe_gateup_flat_q4k_full.md"),
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -356,8 +357,9 @@ def run_epq(args):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         W.step(stream, timers=timers)
-    for _ in range(max(3, args.warmup)):
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
     torch.cuda.synchronize()
 
     def barrier():
@@ -370,10 +372,11 @@ def run_epq(args):
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            g.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):  # replays and events on one stream
+            e0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize()
         barrier()
