@@ -365,6 +365,153 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gemv_kernel(const GemvP
   }
 }
 
+// ------------------------------------------------------------------ one-shot form
+// One vector, and a CTA's whole row range fits shared memory at once
+// (decode projections).  The producer stages the rows with one bulk copy
+// (two with SwiGLU: the gate rows and the up rows) on a single barrier,
+// before the grid-dependency wait when the weights are ready; the consumers
+// take max|x| and sum x^2 (RMS pre-norm), stage x in scaled pairs once, and
+// then row group g computes rows g, g + groups, ... over its column blocks
+// (c, c + tpr, ...; tpr <= 32, so a row is reduced inside its warp).
+constexpr int kFlatMaxX4 = 8;  // float4 of x per thread kept in registers between the passes
+
+template <int FMT, bool SWIGLU>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) gemv_flat_kernel(const GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nthreads = p.groups * p.tpr;
+  const int nwarps = nthreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nblk = p.nblk;
+  // layout: rows (gate, then up) | 16-byte over-read pad | barrier | scratch | x pairs | x column sums
+  const uint32_t rows_bytes = static_cast<uint32_t>(p.tile_rows * p.row_bytes);
+  uint8_t *gate_s = smem;
+  uint8_t *up_s = smem + rows_bytes;
+  uint32_t o = (SWIGLU ? 2u : 1u) * rows_bytes + 16u;
+  o = (o + 15u) & ~15u;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + o);
+  float *scratch = reinterpret_cast<float *>(smem + o + 16);  // [2][nwarps]
+  f2_t *xp = reinterpret_cast<f2_t *>(smem + ((o + 16 + 8u * nwarps + 15u) & ~15u));  // [16][nblk]
+  float *xsum = reinterpret_cast<float *>(xp + 16 * nblk);                                // [nblk]
+
+  const int64_t rb = (static_cast<int64_t>(blockIdx.x) * p.rows_out) / gridDim.x;
+  const int nr = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * p.rows_out) / gridDim.x - rb);
+
+  if (tid == 0) {
+    mbar_init(full, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (tid >= nthreads) {
+    if (tid == nthreads && nr > 0) {
+      if (!p.early_weights) pdl_wait();
+      const uint32_t bytes = static_cast<uint32_t>(nr * p.row_bytes);
+      mbar_arrive_expect_tx(full, SWIGLU ? 2 * bytes : bytes);
+      bulk_g2s(gate_s, p.W + rb * p.row_bytes, bytes, full);
+      if (SWIGLU) bulk_g2s(up_s, p.W + (p.up_rows + rb) * p.row_bytes, bytes, full);
+    }
+    return;
+  }
+
+  pdl_wait();  // x and the residual are produced upstream
+  // pass 1: max|x| and sum x^2 (x kept in registers for pass 2)
+  const XGather xg{p.x_group, p.x_head_dim};
+  const int c4 = p.cols / 4;
+  float4 xv[kFlatMaxX4];
+  float amax = 0.0f, ssq = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kFlatMaxX4; ++k) {
+    const int e4 = (tid - lane) + k * nthreads + lane;
+    xv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e4 < c4) {
+      xv[k] = *reinterpret_cast<const float4 *>(p.x + xg.src(4 * e4));
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(xv[k].x), fabsf(xv[k].y)), fmaxf(fabsf(xv[k].z), fabsf(xv[k].w))));
+      ssq = fmaf(xv[k].x, xv[k].x, fmaf(xv[k].y, xv[k].y, fmaf(xv[k].z, xv[k].z, fmaf(xv[k].w, xv[k].w, ssq))));
+    }
+  }
+  amax = warp_max_all(amax);
+  ssq = warp_sum_xor<32>(ssq);
+  if (lane == 0) {
+    scratch[tid >> 5] = amax;
+    scratch[nwarps + (tid >> 5)] = ssq;
+  }
+  named_sync(1, nthreads);
+  float am = 0.0f, q = 0.0f;
+  for (int w = 0; w < nwarps; ++w) {
+    am = fmaxf(am, scratch[w]);
+    q += scratch[nwarps + w];
+  }
+  const int E = bound_exponent(am);
+  const float outscale =
+      p.rms ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.cols)), p.rms_eps))) : 1.0f;
+  // pass 2: scaled pairs; 8 consecutive threads hold one 32-float column
+#pragma unroll
+  for (int k = 0; k < kFlatMaxX4; ++k) {
+    const int e4 = (tid - lane) + k * nthreads + lane;
+    if ((tid - lane) + k * nthreads < c4) {  // warp-uniform
+      const float4 v = xv[k];
+      const int j = (4 * e4) & 31, col = (4 * e4) >> 5;
+      float sum = (v.x + v.y) + (v.z + v.w);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      if (e4 < c4) {
+        const int base = (j / 2) * nblk + col;
+        xp[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
+                           scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
+        xp[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
+                                  scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
+        if (j == 0) xsum[col] = scale_pow2(sum, -23 - E);
+      }
+    }
+  }
+  named_sync(1, nthreads);
+
+  const int g = tid / p.tpr, c = tid % p.tpr;
+  const bool active = c < nblk;
+  const int cb_bytes = FMT == EPQ_Q4_K ? p.tpr * 144 / 8 : p.tpr * Fmt<FMT>::kBlockBytes;
+  ColConst<FMT> cc;
+  cc.init(active ? c : 0);
+  XCol<1> xc;
+  float xs[1] = {0.0f};
+  if (nr > 0 && !warp_wait(full, 0, p.err, DEVERR_FULL_WAIT, 0)) return;
+  const int iters = (nr + p.groups - 1) / p.groups;  // the same for every warp
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    const int v = g + it * p.groups;
+    const bool have = v < nr && active;
+    float pg = 0.0f, pu = 0.0f;
+    if (have) {
+      const uint8_t *grow = gate_s + static_cast<uint32_t>(v) * p.row_bytes;
+      const uint8_t *urow = up_s + static_cast<uint32_t>(v) * p.row_bytes;
+#pragma unroll 1
+      for (int cb = c, ib = 0; cb < nblk; cb += p.tpr, ++ib) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xc.p[0][i] = xp[i * nblk + cb];
+        xs[0] = xsum[cb];
+        float pr[1] = {0.0f};
+        column_dot<FMT, 1>(grow + ib * cb_bytes, cc, xc, xs, pr);
+        pg += pr[0];
+        if (SWIGLU) {
+          pr[0] = 0.0f;
+          column_dot<FMT, 1>(urow + ib * cb_bytes, cc, xc, xs, pr);
+          pu += pr[0];
+        }
+      }
+    }
+    for (int off = p.tpr / 2; off > 0; off >>= 1) {
+      pg += __shfl_xor_sync(0xffffffffu, pg, off);
+      if (SWIGLU) pu += __shfl_xor_sync(0xffffffffu, pu, off);
+    }
+    if (c == 0 && v < nr) {
+      float val = unscale(pg, E) * outscale;
+      if (SWIGLU) val = silu(val) * (unscale(pu, E) * outscale);
+      store_row(p, 0, rb + v, val);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host
 struct Plan {
   int tpr, groups, gpt, teams, rpg, tile_rows, stages, xstage;
@@ -451,6 +598,37 @@ bool make_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, int n
   return true;
 }
 
+// One-shot form when one vector is computed and a CTA's rows fit shared
+// memory with x beside them.
+bool flat_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, int nvec, const DeviceInfo &dev,
+               Plan *pl) {
+  if (nvec != 1 || cols / 4 > kFlatMaxX4 * kMaxConsumers) return false;
+  const int nblk = cols / 32;
+  pl->tpr = std::min(32, std::max(8, next_pow2(nblk)));
+  pl->groups = kMaxConsumers / pl->tpr;
+  const int64_t g = std::min<int64_t>(dev.sm_count, (rows_out + 7) / 8);
+  pl->grid = static_cast<unsigned>(std::max<int64_t>(1, g));
+  pl->tile_rows = static_cast<int>((rows_out + pl->grid - 1) / pl->grid);
+  pl->gpt = pl->teams = pl->rpg = 1;
+  pl->stages = 1;
+  pl->xstage = 1;
+  pl->stage_bytes = static_cast<uint32_t>(pl->tile_rows * row_bytes);
+  const int nwarps = kMaxConsumers / 32;
+  uint32_t o = (swiglu ? 2u : 1u) * pl->stage_bytes + 16u;
+  o = (o + 15u) & ~15u;
+  o = ((o + 16 + 8u * nwarps + 15u) & ~15u) + 8u * 16 * nblk + 4u * nblk;
+  pl->smem = (o + 15u) & ~15u;
+  return pl->smem <= static_cast<uint32_t>(dev.max_smem_optin);
+}
+
+template <int FMT, bool SW>
+cudaError_t launch_flat(const GemvParams &p, const Plan &pl, cudaStream_t s) {
+  auto k = gemv_flat_kernel<FMT, SW>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3(pl.grid), dim3(pl.groups * pl.tpr + 32), pl.smem, s, p);
+}
+
 template <int FMT, int NV, int RPG, bool SW>
 cudaError_t launch_one(const GemvParams &p, const Plan &pl, cudaStream_t s, bool pdl) {
   auto k = gemv_kernel<FMT, NV, RPG, SW>;
@@ -509,7 +687,9 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   const int64_t rows_out = opts.swiglu ? rows / 2 : rows;
   const bool sw = opts.swiglu != 0;
   Plan pl;
-  if (!make_plan(row_bytes, static_cast<int>(cols), rows_out, sw, std::min(nvec, 2), dev, &pl)) return EPQ_ERR_SHAPE;
+  const bool flat = flat_plan(row_bytes, static_cast<int>(cols), rows_out, sw, nvec, dev, &pl);
+  if (!flat && !make_plan(row_bytes, static_cast<int>(cols), rows_out, sw, std::min(nvec, 2), dev, &pl))
+    return EPQ_ERR_SHAPE;
 
   GemvParams p;
   p.W = static_cast<const uint8_t *>(blocks);
@@ -542,6 +722,16 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
     p.y = y + v0 * p.y_stride;
     p.residual = opts.residual ? opts.residual + v0 * p.y_stride : nullptr;
     cudaError_t e = cudaErrorInvalidValue;
+    if (flat) {
+      switch (fmt) {
+        case EPQ_Q8_0: e = sw ? launch_flat<EPQ_Q8_0, true>(p, pl, s) : launch_flat<EPQ_Q8_0, false>(p, pl, s); break;
+        case EPQ_Q4_0: e = sw ? launch_flat<EPQ_Q4_0, true>(p, pl, s) : launch_flat<EPQ_Q4_0, false>(p, pl, s); break;
+        case EPQ_Q4_1: e = sw ? launch_flat<EPQ_Q4_1, true>(p, pl, s) : launch_flat<EPQ_Q4_1, false>(p, pl, s); break;
+        case EPQ_Q4_K: e = sw ? launch_flat<EPQ_Q4_K, true>(p, pl, s) : launch_flat<EPQ_Q4_K, false>(p, pl, s); break;
+      }
+      if (e != cudaSuccess) return cuda_fail(e);
+      continue;
+    }
     switch (fmt) {
       case EPQ_Q8_0: e = dispatch_fmt<EPQ_Q8_0>(p, pl, s, true, sw); break;
       case EPQ_Q4_0: e = dispatch_fmt<EPQ_Q4_0>(p, pl, s, true, sw); break;

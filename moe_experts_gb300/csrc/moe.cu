@@ -1029,6 +1029,71 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(cons
   float xs[1] = {0.0f};
   if (nrows > 0 && !warp_wait(full, 0, a.err, DEVERR_FULL_WAIT, 0)) return;
   const int iters = (nrows + p.groups - 1) / p.groups;  // the same for every warp
+  const int ncb = (nblk + p.tpr - 1) / p.tpr;
+  if (NT == 1 && ncb <= 2 && iters <= 4) {
+    // one token: this lane's x column blocks are loaded once; the group's
+    // rows (gate and up dots) are independent of each other
+    XCol<1> x1;
+    float xs1[1] = {0.0f};
+    const bool two = ncb == 2 && c + p.tpr < nblk;
+    if (active) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) xc.p[0][q] = xpairs[q * nblk + c];
+      xs[0] = xsum[c];
+      if (two) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) x1.p[0][q] = xpairs[q * nblk + c + p.tpr];
+        xs1[0] = xsum[c + p.tpr];
+      }
+    }
+    float pg[4], pu[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      pg[it] = 0.0f;
+      pu[it] = 0.0f;
+      const int v = g + it * p.groups;
+      if (it < iters && v < nrows && active) {
+        const uint8_t *grow = gate_s + static_cast<uint32_t>(v) * a.gu_row_bytes;
+        const uint8_t *urow = up_s + static_cast<uint32_t>(v) * a.gu_row_bytes;
+        float pr[1] = {0.0f};
+        column_dot<FMT, 1>(grow, cc, xc, xs, pr);
+        pg[it] = pr[0];
+        pr[0] = 0.0f;
+        column_dot<FMT, 1>(urow, cc, xc, xs, pr);
+        pu[it] = pr[0];
+        if (two) {
+          pr[0] = 0.0f;
+          column_dot<FMT, 1>(grow + cb_bytes, cc, x1, xs1, pr);
+          pg[it] += pr[0];
+          pr[0] = 0.0f;
+          column_dot<FMT, 1>(urow + cb_bytes, cc, x1, xs1, pr);
+          pu[it] += pr[0];
+        }
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      if (it < iters) {
+        float gv = pg[it], uv = pu[it];
+        for (int o = p.tpr / 2; o > 0; o >>= 1) {
+          gv += __shfl_xor_sync(0xffffffffu, gv, o);
+          uv += __shfl_xor_sync(0xffffffffu, uv, o);
+        }
+        const int v = g + it * p.groups;
+        if (c == 0 && v < nrows) {
+          const int64_t rv = rb + v;
+          const int slot = static_cast<int>(rv / I);
+          const int i = static_cast<int>(rv - static_cast<int64_t>(slot) * I);
+          const int k = m.list[slot] & 31;
+          const int E = m.expo[0];
+          const float r = m.rms[0];
+          const float hv = silu(unscale(gv, E) * r) * (unscale(uv, E) * r);
+          a.h[static_cast<int64_t>(k) * I + i] = hv;
+          atomicMax(hmax_cta + k, __float_as_uint(fabsf(hv)));
+        }
+      }
+    }
+  } else {
 #pragma unroll 1
   for (int it = 0; it < iters; ++it) {
     const int v = g + it * p.groups;
@@ -1073,6 +1138,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(cons
         atomicMax(hmax_cta + hs, __float_as_uint(fabsf(hv)));
       }
     }
+  }
   }
   // one global max|h| update per (token, slot) and CTA
   __syncwarp();
@@ -1391,6 +1457,43 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_flat_kernel(const 
   XCol<1> xc;
   float xs[1] = {0.0f};
   if (!warp_wait(full, 0, a.err, DEVERR_FULL_WAIT, 0)) return;
+  const int gps = max(1, p.groups / nslots);  // groups per slot (single-token path)
+  const int rows_per = (nr + gps - 1) / gps;
+  if (NT == 1 && nblk <= p.tpr && rows_per <= 8 && nslots <= p.groups) {
+    // one token: group g takes rows part, part + gps, ... of slot g / gps;
+    // the slot's h column is loaded once and the rows' dots are independent
+    const int sl = g / gps, part = g - sl * gps;
+    const bool grp_on = sl < nslots && active;
+    const int k = grp_on ? (m.list[sl] & 31) : 0;
+    float dv[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) dv[rr] = 0.0f;
+    if (grp_on) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xc.p[0][i] = pairs[(k * 16 + i) * nblk + c];
+      xs[0] = hsum[k * nblk + c];
+      const uint8_t *srow = smem + static_cast<uint32_t>(sl) * p.stage_bytes;
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = part + rr * gps;
+        if (rr < rows_per && r < nr) {
+          float pr[1] = {0.0f};
+          column_dot<FMT, 1>(srow + static_cast<uint32_t>(r) * a.dn_row_bytes, cc, xc, xs, pr);
+          dv[rr] = pr[0];
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      if (rr < rows_per) {
+        float v = dv[rr];
+        for (int o = p.tpr / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        const int r = part + rr * gps;
+        if (grp_on && c == 0 && r < nr)
+          contrib[sl * p.tile_rows + r] = (k < a.topk ? m.w[k] : m.gs[0]) * unscale(v, m.expo[k]);
+      }
+    }
+  } else {
   const int npairs = nslots * nr;
   const int iters = (npairs + p.groups - 1) / p.groups;  // the same for every warp
 #pragma unroll 1
@@ -1434,6 +1537,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_flat_kernel(const 
 #pragma unroll
       for (int t = 0; t < NT; ++t) contrib[(s * p.tile_rows + r) * NT + t] = accp[t];
     }
+  }
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(done);
