@@ -411,13 +411,19 @@ __device__ void publish_routing(const MoeArgs &a, const Meta &m, int tid, int nt
 __device__ void route_tokens(const MoeArgs &a, Meta &m, uint32_t *scratch, bool publish) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarps = nthr >> 5;
+  // per-token factors: loaded before the selection, stored after it
+  float tg = 1.0f, tr = 0.0f, tx = 0.0f;
+  if (tid < a.ntok) {  // ntok <= 16 < threads
+    if (a.gvec) tg = __ldcg(a.gshared + tid);
+    tr = __ldcg(a.xstat + 2 * tid + 1);
+    tx = __ldcg(a.xstat + 2 * tid);
+  }
   select_topk(a, m, scratch, publish);
   const int rwarp = nwarps - 1 - warp;  // rwarp 0 ran token 0's softmax
-#pragma unroll 1
-  for (int t = tid; t < a.ntok; t += nthr) {
-    m.gs[t] = a.gvec ? __ldcg(a.gshared + t) : 1.0f;
-    m.rms[t] = __ldcg(a.xstat + 2 * t + 1);
-    m.expo[t] = bound_exponent(__ldcg(a.xstat + 2 * t));
+  if (tid < a.ntok) {
+    m.gs[tid] = tg;
+    m.rms[tid] = tr;
+    m.expo[tid] = bound_exponent(tx);
   }
   if (a.ntok == 1) {
     // one token: its topk distinct experts are the slots, in ascending
@@ -652,27 +658,98 @@ struct EngineArgs {
 // Fill the metadata copy from the routing the gate/up kernel published, with
 // the h exponents from the max|h| accumulators (threads [0, nthr) of the CTA).
 __device__ void load_meta(const MoeArgs &a, Meta &m, int tid, int nthr) {
-  if (tid == 0) {
-    *m.nact = __ldcg(a.meta);
-    *m.nslots = __ldcg(a.meta + 1);
+  // first item of every array: all loads are issued before the first store
+  // (a store waits for its load, and issue is in order)
+  const int i = tid;
+  const int nl = m.slots * a.ntok, nw = a.ntok * a.topk, ne = a.ntok * (a.topk + 1);
+  int n0 = 0, n1 = 0, va = 0, vc = 0, vl = 0;
+  float vw = 0.0f, vg = 1.0f, vr = 0.0f;
+  unsigned vh = 0u;
+  if (i == 0) {
+    n0 = __ldcg(a.meta);
+    n1 = __ldcg(a.meta + 1);
   }
-#pragma unroll 1
-  for (int i = tid; i < m.slots; i += nthr) {
-    m.active[i] = __ldcg(a.active + i);
-    m.cnt[i] = __ldcg(a.cnt + i);
+  if (i < m.slots) {
+    va = __ldcg(a.active + i);
+    vc = __ldcg(a.cnt + i);
   }
-#pragma unroll 1
-  for (int i = tid; i < m.slots * a.ntok; i += nthr) m.list[i] = __ldcg(a.list + i);
-#pragma unroll 1
-  for (int i = tid; i < a.ntok * a.topk; i += nthr) m.w[i] = __ldcg(a.w + i);
-#pragma unroll 1
-  for (int i = tid; i < a.ntok; i += nthr) {
-    m.gs[i] = a.gvec ? __ldcg(a.gshared + i) : 1.0f;
-    m.rms[i] = __ldcg(a.xstat + 2 * i + 1);
+  if (i < nl) vl = __ldcg(a.list + i);
+  if (i < nw) vw = __ldcg(a.w + i);
+  if (i < a.ntok) {
+    if (a.gvec) vg = __ldcg(a.gshared + i);
+    vr = __ldcg(a.xstat + 2 * i + 1);
   }
+  if (i < ne) vh = __ldcg(a.hmax + i);
+  if (i == 0) {
+    *m.nact = n0;
+    *m.nslots = n1;
+  }
+  if (i < m.slots) {
+    m.active[i] = va;
+    m.cnt[i] = vc;
+  }
+  if (i < nl) m.list[i] = vl;
+  if (i < nw) m.w[i] = vw;
+  if (i < a.ntok) {
+    m.gs[i] = vg;
+    m.rms[i] = vr;
+  }
+  if (i < ne) m.expo[i] = bound_exponent(__uint_as_float(vh));
+  // the rest (large token counts only)
 #pragma unroll 1
-  for (int i = tid; i < a.ntok * (a.topk + 1); i += nthr)
-    m.expo[i] = bound_exponent(__uint_as_float(__ldcg(a.hmax + i)));
+  for (int j = tid + nthr; j < m.slots; j += nthr) {
+    m.active[j] = __ldcg(a.active + j);
+    m.cnt[j] = __ldcg(a.cnt + j);
+  }
+#pragma unroll 4
+  for (int j = tid + nthr; j < nl; j += nthr) m.list[j] = __ldcg(a.list + j);
+#pragma unroll 1
+  for (int j = tid + nthr; j < nw; j += nthr) m.w[j] = __ldcg(a.w + j);
+#pragma unroll 1
+  for (int j = tid + nthr; j < ne; j += nthr) m.expo[j] = bound_exponent(__uint_as_float(__ldcg(a.hmax + j)));
+}
+
+// h of every (token, slot) for the down kernels' shared-memory copy: the
+// float4 loads are issued first (with the routing loads), the scaling into
+// pairs waits for the exponents.  hbytes <= kHSmemMax, 512 consumers.
+constexpr int kHStage4 = kHSmemMax / 16 / kMaxConsumers;  // float4 per thread
+
+__device__ __forceinline__ void load_h(const MoeArgs &a, int n4, int tid, int lane, int nthreads,
+                                       float4 (&hv)[kHStage4]) {
+#pragma unroll
+  for (int k = 0; k < kHStage4; ++k) {
+    const int q = (tid - lane) + k * nthreads + lane;
+    hv[k] = q < n4 ? reinterpret_cast<const float4 *>(a.h)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// pair i of column c of slot vector hsi at pairs[(hsi*16 + i)*nblk + c]
+// (neighbouring threads read neighbouring pairs); scaled column sums in
+// hsum[hsi*nblk + c].  8 consecutive threads hold one 32-float column.
+template <int FMT>
+__device__ __forceinline__ void stage_h(const float4 (&hv)[kHStage4], const Meta &m, int I, int nblk, int n4, int tid,
+                                        int lane, int nthreads, f2_t *pairs, float *hsum) {
+#pragma unroll
+  for (int k = 0; k < kHStage4; ++k) {
+    const int q0 = (tid - lane) + k * nthreads;
+    if (q0 >= n4) break;  // warp-uniform; n4 is a multiple of 64
+    const int q = q0 + lane;
+    const float4 v = hv[k];
+    const int hsi = (4 * q) / I;
+    const int col = ((4 * q) - hsi * I) >> 5;
+    const int j = (4 * q) & 31;
+    const int E = m.expo[hsi];
+    float sum = (v.x + v.y) + (v.z + v.w);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    const int base = (hsi * 16 + j / 2) * nblk + col;
+    pairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
+                          scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
+    pairs[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
+                                 scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
+    if (j == 0) hsum[hsi * nblk + col] = scale_pow2(sum, -23 - E);
+  }
 }
 
 // Row reduction of one (unit, entry) for RPG partials: in-warp reduce-scatter,
@@ -930,7 +1007,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
 // h = silu(g) * u.  max|h| is reduced per CTA before one global atomic per
 // (token, slot).  NT >= ntok.
 template <int FMT, int NT>
-__global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(const EngineArgs p) {
+__global__ void __launch_bounds__(kMaxConsumers, 1) gateup_flat_kernel(const EngineArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const MoeArgs &a = p.a;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
@@ -961,24 +1038,32 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(cons
   const int nch = (a.E + 31) / 32;
   const int xwarps = nwarps - min(nwarps - 1, a.ntok * nch);
   if (warp < xwarps) {
-    const int n4 = a.ntok * H / 4;
+    const int n4 = a.ntok * H / 4;  // a multiple of 64: whole warps
+    int Ex[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) Ex[t] = t < a.ntok ? bound_exponent(__ldcg(a.xstat + 2 * t)) : 0;
+    const int stride = xwarps * 32;
 #pragma unroll 1
-    for (int q0 = tid - lane; q0 < n4; q0 += xwarps * 32) {
-      const int q = q0 + lane;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      int t = 0, col = 0, j = 0;
-      if (q < n4) {
-        v = reinterpret_cast<const float4 *>(a.x)[q];
-        t = (4 * q) / H;
-        col = ((4 * q) % H) / 32;
-        j = (4 * q) & 31;
+    for (int q0 = tid - lane; q0 < n4; q0 += 4 * stride) {
+      float4 xv[4];  // four loads in flight before the first store
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * stride + lane;
+        xv[u] = q < n4 ? reinterpret_cast<const float4 *>(a.x)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      const int E = bound_exponent(__ldcg(a.xstat + 2 * t));
-      float sum = (v.x + v.y) + (v.z + v.w);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-      if (q < n4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (q0 + u * stride >= n4) break;  // warp-uniform
+        const int q = q0 + u * stride + lane;
+        const float4 v = xv[u];
+        const int t = (4 * q) / H;
+        const int col = ((4 * q) - t * H) >> 5;
+        const int j = (4 * q) & 31;
+        const int E = t == 0 ? Ex[0] : (t == 1 ? Ex[1] : (t == 2 ? Ex[2] : Ex[3]));
+        float sum = (v.x + v.y) + (v.z + v.w);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         const int base = (t * 16 + j / 2) * nblk + col;
         xpairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
                                scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
@@ -997,9 +1082,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(cons
   uint8_t *gate_s = smem;
   uint8_t *up_s = smem + static_cast<uint32_t>(p.tile_rows) * a.gu_row_bytes;
 
-  if (tid >= nthreads) {
-    // producer: per slot segment of this CTA's rows, the gate rows and the up rows
-    if (tid == nthreads && nrows > 0) {
+  {
+    // the last thread issues, per slot segment of this CTA's rows, the gate
+    // rows and the up rows (there is no separate producer warp)
+    if (tid == nthreads - 1 && nrows > 0) {
       mbar_arrive_expect_tx(full, static_cast<uint32_t>(2 * nrows * a.gu_row_bytes));
       int64_t r0 = rb;
       const int64_t re = rb + nrows;
@@ -1017,7 +1103,6 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) gateup_flat_kernel(cons
         r0 = r1;
       }
     }
-    return;
   }
 
   const int g = tid / p.tpr, c = tid % p.tpr;
@@ -1227,46 +1312,15 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_kernel(const Engin
   Meta m(smem + p.meta_off, a.ntok, a.topk);
   const int nblk = I / 32;
   const int nh = a.ntok * (a.topk + 1);
-  if (p.stage_h) {
-    // the h lines this thread stages below, fetched while the routing loads
-    const int n4 = nh * I / 4;
-    for (int q = tid; q < n4; q += nthreads)
-      if ((q & 7) == 0 || q == tid) prefetch_l1(reinterpret_cast<const float4 *>(a.h) + q);
-  }
+  const int n4 = p.stage_h ? nh * I / 4 : 0;
+  float4 hv[kHStage4];
+  load_h(a, n4, tid, lane, nthreads, hv);  // issued together with the routing loads
   load_meta(a, m, tid, nthreads);
-  // staged h: pair i of column c of slot vector hsi at pairs[(hsi*16 + i)*nblk + c]
-  // (neighbouring threads read neighbouring pairs); scaled column sums after.
   f2_t *pairs = reinterpret_cast<f2_t *>(hs_smem);
   float *hsum = hs_smem + static_cast<int64_t>(nh) * I;  // [nh][nblk]
   named_sync(1, nthreads);  // the h exponents are in m.expo
   if (p.stage_h) {
-    // coalesced: thread q takes 4 consecutive floats; 8 consecutive threads
-    // hold one 32-float column and reduce its sum with shuffles
-    const int n4 = nh * I / 4;
-    for (int q0 = tid - lane; q0 < n4; q0 += nthreads) {
-      const int q = q0 + lane;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      int hsi = 0, col = 0, j = 0;
-      if (q < n4) {
-        v = reinterpret_cast<const float4 *>(a.h)[q];  // L1: prefetched above
-        hsi = (4 * q) / I;
-        col = ((4 * q) % I) / 32;
-        j = (4 * q) & 31;
-      }
-      const int E = m.expo[hsi];
-      float sum = (v.x + v.y) + (v.z + v.w);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-      if (q < n4) {
-        const int base = (hsi * 16 + j / 2) * nblk + col;
-        pairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
-                              scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
-        pairs[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
-                                     scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
-        if (j == 0) hsum[hsi * nblk + col] = scale_pow2(sum, -23 - E);
-      }
-    }
+    stage_h<FMT>(hv, m, I, nblk, n4, tid, lane, nthreads, pairs, hsum);
     named_sync(1, nthreads);
   }
   const int nslots = *m.nslots;
@@ -1414,38 +1468,13 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) down_flat_kernel(const 
   const int nblk = I / 32;
   const int nh = a.ntok * (a.topk + 1);
   const int n4 = nh * I / 4;
-#pragma unroll 1
-  for (int q = tid; q < n4; q += nthreads)
-    if ((q & 7) == 0 || q == tid) prefetch_l1(reinterpret_cast<const float4 *>(a.h) + q);
+  float4 hv[kHStage4];
+  load_h(a, n4, tid, lane, nthreads, hv);
   load_meta(a, m, tid, nthreads);
   f2_t *pairs = reinterpret_cast<f2_t *>(hs_smem);
   float *hsum = hs_smem + static_cast<int64_t>(nh) * I;  // [nh][nblk]
   named_sync(1, nthreads);  // the h exponents are in m.expo
-#pragma unroll 1
-  for (int q0 = tid - lane; q0 < n4; q0 += nthreads) {
-    const int q = q0 + lane;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    int hsi = 0, col = 0, j = 0;
-    if (q < n4) {
-      v = reinterpret_cast<const float4 *>(a.h)[q];  // L1: prefetched above
-      hsi = (4 * q) / I;
-      col = ((4 * q) % I) / 32;
-      j = (4 * q) & 31;
-    }
-    const int E = m.expo[hsi];
-    float sum = (v.x + v.y) + (v.z + v.w);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-    if (q < n4) {
-      const int base = (hsi * 16 + j / 2) * nblk + col;
-      pairs[base] = f2_pack(scale_pow2(v.x, 126 - E - Fmt<FMT>::shift(j)),
-                            scale_pow2(v.y, 126 - E - Fmt<FMT>::shift(j + 1)));
-      pairs[base + nblk] = f2_pack(scale_pow2(v.z, 126 - E - Fmt<FMT>::shift(j + 2)),
-                                   scale_pow2(v.w, 126 - E - Fmt<FMT>::shift(j + 3)));
-      if (j == 0) hsum[hsi * nblk + col] = scale_pow2(sum, -23 - E);
-    }
-  }
+  stage_h<FMT>(hv, m, I, nblk, n4, tid, lane, nthreads, pairs, hsum);
   named_sync(1, nthreads);
   const int nslots = *m.nslots;
 
@@ -1589,8 +1618,10 @@ cudaError_t launch_down_nt(const EngineArgs &p, int rpg, unsigned grid, uint32_t
 
 template <int FMT>
 cudaError_t launch_gateup_flat(const EngineArgs &p, unsigned grid, uint32_t smem, cudaStream_t s) {
-  if (p.a.ntok <= 1) return launch_engine(gateup_flat_kernel<FMT, 1>, p, grid, smem, s, false);
-  return launch_engine(gateup_flat_kernel<FMT, 4>, p, grid, smem, s, false);
+  auto k = p.a.ntok <= 1 ? gateup_flat_kernel<FMT, 1> : gateup_flat_kernel<FMT, 4>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3(grid), dim3(p.groups * p.tpr), smem, s, p);  // consumers only
 }
 
 template <int FMT>
