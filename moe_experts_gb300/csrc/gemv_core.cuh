@@ -81,6 +81,12 @@ __device__ __forceinline__ float f2_sum(f2_t v) {
 __device__ __forceinline__ void f2_fma(f2_t &acc, f2_t a, f2_t b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
+// acc += acc2, lane-wise (the two halves of a split accumulation)
+template <int NV>
+__device__ __forceinline__ void f2_join(f2_t (&acc)[NV], const f2_t (&acc2)[NV]) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc[v]) : "l"(acc2[v]));
+}
 
 // Activations of one 32-weight column for NV vectors, as 16 pairs each.
 template <int NV>
@@ -89,6 +95,8 @@ struct XCol {
 };
 
 // sum over one 32-bit word of 8 nibbles (weights 8i..8i+7) for NV vectors.
+// Callers alternate two accumulators between words (two independent FMA
+// chains per column).
 template <int NV>
 __device__ __forceinline__ void nib_word(uint32_t w, const XCol<NV> &x, int i, f2_t (&acc)[NV]) {
   const f2_t p01 = f2_bits(w & 0x0000000Fu, w & 0x000000F0u);
@@ -155,16 +163,17 @@ struct ColConst {
 template <int FMT, int NV>
 __device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FMT> &cc, const XCol<NV> &x,
                                            const float (&xs)[NV], float (&part)[NV]) {
-  f2_t acc[NV];
+  f2_t acc[NV], acc2[NV];
 #pragma unroll
-  for (int v = 0; v < NV; ++v) acc[v] = 0ull;
+  for (int v = 0; v < NV; ++v) acc[v] = acc2[v] = 0ull;
   if (FMT == EPQ_Q4_K) {
     const uint4 h = *reinterpret_cast<const uint4 *>(row + cc.off);
     const uint4 q = *reinterpret_cast<const uint4 *>(row + cc.qoff);
     nib_word<NV>(q.x, x, 0, acc);
-    nib_word<NV>(q.y, x, 1, acc);
+    nib_word<NV>(q.y, x, 1, acc2);
     nib_word<NV>(q.z, x, 2, acc);
-    nib_word<NV>(q.w, x, 3, acc);
+    nib_word<NV>(q.w, x, 3, acc2);
+    f2_join(acc, acc2);
     const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
     const uint32_t c6 = __funnelshift_r(cc.csel ? h.z : h.y, cc.csel ? h.w : h.z, cc.csh) & 63u;
     const uint32_t k6 = __funnelshift_r(cc.ksel ? h.w : h.z, cc.ksel ? 0u : h.w, cc.ksh) & 63u;
@@ -176,9 +185,10 @@ __device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FM
     const uint32_t *wq = reinterpret_cast<const uint32_t *>(row + cc.qoff);
     const uint32_t dm = *reinterpret_cast<const uint32_t *>(row + cc.off);
     nib_word<NV>(wq[0], x, 0, acc);
-    nib_word<NV>(wq[1], x, 1, acc);
+    nib_word<NV>(wq[1], x, 1, acc2);
     nib_word<NV>(wq[2], x, 2, acc);
-    nib_word<NV>(wq[3], x, 3, acc);
+    nib_word<NV>(wq[3], x, 3, acc2);
+    f2_join(acc, acc2);
     const float d = half_bits_to_float(dm), m = half_bits_to_float(dm >> 16);
 #pragma unroll
     for (int v = 0; v < NV; ++v) part[v] = fmaf(d, f2_sum(acc[v]), m * xs[v]);
@@ -187,9 +197,10 @@ __device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FM
     const uint32_t w0 = wq[0], w1 = wq[1], w2 = wq[2], w3 = wq[3], w4 = wq[4];
     const float d = half_bits_to_float(*reinterpret_cast<const unsigned short *>(row + cc.off));
     nib_word<NV>(__funnelshift_r(w0, w1, cc.qsh), x, 0, acc);
-    nib_word<NV>(__funnelshift_r(w1, w2, cc.qsh), x, 1, acc);
+    nib_word<NV>(__funnelshift_r(w1, w2, cc.qsh), x, 1, acc2);
     nib_word<NV>(__funnelshift_r(w2, w3, cc.qsh), x, 2, acc);
-    nib_word<NV>(__funnelshift_r(w3, w4, cc.qsh), x, 3, acc);
+    nib_word<NV>(__funnelshift_r(w3, w4, cc.qsh), x, 3, acc2);
+    f2_join(acc, acc2);
 #pragma unroll
     for (int v = 0; v < NV; ++v) part[v] = d * (f2_sum(acc[v]) - 8.0f * xs[v]);
   } else {  // Q8_0
@@ -199,7 +210,8 @@ __device__ __forceinline__ void column_dot(const uint8_t *row, const ColConst<FM
 #pragma unroll
     for (int i = 0; i < 9; ++i) w[i] = wq[i];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) byte_word<NV>(__funnelshift_r(w[i], w[i + 1], cc.qsh), x, i, acc);
+    for (int i = 0; i < 8; ++i) byte_word<NV>(__funnelshift_r(w[i], w[i + 1], cc.qsh), x, i, (i & 1) ? acc2 : acc);
+    f2_join(acc, acc2);
 #pragma unroll
     for (int v = 0; v < NV; ++v) part[v] = d * (f2_sum(acc[v]) - 128.0f * xs[v]);
   }
