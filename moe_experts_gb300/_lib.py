@@ -131,7 +131,7 @@ def epq_block_bytes(fmt: int) -> int:
     return int(load().epq_block_bytes(fmt))
 
 
-EPQ_TUNE_TILE_BYTES, EPQ_TUNE_RING_BYTES = 1, 2
+EPQ_TUNE_TILE_BYTES, EPQ_TUNE_RING_BYTES, EPQ_TUNE_GEMV_ENGINE = 1, 2, 3
 
 
 def epq_set_tuning(key: int, value: int) -> int:

@@ -66,10 +66,12 @@ unsigned *device_error_slot() {
 namespace {
 std::atomic<int> g_tile_bytes{32 * 1024};
 std::atomic<int> g_ring_bytes{180 * 1024};
+std::atomic<int> g_gemv_engine{0};
 }  // namespace
 
 int tune_tile_bytes() { return g_tile_bytes.load(std::memory_order_relaxed); }
 int tune_ring_bytes() { return g_ring_bytes.load(std::memory_order_relaxed); }
+int tune_gemv_engine() { return g_gemv_engine.load(std::memory_order_relaxed); }
 
 epq_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -104,6 +106,9 @@ int epq_set_tuning(int key, int value) {
     case EPQ_TUNE_RING_BYTES:
       if (value < 32768 || value > 200704) return -1;
       return epq::g_ring_bytes.exchange(value);
+    case EPQ_TUNE_GEMV_ENGINE:
+      if (value < 0 || value > 2) return -1;
+      return epq::g_gemv_engine.exchange(value);
   }
   return -1;
 }

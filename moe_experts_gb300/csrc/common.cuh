@@ -210,6 +210,8 @@ unsigned *device_error_slot();
 // Current tuning values (see epq_set_tuning).
 int tune_tile_bytes();
 int tune_ring_bytes();
+// 0 = automatic, 1 = CUDA-core engines only, 2 = tensor-core engine where it applies
+int tune_gemv_engine();
 
 // Record a CUDA error for epq_last_cuda_error() and return EPQ_ERR_CUDA.
 epq_status cuda_fail(cudaError_t e);

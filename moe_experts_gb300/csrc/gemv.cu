@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "gemv_core.cuh"
+#include "gemv_tc.cuh"
 
 namespace epq {
 namespace {
@@ -686,6 +687,42 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   const int64_t row_bytes = epq_row_bytes(fmt, cols);
   const int64_t rows_out = opts.swiglu ? rows / 2 : rows;
   const bool sw = opts.swiglu != 0;
+  const int xs = opts.x_ld ? static_cast<int>(opts.x_ld) : static_cast<int>(cols / xg);
+
+  // Q4_K: the tensor-core engine (two vectors per weight pass).  With one
+  // vector it is chosen for the large matrices (>= 48 MB, rows of up to 8192
+  // weights), where its lower instruction count per weight pays; the short
+  // one-vector launches keep the CUDA-core engines, whose prologue is shorter.
+  const int eng = tune_gemv_engine();
+  const bool tc_auto = nvec >= 2 || (rows * row_bytes >= (int64_t(48) << 20) && cols <= 8192);
+  TcPlan tp;
+  if (fmt == EPQ_Q4_K && eng != 1 && (eng == 2 || tc_auto) &&
+      gemv_tc_plan(row_bytes, static_cast<int>(cols), rows_out, sw, dev, &tp)) {
+    TcArgs a;
+    a.W = static_cast<const uint8_t *>(blocks);
+    a.rows_out = rows_out;
+    a.row_bytes = row_bytes;
+    a.cols = static_cast<int>(cols);
+    a.x_stride = xs;
+    a.y_stride = rows_out;
+    a.swiglu = sw ? 1 : 0;
+    a.rms = opts.rms_prenorm;
+    a.rms_eps = opts.rms_eps;
+    a.x_group = xg;
+    a.x_head_dim = opts.x_head_dim;
+    a.early_weights = opts.weights_ready ? 1 : 0;
+    a.err = err;
+    for (int v0 = 0; v0 < nvec; v0 += 2) {
+      a.nv = std::min(2, nvec - v0);
+      a.x = x + v0 * a.x_stride;
+      a.y = y + v0 * a.y_stride;
+      a.residual = opts.residual ? opts.residual + v0 * a.y_stride : nullptr;
+      const cudaError_t e = gemv_tc_launch(tp, a, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return EPQ_OK;
+  }
+
   Plan pl;
   const bool flat = flat_plan(row_bytes, static_cast<int>(cols), rows_out, sw, nvec, dev, &pl);
   if (!flat && !make_plan(row_bytes, static_cast<int>(cols), rows_out, sw, std::min(nvec, 2), dev, &pl))
@@ -707,7 +744,7 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   p.gpt = pl.gpt;
   p.stages = pl.stages;
   p.stage_bytes = pl.stage_bytes;
-  p.x_stride = opts.x_ld ? opts.x_ld : cols / xg;
+  p.x_stride = xs;
   p.y_stride = rows_out;
   p.rms = opts.rms_prenorm;
   p.rms_eps = opts.rms_eps;

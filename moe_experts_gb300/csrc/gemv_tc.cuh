@@ -1,0 +1,40 @@
+// Host interface of the tensor-core Q4_K dequant-GEMV (gemv_tc.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace epq {
+
+// Launch geometry chosen on the host for one matrix shape.
+struct TcPlan {
+  int nsb_tmpl;          // superblocks per warp (template value 1, 2 or 4)
+  bool full;             // every warp has all NSB superblocks (no bounds test)
+  int kp, nb, nbs, stages;
+  uint32_t stage_bytes, smem;
+  unsigned grid;
+};
+
+// Arguments of one launch (one or two vectors).
+struct TcArgs {
+  const uint8_t *W;
+  const float *x;
+  float *y;
+  const float *residual;
+  int64_t rows_out, row_bytes;
+  int cols, nv;
+  int64_t x_stride, y_stride;
+  int swiglu, rms;
+  float rms_eps;
+  int x_group, x_head_dim;
+  int early_weights;
+  unsigned *err;
+};
+
+// False when the shape is outside the kernel's range (cols % 256, 256..16384)
+// or the shared-memory budget cannot hold two stages.
+bool gemv_tc_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, const DeviceInfo &dev,
+                  TcPlan *pl);
+
+cudaError_t gemv_tc_launch(const TcPlan &pl, const TcArgs &a, cudaStream_t s);
+
+}  // namespace epq
