@@ -174,6 +174,51 @@ epq_status epq_gemv_ex(epq_fmt fmt, const void *blocks, const float *x, float *y
                        int64_t rows, int64_t cols, int nvec, const epq_gemv_opts *opts,
                        epq_stream_t stream);
 
+/* ---------------------------------------------------------------- GEMV chain
+ * epq_gemv_chain: a sequence of dependent dequant-GEMVs in one persistent
+ * launch -- the decode step of a dense decoder ([H] "速度上限：带宽 ÷
+ * 权重字节数": a step streams every weight once, so the bound is bandwidth /
+ * weight bytes).  Op k computes exactly what epq_gemv_ex computes with the
+ * same fields (y = [residual +] W x with the RMS pre-norm, SwiGLU and
+ * grouped-head options), and it sees every output of ops 0..k-1: x,
+ * residual and y of op k may be outputs of earlier ops.  The weights of
+ * later ops are streamed while earlier ops finish; between ops a grid-wide
+ * barrier makes the outputs visible.
+ *   fmt      EPQ_Q4_K only (EPQ_ERR_FORMAT otherwise).
+ *   ops      host array of nops (1 .. EPQ_CHAIN_MAX_OPS) descriptors; read
+ *            during the call only (it may be reused afterwards, also under
+ *            stream capture).  Per op: rows, cols as in epq_gemv (cols % 256
+ *            == 0, 256 <= cols <= 16384), blocks/x/y/residual device
+ *            pointers, 16-byte aligned; x_ld floats between the two vectors
+ *            of x (0 = the vector length).
+ *   nvec     1 or 2 (vectors per op; y and residual are [nvec][rows_out]).
+ *   ws, ws_bytes  device workspace of >= epq_gemv_chain_workspace_bytes()
+ *            bytes, 16-byte aligned, zero-filled before its first use and
+ *            not shared by chains that may run at the same time.  A call
+ *            leaves it ready for the next call; after a device-side wait
+ *            timeout (epq_device_error) zero it again.
+ * Accuracy per op as epq_gemv.  Deterministic.  The launch is cooperative
+ * (one CTA per SM, all resident): EPQ_ERR_CUDA if the device cannot host it. */
+#define EPQ_CHAIN_MAX_OPS 256
+typedef struct {
+  const void *blocks;
+  const float *x;
+  float *y;
+  const float *residual;
+  int64_t rows;
+  int64_t cols;
+  int swiglu;
+  int rms_prenorm;
+  float rms_eps;
+  int x_group;
+  int x_head_dim;
+  int64_t x_ld;
+} epq_gemv_op;
+
+size_t epq_gemv_chain_workspace_bytes(void);
+epq_status epq_gemv_chain(epq_fmt fmt, const epq_gemv_op *ops, int nops, int nvec, void *ws,
+                          size_t ws_bytes, epq_stream_t stream);
+
 /* ---------------------------------------------------------------- MoE layer
  * [F] "每层流水线" and "3. Metal 计算着色器"; shapes from [F] "模型架构" and
  * [E] "記憶體怎麼配置的".  For every token t (x_t = row t of x):

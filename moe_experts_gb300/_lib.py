@@ -39,6 +39,13 @@ class GemvOpts(ctypes.Structure):
                 ("x_ld", ctypes.c_int64), ("weights_ready", ctypes.c_int)]
 
 
+class GemvOp(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("swiglu", ctypes.c_int), ("rms_prenorm", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("x_group", ctypes.c_int), ("x_head_dim", ctypes.c_int), ("x_ld", ctypes.c_int64)]
+
+
 class Router(ctypes.Structure):
     _fields_ = [("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("n_experts", ctypes.c_int),
                 ("norm_topk", ctypes.c_int)]
@@ -92,6 +99,8 @@ def load(path: str | None = None):
         "epq_moe_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Router), ctypes.POINTER(Experts), i32, i32]),
         "epq_moe_forward": (i32, [ctypes.POINTER(Router), ctypes.POINTER(Experts), vp, i32, i32,
                                   ctypes.POINTER(MoeOpts), vp, vp, vp, vp, ctypes.c_size_t, vp]),
+        "epq_gemv_chain_workspace_bytes": (ctypes.c_size_t, []),
+        "epq_gemv_chain": (i32, [i32, ctypes.POINTER(GemvOp), i32, i32, vp, ctypes.c_size_t, vp]),
         "epq_moe_forward_noalloc": (i32, [ctypes.POINTER(Router), ctypes.POINTER(Experts), vp, i32, i32,
                                           ctypes.POINTER(MoeOpts), vp, vp, vp, vp]),
     }
@@ -205,6 +214,34 @@ def epq_gemv_ex(fmt: int, blocks: torch.Tensor, x: torch.Tensor, rows: int, cols
     _check("epq_gemv_ex", lib.epq_gemv_ex(fmt, _ptr(blocks), _ptr(x2), _ptr(y), rows, cols, nvec,
                                           ctypes.byref(o), _stream(stream)))
     return y
+
+
+EPQ_CHAIN_MAX_OPS = 256
+
+
+def epq_gemv_chain_workspace_bytes() -> int:
+    return int(load().epq_gemv_chain_workspace_bytes())
+
+
+def gemv_op(blocks: torch.Tensor, x: torch.Tensor, y: torch.Tensor, rows: int, cols: int,
+            residual: torch.Tensor | None = None, swiglu: bool = False, rms_prenorm: bool = False,
+            rms_eps: float = 0.0, x_group: int = 0, x_head_dim: int = 0) -> GemvOp:
+    """One op of epq_gemv_chain; x and y are [nvec, n] views (rows contiguous)."""
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    if x2.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    x_ld = x2.stride(0) if x2.shape[0] > 1 else 0
+    return GemvOp(_ptr(blocks), _ptr(x2), _ptr(y), residual.data_ptr() if residual is not None else None,
+                  int(rows), int(cols), int(swiglu), int(rms_prenorm), float(rms_eps), int(x_group),
+                  int(x_head_dim), int(x_ld))
+
+
+def epq_gemv_chain(fmt: int, ops: list, nvec: int, workspace: torch.Tensor, stream=None) -> None:
+    """Run the ops (GemvOp list) in order in one persistent launch."""
+    lib = load()
+    arr = (GemvOp * len(ops))(*ops)
+    _check("epq_gemv_chain", lib.epq_gemv_chain(fmt, arr, len(ops), nvec, _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 # ------------------------------------------------------------------ MoE layer
