@@ -1,16 +1,18 @@
 """Benchmark of the block-quantized decode path on GB300.
 
-Default workload (the headline): full MoE decode step with Q4_K weights --
-40 layers, hidden 2048, 256 experts (gate/up 512x2048, down 2048x512), top-8
-routed + 1 shared expert, q/k/v/o 2048x2048 Q4_K per layer, router 256x2048
-fp32 with Zipf(1.1) popularity, a 64-token decode run at batch 1.  One
-"step" = the 64-token run (64 x 40 layers of GEMVs + router/top-K + expert
-gate/up+SwiGLU + down + combine), replayed from one CUDA graph.  18.7 GB of
-packed weights stay resident; every step streams 1.1 GB per token, far
-beyond the 129 MB L2, so no flush is needed.
+Default workload (the headline): the full dense 8B-class decode step with
+Q4_K weights -- 32 layers (q 4096x4096, k/v 1024x4096, o 4096x4096, gate/up
+2x14336x4096 with SwiGLU, down 4096x14336, weightless RMS pre-norms, a
+one-token-context attention stand-in) plus the 128256x4096 LM head, batch 1
+(--nvec 2/4/8 for speculative-verify columns).  One "step" = one token
+through all 129 dequant-GEMVs, replayed from one CUDA graph.  4.2 GB of
+packed weights stay resident and every step streams all of them, far beyond
+the 129 MB L2, so no flush is needed.
 
-Other workloads (--workload): gemv4096, layer8b (per --fmt), dense8b
-(--nvec 1/2/4/8), moe_layer (--ntok 1/8).
+Other workloads (--workload): moe_decode (40 MoE layers, hidden 2048, 256
+experts of gate/up 512x2048 + down 2048x512, top-8 + shared expert, Zipf(1.1)
+routing, a 64-token decode run per step).  --chain runs the dense step as
+one epq_gemv_chain launch instead of one launch per matrix.
 
 The JSON line carries: value (tok/s for decode workloads, GB/s otherwise),
 roofline of the dominant kernel (live CUDA-event pairs inside the graph),
@@ -39,7 +41,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture of the kernel as it stands; the summary with its command is the
 # named file.  An entry must go when its kernel changes.
 NCU_TRAFFIC = {
-    "moe_gateup": (10_700_672, "profiles/moe_gateup_flat_q4k_full.md"),
+    ("moe_decode", "moe_gateup"): (10_700_672, "profiles/moe_gateup_flat_q4k_full.md"),
+    ("dense8b", "gemv_gateup"): (66_309_632, "profiles/gemv_tc_gateup_q4k_full.md"),
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -247,7 +250,7 @@ class DenseDecodeWorkload(Workload):
     name = "dense8b"
     unit = "tok/s"
 
-    def __init__(self, epq, dev, fmt, nvec=1, layers=None):
+    def __init__(self, epq, dev, fmt, nvec=1, layers=None, chain=False):
         import torch
         from synthetic import workloads as wl
         self.cfg = c = wl.DenseDecode() if layers is None else wl.DenseDecode(layers=layers)
@@ -274,23 +277,29 @@ class DenseDecodeWorkload(Workload):
         self.head = head
         torch.cuda.synchronize()
         from moe_experts_gb300.decode import DenseDecoder
-        self.model = DenseDecoder(c, fmt, self.layers, head, dev, nvec=nvec)
+        self.model = DenseDecoder(c, fmt, self.layers, head, dev, nvec=nvec, chain=chain)
+        self.chain = chain
         self.x = wl.activations("dense8b", nvec, H, dev)
         self.units_per_step = float(nvec)
         wbytes = c.layers * ((nq + 2 * nkv) * rbH + H * epq.epq_row_bytes(fmt, nq) + 2 * c.inter * rbH
                              + H * rbI) + c.vocab * rbH
         self.bytes_per_token = wbytes
-        self.kernels_per_step = c.layers * 4 + 1
-        self.kernel_bytes = {
-            "gemv_qkv": (nq + 2 * nkv) * rbH + 4 * nvec * (H + nq + 2 * nkv),
-            "gemv_o": H * epq.epq_row_bytes(fmt, nq) + 4 * nvec * (nkv + 2 * H),
-            "gemv_gateup": 2 * c.inter * rbH + 4 * nvec * (H + c.inter),
-            "gemv_down": H * rbI + 4 * nvec * (c.inter + 2 * H),
-        }
+        self.kernels_per_step = 1 if chain else c.layers * 4 + 1
+        if chain:  # the one launch is the dominant (and only) kernel
+            self.kernel_bytes = {"gemv_chain": wbytes + 4 * nvec * (c.layers * (4 * H + 2 * c.inter + nq + 2 * nkv
+                                                                                 + H) + H + c.vocab)}
+        else:
+            self.kernel_bytes = {
+                "gemv_qkv": (nq + 2 * nkv) * rbH + 4 * nvec * (H + nq + 2 * nkv),
+                "gemv_o": H * epq.epq_row_bytes(fmt, nq) + 4 * nvec * (nkv + 2 * H),
+                "gemv_gateup": 2 * c.inter * rbH + 4 * nvec * (H + c.inter),
+                "gemv_down": H * rbI + 4 * nvec * (c.inter + 2 * H),
+            }
 
     def config(self):
         c = self.cfg
         return {"workload": f"dense8b_decode_{'q4k' if self.fmt == 3 else self.fmt}", "layers": c.layers,
+                "launch": "one epq_gemv_chain launch per step" if self.chain else "one launch per matrix",
                 "hidden": c.hidden, "inter": c.inter, "heads": c.heads, "kv_heads": c.kv_heads, "vocab": c.vocab,
                 "nvec": self.nvec, "batch": 1, "weight_bytes_per_step": self.bytes_per_token,
                 "l2": "inputs larger than L2 (4.2 GB/step)"}
@@ -341,7 +350,7 @@ def run_epq(args):
     if args.workload == "moe_decode":
         W = MoEDecodeWorkload(epq, dev, fmt, layers=args.layers)
     elif args.workload == "dense8b":
-        W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers)
+        W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers, chain=args.chain)
     else:
         raise SystemExit(f"unknown workload {args.workload}")
 
@@ -354,12 +363,17 @@ def run_epq(args):
 
     # timers: CUDA event pairs around each kernel of layer 0, for every token
     timers = Timers(torch, W)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        W.step(stream, timers=timers)
+    if args.no_graph:  # direct launches (for profilers that do not follow graph replays)
+        def replay():
+            W.step(stream, timers=timers)
+    else:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            W.step(stream, timers=timers)
+        replay = g.replay
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
-            g.replay()
+            replay()
     torch.cuda.synchronize()
 
     def barrier():
@@ -375,7 +389,7 @@ def run_epq(args):
         with torch.cuda.stream(stream):  # replays and events on one stream
             e0.record(stream)
             for _ in range(args.steps):
-                g.replay()
+                replay()
             e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize()
@@ -395,14 +409,21 @@ def run_epq(args):
     out_dev = torch.empty_like(W.out if hasattr(W, "out") else W.model.logits)
     out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
     x_dev = torch.empty_like(W.x)
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=stream):
-        W.step(stream, x=x_dev, out=out_dev if hasattr(W, "out") else None)
+    if args.no_graph:
+        class _Direct:
+            def replay(self):
+                W.step(stream, x=x_dev, out=out_dev if hasattr(W, "out") else None)
+        g2 = _Direct()
+    else:
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            W.step(stream, x=x_dev, out=out_dev if hasattr(W, "out") else None)
     res_src = out_dev if hasattr(W, "out") else W.model.logits
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        g2.replay()
-        out_host.copy_(res_src, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            x_dev.copy_(x_host, non_blocking=True)
+            g2.replay()
+            out_host.copy_(res_src, non_blocking=True)
     torch.cuda.synchronize()
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
@@ -429,8 +450,8 @@ def run_epq(args):
         ach = W.kernel_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": peak_kind + " copy bandwidth",
-                "traffic": NCU_TRAFFIC[dom][0] if dom in NCU_TRAFFIC else None,
-                "traffic_source": NCU_TRAFFIC[dom][1] if dom in NCU_TRAFFIC else None,
+                "traffic": NCU_TRAFFIC[(W.name, dom)][0] if (W.name, dom) in NCU_TRAFFIC else None,
+                "traffic_source": NCU_TRAFFIC[(W.name, dom)][1] if (W.name, dom) in NCU_TRAFFIC else None,
                 "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
                 "bytes_per_launch": W.kernel_bytes[dom],
                 "all_kernels_us": {k: round(v * 1e3, 3) for k, v in kernel_ms.items()}}
@@ -529,13 +550,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="epq", choices=["epq", "reference"])
-    ap.add_argument("--workload", default="moe_decode", choices=["moe_decode", "dense8b"])
+    ap.add_argument("--workload", default="dense8b", choices=["dense8b", "moe_decode"])
+    ap.add_argument("--chain", action="store_true", help="dense step as one epq_gemv_chain launch")
     ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K"])
     ap.add_argument("--nvec", type=int, default=1)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (smaller cases)")
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each step directly (no CUDA graph)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -33,7 +33,8 @@ def _timed(timers, name, stream, on):
 
 
 class DenseDecoder:
-    """32-layer dense decoder + LM head, Q-format weights, nvec columns.
+    """32-layer dense decoder + LM head, Q-format weights, nvec columns
+    (one library call per matrix, or the whole step as one epq_gemv_chain).
 
     Per layer (h: [nvec, H] residual stream):
       qkv = Wqkv rms(h)                 (q, k, v rows concatenated)
@@ -43,17 +44,45 @@ class DenseDecoder:
     then logits = Whead rms(h).
     """
 
-    def __init__(self, cfg, fmt, layers, head, device, nvec=1):
+    def __init__(self, cfg, fmt, layers, head, device, nvec=1, chain=False):
         self.cfg, self.fmt, self.layers, self.head, self.nvec = cfg, fmt, layers, head, nvec
         H = cfg.hidden
         self.qkv = torch.empty((nvec, cfg.q_rows + 2 * cfg.kv_rows), dtype=torch.float32, device=device)
         self.m = torch.empty((nvec, cfg.inter), dtype=torch.float32, device=device)
         self.h = torch.empty((nvec, H), dtype=torch.float32, device=device)
         self.logits = torch.empty((nvec, cfg.vocab), dtype=torch.float32, device=device)
+        # chain mode: the whole step is one epq_gemv_chain launch (Q4_K, nvec <= 2)
+        self.chain = chain and fmt == L.EPQ_Q4_K and nvec <= 2
+        self.ws = torch.zeros(L.epq_gemv_chain_workspace_bytes() if self.chain else 16, dtype=torch.uint8,
+                              device=device)
+        self._ops = {}
+
+    def chain_ops(self, x):
+        """The step's ops for epq_gemv_chain (same sequence as step())."""
+        c, H = self.cfg, self.cfg.hidden
+        nq, nkv = c.q_rows, c.kv_rows
+        h = self.h
+        ops = []
+        for li, (wqkv, wo, wgu, wd) in enumerate(self.layers):
+            src = x if li == 0 else h
+            ops.append(L.gemv_op(wqkv, src, self.qkv, nq + 2 * nkv, H, rms_prenorm=True, rms_eps=c.rms_eps))
+            ops.append(L.gemv_op(wo, self.qkv[:, nq + nkv:], h, H, nq, residual=src, x_group=c.heads // c.kv_heads,
+                                 x_head_dim=c.head_dim))
+            ops.append(L.gemv_op(wgu, h, self.m, 2 * c.inter, H, swiglu=True, rms_prenorm=True, rms_eps=c.rms_eps))
+            ops.append(L.gemv_op(wd, self.m, h, H, c.inter, residual=h))
+        ops.append(L.gemv_op(self.head, h, self.logits, c.vocab, H, rms_prenorm=True, rms_eps=c.rms_eps))
+        return ops
 
     def step(self, x, stream=None, timers=None):
         """x [nvec, H] (read only) -> self.logits."""
         c, f, H = self.cfg, self.fmt, self.cfg.hidden
+        if self.chain:
+            key = x.data_ptr()
+            if key not in self._ops:
+                self._ops[key] = self.chain_ops(x)
+            with _timed(timers, "gemv_chain", stream, True):
+                L.epq_gemv_chain(f, self._ops[key], self.nvec, self.ws, stream=stream)
+            return self.logits
         nq, nkv = c.q_rows, c.kv_rows
         h = self.h
         for li, (wqkv, wo, wgu, wd) in enumerate(self.layers):
