@@ -68,6 +68,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test without the suspend hint: the thread polls (for waits that
+// are usually short and on the critical path of every thread of the CTA).
+__device__ __forceinline__ bool mbar_test_poll(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -103,6 +117,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   }
 }
 
+// Bounded parity wait that polls without suspending.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code,
+                                               unsigned where = 0) {
+  if (mbar_test_poll(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_test_poll(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(err, code, where);
+      return false;
+    }
+  }
+}
+
 // Warp-uniform bounded wait: lane 0 spins (bounded), the verdict is broadcast,
 // and on success every lane performs its own acquire of the completed phase
 // (which returns at once).  All lanes of the warp must call it.
@@ -112,6 +140,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsign
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, code, where) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) ok = mbar_wait(bar, parity, err, code, where) ? 1 : 0;
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// warp_wait that polls without suspending.
+__device__ __forceinline__ bool warp_wait_poll(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code,
+                                               unsigned where = 0) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_poll(bar, parity, err, code, where) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) ok = mbar_wait_poll(bar, parity, err, code, where) ? 1 : 0;
   return __all_sync(0xffffffffu, ok) != 0;
 }
 

@@ -50,6 +50,7 @@ struct ChainOp {
   int x_stride, y_stride;
   int cols, nsb, nbs, nst, stage0;
   int half;    // 1: 4-row stages, an 8-row block spans two of them
+  int cfg;     // warp geometry: 0 (16 k-parts, 4 superblocks), 1/3 (8, 2), 2 (8, 1)
   int rq, rr;  // CTA b owns rows [b*rq + min(b, rr), ...), rq + (b < rr) of them
   int swiglu, rms;
   float rms_eps;
@@ -81,12 +82,22 @@ __host__ __device__ inline ChainLayout chain_layout(int stages, uint32_t slot_by
   o = al16c(o + 4u * stages);
   L.area = o;  // per warp: x staging / partial sums [slot][block][row 8][vector 2][gate/up]
   o += kWarpArea * kWarps;
-  L.xs = o;  // [superblock][t 4][vector 2][sub-block pair 2]: sums of x
-  o = al16c(o + 4u * nsb_max * 16);
+  L.xs = o;  // [group][superblock][t 4][vector 2][sub-block pair 2]: sums of x
+  o = al16c(o + 4u * nsb_max * 16);  // nsb_max here: the largest groups x superblocks
   L.scratch = o;  // [warp][vector 2]: sums of squares
   o = al16c(o + 4u * 2 * kWarps);
   L.total = o;
   return L;
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(unsigned *p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
@@ -142,12 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
   __syncthreads();
   if (tid == 0)
     for (int h = 0; h < min(S, total); ++h) issue(h, h, 0);  // weights depend on nothing upstream
-  int cs = 0;         // ring slot of this warp's next stage
-  unsigned cph = 0u;  // and the parity of its fill
 
   const int g = lane >> 2, t = lane & 3;
-  const int kq = warp;  // k-part: superblocks kq, kq + 16, ...
   const int cv = t & 1;
+  uint32_t bq[kNSB][8][2];  // x operands of this warp's superblocks (the op's first NSB used)
+  float fsc[kNSB];
   uint32_t magic = kH1024;
   asm volatile("" : "+r"(magic));
   const uint32_t csel = t == 0 ? 0x10u : (t == 1 ? 0x21u : (t == 2 ? 0x43u : 0x54u));
@@ -164,14 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&cbar[0]);  // this warp's outputs of matrix k-1 are written
       if (tid == 0) {
-        if (mbar_wait(&cbar[0], par, p.err, DEVERR_RED_WAIT, k)) {
-          __threadfence();  // the CTA's outputs, visible to the whole GPU
+        if (mbar_wait_poll(&cbar[0], par, p.err, DEVERR_RED_WAIT, k)) {
+          // acq_rel at GPU scope (cumulative: it also releases the writes
+          // this thread acquired from the CTA's warps through cbar[0])
           const unsigned gen0 = ld_acquire_gpu(&p.bar[1]);
-          const unsigned old = atomicAdd(&p.bar[0], 1u);
+          const unsigned old = atom_add_acq_rel_gpu(&p.bar[0], 1u);
           if (old == gridDim.x - 1) {
-            p.bar[0] = 0u;
-            __threadfence();
-            atomicAdd(&p.bar[1], 1u);
+            st_relaxed_gpu(&p.bar[0], 0u);
+            atom_add_acq_rel_gpu(&p.bar[1], 1u);  // release: the reset precedes the new generation
           } else {
             const uint64_t t0 = globaltimer_ns();
             while (ld_acquire_gpu(&p.bar[1]) == gen0) {
@@ -181,177 +191,169 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
               }
             }
           }
-          __threadfence();
         }
         mbar_arrive(&cbar[1]);
       }
-      if (!warp_wait(&cbar[1], par, p.err, DEVERR_RED_WAIT, k)) return;
+      if (!warp_wait_poll(&cbar[1], par, p.err, DEVERR_RED_WAIT, k)) return;
     }
 
-    // ---------------------------------------------------------------- prologue
-    // this warp's x operands (see gemv_tc.cu): one global round trip, the
-    // superblock scales, sums of x per sub-block and of x^2
-    const XGather xg{op.x_group, op.x_head_dim};
-    uint32_t bq[kNSB][8][2];
-    float fsc[kNSB];
-    {
-      uint2 *frag = reinterpret_cast<uint2 *>(area);
-      const int sub = lane >> 2, wi = lane & 3;
-      const int tp = sub >> 1, jj = 4 * (sub & 1) + wi;
-      float4 xr[kNSB][2][2];
+    // ---------------------------------------------------------------- the op
+    // prologue and stages, compiled per warp geometry (KP warps per 8-row
+    // block, NB = 16/KP groups alternating stages, NSB superblocks per warp)
+    auto run = [&](auto kp_tag, auto nsb_tag, auto full_tag) -> bool {
+      constexpr int KP = decltype(kp_tag)::value;
+      constexpr int NSB = decltype(nsb_tag)::value;
+      constexpr bool FULL = decltype(full_tag)::value;
+      constexpr int NB = kWarps / KP;
+      const int kq = warp % KP, grp = warp / KP;
+      const XGather xg{op.x_group, op.x_head_dim};
+      const int o_nsb = op.nsb;
+      float *gxsum = xsum + grp * o_nsb * 16;
+      uint32_t(&bqn)[NSB][8][2] = reinterpret_cast<uint32_t(&)[NSB][8][2]>(bq);
+      float(&fscn)[NSB] = reinterpret_cast<float(&)[NSB]>(fsc);
+      // x operands of this warp's superblocks (see gemv_tc.cu): one global
+      // round trip, the superblock scales, sums of x per sub-block and of x^2
+      {
+        uint2 *frag = reinterpret_cast<uint2 *>(area);
+        const int sub = lane >> 2, wi = lane & 3;
+        const int tp = sub >> 1, jj = 4 * (sub & 1) + wi;
+        float4 xr[NSB][2][2];
 #pragma unroll
-      for (int i = 0; i < kNSB; ++i) {
-        const int sb = kq + i * kKP;
+        for (int i = 0; i < NSB; ++i) {
+          const int sb = kq + i * KP;
 #pragma unroll
-        for (int v = 0; v < 2; ++v) {
-          xr[i][v][0] = xr[i][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (sb < op.nsb && v < p.nv) {
-            const float *src = op.x + v * op.x_stride + xg.src(256 * sb + 8 * lane);
-            xr[i][v][0] = *reinterpret_cast<const float4 *>(src);
-            xr[i][v][1] = *reinterpret_cast<const float4 *>(src + 4);
-          }
-        }
-      }
-      float ssq[2] = {0.0f, 0.0f};
-#pragma unroll
-      for (int i = 0; i < kNSB; ++i) {
-        const int sb = kq + i * kKP;
-        if (sb >= op.nsb) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) bq[i][j][0] = bq[i][j][1] = 0u;
-          fsc[i] = 0.0f;
-          continue;
-        }
-        float fs[2] = {0.0f, 0.0f};
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-          const float q0[8] = {xr[i][v][0].x, xr[i][v][0].y, xr[i][v][0].z, xr[i][v][0].w,
-                               xr[i][v][1].x, xr[i][v][1].y, xr[i][v][1].z, xr[i][v][1].w};
-          float amax = 0.0f, s8 = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            amax = fmaxf(amax, fabsf(q0[e]));
-            ssq[v] = fmaf(q0[e], q0[e], ssq[v]);
-            s8 += q0[e];
-          }
-          amax = warp_max_all(amax);
-          s8 += __shfl_xor_sync(0xffffffffu, s8, 1);
-          s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
-          if (wi == 0) xsum[((sb * 4 + tp) * 2 + v) * 2 + (sub & 1)] = s8;
-          const int sig = min(126, max(-112, 15 - bound_exponent(amax)));
-          fs[v] = exp2i(14 - sig);
-          const float up = exp2i(sig);
-          float q[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) q[e] = q0[e] * up;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint2 hi, lo;
-            hi.x = split_pair(q[h], q[h + 4], false);
-            lo.x = split_pair(q[h], q[h + 4], true);
-            hi.y = split_pair(q[h + 2], q[h + 6], false);
-            lo.y = split_pair(q[h + 2], q[h + 6], true);
-            const int l0 = 4 * (4 * h + 2 * v) + tp;
-            frag[jj * 32 + l0] = hi;
-            frag[jj * 32 + l0 + 4] = lo;
-          }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint2 r = frag[j * 32 + lane];
-          bq[i][j][0] = r.x;
-          bq[i][j][1] = r.y;
-        }
-        fsc[i] = cv ? fs[1] : fs[0];
-        __syncwarp();
-      }
-      const float s0 = warp_sum_xor<32>(ssq[0]), s1 = warp_sum_xor<32>(ssq[1]);
-      if (lane == 0) {
-        scratch[warp * 2] = s0;
-        scratch[warp * 2 + 1] = s1;
-      }
-      __syncwarp();
-    }
-
-    // ---------------------------------------------------------------- stages
-    const int rb = bx * op.rq + min(bx, op.rr);
-    const int re = rb + op.rq + (bx < op.rr ? 1 : 0);
-    const int nblocks = (re - rb + 7) / 8;
-    // the op's fields in registers (the descriptor table is in parameter space)
-    const int o_half = op.half, o_nbs = op.nbs, o_nst = op.nst, o_stage0 = op.stage0, o_nsb = op.nsb;
-    const int M = op.swiglu ? 2 : 1;
-    const uint32_t rbytes = static_cast<uint32_t>(op.row_bytes);
-    const int step = o_half ? 2 : 1;       // stages per pass of the loop
-    const int bps = o_half ? 1 : o_nbs;    // 8-row blocks per pass
-    const int T = o_half ? 4 : 8 * o_nbs;  // rows per stage
-    const bool narrow = o_nsb == kKP;      // one superblock per warp
-    float *myred = reinterpret_cast<float *>(area);  // [slot][block][row][vector][gate/up]
-    // the stage loop, compiled once for one superblock per warp (no bounds
-    // tests) and once for up to four
-    auto stages = [&](auto narrow_tag) -> bool {
-      constexpr bool NARROW = decltype(narrow_tag)::value;
-    for (int i = 0; i < o_nst; i += step) {
-      const int h = o_stage0 + i;
-      const int s = cs;
-      const int s2 = step == 2 ? (cs + 1 == S ? 0 : cs + 1) : cs;  // the pass's last slot
-      bool ok = warp_wait(&full[s], cph, p.err, DEVERR_FULL_WAIT, h);
-      if (ok && step == 2) ok = warp_wait(&full[s2], s2 == 0 ? cph ^ 1u : cph, p.err, DEVERR_FULL_WAIT, h + 1);
-      if (!ok) {
-        if (lane == 0)
-          for (int j = h + 1, sj = s + 1 == S ? 0 : s + 1, pj = s + 1 == S ? cph ^ 1u : cph; j < min(total, h + S);
-               ++j) {
-            mbar_wait(&full[sj], pj, p.err, DEVERR_DRAIN_WAIT, j);
-            if (++sj == S) {
-              sj = 0;
-              pj ^= 1u;
+          for (int v = 0; v < 2; ++v) {
+            xr[i][v][0] = xr[i][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if ((FULL || sb < o_nsb) && v < p.nv) {
+              const float *src = op.x + v * op.x_stride + xg.src(256 * sb + 8 * lane);
+              xr[i][v][0] = *reinterpret_cast<const float4 *>(src);
+              xr[i][v][1] = *reinterpret_cast<const float4 *>(src + 4);
             }
           }
-        return false;
-      }
-      // this lane's row g: stage s (rows 0..T-1 of the pass) or, in 4-row
-      // stages, rows 4..7 of the block from the next slot
-      const uint8_t *sb0 = smem + static_cast<uint32_t>(s) * p.slot_bytes;
-      const uint8_t *sb1 = smem + static_cast<uint32_t>(s2) * p.slot_bytes;
-      const int blk0 = o_half ? i / 2 : i * o_nbs;  // first 8-row block of the pass
-      const int nbl = max(0, min(bps, nblocks - blk0));
-      for (int bi = 0; bi < nbl; ++bi) {
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          if (m == 1 && M == 1) break;
-          float acc = 0.0f, am0 = 0.0f, am1 = 0.0f;
-          const uint8_t *row = o_half ? (g < 4 ? sb0 + static_cast<uint32_t>(m * T + g) * rbytes
-                                               : sb1 + static_cast<uint32_t>(m * T + g - 4) * rbytes)
-                                      : sb0 + static_cast<uint32_t>(m * T + 8 * bi + g) * rbytes;
-          if (NARROW)
-            block_dot<kKP, 1, true>(row, kq, o_nsb, t, magic, csel, ksel, nsh,
-                                    reinterpret_cast<const uint32_t(&)[1][8][2]>(bq),
-                                    reinterpret_cast<const float(&)[1]>(fsc), xsum, acc, am0, am1);
-          else
-            block_dot<kKP, kNSB, false>(row, kq, o_nsb, t, magic, csel, ksel, nsh, bq, fsc, xsum, acc, am0, am1);
-          float p0 = (cv == 0 ? acc : 0.0f) - am0;
-          float p1 = (cv == 1 ? acc : 0.0f) - am1;
-          p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-          p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-          p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-          p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-          if (t < 2) myred[(((s2 * kMaxNbs + bi) * 8 + g) * 2 + t) * 2 + m] = t == 0 ? p0 : p1;
         }
-      }
-      __syncwarp();
-      for (int u = 0; u < step; ++u) {
-        const int su = u == 0 ? s : s2;
-        unsigned old = 0u;
-        if (lane == 0) old = atom_add_acq_rel(&cnt[su], 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
+        float ssq[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < NSB; ++i) {
+          const int sb = kq + i * KP;
+          if (!FULL && sb >= o_nsb) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bqn[i][j][0] = bqn[i][j][1] = 0u;
+            fscn[i] = 0.0f;
+            continue;
+          }
+          float fs[2] = {0.0f, 0.0f};
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const float q0[8] = {xr[i][v][0].x, xr[i][v][0].y, xr[i][v][0].z, xr[i][v][0].w,
+                                 xr[i][v][1].x, xr[i][v][1].y, xr[i][v][1].z, xr[i][v][1].w};
+            float amax = 0.0f, s8 = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              amax = fmaxf(amax, fabsf(q0[e]));
+              ssq[v] = fmaf(q0[e], q0[e], ssq[v]);
+              s8 += q0[e];
+            }
+            amax = warp_max_all(amax);
+            s8 += __shfl_xor_sync(0xffffffffu, s8, 1);
+            s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
+            if (wi == 0) gxsum[((sb * 4 + tp) * 2 + v) * 2 + (sub & 1)] = s8;
+            const int sig = min(126, max(-112, 15 - bound_exponent(amax)));
+            fs[v] = exp2i(14 - sig);
+            const float up = exp2i(sig);
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = q0[e] * up;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint2 hi, lo;
+              hi.x = split_pair(q[h], q[h + 4], false);
+              lo.x = split_pair(q[h], q[h + 4], true);
+              hi.y = split_pair(q[h + 2], q[h + 6], false);
+              lo.y = split_pair(q[h + 2], q[h + 6], true);
+              const int l0 = 4 * (4 * h + 2 * v) + tp;
+              frag[jj * 32 + l0] = hi;
+              frag[jj * 32 + l0 + 4] = lo;
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint2 r = frag[j * 32 + lane];
+            bqn[i][j][0] = r.x;
+            bqn[i][j][1] = r.y;
+          }
+          fscn[i] = cv ? fs[1] : fs[0];
+          __syncwarp();
+        }
+        const float s0 = warp_sum_xor<32>(ssq[0]), s1 = warp_sum_xor<32>(ssq[1]);
+        if (lane == 0) {
+          scratch[warp * 2] = s0;
+          scratch[warp * 2 + 1] = s1;
+        }
         __syncwarp();
-        if (((old + 1u) & (kWarps - 1)) == 0u) {
-          // last warp on this slot; on the pass's last slot it writes the outputs
-          if (u == step - 1) {
+      }
+
+      // stages of this group: h = stage0 + grp + j*NB (4-row stages only
+      // with NB == 1, where a pass takes two consecutive stages)
+      const int rb = bx * op.rq + min(bx, op.rr);
+      const int re = rb + op.rq + (bx < op.rr ? 1 : 0);
+      const int nblocks = (re - rb + 7) / 8;
+      const int o_half = op.half, o_nbs = op.nbs, o_nst = op.nst, o_stage0 = op.stage0;
+      const int M = op.swiglu ? 2 : 1;
+      const uint32_t rbytes = static_cast<uint32_t>(op.row_bytes);
+      const int step = o_half ? 2 : NB;       // stages per pass (of the whole CTA)
+      const int bps = o_half ? 1 : o_nbs;     // 8-row blocks per stage pass
+      const int T = o_half ? 4 : 8 * o_nbs;   // rows per stage
+      float *myred = reinterpret_cast<float *>(area);  // [slot][block][row][vector][gate/up]
+      // ring position of this warp's first stage
+      int h = o_stage0 + (o_half ? 0 : grp);
+      int cs = h % S;
+      unsigned cph = static_cast<unsigned>(h / S) & 1u;
+      for (; h < o_stage0 + o_nst; h += step) {
+        const int s = cs;
+        const int s2 = o_half ? (cs + 1 == S ? 0 : cs + 1) : cs;
+        bool ok = warp_wait_poll(&full[s], cph, p.err, DEVERR_FULL_WAIT, h);
+        if (ok && o_half) ok = warp_wait_poll(&full[s2], s2 == 0 ? cph ^ 1u : cph, p.err, DEVERR_FULL_WAIT, h + 1);
+        if (!ok) return false;
+        const uint8_t *sb0 = smem + static_cast<uint32_t>(s) * p.slot_bytes;
+        const uint8_t *sb1 = smem + static_cast<uint32_t>(s2) * p.slot_bytes;
+        const int i = h - o_stage0;
+        const int blk0 = o_half ? i / 2 : i * o_nbs;  // first 8-row block of the stage
+        const int nbl = max(0, min(bps, nblocks - blk0));
+        for (int bi = 0; bi < nbl; ++bi) {
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            if (m == 1 && M == 1) break;
+            float acc = 0.0f, am0 = 0.0f, am1 = 0.0f;
+            const uint8_t *row = o_half ? (g < 4 ? sb0 + static_cast<uint32_t>(m * T + g) * rbytes
+                                                 : sb1 + static_cast<uint32_t>(m * T + g - 4) * rbytes)
+                                        : sb0 + static_cast<uint32_t>(m * T + 8 * bi + g) * rbytes;
+            block_dot<KP, NSB, FULL>(row, kq, o_nsb, t, magic, csel, ksel, nsh, bqn, fscn, gxsum, acc, am0, am1);
+            float p0 = (cv == 0 ? acc : 0.0f) - am0;
+            float p1 = (cv == 1 ? acc : 0.0f) - am1;
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+            if (t < 2) myred[(((s2 * kMaxNbs + bi) * 8 + g) * 2 + t) * 2 + m] = t == 0 ? p0 : p1;
+          }
+        }
+        __syncwarp();
+        const int nsl = o_half ? 2 : 1;
+        for (int u = 0; u < nsl; ++u) {
+          const int su = u == 0 ? s : s2;
+          unsigned old = 0u;
+          if (lane == 0) old = atom_add_acq_rel(&cnt[su], 1u);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          __syncwarp();
+          if (old + 1u != static_cast<unsigned>(KP)) continue;
+          // last warp of the group on this slot; on the pass's last slot it
+          // writes the outputs; then it resets the count and refills the slot
+          if (u == nsl - 1) {
             float osc0 = 1.0f, osc1 = 1.0f;
             if (op.rms) {
               float q0 = 0.0f, q1 = 0.0f;
-              for (int w = 0; w < kWarps; ++w) {
+              for (int w = grp * KP; w < grp * KP + KP; ++w) {
                 q0 += scratch[w * 2];
                 q1 += scratch[w * 2 + 1];
               }
@@ -363,13 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
               const int row = rb + 8 * (blk0 + bi) + gg;
               if (row < re && v < p.nv) {
                 float sg = 0.0f, su2 = 0.0f;
-                const float *r = reinterpret_cast<const float *>(smem + L.area) +
+                const float *r = reinterpret_cast<const float *>(smem + L.area + grp * KP * kWarpArea) +
                                  (((s2 * kMaxNbs + bi) * 8 + gg) * 2 + v) * 2;
 #pragma unroll
-                for (int q = 0; q < kWarps; ++q) sg += r[q * (kWarpArea / 4)];
+                for (int q = 0; q < KP; ++q) sg += r[q * (kWarpArea / 4)];
                 if (M == 2) {
 #pragma unroll
-                  for (int q = 0; q < kWarps; ++q) su2 += r[q * (kWarpArea / 4) + 1];
+                  for (int q = 0; q < KP; ++q) su2 += r[q * (kWarpArea / 4) + 1];
                 }
                 const float os = v ? osc1 : osc0;
                 float val = sg * os;
@@ -380,22 +382,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
             }
             __syncwarp();
           }
-          if (lane == 0 && h + u + S < total) {
-            fence_proxy_async();  // this CTA's reads of the slot precede the refill
-            issue(h + u + S, su, k);
+          if (lane == 0) {
+            cnt[su] = 0u;  // the slot's next users arrive only after its refill
+            if (h + u + S < total) {
+              fence_proxy_async();  // this CTA's reads of the slot precede the refill
+              issue(h + u + S, su, k);
+            }
           }
         }
-      }
-      // advance this warp's ring position by the pass's stages
-      for (int u = 0; u < step; ++u)
-        if (++cs == S) {
-          cs = 0;
+        // advance by the pass's stages
+        cs += step;
+        while (cs >= S) {
+          cs -= S;
           cph ^= 1u;
         }
-    }
+      }
       return true;
     };
-    if (!(narrow ? stages(std::true_type{}) : stages(std::false_type{}))) return;
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
+    using I4 = std::integral_constant<int, 4>;
+    using I8 = std::integral_constant<int, 8>;
+    using I16 = std::integral_constant<int, 16>;
+    bool ok = true;
+    switch (op.cfg) {
+      case 0: ok = run(I16{}, I4{}, std::false_type{}); break;   // 17..64 superblocks
+      case 1: ok = run(I8{}, I2{}, std::true_type{}); break;     // 16 superblocks
+      case 2: ok = run(I8{}, I1{}, std::false_type{}); break;    // 1..8 superblocks
+      case 3: ok = run(I8{}, I2{}, std::false_type{}); break;    // 9..15 superblocks
+      default: ok = run(I16{}, I2{}, std::false_type{}); break;  // (unused)
+    }
+    if (!ok) {
+      // leave no copy in flight into this CTA's shared memory (bounded waits)
+      if (lane == 0)
+        for (int j = 0; j < S; ++j) mbar_wait(&full[j], 0u, p.err, DEVERR_DRAIN_WAIT, j);
+      return;
+    }
   }
 }
 
@@ -446,7 +468,8 @@ extern "C" epq_status epq_gemv_chain(epq_fmt fmt, const epq_gemv_op *ops, int no
     if (o.x_ld < 0 || o.x_ld > (int64_t(1) << 30) || (o.x_ld && (o.x_ld % 4 || o.x_ld < o.cols / xg)))
       return EPQ_ERR_ARG;
     slot = std::max<int64_t>(slot, (o.swiglu ? 16 : 4) * epq_row_bytes(fmt, o.cols));
-    nsb_max = std::max(nsb_max, static_cast<int>(o.cols / 256));
+    // sums of x: one copy per warp group (two groups below 17 superblocks)
+    nsb_max = std::max(nsb_max, static_cast<int>(o.cols / 256) * (o.cols / 256 > 16 ? 1 : 2));
   }
   slot = (slot + 15) & ~int64_t(15);
   // partial sums of every slot fit each warp's area: stages * 3 blocks * 32 floats
@@ -480,7 +503,8 @@ extern "C" epq_status epq_gemv_chain(epq_fmt fmt, const epq_gemv_op *ops, int no
     const int64_t rows_cta = (rows_out + grid - 1) / grid;
     c.rq = static_cast<int>(rows_out / grid);
     c.rr = static_cast<int>(rows_out % grid);
-    c.half = block > slot ? 1 : 0;
+    c.cfg = c.nsb > 16 ? 0 : (c.nsb == 16 ? 1 : (c.nsb <= 8 ? 2 : 3));
+    c.half = block > slot ? 1 : 0;  // only rows of > 16 superblocks (cfg 0, one group)
     c.nbs = c.half ? 1 : static_cast<int>(std::min<int64_t>(kMaxNbs, slot / block));
     c.nst = c.half ? static_cast<int>(2 * ((rows_cta + 7) / 8))
                    : static_cast<int>(((rows_cta + 7) / 8 + c.nbs - 1) / c.nbs);
