@@ -283,7 +283,8 @@ class DenseDecodeWorkload(Workload):
         self.units_per_step = float(nvec)
         wbytes = c.layers * ((nq + 2 * nkv) * rbH + H * epq.epq_row_bytes(fmt, nq) + 2 * c.inter * rbH
                              + H * rbI) + c.vocab * rbH
-        self.bytes_per_token = wbytes
+        self.weight_bytes_per_step = wbytes
+        self.bytes_per_token = wbytes / nvec  # one weight pass serves all nvec columns
         self.kernels_per_step = 1 if chain else c.layers * 4 + 1
         if chain:  # the one launch is the dominant (and only) kernel
             self.kernel_bytes = {"gemv_chain": wbytes + 4 * nvec * (c.layers * (4 * H + 2 * c.inter + nq + 2 * nkv
@@ -301,7 +302,7 @@ class DenseDecodeWorkload(Workload):
         return {"workload": f"dense8b_decode_{'q4k' if self.fmt == 3 else self.fmt}", "layers": c.layers,
                 "launch": "one epq_gemv_chain launch per step" if self.chain else "one launch per matrix",
                 "hidden": c.hidden, "inter": c.inter, "heads": c.heads, "kv_heads": c.kv_heads, "vocab": c.vocab,
-                "nvec": self.nvec, "batch": 1, "weight_bytes_per_step": self.bytes_per_token,
+                "nvec": self.nvec, "batch": 1, "weight_bytes_per_step": self.weight_bytes_per_step,
                 "l2": "inputs larger than L2 (4.2 GB/step)"}
 
     def step(self, stream, x=None, out=None, timers=None):

@@ -712,6 +712,14 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
     a.x_head_dim = opts.x_head_dim;
     a.early_weights = opts.weights_ready ? 1 : 0;
     a.err = err;
+    if (nvec > 2) {  // all vectors in one weight pass where the shape allows
+      a.x = x;
+      a.y = y;
+      a.residual = opts.residual;
+      a.nv = nvec;
+      cudaError_t e = cudaSuccess;
+      if (gemv_tc_multi_launch(a, nvec, dev, s, &e)) return e == cudaSuccess ? EPQ_OK : cuda_fail(e);
+    }
     for (int v0 = 0; v0 < nvec; v0 += 2) {
       a.nv = std::min(2, nvec - v0);
       a.x = x + v0 * a.x_stride;

@@ -37,4 +37,8 @@ bool gemv_tc_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, co
 
 cudaError_t gemv_tc_launch(const TcPlan &pl, const TcArgs &a, cudaStream_t s);
 
+// 3..8 vectors in one weight pass (rows of 4096 weights); false when the
+// shape is not covered (the caller then runs one pass per vector pair).
+bool gemv_tc_multi_launch(const TcArgs &a, int nvec, const DeviceInfo &dev, cudaStream_t s, cudaError_t *err);
+
 }  // namespace epq

@@ -161,3 +161,53 @@ def test_tc_full_size_sampled(tc_engine, cuda_dev):
         _check(y[:, idx.to(cuda_dev)].cpu().numpy(), oracle.gemv_f64(Q4K, packed, xs, cols),
                oracle.gemv_bound(Q4K, packed, xs, cols), what=f"full {rows}x{cols}")
         del W, blocks
+
+
+@pytest.mark.parametrize("nvec", [3, 4, 5, 8])
+@pytest.mark.parametrize("rows", [1, 9, 1234])
+def test_tc_multi_vector_one_pass(tc_engine, cuda_dev, nvec, rows):
+    """3..8 vectors over 4096-column rows share one weight pass."""
+    cols = 4096
+    W = synthetic.student_t((rows, cols), seed=rows + nvec, device=cuda_dev)
+    blocks = tc_engine.epq_quantize(Q4K, W)
+    x = synthetic.normal((nvec, cols), seed=7 + nvec).numpy()
+    x = (x * np.float32(4.0) ** np.arange(nvec, dtype=np.float32)[:, None]).astype(np.float32)
+    y = tc_engine.epq_gemv(Q4K, blocks, torch.from_numpy(x).to(cuda_dev), rows, cols).cpu().numpy()
+    packed = blocks.cpu().numpy()
+    _check(y, oracle.gemv_f64(Q4K, packed, x, cols), oracle.gemv_bound(Q4K, packed, x, cols),
+           what=f"{rows} rows nvec={nvec}")
+
+
+@pytest.mark.parametrize("nvec", [4, 8])
+def test_tc_multi_vector_options(tc_engine, cuda_dev, nvec):
+    """SwiGLU pairs, residual + RMS pre-norm and grouped heads with 4 and 8 vectors."""
+    cols, I, rows, eps = 4096, 700, 500, 1e-6
+    # SwiGLU
+    W = synthetic.student_t((2 * I, cols), seed=41).numpy()
+    packed = oracle.quantize(Q4K, W)
+    x = synthetic.normal((nvec, cols), seed=42).numpy()
+    h = tc_engine.epq_gemv_ex(Q4K, torch.from_numpy(packed).to(cuda_dev), torch.from_numpy(x).to(cuda_dev),
+                              2 * I, cols, swiglu=True).cpu().numpy()
+    y = oracle.gemv_f64(Q4K, packed, x, cols)
+    A = oracle.gemv_bound(Q4K, packed, x, cols)
+    g, u, Ag, Au = y[:, :I], y[:, I:], A[:, :I], A[:, I:]
+    silu = g / (1 + np.exp(-g))
+    bound = TOL * (1.1 * Ag * np.abs(u) + np.abs(silu) * Au) + 1e-6 * np.abs(silu * u)
+    assert (np.abs(h - silu * u) <= bound + 1e-30).all()
+    # residual (in place) + RMS pre-norm
+    W = synthetic.student_t((rows, cols), seed=43).numpy()
+    packed = oracle.quantize(Q4K, W)
+    res = synthetic.normal((nvec, rows), seed=44).numpy()
+    yt = torch.from_numpy(res).to(cuda_dev).clone()
+    tc_engine.epq_gemv_ex(Q4K, torch.from_numpy(packed).to(cuda_dev), torch.from_numpy(x).to(cuda_dev), rows, cols,
+                          y=yt, residual=yt, rms_prenorm=True, rms_eps=eps)
+    xn = oracle.rmsnorm_f64(x, eps)
+    _check(yt.cpu().numpy(), res + oracle.gemv_f64(Q4K, packed, xn, cols),
+           oracle.gemv_bound(Q4K, packed, xn, cols) + np.abs(res), what="residual+prenorm")
+    # grouped heads
+    hd, grp = 128, 4
+    v = synthetic.normal((nvec, cols // grp), seed=45).numpy()
+    xe = np.concatenate([np.tile(v[:, k * hd:(k + 1) * hd], (1, grp)) for k in range(cols // grp // hd)], axis=1)
+    yg = tc_engine.epq_gemv_ex(Q4K, torch.from_numpy(packed).to(cuda_dev), torch.from_numpy(v).to(cuda_dev), rows,
+                               cols, x_group=grp, x_head_dim=hd).cpu().numpy()
+    _check(yg, oracle.gemv_f64(Q4K, packed, xe, cols), oracle.gemv_bound(Q4K, packed, xe, cols), what="grouped")
