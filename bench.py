@@ -328,7 +328,7 @@ class DenseDecodeWorkload(Workload):
         dt = time.perf_counter() - t0
         # scale by bytes: the sample covered qkv + gate/up of `done` layers
         rate = nbytes / dt
-        return self.nvec * rate / self.bytes_per_token, \
+        return rate / self.bytes_per_token, \
             f"{done} layers' qkv+gate/up GEMVs (oracle, float64), scaled by bytes to the full step"
 
 
