@@ -129,7 +129,12 @@ epq_status epq_dequantize(epq_fmt fmt, const void *blocks, int64_t rows, int64_t
  *   y[v][i] = sum_j deq(W)[i][j] * x[v][j], accumulated in float32.
  * Accuracy: |y - y_ref| <= 1e-4 * sum_j |deq(W)[i][j] x[v][j]| (float64 ref).
  * The entries of x must be finite with max|x| < 2^100; entries more than
- * about 2^100 below max|x| count as zero.
+ * about 2^100 below max|x| count as zero.  Q4_K through the tensor-core
+ * engine (see EPQ_TUNE_GEMV_ENGINE): x is split into fp16 hi + lo parts
+ * scaled per 256-column block, so entries more than about 2^38 below the
+ * largest |x| of their 256-column block keep less precision (their fp16
+ * parts become subnormal); the bound can fail only for inputs whose tiny
+ * entries carry the result. */
  * Requirements: 1 <= nvec <= 8, rows >= 1, cols % 256 == 0 and
  * 256 <= cols <= 16384 (EPQ_ERR_SHAPE), blocks/x/y 16-byte aligned.
  * y must not overlap x or blocks. */
