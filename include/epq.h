@@ -134,7 +134,7 @@ epq_status epq_dequantize(epq_fmt fmt, const void *blocks, int64_t rows, int64_t
  * scaled per 256-column block, so entries more than about 2^38 below the
  * largest |x| of their 256-column block keep less precision (their fp16
  * parts become subnormal); the bound can fail only for inputs whose tiny
- * entries carry the result. */
+ * entries carry the result.
  * Requirements: 1 <= nvec <= 8, rows >= 1, cols % 256 == 0 and
  * 256 <= cols <= 16384 (EPQ_ERR_SHAPE), blocks/x/y 16-byte aligned.
  * y must not overlap x or blocks. */
