@@ -39,7 +39,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kKP = 16;   // warps per 8-row block (k-parts)
 constexpr int kNSB = 4;   // superblocks per warp: rows of up to 64 superblocks
 constexpr int kMaxNbs = 3;
-constexpr uint32_t kWarpArea = 2048;  // per-warp staging (prologue) / partial sums (stages)
+constexpr uint32_t kWarpArea = kFragWarpBytes;  // per-warp staging (prologue) / partial sums (stages)
 
 struct ChainOp {
   const uint8_t *W;
@@ -219,16 +219,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
         const int tp = sub >> 1, jj = 4 * (sub & 1) + wi;
         float4 xr[NSB][2][2];
 #pragma unroll
-        for (int i = 0; i < NSB; ++i) {
-          const int sb = kq + i * KP;
+        for (int v = 0; v < 2; ++v) {
+          if (v < p.nv) {
+            const float *xv = op.x + v * op.x_stride;
 #pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            xr[i][v][0] = xr[i][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if ((FULL || sb < o_nsb) && v < p.nv) {
-              const float *src = op.x + v * op.x_stride + xg.src(256 * sb + 8 * lane);
+            for (int i = 0; i < NSB; ++i) {
+              const int sb = FULL ? kq + i * KP : min(kq + i * KP, o_nsb - 1);
+              const float *src = xv + xg.src(256 * sb + 8 * lane);
+              // written by the previous op of this launch: coherent loads
               xr[i][v][0] = *reinterpret_cast<const float4 *>(src);
               xr[i][v][1] = *reinterpret_cast<const float4 *>(src + 4);
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < NSB; ++i) xr[i][v][0] = xr[i][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
         float ssq[2] = {0.0f, 0.0f};
@@ -244,6 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
           float fs[2] = {0.0f, 0.0f};
 #pragma unroll
           for (int v = 0; v < 2; ++v) {
+            if (v >= p.nv) {  // no such vector: zero operands, nothing to convert
+              if (wi == 0) gxsum[((sb * 4 + tp) * 2 + v) * 2 + (sub & 1)] = 0.0f;
+              fs[v] = 0.0f;
+            #pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int l0 = 4 * (4 * h + 2 * v) + tp;
+                frag[jj * kFragRow + l0] = frag[jj * kFragRow + l0 + 4] = make_uint2(0u, 0u);
+              }
+              continue;
+            }
             const float q0[8] = {xr[i][v][0].x, xr[i][v][0].y, xr[i][v][0].z, xr[i][v][0].w,
                                  xr[i][v][1].x, xr[i][v][1].y, xr[i][v][1].z, xr[i][v][1].w};
             float amax = 0.0f, s8 = 0.0f;
@@ -271,14 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
               hi.y = split_pair(q[h + 2], q[h + 6], false);
               lo.y = split_pair(q[h + 2], q[h + 6], true);
               const int l0 = 4 * (4 * h + 2 * v) + tp;
-              frag[jj * 32 + l0] = hi;
-              frag[jj * 32 + l0 + 4] = lo;
+              frag[jj * kFragRow + l0] = hi;
+              frag[jj * kFragRow + l0 + 4] = lo;
             }
           }
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint2 r = frag[j * 32 + lane];
+            const uint2 r = frag[j * kFragRow + lane];
             bqn[i][j][0] = r.x;
             bqn[i][j][1] = r.y;
           }

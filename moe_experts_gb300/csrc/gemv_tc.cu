@@ -109,7 +109,7 @@ __host__ __device__ inline TcLayout tc_layout(int stages, uint32_t stage_bytes, 
   // per-warp staging of one superblock's x operands in consumer lane order,
   // [warp][j 8][lane 32][2]; it lives in the last ring slots while they are
   // not yet filled (small rings get a separate area)
-  const uint32_t fb = 16u * 8u * 32u * 8u;
+  const uint32_t fb = 16u * kFragWarpBytes;
   const int held = static_cast<int>((fb + stage_bytes - 1) / stage_bytes);
   if (held < stages) {
     L.held = held;
@@ -166,10 +166,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_q4k_tc_kernel(const TcPara
   }
   __syncthreads();
   pdl_launch_dependents();
-  if (tid == 0) {
-    if (!p.early_weights) pdl_wait();
-    for (int i = 0; i < min(p.stages - L.held, nst); ++i) issue(i);
-  }
+  // Weights may stream before the grid-dependency wait, but only one stage:
+  // the x loads issued after the wait would otherwise queue behind this SM's
+  // whole ring of weight copies (~200 KB, several microseconds).  The other
+  // stages are issued once every warp has issued its x loads.
+  const int npre = p.early_weights ? min(1, min(p.stages - L.held, nst)) : 0;
+  if (tid == 0)
+    for (int i = 0; i < npre; ++i) issue(i);
 
   // ------------------------------------------------------------------ prologue
   // Each warp converts the x operands of its own superblocks: lane l loads
@@ -187,22 +190,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_q4k_tc_kernel(const TcPara
   uint32_t bq[NSB][8][2];
   float fsc[NSB];
   {
-    uint2 *frag = reinterpret_cast<uint2 *>(smem + L.frag) + warp * 256;
+    uint2 *frag = reinterpret_cast<uint2 *>(smem + L.frag) + warp * (kFragWarpBytes / 8);
     const int sub = lane >> 2, wi = lane & 3;          // sub-block and word of this lane's columns
     const int tp = sub >> 1, jj = 4 * (sub & 1) + wi;   // consumer lane group t' and MMA index j
+    // every load of a vector is issued before any is used (one round trip);
+    // superblocks past the row end read the last one and are zeroed later
     float4 xr[NSB][2][2];
 #pragma unroll
-    for (int i = 0; i < NSB; ++i) {
-      const int sb = kq + i * KP;
+    for (int v = 0; v < 2; ++v) {
+      if (v < p.nv) {
+        const float *xv = p.x + v * p.x_stride;
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        xr[i][v][0] = xr[i][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if ((FULL || sb < p.nsb) && v < p.nv) {
-          const float *src = p.x + v * p.x_stride + xg.src(256 * sb + 8 * lane);
-          xr[i][v][0] = *reinterpret_cast<const float4 *>(src);
-          xr[i][v][1] = *reinterpret_cast<const float4 *>(src + 4);
+        for (int i = 0; i < NSB; ++i) {
+          const int sb = FULL ? kq + i * KP : min(kq + i * KP, p.nsb - 1);
+          const float *src = xv + xg.src(256 * sb + 8 * lane);
+          xr[i][v][0] = ldg4(src);
+          xr[i][v][1] = ldg4(src + 4);
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < NSB; ++i) xr[i][v][0] = xr[i][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    }
+    // the x loads are in flight: now the rest of the initial weight copies
+    named_sync(2, kTcThreads);  // prologue only: no warp has left yet
+    if (tid == 0)
+      for (int i = npre; i < min(p.stages - L.held, nst); ++i) issue(i);
+    if (!FULL) {
+#pragma unroll
+      for (int i = 0; i < NSB; ++i)
+        if (kq + i * KP >= p.nsb)
+          xr[i][0][0] = xr[i][0][1] = xr[i][1][0] = xr[i][1][1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float ssq[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -211,6 +229,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_q4k_tc_kernel(const TcPara
       float fs[2] = {0.0f, 0.0f};
 #pragma unroll
       for (int v = 0; v < 2; ++v) {
+        if (v >= p.nv) {  // no such vector: zero operands, nothing to convert
+          if (wi == 0 && (FULL || sb < p.nsb)) gxsum[((sb * 4 + tp) * 2 + v) * 2 + (sub & 1)] = 0.0f;
+          fs[v] = 0.0f;
+        #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int l0 = 4 * (4 * h + 2 * v) + tp;
+            frag[jj * kFragRow + l0] = frag[jj * kFragRow + l0 + 4] = make_uint2(0u, 0u);
+          }
+          continue;
+        }
         const float q0[8] = {xr[i][v][0].x, xr[i][v][0].y, xr[i][v][0].z, xr[i][v][0].w,
                              xr[i][v][1].x, xr[i][v][1].y, xr[i][v][1].z, xr[i][v][1].w};
         float amax = 0.0f, s8 = 0.0f;
@@ -242,14 +270,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_q4k_tc_kernel(const TcPara
           hi.y = split_pair(q[h + 2], q[h + 6], false);
           lo.y = split_pair(q[h + 2], q[h + 6], true);
           const int l0 = 4 * (4 * h + 2 * v) + tp;
-          frag[jj * 32 + l0] = hi;
-          frag[jj * 32 + l0 + 4] = lo;
+          frag[jj * kFragRow + l0] = hi;
+          frag[jj * kFragRow + l0 + 4] = lo;
         }
       }
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint2 r = frag[j * 32 + lane];
+        const uint2 r = frag[j * kFragRow + lane];
         bq[i][j][0] = r.x;
         bq[i][j][1] = r.y;
       }

@@ -74,6 +74,21 @@ __device__ __forceinline__ void mma_word(uint32_t w, const SubMul &m, uint32_t b
   mma16816(c, a0, a1, a2, a3, b0, b1);
 }
 
+// Per-warp staging of one superblock's x operands: 8 rows (one per MMA) of
+// 32 lane records, padded to 34: a half-warp of converting lanes stores to
+// 8 rows x 2 lane groups at once, and a row stride of 2 mod 16 records puts
+// those 16 eight-byte stores in distinct bank pairs.
+constexpr int kFragRow = 34;
+constexpr uint32_t kFragWarpBytes = 8u * kFragRow * 8u;
+
+// 16-byte load of x through the read-only path (x is not written by the
+// kernel that reads it).
+__device__ __forceinline__ float4 ldg4(const float *p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
 // x pair (already scaled) -> fp16 pair of the hi parts, or of the remainders.
 __device__ __forceinline__ uint32_t split_pair(float xa, float xb, bool lo) {
   const __half2 h = __floats2half2_rn(xa, xb);

@@ -62,7 +62,7 @@ __host__ __device__ inline MultiLayout multi_layout(int stages, uint32_t stage_b
   o = al16m(o + 4u * 16 * 4 * V * 2);
   L.scratch = o;  // [warp][vector V]: sums of squares
   o = al16m(o + 4u * kMWarps * V);
-  const uint32_t fb = 16u * 8u * 32u * 8u;  // per-warp staging of one superblock's operands
+  const uint32_t fb = 16u * kFragWarpBytes;  // per-warp staging of one superblock's operands
   const int held = static_cast<int>((fb + stage_bytes - 1) / stage_bytes);
   if (held < stages) {
     L.held = held;
@@ -130,19 +130,19 @@ __global__ void __launch_bounds__(kMThreads, 1) gemv_q4k_tc_multi_kernel(const M
   uint32_t bq[NVP][8][2];
   float fsc[NVP];
   {
-    uint2 *frag = reinterpret_cast<uint2 *>(smem + L.frag) + warp * 256;
+    uint2 *frag = reinterpret_cast<uint2 *>(smem + L.frag) + warp * (kFragWarpBytes / 8);
     const int sub = lane >> 2, wi = lane & 3;
     const int tp = sub >> 1, jj = 4 * (sub & 1) + wi;
     float4 xr[V][2];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      xr[v][0] = xr[v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (v < p.nv) {
-        const float *src = p.x + v * p.x_stride + xg.src(256 * sb + 8 * lane);
-        xr[v][0] = *reinterpret_cast<const float4 *>(src);
-        xr[v][1] = *reinterpret_cast<const float4 *>(src + 4);
-      }
+    for (int v = 0; v < V; ++v) {  // loads of absent vectors read vector 0 (zeroed below)
+      const float *src = p.x + (v < p.nv ? v : 0) * p.x_stride + xg.src(256 * sb + 8 * lane);
+      xr[v][0] = ldg4(src);
+      xr[v][1] = ldg4(src + 4);
     }
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+      if (v >= p.nv) xr[v][0] = xr[v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int pp = 0; pp < NVP; ++pp) {
       float fs[2];
@@ -178,14 +178,14 @@ __global__ void __launch_bounds__(kMThreads, 1) gemv_q4k_tc_multi_kernel(const M
           hi.y = split_pair(q[h + 2], q[h + 6], false);
           lo.y = split_pair(q[h + 2], q[h + 6], true);
           const int l0 = 4 * (4 * h + 2 * w2) + tp;
-          frag[jj * 32 + l0] = hi;
-          frag[jj * 32 + l0 + 4] = lo;
+          frag[jj * kFragRow + l0] = hi;
+          frag[jj * kFragRow + l0 + 4] = lo;
         }
       }
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint2 r = frag[j * 32 + lane];
+        const uint2 r = frag[j * kFragRow + lane];
         bq[pp][j][0] = r.x;
         bq[pp][j][1] = r.y;
       }
