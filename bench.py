@@ -11,8 +11,11 @@ the 129 MB L2, so no flush is needed.
 
 Other workloads (--workload): moe_decode (40 MoE layers, hidden 2048, 256
 experts of gate/up 512x2048 + down 2048x512, top-8 + shared expert, Zipf(1.1)
-routing, a 64-token decode run per step).  --chain runs the dense step as
-one epq_gemv_chain launch instead of one launch per matrix.
+routing, a 64-token decode run per step); moe_layer (one MoE layer of hidden
+4096 with 512 experts of gate/up 2x1024x4096 + down 4096x1024, top-4 + shared
+expert, --ntok 1 or 8 tokens per forward; value = effective weight GB/s).
+--chain runs the dense step as one epq_gemv_chain launch instead of one
+launch per matrix.
 
 The JSON line carries: value (tok/s for decode workloads, GB/s otherwise),
 roofline of the dominant kernel (live CUDA-event pairs inside the graph),
@@ -246,6 +249,119 @@ class MoEDecodeWorkload(Workload):
         return 1.0 / per_token, f"1 token through {done} of {c.layers} layers (oracle, float64), scaled to 40 layers"
 
 
+class MoELayerWorkload(Workload):
+    """One MoE layer (hidden 4096, 512 experts of gate/up 2x1024x4096 + down
+    4096x1024, Q4_K, 3.6 GB resident; one shared expert; router 512x4096
+    fp32; top-4), ntok tokens per forward.  A step is one forward on each of
+    `replicas` (router, shared expert, x) sets that share the routed experts:
+    the replicas' routers and shared experts together exceed 4x L2, and each
+    x routes differently, so no forward finds its weights in L2 except by
+    chance (a routed expert chosen again within the last ~3 forwards)."""
+    name = "moe_layer"
+    unit = "GB/s"
+
+    def __init__(self, epq, dev, fmt, ntok=1, replicas=None):
+        import torch
+        from synthetic import workloads as wl
+        self.cfg = c = wl.MoELayer()
+        self.fmt, self.dev, self.epq, self.ntok = fmt, dev, epq, ntok
+        H, I, E, K = c.hidden, c.inter, c.n_experts, c.topk
+        rbH, rbI = epq.epq_row_bytes(fmt, H), epq.epq_row_bytes(fmt, I)
+        self.expert_bytes = 2 * I * rbH + H * rbI
+        gu = torch.empty((E, 2 * I, rbH), dtype=torch.uint8, device=dev)
+        dn = torch.empty((E, H, rbI), dtype=torch.uint8, device=dev)
+        for e in range(E):  # one generator call per expert (the tests regenerate single experts)
+            epq.epq_quantize(fmt, wl.weight("moe_layer", 0, 10, 2 * I, H, dev, expert=e), blocks=gu[e])
+            epq.epq_quantize(fmt, wl.weight("moe_layer", 0, 11, H, I, dev, expert=e), blocks=dn[e])
+        per_rep = E * H * 4 + self.expert_bytes
+        self.R = replicas if replicas else max(1, math.ceil(4 * 129e6 / per_rep))
+        self.layers = []
+        for r in range(self.R):
+            Rw, _ = wl.moe_router("moe_layer", r, E, H, dev, None)
+            sgu = epq.epq_quantize(fmt, wl.weight("moe_layer", r, 12, 2 * I, H, dev))
+            sdn = epq.epq_quantize(fmt, wl.weight("moe_layer", r, 13, H, I, dev))
+            self.layers.append(epq.MoELayer(fmt, Rw, gu, dn, shared_gate_up=sgu, shared_down=sdn))
+        self.gate_up, self.down = gu, dn
+        self.x = torch.stack([wl.activations("moe_layer", ntok, H, dev, stream_id=r) for r in range(self.R)])
+        self.out = torch.empty_like(self.x)
+        self.ws = torch.empty(self.layers[0].workspace_bytes(ntok, K), dtype=torch.uint8, device=dev)
+        # distinct routed experts of each forward (the bytes it must stream)
+        idx = torch.empty((ntok, K), dtype=torch.int32, device=dev)
+        self.distinct = []
+        for r in range(self.R):
+            epq.epq_moe_forward(self.layers[r], self.x[r], K, y=self.out[r], topk_idx=idx, workspace=self.ws)
+            self.distinct.append(len(set(idx.cpu().flatten().tolist())))
+        torch.cuda.synchronize()
+        nd = sum(self.distinct) / self.R
+        act = 4 * ntok * H * 2  # x in, y out
+        self.bytes_per_forward = E * H * 4 + (nd + 1) * self.expert_bytes + act
+        self.units_per_step = self.R * self.bytes_per_forward / 1e9   # GB per step
+        self.tokens_per_step = self.R * ntok
+        self.kernels_per_step = 3 * self.R
+        self.kernel_bytes = {
+            "moe_router": E * H * 4 + 4 * ntok * H,
+            "moe_gateup": (nd + 1) * 2 * I * rbH + 4 * ntok * (H + (K + 1) * I),
+            "moe_down": (nd + 1) * H * rbI + 4 * ntok * ((K + 1) * I + 2 * H),
+        }
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "moe_layer_q4k", "hidden": c.hidden, "experts": c.n_experts, "inter": c.inter,
+                "topk": c.topk, "shared_experts": 1, "ntok": self.ntok, "forwards_per_step": self.R,
+                "distinct_routed_experts_avg": round(sum(self.distinct) / self.R, 2),
+                "bytes_per_forward": int(self.bytes_per_forward), "router": "fp32 student-t",
+                "l2": f"{self.R} router+shared replicas ({self.R * (c.n_experts * c.hidden * 4 + self.expert_bytes) / 1e6:.0f}"
+                      " MB > 4x L2), x per replica, routed experts drawn from 3.6 GB"}
+
+    def step(self, stream, x=None, out=None, timers=None):
+        x = self.x if x is None else x
+        out = self.out if out is None else out
+        e, K = self.epq, self.cfg.topk
+        for r in range(self.R):
+            if timers is None:
+                e.epq_moe_forward(self.layers[r], x[r], K, y=out[r], workspace=self.ws, stream=stream)
+                continue
+            for name, st in (("moe_router", e.EPQ_MOE_ROUTE), ("moe_gateup", e.EPQ_MOE_GATE_UP),
+                             ("moe_down", e.EPQ_MOE_DOWN)):
+                a, b = timers.pair(name)
+                a.record(stream)
+                e.epq_moe_forward(self.layers[r], x[r], K, y=out[r], workspace=self.ws, stages=st, stream=stream)
+                b.record(stream)
+
+    def extra(self, value):
+        return {"tok_per_s": round(value / self.bytes_per_forward * 1e9 * self.ntok, 1),
+                "us_per_forward": round(self.bytes_per_forward / (value * 1e9) * 1e6, 3)}
+
+    def oracle_sample(self, budget_s=20.0):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        H, I, K = c.hidden, c.inter, c.topk
+        layer = self.layers[0]
+        R = layer.router.cpu().numpy()
+        sgu, sdn = layer.shared_gate_up.cpu().numpy(), layer.shared_down.cpu().numpy()
+        xs = self.x[0].cpu().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        nbytes, done = 0, 0
+        while True:
+            x = xs[done % self.ntok]
+            logits = oracle.router_logits_f64(R, x[None], None)
+            idx = oracle.topk_select(logits, K)
+            w = oracle.combine_weights(logits, idx, True)
+            y = x.copy()
+            for k, ex in enumerate(idx[0]):
+                o = oracle.expert_forward_f64(self.fmt, self.gate_up[int(ex)].cpu().numpy(),
+                                              self.down[int(ex)].cpu().numpy(), H, I, x)[0]
+                y += w[0, k] * o[0]
+            y += oracle.expert_forward_f64(self.fmt, sgu, sdn, H, I, x)[0][0]
+            nbytes += R.nbytes + (K + 1) * self.expert_bytes
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return nbytes / dt / 1e9, f"{done} single-token forwards of the layer (oracle, float64), router + {K} + 1 experts each"
+
+
 class DenseDecodeWorkload(Workload):
     name = "dense8b"
     unit = "tok/s"
@@ -350,6 +466,8 @@ def run_epq(args):
     fmt = epq.FORMATS[args.fmt]
     if args.workload == "moe_decode":
         W = MoEDecodeWorkload(epq, dev, fmt, layers=args.layers)
+    elif args.workload == "moe_layer":
+        W = MoELayerWorkload(epq, dev, fmt, ntok=args.ntok)
     elif args.workload == "dense8b":
         W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers, chain=args.chain)
     else:
@@ -362,16 +480,25 @@ def run_epq(args):
     stream.synchronize()
     assert epq.epq_device_error() == 0, "device-side wait timed out during warm-up"
 
-    # timers: CUDA event pairs around each kernel of layer 0, for every token
+    # The timed steps carry no instrumentation.  Per-kernel durations come
+    # from a second capture of the same step with CUDA event pairs around the
+    # kernels of its first layer, replayed after the timed region.
     timers = Timers(torch, W)
     if args.no_graph:  # direct launches (for profilers that do not follow graph replays)
         def replay():
+            W.step(stream)
+
+        def replay_timed():
             W.step(stream, timers=timers)
     else:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            W.step(stream, timers=timers)
+            W.step(stream)
         replay = g.replay
+        gt = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gt, stream=stream):
+            W.step(stream, timers=timers)
+        replay_timed = gt.replay
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             replay()
@@ -396,6 +523,10 @@ def run_epq(args):
         torch.cuda.synchronize()
         barrier()
     ms = e0.elapsed_time(e1) / args.steps
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, min(args.steps, 5))):
+            replay_timed()
+    torch.cuda.synchronize()
     kernel_ms = timers.averages()
     clocks = clk.summary()
     err = epq.epq_device_error()
@@ -456,7 +587,7 @@ def run_epq(args):
                 "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
                 "bytes_per_launch": W.kernel_bytes[dom],
                 "all_kernels_us": {k: round(v * 1e3, 3) for k, v in kernel_ms.items()}}
-    eff_gbs = W.bytes_per_token * (value / ws) / 1e9 if W.unit == "tok/s" else None
+    eff_gbs = W.bytes_per_token * (value / ws) / 1e9 if W.unit == "tok/s" else value / ws
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": W.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -470,6 +601,8 @@ def run_epq(args):
                 "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4},
         "device_error": err,
     }
+    if hasattr(W, "extra"):
+        line.update(W.extra(value / ws))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, sample = W.oracle_sample(budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": W.unit, "cores": os.cpu_count(), "kind": "oracle",
@@ -522,6 +655,8 @@ def run_reference(args):
     if args.workload == "moe_decode":
         W = MoEDecodeWorkload(epq, dev, fmt, layers=max(1, args.ref_layers))
         W.cfg = __import__("synthetic.workloads", fromlist=["MoEDecode"]).MoEDecode()
+    elif args.workload == "moe_layer":
+        W = MoELayerWorkload(epq, dev, fmt, ntok=args.ntok, replicas=1)
     else:
         W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=max(1, args.ref_layers))
     per_step = args.cpu_budget / max(1, args.steps + args.warmup)
@@ -533,7 +668,7 @@ def run_reference(args):
             vals.append(v)
     dt = time.perf_counter() - t_all
     value = statistics.mean(vals)
-    ms = 1e3 * W.units_per_step / value if W.unit == "tok/s" else None
+    ms = 1e3 * W.units_per_step / value
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": W.unit, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3) if ms else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
@@ -551,7 +686,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="epq", choices=["epq", "reference"])
-    ap.add_argument("--workload", default="dense8b", choices=["dense8b", "moe_decode"])
+    ap.add_argument("--workload", default="dense8b", choices=["dense8b", "moe_decode", "moe_layer"])
+    ap.add_argument("--ntok", type=int, default=1, help="tokens per MoE layer forward (moe_layer)")
     ap.add_argument("--chain", action="store_true", help="dense step as one epq_gemv_chain launch")
     ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K"])
     ap.add_argument("--nvec", type=int, default=1)

@@ -42,14 +42,17 @@ class _Model:
         self.grp = nq // nkv
         self.eps = 1e-5
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-        self.W = []
+        # float32 weights stay on the device: the check packs its sampled rows with the oracle
+        self.W, self.Wf = [], []
         for l in range(L):
-            mats = {}
+            mats, fl = {}, {}
             for name, (r, c) in {"qkv": (nq + 2 * nkv, H), "o": (H, nq), "gu": (2 * I, H), "d": (H, I)}.items():
-                w = synthetic.student_t((r, c), seed=seed * 100 + l * 10 + len(mats), device=dev)
-                mats[name] = epq.epq_quantize(Q4K, w)
+                fl[name] = synthetic.student_t((r, c), seed=seed * 100 + l * 10 + len(mats), device=dev)
+                mats[name] = epq.epq_quantize(Q4K, fl[name])
             self.W.append(mats)
-        self.head = epq.epq_quantize(Q4K, synthetic.student_t((V, H), seed=seed * 100 + 99, device=dev))
+            self.Wf.append(fl)
+        self.headf = synthetic.student_t((V, H), seed=seed * 100 + 99, device=dev)
+        self.head = epq.epq_quantize(Q4K, self.headf)
         self.x = synthetic.normal((nvec, H), seed=seed + 7, device=dev)
         f = lambda n: torch.empty((nvec, n), dtype=torch.float32, device=dev)
         self.buf = [{"qkv": f(nq + 2 * nkv), "h1": f(H), "m": f(I), "h2": f(H)} for _ in range(L)]
@@ -75,6 +78,13 @@ class _Model:
     def run(self, stream=None):
         self.epq.epq_gemv_chain(Q4K, self.ops(), self.nvec, self.ws, stream=stream)
 
+    def packed(self, blocks, wf, rows):
+        """Oracle packing of the sampled rows (the GPU's packing must equal it)."""
+        ix = torch.from_numpy(rows).to(self.dev)
+        pk = oracle.quantize(Q4K, wf[ix].cpu().numpy())
+        assert np.array_equal(pk, blocks[ix].cpu().numpy())
+        return pk
+
     def check(self, rows_sample=None):
         """Every op against the oracle on the chain's own inputs."""
         cpu = lambda a: a.cpu().numpy()
@@ -84,10 +94,10 @@ class _Model:
                 rng.choice(n, rows_sample, replace=False))
         h = cpu(self.x).astype(np.float64)
         for l in range(self.L):
-            W, B = self.W[l], self.buf[l]
+            W, B, Wf = self.W[l], self.buf[l], self.Wf[l]
             # qkv = W rms(h)
             r = pick(self.nq + 2 * self.nkv)
-            pk = cpu(W["qkv"][torch.from_numpy(r).to(self.dev)])
+            pk = self.packed(W["qkv"], Wf["qkv"], r)
             xn = oracle.rmsnorm_f64(h, self.eps)
             _within(cpu(B["qkv"])[:, r], oracle.gemv_f64(Q4K, pk, xn, self.H), oracle.gemv_bound(Q4K, pk, xn, self.H),
                     f"layer {l} qkv")
@@ -95,7 +105,7 @@ class _Model:
             v = cpu(B["qkv"])[:, self.nq + self.nkv:].astype(np.float64)
             xe = _expand_heads(v, self.hd, self.grp)
             r = pick(self.H)
-            pk = cpu(W["o"][torch.from_numpy(r).to(self.dev)])
+            pk = self.packed(W["o"], Wf["o"], r)
             ref = h[:, r] + oracle.gemv_f64(Q4K, pk, xe, self.nq)
             _within(cpu(B["h1"])[:, r], ref, oracle.gemv_bound(Q4K, pk, xe, self.nq) + np.abs(h[:, r]),
                     f"layer {l} o")
@@ -103,7 +113,7 @@ class _Model:
             # m = silu(Wg rms(h1)) * (Wu rms(h1))
             r = pick(self.I)
             rr = np.concatenate([r, r + self.I])
-            pk = cpu(W["gu"][torch.from_numpy(rr).to(self.dev)])
+            pk = self.packed(W["gu"], Wf["gu"], rr)
             xn = oracle.rmsnorm_f64(h1, self.eps)
             y = oracle.gemv_f64(Q4K, pk, xn, self.H)
             A = oracle.gemv_bound(Q4K, pk, xn, self.H)
@@ -116,13 +126,13 @@ class _Model:
             # h2 = h1 + Wd m
             m = cpu(B["m"]).astype(np.float64)
             r = pick(self.H)
-            pk = cpu(W["d"][torch.from_numpy(r).to(self.dev)])
+            pk = self.packed(W["d"], Wf["d"], r)
             ref = h1[:, r] + oracle.gemv_f64(Q4K, pk, m, self.I)
             _within(cpu(B["h2"])[:, r], ref, oracle.gemv_bound(Q4K, pk, m, self.I) + np.abs(h1[:, r]),
                     f"layer {l} down")
             h = cpu(B["h2"]).astype(np.float64)
         r = pick(self.V)
-        pk = cpu(self.head[torch.from_numpy(r).to(self.dev)])
+        pk = self.packed(self.head, self.headf, r)
         xn = oracle.rmsnorm_f64(h, self.eps)
         _within(cpu(self.logits)[:, r], oracle.gemv_f64(Q4K, pk, xn, self.H), oracle.gemv_bound(Q4K, pk, xn, self.H),
                 "head")

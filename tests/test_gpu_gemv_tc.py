@@ -156,7 +156,9 @@ def test_tc_full_size_sampled(tc_engine, cuda_dev):
         blocks = tc_engine.epq_quantize(Q4K, W)
         y = tc_engine.epq_gemv(Q4K, blocks, x, rows, cols)
         idx = torch.randperm(rows, generator=torch.Generator().manual_seed(rows))[:128].sort().values
-        packed = blocks[idx.to(cuda_dev)].cpu().numpy()
+        # the oracle packs the sampled rows itself; the GPU's packing must match bit for bit
+        packed = oracle.quantize(Q4K, W[idx.to(cuda_dev)].cpu().numpy())
+        assert np.array_equal(packed, blocks[idx.to(cuda_dev)].cpu().numpy())
         xs = x.cpu().numpy()
         _check(y[:, idx.to(cuda_dev)].cpu().numpy(), oracle.gemv_f64(Q4K, packed, xs, cols),
                oracle.gemv_bound(Q4K, packed, xs, cols), what=f"full {rows}x{cols}")
@@ -168,12 +170,12 @@ def test_tc_full_size_sampled(tc_engine, cuda_dev):
 def test_tc_multi_vector_one_pass(tc_engine, cuda_dev, nvec, rows):
     """3..8 vectors over 4096-column rows share one weight pass."""
     cols = 4096
-    W = synthetic.student_t((rows, cols), seed=rows + nvec, device=cuda_dev)
-    blocks = tc_engine.epq_quantize(Q4K, W)
+    W = synthetic.student_t((rows, cols), seed=rows + nvec).numpy()
+    packed = oracle.quantize(Q4K, W)
+    blocks = torch.from_numpy(packed).to(cuda_dev)
     x = synthetic.normal((nvec, cols), seed=7 + nvec).numpy()
     x = (x * np.float32(4.0) ** np.arange(nvec, dtype=np.float32)[:, None]).astype(np.float32)
     y = tc_engine.epq_gemv(Q4K, blocks, torch.from_numpy(x).to(cuda_dev), rows, cols).cpu().numpy()
-    packed = blocks.cpu().numpy()
     _check(y, oracle.gemv_f64(Q4K, packed, x, cols), oracle.gemv_bound(Q4K, packed, x, cols),
            what=f"{rows} rows nvec={nvec}")
 

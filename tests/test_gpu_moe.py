@@ -139,6 +139,32 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES)
 def test_moe_parity(epq_lib, cuda_dev, case):
+    _parity_case(epq_lib, cuda_dev, case)
+
+
+# Q4_K with one or two tokens runs on the tensor-core expert kernels unless
+# the CUDA-core engines are forced: both against the oracle.
+TC_CASES = [
+    # fmt, E, H, I, topk, ntok, shared, gate_vec, bias, norm, rms
+    (oracle.Q4_K, 16, 1024, 512, 4, 1, True, True, True, True, 1e-6),
+    (oracle.Q4_K, 16, 1024, 512, 4, 2, True, False, True, True, None),
+    (oracle.Q4_K, 12, 1280, 768, 3, 2, True, False, False, False, 1e-5),  # 5 superblocks of x, 3 per h
+    (oracle.Q4_K, 6, 256, 256, 6, 2, False, False, False, True, None),    # every expert chosen, no shared
+    (oracle.Q4_K, 40, 4096, 256, 2, 1, True, False, False, True, None),   # slot boundaries inside stages
+]
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("case", TC_CASES)
+def test_moe_q4k_engines(epq_lib, cuda_dev, case, engine):
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, engine)
+    try:
+        _parity_case(epq_lib, cuda_dev, case)
+    finally:
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
+
+
+def _parity_case(epq_lib, cuda_dev, case):
     fmt, E, H, I, topk, ntok, shared, gvec, bias, norm, rms = case
     mw = _make(fmt, E, H, I, seed=E * 100 + H + I + fmt, shared=shared, gate_vec=gvec, bias=bias, norm=norm)
     x = synthetic.normal((ntok, H), seed=H + ntok, scale=2.0).numpy()
@@ -203,3 +229,65 @@ def test_moe_argument_errors(epq_lib, cuda_dev):
     assert e.value.status == 5
     with pytest.raises(epq_lib.EpqError):
         epq_lib.epq_moe_forward(layer, torch.zeros((17, 256), device=cuda_dev), 2)   # ntok > 16
+
+
+class _OraclePackedExperts:
+    """Expert e's packed blocks, packed by the oracle on first use from the
+    seeded float32 weights (the generator call the GPU side packed)."""
+
+    def __init__(self, fmt, gen):
+        self.fmt, self.gen, self.cache = fmt, gen, {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = oracle.quantize(self.fmt, self.gen(e).cpu().numpy())
+        return self.cache[e]
+
+
+@pytest.mark.parametrize("ntok", [1, 8])
+def test_moe_full_size_layer(epq_lib, cuda_dev, ntok):
+    """The single MoE layer at full size, in the bench's launch configuration:
+    hidden 4096, 512 Q4_K experts of gate/up 2x1024x4096 + down 4096x1024
+    (3.6 GB), a shared expert, router 512x4096 fp32, top-4; 1 and 8 tokens.
+    Top-K against the oracle's, every selected expert stage-wise, and the
+    GPU's packing of each selected expert bit-exact with the oracle's."""
+    from synthetic import workloads as wl
+    c = wl.MoELayer()
+    H, I, E, K = c.hidden, c.inter, c.n_experts, c.topk
+    fmt = oracle.Q4_K
+    gen_gu = lambda e: wl.weight("moe_layer", 0, 10, 2 * I, H, cuda_dev, expert=e)
+    gen_dn = lambda e: wl.weight("moe_layer", 0, 11, H, I, cuda_dev, expert=e)
+    gu = torch.empty((E, 2 * I, epq_lib.epq_row_bytes(fmt, H)), dtype=torch.uint8, device=cuda_dev)
+    dn = torch.empty((E, H, epq_lib.epq_row_bytes(fmt, I)), dtype=torch.uint8, device=cuda_dev)
+    for e in range(E):
+        epq_lib.epq_quantize(fmt, gen_gu(e), blocks=gu[e])
+        epq_lib.epq_quantize(fmt, gen_dn(e), blocks=dn[e])
+    R, _ = wl.moe_router("moe_layer", 0, E, H, cuda_dev, None)
+    sgu_f = wl.weight("moe_layer", 0, 12, 2 * I, H, cuda_dev)
+    sdn_f = wl.weight("moe_layer", 0, 13, H, I, cuda_dev)
+    layer = epq_lib.MoELayer(fmt, R, gu, dn, shared_gate_up=epq_lib.epq_quantize(fmt, sgu_f),
+                             shared_down=epq_lib.epq_quantize(fmt, sdn_f))
+    mw = MoEWeights(fmt=fmt, hidden=H, inter=I, router=R.cpu().numpy(),
+                    gate_up=_OraclePackedExperts(fmt, gen_gu), down=_OraclePackedExperts(fmt, gen_dn),
+                    shared_gate_up=oracle.quantize(fmt, sgu_f.cpu().numpy()),
+                    shared_down=oracle.quantize(fmt, sdn_f.cpu().numpy()))
+    assert np.array_equal(mw.shared_gate_up, layer.shared_gate_up.cpu().numpy())
+    x = wl.activations("moe_layer", ntok, H, cuda_dev).cpu().numpy()
+    y, idx, w, h, logits = _run(epq_lib, layer, x, K, cuda_dev)
+    ref = oracle.moe_forward_f64(mw, x, K)
+    Al = np.abs(ref.xin) @ np.abs(mw.router.astype(np.float64)).T
+    assert (np.abs(logits - ref.logits) <= TOL * Al + 1e-6).all()
+    _check_topk(ref, idx, K, mw.router, ref.xin)
+    for e in sorted(set(idx.flatten().tolist())):
+        assert np.array_equal(mw.gate_up[e], gu[e].cpu().numpy()), e
+        assert np.array_equal(mw.down[e], dn[e].cpu().numpy()), e
+    same = (idx == ref.idx).all()
+    if same:
+        assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
+    _stagewise(mw, x, K, idx, w, h, y, ref.xin)
+    if same:
+        _end_to_end(mw, x, ref, y)
+    assert epq_lib.epq_device_error() == 0
+    del gu, dn
+    torch.cuda.empty_cache()
