@@ -41,6 +41,7 @@ namespace {
 constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kRouterXSmem = 40 * 1024;  // stage x in shared memory up to this size (static smem stays < 48 KB)
 constexpr int kRouterChunk = 16;         // 16-byte loads of a router row in flight per lane
+constexpr int64_t kRouterStageMax = 160 * 1024;  // staged router: shared memory for the CTA's rows
 
 // chunk j0.. of router row r (zeros past the row or for r >= r_end)
 __device__ __forceinline__ void router_chunk(const MoeArgs &a, int r, int r_end, int j0, int lane,
@@ -60,18 +61,36 @@ __device__ __forceinline__ void router_chunk(const MoeArgs &a, int r, int r_end,
 // is a weight: nothing upstream writes it).  CTA 0 publishes max|x| and the
 // RMS factor per token and clears the max|h| accumulators of the gate/up
 // kernel.
-template <int NT>
+//
+// STAGED: the CTA's rows of R (all but the gate-vector row) arrive in
+// dynamic shared memory through one bulk copy issued before the wait, so the
+// whole router matrix streams while the previous kernel finishes; the dot
+// products then read the same values in the same order from shared memory.
+template <int NT, bool STAGED>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a) {
+  extern __shared__ __align__(16) uint8_t r_rows[];  // STAGED: [rows of this CTA][H]
   __shared__ float s_part[2][kRouterWarps][NT];
   __shared__ float s_rms[NT];
   __shared__ __align__(16) float s_x[kRouterXSmem / 4];
+  __shared__ __align__(8) uint64_t r_bar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nrows = a.E + (a.gvec ? 1 : 0);
   const int r_begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * nrows) / gridDim.x);
   const int r_end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * nrows) / gridDim.x);
   const int n4 = a.H / 4;  // multiple of 64
   float4 wv[kRouterChunk];
-  router_chunk(a, r_begin + warp, r_end, 0, lane, wv);
+  if (STAGED) {
+    if (tid == 0) {
+      mbar_init(&r_bar, 1);
+      fence_mbar_init();
+      const int nr = max(0, min(r_end, a.E) - r_begin);
+      const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.H) * 4u;
+      mbar_arrive_expect_tx(&r_bar, bytes);
+      if (bytes) bulk_g2s(r_rows, a.R + static_cast<int64_t>(r_begin) * a.H, bytes, &r_bar);
+    }
+  } else {
+    router_chunk(a, r_begin + warp, r_end, 0, lane, wv);
+  }
   pdl_launch_dependents();
   pdl_wait();
 
@@ -113,14 +132,27 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
     for (int i = tid; i < a.ntok * (a.topk + 1); i += kRouterThreads) a.hmax[i] = 0u;
   __syncthreads();
   const float *xbase = xs ? s_x : a.x;
+  if (STAGED && !warp_wait(&r_bar, 0, a.err, DEVERR_FULL_WAIT, 0)) {
+    if (lane == 0) mbar_wait(&r_bar, 0, a.err, DEVERR_DRAIN_WAIT, 0);  // no copy in flight at exit
+    return;
+  }
 
-  bool preloaded = true;
+  bool preloaded = !STAGED;
   for (int r = r_begin + warp; r < r_end; r += kRouterWarps) {
     float acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
     for (int j0 = 0; j0 < n4; j0 += 32 * kRouterChunk) {
-      if (!preloaded) router_chunk(a, r, r_end, j0, lane, wv);
+      if (STAGED && r < a.E) {
+        const float4 *wrow = reinterpret_cast<const float4 *>(r_rows) + static_cast<int64_t>(r - r_begin) * n4;
+#pragma unroll
+        for (int u = 0; u < kRouterChunk; ++u) {
+          const int j = j0 + u * 32 + lane;
+          wv[u] = j < n4 ? wrow[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      } else if (!preloaded) {
+        router_chunk(a, r, r_end, j0, lane, wv);
+      }
       preloaded = false;
 #pragma unroll
       for (int u = 0; u < kRouterChunk; ++u) {
@@ -1334,11 +1366,26 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   cudaError_t e = cudaSuccess;
   if (stages & EPQ_MOE_ROUTE) {
     const int nrows = E + (a.gvec ? 1 : 0);
-    const unsigned rgrid = static_cast<unsigned>(
-        std::max(1, std::min(2 * dev.sm_count, (nrows + kRouterWarps - 1) / kRouterWarps)));
-    if (ntok <= 1) e = launch_pdl(router_kernel<1>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
-    else if (ntok <= 4) e = launch_pdl(router_kernel<4>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
-    else e = launch_pdl(router_kernel<kMaxTok>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+    // staged form when every CTA's rows of R fit shared memory (one CTA per SM)
+    const int sgrid = std::max(1, std::min(dev.sm_count, nrows));
+    const int64_t srows = (nrows + sgrid - 1) / sgrid;
+    const uint32_t ssmem = static_cast<uint32_t>(srows * H * 4);
+    const bool staged = srows * H * 4 <= kRouterStageMax && (reinterpret_cast<uintptr_t>(a.R) & 15) == 0;
+    if (staged) {
+      auto launch = [&](auto k) {
+        cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem);
+        return r != cudaSuccess ? r : launch_pdl(k, dim3(sgrid), dim3(kRouterThreads), ssmem, s, a);
+      };
+      if (ntok <= 1) e = launch(router_kernel<1, true>);
+      else if (ntok <= 4) e = launch(router_kernel<4, true>);
+      else e = launch(router_kernel<kMaxTok, true>);
+    } else {
+      const unsigned rgrid = static_cast<unsigned>(
+          std::max(1, std::min(2 * dev.sm_count, (nrows + kRouterWarps - 1) / kRouterWarps)));
+      if (ntok <= 1) e = launch_pdl(router_kernel<1, false>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+      else if (ntok <= 4) e = launch_pdl(router_kernel<4, false>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+      else e = launch_pdl(router_kernel<kMaxTok, false>, dim3(rgrid), dim3(kRouterThreads), 0, s, a);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     if (!(stages & EPQ_MOE_GATE_UP) && (topk_idx || topk_w || (stages & EPQ_MOE_DOWN))) {
       // the gate/up kernel routes for itself; without it, route here when

@@ -46,7 +46,8 @@ struct MtParams {
   MoeArgs a;
   int stages;
   uint32_t stage_bytes;
-  int nsbx;  // superblocks of the x operand (gate/up: H/256; down: max slots * I/256)
+  int nsbx;      // superblocks of the x operand (gate/up: H/256; down: max slots * I/256)
+  int frag_sep;  // 1: the x staging area has its own space (else the last ring slots)
 };
 
 // Shared memory: the ring, its barriers and counters, the partial sums,
@@ -58,7 +59,7 @@ struct MtLayout {
 };
 
 __host__ __device__ inline MtLayout mt_layout(int stages, uint32_t stage_bytes, int kp, int m, int nsbx, int ntok,
-                                              int topk) {
+                                              int topk, bool sep) {
   MtLayout L;
   uint32_t o = mt_al16(static_cast<uint32_t>(stages) * stage_bytes);
   L.full = o;
@@ -73,7 +74,7 @@ __host__ __device__ inline MtLayout mt_layout(int stages, uint32_t stage_bytes, 
   o = mt_al16(o + 4u * meta_words(ntok, topk));
   const uint32_t fb = 16u * kFragWarpBytes;
   const int held = static_cast<int>((fb + stage_bytes - 1) / stage_bytes);
-  if (held < stages) {
+  if (!sep && held < stages) {
     L.held = held;
     L.frag = static_cast<uint32_t>(stages - held) * stage_bytes;
   } else {
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kMtThreads, 1) moe_gateup_tc_kernel(const MtPa
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NB = kMtWarps / KP;
   const MoeArgs &a = p.a;
-  const MtLayout L = mt_layout(p.stages, p.stage_bytes, KP, 2, p.nsbx, a.ntok, a.topk);
+  const MtLayout L = mt_layout(p.stages, p.stage_bytes, KP, 2, p.nsbx, a.ntok, a.topk, p.frag_sep);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
   unsigned *cnt = reinterpret_cast<unsigned *>(smem + L.cnt);
   float *red = reinterpret_cast<float *>(smem + L.red);
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kMtThreads, 1) moe_down_tc_kernel(const MtPara
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NB = kMtWarps / KP;
   const MoeArgs &a = p.a;
-  const MtLayout L = mt_layout(p.stages, p.stage_bytes, KP, 1, p.nsbx, a.ntok, a.topk);
+  const MtLayout L = mt_layout(p.stages, p.stage_bytes, KP, 1, p.nsbx, a.ntok, a.topk, p.frag_sep);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
   unsigned *cnt = reinterpret_cast<unsigned *>(smem + L.cnt);
   float *red = reinterpret_cast<float *>(smem + L.red);
@@ -565,18 +566,25 @@ void mt_split(int n, int *kp, int *nsbw) {
   *nsbw = w <= 1 ? 1 : (w <= 2 ? 2 : (w <= 4 ? 4 : 0));
 }
 
-// Deepest ring (a multiple of the group count, <= 16, >= `need` stages
-// when possible) that fits shared memory; 0 when none does.
+// Deepest ring (a multiple of the group count, <= 16, at least min_stages)
+// that fits shared memory, 0 when none does; *sep: whether the x staging
+// area gets its own space at that depth (preferred: with it in the ring, the
+// slots it occupies are filled only after every warp's conversion).
 int mt_depth(int want, int min_stages, uint32_t stage_bytes, int kp, int m, int nsbx, int ntok, int topk,
-             const DeviceInfo &dev) {
+             const DeviceInfo &dev, int *sep) {
   const int nb = kMtWarps / kp;
   int st = std::max(std::max(want, min_stages), 2);
   st = std::min(16, (st + nb - 1) / nb * nb);
   st = std::max(st, nb);
+  const uint32_t cap = static_cast<uint32_t>(dev.max_smem_optin);
   for (; st >= nb; st -= nb) {
     if (st < min_stages) return 0;
-    if (mt_layout(st, stage_bytes, kp, m, nsbx, ntok, topk).total <= static_cast<uint32_t>(dev.max_smem_optin))
-      return st;
+    for (int sp = 1; sp >= 0; --sp) {
+      if (mt_layout(st, stage_bytes, kp, m, nsbx, ntok, topk, sp != 0).total <= cap) {
+        *sep = sp;
+        return st;
+      }
+    }
   }
   return 0;
 }
@@ -596,9 +604,9 @@ bool moe_tc_plan(const MoeArgs &a, int max_slots, const DeviceInfo &dev, MoeTcPl
   // the routing scratch lives in the ring
   const int g_min = static_cast<int>((4u * kSelScratchWords + pl->g_stage_bytes - 1) / pl->g_stage_bytes);
   pl->g_stages = mt_depth(static_cast<int>((g_rows + 7) / 8), g_min, pl->g_stage_bytes, pl->g_kp, 2, a.H / 256,
-                          a.ntok, a.topk, dev);
+                          a.ntok, a.topk, dev, &pl->g_sep);
   if (!pl->g_stages) return false;
-  pl->g_smem = mt_layout(pl->g_stages, pl->g_stage_bytes, pl->g_kp, 2, a.H / 256, a.ntok, a.topk).total;
+  pl->g_smem = mt_layout(pl->g_stages, pl->g_stage_bytes, pl->g_kp, 2, a.H / 256, a.ntok, a.topk, pl->g_sep).total;
   // down
   pl->d_nsbx = max_slots * (a.I / 256);
   mt_split(pl->d_nsbx, &pl->d_kp, &pl->d_nsbw);
@@ -607,9 +615,10 @@ bool moe_tc_plan(const MoeArgs &a, int max_slots, const DeviceInfo &dev, MoeTcPl
   if (static_cast<int64_t>(pl->d_stage_bytes) >= (1 << 20)) return false;  // one barrier's transaction count
   const int64_t d_rows = (a.H + grid - 1) / grid;
   pl->d_stages = mt_depth(static_cast<int>((d_rows + 7) / 8), 1, pl->d_stage_bytes, pl->d_kp, 1, pl->d_nsbx,
-                          a.ntok, a.topk, dev);
+                          a.ntok, a.topk, dev, &pl->d_sep);
   if (!pl->d_stages) return false;
-  pl->d_smem = mt_layout(pl->d_stages, pl->d_stage_bytes, pl->d_kp, 1, pl->d_nsbx, a.ntok, a.topk).total;
+  pl->d_smem =
+      mt_layout(pl->d_stages, pl->d_stage_bytes, pl->d_kp, 1, pl->d_nsbx, a.ntok, a.topk, pl->d_sep).total;
   return true;
 }
 
@@ -619,6 +628,7 @@ cudaError_t moe_tc_gateup_launch(const MoeTcPlan &pl, const MoeArgs &a, cudaStre
   p.stages = pl.g_stages;
   p.stage_bytes = pl.g_stage_bytes;
   p.nsbx = a.H / 256;
+  p.frag_sep = pl.g_sep;
   const unsigned gr = pl.grid;
   const uint32_t sm = pl.g_smem;
   const int kp = pl.g_kp, w = pl.g_nsbw;
@@ -651,6 +661,7 @@ cudaError_t moe_tc_down_launch(const MoeTcPlan &pl, const MoeArgs &a, cudaStream
   p.stages = pl.d_stages;
   p.stage_bytes = pl.d_stage_bytes;
   p.nsbx = pl.d_nsbx;
+  p.frag_sep = pl.d_sep;
   const unsigned gr = pl.grid;
   const uint32_t sm = pl.d_smem;
   const int kp = pl.d_kp, w = pl.d_nsbw;

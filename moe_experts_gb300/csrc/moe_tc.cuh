@@ -12,11 +12,11 @@ struct MoeTcPlan {
   // gate/up + SwiGLU: KP k-parts of NSB superblocks each, FULL when they
   // cover the H/256 superblocks exactly; ring of `stages` stages of 8 gate
   // rows + 8 up rows
-  int g_kp, g_nsbw, g_full, g_stages;
+  int g_kp, g_nsbw, g_full, g_stages, g_sep;
   uint32_t g_stage_bytes, g_smem;
   // down + combine: the x operand spans up to d_nsbx superblocks (every
   // slot's I/256); a stage holds 8 rows of every slot's down matrix
-  int d_kp, d_nsbw, d_stages, d_nsbx;
+  int d_kp, d_nsbw, d_stages, d_nsbx, d_sep;
   uint32_t d_stage_bytes, d_smem;
 };
 
