@@ -44,8 +44,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture of the kernel as it stands; the summary with its command is the
 # named file.  An entry must go when its kernel changes.
 NCU_TRAFFIC = {
-    ("moe_decode", "moe_gateup"): (10_700_672, "profiles/moe_gateup_flat_q4k_full.md"),
-    ("dense8b", "gemv_gateup"): (66_309_632, "profiles/gemv_tc_gateup_q4k_full.md"),
+    ("moe_decode", "moe_gateup"): (10_683_904, "profiles/moe_tc_gateup_down_q4k_full.md"),
+    ("dense8b", "gemv_gateup"): (66_333_184, "profiles/gemv_tc_gateup_q4k_full.md"),
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -401,6 +401,11 @@ class DenseDecodeWorkload(Workload):
                              + H * rbI) + c.vocab * rbH
         self.weight_bytes_per_step = wbytes
         self.bytes_per_token = wbytes / nvec  # one weight pass serves all nvec columns
+        # packed bytes of the full step (the oracle's rate is scaled to it even
+        # when fewer layers are built, as in the reference arm)
+        full = wl.DenseDecode()
+        self.full_step_bytes = full.layers * ((nq + 2 * nkv) * rbH + H * epq.epq_row_bytes(fmt, nq) +
+                                              2 * c.inter * rbH + H * rbI) + c.vocab * rbH
         self.kernels_per_step = 1 if chain else c.layers * 4 + 1
         if chain:  # the one launch is the dominant (and only) kernel
             self.kernel_bytes = {"gemv_chain": wbytes + 4 * nvec * (c.layers * (4 * H + 2 * c.inter + nq + 2 * nkv
@@ -444,7 +449,7 @@ class DenseDecodeWorkload(Workload):
         dt = time.perf_counter() - t0
         # scale by bytes: the sample covered qkv + gate/up of `done` layers
         rate = nbytes / dt
-        return rate / self.bytes_per_token, \
+        return rate / (self.full_step_bytes / self.nvec), \
             f"{done} layers' qkv+gate/up GEMVs (oracle, float64), scaled by bytes to the full step"
 
 

@@ -94,7 +94,7 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *   EPQ_TUNE_RING_BYTES  shared-memory ring budget per CTA (32768 .. 200704)
  *   EPQ_TUNE_GEMV_ENGINE dense GEMV engine: 0 automatic (Q4_K uses the
  *                        tensor-core engine for two or more vectors and for
- *                        one vector over matrices of >= 8 MiB), 1 CUDA-core
+ *                        one vector over matrices of >= 2 MiB), 1 CUDA-core
  *                        engines only,
  *                        2 tensor-core engine wherever it applies (Q4_K)
  * Returns the previous value, or -1 for an unknown key or a value out of

@@ -690,12 +690,12 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   const int xs = opts.x_ld ? static_cast<int>(opts.x_ld) : static_cast<int>(cols / xg);
 
   // Q4_K: the tensor-core engine (two vectors per weight pass, more in the
-  // multi-vector form).  With one vector it is chosen for matrices of >= 8
-  // MiB (a 4096x4096 projection and up), where its lower instruction count
+  // multi-vector form).  With one vector it is chosen for matrices of >= 2
+  // MiB (a 2048x2048 projection and up), where its lower instruction count
   // per weight pays; smaller one-vector launches keep the one-shot CUDA-core
   // form, whose prologue is shorter.
   const int eng = tune_gemv_engine();
-  const bool tc_auto = nvec >= 2 || rows * row_bytes >= (int64_t(8) << 20);
+  const bool tc_auto = nvec >= 2 || rows * row_bytes >= (int64_t(2) << 20);
   TcPlan tp;
   if (fmt == EPQ_Q4_K && eng != 1 && (eng == 2 || tc_auto) &&
       gemv_tc_plan(row_bytes, static_cast<int>(cols), rows_out, sw, dev, &tp)) {
