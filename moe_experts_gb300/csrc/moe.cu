@@ -444,6 +444,26 @@ struct SlotIds {
 };
 
 // ------------------------------------------------------------------ 2. gate/up
+// Virtual rows [rb, re) of CTA b out of G when each row of slot s costs
+// max(1, cnt[s]) units: the CTAs get equal shares of the total, and every
+// CTA evaluates the same monotonic map, so the ranges tile the rows exactly.
+__device__ __forceinline__ void weighted_rows(const Meta &m, int I, int nslots, int b, int G, int64_t &rb,
+                                              int64_t &re) {
+  int64_t W = 0;
+  for (int s = 0; s < nslots; ++s) W += static_cast<int64_t>(I) * max(1, m.cnt[s]);
+  auto row_at = [&](int64_t w) -> int64_t {  // first row whose work starts at or after w
+    int64_t acc = 0;
+    for (int s = 0; s < nslots; ++s) {
+      const int64_t c = max(1, m.cnt[s]);
+      if (w < acc + static_cast<int64_t>(I) * c) return static_cast<int64_t>(s) * I + (w - acc + c - 1) / c;
+      acc += static_cast<int64_t>(I) * c;
+    }
+    return static_cast<int64_t>(nslots) * I;
+  };
+  rb = row_at(W * b / G);
+  re = row_at(W * (b + 1) / G);
+}
+
 template <int FMT, int RPG>
 __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const EngineArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -492,9 +512,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) gateup_kernel(const Eng
 
   const int I = a.I;
   const int nact = *m.nact;
-  const int64_t total = static_cast<int64_t>(*m.nslots) * I;
-  const int64_t rb = (static_cast<int64_t>(blockIdx.x) * total) / gridDim.x;
-  const int64_t re = (static_cast<int64_t>(blockIdx.x + 1) * total) / gridDim.x;
+  // every entry of a slot is one more dot product per row: equal shares of
+  // rows x entries, not of rows (the shared expert serves every token)
+  int64_t rb, re;
+  weighted_rows(m, I, *m.nslots, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), rb, re);
   auto tile_len = [&](int64_t r0) {
     const int64_t lim = min(re, (r0 / I + 1) * I);
     return static_cast<int>(min(static_cast<int64_t>(p.tile_rows), lim - r0));
