@@ -235,7 +235,11 @@ epq_status epq_gemv_chain(epq_fmt fmt, const epq_gemv_op *ops, int nops, int nve
  *   E_e(v) = down_e( silu(gate_e v) * (up_e v) )  (silu(g) = g/(1+exp(-g)))
  *   y_t    = x_t + sum_k w_tk E_{e_k}(xin_t) + g_t E_shared(xin_t)
  *            g_t = 1, or sigmoid(shared_gate_vec . xin_t) when given.
- * Tokens that pick the same expert share one pass over its weights. */
+ * Tokens that pick the same expert share one pass over its weights, except
+ * that a Q4_K call of three or more tokens running all stages is processed
+ * as chunks of two tokens on the tensor-core kernels (an expert chosen in
+ * two chunks is read once per chunk); EPQ_TUNE_GEMV_ENGINE = 1 keeps one
+ * pass for all tokens on the CUDA-core kernels. */
 typedef struct {
   const float *weight; /* [n_experts][hidden] float32, 16-byte aligned */
   const float *bias;   /* [n_experts] or NULL */
@@ -272,6 +276,10 @@ typedef struct {
                         one layer may be issued by separate calls in order
                         with the same arguments and workspace (the workspace
                         carries the logits, routing and h between them).
+                        Separate stage calls are never split into chunks of
+                        two tokens, so for a Q4_K call of more than two
+                        tokens they run the CUDA-core kernels (same result
+                        within the GEMV bound, not bit for bit).
                         The gate/up stage computes the routing; a call with
                         the router stage but not the gate/up stage adds a
                         one-CTA routing kernel when it returns topk_idx /

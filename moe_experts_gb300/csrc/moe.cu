@@ -41,7 +41,7 @@ namespace {
 constexpr int kRouterWarps = kRouterThreads / 32;
 constexpr int kRouterXSmem = 40 * 1024;  // stage x in shared memory up to this size (static smem stays < 48 KB)
 constexpr int kRouterChunk = 16;         // 16-byte loads of a router row in flight per lane
-constexpr int64_t kRouterStageMax = 160 * 1024;  // staged router: shared memory for the CTA's rows
+constexpr int64_t kRouterStageMax = 200 * 1024;  // staged router: shared memory for the CTA's rows and x
 
 // chunk j0.. of router row r (zeros past the row or for r >= r_end)
 __device__ __forceinline__ void router_chunk(const MoeArgs &a, int r, int r_end, int j0, int lane,
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
   extern __shared__ __align__(16) uint8_t r_rows[];  // STAGED: [rows of this CTA][H]
   __shared__ float s_part[2][kRouterWarps][NT];
   __shared__ float s_rms[NT];
-  __shared__ __align__(16) float s_x[kRouterXSmem / 4];
+  __shared__ __align__(16) float s_x[STAGED ? 4 : kRouterXSmem / 4];  // STAGED: x follows the rows
   __shared__ __align__(8) uint64_t r_bar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nrows = a.E + (a.gvec ? 1 : 0);
@@ -95,14 +95,16 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
   pdl_wait();
 
   // x staged in shared memory; per-token sum of squares and max |x|
-  const bool xs = static_cast<int64_t>(a.ntok) * a.H * 4 <= kRouterXSmem;
+  const bool xs = STAGED || static_cast<int64_t>(a.ntok) * a.H * 4 <= kRouterXSmem;
+  float *xsm = STAGED ? reinterpret_cast<float *>(r_rows) + static_cast<int64_t>(max(0, min(r_end, a.E) - r_begin)) * a.H
+                      : s_x;
   for (int t = 0; t < a.ntok; ++t) {
     float ss = 0.0f, mx = 0.0f;
     const float4 *src = reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(t) * a.H);
 #pragma unroll 4
     for (int j = tid; j < n4; j += kRouterThreads) {
       const float4 v = src[j];
-      if (xs) reinterpret_cast<float4 *>(s_x + t * a.H)[j] = v;
+      if (xs) reinterpret_cast<float4 *>(xsm + t * a.H)[j] = v;
       ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const MoeArgs a)
   if (blockIdx.x == 0)
     for (int i = tid; i < a.ntok * (a.topk + 1); i += kRouterThreads) a.hmax[i] = 0u;
   __syncthreads();
-  const float *xbase = xs ? s_x : a.x;
+  const float *xbase = xs ? xsm : a.x;
   if (STAGED && !warp_wait(&r_bar, 0, a.err, DEVERR_FULL_WAIT, 0)) {
     if (lane == 0) mbar_wait(&r_bar, 0, a.err, DEVERR_DRAIN_WAIT, 0);  // no copy in flight at exit
     return;
@@ -1338,6 +1340,25 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const WsLayout L = ws_layout(ntok, topk, E, I);
   if (!workspace || workspace_bytes < L.total) return EPQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return EPQ_ERR_ALIGN;
+  // Q4_K with three or more tokens, all stages in this call: the tensor-core
+  // expert kernels take two tokens per pass, so the call runs as chunks of
+  // two tokens (router, gate/up, down each; an expert chosen in two chunks
+  // is read once per chunk).  Measured faster than the CUDA-core engines,
+  // which read every chosen expert once for all tokens.
+  if (ntok > 2 && ((o.stages & 7) == 0 || (o.stages & 7) == 7) && experts->fmt == EPQ_Q4_K &&
+      tune_gemv_engine() != 1) {
+    for (int t0 = 0; t0 < ntok; t0 += 2) {
+      const int nt = std::min(2, ntok - t0);
+      epq_moe_opts oc = o;
+      if (o.logits_out) oc.logits_out = o.logits_out + static_cast<int64_t>(t0) * E;
+      if (o.h_out) oc.h_out = o.h_out + static_cast<int64_t>(t0) * (topk + 1) * I;
+      st = epq_moe_forward(router, experts, x + static_cast<int64_t>(t0) * H, nt, topk, &oc,
+                           y + static_cast<int64_t>(t0) * H, topk_idx ? topk_idx + t0 * topk : nullptr,
+                           topk_w ? topk_w + t0 * topk : nullptr, workspace, workspace_bytes, stream);
+      if (st != EPQ_OK) return st;
+    }
+    return EPQ_OK;
+  }
   DeviceInfo dev;
   if (!current_device(&dev) || dev.major * 10 + dev.minor < 100) return EPQ_ERR_DEVICE;
   unsigned *err = device_error_slot();
@@ -1390,8 +1411,10 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
     // staged form when every CTA's rows of R fit shared memory (one CTA per SM)
     const int sgrid = std::max(1, std::min(dev.sm_count, nrows));
     const int64_t srows = (nrows + sgrid - 1) / sgrid;
-    const uint32_t ssmem = static_cast<uint32_t>(srows * H * 4);
-    const bool staged = srows * H * 4 <= kRouterStageMax && (reinterpret_cast<uintptr_t>(a.R) & 15) == 0;
+    // dynamic shared memory: the CTA's rows of R, then x of every token
+    const int64_t sbytes = (srows + ntok) * H * 4;
+    const uint32_t ssmem = static_cast<uint32_t>(sbytes);
+    const bool staged = sbytes <= kRouterStageMax && (reinterpret_cast<uintptr_t>(a.R) & 15) == 0;
     if (staged) {
       auto launch = [&](auto k) {
         cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem);

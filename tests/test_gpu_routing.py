@@ -116,10 +116,22 @@ def test_workspace_needs_no_initialisation(epq_lib, cuda_dev):
         assert torch.equal(y0, y1)
 
 
-def test_stage_split_equals_single_call(epq_lib, cuda_dev):
+@pytest.mark.parametrize("ntok,engine", [(2, 0), (4, 1)])
+def test_stage_split_equals_single_call(epq_lib, cuda_dev, ntok, engine):
     """Router, gate/up and down issued as three calls give the single call's
-    output bit for bit (the gate/up kernel routes from the stored logits)."""
-    fmt, E, H, I, topk, ntok = oracle.Q4_K, 24, 1024, 256, 3, 4
+    output bit for bit (the gate/up kernel routes from the stored logits).
+    Same engine on both sides: two tokens on the tensor-core kernels, four
+    on the CUDA-core ones (a single Q4_K call of more than two tokens would
+    otherwise run in chunks of two on the tensor cores)."""
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, engine)
+    try:
+        _stage_split(epq_lib, cuda_dev, ntok)
+    finally:
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
+
+
+def _stage_split(epq_lib, cuda_dev, ntok):
+    fmt, E, H, I, topk = oracle.Q4_K, 24, 1024, 256, 3
     R = synthetic.student_t((E, H), seed=41).numpy()
     gu = np.stack([oracle.quantize(fmt, synthetic.student_t((2 * I, H), seed=50 + e).numpy()) for e in range(E)])
     dn = np.stack([oracle.quantize(fmt, synthetic.student_t((H, I), seed=90 + e).numpy()) for e in range(E)])
