@@ -288,26 +288,38 @@ class MoELayerWorkload(Workload):
         # distinct routed experts of each forward (the bytes it must stream)
         idx = torch.empty((ntok, K), dtype=torch.int32, device=dev)
         self.distinct = []
+        # Q4_K calls of more than two tokens run as chunks of two (router,
+        # gate/up, down per chunk): the launches, and the bytes each streams
+        self.chunks = [(0, ntok)] if (ntok <= 2 or fmt != epq.EPQ_Q4_K) else \
+            [(t0, min(2, ntok - t0)) for t0 in range(0, ntok, 2)]
+        chunk_distinct = []
         for r in range(self.R):
             epq.epq_moe_forward(self.layers[r], self.x[r], K, y=self.out[r], topk_idx=idx, workspace=self.ws)
-            self.distinct.append(len(set(idx.cpu().flatten().tolist())))
+            ids = idx.cpu().tolist()
+            self.distinct.append(len({e for row in ids for e in row}))
+            for t0, nt in self.chunks:
+                chunk_distinct.append(len({e for row in ids[t0:t0 + nt] for e in row}))
         torch.cuda.synchronize()
         nd = sum(self.distinct) / self.R
+        ndc = sum(chunk_distinct) / len(chunk_distinct)
+        ntc = ntok / len(self.chunks)
         act = 4 * ntok * H * 2  # x in, y out
         self.bytes_per_forward = E * H * 4 + (nd + 1) * self.expert_bytes + act
         self.units_per_step = self.R * self.bytes_per_forward / 1e9   # GB per step
         self.tokens_per_step = self.R * ntok
-        self.kernels_per_step = 3 * self.R
+        self.kernels_per_step = 3 * self.R * len(self.chunks)
+        # algorithmic bytes of one launch of each kernel (per chunk)
         self.kernel_bytes = {
-            "moe_router": E * H * 4 + 4 * ntok * H,
-            "moe_gateup": (nd + 1) * 2 * I * rbH + 4 * ntok * (H + (K + 1) * I),
-            "moe_down": (nd + 1) * H * rbI + 4 * ntok * ((K + 1) * I + 2 * H),
+            "moe_router": E * H * 4 + 4 * ntc * H,
+            "moe_gateup": (ndc + 1) * 2 * I * rbH + 4 * ntc * (H + (K + 1) * I),
+            "moe_down": (ndc + 1) * H * rbI + 4 * ntc * ((K + 1) * I + 2 * H),
         }
 
     def config(self):
         c = self.cfg
         return {"workload": "moe_layer_q4k", "hidden": c.hidden, "experts": c.n_experts, "inter": c.inter,
                 "topk": c.topk, "shared_experts": 1, "ntok": self.ntok, "forwards_per_step": self.R,
+                "token_chunks_per_forward": len(self.chunks),
                 "distinct_routed_experts_avg": round(sum(self.distinct) / self.R, 2),
                 "bytes_per_forward": int(self.bytes_per_forward), "router": "fp32 student-t",
                 "l2": f"{self.R} router+shared replicas ({self.R * (c.n_experts * c.hidden * 4 + self.expert_bytes) / 1e6:.0f}"
@@ -321,12 +333,15 @@ class MoELayerWorkload(Workload):
             if timers is None:
                 e.epq_moe_forward(self.layers[r], x[r], K, y=out[r], workspace=self.ws, stream=stream)
                 continue
-            for name, st in (("moe_router", e.EPQ_MOE_ROUTE), ("moe_gateup", e.EPQ_MOE_GATE_UP),
-                             ("moe_down", e.EPQ_MOE_DOWN)):
-                a, b = timers.pair(name)
-                a.record(stream)
-                e.epq_moe_forward(self.layers[r], x[r], K, y=out[r], workspace=self.ws, stages=st, stream=stream)
-                b.record(stream)
+            # the same kernels per chunk as the plain call, one stage per call
+            for t0, nt in self.chunks:
+                for name, st in (("moe_router", e.EPQ_MOE_ROUTE), ("moe_gateup", e.EPQ_MOE_GATE_UP),
+                                 ("moe_down", e.EPQ_MOE_DOWN)):
+                    a, b = timers.pair(name)
+                    a.record(stream)
+                    e.epq_moe_forward(self.layers[r], x[r][t0:t0 + nt], K, y=out[r][t0:t0 + nt], workspace=self.ws,
+                                      stages=st, stream=stream)
+                    b.record(stream)
 
     def extra(self, value):
         return {"tok_per_s": round(value / self.bytes_per_forward * 1e9 * self.ntok, 1),
