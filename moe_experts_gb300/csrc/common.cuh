@@ -131,7 +131,7 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity, u
   }
 }
 
-// Warp-uniform bounded wait: lane 0 spins (bounded), the verdict is broadcast,
+// Warp-uniform bounded wait: lane 0 spins (bounded), the outcome is broadcast,
 // and on success every lane performs its own acquire of the completed phase
 // (which returns at once).  All lanes of the warp must call it.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *err, unsigned code,

@@ -1,6 +1,6 @@
 """GPU parity of the dequant-GEMV against the float64 oracle.
 
-Bar (spec tolerance): |y_gpu - y_ref| <= 1e-4 * sum_j |deq(W)_ij x_j|
+Bar (the accuracy target of the GEMV): |y_gpu - y_ref| <= 1e-4 * sum_j |deq(W)_ij x_j|
 per row and vector.  Special inputs make exact results exact: a one-hot x
 returns a column of deq(W) bit for bit.
 """

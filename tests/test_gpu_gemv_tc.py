@@ -2,7 +2,7 @@
 oracle, with the engine forced on for every shape (the automatic choice uses
 it only for large matrices and for two or more vectors).
 
-Bar (spec tolerance): |y_gpu - y_ref| <= 1e-4 * sum_j |deq(W)_ij x_j|
+Bar (the accuracy target of the GEMV): |y_gpu - y_ref| <= 1e-4 * sum_j |deq(W)_ij x_j|
 per row and vector.  Shapes cover one and several stages per CTA, ragged row
 counts (rows not a multiple of the 8-row MMA block), every warp split of the
 engine (1 to 16 warps per row block, 1 to 4 superblocks per warp, superblock
