@@ -25,3 +25,22 @@ def test_status_strings(epq_lib):
     assert epq_lib.epq_status_string(0) == "ok"
     assert "align" in epq_lib.epq_status_string(4)
     assert epq_lib.epq_status_string(99) == "unknown status"
+
+
+def test_tuning_keys(epq_lib):
+    """epq_set_tuning returns the previous value, and leaves the setting
+    unchanged (returning -1) for an unknown key or a value out of range."""
+    e = epq_lib
+    cases = [(e.EPQ_TUNE_GEMV_ENGINE, 2, (-1, 3)), (e.EPQ_TUNE_TILE_BYTES, 65536, (4095, 131073)),
+             (e.EPQ_TUNE_RING_BYTES, 65536, (32767, 200705))]
+    for key, value, bad in cases:
+        prev = e.epq_set_tuning(key, value)
+        assert prev >= 0
+        for b in bad:
+            assert e.epq_set_tuning(key, b) == -1
+        assert e.epq_set_tuning(key, prev) == value  # restored; the bad values changed nothing
+    assert e.epq_set_tuning(99, 1) == -1
+
+
+def test_chain_workspace_size(epq_lib):
+    assert epq_lib.epq_gemv_chain_workspace_bytes() >= 8
