@@ -92,11 +92,12 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *   EPQ_TUNE_TILE_BYTES  target packed bytes per pipeline stage of the GEMV
  *                        engines (4096 .. 131072)
  *   EPQ_TUNE_RING_BYTES  shared-memory ring budget per CTA (32768 .. 200704)
- *   EPQ_TUNE_GEMV_ENGINE dense GEMV engine: 0 automatic (Q4_K uses the
- *                        tensor-core engine for two or more vectors and for
- *                        one vector over matrices of >= 2 MiB), 1 CUDA-core
- *                        engines only,
- *                        2 tensor-core engine wherever it applies (Q4_K)
+ *   EPQ_TUNE_GEMV_ENGINE engine of the Q4_K GEMVs and MoE experts:
+ *                        0 automatic (the tensor-core engine for two or more
+ *                        vectors, for one vector over matrices of >= 2 MiB,
+ *                        and for the MoE expert stages), 1 CUDA-core engines
+ *                        only (also for the MoE experts), 2 tensor-core
+ *                        engine wherever it applies
  * Returns the previous value, or -1 for an unknown key or a value out of
  * range (nothing changes then).  Affects launches issued afterwards. */
 enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2, EPQ_TUNE_GEMV_ENGINE = 3 };
