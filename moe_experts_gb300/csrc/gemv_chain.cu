@@ -36,7 +36,6 @@ using namespace tc;
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kKP = 16;   // warps per 8-row block (k-parts)
 constexpr int kNSB = 4;   // superblocks per warp: rows of up to 64 superblocks
 constexpr int kMaxNbs = 3;
 constexpr uint32_t kWarpArea = kFragWarpBytes;  // per-warp staging (prologue) / partial sums (stages)
