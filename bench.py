@@ -123,6 +123,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(v, device="cpu"):
+    """The largest v over the ranks of the process group (a job's time is its
+    slowest rank's); v itself without a group or with a single rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, n_ranks, ms):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time (ms)."""
+    return units_per_rank * n_ranks / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ workloads
 class Workload:
     name = ""
@@ -550,11 +567,7 @@ def run_epq(args):
     kernel_ms = timers.averages()
     clocks = clk.summary()
     err = epq.epq_device_error()
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     # ---- end to end: host (pinned) inputs in, results back to host, per step
     x_host = W.x.cpu().pin_memory()
@@ -589,10 +602,9 @@ def run_epq(args):
             out_host.copy_(res_src, non_blocking=True)
     e3.record(stream)
     e3.synchronize()
-    e2e_ms = e2.elapsed_time(e3) / n_e2e
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / n_e2e, dev)
 
-    units = W.units_per_step * ws
-    value = units / (ms * 1e-3)
+    value = job_rate(W.units_per_step, ws, ms)
     peak, peak_kind = measured_peaks()
     # dominant kernel: largest total time per step
     launches = {k: W.kernels_per_step // len(W.kernel_bytes) for k in W.kernel_bytes}
@@ -617,7 +629,7 @@ def run_epq(args):
         "pct_of_measured_hbm": round(100 * eff_gbs / peak, 2) if eff_gbs else None,
         "pct_of_nominal_8tbs": round(100 * eff_gbs / NOMINAL_HBM_GBS, 2) if eff_gbs else None,
         "roofline": roof, "clocks": clocks, "gpu_launches": W.kernels_per_step * args.steps,
-        "e2e": {"value": round(W.units_per_step * ws / (e2e_ms * 1e-3), 3), "unit": W.unit,
+        "e2e": {"value": round(job_rate(W.units_per_step, ws, e2e_ms), 3), "unit": W.unit,
                 "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4},
         "device_error": err,
     }
