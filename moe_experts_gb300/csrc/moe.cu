@@ -1527,7 +1527,12 @@ epq_status fixed_scratch_ptr(void **out) {
   if (!g_fixed_ptr[dev]) {
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_fixed_scratch);
-    if (e != cudaSuccess || !p) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    if (e != cudaSuccess || !p) {
+      // clear the runtime's sticky last-error slot, so that the next launch
+      // of any entry point does not report this failed lookup as its own
+      cudaGetLastError();
+      return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    }
     g_fixed_ptr[dev] = p;
   }
   *out = g_fixed_ptr[dev];

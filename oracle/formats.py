@@ -88,13 +88,16 @@ def _f16_from_bytes(b: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(b).view("<f2").reshape(-1).astype(np.float16)
 
 
-def _rint_clip(num: np.ndarray, den: np.ndarray, lo: int, hi: int) -> np.ndarray:
-    """clamp(rint(num / den), lo, hi) in float32; 0 where den == 0."""
+def _nearest_codes(w: np.ndarray, step: np.ndarray, offset, lo: int, hi: int) -> np.ndarray:
+    """Codes of an affine grid, in float32: the integer nearest to
+    (w + offset) / step (ties to even), clamped to [lo, hi]; 0 wherever the
+    step is 0 (reading 3)."""
+    w = np.asarray(w, _F32)
+    step = np.asarray(step, _F32)
     with np.errstate(divide="ignore", invalid="ignore"):
-        q = np.rint(np.asarray(num, _F32) / np.asarray(den, _F32))
-    q = np.clip(q, _F32(lo), _F32(hi))
-    q = np.where(np.asarray(den) == 0, _F32(0), q)
-    return q
+        t = (w + np.asarray(offset, _F32)) / step
+    code = np.clip(np.rint(t), _F32(lo), _F32(hi))
+    return np.where(step == 0, _F32(0), code)
 
 
 def _pack_nibbles(n: np.ndarray) -> np.ndarray:
@@ -109,97 +112,6 @@ def _unpack_nibbles(b: np.ndarray) -> np.ndarray:
     out[..., 0::2] = b & 0x0F
     out[..., 1::2] = b >> 4
     return out
-
-
-# ---------------------------------------------------------------- Q8_0
-def _quant_q8_0(b: np.ndarray):
-    """b: [nb, 32] float32 -> (d fp16 [nb], q int8 [nb, 32])."""
-    amax = np.max(np.abs(b), axis=1)
-    d = _f16(amax / _F32(127.0))
-    q = _rint_clip(b, _F(d)[:, None], -127, 127)
-    return d, q.astype(np.int8)
-
-
-def _pack_q8_0(d, q):
-    out = np.empty((d.shape[0], 34), np.uint8)
-    out[:, 0:2] = _f16_bytes(d)
-    out[:, 2:34] = q.view(np.uint8)
-    return out
-
-
-def _deq_q8_0(blk: np.ndarray) -> np.ndarray:
-    d = _F(_f16_from_bytes(blk[:, 0:2]))
-    q = np.ascontiguousarray(blk[:, 2:34]).view(np.int8).astype(_F32)
-    return d[:, None] * q
-
-
-# ---------------------------------------------------------------- Q4_0
-def _quant_q4_0(b: np.ndarray):
-    i_star = np.argmax(np.abs(b), axis=1)            # first index on ties
-    vmax = b[np.arange(b.shape[0]), i_star]          # signed value
-    d = _f16(vmax / _F32(-8.0))
-    q = _rint_clip(b, _F(d)[:, None], -8, 7)
-    return d, (q + _F32(8)).astype(np.uint8)
-
-
-def _pack_q4_0(d, n):
-    out = np.empty((d.shape[0], 18), np.uint8)
-    out[:, 0:2] = _f16_bytes(d)
-    out[:, 2:18] = _pack_nibbles(n)
-    return out
-
-
-def _deq_q4_0(blk):
-    d = _F(_f16_from_bytes(blk[:, 0:2]))
-    n = _unpack_nibbles(blk[:, 2:18]).astype(_F32)
-    return d[:, None] * (n - _F32(8))
-
-
-# ---------------------------------------------------------------- Q4_1
-def _quant_q4_1(b: np.ndarray):
-    lo = np.min(b, axis=1)
-    hi = np.max(b, axis=1)
-    d = _f16((hi - lo) / _F32(15.0))
-    m = _f16(lo)
-    n = _rint_clip(b - _F(m)[:, None], _F(d)[:, None], 0, 15)
-    return d, m, n.astype(np.uint8)
-
-
-def _pack_q4_1(d, m, n):
-    out = np.empty((d.shape[0], 20), np.uint8)
-    out[:, 0:2] = _f16_bytes(d)
-    out[:, 2:4] = _f16_bytes(m)
-    out[:, 4:20] = _pack_nibbles(n)
-    return out
-
-
-def _deq_q4_1(blk):
-    d = _F(_f16_from_bytes(blk[:, 0:2]))
-    m = _F(_f16_from_bytes(blk[:, 2:4]))
-    n = _unpack_nibbles(blk[:, 4:20]).astype(_F32)
-    return n * d[:, None] + m[:, None]
-
-
-# ---------------------------------------------------------------- Q4_K
-def _quant_q4_k(b: np.ndarray):
-    """b: [nsb, 8, 32] float32 superblocks.
-
-    Returns (d, dmin) fp16 [nsb], (c, k) uint8 [nsb, 8], n uint8 [nsb, 8, 32].
-    """
-    lo = np.minimum(np.min(b, axis=2), _F32(0))      # sub-block minimum, clamped <= 0
-    hi = np.max(b, axis=2)
-    sc = (hi - lo) / _F32(15.0)                       # sub-block scale
-    mn = _F32(0) - lo                                 # sub-block min (+0 when lo is 0)
-    d = _f16(np.max(sc, axis=1) / _F32(63.0))
-    dmin = _f16(np.max(mn, axis=1) / _F32(63.0))
-    dF, dminF = _F(d)[:, None], _F(dmin)[:, None]
-    c = _rint_clip(sc, dF, 1, 63)
-    c = np.where(dF == 0, _F32(1), c)                 # reading 3: zero d -> code 1
-    k = _rint_clip(mn, dminF, 0, 63)
-    S = dF * c                                        # exact: 11 x 6 significant bits
-    M = dminF * k
-    n = _rint_clip(b + M[:, :, None], S[:, :, None], 0, 15)
-    return d, dmin, c.astype(np.uint8), k.astype(np.uint8), n.astype(np.uint8)
 
 
 def _pack_scales(c: np.ndarray, k: np.ndarray) -> np.ndarray:
@@ -224,23 +136,110 @@ def _unpack_scales(s: np.ndarray):
     return codes[:, :8], codes[:, 8:]
 
 
-def _pack_q4_k(d, dmin, c, k, n):
-    out = np.empty((d.shape[0], 144), np.uint8)
+# ---------------------------------------------------------------- encoders
+# Every format codes a run of weights on an affine grid w ~ step * n - offset
+# with small integers n; the formats differ in how the grid of a run is
+# chosen and stored.  Each encoder takes runs [nb, run] (float32, -0 already
+# mapped to +0) and returns the packed bytes [nb, block_bytes].
+
+def _encode_q8_0(runs: np.ndarray) -> np.ndarray:
+    """Symmetric grid through 0 whose step puts the largest |w| at 127."""
+    step = _f16(np.max(np.abs(runs), axis=1) / _F32(127.0))
+    n = _nearest_codes(runs, _F(step)[:, None], _F32(0), -127, 127)
+    out = np.empty((runs.shape[0], 34), np.uint8)
+    out[:, 0:2] = _f16_bytes(step)
+    out[:, 2:34] = n.astype(np.int8).view(np.uint8)
+    return out
+
+
+def _encode_q4_0(runs: np.ndarray) -> np.ndarray:
+    """Symmetric grid whose step is the signed weight of largest magnitude
+    (first such index) over -8, so that this weight sits on code -8; codes
+    -8..7 are stored with an offset of 8."""
+    first_peak = np.argmax(np.abs(runs), axis=1)
+    signed_peak = np.take_along_axis(runs, first_peak[:, None], axis=1)[:, 0]
+    step = _f16(signed_peak / _F32(-8.0))
+    n = _nearest_codes(runs, _F(step)[:, None], _F32(0), -8, 7)
+    out = np.empty((runs.shape[0], 18), np.uint8)
+    out[:, 0:2] = _f16_bytes(step)
+    out[:, 2:18] = _pack_nibbles(n + _F32(8))
+    return out
+
+
+def _encode_q4_1(runs: np.ndarray) -> np.ndarray:
+    """Grid from the run's minimum m (stored) with step (max - min) / 15."""
+    lowest, highest = np.min(runs, axis=1), np.max(runs, axis=1)
+    step = _f16((highest - lowest) / _F32(15.0))
+    base = _f16(lowest)
+    n = _nearest_codes(runs, _F(step)[:, None], -_F(base)[:, None], 0, 15)
+    out = np.empty((runs.shape[0], 20), np.uint8)
+    out[:, 0:2] = _f16_bytes(step)
+    out[:, 2:4] = _f16_bytes(base)
+    out[:, 4:20] = _pack_nibbles(n)
+    return out
+
+
+def _encode_q4_k(sbs: np.ndarray) -> np.ndarray:
+    """Two-level grid over superblocks [nsb, 8, 32].  Each sub-block's grid
+    starts at floor = min(its minimum, 0) and spans its range in 15 steps;
+    the eight steps are coded as 6-bit multiples (1..63) of one fp16 factor
+    d = largest step / 63, the eight lifts -floor as 6-bit multiples (0..63)
+    of dmin = largest lift / 63; weights are then coded on the sub-block's
+    stored grid (step c*d, lift k*dmin)."""
+    floor = np.minimum(np.min(sbs, axis=2), _F32(0))
+    sub_step = (np.max(sbs, axis=2) - floor) / _F32(15.0)
+    sub_lift = _F32(0) - floor
+    d = _f16(np.max(sub_step, axis=1) / _F32(63.0))
+    dmin = _f16(np.max(sub_lift, axis=1) / _F32(63.0))
+    dF, dminF = _F(d)[:, None], _F(dmin)[:, None]
+    c = np.where(dF == 0, _F32(1), _nearest_codes(sub_step, dF, _F32(0), 1, 63))
+    k = _nearest_codes(sub_lift, dminF, _F32(0), 0, 63)
+    step = dF * c           # exact: 11 x 6 significant bits
+    lift = dminF * k        # exact
+    n = _nearest_codes(sbs, step[:, :, None], lift[:, :, None], 0, 15)
+    out = np.empty((sbs.shape[0], 144), np.uint8)
     out[:, 0:2] = _f16_bytes(d)
     out[:, 2:4] = _f16_bytes(dmin)
-    out[:, 4:16] = _pack_scales(c, k)
+    out[:, 4:16] = _pack_scales(c.astype(np.uint8), k.astype(np.uint8))
     out[:, 16:144] = _pack_nibbles(n).reshape(-1, 128)
     return out
 
 
-def _deq_q4_k(blk):
+# ---------------------------------------------------------------- decoders
+# w = step * n - offset with one rounding (step * n is exact in float32).
+
+def _decode_q8_0(blk):
+    step = _F(_f16_from_bytes(blk[:, 0:2]))
+    n = np.ascontiguousarray(blk[:, 2:34]).view(np.int8).astype(_F32)
+    return step[:, None] * n
+
+
+def _decode_q4_0(blk):
+    step = _F(_f16_from_bytes(blk[:, 0:2]))
+    n = _unpack_nibbles(blk[:, 2:18]).astype(_F32) - _F32(8)
+    return step[:, None] * n
+
+
+def _decode_q4_1(blk):
+    step = _F(_f16_from_bytes(blk[:, 0:2]))
+    base = _F(_f16_from_bytes(blk[:, 2:4]))
+    n = _unpack_nibbles(blk[:, 4:20]).astype(_F32)
+    return n * step[:, None] + base[:, None]
+
+
+def _decode_q4_k(blk):
     d = _F(_f16_from_bytes(blk[:, 0:2]))
     dmin = _F(_f16_from_bytes(blk[:, 2:4]))
     c, k = _unpack_scales(blk[:, 4:16])
-    S = d[:, None] * c.astype(_F32)                   # [n, 8]
-    M = dmin[:, None] * k.astype(_F32)
+    step = d[:, None] * c.astype(_F32)                 # [n, 8]
+    lift = dmin[:, None] * k.astype(_F32)
     n = _unpack_nibbles(blk[:, 16:144].reshape(-1, 8, 16)).astype(_F32)   # [n, 8, 32]
-    return (n * S[:, :, None] - M[:, :, None]).reshape(-1, 256)
+    return (n * step[:, :, None] - lift[:, :, None]).reshape(-1, 256)
+
+
+_ENCODERS = {Q8_0: (_encode_q8_0, (-1, 32)), Q4_0: (_encode_q4_0, (-1, 32)),
+             Q4_1: (_encode_q4_1, (-1, 32)), Q4_K: (_encode_q4_k, (-1, 8, 32))}
+_DECODERS = {Q8_0: _decode_q8_0, Q4_0: _decode_q4_0, Q4_1: _decode_q4_1, Q4_K: _decode_q4_k}
 
 
 # ---------------------------------------------------------------- public
@@ -252,37 +251,22 @@ def quantize(fmt: int, W: np.ndarray) -> np.ndarray:
     W = W + _F32(0)                                   # reading 6: -0 -> +0
     rows, cols = W.shape
     rb = row_bytes(fmt, cols)
+    if fmt not in _ENCODERS:
+        raise ValueError(f"unknown format {fmt}")
     if rb < 0:
         raise ValueError(f"cols={cols} is not a multiple of {BLOCK_WEIGHTS[fmt]}")
-    if fmt == Q8_0:
-        blk = _pack_q8_0(*_quant_q8_0(W.reshape(-1, 32)))
-    elif fmt == Q4_0:
-        blk = _pack_q4_0(*_quant_q4_0(W.reshape(-1, 32)))
-    elif fmt == Q4_1:
-        blk = _pack_q4_1(*_quant_q4_1(W.reshape(-1, 32)))
-    elif fmt == Q4_K:
-        blk = _pack_q4_k(*_quant_q4_k(W.reshape(-1, 8, 32)))
-    else:
-        raise ValueError(f"unknown format {fmt}")
-    return blk.reshape(rows, rb)
+    encode, run_shape = _ENCODERS[fmt]
+    return encode(W.reshape(run_shape)).reshape(rows, rb)
 
 
 def dequantize(fmt: int, packed: np.ndarray, cols: int) -> np.ndarray:
     """packed uint8 [rows, row_bytes] -> float32 [rows, cols]."""
+    if fmt not in _DECODERS:
+        raise ValueError(f"unknown format {fmt}")
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     rb = row_bytes(fmt, cols)
     rows = packed.size // rb
-    blk = packed.reshape(-1, BLOCK_BYTES[fmt])
-    if fmt == Q8_0:
-        v = _deq_q8_0(blk)
-    elif fmt == Q4_0:
-        v = _deq_q4_0(blk)
-    elif fmt == Q4_1:
-        v = _deq_q4_1(blk)
-    elif fmt == Q4_K:
-        v = _deq_q4_k(blk)
-    else:
-        raise ValueError(f"unknown format {fmt}")
+    v = _DECODERS[fmt](packed.reshape(-1, BLOCK_BYTES[fmt]))
     return np.ascontiguousarray(v, dtype=_F32).reshape(rows, cols)
 
 
