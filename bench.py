@@ -9,19 +9,28 @@ through all 129 dequant-GEMVs, replayed from one CUDA graph.  4.2 GB of
 packed weights stay resident and every step streams all of them, far beyond
 the 129 MB L2, so no flush is needed.
 
-Other workloads (--workload): moe_decode (40 MoE layers, hidden 2048, 256
+Other workloads (--workload): gemv4096 (the single Q4_K 4096x4096
+dequant-GEMV, rotated over ceil(4 L2 / 9.4 MB) = 55 copies per step so that no
+launch finds its weights in L2); moe_decode (40 MoE layers, hidden 2048, 256
 experts of gate/up 512x2048 + down 2048x512, top-8 + shared expert, Zipf(1.1)
 routing, a 64-token decode run per step); moe_layer (one MoE layer of hidden
 4096 with 512 experts of gate/up 2x1024x4096 + down 4096x1024, top-4 + shared
 expert, --ntok 1 or 8 tokens per forward; value = effective weight GB/s).
---chain runs the dense step as one epq_gemv_chain launch instead of one
-launch per matrix.
+The default run also measures gemv4096, moe_layer (1 and 8 tokens) and
+moe_decode and reports each as a sub-object of the headline line
+(--no-sub skips them).  --chain runs the dense step as one epq_gemv_chain
+launch instead of one launch per matrix.
 
 The JSON line carries: value (tok/s for decode workloads, GB/s otherwise),
-roofline of the dominant kernel (live CUDA-event pairs inside the graph),
-e2e (host buffers, H2D + D2H inside the timed region), clocks sampled
-during the timed region, gpu_launches, and the CPU baseline (the oracle on
-a bounded sample).  --impl reference times the oracle itself.
+the mean over the K bracketed steps plus the median and minimum of K
+individually timed replays, the roofline of the dominant kernel (its time
+per launch from a graph of back-to-back launches of that kernel alone on
+distinct weights, programmatic dependent launch as in the step), e2e (host
+buffers, H2D + D2H inside the timed region), clocks sampled during the timed
+region, gpu_launches, and the CPU baseline: the plain C++ oracle's float32
+dequant-GEMV at 1 thread and at all host threads (guided row split) on a
+bounded sample.  --impl reference times that oracle itself, one bounded
+sample per step.
 """
 from __future__ import annotations
 
@@ -155,6 +164,52 @@ def quantize_into(epq, fmt, W, out=None):
     return epq.epq_quantize(fmt, W, blocks=out)
 
 
+class Gemv4096Workload(Workload):
+    """The single Q4_K dequant-GEMV (W 4096x4096 Student-t(5)*0.02, x ~ N(0,1),
+    batch 1), one launch per copy over ceil(4 L2 / row bytes) copies of the
+    packed matrix, so every launch streams its 9.4 MB from HBM.  Launches are
+    chained with programmatic dependent launch as in a decode step (the
+    weights stream while the previous launch drains)."""
+    name = "gemv4096"
+    unit = "GB/s"
+
+    def __init__(self, epq, dev, fmt, nvec=1):
+        import torch
+        from synthetic import workloads as wl
+        self.fmt, self.dev, self.epq, self.nvec = fmt, dev, epq, nvec
+        n = 4096
+        packed = epq.epq_quantize(fmt, wl.weight("gemv4096", 0, 0, n, n, dev))
+        self.matrix_bytes = packed.numel()
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.copies = max(2, math.ceil(4 * l2 / self.matrix_bytes))
+        self.W = packed.unsqueeze(0).repeat(self.copies, 1, 1).contiguous()
+        self.x = wl.activations("gemv4096", nvec, n, dev)
+        self.out = torch.empty((self.copies, nvec, n), dtype=torch.float32, device=dev)
+        self.bytes_per_launch = self.matrix_bytes + 4 * nvec * (n + n)
+        self.units_per_step = self.copies * self.matrix_bytes / 1e9         # weight GB per step
+        self.kernels_per_step = self.copies
+        self.kernel_bytes = {"gemv4096": self.bytes_per_launch}
+        self.launches = {"gemv4096": self.copies}
+        self.full_step_bytes = self.copies * self.matrix_bytes
+
+    def config(self):
+        return {"workload": "gemv4096_q4k", "rows": 4096, "cols": 4096, "nvec": self.nvec, "batch": 1,
+                "packed_bytes": self.matrix_bytes, "copies_per_step": self.copies,
+                "l2": f"{self.copies} rotating copies ({self.copies * self.matrix_bytes / 1e6:.0f} MB > 4x L2)"}
+
+    def step(self, stream, x=None, out=None, timers=None):
+        x = self.x if x is None else x
+        out = self.out if out is None else out
+        for c in range(self.copies):
+            self.epq.epq_gemv_ex(self.fmt, self.W[c], x, 4096, 4096, y=out[c], weights_ready=True, stream=stream)
+
+    def kernel_bench(self, name):
+        return (lambda s: self.step(s)), self.copies
+
+    def cpu_mats(self):
+        return [(self.W[0].cpu().numpy(), 4096)], self.full_step_bytes
+
+
 class MoEDecodeWorkload(Workload):
     name = "moe_decode"
     unit = "tok/s"
@@ -195,7 +250,9 @@ class MoEDecodeWorkload(Workload):
         self.units_per_step = float(self.T)
         self.bytes_per_token = c.layers * (4 * H * rbH + E * H * 4 + (c.topk + 1) * (2 * I * rbH + H * rbI))
         self.kernels_per_step = self.T * c.layers * 5
-        # dominant-kernel candidates: name -> (algorithmic bytes per launch, launches per step)
+        self.launches = {k: self.T * c.layers for k in ("gemv_qkv", "gemv_o", "moe_router", "moe_gateup",
+                                                          "moe_down")}
+        # dominant-kernel candidates: name -> algorithmic bytes per launch
         self.kernel_bytes = {
             "gemv_qkv": 3 * H * rbH + 4 * (H + 3 * H),
             "gemv_o": H * rbH + 4 * (H + 2 * H),
@@ -223,6 +280,54 @@ class MoEDecodeWorkload(Workload):
         out = self.out if out is None else out
         for t in range(self.T):
             self.model.token(x[t:t + 1], out[t:t + 1], stream=stream, timers=timers if t < 64 else None)
+
+    def kernel_bench(self, name):
+        """One launch of the named kernel per layer (40 back to back, each
+        layer's own weights) on the decoder's buffers."""
+        e, c, f, H = self.epq, self.cfg, self.fmt, self.cfg.hidden
+        m = self.model
+        st = {"moe_router": e.EPQ_MOE_ROUTE, "moe_gateup": e.EPQ_MOE_GATE_UP, "moe_down": e.EPQ_MOE_DOWN}
+
+        def run(s):
+            for wqkv, wo, moe in self.layers:
+                if name == "gemv_qkv":
+                    e.epq_gemv_ex(f, wqkv, m.h, 3 * H, H, y=m.qkv, rms_prenorm=True, rms_eps=c.rms_eps,
+                                  weights_ready=True, stream=s)
+                elif name == "gemv_o":
+                    e.epq_gemv_ex(f, wo, m.qkv[:, 2 * H:], H, H, y=self.out[:1], residual=m.h, weights_ready=True,
+                                  stream=s)
+                else:
+                    e.epq_moe_forward(moe, m.h, c.topk, y=self.out[:1], workspace=m.ws, rms_prenorm=True,
+                                      rms_eps=c.rms_eps, stages=st[name], stream=s)
+        return run, c.layers
+
+    def routing_report(self, stream):
+        """Realised expert popularity of one 64-token run (untimed): per layer,
+        the experts' selection counts ranked, pooled over layers; the slope of
+        log(count) on log(rank) over the experts chosen at least once."""
+        import numpy as np
+        import torch
+        c = self.cfg
+        idx = torch.empty((self.T, c.layers, c.topk), dtype=torch.int32, device=self.dev)
+        with torch.cuda.stream(stream):
+            for t in range(self.T):
+                self.model.token(self.x[t:t + 1], self.out[t:t + 1], stream=stream, idx_out=idx[t])
+        stream.synchronize()
+        sel = idx.cpu().numpy()
+        ranked = np.zeros(c.n_experts)
+        touched = []
+        for l in range(c.layers):
+            cnt = np.bincount(sel[:, l, :].reshape(-1), minlength=c.n_experts)
+            touched.append(int((cnt > 0).sum()))
+            ranked += np.sort(cnt)[::-1]
+        ranked /= c.layers
+        r = np.arange(1, c.n_experts + 1)
+        keep = ranked > 0
+        slope = float(np.polyfit(np.log(r[keep]), np.log(ranked[keep]), 1)[0])
+        return {"selections_per_layer": self.T * c.topk, "experts_touched_per_layer_avg": round(float(np.mean(touched)), 1),
+                "rank_frequency_top10": [round(float(v), 2) for v in ranked[:10]],
+                "rank_frequency_at_rank_50_100_150": [round(float(ranked[i]), 2) for i in (49, 99, 149)],
+                "fitted_log_log_slope": round(slope, 3), "router_zipf_s": c.zipf_s}
 
     # ---- oracle on a bounded sample (a few layers of one token)
     def oracle_sample(self, budget_s=20.0):
@@ -325,6 +430,7 @@ class MoELayerWorkload(Workload):
         self.units_per_step = self.R * self.bytes_per_forward / 1e9   # GB per step
         self.tokens_per_step = self.R * ntok
         self.kernels_per_step = 3 * self.R * len(self.chunks)
+        self.launches = {k: self.R * len(self.chunks) for k in ("moe_router", "moe_gateup", "moe_down")}
         # algorithmic bytes of one launch of each kernel (per chunk)
         self.kernel_bytes = {
             "moe_router": E * H * 4 + 4 * ntc * H,
@@ -359,6 +465,19 @@ class MoELayerWorkload(Workload):
                     e.epq_moe_forward(self.layers[r], x[r][t0:t0 + nt], K, y=out[r][t0:t0 + nt], workspace=self.ws,
                                       stages=st, stream=stream)
                     b.record(stream)
+
+    def kernel_bench(self, name):
+        """The named stage of every chunk of every replica's forward, back to
+        back (the same kernels as the timed call)."""
+        e, K = self.epq, self.cfg.topk
+        st = {"moe_router": e.EPQ_MOE_ROUTE, "moe_gateup": e.EPQ_MOE_GATE_UP, "moe_down": e.EPQ_MOE_DOWN}[name]
+
+        def run(s):
+            for r in range(self.R):
+                for t0, nt in self.chunks:
+                    e.epq_moe_forward(self.layers[r], self.x[r][t0:t0 + nt], K, y=self.out[r][t0:t0 + nt],
+                                      workspace=self.ws, stages=st, stream=s)
+        return run, self.R * len(self.chunks)
 
     def extra(self, value):
         return {"tok_per_s": round(value / self.bytes_per_forward * 1e9 * self.ntok, 1),
@@ -426,6 +545,7 @@ class DenseDecodeWorkload(Workload):
         torch.cuda.synchronize()
         from moe_experts_gb300.decode import DenseDecoder
         self.model = DenseDecoder(c, fmt, self.layers, head, dev, nvec=nvec, chain=chain)
+        self.scratch = torch.empty((nvec, H), dtype=torch.float32, device=dev)
         self.chain = chain
         self.x = wl.activations("dense8b", nvec, H, dev)
         self.units_per_step = float(nvec)
@@ -439,6 +559,9 @@ class DenseDecodeWorkload(Workload):
         self.full_step_bytes = full.layers * ((nq + 2 * nkv) * rbH + H * epq.epq_row_bytes(fmt, nq) +
                                               2 * c.inter * rbH + H * rbI) + c.vocab * rbH
         self.kernels_per_step = 1 if chain else c.layers * 4 + 1
+        self.launches = {"gemv_chain": 1} if chain else {"gemv_qkv": c.layers, "gemv_o": c.layers,
+                                                          "gemv_gateup": c.layers, "gemv_down": c.layers,
+                                                          "gemv_head": 1}
         if chain:  # the one launch is the dominant (and only) kernel
             self.kernel_bytes = {"gemv_chain": wbytes + 4 * nvec * (c.layers * (4 * H + 2 * c.inter + nq + 2 * nkv
                                                                                  + H) + H + c.vocab)}
@@ -448,6 +571,7 @@ class DenseDecodeWorkload(Workload):
                 "gemv_o": H * epq.epq_row_bytes(fmt, nq) + 4 * nvec * (nkv + 2 * H),
                 "gemv_gateup": 2 * c.inter * rbH + 4 * nvec * (H + c.inter),
                 "gemv_down": H * rbI + 4 * nvec * (c.inter + 2 * H),
+                "gemv_head": c.vocab * rbH + 4 * nvec * (H + c.vocab),
             }
 
     def config(self):
@@ -461,31 +585,251 @@ class DenseDecodeWorkload(Workload):
     def step(self, stream, x=None, out=None, timers=None):
         self.model.step(self.x if x is None else x, stream=stream, timers=timers)
 
-    def oracle_sample(self, budget_s=20.0):
-        import numpy as np
-        import oracle
+    def kernel_bench(self, name):
+        """The named projection of every layer back to back (each layer's own
+        weights, programmatic dependent launch as in the step) on the
+        decoder's buffers; the LM head four times."""
+        e, c, f, H = self.epq, self.cfg, self.fmt, self.cfg.hidden
+        m = self.model
+        nq, nkv = c.q_rows, c.kv_rows
+        if name == "gemv_chain":
+            return (lambda s: self.step(s)), 1
+
+        def run(s):
+            if name == "gemv_head":
+                for _ in range(4):
+                    e.epq_gemv_ex(f, self.head, m.h, c.vocab, H, y=m.logits, rms_prenorm=True, rms_eps=c.rms_eps,
+                                  weights_ready=True, stream=s)
+                return
+            for wqkv, wo, wgu, wd in self.layers:
+                if name == "gemv_qkv":
+                    e.epq_gemv_ex(f, wqkv, m.h, nq + 2 * nkv, H, y=m.qkv, rms_prenorm=True, rms_eps=c.rms_eps,
+                                  weights_ready=True, stream=s)
+                elif name == "gemv_o":
+                    e.epq_gemv_ex(f, wo, m.qkv[:, nq + nkv:], H, nq, y=self.scratch, residual=m.h,
+                                  x_group=c.heads // c.kv_heads, x_head_dim=c.head_dim, weights_ready=True, stream=s)
+                elif name == "gemv_gateup":
+                    e.epq_gemv_ex(f, wgu, m.h, 2 * c.inter, H, y=m.m, rms_prenorm=True, rms_eps=c.rms_eps,
+                                  swiglu=True, weights_ready=True, stream=s)
+                elif name == "gemv_down":
+                    e.epq_gemv_ex(f, wd, m.m, H, c.inter, y=self.scratch, residual=m.h, weights_ready=True, stream=s)
+        return run, (4 if name == "gemv_head" else c.layers)
+
+    def cpu_mats(self):
+        """A bounded sample for the CPU oracle: layer 0's four projections and
+        1/16 of the LM head rows (packed bytes and columns each)."""
         c = self.cfg
-        H = c.hidden
-        x = self.x.cpu().numpy().astype(np.float64)
-        t0 = time.perf_counter()
-        done = 0
-        nbytes = 0
-        for wqkv, wo, wgu, wd in self.layers:
-            for w, cols in ((wqkv, H), (wgu, H)):
-                p = w.cpu().numpy()
-                oracle.gemv_f64(self.fmt, p, x, cols)
-                nbytes += p.size
-            done += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-        dt = time.perf_counter() - t0
-        # scale by bytes: the sample covered qkv + gate/up of `done` layers
-        rate = nbytes / dt
-        return rate / (self.full_step_bytes / self.nvec), \
-            f"{done} layers' qkv+gate/up GEMVs (oracle, float64), scaled by bytes to the full step"
+        wqkv, wo, wgu, wd = self.layers[0]
+        mats = [(wqkv.cpu().numpy(), c.hidden), (wo.cpu().numpy(), c.q_rows), (wgu.cpu().numpy(), c.hidden),
+                (wd.cpu().numpy(), c.inter), (self.head[:c.vocab // 16].cpu().numpy(), c.hidden)]
+        return mats, self.full_step_bytes
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_gemv_rate(fmt, mats, budget_s, threads):
+    """Bytes/s of the C++ oracle's float32 dequant-GEMV over the sample
+    matrices (packed uint8 [rows, row_bytes], cols), repeated until the
+    budget is spent; returns (bytes per second, passes over the sample)."""
+    import numpy as np
+    from oracle import cref
+    xs = [np.random.default_rng(7).standard_normal((1, cols)).astype(np.float32) for _, cols in mats]
+    ys = [np.empty((1, p.shape[0]), np.float32) for p, _ in mats]
+    nbytes, passes = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        for (p, cols), x, y in zip(mats, xs, ys):
+            cref.gemv_f32(fmt, p, x, cols, threads=threads, out=y)
+            nbytes += p.size
+        passes += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return nbytes / (time.perf_counter() - t0), passes
+
+
+def cpu_baseline_gemv(W, budget_s):
+    """The plain C++ oracle (float32, -O3, no intrinsics) at 1 thread and at
+    every host thread, scaled by packed bytes to the workload's step."""
+    from oracle import cref
+    mats, step_bytes = W.cpu_mats()
+    nthreads = cref.hardware_threads()
+    sample_bytes = sum(p.size for p, _ in mats)
+    out = {}
+    for th in (1, nthreads):
+        rate, passes = cpu_gemv_rate(W.fmt, mats, budget_s / 2, th)
+        out[th] = (rate, passes)
+    to_unit = (lambda r: r / step_bytes * W.units_per_step) if W.unit == "tok/s" else (lambda r: r / 1e9)
+    desc = (f"{len(mats)} matrices, {sample_bytes / 1e6:.0f} MB packed ({W.name}: "
+            + ("layer 0's q/k/v, o, gate/up, down and 1/16 of the LM head" if W.name == "dense8b" else "the matrix")
+            + "), scaled by bytes to the step; C++ oracle float32 dequant-GEMV, guided row split")
+    return {"value": round(to_unit(out[nthreads][0]), 6), "unit": W.unit, "cores": nthreads, "kind": "oracle",
+            "sample": desc, "passes": out[nthreads][1],
+            "single_thread": {"value": round(to_unit(out[1][0]), 6), "cores": 1, "passes": out[1][1]}}
+
+
+def cpu_baseline_moe(W, budget_s):
+    v, sample = W.oracle_sample(budget_s=budget_s)
+    return {"value": round(v, 6), "unit": W.unit, "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
 
 
 # ------------------------------------------------------------------ timing
+def graph_of(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn(stream)
+    return g
+
+
+def time_replays(torch, stream, replay, steps):
+    """Mean over `steps` back-to-back replays bracketed by one event pair,
+    plus the median and minimum of `steps` individually timed replays."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            replay()
+        e1.record(stream)
+    e1.synchronize()
+    mean = e0.elapsed_time(e1) / steps
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in pairs:
+            a.record(stream)
+            replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    per = sorted(a.elapsed_time(b) for a, b in pairs)
+    return mean, statistics.median(per), per[0]
+
+
+def kernel_times(torch, W, stream, reps=3):
+    """Per-launch time of each kernel of the step, in the regime the step runs
+    it: a CUDA graph of N back-to-back launches of that kernel alone (distinct
+    weights, programmatic dependent launch as in the step), CUDA events
+    around `reps` replays; ms per launch."""
+    out = {}
+    for name in W.kernel_bytes:
+        fn, n = W.kernel_bench(name)
+        g = graph_of(torch, stream, fn)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+        mean, _, _ = time_replays(torch, stream, g.replay, reps)
+        out[name] = mean / n
+        del g
+    return out
+
+
+def roofline(W, ktimes, step_ms, peak, peak_kind):
+    if not ktimes:
+        return None
+    dom = max(ktimes, key=lambda k: ktimes[k] * W.launches[k])
+    ach = W.kernel_bytes[dom] / (ktimes[dom] * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get((W.name, dom))
+    total = sum(ktimes[k] * W.launches[k] for k in ktimes)
+    return {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "peak_kind": peak_kind + " copy bandwidth",
+            "traffic": tr[0] if tr else None, "traffic_source": tr[1] if tr else None,
+            "avg_launch_us": round(ktimes[dom] * 1e3, 3), "bytes_per_launch": W.kernel_bytes[dom],
+            "time_source": "graph of back-to-back launches of this kernel alone (distinct weights, PDL as in the "
+                           "step), CUDA events around the replays",
+            "kernels_us": {k: round(v * 1e3, 3) for k, v in ktimes.items()},
+            "launches_per_step": W.launches,
+            "sum_of_kernels_over_step": round(total / step_ms, 3)}
+
+
+def make_workload(epq, dev, fmt, args, name=None, ntok=None):
+    name = name or args.workload
+    if name == "moe_decode":
+        return MoEDecodeWorkload(epq, dev, fmt, layers=args.layers)
+    if name == "moe_layer":
+        return MoELayerWorkload(epq, dev, fmt, ntok=ntok or args.ntok)
+    if name == "gemv4096":
+        return Gemv4096Workload(epq, dev, fmt, nvec=args.nvec)
+    if name == "dense8b":
+        return DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers, chain=args.chain)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def measure_workload(torch, epq, W, stream, steps, warmup, no_graph=False, clk=None):
+    """Warm, capture and time one workload; returns a dict of measurements."""
+    with torch.cuda.stream(stream):
+        W.step(stream)
+    stream.synchronize()
+    assert epq.epq_device_error() == 0, "device-side wait timed out during warm-up"
+    if no_graph:
+        replay = lambda: W.step(stream)
+    else:
+        g = graph_of(torch, stream, W.step)
+        replay = g.replay
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            replay()
+    torch.cuda.synchronize()
+    mean, med, mn = time_replays(torch, stream, replay, steps)
+    return {"ms": mean, "ms_median": med, "ms_min": mn}
+
+
+def e2e_measure(torch, W, stream, steps, no_graph):
+    """Same step with pinned host input copied in and the result read back
+    inside the timed region."""
+    x_host = W.x.cpu().pin_memory()
+    res_dev = W.out if hasattr(W, "out") else W.model.logits
+    out_host = torch.empty(res_dev.shape, dtype=res_dev.dtype).pin_memory()
+    x_dev = torch.empty_like(W.x)
+    out_arg = res_dev if hasattr(W, "out") else None
+    if no_graph:
+        run = lambda: W.step(stream, x=x_dev, out=out_arg)
+    else:
+        g2 = graph_of(torch, stream, lambda s: W.step(s, x=x_dev, out=out_arg))
+        run = g2.replay
+
+    def one():
+        x_dev.copy_(x_host, non_blocking=True)
+        run()
+        out_host.copy_(res_dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(steps, 5))
+    with torch.cuda.stream(stream):
+        e2.record(stream)
+        for _ in range(n):
+            one()
+        e3.record(stream)
+    e3.synchronize()
+    return e2.elapsed_time(e3) / n, x_host.numel() * 4, out_host.numel() * 4
+
+
+def eff_gbs(W, value_per_gpu):
+    return W.bytes_per_token * value_per_gpu / 1e9 if W.unit == "tok/s" else value_per_gpu
+
+
+def sub_object(torch, epq, W, stream, args, peak, peak_kind):
+    """A compact measurement of one more workload for the headline line."""
+    steps = max(5, min(args.steps, 10))
+    m = measure_workload(torch, epq, W, stream, steps, 3)
+    value = W.units_per_step / (m["ms"] * 1e-3)
+    kt = kernel_times(torch, W, stream, reps=2)
+    g = eff_gbs(W, value)
+    obj = {"workload": W.config()["workload"], "value": round(value, 3), "unit": W.unit,
+           "ms_per_step": round(m["ms"], 4), "ms_per_step_median": round(m["ms_median"], 4),
+           "ms_per_step_min": round(m["ms_min"], 4), "steps": steps,
+           "effective_weight_gbs": round(g, 1), "pct_of_measured_hbm": round(100 * g / peak, 2),
+           "roofline": roofline(W, kt, m["ms"], peak, peak_kind), "config": W.config()}
+    if hasattr(W, "extra"):
+        obj.update(W.extra(value))
+    if hasattr(W, "routing_report"):
+        obj["routing"] = W.routing_report(stream)
+    obj["device_error"] = epq.epq_device_error()
+    return obj
+
+
 def run_epq(args):
     import torch
     import moe_experts_gb300 as epq
@@ -501,51 +845,28 @@ def run_epq(args):
     _build.build()
     epq.load()
     fmt = epq.FORMATS[args.fmt]
-    if args.workload == "moe_decode":
-        W = MoEDecodeWorkload(epq, dev, fmt, layers=args.layers)
-    elif args.workload == "moe_layer":
-        W = MoELayerWorkload(epq, dev, fmt, ntok=args.ntok)
-    elif args.workload == "dense8b":
-        W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers, chain=args.chain)
-    else:
-        raise SystemExit(f"unknown workload {args.workload}")
-
+    W = make_workload(epq, dev, fmt, args)
     stream = torch.cuda.Stream(device=dev)
-    # warm the kernels (sets smem attributes) outside capture
-    with torch.cuda.stream(stream):
-        W.step(stream)
-    stream.synchronize()
-    assert epq.epq_device_error() == 0, "device-side wait timed out during warm-up"
-
-    # The timed steps carry no instrumentation.  Per-kernel durations come
-    # from a second capture of the same step with CUDA event pairs around the
-    # kernels of its first layer, replayed after the timed region.
-    timers = Timers(torch, W)
-    if args.no_graph:  # direct launches (for profilers that do not follow graph replays)
-        def replay():
-            W.step(stream)
-
-        def replay_timed():
-            W.step(stream, timers=timers)
-    else:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            W.step(stream)
-        replay = g.replay
-        gt = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gt, stream=stream):
-            W.step(stream, timers=timers)
-        replay_timed = gt.replay
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            replay()
-    torch.cuda.synchronize()
 
     def barrier():
         if ws > 1:
             import torch.distributed as dist
             dist.barrier()
 
+    # warm + capture outside the clock record
+    with torch.cuda.stream(stream):
+        W.step(stream)
+    stream.synchronize()
+    assert epq.epq_device_error() == 0, "device-side wait timed out during warm-up"
+    if args.no_graph:
+        replay = lambda: W.step(stream)
+    else:
+        g = graph_of(torch, stream, W.step)
+        replay = g.replay
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            replay()
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -559,86 +880,55 @@ def run_epq(args):
         e1.synchronize()
         torch.cuda.synchronize()
         barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, min(args.steps, 5))):
-            replay_timed()
-    torch.cuda.synchronize()
-    kernel_ms = timers.averages()
-    clocks = clk.summary()
+        clocks = clk.summary()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    # the same replays timed one by one (median and minimum)
+    _, ms_med, ms_min = time_replays(torch, stream, replay, args.steps)
+    ktimes = kernel_times(torch, W, stream) if not args.no_graph else {}
     err = epq.epq_device_error()
-    ms = max_over_ranks(ms, dev)
-
-    # ---- end to end: host (pinned) inputs in, results back to host, per step
-    x_host = W.x.cpu().pin_memory()
-    out_dev = torch.empty_like(W.out if hasattr(W, "out") else W.model.logits)
-    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
-    x_dev = torch.empty_like(W.x)
-    if args.no_graph:
-        class _Direct:
-            def replay(self):
-                W.step(stream, x=x_dev, out=out_dev if hasattr(W, "out") else None)
-        g2 = _Direct()
-    else:
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            W.step(stream, x=x_dev, out=out_dev if hasattr(W, "out") else None)
-    res_src = out_dev if hasattr(W, "out") else W.model.logits
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            x_dev.copy_(x_host, non_blocking=True)
-            g2.replay()
-            out_host.copy_(res_src, non_blocking=True)
-    torch.cuda.synchronize()
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    n_e2e = max(1, min(args.steps, 5))
-    barrier()
-    e2.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(n_e2e):
-            x_dev.copy_(x_host, non_blocking=True)
-            g2.replay()
-            out_host.copy_(res_src, non_blocking=True)
-    e3.record(stream)
-    e3.synchronize()
-    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / n_e2e, dev)
+    e2e_ms, h2d, d2h = e2e_measure(torch, W, stream, args.steps, args.no_graph)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     value = job_rate(W.units_per_step, ws, ms)
     peak, peak_kind = measured_peaks()
-    # dominant kernel: largest total time per step
-    launches = {k: W.kernels_per_step // len(W.kernel_bytes) for k in W.kernel_bytes}
-    dom = max(kernel_ms, key=lambda k: kernel_ms[k] * launches[k]) if kernel_ms else None
-    roof = None
-    if dom:
-        ach = W.kernel_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_kind": peak_kind + " copy bandwidth",
-                "traffic": NCU_TRAFFIC[(W.name, dom)][0] if (W.name, dom) in NCU_TRAFFIC else None,
-                "traffic_source": NCU_TRAFFIC[(W.name, dom)][1] if (W.name, dom) in NCU_TRAFFIC else None,
-                "avg_launch_us": round(kernel_ms[dom] * 1e3, 3),
-                "bytes_per_launch": W.kernel_bytes[dom],
-                "all_kernels_us": {k: round(v * 1e3, 3) for k, v in kernel_ms.items()}}
-    eff_gbs = W.bytes_per_token * (value / ws) / 1e9 if W.unit == "tok/s" else value / ws
+    g_eff = eff_gbs(W, value / ws)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": W.unit, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "ms_per_step_median": round(ms_med, 4),
+        "ms_per_step_min": round(ms_min, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "q4k weights / f32 activations / f32 accumulate", "data": "synthetic",
         "config": {**W.config(), "parallelism": f"replicas{ws}" if ws > 1 else "single"},
-        "effective_weight_gbs": round(eff_gbs, 1) if eff_gbs else None,
-        "pct_of_measured_hbm": round(100 * eff_gbs / peak, 2) if eff_gbs else None,
-        "pct_of_nominal_8tbs": round(100 * eff_gbs / NOMINAL_HBM_GBS, 2) if eff_gbs else None,
-        "roofline": roof, "clocks": clocks, "gpu_launches": W.kernels_per_step * args.steps,
+        "effective_weight_gbs": round(g_eff, 1),
+        "pct_of_measured_hbm": round(100 * g_eff / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * g_eff / NOMINAL_HBM_GBS, 2),
+        "roofline": roofline(W, ktimes, ms, peak, peak_kind), "clocks": clocks,
+        "gpu_launches": W.kernels_per_step * args.steps,
         "e2e": {"value": round(job_rate(W.units_per_step, ws, e2e_ms), 3), "unit": W.unit,
-                "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": out_host.numel() * 4},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "device_error": err,
     }
     if hasattr(W, "extra"):
         line.update(W.extra(value / ws))
+    if hasattr(W, "routing_report") and rank == 0:
+        line["routing"] = W.routing_report(stream)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, sample = W.oracle_sample(budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(v, 6), "unit": W.unit, "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": sample}
+        if hasattr(W, "cpu_mats"):
+            line["cpu_baseline"] = cpu_baseline_gemv(W, args.cpu_budget)
+        else:
+            line["cpu_baseline"] = cpu_baseline_moe(W, args.cpu_budget)
+    if rank == 0 and ws == 1 and args.workload == "dense8b" and not (args.no_sub or args.chain or args.no_graph):
+        # the other configurations, measured in the same run (compact)
+        del g, replay, W
+        torch.cuda.empty_cache()
+        subs = {}
+        for key, name, ntok in (("gemv4096", "gemv4096", None), ("moe_layer_1tok", "moe_layer", 1),
+                                ("moe_layer_8tok", "moe_layer", 8), ("moe_decode", "moe_decode", None)):
+            Wk = make_workload(epq, dev, fmt, argparse.Namespace(**{**vars(args), "layers": None, "nvec": 1}),
+                               name=name, ntok=ntok)
+            subs[key] = sub_object(torch, epq, Wk, stream, args, peak, peak_kind)
+            del Wk
+            torch.cuda.empty_cache()
+        line["sub_workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -646,69 +936,96 @@ def run_epq(args):
         dist.destroy_process_group()
 
 
-class Timers:
-    """CUDA event pairs recorded (as graph nodes) around each kernel of
-    layer 0 for every token of the step; averaged after the timed region."""
-
-    def __init__(self, torch, W):
-        self.torch = torch
-        self.pairs = {}
-        self.names = list(W.kernel_bytes)
-
-    def pair(self, name):
-        t = self.torch
-        a = t.cuda.Event(enable_timing=True, external=True)
-        b = t.cuda.Event(enable_timing=True, external=True)
-        self.pairs.setdefault(name, []).append((a, b))
-        return a, b
-
-    def averages(self):
-        out = {}
-        for k, ps in self.pairs.items():
-            v = [a.elapsed_time(b) for a, b in ps]
-            out[k] = sum(v) / len(v)
-        return out
-
-
 def run_reference(args):
-    """The oracle, timed on the host cores, on a bounded sample of the same
-    workload (the other ranks of a multi-GPU launch exit without work)."""
+    """The oracle, timed on the host cores: each step is one bounded sample of
+    the same workload (the other ranks of a multi-GPU launch exit without
+    work).  Inputs are drawn with the same generators and packed by the
+    oracle itself."""
     ws, rank, local = dist_env()
     if rank != 0:
         return
+    import numpy as np
     import torch
-    import moe_experts_gb300 as epq
-    from moe_experts_gb300 import build as _build
-    _build.build()
-    epq.load()
-    dev = torch.device(f"cuda:{local}")
-    fmt = epq.FORMATS[args.fmt]
-    # the reference arm only needs the packed weights of the sampled layers
-    if args.workload == "moe_decode":
-        W = MoEDecodeWorkload(epq, dev, fmt, layers=max(1, args.ref_layers))
-        W.cfg = __import__("synthetic.workloads", fromlist=["MoEDecode"]).MoEDecode()
-    elif args.workload == "moe_layer":
-        W = MoELayerWorkload(epq, dev, fmt, ntok=args.ntok, replicas=1)
-    else:
-        W = DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=max(1, args.ref_layers))
-    per_step = args.cpu_budget / max(1, args.steps + args.warmup)
-    vals = []
+    from oracle import cref
+    from synthetic import workloads as wl
+    fmt = {"Q8_0": 0, "Q4_0": 1, "Q4_1": 2, "Q4_K": 3}[args.fmt]
+    nthreads = cref.hardware_threads()
     t_all = time.perf_counter()
-    for i in range(args.warmup + args.steps):
-        v, sample = W.oracle_sample(budget_s=per_step)
-        if i >= args.warmup:
-            vals.append(v)
-    dt = time.perf_counter() - t_all
-    value = statistics.mean(vals)
-    ms = 1e3 * W.units_per_step / value
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": W.unit, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3) if ms else None,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-            "data": "synthetic", "config": W.config(),
-            "cpu_baseline": {"value": round(value, 6), "unit": W.unit, "cores": os.cpu_count(), "kind": "oracle",
+    if args.workload in ("dense8b", "gemv4096"):
+        pack = lambda Wf: cref.quantize(fmt, Wf.numpy(), threads=nthreads)
+        rb = lambda cols: cref.row_bytes(fmt, cols)
+        if args.workload == "dense8b":
+            c = wl.DenseDecode()
+            H, nq, nkv, I, V = c.hidden, c.q_rows, c.kv_rows, c.inter, c.vocab
+            mats = [(np.concatenate([pack(wl.weight("dense8b", 0, 0, nq, H, "cpu")),
+                                     pack(wl.weight("dense8b", 0, 1, nkv, H, "cpu")),
+                                     pack(wl.weight("dense8b", 0, 2, nkv, H, "cpu"))]), H),
+                    (pack(wl.weight("dense8b", 0, 3, H, nq, "cpu")), nq),
+                    (np.concatenate([pack(wl.weight("dense8b", 0, 4, I, H, "cpu")),
+                                     pack(wl.weight("dense8b", 0, 5, I, H, "cpu"))]), H),
+                    (pack(wl.weight("dense8b", 0, 6, H, I, "cpu")), I),
+                    (pack(wl.weight("dense8b", 0, 7, V // 16, H, "cpu")), H)]
+            step_bytes = c.layers * ((nq + 2 * nkv) * rb(H) + H * rb(nq) + 2 * I * rb(H) + H * rb(I)) + V * rb(H)
+            unit, units = "tok/s", float(args.nvec)
+            cfg = {"workload": "dense8b_decode_q4k", "layers": c.layers, "hidden": H, "inter": I, "vocab": V,
+                   "nvec": args.nvec, "batch": 1}
+            desc = "layer 0's q/k/v, o, gate/up, down and 1/16 of the LM head, scaled by bytes to the full step"
+        else:
+            packed = pack(wl.weight("gemv4096", 0, 0, 4096, 4096, "cpu"))
+            mats = [(packed, 4096)]
+            step_bytes = packed.size
+            unit, units = "GB/s", packed.size / 1e9
+            cfg = {"workload": "gemv4096_q4k", "rows": 4096, "cols": 4096, "nvec": args.nvec, "batch": 1}
+            desc = "the 4096x4096 matrix, one GEMV per step"
+        sample_bytes = sum(p.size for p, _ in mats)
+        xs = [np.random.default_rng(3).standard_normal((args.nvec, cols)).astype(np.float32) for _, cols in mats]
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            for (p, cols), x in zip(mats, xs):
+                cref.gemv_f32(fmt, p, x, cols, threads=nthreads)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        t_step = statistics.mean(times)
+        value = units / (t_step * step_bytes / sample_bytes) if unit == "tok/s" else sample_bytes / t_step / 1e9
+        ms_sample = 1e3 * t_step
+        dtype = "f32 (C++ oracle)"
+        sample = (f"{desc}; {sample_bytes / 1e6:.0f} MB packed per step, C++ oracle float32 dequant-GEMV, "
+                  f"{nthreads} threads, guided row split")
+    else:
+        import moe_experts_gb300 as epq
+        from moe_experts_gb300 import build as _build
+        _build.build()
+        epq.load()
+        dev = torch.device(f"cuda:{local}")
+        efmt = epq.FORMATS[args.fmt]
+        if args.workload == "moe_decode":
+            W = MoEDecodeWorkload(epq, dev, efmt, layers=1)
+            W.cfg = wl.MoEDecode()
+        else:
+            W = MoELayerWorkload(epq, dev, efmt, ntok=args.ntok, replicas=1)
+        unit, cfg, dtype = W.unit, W.config(), "f64 (numpy oracle)"
+        per_step = args.cpu_budget / max(1, args.steps + args.warmup)
+        vals, times = [], []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            v, sample = W.oracle_sample(budget_s=per_step)
+            if i >= args.warmup:
+                vals.append(v)
+                times.append(time.perf_counter() - t0)
+        value = statistics.mean(vals)
+        ms_sample = 1e3 * statistics.mean(times)
+        nthreads = os.cpu_count()
+    wall = time.perf_counter() - t_all
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_sample, 3),
+            "ms_per_step_meaning": "wall time of one bounded sample step (what each timed step ran)",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": nthreads, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": round(value, 6), "unit": W.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "wall_s": round(dt, 1)}
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
     print(json.dumps(line), flush=True)
 
 
@@ -718,15 +1035,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="epq", choices=["epq", "reference"])
-    ap.add_argument("--workload", default="dense8b", choices=["dense8b", "moe_decode", "moe_layer"])
+    ap.add_argument("--workload", default="dense8b", choices=["dense8b", "gemv4096", "moe_decode", "moe_layer"])
     ap.add_argument("--ntok", type=int, default=1, help="tokens per MoE layer forward (moe_layer)")
     ap.add_argument("--chain", action="store_true", help="dense step as one epq_gemv_chain launch")
     ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K"])
     ap.add_argument("--nvec", type=int, default=1)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (smaller cases)")
-    ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="skip the other workloads' sub-objects")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly (no CUDA graph)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -98,9 +98,16 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *                        and for the MoE expert stages), 1 CUDA-core engines
  *                        only (also for the MoE experts), 2 tensor-core
  *                        engine wherever it applies
+ *   EPQ_TUNE_EARLY_STAGES pipeline stages the tensor-core GEMV issues before
+ *                        its grid-dependency wait when weights_ready is set
+ *                        (0 .. 16, default 1)
+ *   EPQ_TUNE_TC_SPLIT    warps that share one 8-row block of the tensor-core
+ *                        GEMV (1, 2, 4, 8 or 16; 0 = chosen by shape, the
+ *                        default)
  * Returns the previous value, or -1 for an unknown key or a value out of
  * range (nothing changes then).  Affects launches issued afterwards. */
-enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2, EPQ_TUNE_GEMV_ENGINE = 3 };
+enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2, EPQ_TUNE_GEMV_ENGINE = 3, EPQ_TUNE_EARLY_STAGES = 4,
+       EPQ_TUNE_TC_SPLIT = 5 };
 int epq_set_tuning(int key, int value);
 
 /* ---------------------------------------------------------------- packing
@@ -331,6 +338,35 @@ epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts,
 epq_status epq_moe_forward_noalloc(const epq_router *router, const epq_experts *experts, const float *x,
                                    int ntok, int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx,
                                    float *topk_w, epq_stream_t stream);
+
+/* ---------------------------------------------------------------- attention
+ * epq_attention_decode: one decode step of attention over a Q8_0 key/value
+ * cache with a skip threshold ("smolmaxxing", compute table, row
+ * "带阈值的 Q8_0 注意力": all key dot products first, so the softmax maximum M
+ * is known; positions with score < M + skip_log skip the exponential and the
+ * value read).  Batch 1; query head hq reads key/value head hq / group with
+ * group = n_heads / n_kv_heads (1, 2, 4 or 8).
+ *   q             float32 [n_heads][head_dim]
+ *   k_new, v_new  float32 [n_kv_heads][head_dim]: the step's key and value;
+ *                 they are quantized to Q8_0 (32-element blocks, the
+ *                 packer's arithmetic) and stored at position `pos` first.
+ *   k_cache, v_cache  [n_kv_heads][max_pos][epq_kv_row_bytes(head_dim)]:
+ *                 row (h, p) holds the head_dim/32 fp16 block factors, then
+ *                 the head_dim int8 codes (element = factor * code).  Rows
+ *                 0..pos-1 must hold earlier positions; row pos is written.
+ *   scores s_p = scale * sum_e q[e] * k_p[e] (k dequantized, float32 sums);
+ *   M = max_p s_p; kept positions: s_p >= M + skip_log (skip_log = -inf
+ *   keeps all); out[hq] = sum_kept exp(s_p - M) v_p / sum_kept exp(s_p - M).
+ *   out           float32 [n_heads][head_dim]
+ *   scores_out    NULL or float32 [n_heads][max_pos]: the scores of
+ *                 positions 0..pos (for checking).
+ * Requirements: head_dim 128 or 256, 0 <= pos < max_pos, pos < 16384,
+ * scale > 0, 16-byte aligned pointers.  Deterministic (fixed summation
+ * order).  One launch: a cluster of up to 8 CTAs per key/value head. */
+int64_t epq_kv_row_bytes(int head_dim);
+epq_status epq_attention_decode(const float *q, const float *k_new, const float *v_new, void *k_cache,
+                                void *v_cache, int n_heads, int n_kv_heads, int head_dim, int pos, int max_pos,
+                                float scale, float skip_log, float *out, float *scores_out, epq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -103,6 +103,8 @@ def load(path: str | None = None):
         "epq_gemv_chain": (i32, [i32, ctypes.POINTER(GemvOp), i32, i32, vp, ctypes.c_size_t, vp]),
         "epq_moe_forward_noalloc": (i32, [ctypes.POINTER(Router), ctypes.POINTER(Experts), vp, i32, i32,
                                           ctypes.POINTER(MoeOpts), vp, vp, vp, vp]),
+        "epq_kv_row_bytes": (i64, [i32]),
+        "epq_attention_decode": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -140,7 +142,7 @@ def epq_block_bytes(fmt: int) -> int:
     return int(load().epq_block_bytes(fmt))
 
 
-EPQ_TUNE_TILE_BYTES, EPQ_TUNE_RING_BYTES, EPQ_TUNE_GEMV_ENGINE = 1, 2, 3
+EPQ_TUNE_TILE_BYTES, EPQ_TUNE_RING_BYTES, EPQ_TUNE_GEMV_ENGINE, EPQ_TUNE_EARLY_STAGES, EPQ_TUNE_TC_SPLIT = 1, 2, 3, 4, 5
 
 
 def epq_set_tuning(key: int, value: int) -> int:
@@ -311,3 +313,34 @@ def epq_moe_forward_noalloc(layer: MoELayer, x: torch.Tensor, topk: int, y: torc
         ctypes.byref(layer._r), ctypes.byref(layer._x), _ptr(x), x.shape[0], topk, ctypes.byref(o), _ptr(y),
         _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
     return y
+
+
+# ------------------------------------------------------------------ attention
+def epq_kv_row_bytes(head_dim: int) -> int:
+    return int(load().epq_kv_row_bytes(head_dim))
+
+
+class KVCache:
+    """Device Q8_0 key and value caches of one layer: uint8
+    [n_kv_heads, max_pos, epq_kv_row_bytes(head_dim)] each."""
+
+    def __init__(self, n_kv_heads: int, head_dim: int, max_pos: int, device):
+        rb = epq_kv_row_bytes(head_dim)
+        if rb < 0:
+            raise ValueError(f"head_dim {head_dim} not supported")
+        self.n_kv_heads, self.head_dim, self.max_pos = n_kv_heads, head_dim, max_pos
+        self.k = torch.zeros((n_kv_heads, max_pos, rb), dtype=torch.uint8, device=device)
+        self.v = torch.zeros_like(self.k)
+
+
+def epq_attention_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: KVCache, n_heads: int,
+                         pos: int, scale: float, skip_log: float = float("-inf"), out: torch.Tensor | None = None,
+                         scores_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q [n_heads*D], k_new/v_new [n_kv*D] (float32, device) -> out [n_heads*D]."""
+    lib = load()
+    if out is None:
+        out = torch.empty(n_heads * cache.head_dim, dtype=torch.float32, device=q.device)
+    _check("epq_attention_decode", lib.epq_attention_decode(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cache.k), _ptr(cache.v), n_heads, cache.n_kv_heads, cache.head_dim,
+        int(pos), cache.max_pos, float(scale), float(skip_log), _ptr(out), _ptr(scores_out), _stream(stream)))
+    return out

@@ -67,11 +67,15 @@ namespace {
 std::atomic<int> g_tile_bytes{32 * 1024};
 std::atomic<int> g_ring_bytes{180 * 1024};
 std::atomic<int> g_gemv_engine{0};
+std::atomic<int> g_early_stages{1};
+std::atomic<int> g_tc_split{0};
 }  // namespace
 
 int tune_tile_bytes() { return g_tile_bytes.load(std::memory_order_relaxed); }
 int tune_ring_bytes() { return g_ring_bytes.load(std::memory_order_relaxed); }
 int tune_gemv_engine() { return g_gemv_engine.load(std::memory_order_relaxed); }
+int tune_early_stages() { return g_early_stages.load(std::memory_order_relaxed); }
+int tune_tc_split() { return g_tc_split.load(std::memory_order_relaxed); }
 
 epq_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -109,6 +113,12 @@ int epq_set_tuning(int key, int value) {
     case EPQ_TUNE_GEMV_ENGINE:
       if (value < 0 || value > 2) return -1;
       return epq::g_gemv_engine.exchange(value);
+    case EPQ_TUNE_EARLY_STAGES:
+      if (value < 0 || value > 16) return -1;
+      return epq::g_early_stages.exchange(value);
+    case EPQ_TUNE_TC_SPLIT:
+      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8 && value != 16) return -1;
+      return epq::g_tc_split.exchange(value);
   }
   return -1;
 }

@@ -1,0 +1,365 @@
+// Decode-step attention over a Q8_0 key/value cache with a skip threshold
+// (epq_attention_decode).
+//
+// "smolmaxxing", compute table, row "带阈值的 Q8_0 注意力": the keys and values
+// of the cache are held in Q8_0 blocks; every key dot product of the step is
+// computed first, so the softmax maximum M is known before any exponential,
+// and positions whose score falls below M + ln(1e-4) are skipped -- no
+// exponential and no read of their value row.  The kept positions get the
+// usual softmax weights exp(s - M) / sum exp(s - M) over the kept set.
+//
+// One token (batch 1), grouped heads: query head hq reads key/value head
+// hq / group.  A step appends the token's own key and value (quantized to
+// Q8_0 with the packer's arithmetic) at position `pos` and attends over
+// positions 0..pos.
+//
+// Organisation: one thread-block cluster of C CTAs per key/value head (the
+// positions split evenly over the C CTAs).
+//   phase 0  CTA rank 0 quantizes the new key and value rows into the cache;
+//            a cluster barrier publishes them;
+//   phase 1  each warp takes positions in turn: lane l holds 4 consecutive
+//            elements of the key row (one 32-bit load of codes plus its
+//            block's fp16 factor) and multiplies them with the `group`
+//            query heads kept in shared memory; the warp sums the products;
+//            scores stay in shared memory (and optionally go to scores_out);
+//            each CTA writes its per-head maximum into every cluster CTA's
+//            shared memory (distributed shared memory), one cluster barrier;
+//   phase 2  each CTA forms the weights of its positions against the
+//            cluster-wide maximum, skips the positions below the threshold
+//            (for every query head of the group), accumulates the weighted
+//            value rows and the weight sums, reduces over its warps and
+//            writes the partial into cluster rank 0's shared memory; after a
+//            cluster barrier rank 0 adds the C partials in rank order and
+//            writes out = sum w v / sum w.
+// Every sum runs in a fixed order, so the result is bitwise reproducible.
+// There is no pipeline wait in this kernel (plain loads, cluster barriers
+// that every thread reaches).
+//
+// Cache row layout (this library's own byte order; the values are Q8_0
+// blocks of 32 elements, fp16 factor d and int8 codes q, element = d * q):
+// position p of key/value head h is the D + D/16 byte row at
+// (h * max_pos + p) * (D + D/16): the D/32 fp16 factors first, then the D
+// int8 codes, so that a lane's 4 codes are one aligned 32-bit word.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace epq {
+namespace {
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kMaxGroup = 8;       // query heads per key/value head
+constexpr int kMaxCluster = 8;
+constexpr int kMaxPosPerCta = 2048;
+
+struct AttnParams {
+  const float *q;               // [n_heads][D]
+  const float *k_new, *v_new;   // [n_kv][D] (the step's key and value)
+  uint8_t *k_cache, *v_cache;   // [n_kv][max_pos][row]
+  float *out;                   // [n_heads][D]
+  float *scores;                // NULL or [n_heads][max_pos]
+  int n_kv, D, group, pos, max_pos, C;
+  float scale, skip_log;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v at the shared-memory address `local` of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster(const float *local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Q8_0 of one 32-element run held one element per lane (the packer's
+// arithmetic: factor fp16(max|x| / 127), codes rint(x / factor) clamped to
+// +-127, zero codes for a zero factor).
+__device__ __forceinline__ void q8_block_lane(float x, uint16_t *d_out, int8_t *q_out) {
+  x = __fadd_rn(x, 0.0f);  // -0 -> +0
+  float a = fabsf(x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const __half dh = __float2half_rn(__fdiv_rn(a, 127.0f));
+  const float d = __half2float(dh);
+  float q = 0.0f;
+  if (d != 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(x, d)), -127.0f), 127.0f);
+  *q_out = static_cast<int8_t>(q);
+  if ((threadIdx.x & 31) == 0) *d_out = __half_as_ushort(dh);
+}
+
+__device__ __forceinline__ float i8(uint32_t w, int b) {
+  return static_cast<float>(static_cast<int8_t>((w >> (8 * b)) & 0xFFu));
+}
+
+template <int G>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(16) float sm[];
+  const int D = p.D;
+  const int C = p.C;
+  const uint32_t rank = cluster_rank();
+  const int h = blockIdx.x / C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row_bytes = D + D / 16;
+  const int nblk = D / 32;
+  // positions of this CTA
+  const int npos = p.pos + 1;
+  const int p0 = static_cast<int>((static_cast<int64_t>(rank) * npos) / C);
+  const int p1 = static_cast<int>((static_cast<int64_t>(rank + 1) * npos) / C);
+  const int n = p1 - p0;
+
+  float *qs = sm;                                  // [G][D]
+  float *sc = qs + G * D;                          // [G][kMaxPosPerCta]
+  float *cmax = sc + G * kMaxPosPerCta;            // [C][G] maxima from every cluster CTA
+  float *red = cmax + kMaxCluster * G;             // [warp][G][D + 1]: warp partials
+  float *part = red + kAttnWarps * G * (D + 1);    // [C][G][D + 1]: rank 0 only
+
+  pdl_launch_dependents();
+  pdl_wait();  // q, k_new and v_new come from the preceding projection
+
+  // ---------------------------------------------------------------- phase 0
+  uint8_t *krow_new = p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
+  uint8_t *vrow_new = p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
+  if (rank == 0) {
+    // warps 0..nblk-1 quantize the key blocks, the next nblk warps the value blocks
+    for (int b = warp; b < 2 * nblk; b += kAttnWarps) {
+      const bool isv = b >= nblk;
+      const int bb = isv ? b - nblk : b;
+      const float x = (isv ? p.v_new : p.k_new)[h * D + 32 * bb + lane];
+      uint8_t *row = isv ? vrow_new : krow_new;
+      uint16_t d;
+      int8_t q;
+      q8_block_lane(x, &d, &q);
+      row[2 * nblk + 32 * bb + lane] = static_cast<uint8_t>(q);
+      if (lane == 0) *reinterpret_cast<uint16_t *>(row + 2 * bb) = d;
+    }
+    __threadfence();  // the cache rows precede the release of the cluster barrier
+  }
+  for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = p.q[(h * G + i / D) * D + i % D];
+  cluster_sync();
+
+  // ---------------------------------------------------------------- phase 1
+  // lane l: elements 4l..4l+3 of each 128-element chunk (D/128 chunks)
+  const int nch = D / 128;
+  float wmax[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) wmax[g] = -INFINITY;
+  for (int i = warp; i < n; i += kAttnWarps) {
+    const uint8_t *row = p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i) * row_bytes;
+    float acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+    for (int c = 0; c < nch; ++c) {
+      const int e0 = 128 * c + 4 * lane;
+      const uint32_t w = __ldcg(reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0));
+      const float d = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32)))));
+      const float k0 = d * i8(w, 0), k1 = d * i8(w, 1), k2 = d * i8(w, 2), k3 = d * i8(w, 3);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float4 qv = *reinterpret_cast<const float4 *>(qs + g * D + e0);
+        acc[g] = fmaf(k0, qv.x, fmaf(k1, qv.y, fmaf(k2, qv.z, fmaf(k3, qv.w, acc[g]))));
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float s = warp_sum(acc[g]) * p.scale;
+      wmax[g] = fmaxf(wmax[g], s);
+      if (lane == 0) sc[g * kMaxPosPerCta + i] = s;
+    }
+  }
+  // CTA maxima -> every cluster CTA's cmax[rank][g]
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    if (lane == 0) red[warp * G + g] = wmax[g];  // red holds the warp maxima until phase 2
+  __syncthreads();
+  if (tid < G) {
+    float m = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) m = fmaxf(m, red[w * G + tid]);
+    for (int r = 0; r < C; ++r) st_cluster(&cmax[rank * G + tid], static_cast<uint32_t>(r), m);
+  }
+  if (p.scores) {
+    for (int idx = tid; idx < G * n; idx += kAttnThreads) {
+      const int g = idx / n, i = idx % n;
+      p.scores[static_cast<int64_t>(h * G + g) * p.max_pos + p0 + i] = sc[g * kMaxPosPerCta + i];
+    }
+  }
+  cluster_sync();
+
+  // ---------------------------------------------------------------- phase 2
+  float M[G], thr[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float m = -INFINITY;
+    for (int r = 0; r < C; ++r) m = fmaxf(m, cmax[r * G + g]);
+    M[g] = m;
+    thr[g] = m + p.skip_log;
+  }
+  float o[G][4 * 2];  // up to D = 256: two 128-element chunks of 4 per lane
+  float ws[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    ws[g] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[g][j] = 0.0f;
+  }
+  for (int i = warp; i < n; i += kAttnWarps) {
+    float w[G];
+    bool any = false;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float s = sc[g * kMaxPosPerCta + i];
+      w[g] = s >= thr[g] ? expf(s - M[g]) : 0.0f;
+      any = any || s >= thr[g];
+    }
+    if (!any) continue;  // warp-uniform: every lane read the same scores
+    const uint8_t *row = p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i) * row_bytes;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      if (c >= nch) break;
+      const int e0 = 128 * c + 4 * lane;
+      const uint32_t wv = __ldcg(reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0));
+      const float d = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32)))));
+      const float v0 = d * i8(wv, 0), v1 = d * i8(wv, 1), v2 = d * i8(wv, 2), v3 = d * i8(wv, 3);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        o[g][4 * c + 0] = fmaf(w[g], v0, o[g][4 * c + 0]);
+        o[g][4 * c + 1] = fmaf(w[g], v1, o[g][4 * c + 1]);
+        o[g][4 * c + 2] = fmaf(w[g], v2, o[g][4 * c + 2]);
+        o[g][4 * c + 3] = fmaf(w[g], v3, o[g][4 * c + 3]);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) ws[g] += w[g];
+  }
+  // warp partials -> shared memory, then the CTA sum (warp order) -> rank 0
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float *rw = red + (warp * G + g) * (D + 1);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      if (c >= nch) break;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) rw[128 * c + 4 * lane + j] = o[g][4 * c + j];
+    }
+    if (lane == 0) rw[D] = ws[g];
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * (D + 1); idx += kAttnThreads) {
+    float s = 0.0f;
+    for (int w = 0; w < kAttnWarps; ++w) s += red[w * G * (D + 1) + idx];
+    st_cluster(&part[rank * G * (D + 1) + idx], 0u, s);
+  }
+  cluster_sync();
+  if (rank == 0) {
+    for (int idx = tid; idx < G * D; idx += kAttnThreads) {
+      const int g = idx / D, e = idx % D;
+      float num = 0.0f, den = 0.0f;
+      for (int r = 0; r < C; ++r) {
+        num += part[(r * G + g) * (D + 1) + e];
+        den += part[(r * G + g) * (D + 1) + D];
+      }
+      p.out[(h * G + g) * D + e] = num / den;
+    }
+  }
+}
+
+size_t attn_smem(int G, int D, int C) {
+  return sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * kMaxPosPerCta + kMaxCluster * G +
+                          static_cast<size_t>(kAttnWarps) * G * (D + 1) + static_cast<size_t>(C) * G * (D + 1));
+}
+
+template <int G>
+cudaError_t launch_attn(const AttnParams &p, cudaStream_t s) {
+  auto k = attn_decode_kernel<G>;
+  const size_t smem = attn_smem(G, p.D, p.C);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_kv * p.C));
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+}  // namespace
+}  // namespace epq
+
+using namespace epq;
+
+extern "C" int64_t epq_kv_row_bytes(int head_dim) {
+  if (head_dim <= 0 || head_dim % 128 || head_dim > 256) return -1;
+  return head_dim + head_dim / 16;
+}
+
+extern "C" epq_status epq_attention_decode(const float *q, const float *k_new, const float *v_new, void *k_cache,
+                                           void *v_cache, int n_heads, int n_kv_heads, int head_dim, int pos,
+                                           int max_pos, float scale, float skip_log, float *out, float *scores_out,
+                                           epq_stream_t stream) {
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !out) return EPQ_ERR_ARG;
+  if (n_kv_heads < 1 || n_heads < n_kv_heads || n_heads % n_kv_heads) return EPQ_ERR_SHAPE;
+  const int G = n_heads / n_kv_heads;
+  if (G > kMaxGroup || (G & (G - 1))) return EPQ_ERR_SHAPE;
+  if (epq_kv_row_bytes(head_dim) < 0) return EPQ_ERR_SHAPE;
+  if (max_pos < 1 || pos < 0 || pos >= max_pos) return EPQ_ERR_ARG;
+  if (!(scale > 0.0f) || std::isnan(skip_log)) return EPQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(out) || (scores_out && !aligned16(scores_out)))
+    return EPQ_ERR_ALIGN;
+  // positions per CTA bounded by its shared-memory score buffer
+  int C = 1;
+  while (C < kMaxCluster && (pos + 1 + C - 1) / C > 256) C *= 2;
+  if ((pos + 1 + C - 1) / C > kMaxPosPerCta) return EPQ_ERR_SHAPE;
+  DeviceInfo dev;
+  if (!current_device(&dev) || dev.major * 10 + dev.minor < 100) return EPQ_ERR_DEVICE;
+  AttnParams p;
+  p.q = q;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache = static_cast<uint8_t *>(k_cache);
+  p.v_cache = static_cast<uint8_t *>(v_cache);
+  p.out = out;
+  p.scores = scores_out;
+  p.n_kv = n_kv_heads;
+  p.D = head_dim;
+  p.group = G;
+  p.pos = pos;
+  p.max_pos = max_pos;
+  p.C = C;
+  p.scale = scale;
+  p.skip_log = skip_log;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (G) {
+    case 1: e = launch_attn<1>(p, s); break;
+    case 2: e = launch_attn<2>(p, s); break;
+    case 4: e = launch_attn<4>(p, s); break;
+    case 8: e = launch_attn<8>(p, s); break;
+  }
+  return e == cudaSuccess ? EPQ_OK : cuda_fail(e);
+}

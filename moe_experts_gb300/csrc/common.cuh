@@ -250,6 +250,10 @@ int tune_tile_bytes();
 int tune_ring_bytes();
 // 0 = automatic, 1 = CUDA-core engines only, 2 = tensor-core engine where it applies
 int tune_gemv_engine();
+// stages a tensor-core GEMV issues before its grid-dependency wait (weights_ready)
+int tune_early_stages();
+// k-parts (warps per 8-row block) of the tensor-core GEMV, 0 = chosen by shape
+int tune_tc_split();
 
 // Record a CUDA error for epq_last_cuda_error() and return EPQ_ERR_CUDA.
 epq_status cuda_fail(cudaError_t e);

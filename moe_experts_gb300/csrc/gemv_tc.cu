@@ -80,7 +80,7 @@ struct TcParams {
   int rms;
   float rms_eps;
   int x_group, x_head_dim;
-  int early_weights;
+  int early_weights;  // stages issued before the grid-dependency wait
   unsigned *err;
 };
 
@@ -166,11 +166,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_q4k_tc_kernel(const TcPara
   }
   __syncthreads();
   pdl_launch_dependents();
-  // Weights may stream before the grid-dependency wait, but only one stage:
-  // the x loads issued after the wait would otherwise queue behind this SM's
-  // whole ring of weight copies (~200 KB, several microseconds).  The other
-  // stages are issued once every warp has issued its x loads.
-  const int npre = p.early_weights ? min(1, min(p.stages - L.held, nst)) : 0;
+  // Weights may stream before the grid-dependency wait, but few stages (one
+  // by default, p.early_weights): the x loads issued after the wait would
+  // otherwise queue behind this SM's whole ring of weight copies (~200 KB,
+  // several microseconds).  The other stages are issued once every warp has
+  // issued its x loads.
+  const int npre = min(p.early_weights, min(p.stages - L.held, nst));
   if (tid == 0)
     for (int i = 0; i < npre; ++i) issue(i);
 
@@ -428,6 +429,7 @@ bool gemv_tc_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, co
   const int want = blocks_cta >= 24 ? 4 : (blocks_cta >= 6 ? 2 : 1);
   int kp = 1;
   while (kp < kTcWarps && (nsb + kp - 1) / kp > want) kp *= 2;
+  if (tune_tc_split() > 0 && (nsb + tune_tc_split() - 1) / tune_tc_split() <= 4) kp = tune_tc_split();
   int nsbw = (nsb + kp - 1) / kp;
   nsbw = nsbw <= 1 ? 1 : (nsbw <= 2 ? 2 : 4);
   while (!tc_combo(kp, nsbw) && kp < kTcWarps) {
@@ -488,7 +490,7 @@ cudaError_t gemv_tc_launch(const TcPlan &pl, const TcArgs &a, cudaStream_t s) {
   p.rms_eps = a.rms_eps;
   p.x_group = a.x_group;
   p.x_head_dim = a.x_head_dim;
-  p.early_weights = a.early_weights;
+  p.early_weights = a.early_weights ? tune_early_stages() : 0;
   p.err = a.err;
   const bool sw = a.swiglu != 0;
 #define EPQ_TC_CASE(KP, NSB)                                                                        \

@@ -119,8 +119,10 @@ class MoEDecoder:
         ws = max(layer.workspace_bytes(1, cfg.topk) for (_, _, layer) in layers)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
 
-    def token(self, x, out, stream=None, timers=None):
-        """x [1, H] (read only) -> out [1, H], the hidden state after the last layer."""
+    def token(self, x, out, stream=None, timers=None, idx_out=None):
+        """x [1, H] (read only) -> out [1, H], the hidden state after the last layer.
+
+        idx_out (optional, int32 [layers, topk]): each layer's selected experts."""
         c, f, H = self.cfg, self.fmt, self.cfg.hidden
         h = self.h
         n = len(self.layers)
@@ -142,5 +144,5 @@ class MoEDecoder:
                                           rms_eps=c.rms_eps, stages=st, stream=stream)
             else:
                 L.epq_moe_forward(moe, h, c.topk, y=y, workspace=self.ws, rms_prenorm=True, rms_eps=c.rms_eps,
-                                  stream=stream)
+                                  topk_idx=None if idx_out is None else idx_out[li:li + 1], stream=stream)
         return out

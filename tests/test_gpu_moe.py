@@ -2,10 +2,13 @@
 down + weighted combine + residual) against the float64 oracle.
 
 Acceptance (per token):
-* top-K indices identical to the oracle's; when the oracle's margin between
-  the K-th and (K+1)-th logit is below the router GEMV's error bound the
-  case is "tie-ambiguous" and the GPU's set must merely be valid (every
-  chosen logit within the bound of every unchosen one);
+* top-K indices identical to the oracle's.  A token whose float64 margin
+  between the K-th and (K+1)-th logit is within twice the router GEMV's
+  error bound is "tie-ambiguous" (float32 rounding may legitimately swap
+  the two); such inputs are never accepted silently: the input seed is
+  replaced (deterministically) before anything runs on the GPU, the number
+  of replacements is reported, and the test asserts that the inputs it
+  finally runs have no ambiguous token;
 * stage-wise, as in the EPM page's three-level verification: the SwiGLU
   outputs h (returned through h_out) against the oracle's on the same
   selection; then y against the oracle's down + combine fed with the GPU's
@@ -59,20 +62,40 @@ def _run(epq, layer, x, topk, dev, rms_eps=None):
     return (y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), h.cpu().numpy(), logits.cpu().numpy())
 
 
-def _check_topk(ref, idx_gpu, topk, router, xin):
-    """Identical top-K unless tie-ambiguous; ambiguous cases must be valid."""
-    Abound = np.abs(xin) @ np.abs(router.astype(np.float64)).T      # router GEMV error scale
-    for t in range(idx_gpu.shape[0]):
+def _ambiguous_tokens(ref, topk, router):
+    """Tokens whose K-th / (K+1)-th logit margin is within 2x the router
+    GEMV bound 1e-4 * max_e sum_j |R_ej x_j| (float64 oracle logits)."""
+    Abound = np.abs(ref.xin) @ np.abs(router.astype(np.float64)).T
+    out = []
+    for t in range(ref.logits.shape[0]):
         l = ref.logits[t]
+        if topk >= l.size:
+            continue
         order = np.argsort(-l, kind="stable")
-        margin = l[order[topk - 1]] - (l[order[topk]] if topk < l.size else -np.inf)
-        eps = 1e-4 * Abound[t].max()
-        if margin > eps:
-            assert idx_gpu[t].tolist() == ref.idx[t].tolist(), (t, idx_gpu[t], ref.idx[t])
-        else:
-            chosen = set(idx_gpu[t].tolist())
-            others = [e for e in range(l.size) if e not in chosen]
-            assert min(l[list(chosen)]) >= (max(l[others]) if others else -np.inf) - eps
+        margin = l[order[topk - 1]] - l[order[topk]]
+        if margin <= 2 * TOL * Abound[t].max():
+            out.append(t)
+    return out
+
+
+def _unambiguous_inputs(mw, draw, topk, rms, tries=20):
+    """Draw x with draw(attempt) until no token is tie-ambiguous; returns
+    (x, oracle result, replacements)."""
+    for attempt in range(tries):
+        x = draw(attempt)
+        ref = oracle.moe_forward_f64(mw, x, topk, rms_eps=rms)
+        if not _ambiguous_tokens(ref, topk, mw.router):
+            if attempt:
+                print(f"tie-ambiguous input replaced {attempt} time(s)")
+            return x, ref, attempt
+    raise AssertionError("no unambiguous input found")
+
+
+def _check_topk(ref, idx_gpu, topk, router):
+    """Identical top-K; the inputs were chosen with no ambiguous token."""
+    assert not _ambiguous_tokens(ref, topk, router)
+    for t in range(idx_gpu.shape[0]):
+        assert idx_gpu[t].tolist() == ref.idx[t].tolist(), (t, idx_gpu[t], ref.idx[t])
 
 
 def _stagewise(mw, x, topk, idx, wts, h_gpu, y_gpu, xin, rms=False):
@@ -167,20 +190,17 @@ def test_moe_q4k_engines(epq_lib, cuda_dev, case, engine):
 def _parity_case(epq_lib, cuda_dev, case):
     fmt, E, H, I, topk, ntok, shared, gvec, bias, norm, rms = case
     mw = _make(fmt, E, H, I, seed=E * 100 + H + I + fmt, shared=shared, gate_vec=gvec, bias=bias, norm=norm)
-    x = synthetic.normal((ntok, H), seed=H + ntok, scale=2.0).numpy()
+    draw = lambda a: synthetic.normal((ntok, H), seed=H + ntok + 7919 * a, scale=2.0).numpy()
+    x, ref, _ = _unambiguous_inputs(mw, draw, topk, rms)
     layer = _to_gpu(epq_lib, mw, cuda_dev)
     y, idx, w, h, logits = _run(epq_lib, layer, x, topk, cuda_dev, rms_eps=rms)
-    ref = oracle.moe_forward_f64(mw, x, topk, rms_eps=rms)
     # router logits within the GEMV bound
     Al = np.abs(ref.xin) @ np.abs(mw.router.astype(np.float64)).T
     assert (np.abs(logits - ref.logits) <= TOL * Al + 1e-6).all()
-    _check_topk(ref, idx, topk, mw.router, ref.xin)
-    same = (idx == ref.idx).all()
-    if same:
-        assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
+    _check_topk(ref, idx, topk, mw.router)
+    assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
     _stagewise(mw, x, topk, idx, w, h, y, ref.xin)
-    if same:
-        _end_to_end(mw, x, ref, y)
+    _end_to_end(mw, x, ref, y)
     assert epq_lib.epq_device_error() == 0
 
 
@@ -273,21 +293,18 @@ def test_moe_full_size_layer(epq_lib, cuda_dev, ntok):
                     shared_gate_up=oracle.quantize(fmt, sgu_f.cpu().numpy()),
                     shared_down=oracle.quantize(fmt, sdn_f.cpu().numpy()))
     assert np.array_equal(mw.shared_gate_up, layer.shared_gate_up.cpu().numpy())
-    x = wl.activations("moe_layer", ntok, H, cuda_dev).cpu().numpy()
+    draw = lambda a: wl.activations("moe_layer", ntok, H, cuda_dev, stream_id=a).cpu().numpy()
+    x, ref, _ = _unambiguous_inputs(mw, draw, K, None)
     y, idx, w, h, logits = _run(epq_lib, layer, x, K, cuda_dev)
-    ref = oracle.moe_forward_f64(mw, x, K)
     Al = np.abs(ref.xin) @ np.abs(mw.router.astype(np.float64)).T
     assert (np.abs(logits - ref.logits) <= TOL * Al + 1e-6).all()
-    _check_topk(ref, idx, K, mw.router, ref.xin)
+    _check_topk(ref, idx, K, mw.router)
     for e in sorted(set(idx.flatten().tolist())):
         assert np.array_equal(mw.gate_up[e], gu[e].cpu().numpy()), e
         assert np.array_equal(mw.down[e], dn[e].cpu().numpy()), e
-    same = (idx == ref.idx).all()
-    if same:
-        assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
+    assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
     _stagewise(mw, x, K, idx, w, h, y, ref.xin)
-    if same:
-        _end_to_end(mw, x, ref, y)
+    _end_to_end(mw, x, ref, y)
     assert epq_lib.epq_device_error() == 0
     del gu, dn
     torch.cuda.empty_cache()

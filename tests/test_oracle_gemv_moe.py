@@ -203,3 +203,59 @@ def test_moe_single_expert_all_tokens():
     assert (r.idx == 0).all() and np.allclose(r.w, 1.0)
     o = oracle.expert_forward_f64(Q4_1, mw.gate_up[0], mw.down[0], 256, 256, x)[0]
     assert np.allclose(r.y, x + o, rtol=1e-12)
+
+
+def _diag_q8(value: float, n: int) -> np.ndarray:
+    """Q8_0 packing of value * identity (n x n): each row's only nonzero
+    block holds `value` at the diagonal; value = 127 * 2^-p packs exactly
+    (scale 2^-p, code 127)."""
+    W = np.zeros((n, n), np.float32)
+    np.fill_diagonal(W, value)
+    return oracle.quantize(oracle.Q8_0, W)
+
+
+def test_moe_combine_and_sigmoid_gate_closed_form():
+    """Pins the weighted combine and the sigmoid shared gate with values
+    worked out by hand, independent of the oracle's own expert code.
+
+    Two routed experts with diagonal gate, up and down matrices (every
+    entry exactly representable) and one shared expert.  Expert e maps
+    x_j to o_j = c_e * (a_e x_j) / (1 + exp(-a_e x_j)) * (b_e x_j).  The
+    router sends x_0 = 1 to logits (ln 3, 0), so the softmax weights are
+    exactly (3/4, 1/4); with both chosen and renormalised they stay
+    (3/4, 1/4), with one chosen and renormalised it is 1, without
+    renormalisation 3/4.  The shared gate vector is orthogonal to x, so
+    sigmoid(g . x) = 1/2."""
+    n = 32
+    vals = {0: (127 * 2.0 ** -7, 127 * 2.0 ** -8, 127 * 2.0 ** -6),     # a, b, c per expert
+            1: (127 * 2.0 ** -6, 127 * 2.0 ** -7, 127 * 2.0 ** -9),
+            "s": (127 * 2.0 ** -8, 127 * 2.0 ** -6, 127 * 2.0 ** -7)}
+    gu = {k: np.concatenate([_diag_q8(a, n), _diag_q8(b, n)]) for k, (a, b, _) in vals.items()}
+    dn = {k: _diag_q8(c, n) for k, (_, _, c) in vals.items()}
+    x = np.linspace(-1.5, 1.25, n).astype(np.float32)
+    x[0] = 1.0
+    x[1] = x[2] = np.float32(0.5)
+    R = np.zeros((2, n), np.float32)
+    R[0, 0] = np.float32(np.log(3.0))          # logit of expert 0: ln 3 * x_0
+    g = np.zeros(n, np.float32)
+    g[1], g[2] = 1.0, -1.0                      # g . x = x_1 - x_2 = 0
+    lnw = float(np.float32(np.log(3.0)))        # the logit as stored (float32)
+    p0 = np.exp(lnw) / (np.exp(lnw) + 1.0)      # 3/4 up to float32(ln 3)
+
+    def expert(k):
+        a, b, c = vals[k]
+        xd = x.astype(np.float64)
+        return c * (a * xd) / (1.0 + np.exp(-a * xd)) * (b * xd)
+
+    mw = MoEWeights(fmt=oracle.Q8_0, hidden=n, inter=n, router=R,
+                    gate_up=np.stack([gu[0], gu[1]]), down=np.stack([dn[0], dn[1]]),
+                    shared_gate_up=gu["s"], shared_down=dn["s"], shared_gate_vec=g)
+    for topk, norm, w in ((2, True, (p0, 1 - p0)), (1, True, (1.0,)), (1, False, (p0,))):
+        mw.norm_topk = norm
+        r = oracle.moe_forward_f64(mw, x[None], topk)
+        assert r.idx[0].tolist() == [0, 1][:topk]
+        assert np.allclose(r.w[0], w, rtol=1e-15, atol=0)
+        assert r.shared_gate[0] == 0.5
+        y = x.astype(np.float64) + sum(wk * expert(k) for k, wk in enumerate(w)) + 0.5 * expert("s")
+        assert np.allclose(r.y[0], y, rtol=1e-13, atol=1e-15)
+    assert abs(p0 - 0.75) < 1e-7

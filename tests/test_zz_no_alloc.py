@@ -48,9 +48,28 @@ def _bound(mw, x, ref):
     return b
 
 
-def test_noalloc_matches_workspace_entry(epq_lib, cuda_dev):
-    fmt, E, H, I, topk, ntok = oracle.Q4_K, 16, 1024, 512, 4, 3
-    mw, layer = _layer(epq_lib, cuda_dev, fmt, E, H, I, seed=4321)
+# fmt, E, H, I, topk, ntok, engine (EPQ_TUNE_GEMV_ENGINE)
+CASES = [
+    (oracle.Q4_K, 16, 1024, 512, 4, 3, 0),    # Q4_K, 3 tokens: chunks of two on the tensor-core kernels
+    (oracle.Q4_K, 16, 1024, 512, 4, 3, 1),    # the same on the CUDA-core kernels, one pass
+    (oracle.Q4_0, 16, 1024, 512, 4, 3, 0),    # another format: CUDA-core kernels
+    (oracle.Q4_0, 32, 1024, 1792, 8, 16, 0),  # workspace 1,046,784 B: all but 1.8 KB of the array
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_noalloc_matches_workspace_entry(epq_lib, cuda_dev, case):
+    fmt, E, H, I, topk, ntok, engine = case
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, engine)
+    try:
+        _noalloc_case(epq_lib, cuda_dev, fmt, E, H, I, topk, ntok)
+    finally:
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
+
+
+def _noalloc_case(epq_lib, cuda_dev, fmt, E, H, I, topk, ntok):
+    mw, layer = _layer(epq_lib, cuda_dev, fmt, E, H, I, seed=4321 + I)
+    assert layer.workspace_bytes(ntok, topk) <= (1 << 20)
     x = synthetic.normal((ntok, H), seed=99, scale=2.0).numpy()
     xs = torch.from_numpy(x).to(cuda_dev)
 
