@@ -214,9 +214,10 @@ class MoEDecodeWorkload(Workload):
     name = "moe_decode"
     unit = "tok/s"
 
-    def __init__(self, epq, dev, fmt, layers=None):
+    def __init__(self, epq, dev, fmt, layers=None, attn_ctx=None):
         from synthetic import workloads as wl
         self.cfg = c = wl.MoEDecode() if layers is None else wl.MoEDecode(layers=layers)
+        self.attn_ctx = attn_ctx
         self.fmt, self.dev, self.epq = fmt, dev, epq
         H, I, E = c.hidden, c.inter, c.n_experts
         rbH, rbI = epq.epq_row_bytes(fmt, H), epq.epq_row_bytes(fmt, I)
@@ -243,15 +244,17 @@ class MoEDecodeWorkload(Workload):
             self.layers.append((wqkv, wo, layer))
         torch.cuda.synchronize()
         from moe_experts_gb300.decode import MoEDecoder
-        self.model = MoEDecoder(c, fmt, self.layers, dev)
+        self.model = MoEDecoder(c, fmt, self.layers, dev, attn_ctx=attn_ctx, max_new=c.tokens)
         self.T = c.tokens
         self.x = wl.activations("moe_decode", self.T, H, dev)
         self.out = torch.empty((self.T, H), dtype=torch.float32, device=dev)
         self.units_per_step = float(self.T)
         self.bytes_per_token = c.layers * (4 * H * rbH + E * H * 4 + (c.topk + 1) * (2 * I * rbH + H * rbI))
-        self.kernels_per_step = self.T * c.layers * 5
+        self.kernels_per_step = self.T * c.layers * (5 if attn_ctx is None else 6)
         self.launches = {k: self.T * c.layers for k in ("gemv_qkv", "gemv_o", "moe_router", "moe_gateup",
                                                           "moe_down")}
+        if attn_ctx is not None:
+            self.launches["attention"] = self.T * c.layers
         # dominant-kernel candidates: name -> algorithmic bytes per launch
         self.kernel_bytes = {
             "gemv_qkv": 3 * H * rbH + 4 * (H + 3 * H),
@@ -260,10 +263,16 @@ class MoEDecodeWorkload(Workload):
             "moe_gateup": (c.topk + 1) * 2 * I * rbH + 4 * (H + (c.topk + 1) * I),
             "moe_down": (c.topk + 1) * H * rbI + 4 * ((c.topk + 1) * I + 2 * H),
         }
+        if attn_ctx is not None:  # an upper bound: value rows of skipped positions are not read
+            self.kernel_bytes["attention"] = 2 * c.heads * (attn_ctx + c.tokens // 2) * epq.epq_kv_row_bytes(
+                c.head_dim) + 4 * 4 * H
 
     def config(self):
         c = self.cfg
-        return {"workload": "moe_decode_q4k", "layers": c.layers, "hidden": c.hidden, "experts": c.n_experts,
+        return {"workload": "moe_decode_q4k" + ("" if self.attn_ctx is None else f"_attn{self.attn_ctx}"),
+                "attention": "one-token-context stand-in" if self.attn_ctx is None else
+                f"Q8_0 KV cache, {self.attn_ctx} cached positions + the 64-token run, ln(1e-4) skip threshold",
+                "layers": c.layers, "hidden": c.hidden, "experts": c.n_experts,
                 "inter": c.inter, "topk": c.topk, "shared_experts": 1, "tokens_per_step": c.tokens, "batch": 1,
                 "router": "fp32 zipf(1.1)", "weights_resident_gb": round(self.resident_gb(), 2),
                 "bytes_per_token": self.bytes_per_token, "l2": "inputs larger than L2 (1.1 GB/token)"}
@@ -279,7 +288,8 @@ class MoEDecodeWorkload(Workload):
         x = self.x if x is None else x
         out = self.out if out is None else out
         for t in range(self.T):
-            self.model.token(x[t:t + 1], out[t:t + 1], stream=stream, timers=timers if t < 64 else None)
+            self.model.token(x[t:t + 1], out[t:t + 1], stream=stream, timers=timers if t < 64 else None,
+                             pos=None if self.attn_ctx is None else self.attn_ctx + t)
 
     def kernel_bench(self, name):
         """One launch of the named kernel per layer (40 back to back, each
@@ -289,13 +299,17 @@ class MoEDecodeWorkload(Workload):
         st = {"moe_router": e.EPQ_MOE_ROUTE, "moe_gateup": e.EPQ_MOE_GATE_UP, "moe_down": e.EPQ_MOE_DOWN}
 
         def run(s):
-            for wqkv, wo, moe in self.layers:
-                if name == "gemv_qkv":
+            for li, (wqkv, wo, moe) in enumerate(self.layers):
+                if name == "attention":
+                    q = m.qkv[0]
+                    e.epq_attention_decode(q[:H], q[H:2 * H], q[2 * H:], m.caches[li], c.heads, self.attn_ctx,
+                                           1.0 / math.sqrt(c.head_dim), math.log(1e-4), out=m.attn[0], stream=s)
+                elif name == "gemv_qkv":
                     e.epq_gemv_ex(f, wqkv, m.h, 3 * H, H, y=m.qkv, rms_prenorm=True, rms_eps=c.rms_eps,
                                   weights_ready=True, stream=s)
                 elif name == "gemv_o":
-                    e.epq_gemv_ex(f, wo, m.qkv[:, 2 * H:], H, H, y=self.out[:1], residual=m.h, weights_ready=True,
-                                  stream=s)
+                    e.epq_gemv_ex(f, wo, m.qkv[:, 2 * H:] if self.attn_ctx is None else m.attn, H, H,
+                                  y=self.out[:1], residual=m.h, weights_ready=True, stream=s)
                 else:
                     e.epq_moe_forward(moe, m.h, c.topk, y=self.out[:1], workspace=m.ws, rms_prenorm=True,
                                       rms_eps=c.rms_eps, stages=st[name], stream=s)
@@ -311,7 +325,8 @@ class MoEDecodeWorkload(Workload):
         idx = torch.empty((self.T, c.layers, c.topk), dtype=torch.int32, device=self.dev)
         with torch.cuda.stream(stream):
             for t in range(self.T):
-                self.model.token(self.x[t:t + 1], self.out[t:t + 1], stream=stream, idx_out=idx[t])
+                self.model.token(self.x[t:t + 1], self.out[t:t + 1], stream=stream, idx_out=idx[t],
+                                 pos=None if self.attn_ctx is None else self.attn_ctx + t)
         stream.synchronize()
         sel = idx.cpu().numpy()
         ranked = np.zeros(c.n_experts)
@@ -517,10 +532,11 @@ class DenseDecodeWorkload(Workload):
     name = "dense8b"
     unit = "tok/s"
 
-    def __init__(self, epq, dev, fmt, nvec=1, layers=None, chain=False):
+    def __init__(self, epq, dev, fmt, nvec=1, layers=None, chain=False, attn_ctx=None):
         import torch
         from synthetic import workloads as wl
         self.cfg = c = wl.DenseDecode() if layers is None else wl.DenseDecode(layers=layers)
+        self.attn_ctx = attn_ctx if (nvec == 1 and not chain) else None
         self.fmt, self.dev, self.epq, self.nvec = fmt, dev, epq, nvec
         H = c.hidden
         rbH, rbI = epq.epq_row_bytes(fmt, H), epq.epq_row_bytes(fmt, c.inter)
@@ -544,7 +560,7 @@ class DenseDecodeWorkload(Workload):
         self.head = head
         torch.cuda.synchronize()
         from moe_experts_gb300.decode import DenseDecoder
-        self.model = DenseDecoder(c, fmt, self.layers, head, dev, nvec=nvec, chain=chain)
+        self.model = DenseDecoder(c, fmt, self.layers, head, dev, nvec=nvec, chain=chain, attn_ctx=self.attn_ctx)
         self.scratch = torch.empty((nvec, H), dtype=torch.float32, device=dev)
         self.chain = chain
         self.x = wl.activations("dense8b", nvec, H, dev)
@@ -558,7 +574,7 @@ class DenseDecodeWorkload(Workload):
         full = wl.DenseDecode()
         self.full_step_bytes = full.layers * ((nq + 2 * nkv) * rbH + H * epq.epq_row_bytes(fmt, nq) +
                                               2 * c.inter * rbH + H * rbI) + c.vocab * rbH
-        self.kernels_per_step = 1 if chain else c.layers * 4 + 1
+        self.kernels_per_step = 1 if chain else c.layers * (4 if self.attn_ctx is None else 5) + 1
         self.launches = {"gemv_chain": 1} if chain else {"gemv_qkv": c.layers, "gemv_o": c.layers,
                                                           "gemv_gateup": c.layers, "gemv_down": c.layers,
                                                           "gemv_head": 1}
@@ -573,10 +589,19 @@ class DenseDecodeWorkload(Workload):
                 "gemv_down": H * rbI + 4 * nvec * (c.inter + 2 * H),
                 "gemv_head": c.vocab * rbH + 4 * nvec * (H + c.vocab),
             }
+            if self.attn_ctx is not None:
+                # key and value rows of every cached position and the step's own (value rows of skipped
+                # positions are not read, so this is an upper bound of the bytes streamed)
+                self.kernel_bytes["attention"] = 2 * c.kv_heads * (self.attn_ctx + 1) * epq.epq_kv_row_bytes(
+                    c.head_dim) + 4 * (2 * nq + 2 * nkv)
+                self.launches["attention"] = c.layers
 
     def config(self):
         c = self.cfg
-        return {"workload": f"dense8b_decode_{'q4k' if self.fmt == 3 else self.fmt}", "layers": c.layers,
+        return {"workload": f"dense8b_decode_{'q4k' if self.fmt == 3 else self.fmt}" +
+                ("" if self.attn_ctx is None else f"_attn{self.attn_ctx}"),
+                "attention": "one-token-context stand-in" if self.attn_ctx is None else
+                f"Q8_0 KV cache, {self.attn_ctx} cached positions, ln(1e-4) skip threshold", "layers": c.layers,
                 "launch": "one epq_gemv_chain launch per step" if self.chain else "one launch per matrix",
                 "hidden": c.hidden, "inter": c.inter, "heads": c.heads, "kv_heads": c.kv_heads, "vocab": c.vocab,
                 "nvec": self.nvec, "batch": 1, "weight_bytes_per_step": self.weight_bytes_per_step,
@@ -596,6 +621,12 @@ class DenseDecodeWorkload(Workload):
             return (lambda s: self.step(s)), 1
 
         def run(s):
+            if name == "attention":
+                q = m.qkv[0]
+                for li in range(c.layers):
+                    e.epq_attention_decode(q[:nq], q[nq:nq + nkv], q[nq + nkv:], m.caches[li], c.heads, m.pos,
+                                           1.0 / math.sqrt(c.head_dim), math.log(1e-4), out=m.attn[0], stream=s)
+                return
             if name == "gemv_head":
                 for _ in range(4):
                     e.epq_gemv_ex(f, self.head, m.h, c.vocab, H, y=m.logits, rms_prenorm=True, rms_eps=c.rms_eps,
@@ -605,6 +636,8 @@ class DenseDecodeWorkload(Workload):
                 if name == "gemv_qkv":
                     e.epq_gemv_ex(f, wqkv, m.h, nq + 2 * nkv, H, y=m.qkv, rms_prenorm=True, rms_eps=c.rms_eps,
                                   weights_ready=True, stream=s)
+                elif name == "gemv_o" and self.attn_ctx is not None:
+                    e.epq_gemv_ex(f, wo, m.attn, H, nq, y=self.scratch, residual=m.h, weights_ready=True, stream=s)
                 elif name == "gemv_o":
                     e.epq_gemv_ex(f, wo, m.qkv[:, nq + nkv:], H, nq, y=self.scratch, residual=m.h,
                                   x_group=c.heads // c.kv_heads, x_head_dim=c.head_dim, weights_ready=True, stream=s)
@@ -739,16 +772,19 @@ def roofline(W, ktimes, step_ms, peak, peak_kind):
             "sum_of_kernels_over_step": round(total / step_ms, 3)}
 
 
-def make_workload(epq, dev, fmt, args, name=None, ntok=None):
+def make_workload(epq, dev, fmt, args, name=None, ntok=None, attn_ctx=-1):
     name = name or args.workload
+    if attn_ctx == -1:
+        attn_ctx = args.attn_ctx
     if name == "moe_decode":
-        return MoEDecodeWorkload(epq, dev, fmt, layers=args.layers)
+        return MoEDecodeWorkload(epq, dev, fmt, layers=args.layers, attn_ctx=attn_ctx)
     if name == "moe_layer":
         return MoELayerWorkload(epq, dev, fmt, ntok=ntok or args.ntok)
     if name == "gemv4096":
         return Gemv4096Workload(epq, dev, fmt, nvec=args.nvec)
     if name == "dense8b":
-        return DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers, chain=args.chain)
+        return DenseDecodeWorkload(epq, dev, fmt, nvec=args.nvec, layers=args.layers, chain=args.chain,
+                                   attn_ctx=attn_ctx)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -921,10 +957,12 @@ def run_epq(args):
         del g, replay, W
         torch.cuda.empty_cache()
         subs = {}
-        for key, name, ntok in (("gemv4096", "gemv4096", None), ("moe_layer_1tok", "moe_layer", 1),
-                                ("moe_layer_8tok", "moe_layer", 8), ("moe_decode", "moe_decode", None)):
+        for key, name, ntok, ctx in (("gemv4096", "gemv4096", None, None), ("moe_layer_1tok", "moe_layer", 1, None),
+                                     ("moe_layer_8tok", "moe_layer", 8, None), ("moe_decode", "moe_decode", None, None),
+                                     ("dense8b_attn1024", "dense8b", None, 1024),
+                                     ("moe_decode_attn1024", "moe_decode", None, 1024)):
             Wk = make_workload(epq, dev, fmt, argparse.Namespace(**{**vars(args), "layers": None, "nvec": 1}),
-                               name=name, ntok=ntok)
+                               name=name, ntok=ntok, attn_ctx=ctx)
             subs[key] = sub_object(torch, epq, Wk, stream, args, peak, peak_kind)
             del Wk
             torch.cuda.empty_cache()
@@ -1040,6 +1078,8 @@ def main():
     ap.add_argument("--chain", action="store_true", help="dense step as one epq_gemv_chain launch")
     ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K"])
     ap.add_argument("--nvec", type=int, default=1)
+    ap.add_argument("--attn-ctx", type=int, default=None,
+                    help="decode with KV-cache attention over this many cached positions (dense8b, moe_decode)")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (smaller cases)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

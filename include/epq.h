@@ -100,10 +100,10 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *                        engine wherever it applies
  *   EPQ_TUNE_EARLY_STAGES pipeline stages the tensor-core GEMV issues before
  *                        its grid-dependency wait when weights_ready is set
- *                        (0 .. 16, default 1)
+ *                        (0 .. 16, default 4)
  *   EPQ_TUNE_TC_SPLIT    warps that share one 8-row block of the tensor-core
  *                        GEMV (1, 2, 4, 8 or 16; 0 = chosen by shape, the
- *                        default)
+ *                        default: 8 for rows of 8..32 superblocks)
  * Returns the previous value, or -1 for an unknown key or a value out of
  * range (nothing changes then).  Affects launches issued afterwards. */
 enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2, EPQ_TUNE_GEMV_ENGINE = 3, EPQ_TUNE_EARLY_STAGES = 4,

@@ -67,7 +67,7 @@ namespace {
 std::atomic<int> g_tile_bytes{32 * 1024};
 std::atomic<int> g_ring_bytes{180 * 1024};
 std::atomic<int> g_gemv_engine{0};
-std::atomic<int> g_early_stages{1};
+std::atomic<int> g_early_stages{4};
 std::atomic<int> g_tc_split{0};
 }  // namespace
 

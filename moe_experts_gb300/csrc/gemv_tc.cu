@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_q4k_tc_kernel(const TcPara
   }
   __syncthreads();
   pdl_launch_dependents();
-  // Weights may stream before the grid-dependency wait, but few stages (one
+  // Weights may stream before the grid-dependency wait, but few stages (four
   // by default, p.early_weights): the x loads issued after the wait would
   // otherwise queue behind this SM's whole ring of weight copies (~200 KB,
   // several microseconds).  The other stages are issued once every warp has
@@ -426,9 +426,12 @@ bool gemv_tc_plan(int64_t row_bytes, int cols, int64_t rows_out, bool swiglu, co
   // superblocks per warp and row block: more when a CTA has many blocks (the
   // per-block reduction is then shared by more work), fewer for short CTAs
   // (more warps on each block)
+  // (measured on the dense decode step: 8 warps per block for rows of up to
+  // 32 superblocks beat 4 and 16; wider rows keep 16)
   const int want = blocks_cta >= 24 ? 4 : (blocks_cta >= 6 ? 2 : 1);
   int kp = 1;
   while (kp < kTcWarps && (nsb + kp - 1) / kp > want) kp *= 2;
+  if (nsb <= 32 && nsb >= 8) kp = 8;
   if (tune_tc_split() > 0 && (nsb + tune_tc_split() - 1) / tune_tc_split() <= 4) kp = tune_tc_split();
   int nsbw = (nsb + kp - 1) / kp;
   nsbw = nsbw <= 1 ? 1 : (nsbw <= 2 ? 2 : 4);

@@ -106,3 +106,48 @@ def test_dense_step_full_size_layer(epq_lib, cuda_dev):
     _decoder_matches(m, logits, h)
     del m
     torch.cuda.empty_cache()
+
+
+def test_dense_step_with_kv_attention_equals_isolated_calls(epq_lib, cuda_dev):
+    """Attention mode (epq_attention_decode over a Q8_0 cache of 300
+    positions between the qkv and o projections): the chained step equals
+    the same calls issued in isolation, eagerly and from a CUDA graph."""
+    import math
+    from moe_experts_gb300.decode import SKIP_LOG, DenseDecoder
+    m = _Model(epq_lib, cuda_dev, 1, L=2, seed=13, hd=128)
+    cfg = _Cfg(m)
+    layers = [(m.W[l]["qkv"], m.W[l]["o"], m.W[l]["gu"], m.W[l]["d"]) for l in range(m.L)]
+    dec = DenseDecoder(cfg, Q4K, layers, m.head, m.dev, nvec=1, attn_ctx=300)
+    e, H, nq, nkv = epq_lib, m.H, m.nq, m.nkv
+    # isolated: fresh buffers, a synchronisation after every call
+    h = m.x.clone()
+    for l in range(m.L):
+        W = m.W[l]
+        qkv = e.epq_gemv_ex(Q4K, W["qkv"], h, nq + 2 * nkv, H, rms_prenorm=True, rms_eps=m.eps)
+        torch.cuda.synchronize()
+        att = e.epq_attention_decode(qkv[0, :nq].contiguous(), qkv[0, nq:nq + nkv].contiguous(),
+                                     qkv[0, nq + nkv:].contiguous(), dec.caches[l], cfg.heads, 300,
+                                     1.0 / math.sqrt(cfg.head_dim), SKIP_LOG)
+        torch.cuda.synchronize()
+        h1 = e.epq_gemv_ex(Q4K, W["o"], att.view(1, -1), H, nq, residual=h)
+        torch.cuda.synchronize()
+        mm = e.epq_gemv_ex(Q4K, W["gu"], h1, 2 * m.I, H, swiglu=True, rms_prenorm=True, rms_eps=m.eps)
+        torch.cuda.synchronize()
+        h = e.epq_gemv_ex(Q4K, W["d"], mm, H, m.I, residual=h1)
+        torch.cuda.synchronize()
+    ref = e.epq_gemv_ex(Q4K, m.head, h, m.V, H, rms_prenorm=True, rms_eps=m.eps)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=m.dev)
+    with torch.cuda.stream(s):
+        dec.step(m.x, stream=s)
+    s.synchronize()
+    assert torch.equal(dec.logits, ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dec.step(m.x, stream=s)
+    for _ in range(2):
+        dec.logits.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(dec.logits, ref)
+    assert epq_lib.epq_device_error() == 0
