@@ -30,7 +30,7 @@ renormalisation of the top-K weights and the magnitude of MoE outputs have no
 printed value; both follow the definitions in ``oracle.moe``.
 """
 from .formats import (  # noqa: F401
-    Q8_0, Q4_0, Q4_1, Q4_K, FORMATS, BLOCK_WEIGHTS, BLOCK_BYTES,
+    Q8_0, Q4_0, Q4_1, Q4_K, Q2_K, Q6_K, FORMATS, BLOCK_WEIGHTS, BLOCK_BYTES,
     row_bytes, bits_per_weight, quantize, dequantize, quantize_dequantize,
 )
 from .gemv import gemv_f64, gemv_bound  # noqa: F401

@@ -35,6 +35,14 @@
 //     even j; Q4_K sub-block s owns qs[16s..16s+15]; its 6-bit codes c_0..c_7
 //     then k_0..k_7 form a little-endian 96-bit stream (code t at bits
 //     6t..6t+5).
+//   * Q2_K and Q6_K (named by "smolmaxxing" and by "EPM ... 記憶體怎麼配置的",
+//     which fixes Q6_K at 210 B per 256 weights) follow the same two-level
+//     idea with 16-weight sub-blocks; their rows are stored plane by plane
+//     (nsb superblocks per row):
+//       Q2_K  codes[64 nsb] | sub-block codes c | k << 4 [16 nsb] | f16 d, dmin [nsb]
+//       Q6_K  low nibbles[128 nsb] | high 2 bits[64 nsb] | int8 scales[16 nsb] | f16 d[nsb]
+//     A sub-block's sixteen 2-bit fields (Q2_K codes, Q6_K high parts) share
+//     one little-endian 32-bit word; position i starts at bit kField[i].
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -44,18 +52,21 @@
 
 namespace {
 
-enum { kQ8_0 = 0, kQ4_0 = 1, kQ4_1 = 2, kQ4_K = 3 };
+enum { kQ8_0 = 0, kQ4_0 = 1, kQ4_1 = 2, kQ4_K = 3, kQ2_K = 4, kQ6_K = 5 };
 
-int block_weights(int fmt) { return fmt == kQ4_K ? 256 : (fmt >= 0 && fmt <= 2 ? 32 : -1); }
+int block_weights(int fmt) { return fmt >= kQ4_K && fmt <= kQ6_K ? 256 : (fmt >= 0 && fmt <= 2 ? 32 : -1); }
 int block_bytes(int fmt) {
   switch (fmt) {
     case kQ8_0: return 34;
     case kQ4_0: return 18;
     case kQ4_1: return 20;
     case kQ4_K: return 144;
+    case kQ2_K: return 84;
+    case kQ6_K: return 210;
   }
   return -1;
 }
+bool planar(int fmt) { return fmt == kQ2_K || fmt == kQ6_K; }
 
 // ---------------------------------------------------------------- fp16
 // IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -271,6 +282,130 @@ void q4_k_decode(const uint8_t *in, float *w) {
   }
 }
 
+const int kField[16] = {4, 8, 6, 10, 20, 24, 22, 26, 28, 0, 30, 2, 12, 16, 14, 18};
+
+uint32_t get_word(const uint8_t *p) {
+  return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) | (static_cast<uint32_t>(p[2]) << 16) |
+         (static_cast<uint32_t>(p[3]) << 24);
+}
+void put_word(uint8_t *p, uint32_t v) {
+  for (int b = 0; b < 4; ++b) p[b] = static_cast<uint8_t>(v >> (8 * b));
+}
+int get_field(const uint8_t *words, int i) { return (get_word(words + 4 * (i >> 4)) >> kField[i & 15]) & 3; }
+void or_field(uint8_t *words, int i, int v) {
+  uint8_t *p = words + 4 * (i >> 4);
+  put_word(p, get_word(p) | (static_cast<uint32_t>(v) << kField[i & 15]));
+}
+
+// ---------------------------------------------------------------- Q2_K
+// A superblock of 256 weights = 16 sub-blocks of 16, each an affine grid of
+// four levels from min(sub-block minimum, 0); the sixteen steps are 4-bit
+// multiples c (1..15) of one fp16 factor d = largest step / 15, the lifts
+// 4-bit multiples k (0..15) of dmin = largest lift / 15.  The superblock's
+// entries go to three planes of the row: codes (64 B), sub-block codes
+// (16 B), factors (4 B).
+void q2_k_encode(const float *w, uint8_t *codes, uint8_t *sub, uint8_t *fac) {
+  float step[16], lift[16], step_top = 0.0f, lift_top = 0.0f;
+  for (int s = 0; s < 16; ++s) {
+    float lo = 0.0f, hi = w[16 * s];
+    for (int j = 0; j < 16; ++j) {
+      lo = std::fmin(lo, w[16 * s + j]);
+      hi = std::fmax(hi, w[16 * s + j]);
+    }
+    step[s] = (hi - lo) / 3.0f;
+    lift[s] = 0.0f - lo;
+    step_top = std::fmax(step_top, step[s]);
+    lift_top = std::fmax(lift_top, lift[s]);
+  }
+  const uint16_t dh = f32_to_f16(step_top / 15.0f), mh = f32_to_f16(lift_top / 15.0f);
+  const float d = f16_to_f32(dh), dmin = f16_to_f32(mh);
+  put_f16(fac, dh);
+  put_f16(fac + 2, mh);
+  std::memset(codes, 0, 64);
+  for (int s = 0; s < 16; ++s) {
+    const int c = d == 0.0f ? 1 : code_of(step[s] / d, 1.0f, 15.0f);
+    const int k = dmin == 0.0f ? 0 : code_of(lift[s] / dmin, 0.0f, 15.0f);
+    sub[s] = static_cast<uint8_t>(c | (k << 4));
+    const float S = d * static_cast<float>(c), M = dmin * static_cast<float>(k);  // exact
+    for (int j = 0; j < 16; ++j) {
+      const int i = 16 * s + j;
+      const int n = S == 0.0f ? 0 : code_of((w[i] + M) / S, 0.0f, 3.0f);
+      or_field(codes, i, n);
+    }
+  }
+}
+
+void q2_k_decode(const uint8_t *codes, const uint8_t *sub, const uint8_t *fac, float *w) {
+  const float d = f16_to_f32(get_f16(fac)), dmin = f16_to_f32(get_f16(fac + 2));
+  for (int s = 0; s < 16; ++s) {
+    const float S = d * static_cast<float>(sub[s] & 15), M = dmin * static_cast<float>(sub[s] >> 4);
+    for (int j = 0; j < 16; ++j) {
+      const int i = 16 * s + j;
+      w[i] = static_cast<float>(get_field(codes, i)) * S - M;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- Q6_K
+// A superblock of 256 weights = 16 sub-blocks of 16, symmetric: a
+// sub-block's scale is its signed weight of largest magnitude (first index on
+// ties) over -32, so that weight lands on code -32; the scales are int8
+// multiples of one fp16 factor d = largest |scale| / 127; codes -32..31
+// stored as u = code + 32 in two planes (low nibbles, high 2 bits).
+void q6_k_encode(const float *w, uint8_t *ql, uint8_t *qh, uint8_t *sc, uint8_t *dp) {
+  float scale[16], top = 0.0f;
+  for (int s = 0; s < 16; ++s) {
+    int peak = 16 * s;
+    for (int j = 1; j < 16; ++j)
+      if (std::fabs(w[16 * s + j]) > std::fabs(w[peak])) peak = 16 * s + j;
+    scale[s] = w[peak] / -32.0f;
+    top = std::fmax(top, std::fabs(scale[s]));
+  }
+  const uint16_t dh = f32_to_f16(top / 127.0f);
+  const float d = f16_to_f32(dh);
+  put_f16(dp, dh);
+  std::memset(ql, 0, 128);
+  std::memset(qh, 0, 64);
+  for (int s = 0; s < 16; ++s) {
+    const int c = d == 0.0f ? 0 : code_of(scale[s] / d, -127.0f, 127.0f);
+    sc[s] = static_cast<uint8_t>(static_cast<int8_t>(c));
+    const float S = d * static_cast<float>(c);  // exact
+    for (int j = 0; j < 16; ++j) {
+      const int i = 16 * s + j;
+      const int u = (S == 0.0f ? 0 : code_of(w[i] / S, -32.0f, 31.0f)) + 32;
+      set_nibble(ql, i, u & 15);
+      or_field(qh, i, u >> 4);
+    }
+  }
+}
+
+void q6_k_decode(const uint8_t *ql, const uint8_t *qh, const uint8_t *sc, const uint8_t *dp, float *w) {
+  const float d = f16_to_f32(get_f16(dp));
+  for (int s = 0; s < 16; ++s) {
+    const float S = d * static_cast<float>(static_cast<int8_t>(sc[s]));
+    for (int j = 0; j < 16; ++j) {
+      const int i = 16 * s + j;
+      const int u = get_nibble(ql, i) | (get_field(qh, i) << 4);
+      w[i] = static_cast<float>(u - 32) * S;
+    }
+  }
+}
+
+// Superblock b of a planar row (nsb superblocks): encode / decode in place.
+void encode_planar(int fmt, const float *w, uint8_t *row, int64_t nsb, int64_t b) {
+  if (fmt == kQ2_K)
+    q2_k_encode(w, row + 64 * b, row + 64 * nsb + 16 * b, row + 80 * nsb + 4 * b);
+  else
+    q6_k_encode(w, row + 128 * b, row + 128 * nsb + 64 * b, row + 192 * nsb + 16 * b, row + 208 * nsb + 2 * b);
+}
+
+void decode_planar(int fmt, const uint8_t *row, int64_t nsb, int64_t b, float *w) {
+  if (fmt == kQ2_K)
+    q2_k_decode(row + 64 * b, row + 64 * nsb + 16 * b, row + 80 * nsb + 4 * b, w);
+  else
+    q6_k_decode(row + 128 * b, row + 128 * nsb + 64 * b, row + 192 * nsb + 16 * b, row + 208 * nsb + 2 * b, w);
+}
+
 void encode_block(int fmt, const float *w, uint8_t *out) {
   switch (fmt) {
     case kQ8_0: q8_0_encode(w, out); break;
@@ -354,7 +489,8 @@ int eref_quantize(int fmt, const float *W, int64_t rows, int64_t cols, uint8_t *
       for (int64_t b = 0; b < nb; ++b) {
         const float *src = W + r * cols + b * bw;
         for (int j = 0; j < bw; ++j) buf[j] = src[j] + 0.0f;  // -0 -> +0
-        encode_block(fmt, buf, out + (r * nb + b) * bb);
+        if (planar(fmt)) encode_planar(fmt, buf, out + r * nb * bb, nb, b);
+        else encode_block(fmt, buf, out + (r * nb + b) * bb);
       }
   });
   return 0;
@@ -365,7 +501,10 @@ int eref_dequantize(int fmt, const uint8_t *blocks, int64_t rows, int64_t cols, 
   const int bw = block_weights(fmt), bb = block_bytes(fmt);
   const int64_t nb = cols / bw;
   for (int64_t r = 0; r < rows; ++r)
-    for (int64_t b = 0; b < nb; ++b) decode_block(fmt, blocks + (r * nb + b) * bb, out + r * cols + b * bw);
+    for (int64_t b = 0; b < nb; ++b) {
+      if (planar(fmt)) decode_planar(fmt, blocks + r * nb * bb, nb, b, out + r * cols + b * bw);
+      else decode_block(fmt, blocks + (r * nb + b) * bb, out + r * cols + b * bw);
+    }
   return 0;
 }
 
@@ -383,7 +522,8 @@ int eref_gemv_f64(int fmt, const uint8_t *blocks, const float *x, int64_t rows, 
         double acc = 0.0, mag = 0.0;
         const float *xv = x + v * cols;
         for (int64_t b = 0; b < nb; ++b) {
-          decode_block(fmt, blocks + (r * nb + b) * bb, w);
+          if (planar(fmt)) decode_planar(fmt, blocks + r * nb * bb, nb, b, w);
+          else decode_block(fmt, blocks + (r * nb + b) * bb, w);
           for (int j = 0; j < bw; ++j) {
             const double t = static_cast<double>(w[j]) * static_cast<double>(xv[b * bw + j]);
             acc += t;
@@ -411,7 +551,8 @@ int eref_gemv_f32(int fmt, const uint8_t *blocks, const float *x, int64_t rows, 
     for (int64_t r = r0; r < r1; ++r) {
       float part[8][8] = {};
       for (int64_t b = 0; b < nb; ++b) {
-        decode_block(fmt, blocks + (r * nb + b) * bb, w);
+        if (planar(fmt)) decode_planar(fmt, blocks + r * nb * bb, nb, b, w);
+        else decode_block(fmt, blocks + (r * nb + b) * bb, w);
         for (int v = 0; v < nvec; ++v) {
           const float *xv = x + v * cols + b * bw;
           for (int j = 0; j < bw; j += 8)

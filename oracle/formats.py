@@ -15,6 +15,22 @@ Oracle code (test infrastructure only).  Follows the handbook page
   coded in 6 bits against two fp16 superblock factors (largest scale / 63
   and largest min / 63).  Scale codes are kept in 1..63, min codes in 0..63.
 
+Two more K-quant formats that the pages name without defining them -- Q2_K
+(the 2-bit experts of "smolmaxxing" and the 2-bit experts of "Flash-MoE")
+and Q6_K (the down projections of "EPM ... 記憶體怎麼配置的", 2,039,808 B per
+expert, i.e. 210 B per 256 weights) -- follow the same two-level idea at
+the sizes those pages fix:
+
+* Q2_K: superblocks of 256 = 16 sub-blocks of 16 weights; per sub-block an
+  affine grid of 4 levels (step = range over 3 from min(min, 0), lift =
+  -that floor), steps and lifts coded as 4-bit multiples of two fp16
+  factors (largest / 15); 2-bit codes.  84 B per superblock (2.625 bits).
+* Q6_K: superblocks of 256 = 16 sub-blocks of 16; symmetric like Q4_0: the
+  sub-block scale is its signed largest-magnitude weight over -32 (that
+  weight lands on code -32), coded as an int8 multiple of one fp16 factor
+  (largest |scale| / 127); 6-bit codes -32..31.  210 B per superblock
+  (6.5625 bits).  A Q6_K weight is exact in float32 (18 x 6 bits).
+
 Readings where the page is silent (each is listed in the design notes):
 
 1. All quantizer arithmetic is IEEE float32: true division, ``rint`` with
@@ -36,6 +52,20 @@ Readings where the page is silent (each is listed in the design notes):
    six-bit codes (8 scale codes then 8 min codes) form a little-endian
    96-bit stream, code t at bits 6t..6t+5.  Rows are contiguous and blocks
    run in column order within a row.
+   Q2_K and Q6_K rows are stored plane by plane (every plane's entries stay
+   aligned to their own size for wide loads), for a row of nsb superblocks:
+     Q2_K  codes[64 nsb] | sub-block codes[16 nsb] | f16 (d, dmin)[nsb]
+           sub-block s of a superblock owns the little-endian 32-bit word
+           s of its 64 code bytes; sub-block code byte = c | k << 4
+     Q6_K  low nibbles[128 nsb] | high bits[64 nsb] | int8 scale codes[16 nsb]
+           | f16 d[nsb]; u = code + 32 in 0..63: u & 15 of superblock
+           weight j in byte j>>1 of its 128 (low nibble when j is even);
+           u >> 4 of sub-block s in word s of its 64 high-bit bytes
+   A 2-bit field (a Q2_K code, a Q6_K high part) of position i = 0..15 of a
+   sub-block starts at bit FIELD[i] of the sub-block's word, FIELD = (4, 8,
+   6, 10, 20, 24, 22, 26, 28, 0, 30, 2, 12, 16, 14, 18): an order that lets
+   a decoder reach two fields at a time in fp16 mantissa position with one
+   mask, after at most one shift and one rotation of the word.
 6. Signed zeros: inputs are first mapped ``x -> x + 0`` (so -0 becomes +0)
    and the Q4_K min is formed as ``0 - lo``; every max/min then has one
    well-defined result and a zero factor is always +0 (Q4_0's factor of an
@@ -46,11 +76,11 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_0, Q4_1, Q4_K = 0, 1, 2, 3
-FORMATS = (Q8_0, Q4_0, Q4_1, Q4_K)
-NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_1: "Q4_1", Q4_K: "Q4_K"}
-BLOCK_WEIGHTS = {Q8_0: 32, Q4_0: 32, Q4_1: 32, Q4_K: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_1: 20, Q4_K: 144}
+Q8_0, Q4_0, Q4_1, Q4_K, Q2_K, Q6_K = 0, 1, 2, 3, 4, 5
+FORMATS = (Q8_0, Q4_0, Q4_1, Q4_K, Q2_K, Q6_K)
+NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_1: "Q4_1", Q4_K: "Q4_K", Q2_K: "Q2_K", Q6_K: "Q6_K"}
+BLOCK_WEIGHTS = {Q8_0: 32, Q4_0: 32, Q4_1: 32, Q4_K: 256, Q2_K: 256, Q6_K: 256}
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_1: 20, Q4_K: 144, Q2_K: 84, Q6_K: 210}
 
 _F32 = np.float32
 
@@ -205,6 +235,76 @@ def _encode_q4_k(sbs: np.ndarray) -> np.ndarray:
     return out
 
 
+def _encode_q2_k(sbs: np.ndarray):
+    """Superblocks [nsb, 16, 16] -> planes (codes [nsb, 64], sub-block codes
+    [nsb, 16], factors [nsb, 4])."""
+    floor = np.minimum(np.min(sbs, axis=2), _F32(0))
+    sub_step = (np.max(sbs, axis=2) - floor) / _F32(3.0)
+    sub_lift = _F32(0) - floor
+    d = _f16(np.max(sub_step, axis=1) / _F32(15.0))
+    dmin = _f16(np.max(sub_lift, axis=1) / _F32(15.0))
+    dF, dminF = _F(d)[:, None], _F(dmin)[:, None]
+    c = np.where(dF == 0, _F32(1), _nearest_codes(sub_step, dF, _F32(0), 1, 15))
+    k = _nearest_codes(sub_lift, dminF, _F32(0), 0, 15)
+    step = dF * c           # exact: 11 x 4 significant bits
+    lift = dminF * k        # exact
+    n = _nearest_codes(sbs, step[:, :, None], lift[:, :, None], 0, 3)
+    codes = _fields_to_words(n).reshape(-1, 64)
+    sub = (c.astype(np.uint8) | (k.astype(np.uint8) << 4)).astype(np.uint8)
+    fac = np.concatenate([_f16_bytes(d), _f16_bytes(dmin)], axis=1)
+    return codes, sub, fac
+
+
+def _encode_q6_k(sbs: np.ndarray):
+    """Superblocks [nsb, 16, 16] -> planes (low nibbles [nsb, 128], high bits
+    [nsb, 64], scale codes [nsb, 16], factor [nsb, 2])."""
+    first_peak = np.argmax(np.abs(sbs), axis=2)
+    signed_peak = np.take_along_axis(sbs, first_peak[:, :, None], axis=2)[:, :, 0]
+    sub_scale = signed_peak / _F32(-32.0)
+    d = _f16(np.max(np.abs(sub_scale), axis=1) / _F32(127.0))
+    dF = _F(d)[:, None]
+    c = _nearest_codes(sub_scale, dF, _F32(0), -127, 127)
+    step = dF * c           # exact: 11 x 7 significant bits
+    n = _nearest_codes(sbs, step[:, :, None], _F32(0), -32, 31)
+    u = (n + _F32(32)).astype(np.uint8).reshape(-1, 256)
+    ql = (u[:, 0::2] & 15) | ((u[:, 1::2] & 15) << 4)
+    qh = _fields_to_words((u >> 4).reshape(-1, 16, 16)).reshape(-1, 64)
+    return ql.astype(np.uint8), qh, c.astype(np.int8).view(np.uint8), _f16_bytes(d)
+
+
+FIELD = (4, 8, 6, 10, 20, 24, 22, 26, 28, 0, 30, 2, 12, 16, 14, 18)
+
+
+def _fields_to_words(f: np.ndarray) -> np.ndarray:
+    """2-bit values [n, 16 sub-blocks, 16 positions] -> [n, 16 * 4] bytes:
+    one little-endian word per sub-block, position i at bit FIELD[i]."""
+    f = np.asarray(f).astype(np.uint32)
+    words = np.zeros(f.shape[:2], np.uint32)
+    for i, b in enumerate(FIELD):
+        words |= f[:, :, i] << np.uint32(b)
+    return np.ascontiguousarray(words.astype("<u4")).view(np.uint8).reshape(f.shape[0], -1)
+
+
+def _words_to_fields(b: np.ndarray) -> np.ndarray:
+    """Inverse of _fields_to_words: [n, 64] bytes -> [n, 16, 16] values."""
+    words = np.ascontiguousarray(b).view("<u4").reshape(b.shape[0], 16).astype(np.uint32)
+    return np.stack([(words >> np.uint32(FIELD[i])) & np.uint32(3) for i in range(16)], axis=2)
+
+
+def _rows_from_planes(planes, rows: int):
+    """Per-superblock planes [rows * nsb, w] -> rows of consecutive planes."""
+    return np.concatenate([p.reshape(rows, -1) for p in planes], axis=1)
+
+
+def _planes_of_rows(packed: np.ndarray, nsb: int, widths):
+    """Inverse of _rows_from_planes: [rows, sum(w) * nsb] -> [rows * nsb, w] each."""
+    out, o = [], 0
+    for w in widths:
+        out.append(np.ascontiguousarray(packed[:, o:o + w * nsb]).reshape(-1, w))
+        o += w * nsb
+    return out
+
+
 # ---------------------------------------------------------------- decoders
 # w = step * n - offset with one rounding (step * n is exact in float32).
 
@@ -237,6 +337,31 @@ def _decode_q4_k(blk):
     return (n * step[:, :, None] - lift[:, :, None]).reshape(-1, 256)
 
 
+def _decode_q2_k(codes, sub, fac):
+    d = _F(_f16_from_bytes(fac[:, 0:2]))
+    dmin = _F(_f16_from_bytes(fac[:, 2:4]))
+    c = (sub & 15).astype(_F32)
+    k = (sub >> 4).astype(_F32)
+    step = d[:, None] * c                              # [n, 16]
+    lift = dmin[:, None] * k
+    n = _words_to_fields(codes).astype(_F32)
+    return (n * step[:, :, None] - lift[:, :, None]).reshape(-1, 256)
+
+
+def _decode_q6_k(ql, qh, sc, dbytes):
+    d = _F(_f16_from_bytes(dbytes))
+    c = sc.view(np.int8).astype(_F32)
+    step = d[:, None] * c
+    lo = np.empty((ql.shape[0], 256), np.uint8)
+    lo[:, 0::2] = ql & 15
+    lo[:, 1::2] = ql >> 4
+    hi = _words_to_fields(qh).reshape(-1, 256).astype(np.uint8)
+    n = (lo | (hi << 4)).astype(_F32) - _F32(32)
+    return (n.reshape(-1, 16, 16) * step[:, :, None]).reshape(-1, 256)
+
+
+_PLANES = {Q2_K: (_encode_q2_k, _decode_q2_k, (64, 16, 4)), Q6_K: (_encode_q6_k, _decode_q6_k, (128, 64, 16, 2))}
+
 _ENCODERS = {Q8_0: (_encode_q8_0, (-1, 32)), Q4_0: (_encode_q4_0, (-1, 32)),
              Q4_1: (_encode_q4_1, (-1, 32)), Q4_K: (_encode_q4_k, (-1, 8, 32))}
 _DECODERS = {Q8_0: _decode_q8_0, Q4_0: _decode_q4_0, Q4_1: _decode_q4_1, Q4_K: _decode_q4_k}
@@ -251,21 +376,27 @@ def quantize(fmt: int, W: np.ndarray) -> np.ndarray:
     W = W + _F32(0)                                   # reading 6: -0 -> +0
     rows, cols = W.shape
     rb = row_bytes(fmt, cols)
-    if fmt not in _ENCODERS:
+    if fmt not in _ENCODERS and fmt not in _PLANES:
         raise ValueError(f"unknown format {fmt}")
     if rb < 0:
         raise ValueError(f"cols={cols} is not a multiple of {BLOCK_WEIGHTS[fmt]}")
+    if fmt in _PLANES:
+        return _rows_from_planes(_PLANES[fmt][0](W.reshape(-1, 16, 16)), rows)
     encode, run_shape = _ENCODERS[fmt]
     return encode(W.reshape(run_shape)).reshape(rows, rb)
 
 
 def dequantize(fmt: int, packed: np.ndarray, cols: int) -> np.ndarray:
     """packed uint8 [rows, row_bytes] -> float32 [rows, cols]."""
-    if fmt not in _DECODERS:
+    if fmt not in _DECODERS and fmt not in _PLANES:
         raise ValueError(f"unknown format {fmt}")
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     rb = row_bytes(fmt, cols)
     rows = packed.size // rb
+    if fmt in _PLANES:
+        _, decode, widths = _PLANES[fmt]
+        v = decode(*_planes_of_rows(packed.reshape(rows, rb), cols // 256, widths))
+        return np.ascontiguousarray(v, dtype=_F32).reshape(rows, cols)
     v = _DECODERS[fmt](packed.reshape(-1, BLOCK_BYTES[fmt]))
     return np.ascontiguousarray(v, dtype=_F32).reshape(rows, cols)
 

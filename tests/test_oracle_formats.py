@@ -285,6 +285,9 @@ def test_error_bound_per_weight():
     assert (np.abs(deq - xb) <= (step / 2 + slack)[:, None]).all()
 
 
+PLANE_WIDTHS = {oracle.Q2_K: (64, 16, 4), oracle.Q6_K: (128, 64, 16, 2)}
+
+
 def test_row_independence_and_block_order():
     """Packing row by row equals packing the matrix; blocks follow column order."""
     rng = np.random.default_rng(9)
@@ -294,6 +297,14 @@ def test_row_independence_and_block_order():
         for r in range(3):
             assert whole[r].tobytes() == oracle.quantize(fmt, x[r:r + 1])[0].tobytes()
         bw, bb = oracle.BLOCK_WEIGHTS[fmt], oracle.BLOCK_BYTES[fmt]
-        for blk in range(512 // bw):
-            single = oracle.quantize(fmt, x[0:1, blk * bw:(blk + 1) * bw])[0]
-            assert whole[0, blk * bb:(blk + 1) * bb].tobytes() == single.tobytes()
+        singles = [oracle.quantize(fmt, x[0:1, blk * bw:(blk + 1) * bw])[0] for blk in range(512 // bw)]
+        if fmt in PLANE_WIDTHS:
+            # plane by plane: every plane holds the superblocks' entries in column order
+            expected, o = [], 0
+            for w in PLANE_WIDTHS[fmt]:
+                expected += [sb[o:o + w] for sb in singles]
+                o += w
+            assert whole[0].tobytes() == np.concatenate(expected).tobytes()
+        else:
+            for blk, single in enumerate(singles):
+                assert whole[0, blk * bb:(blk + 1) * bb].tobytes() == single.tobytes()

@@ -63,8 +63,9 @@ def test_gemv_linearity_and_quantized_is_close_to_dense():
         assert (np.abs(y[0] + y[1] - y[2]) <= 2.0 ** -23 * (A[0] + A[1])).all()
         dense = W.astype(np.float64) @ x1.astype(np.float64)
         rel = np.linalg.norm(y[0] - dense) / np.linalg.norm(dense)
-        # the output error follows the weight error (page: 0.0068 .. 0.108)
-        assert rel < (0.02 if fmt == Q8_0 else 0.25)
+        # the output error follows the weight error (page: 0.0068 .. 0.108;
+        # 2-bit codes: about 0.36)
+        assert rel < {Q8_0: 0.02, oracle.Q2_K: 0.45}.get(fmt, 0.25)
 
 
 # ------------------------------------------------------------------ router / top-K
