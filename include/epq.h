@@ -63,8 +63,25 @@ typedef enum {
  * fp16 little-endian; weight j of a 32-run lives in byte j>>1 (low nibble for
  * even j); Q4_K sub-block s owns qs[16s..16s+15]; its 6-bit codes c_0..c_7,
  * k_0..k_7 form a little-endian 96-bit stream, code t at bits 6t..6t+5.  A
- * row is a contiguous run of blocks in column order; rows are contiguous. */
-typedef enum { EPQ_Q8_0 = 0, EPQ_Q4_0 = 1, EPQ_Q4_1 = 2, EPQ_Q4_K = 3 } epq_fmt;
+ * row is a contiguous run of blocks in column order; rows are contiguous.
+ *
+ * Two K-quants with 16-weight sub-blocks, sized by "EPM ... 記憶體怎麼配置的"
+ * (Q6_K: 210 B per 256 weights) and the 2-bit experts of "smolmaxxing":
+ *   EPQ_Q2_K 256 weights,  84 B: sub-block s (weights 16s..16s+15) has
+ *             step code c_s (1..15) and lift code k_s (0..15) against fp16
+ *             d and dmin; codes n 0..3:  w = d*c_s*n - dmin*k_s
+ *   EPQ_Q6_K 256 weights, 210 B: int8 scale code c_s against fp16 d; codes
+ *             m -32..31:  w = d*c_s*m   (exact in float32)
+ * Their rows are stored plane by plane (nsb = cols/256 superblocks):
+ *   Q2_K  u8 codes[64 nsb] | u8 (c | k<<4)[16 nsb] | f16 (d, dmin)[nsb]
+ *   Q6_K  u8 low nibbles[128 nsb] | u8 high parts[64 nsb] | int8 c[16 nsb]
+ *         | f16 d[nsb]
+ * with u = m + 32 for Q6_K: u & 15 of superblock weight j in byte j>>1 of
+ * the superblock's 128 (low nibble when j is even); the 2-bit fields (Q2_K
+ * codes n, Q6_K high parts u >> 4) of sub-block s fill its little-endian
+ * 32-bit word s, position i at bit FIELD[i], FIELD = {4, 8, 6, 10, 20, 24,
+ * 22, 26, 28, 0, 30, 2, 12, 16, 14, 18}. */
+typedef enum { EPQ_Q8_0 = 0, EPQ_Q4_0 = 1, EPQ_Q4_1 = 2, EPQ_Q4_K = 3, EPQ_Q2_K = 4, EPQ_Q6_K = 5 } epq_fmt;
 
 const char *epq_status_string(epq_status s);
 
@@ -271,6 +288,12 @@ typedef struct {
   const void *shared_gate_up;    /* NULL: no shared expert */
   const void *shared_down;
   const float *shared_gate_vec;  /* NULL: shared weight 1; else [H] */
+  /* Mixed per-tensor recipe ("EPM ... 記憶體怎麼配置的": Q4_K gate/up with
+   * Q6_K down): when down_fmt_set is 1 the down projections (routed and
+   * shared) are stored in down_fmt and the gate/up matrices in fmt; when 0
+   * (zero-initialised struct) both use fmt. */
+  int down_fmt_set;
+  epq_fmt down_fmt;
 } epq_experts;
 
 typedef struct {

@@ -19,8 +19,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libepq.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "epq.h")
 
-EPQ_Q8_0, EPQ_Q4_0, EPQ_Q4_1, EPQ_Q4_K = 0, 1, 2, 3
-FORMATS = {"Q8_0": EPQ_Q8_0, "Q4_0": EPQ_Q4_0, "Q4_1": EPQ_Q4_1, "Q4_K": EPQ_Q4_K}
+EPQ_Q8_0, EPQ_Q4_0, EPQ_Q4_1, EPQ_Q4_K, EPQ_Q2_K, EPQ_Q6_K = 0, 1, 2, 3, 4, 5
+FORMATS = {"Q8_0": EPQ_Q8_0, "Q4_0": EPQ_Q4_0, "Q4_1": EPQ_Q4_1, "Q4_K": EPQ_Q4_K, "Q2_K": EPQ_Q2_K,
+           "Q6_K": EPQ_Q6_K}
 
 _lib = None
 
@@ -55,7 +56,8 @@ class Experts(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int), ("n_experts", ctypes.c_int), ("hidden", ctypes.c_int),
                 ("inter", ctypes.c_int), ("gate_up", ctypes.c_void_p), ("gate_up_stride", ctypes.c_int64),
                 ("down", ctypes.c_void_p), ("down_stride", ctypes.c_int64), ("shared_gate_up", ctypes.c_void_p),
-                ("shared_down", ctypes.c_void_p), ("shared_gate_vec", ctypes.c_void_p)]
+                ("shared_down", ctypes.c_void_p), ("shared_gate_vec", ctypes.c_void_p),
+                ("down_fmt_set", ctypes.c_int), ("down_fmt", ctypes.c_int)]
 
 
 class MoeOpts(ctypes.Structure):
@@ -256,21 +258,25 @@ class MoELayer:
 
     router [E, H] float32; gate_up uint8 [E, 2*I, row_bytes(H)] (gate rows
     then up rows); down uint8 [E, H, row_bytes(I)]; optional shared expert
-    (same shapes without E) and shared gate vector [H].
+    (same shapes without E) and shared gate vector [H].  down_fmt: the
+    format of the down projections when it differs from fmt (a mixed
+    per-tensor recipe).
     """
 
     def __init__(self, fmt, router, gate_up, down, router_bias=None, shared_gate_up=None, shared_down=None,
-                 shared_gate_vec=None, norm_topk=True):
+                 shared_gate_vec=None, norm_topk=True, down_fmt=None):
         self.fmt = int(fmt)
+        self.down_fmt = self.fmt if down_fmt is None else int(down_fmt)
         self.router, self.router_bias = router, router_bias
         self.gate_up, self.down = gate_up, down
         self.shared_gate_up, self.shared_down, self.shared_gate_vec = shared_gate_up, shared_down, shared_gate_vec
         self.E, self.H = router.shape
-        self.I = down.shape[2] * epq_block_weights(self.fmt) // epq_block_bytes(self.fmt)
+        self.I = down.shape[2] * epq_block_weights(self.down_fmt) // epq_block_bytes(self.down_fmt)
         self.norm_topk = bool(norm_topk)
         self._r = Router(_addr(router), _addr(router_bias), self.E, int(self.norm_topk))
         self._x = Experts(self.fmt, self.E, self.H, self.I, _addr(gate_up), gate_up[0].numel(), _addr(down),
-                          down[0].numel(), _addr(shared_gate_up), _addr(shared_down), _addr(shared_gate_vec))
+                          down[0].numel(), _addr(shared_gate_up), _addr(shared_down), _addr(shared_gate_vec),
+                          int(self.down_fmt != self.fmt), self.down_fmt)
 
     def workspace_bytes(self, ntok: int, topk: int) -> int:
         return int(load().epq_moe_workspace_bytes(ctypes.byref(self._r), ctypes.byref(self._x), ntok, topk))

@@ -144,7 +144,9 @@ int64_t epq_block_weights(epq_fmt fmt) {
     case EPQ_Q8_0:
     case EPQ_Q4_0:
     case EPQ_Q4_1: return 32;
-    case EPQ_Q4_K: return 256;
+    case EPQ_Q4_K:
+    case EPQ_Q2_K:
+    case EPQ_Q6_K: return 256;
   }
   return -1;
 }
@@ -155,6 +157,8 @@ int64_t epq_block_bytes(epq_fmt fmt) {
     case EPQ_Q4_0: return 18;
     case EPQ_Q4_1: return 20;
     case EPQ_Q4_K: return 144;
+    case EPQ_Q2_K: return 84;
+    case EPQ_Q6_K: return 210;
   }
   return -1;
 }

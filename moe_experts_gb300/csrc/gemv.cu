@@ -688,6 +688,7 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   const int64_t rows_out = opts.swiglu ? rows / 2 : rows;
   const bool sw = opts.swiglu != 0;
   const int xs = opts.x_ld ? static_cast<int>(opts.x_ld) : static_cast<int>(cols / xg);
+  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K) return gemv_k16_launch(fmt, blocks, x, y, rows, cols, nvec, opts, xs, dev, s);
 
   // Q4_K: the tensor-core engine (two vectors per weight pass, more in the
   // multi-vector form).  With one vector it is chosen for matrices of >= 2

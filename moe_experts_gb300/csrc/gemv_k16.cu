@@ -1,0 +1,292 @@
+// Tensor-core dequant-GEMV for Q2_K and Q6_K (epq_gemv / epq_gemv_ex).
+//
+// [H] "速度上限：带宽 ÷ 权重字节数": batch-1 decode streams every packed
+// weight once per token.  The operand decode and the MMA layout are those of
+// k16_core.cuh; this file adds the CTA organisation:
+//   * a CTA of 8 warps owns RG row groups (16 output rows each; 8 gate + 8
+//     up rows with SwiGLU) and splits the superblocks of every row between
+//     KP = 8 / RG warps (warp kq takes superblocks kq, kq + KP, ...);
+//   * the CTA first converts all of x into the shared-memory operand records
+//     (one warp per (vector, superblock)), together with the per-superblock
+//     scales, the sub-block sums of x (Q2_K) and the sums of squares (RMS
+//     pre-norm);
+//   * each warp streams its rows' planes straight into registers (16-byte
+//     loads, no L1 allocation), one superblock ahead of the MMAs;
+//   * row totals: the 4 lanes of a row add their owners' parts with two
+//     butterflies, the KP warps' partials are added in k-part order through
+//     shared memory (deterministic), then the epilogue applies the RMS
+//     scale, SwiGLU and the residual.
+// Rows run past the end of the matrix read the last row and store nothing.
+#include <algorithm>
+
+#include "k16_core.cuh"
+
+namespace epq {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+struct K16Params {
+  const uint8_t *W;
+  const float *x;
+  float *y;
+  const float *residual;
+  int64_t rows_out;
+  int64_t up_rows;  // swiglu: row distance gate -> up
+  int64_t row_bytes;
+  int nsb;
+  int rg, kp;  // row groups per CTA, warps per row group
+  int nv;      // vectors in this launch (<= NV)
+  int64_t x_stride, y_stride;
+  int rms;
+  float rms_eps;
+  int x_group, x_head_dim;
+  int early;  // weights may be read before the grid-dependency wait
+};
+
+struct K16Layout {
+  uint32_t frag, ps, xsum, red, ssq, total;
+};
+
+__host__ __device__ inline uint32_t al16(uint32_t v) { return (v + 15u) & ~15u; }
+
+__host__ __device__ inline K16Layout k16_layout(int nv, int nsb, bool q2k) {
+  K16Layout L;
+  uint32_t o = 0;
+  L.frag = o;
+  o += static_cast<uint32_t>(nv * nsb) * k16::kSbFragBytes;
+  L.ps = o;
+  o = al16(o + 4u * nv * nsb);
+  L.xsum = o;
+  if (q2k) o = al16(o + 4u * nv * nsb * 16);
+  L.red = o;  // [warp][16 rows][nv]
+  o = al16(o + 4u * kWarps * 16 * nv);
+  L.ssq = o;  // [warp][nv]
+  o = al16(o + 4u * kWarps * nv);
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+
+__device__ __forceinline__ int x_src(int j, int group, int head_dim) {
+  if (group <= 1) return j;
+  const int span = head_dim * group;
+  return (j / span) * head_dim + (j % head_dim);
+}
+
+template <int FMT, int NV, int ALIGN, bool SW>
+__global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const K16Layout L = k16_layout(NV, p.nsb, FMT == EPQ_Q2_K);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int kq = warp % p.kp, rgl = warp / p.kp;
+  const int64_t rg = static_cast<int64_t>(blockIdx.x) * p.rg + rgl;
+  constexpr int kOut = SW ? 8 : 16;  // outputs per row group
+  // rows of A held by this lane: g (lo) and g + 8 (hi)
+  int64_t r_lo, r_hi;
+  if (SW) {
+    const int64_t o = min(rg * 8 + g, p.rows_out - 1);
+    r_lo = o;
+    r_hi = p.up_rows + o;
+  } else {
+    r_lo = min(rg * 16 + g, p.rows_out - 1);
+    r_hi = min(rg * 16 + g + 8, p.rows_out - 1);
+  }
+  const bool active = rgl < p.rg && rg * kOut < p.rows_out;
+  const uint8_t *row_lo = p.W + r_lo * p.row_bytes;
+  const uint8_t *row_hi = p.W + r_hi * p.row_bytes;
+  const int64_t nsb = p.nsb;
+
+  k16::RowOps<FMT> cur_lo, cur_hi, nxt_lo, nxt_hi;
+  int sb = kq;
+  const bool has_work = active && sb < p.nsb;
+  if (has_work && p.early) {
+    k16::load_ops<FMT, ALIGN>(cur_lo, row_lo, nsb, sb, t);
+    k16::load_ops<FMT, ALIGN>(cur_hi, row_hi, nsb, sb, t);
+  }
+  pdl_wait();
+  if (has_work && !p.early) {
+    k16::load_ops<FMT, ALIGN>(cur_lo, row_lo, nsb, sb, t);
+    k16::load_ops<FMT, ALIGN>(cur_hi, row_hi, nsb, sb, t);
+  }
+
+  // ---------------------------------------------------------------- x staging
+  float ssq[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) ssq[v] = 0.0f;
+  float *ps_s = reinterpret_cast<float *>(smem + L.ps);
+  float *xsum_s = reinterpret_cast<float *>(smem + L.xsum);
+  for (int u = warp; u < NV * p.nsb; u += kWarps) {
+    const int v = u / p.nsb, b = u % p.nsb;
+    float xv[8];
+    const int j0 = b * 256 + 16 * (lane >> 1) + 8 * (lane & 1);
+    if (v < p.nv) {
+      const float *xr = p.x + v * p.x_stride;
+      if (p.x_group <= 1) {
+        const float4 a = *reinterpret_cast<const float4 *>(xr + j0);
+        const float4 c = *reinterpret_cast<const float4 *>(xr + j0 + 4);
+        xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w, xv[4] = c.x, xv[5] = c.y, xv[6] = c.z, xv[7] = c.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[e] = xr[x_src(j0 + e, p.x_group, p.x_head_dim)];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
+    }
+    float sq = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sq = fmaf(xv[e], xv[e], sq);
+#pragma unroll
+    for (int w = 0; w < NV; ++w)
+      if (w == v) ssq[w] += sq;
+    uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
+    const float pv =
+        k16::stage_superblock(xv, frag_sb, lane, FMT == EPQ_Q2_K ? xsum_s + (v * p.nsb + b) * 16 : nullptr);
+    if (lane == 0) ps_s[v * p.nsb + b] = pv;
+  }
+  float *ssq_s = reinterpret_cast<float *>(smem + L.ssq);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const float s = warp_sum_xor<32>(ssq[v]);
+    if (lane == 0) ssq_s[warp * NV + v] = s;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- main loop
+  float acc[2][NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) acc[0][v] = acc[1][v] = 0.0f;
+  const uint32_t frag0 = smem_addr(smem + L.frag) + k16::lane_slot(lane);
+  const uint32_t vstride = static_cast<uint32_t>(p.nsb) * k16::kSbFragBytes;
+  if (has_work) {
+    for (;;) {
+      const int nx = sb + p.kp;
+      if (nx < p.nsb) {
+        k16::load_ops<FMT, ALIGN>(nxt_lo, row_lo, nsb, nx, t);
+        k16::load_ops<FMT, ALIGN>(nxt_hi, row_hi, nsb, nx, t);
+      }
+      float ps[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsb + sb];
+      k16::superblock<FMT, NV>(cur_lo, cur_hi, frag0 + static_cast<uint32_t>(sb) * k16::kSbFragBytes, vstride, ps,
+                               xsum_s + sb * 16, p.nsb * 16, t, acc);
+      if (nx >= p.nsb) break;
+      sb = nx;
+      cur_lo = nxt_lo;
+      cur_hi = nxt_hi;
+    }
+  }
+  pdl_launch_dependents();
+
+  // ---------------------------------------------------------------- row totals
+  float *red = reinterpret_cast<float *>(smem + L.red);
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      float s = acc[r][v];
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if (t == 0) red[(warp * 16 + g + 8 * r) * NV + v] = s;
+    }
+  __syncthreads();
+  const int nout = p.rg * kOut * NV;
+  for (int idx = threadIdx.x; idx < nout; idx += kThreads) {
+    const int v = idx % NV, o = (idx / NV) % kOut, gl = idx / (NV * kOut);
+    const int64_t i = (static_cast<int64_t>(blockIdx.x) * p.rg + gl) * kOut + o;
+    if (v >= p.nv || i >= p.rows_out) continue;
+    float rs = 1.0f;
+    if (p.rms) {
+      float q = 0.0f;
+      for (int w = 0; w < kWarps; ++w) q += ssq_s[w * NV + v];
+      rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.nsb * 256)), p.rms_eps)));
+    }
+    float a = 0.0f, b = 0.0f;
+    for (int k = 0; k < p.kp; ++k) {
+      const float *rr = red + ((gl * p.kp + k) * 16) * NV;
+      a += rr[o * NV + v];
+      if (SW) b += rr[(o + 8) * NV + v];
+    }
+    float val = a * rs;
+    if (SW) val = silu(val) * (b * rs);
+    if (p.residual) val += p.residual[v * p.y_stride + i];
+    p.y[v * p.y_stride + i] = val;
+  }
+}
+
+template <int FMT, int NV, int ALIGN, bool SW>
+cudaError_t launch_k16(const K16Params &p, unsigned grid, uint32_t smem, cudaStream_t s) {
+  auto k = gemv_k16_kernel<FMT, NV, ALIGN, SW>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3(grid), dim3(kThreads), smem, s, p);
+}
+
+template <int FMT, int NV, int ALIGN>
+cudaError_t dispatch_sw(const K16Params &p, bool sw, unsigned grid, uint32_t smem, cudaStream_t s) {
+  return sw ? launch_k16<FMT, NV, ALIGN, true>(p, grid, smem, s) : launch_k16<FMT, NV, ALIGN, false>(p, grid, smem, s);
+}
+
+template <int FMT, int NV>
+cudaError_t dispatch_k16(const K16Params &p, int align, bool sw, unsigned grid, uint32_t smem, cudaStream_t s) {
+  if (align == 16) return dispatch_sw<FMT, NV, 16>(p, sw, grid, smem, s);
+  if (align == 4) return dispatch_sw<FMT, NV, 4>(p, sw, grid, smem, s);
+  if constexpr (FMT == EPQ_Q6_K) return dispatch_sw<FMT, NV, 2>(p, sw, grid, smem, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+// Called by gemv_launch (gemv.cu) after the common argument checks.
+epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, float *y, int64_t rows, int64_t cols,
+                           int nvec, const epq_gemv_opts &o, int64_t x_stride, const DeviceInfo &dev,
+                           cudaStream_t s) {
+  const int64_t row_bytes = epq_row_bytes(fmt, cols);
+  const bool sw = o.swiglu != 0;
+  const int64_t rows_out = sw ? rows / 2 : rows;
+  const int nsb = static_cast<int>(cols / 256);
+  const int nvl = std::min(nvec, 2);
+  const K16Layout L = k16_layout(nvl, nsb, fmt == EPQ_Q2_K);
+  if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) return EPQ_ERR_SHAPE;
+  const int64_t ngroups = (rows_out + (sw ? 7 : 15)) / (sw ? 8 : 16);
+  int rg = 8;
+  while (rg > 1 && (ngroups + rg - 1) / rg < 2ll * dev.sm_count) rg >>= 1;
+  K16Params p;
+  p.W = static_cast<const uint8_t *>(blocks);
+  p.rows_out = rows_out;
+  p.up_rows = sw ? rows_out : 0;
+  p.row_bytes = row_bytes;
+  p.nsb = nsb;
+  p.rg = rg;
+  p.kp = kWarps / rg;
+  p.x_stride = x_stride;
+  p.y_stride = rows_out;
+  p.rms = o.rms_prenorm;
+  p.rms_eps = o.rms_eps;
+  p.x_group = o.x_group > 1 ? o.x_group : 1;
+  p.x_head_dim = o.x_head_dim;
+  p.early = o.weights_ready ? 1 : 0;
+  const unsigned grid = static_cast<unsigned>((ngroups + rg - 1) / rg);
+  const int align = row_bytes % 16 == 0 ? 16 : (row_bytes % 4 == 0 ? 4 : 2);
+  for (int v0 = 0; v0 < nvec; v0 += 2) {
+    p.nv = std::min(2, nvec - v0);
+    p.x = x + v0 * x_stride;
+    p.y = y + v0 * rows_out;
+    p.residual = o.residual ? o.residual + v0 * rows_out : nullptr;
+    cudaError_t e;
+    if (fmt == EPQ_Q2_K)
+      e = nvl == 1 ? dispatch_k16<EPQ_Q2_K, 1>(p, align, sw, grid, L.total, s)
+                   : dispatch_k16<EPQ_Q2_K, 2>(p, align, sw, grid, L.total, s);
+    else
+      e = nvl == 1 ? dispatch_k16<EPQ_Q6_K, 1>(p, align, sw, grid, L.total, s)
+                   : dispatch_k16<EPQ_Q6_K, 2>(p, align, sw, grid, L.total, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return EPQ_OK;
+}
+
+}  // namespace epq

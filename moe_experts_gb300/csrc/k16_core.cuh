@@ -1,0 +1,343 @@
+// Device building blocks of the tensor-core dequant-GEMV for the K-quants
+// with 16-weight sub-blocks, Q2_K and Q6_K (gemv_k16.cu and the expert
+// kernels).
+//
+// The formats (two-level K-quants, "EPM ... 記憶體怎麼配置的" fixes Q6_K at
+// 210 B per 256 weights; the 2-bit experts of "smolmaxxing"):
+//   Q2_K  w = d*c_s*n - dmin*k_s,  n 0..3, c_s 1..15, k_s 0..15
+//   Q6_K  w = d*c_s*(u - 32),       u 0..63, c_s int8
+// A row of nsb superblocks is stored plane by plane; lane t of a warp reads
+// the entries of sub-blocks 4t..4t+3 of each plane, which are contiguous:
+//   Q2_K  code words[16 nsb] (one 32-bit word per sub-block) | c | k<<4 [16 nsb]
+//         | f16 d, dmin [nsb]
+//   Q6_K  low nibbles[128 nsb] (8 bytes per sub-block) | high parts[16 nsb words]
+//         | int8 c[16 nsb] | f16 d[nsb]
+// A 2-bit field (Q2_K code, Q6_K high part) of sub-block position i sits at
+// bit kField[i] of the sub-block's word, kField = {4, 8, 6, 10, 20, 24, 22,
+// 26, 28, 0, 30, 2, 12, 16, 14, 18}: masking the word W with 0x00300030
+// isolates positions (0, 4) at fp16 mantissa bits 4-5 of its two halves,
+// 0x03000300 positions (1, 5) at bits 8-9; W >> 2 gives (2, 6) and (3, 7)
+// the same way, rotr(W, 24) gives (8, 12), (9, 13) and rotr(W, 24) >> 2 gives
+// (10, 14), (11, 15).  The low nibbles of positions (0, 4) are at bits 0-3
+// of the sub-block's first nibble word, (1, 5) at bits 4-7, and (2, 6),
+// (3, 7) the same after a shift by 8 (second word: positions 8..15).  So a
+// pair of codes becomes an fp16 pair with one or two logic ops and one
+// packed fp16 FMA, exactly:
+//   Q2_K  (W & m) read as fp16 = n * 2^-20 (mask A) or n * 2^-16 (mask B);
+//         times 2^10 or 2^6 gives n * 2^-10
+//   Q6_K  (N & nibble mask) | (W & field mask) read as fp16 = u * 2^-24
+//         (A) or u * 2^-20 (B); u * 2^14 - 2^-5 or u * 2^10 - 2^-5 gives
+//         (u - 32) * 2^-10
+//
+// MMA layout (m16n8k16, A row-major, B column-major), one warp per 16 rows:
+//   * A rows are the 16 weight rows; lane (g, t) holds rows g and g + 8;
+//   * the warp walks a superblock in 4 groups q; in group q lane t owns
+//     sub-block 4t + q of both its rows, and the group's 4 MMAs take
+//     positions (0,4)(1,5) | (2,6)(3,7) | (8,12)(9,13) | (10,14)(11,15) of it
+//     in the k-slots {2t, 2t+1} and {2t+8, 2t+9};
+//   * the 8 columns of B are (owner t' = n >> 1, part = n & 1): x at the
+//     positions of owner t''s sub-block, split into fp16 hi and lo parts,
+//     zero in the k-slots of the other owners (block-diagonal B);
+//   * so after a group's 4 MMAs, C[row][(t, part)] is the dot product of
+//     the row's sub-block 4t + q with that part of x, and lane (g, t) holds
+//     exactly the two parts of its own sub-block for rows g and g + 8: the
+//     sub-block scale c (and for Q2_K the lift k * sum(x)) is applied in
+//     float32 right there, no data leaves the lane until the row reduction.
+// x is split per (vector, superblock) with a power-of-two scale 2^sigma that
+// maps its largest |x| into [2^14, 2^15); the superblock factor d is
+// multiplied by 2^(10 - sigma) to undo both scales.
+#pragma once
+
+#include "common.cuh"
+
+namespace epq {
+namespace k16 {
+
+// x operands of one (vector, superblock): [group 4][mma 4][slot 9][8 B];
+// slots 0..7 = (owner t, part), slot 8 = zeros for the lanes whose column
+// belongs to another owner.
+constexpr int kSlotBytes = 8;
+constexpr int kMmaBytes = 9 * kSlotBytes;
+constexpr int kSbFragBytes = 16 * kMmaBytes;  // 1152
+
+// fp16 pair constants
+constexpr uint32_t kH2p14 = 0x74007400u;    // {2^14, 2^14}
+constexpr uint32_t kH2p10 = 0x64006400u;    // {2^10, 2^10}
+constexpr uint32_t kH2p6 = 0x54005400u;     // {2^6, 2^6}
+constexpr uint32_t kHm2m5 = 0xA800A800u;    // {-2^-5, -2^-5}
+constexpr uint32_t kMaskA = 0x00300030u;    // 2-bit fields at bits 4-5 of each half
+constexpr uint32_t kMaskB = 0x03000300u;    // 2-bit fields at bits 8-9
+constexpr uint32_t kNibA = 0x000F000Fu;     // nibbles at bits 0-3
+constexpr uint32_t kNibB = 0x00F000F0u;     // nibbles at bits 4-7
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t rotr(uint32_t w, int s) { return __funnelshift_r(w, w, s); }
+
+__device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint2 b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Streaming loads of packed weights (read once, not kept in L1).
+__device__ __forceinline__ uint4 ldg_stream16(const uint8_t *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream4(const uint8_t *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+// A 32-bit word at a 2-byte boundary.
+__device__ __forceinline__ uint32_t ldg_w2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p + 2) << 16); }
+
+// A word of a plane: ALIGN is the row alignment (16, 4 or 2 bytes).
+template <int ALIGN>
+__device__ __forceinline__ uint32_t ldg_word(const uint8_t *p) {
+  if constexpr (ALIGN >= 4) return ldg_stream4(p);
+  else return ldg_w2(p);
+}
+
+// Exact float of a byte / of an int8 byte (magic-number conversion).
+__device__ __forceinline__ float u8_to_float(uint32_t b) { return __uint_as_float(0x4B000000u | b) - 8388608.0f; }
+__device__ __forceinline__ float s8_to_float(uint32_t b) {
+  return __uint_as_float(0x4B000000u | ((b ^ 0x80u) & 0xFFu)) - 8388736.0f;
+}
+
+// ------------------------------------------------------------------ packed operands
+// What lane t reads of one row for one superblock.
+template <int FMT>
+struct RowOps;
+
+template <>
+struct RowOps<EPQ_Q2_K> {
+  uint32_t q[4];  // code words of sub-blocks 4t..4t+3
+  uint32_t sub;   // their c | k << 4 bytes
+  uint32_t fac;   // d | dmin << 16
+};
+
+template <>
+struct RowOps<EPQ_Q6_K> {
+  uint32_t ql[8];  // low nibbles of sub-blocks 4t..4t+3 (two words each)
+  uint32_t qh[4];  // their high-part words
+  uint32_t sc;     // their int8 scale codes
+  uint32_t d;      // f16 d
+};
+
+// ALIGN: the rows start on 16-byte boundaries (row bytes % 16 == 0: wide
+// planes read 16 bytes at a time), on 4-byte boundaries (word loads) or, for
+// Q6_K rows of an odd number of superblocks, on 2-byte boundaries.
+template <int FMT, int ALIGN>
+__device__ __forceinline__ void load_ops(RowOps<FMT> &o, const uint8_t *row, int64_t nsb, int sb, int t) {
+  if constexpr (FMT == EPQ_Q2_K) {
+    const uint8_t *qp = row + 64 * static_cast<int64_t>(sb) + 16 * t;
+    if constexpr (ALIGN == 16) {
+      const uint4 v = ldg_stream16(qp);
+      o.q[0] = v.x, o.q[1] = v.y, o.q[2] = v.z, o.q[3] = v.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o.q[i] = ldg_word<ALIGN>(qp + 4 * i);
+    }
+    o.sub = ldg_word<ALIGN>(row + 64 * nsb + 16 * static_cast<int64_t>(sb) + 4 * t);
+    o.fac = ldg_word<ALIGN>(row + 80 * nsb + 4 * static_cast<int64_t>(sb));
+  } else {
+    const uint8_t *lp = row + 128 * static_cast<int64_t>(sb) + 32 * t;
+    const uint8_t *hp = row + 128 * nsb + 64 * static_cast<int64_t>(sb) + 16 * t;
+    if constexpr (ALIGN == 16) {
+      const uint4 a = ldg_stream16(lp), b = ldg_stream16(lp + 16), h = ldg_stream16(hp);
+      o.ql[0] = a.x, o.ql[1] = a.y, o.ql[2] = a.z, o.ql[3] = a.w;
+      o.ql[4] = b.x, o.ql[5] = b.y, o.ql[6] = b.z, o.ql[7] = b.w;
+      o.qh[0] = h.x, o.qh[1] = h.y, o.qh[2] = h.z, o.qh[3] = h.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o.ql[i] = ldg_word<ALIGN>(lp + 4 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o.qh[i] = ldg_word<ALIGN>(hp + 4 * i);
+    }
+    o.sc = ldg_word<ALIGN>(row + 192 * nsb + 16 * static_cast<int64_t>(sb) + 4 * t);
+    o.d = ldg_u16(row + 208 * nsb + 2 * static_cast<int64_t>(sb));
+  }
+}
+
+// The 8 fp16 operand pairs of one sub-block of one row, in MMA order:
+// p[2i] and p[2i+1] feed MMA i (k-slots {2t, 2t+1} and {2t+8, 2t+9}).
+__device__ __forceinline__ void pairs_q2k(uint32_t w, uint32_t (&p)[8]) {
+  const uint32_t w2 = w >> 2, r = rotr(w, 24), r2 = r >> 2;
+  p[0] = hmul2(w & kMaskA, kH2p10);
+  p[1] = hmul2(w & kMaskB, kH2p6);
+  p[2] = hmul2(w2 & kMaskA, kH2p10);
+  p[3] = hmul2(w2 & kMaskB, kH2p6);
+  p[4] = hmul2(r & kMaskA, kH2p10);
+  p[5] = hmul2(r & kMaskB, kH2p6);
+  p[6] = hmul2(r2 & kMaskA, kH2p10);
+  p[7] = hmul2(r2 & kMaskB, kH2p6);
+}
+
+__device__ __forceinline__ void pairs_q6k(uint32_t n0, uint32_t n1, uint32_t w, uint32_t (&p)[8]) {
+  const uint32_t w2 = w >> 2, r = rotr(w, 24), r2 = r >> 2;
+  const uint32_t m0 = n0 >> 8, m1 = n1 >> 8;
+  p[0] = hfma2((n0 & kNibA) | (w & kMaskA), kH2p14, kHm2m5);
+  p[1] = hfma2((n0 & kNibB) | (w & kMaskB), kH2p10, kHm2m5);
+  p[2] = hfma2((m0 & kNibA) | (w2 & kMaskA), kH2p14, kHm2m5);
+  p[3] = hfma2((m0 & kNibB) | (w2 & kMaskB), kH2p10, kHm2m5);
+  p[4] = hfma2((n1 & kNibA) | (r & kMaskA), kH2p14, kHm2m5);
+  p[5] = hfma2((n1 & kNibB) | (r & kMaskB), kH2p10, kHm2m5);
+  p[6] = hfma2((m1 & kNibA) | (r2 & kMaskA), kH2p14, kHm2m5);
+  p[7] = hfma2((m1 & kNibB) | (r2 & kMaskB), kH2p10, kHm2m5);
+}
+
+// ------------------------------------------------------------------ one superblock
+// Adds one superblock's contribution to acc[row 0 = g, 1 = g + 8][vector]
+// (partial: only lane t's owner sub-blocks; the 4 lanes of a row sum later).
+//   frag   shared address of this superblock's x operands for vector 0 plus
+//          the lane's slot offset; vector v adds v * vstride
+//   ps     2^(10 - sigma) of this superblock per vector
+//   xsum   Q2_K: shared float sums of x over the superblock's 16 sub-blocks
+//          for vector 0; vector v adds v * xstride floats
+template <int FMT, int NV>
+__device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<FMT> &hi, uint32_t frag,
+                                           uint32_t vstride, const float (&ps)[NV], const float *xsum, int xstride,
+                                           int t, float (&acc)[2][NV]) {
+  float cs[2][NV], ms[2][NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) cs[0][v] = cs[1][v] = ms[0][v] = ms[1][v] = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t pl[8], ph[8];
+    if constexpr (FMT == EPQ_Q2_K) {
+      pairs_q2k(lo.q[q], pl);
+      pairs_q2k(hi.q[q], ph);
+    } else {
+      pairs_q6k(lo.ql[2 * q], lo.ql[2 * q + 1], lo.qh[q], pl);
+      pairs_q6k(hi.ql[2 * q], hi.ql[2 * q + 1], hi.qh[q], ph);
+    }
+    float c[NV][4];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) c[v][0] = c[v][1] = c[v][2] = c[v][3] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a[4] = {pl[2 * i], ph[2 * i], pl[2 * i + 1], ph[2 * i + 1]};
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+        mma(c[v], a, lds64(frag + v * vstride + static_cast<uint32_t>((q * 4 + i) * kMmaBytes)));
+    }
+    if constexpr (FMT == EPQ_Q2_K) {
+      const uint32_t bl = (lo.sub >> (8 * q)) & 0xFFu, bh = (hi.sub >> (8 * q)) & 0xFFu;
+      const float cl = u8_to_float(bl & 15u), kl = u8_to_float(bl >> 4);
+      const float ch = u8_to_float(bh & 15u), kh = u8_to_float(bh >> 4);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float X = xsum[v * xstride + 4 * t + q];
+        cs[0][v] = fmaf(cl, c[v][0] + c[v][1], cs[0][v]);
+        cs[1][v] = fmaf(ch, c[v][2] + c[v][3], cs[1][v]);
+        ms[0][v] = fmaf(kl, X, ms[0][v]);
+        ms[1][v] = fmaf(kh, X, ms[1][v]);
+      }
+    } else {
+      const float cl = s8_to_float((lo.sc >> (8 * q)) & 0xFFu), ch = s8_to_float((hi.sc >> (8 * q)) & 0xFFu);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        cs[0][v] = fmaf(cl, c[v][0] + c[v][1], cs[0][v]);
+        cs[1][v] = fmaf(ch, c[v][2] + c[v][3], cs[1][v]);
+      }
+    }
+  }
+  if constexpr (FMT == EPQ_Q2_K) {
+    const float dl = half_bits_to_float(lo.fac), ml = half_bits_to_float(lo.fac >> 16);
+    const float dh = half_bits_to_float(hi.fac), mh = half_bits_to_float(hi.fac >> 16);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      acc[0][v] = fmaf(dl * ps[v], cs[0][v], fmaf(-ml, ms[0][v], acc[0][v]));
+      acc[1][v] = fmaf(dh * ps[v], cs[1][v], fmaf(-mh, ms[1][v], acc[1][v]));
+    }
+  } else {
+    const float dl = half_bits_to_float(lo.d), dh = half_bits_to_float(hi.d);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      acc[0][v] = fmaf(dl * ps[v], cs[0][v], acc[0][v]);
+      acc[1][v] = fmaf(dh * ps[v], cs[1][v], acc[1][v]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ x staging
+// One warp converts one (vector, superblock) of x: lane l holds positions
+// 8h..8h+7 (h = l & 1) of sub-block s = l >> 1, already gathered into xv.
+// Writes the operand slots of sub-block s, the zero slots (lanes of owner 0),
+// and returns 2^(10 - sigma) (same on every lane).  sum16 receives the
+// sub-block's sum of x (lanes with h = 0 hold it).
+__device__ __forceinline__ float stage_superblock(const float (&xv)[8], uint8_t *frag_sb, int lane, float *sum16) {
+  float m = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
+  m = warp_max_all(m);
+  int sigma = 0;
+  if (m > 0.0f) {
+    const int e = static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127;  // floor(log2 m) for normal m
+    sigma = min(100, max(-100, 14 - e));
+  }
+  const int s = lane >> 1, h = lane & 1, q = s & 3, o = s >> 2;
+  uint32_t hi[4], lo[4];  // fp16 pairs (2i', 2i'+4), (2i'+1, 2i'+5) for i' = 0, 1
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int a = (k >> 1) * 2 + (k & 1);  // k = 2 i' + r: pair of positions (a, a + 4)
+    const float xa = scale_pow2(xv[a], sigma), xb = scale_pow2(xv[a + 4], sigma);
+    const __half2 hh = __floats2half2_rn(xa, xb);
+    const float2 hf = __half22float2(hh);
+    const __half2 ll = __floats2half2_rn(xa - hf.x, xb - hf.y);
+    hi[k] = *reinterpret_cast<const uint32_t *>(&hh);
+    lo[k] = *reinterpret_cast<const uint32_t *>(&ll);
+  }
+#pragma unroll
+  for (int ip = 0; ip < 2; ++ip) {
+    const int i = 2 * h + ip;
+    uint8_t *m0 = frag_sb + (q * 4 + i) * kMmaBytes;
+    *reinterpret_cast<uint2 *>(m0 + (2 * o) * kSlotBytes) = make_uint2(hi[2 * ip], hi[2 * ip + 1]);
+    *reinterpret_cast<uint2 *>(m0 + (2 * o + 1) * kSlotBytes) = make_uint2(lo[2 * ip], lo[2 * ip + 1]);
+    if (o == 0) *reinterpret_cast<uint2 *>(m0 + 8 * kSlotBytes) = make_uint2(0u, 0u);
+  }
+  if (sum16) {
+    float sx = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sx += xv[e];
+    const float other = __shfl_xor_sync(0xffffffffu, sx, 1);
+    if (h == 0) sum16[s] = sx + other;
+  }
+  return exp2i(10 - sigma);
+}
+
+// Lane's byte offset into a (group, mma) record: its own column's slot when
+// the column belongs to its owner, else the zero slot.
+__device__ __forceinline__ uint32_t lane_slot(int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  return (g >> 1) == t ? static_cast<uint32_t>((2 * t + (g & 1)) * kSlotBytes) : 8u * kSlotBytes;
+}
+
+}  // namespace k16
+}  // namespace epq

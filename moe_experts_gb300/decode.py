@@ -42,8 +42,11 @@ def kv_caches(n_layers, n_kv, head_dim, ctx, max_pos, device, seed):
         if ctx > 0:
             for dst in (c.k, c.v):
                 gen.manual_seed(seed * 1000 + li * 2 + (dst is c.v))
-                x = torch.randn((n_kv * ctx, head_dim), generator=gen, device=device, dtype=torch.float32)
-                b = L.epq_quantize(L.EPQ_Q8_0, x).view(n_kv, ctx, nblk, 34)
+                n = n_kv * ctx * head_dim
+                x = torch.zeros(-(-n // 256) * 256, device=device, dtype=torch.float32)
+                x[:n] = torch.randn(n, generator=gen, device=device, dtype=torch.float32)
+                # Q8_0 blocks are independent 32-runs: pack as rows of 256 and drop the padding
+                b = L.epq_quantize(L.EPQ_Q8_0, x.view(-1, 256)).view(-1)[:n // 32 * 34].view(n_kv, ctx, nblk, 34)
                 dst[:, :ctx, :2 * nblk] = b[..., :2].reshape(n_kv, ctx, 2 * nblk)
                 dst[:, :ctx, 2 * nblk:] = b[..., 2:].reshape(n_kv, ctx, head_dim)
         caches.append(c)

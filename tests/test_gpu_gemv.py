@@ -85,7 +85,7 @@ def test_gemv_zero_x_and_deterministic(epq_lib, cuda_dev):
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
 
 
-@pytest.mark.parametrize("fmt", [oracle.Q4_K, oracle.Q4_0])
+@pytest.mark.parametrize("fmt", [oracle.Q4_K, oracle.Q4_0, oracle.Q2_K, oracle.Q6_K])
 def test_gemv_ex_residual_and_prenorm(epq_lib, cuda_dev, fmt):
     rows, cols, nvec, eps = 200, 2048, 2, 1e-6
     W, packed, x = _case(fmt, rows, cols, nvec, seed=11)
@@ -120,9 +120,10 @@ def test_gemv_ex_swiglu(epq_lib, cuda_dev, fmt):
     assert (err <= bound + 1e-30).all(), (err / (bound + 1e-30)).max()
 
 
-def test_gemv_ex_grouped_heads(epq_lib, cuda_dev):
+@pytest.mark.parametrize("fmt", [oracle.Q4_K, oracle.Q2_K, oracle.Q6_K])
+def test_gemv_ex_grouped_heads(epq_lib, cuda_dev, fmt):
     """x_group: each 128-float head of x feeds 4 consecutive heads of the product."""
-    fmt, rows, cols, hd, grp = oracle.Q4_K, 64, 4096, 128, 4
+    rows, cols, hd, grp = 64, 4096, 128, 4
     W, packed, _ = _case(fmt, rows, cols, 1, seed=31)
     v = synthetic.normal((1, cols // grp), seed=32).numpy()
     xe = np.stack([np.concatenate([np.tile(v[0, h * hd:(h + 1) * hd], grp) for h in range(cols // grp // hd)])])
