@@ -80,10 +80,11 @@ def silu_f64(g: np.ndarray) -> np.ndarray:
 
 
 def expert_forward_f64(fmt: int, gate_up: np.ndarray, down: np.ndarray,
-                       hidden: int, inter: int, x: np.ndarray):
-    """One expert on x [n, hidden] -> (o [n, hidden], g, u, h [n, inter])."""
+                       hidden: int, inter: int, x: np.ndarray, down_fmt: int | None = None):
+    """One expert on x [n, hidden] -> (o [n, hidden], g, u, h [n, inter]).
+    down_fmt: the down matrix's format when it differs from fmt."""
     GU = dequantize(fmt, gate_up, hidden).astype(np.float64)     # [2*inter, hidden]
-    D = dequantize(fmt, down, inter).astype(np.float64)          # [hidden, inter]
+    D = dequantize(fmt if down_fmt is None else down_fmt, down, inter).astype(np.float64)   # [hidden, inter]
     x = np.atleast_2d(np.asarray(x, np.float64))
     g = x @ GU[:inter].T
     u = x @ GU[inter:].T
@@ -96,7 +97,10 @@ class MoEWeights:
     """Packed expert weights as the library stores them.
 
     gate_up: uint8 [E, 2*inter, row_bytes(hidden)]; down: uint8
-    [E, hidden, row_bytes(inter)]; router: float32 [E, hidden].
+    [E, hidden, row_bytes(inter)]; router: float32 [E, hidden].  down_fmt:
+    the down projections' format in a mixed per-tensor recipe (the Q6_K
+    ffn_down_exps next to Q4_K gate/up of "EPM ... 記憶體怎麼配置的"); None =
+    fmt.
     """
     fmt: int
     hidden: int
@@ -109,6 +113,7 @@ class MoEWeights:
     shared_down: np.ndarray | None = None
     shared_gate_vec: np.ndarray | None = None
     norm_topk: bool = True
+    down_fmt: int | None = None
 
     @property
     def n_experts(self) -> int:
@@ -141,7 +146,7 @@ def moe_forward_f64(mw: MoEWeights, x: np.ndarray, topk: int,
         for slot in range(topk):
             e = int(idx[t, slot])
             o, g, u, h = expert_forward_f64(mw.fmt, mw.gate_up[e], mw.down[e],
-                                            mw.hidden, mw.inter, xin[t])
+                                            mw.hidden, mw.inter, xin[t], mw.down_fmt)
             y[t] += w[t, slot] * o[0]
             if keep_stages:
                 stages[(t, slot)] = (g[0], u[0], h[0], o[0])
@@ -152,7 +157,7 @@ def moe_forward_f64(mw: MoEWeights, x: np.ndarray, topk: int,
             gs = np.ones(x.shape[0])
         for t in range(x.shape[0]):
             o, g, u, h = expert_forward_f64(mw.fmt, mw.shared_gate_up, mw.shared_down,
-                                            mw.hidden, mw.inter, xin[t])
+                                            mw.hidden, mw.inter, xin[t], mw.down_fmt)
             y[t] += gs[t] * o[0]
             if keep_stages:
                 stages[(t, topk)] = (g[0], u[0], h[0], o[0])
