@@ -32,6 +32,7 @@
 #include "gemv_core.cuh"
 
 #include "moe_common.cuh"
+#include "moe_k16.cuh"
 #include "moe_tc.cuh"
 
 namespace epq {
@@ -1296,7 +1297,9 @@ cudaError_t launch_down(const EngineArgs &p, int rpg, unsigned grid, uint32_t sm
 
 epq_status check_moe(const epq_router *r, const epq_experts *x, int ntok, int topk) {
   if (!r || !x) return EPQ_ERR_ARG;
-  if (epq_block_weights(x->fmt) < 0) return EPQ_ERR_FORMAT;
+  if (x->down_fmt_set != 0 && x->down_fmt_set != 1) return EPQ_ERR_ARG;
+  const epq_fmt gf = x->fmt, df = x->down_fmt_set ? x->down_fmt : x->fmt;
+  if (epq_block_weights(gf) < 0 || epq_block_weights(df) < 0) return EPQ_ERR_FORMAT;
   if (!r->weight || !x->gate_up || !x->down) return EPQ_ERR_ARG;
   if (r->n_experts < 1 || r->n_experts > kMaxExperts || x->n_experts != r->n_experts) return EPQ_ERR_ARG;
   if (ntok < 1 || ntok > kMaxTok || topk < 1 || topk > kMaxTopk || topk > r->n_experts) return EPQ_ERR_ARG;
@@ -1305,8 +1308,8 @@ epq_status check_moe(const epq_router *r, const epq_experts *x, int ntok, int to
   if ((x->shared_gate_up == nullptr) != (x->shared_down == nullptr)) return EPQ_ERR_ARG;
   if (x->gate_up_stride < 0 || x->down_stride < 0 || x->gate_up_stride % 16 || x->down_stride % 16)
     return EPQ_ERR_ALIGN;
-  const int64_t gu = 2ll * x->inter * epq_row_bytes(x->fmt, x->hidden);
-  const int64_t dn = static_cast<int64_t>(x->hidden) * epq_row_bytes(x->fmt, x->inter);
+  const int64_t gu = 2ll * x->inter * epq_row_bytes(gf, x->hidden);
+  const int64_t dn = static_cast<int64_t>(x->hidden) * epq_row_bytes(df, x->inter);
   if ((x->gate_up_stride && x->gate_up_stride < gu) || (x->down_stride && x->down_stride < dn)) return EPQ_ERR_ARG;
   if (!aligned16(r->weight) || !aligned16(x->gate_up) || !aligned16(x->down) ||
       (x->shared_gate_up && (!aligned16(x->shared_gate_up) || !aligned16(x->shared_down))) ||
@@ -1340,15 +1343,38 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const WsLayout L = ws_layout(ntok, topk, E, I);
   if (!workspace || workspace_bytes < L.total) return EPQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return EPQ_ERR_ALIGN;
+  const epq_fmt gf = experts->fmt, df = experts->down_fmt_set ? experts->down_fmt : experts->fmt;
+  const bool k16g = gf == EPQ_Q2_K || gf == EPQ_Q6_K, k16d = df == EPQ_Q2_K || df == EPQ_Q6_K;
+  const bool whole = (o.stages & 7) == 0 || (o.stages & 7) == 7;
+  // Tokens per pass of the Q2_K / Q6_K expert kernels: two when their
+  // operands fit shared memory, else one.
+  int k16_chunk = 0;
+  if (k16g || k16d) {
+    DeviceInfo dv;
+    if (!current_device(&dv) || dv.major * 10 + dv.minor < 100) return EPQ_ERR_DEVICE;
+    MoeArgs q = {};
+    q.H = H;
+    q.I = I;
+    q.topk = topk;
+    const int shared = experts->shared_gate_up != nullptr ? 1 : 0;
+    for (int c = 2; c >= 1 && !k16_chunk; --c) {
+      q.ntok = c;
+      if (moe_k16_fits(q, std::min(E, c * topk) + shared, k16g, k16d, dv)) k16_chunk = c;
+    }
+    if (!k16_chunk) return EPQ_ERR_SHAPE;
+    if (ntok > k16_chunk && !whole) return EPQ_ERR_SHAPE;  // stage calls are not split into token chunks
+  }
   // Q4_K with three or more tokens, all stages in this call: the tensor-core
   // expert kernels take two tokens per pass, so the call runs as chunks of
   // two tokens (router, gate/up, down each; an expert chosen in two chunks
   // is read once per chunk).  Measured faster than the CUDA-core engines,
-  // which read every chosen expert once for all tokens.
-  if (ntok > 2 && ((o.stages & 7) == 0 || (o.stages & 7) == 7) && experts->fmt == EPQ_Q4_K &&
-      tune_gemv_engine() != 1) {
-    for (int t0 = 0; t0 < ntok; t0 += 2) {
-      const int nt = std::min(2, ntok - t0);
+  // which read every chosen expert once for all tokens.  Calls with a
+  // Q2_K / Q6_K stage run as chunks of k16_chunk tokens.
+  const int chunk = k16_chunk ? k16_chunk : 2;
+  if (ntok > chunk && whole &&
+      (k16_chunk || (gf == EPQ_Q4_K && df == EPQ_Q4_K && tune_gemv_engine() != 1))) {
+    for (int t0 = 0; t0 < ntok; t0 += chunk) {
+      const int nt = std::min(chunk, ntok - t0);
       epq_moe_opts oc = o;
       if (o.logits_out) oc.logits_out = o.logits_out + static_cast<int64_t>(t0) * E;
       if (o.h_out) oc.h_out = o.h_out + static_cast<int64_t>(t0) * (topk + 1) * I;
@@ -1379,8 +1405,8 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   a.rms = o.rms_prenorm;
   a.eps = o.rms_eps;
   a.has_shared = experts->shared_gate_up != nullptr;
-  a.gu_row_bytes = epq_row_bytes(experts->fmt, H);
-  a.dn_row_bytes = epq_row_bytes(experts->fmt, I);
+  a.gu_row_bytes = epq_row_bytes(gf, H);
+  a.dn_row_bytes = epq_row_bytes(df, I);
   a.gate_up = static_cast<const uint8_t *>(experts->gate_up);
   a.gu_stride = experts->gate_up_stride ? experts->gate_up_stride : 2ll * I * a.gu_row_bytes;
   a.down = static_cast<const uint8_t *>(experts->down);
@@ -1441,65 +1467,90 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   }
 
   const int max_slots = std::min(E, ntok * topk) + (a.has_shared ? 1 : 0);
-  // Q4_K with one or two tokens: the tensor-core expert kernels (moe_tc.cu)
-  // for both stages, unless the CUDA-core engines are forced
+  // Engines per stage: Q2_K / Q6_K matrices run the k16 kernels (moe_k16.cu);
+  // Q4_K with one or two tokens the tensor-core kernels (moe_tc.cu) unless
+  // the CUDA-core engines are forced; everything else the CUDA-core kernels
+  // below.  A CUDA-core down kernel reads the max |h| words, which the
+  // tensor-core gate/up kernel does not keep: that pairing runs the
+  // CUDA-core gate/up.
+  enum { kCC = 0, kTC = 1, kK16 = 2 };
   MoeTcPlan tp;
-  if (experts->fmt == EPQ_Q4_K && tune_gemv_engine() != 1 && moe_tc_plan(a, max_slots, dev, &tp)) {
-    if (stages & EPQ_MOE_GATE_UP) {
+  const bool tc_ok = tune_gemv_engine() != 1 && (gf == EPQ_Q4_K || df == EPQ_Q4_K) && !(k16g && k16d) &&
+                     moe_tc_plan(a, max_slots, dev, &tp);
+  const int d_eng = k16d ? kK16 : (df == EPQ_Q4_K && tc_ok ? kTC : kCC);
+  int g_eng = k16g ? kK16 : (gf == EPQ_Q4_K && tc_ok ? kTC : kCC);
+  if (g_eng == kTC && d_eng == kCC) g_eng = kCC;
+  if ((g_eng == kK16 || d_eng == kK16) && ntok > 2) return EPQ_ERR_SHAPE;
+
+  if (stages & EPQ_MOE_GATE_UP) {
+    if (g_eng == kK16) {
+      e = moe_k16_gateup_launch(gf, a, max_slots, d_eng == kCC, dev, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    } else if (g_eng == kTC) {
       e = moe_tc_gateup_launch(tp, a, s);
       if (e != cudaSuccess) return cuda_fail(e);
-    }
-    if (stages & EPQ_MOE_DOWN) {
-      e = moe_tc_down_launch(tp, a, s);
+    } else {
+      EnginePlan gp;
+      const unsigned ggrid = static_cast<unsigned>(dev.sm_count);
+      const int64_t g_hint = (static_cast<int64_t>(max_slots) * I + ggrid - 1) / ggrid;
+      const bool gflat = flat_gateup_plan(H, a.gu_row_bytes, I, ggrid, max_slots, ntok, topk, dev, &gp);
+      if (!gflat && !engine_plan(H, 2 * a.gu_row_bytes, true, g_hint, ntok, topk, I, false, dev, &gp))
+        return EPQ_ERR_SHAPE;
+      // the gate/up kernel routes in its stage area before the first copy
+      if (static_cast<int64_t>(gp.stages) * gp.stage_bytes < 4ll * kSelScratchWords) return EPQ_ERR_SHAPE;
+      EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_h, gp.stage_bytes, gp.bar_off,
+                    gp.red_off, gp.meta_off, gp.hs_off, gp.acc_off};
+      if (gflat) switch (gf) {
+        case EPQ_Q8_0: e = launch_gateup_flat<EPQ_Q8_0>(ga, ggrid, gp.smem, s); break;
+        case EPQ_Q4_0: e = launch_gateup_flat<EPQ_Q4_0>(ga, ggrid, gp.smem, s); break;
+        case EPQ_Q4_1: e = launch_gateup_flat<EPQ_Q4_1>(ga, ggrid, gp.smem, s); break;
+        case EPQ_Q4_K: e = launch_gateup_flat<EPQ_Q4_K>(ga, ggrid, gp.smem, s); break;
+        default: return EPQ_ERR_FORMAT;
+      }
+      else switch (gf) {
+        case EPQ_Q8_0: e = launch_gateup<EPQ_Q8_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
+        case EPQ_Q4_0: e = launch_gateup<EPQ_Q4_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
+        case EPQ_Q4_1: e = launch_gateup<EPQ_Q4_1>(ga, gp.rpg, ggrid, gp.smem, s); break;
+        case EPQ_Q4_K: e = launch_gateup<EPQ_Q4_K>(ga, gp.rpg, ggrid, gp.smem, s); break;
+        default: return EPQ_ERR_FORMAT;
+      }
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    return EPQ_OK;
   }
 
-  EnginePlan gp, dp;
-  const unsigned ggrid = static_cast<unsigned>(dev.sm_count);
-  const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
-  const int64_t g_hint = (static_cast<int64_t>(max_slots) * I + ggrid - 1) / ggrid;
-  const int64_t d_hint = (H + dgrid - 1) / dgrid;
-  const bool gflat = flat_gateup_plan(H, a.gu_row_bytes, I, ggrid, max_slots, ntok, topk, dev, &gp);
-  if (!gflat && !engine_plan(H, 2 * a.gu_row_bytes, true, g_hint, ntok, topk, I, false, dev, &gp))
-    return EPQ_ERR_SHAPE;
-  // the gate/up kernel routes in its stage area before the first copy
-  if (static_cast<int64_t>(gp.stages) * gp.stage_bytes < 4ll * kSelScratchWords) return EPQ_ERR_SHAPE;
-  const bool flat = flat_down_plan(I, a.dn_row_bytes, H, dgrid, max_slots, ntok, topk, dev, &dp);
-  if (!flat && !engine_plan(I, a.dn_row_bytes, false, d_hint, ntok, topk, I, true, dev, &dp)) return EPQ_ERR_SHAPE;
-
-  EngineArgs ga{a, gp.tpr, gp.groups, gp.tile_rows, gp.stages, gp.stage_h, gp.stage_bytes, gp.bar_off,
-                gp.red_off, gp.meta_off, gp.hs_off, gp.acc_off};
-  if ((stages & EPQ_MOE_GATE_UP) && gflat) switch (experts->fmt) {
-    case EPQ_Q8_0: e = launch_gateup_flat<EPQ_Q8_0>(ga, ggrid, gp.smem, s); break;
-    case EPQ_Q4_0: e = launch_gateup_flat<EPQ_Q4_0>(ga, ggrid, gp.smem, s); break;
-    case EPQ_Q4_1: e = launch_gateup_flat<EPQ_Q4_1>(ga, ggrid, gp.smem, s); break;
-    case EPQ_Q4_K: e = launch_gateup_flat<EPQ_Q4_K>(ga, ggrid, gp.smem, s); break;
+  if (stages & EPQ_MOE_DOWN) {
+    if (d_eng == kK16) {
+      e = moe_k16_down_launch(df, a, max_slots, dev, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    } else if (d_eng == kTC) {
+      e = moe_tc_down_launch(tp, a, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    } else {
+      EnginePlan dp;
+      const unsigned dgrid = static_cast<unsigned>(std::max(1, std::min(dev.sm_count, (H + 7) / 8)));
+      const int64_t d_hint = (H + dgrid - 1) / dgrid;
+      const bool flat = flat_down_plan(I, a.dn_row_bytes, H, dgrid, max_slots, ntok, topk, dev, &dp);
+      if (!flat && !engine_plan(I, a.dn_row_bytes, false, d_hint, ntok, topk, I, true, dev, &dp))
+        return EPQ_ERR_SHAPE;
+      EngineArgs da{a, dp.tpr, dp.groups, dp.tile_rows, dp.stages, dp.stage_h, dp.stage_bytes, dp.bar_off,
+                    dp.red_off, dp.meta_off, dp.hs_off, dp.acc_off};
+      if (flat) switch (df) {
+        case EPQ_Q8_0: e = launch_down_flat<EPQ_Q8_0>(da, dgrid, dp.smem, s); break;
+        case EPQ_Q4_0: e = launch_down_flat<EPQ_Q4_0>(da, dgrid, dp.smem, s); break;
+        case EPQ_Q4_1: e = launch_down_flat<EPQ_Q4_1>(da, dgrid, dp.smem, s); break;
+        case EPQ_Q4_K: e = launch_down_flat<EPQ_Q4_K>(da, dgrid, dp.smem, s); break;
+        default: return EPQ_ERR_FORMAT;
+      }
+      else switch (df) {
+        case EPQ_Q8_0: e = launch_down<EPQ_Q8_0>(da, dp.rpg, dgrid, dp.smem, s); break;
+        case EPQ_Q4_0: e = launch_down<EPQ_Q4_0>(da, dp.rpg, dgrid, dp.smem, s); break;
+        case EPQ_Q4_1: e = launch_down<EPQ_Q4_1>(da, dp.rpg, dgrid, dp.smem, s); break;
+        case EPQ_Q4_K: e = launch_down<EPQ_Q4_K>(da, dp.rpg, dgrid, dp.smem, s); break;
+        default: return EPQ_ERR_FORMAT;
+      }
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
   }
-  else if (stages & EPQ_MOE_GATE_UP) switch (experts->fmt) {
-    case EPQ_Q8_0: e = launch_gateup<EPQ_Q8_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
-    case EPQ_Q4_0: e = launch_gateup<EPQ_Q4_0>(ga, gp.rpg, ggrid, gp.smem, s); break;
-    case EPQ_Q4_1: e = launch_gateup<EPQ_Q4_1>(ga, gp.rpg, ggrid, gp.smem, s); break;
-    case EPQ_Q4_K: e = launch_gateup<EPQ_Q4_K>(ga, gp.rpg, ggrid, gp.smem, s); break;
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
-
-  EngineArgs da{a, dp.tpr, dp.groups, dp.tile_rows, dp.stages, dp.stage_h, dp.stage_bytes, dp.bar_off,
-                dp.red_off, dp.meta_off, dp.hs_off, dp.acc_off};
-  if ((stages & EPQ_MOE_DOWN) && flat) switch (experts->fmt) {
-    case EPQ_Q8_0: e = launch_down_flat<EPQ_Q8_0>(da, dgrid, dp.smem, s); break;
-    case EPQ_Q4_0: e = launch_down_flat<EPQ_Q4_0>(da, dgrid, dp.smem, s); break;
-    case EPQ_Q4_1: e = launch_down_flat<EPQ_Q4_1>(da, dgrid, dp.smem, s); break;
-    case EPQ_Q4_K: e = launch_down_flat<EPQ_Q4_K>(da, dgrid, dp.smem, s); break;
-  }
-  else if (stages & EPQ_MOE_DOWN) switch (experts->fmt) {
-    case EPQ_Q8_0: e = launch_down<EPQ_Q8_0>(da, dp.rpg, dgrid, dp.smem, s); break;
-    case EPQ_Q4_0: e = launch_down<EPQ_Q4_0>(da, dp.rpg, dgrid, dp.smem, s); break;
-    case EPQ_Q4_1: e = launch_down<EPQ_Q4_1>(da, dp.rpg, dgrid, dp.smem, s); break;
-    case EPQ_Q4_K: e = launch_down<EPQ_Q4_K>(da, dp.rpg, dgrid, dp.smem, s); break;
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
   return EPQ_OK;
 }
 

@@ -27,16 +27,17 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-4
 
 
-def _make(fmt, E, H, I, seed, shared=True, gate_vec=False, bias=False, norm=True):
+def _make(fmt, E, H, I, seed, shared=True, gate_vec=False, bias=False, norm=True, down_fmt=None):
+    dfmt = fmt if down_fmt is None else down_fmt
     R = synthetic.student_t((E, H), seed=seed).numpy()
     gu = np.stack([oracle.quantize(fmt, synthetic.student_t((2 * I, H), seed=seed + 1 + e).numpy()) for e in range(E)])
-    dn = np.stack([oracle.quantize(fmt, synthetic.student_t((H, I), seed=seed + 1000 + e).numpy()) for e in range(E)])
-    mw = MoEWeights(fmt=fmt, hidden=H, inter=I, router=R, gate_up=gu, down=dn, norm_topk=norm)
+    dn = np.stack([oracle.quantize(dfmt, synthetic.student_t((H, I), seed=seed + 1000 + e).numpy()) for e in range(E)])
+    mw = MoEWeights(fmt=fmt, hidden=H, inter=I, router=R, gate_up=gu, down=dn, norm_topk=norm, down_fmt=down_fmt)
     if bias:
         mw.router_bias = synthetic.normal((E,), seed=seed + 5).numpy()
     if shared:
         mw.shared_gate_up = oracle.quantize(fmt, synthetic.student_t((2 * I, H), seed=seed + 7).numpy())
-        mw.shared_down = oracle.quantize(fmt, synthetic.student_t((H, I), seed=seed + 8).numpy())
+        mw.shared_down = oracle.quantize(dfmt, synthetic.student_t((H, I), seed=seed + 8).numpy())
         if gate_vec:
             mw.shared_gate_vec = synthetic.normal((H,), seed=seed + 9, scale=0.05).numpy()
     return mw
@@ -46,7 +47,7 @@ def _to_gpu(epq, mw, dev):
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     return epq.MoELayer(mw.fmt, t(mw.router), t(mw.gate_up), t(mw.down), router_bias=t(mw.router_bias),
                         shared_gate_up=t(mw.shared_gate_up), shared_down=t(mw.shared_down),
-                        shared_gate_vec=t(mw.shared_gate_vec), norm_topk=mw.norm_topk)
+                        shared_gate_vec=t(mw.shared_gate_vec), norm_topk=mw.norm_topk, down_fmt=mw.down_fmt)
 
 
 def _run(epq, layer, x, topk, dev, rms_eps=None):
@@ -101,6 +102,7 @@ def _check_topk(ref, idx_gpu, topk, router):
 def _stagewise(mw, x, topk, idx, wts, h_gpu, y_gpu, xin, rms=False):
     """h vs oracle on the GPU's selection; y vs down+combine fed with h_gpu."""
     fmt, H, I = mw.fmt, mw.hidden, mw.inter
+    dfmt = fmt if mw.down_fmt is None else mw.down_fmt
     ntok = x.shape[0]
     y_ref = x.astype(np.float64).copy()
     y_bound = 1e-6 * np.abs(x.astype(np.float64))
@@ -119,8 +121,8 @@ def _stagewise(mw, x, topk, idx, wts, h_gpu, y_gpu, xin, rms=False):
             hb = TOL * (1.1 * Ag * np.abs(u) + np.abs(silu) * Au) + 1e-6 * np.abs(h_ref) + 1e-30
             err = np.abs(h_gpu[t, k] - h_ref)
             assert (err <= hb).all(), f"h token {t} slot {k}: worst {(err / hb).max():.3g}"
-            o = oracle.gemv_f64(fmt, D, h_gpu[t, k], I)[0]
-            Ao = oracle.gemv_bound(fmt, D, h_gpu[t, k], I)[0]
+            o = oracle.gemv_f64(dfmt, D, h_gpu[t, k], I)[0]
+            Ao = oracle.gemv_bound(dfmt, D, h_gpu[t, k], I)[0]
             if e >= 0:
                 wk = float(wts[t, k])
             elif mw.shared_gate_vec is not None:
@@ -135,6 +137,7 @@ def _stagewise(mw, x, topk, idx, wts, h_gpu, y_gpu, xin, rms=False):
 
 def _end_to_end(mw, x, ref, y_gpu):
     fmt, H, I = mw.fmt, mw.hidden, mw.inter
+    dfmt = fmt if mw.down_fmt is None else mw.down_fmt
     bound = np.abs(x.astype(np.float64)).copy()
     for t in range(x.shape[0]):
         slots = [(ref.w[t, k], mw.gate_up[e], mw.down[e]) for k, e in enumerate(ref.idx[t])]
@@ -142,8 +145,8 @@ def _end_to_end(mw, x, ref, y_gpu):
             gs = ref.shared_gate[t] if ref.shared_gate is not None else 1.0
             slots.append((gs, mw.shared_gate_up, mw.shared_down))
         for wk, GU, D in slots:
-            _, g, u, h = oracle.expert_forward_f64(fmt, GU, D, H, I, ref.xin[t])
-            bound[t] += abs(wk) * oracle.gemv_bound(fmt, D, h[0], I)[0]
+            _, g, u, h = oracle.expert_forward_f64(fmt, GU, D, H, I, ref.xin[t], mw.down_fmt)
+            bound[t] += abs(wk) * oracle.gemv_bound(dfmt, D, h[0], I)[0]
     err = np.abs(y_gpu - ref.y)
     assert (err <= 1e-3 * bound).all(), f"end to end: worst {(err / (1e-3 * bound)).max():.3g}"
 
@@ -187,9 +190,47 @@ def test_moe_q4k_engines(epq_lib, cuda_dev, case, engine):
         epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
 
 
-def _parity_case(epq_lib, cuda_dev, case):
+# Q2_K / Q6_K experts (the 2-bit experts of "smolmaxxing") and mixed
+# per-tensor recipes (the Q4_K gate/up + Q6_K down experts of "EPM ...
+# 記憶體怎麼配置的"), each stage on its own engine: the k16 tensor-core
+# kernels for Q2_K / Q6_K matrices, the Q4_K tensor-core or CUDA-core
+# kernels for the other stage.
+K16_CASES = [
+    # fmt, down fmt, E, H, I, topk, ntok, shared, gate_vec, bias, norm, rms
+    (oracle.Q2_K, None, 16, 1024, 512, 4, 1, True, True, True, True, 1e-6),
+    (oracle.Q2_K, None, 16, 1024, 512, 4, 2, True, False, True, True, None),
+    (oracle.Q6_K, None, 12, 1280, 768, 3, 2, True, False, False, False, 1e-5),  # odd superblock counts
+    (oracle.Q6_K, None, 8, 512, 256, 2, 5, True, False, False, True, None),     # 5 tokens in chunks
+    (oracle.Q4_K, oracle.Q6_K, 16, 1024, 512, 4, 1, True, False, True, True, None),
+    (oracle.Q4_K, oracle.Q6_K, 16, 2048, 512, 8, 3, True, True, False, True, 1e-6),
+    (oracle.Q2_K, oracle.Q4_K, 8, 512, 512, 2, 2, True, False, False, True, None),
+    (oracle.Q8_0, oracle.Q2_K, 6, 256, 512, 3, 2, False, False, True, False, None),
+    (oracle.Q6_K, oracle.Q8_0, 6, 512, 256, 2, 2, True, False, False, True, 1e-6),
+    (oracle.Q2_K, None, 6, 256, 256, 6, 2, False, False, False, True, None),    # every expert chosen
+]
+
+
+@pytest.mark.parametrize("case", K16_CASES)
+def test_moe_k16_formats_and_mixed(epq_lib, cuda_dev, case):
+    fmt, dfmt = case[0], case[1]
+    _parity_case(epq_lib, cuda_dev, (fmt,) + case[2:], down_fmt=dfmt)
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+def test_moe_mixed_recipe_engines(epq_lib, cuda_dev, engine):
+    """Q4_K gate/up with Q6_K down with the Q4_K stage on either engine."""
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, engine)
+    try:
+        _parity_case(epq_lib, cuda_dev, (oracle.Q4_K, 16, 1024, 512, 4, 2, True, False, True, True, None),
+                     down_fmt=oracle.Q6_K)
+    finally:
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
+
+
+def _parity_case(epq_lib, cuda_dev, case, down_fmt=None):
     fmt, E, H, I, topk, ntok, shared, gvec, bias, norm, rms = case
-    mw = _make(fmt, E, H, I, seed=E * 100 + H + I + fmt, shared=shared, gate_vec=gvec, bias=bias, norm=norm)
+    mw = _make(fmt, E, H, I, seed=E * 100 + H + I + fmt, shared=shared, gate_vec=gvec, bias=bias, norm=norm,
+               down_fmt=down_fmt)
     draw = lambda a: synthetic.normal((ntok, H), seed=H + ntok + 7919 * a, scale=2.0).numpy()
     x, ref, _ = _unambiguous_inputs(mw, draw, topk, rms)
     layer = _to_gpu(epq_lib, mw, cuda_dev)
@@ -298,6 +339,49 @@ def test_moe_full_size_layer(epq_lib, cuda_dev, ntok):
     y, idx, w, h, logits = _run(epq_lib, layer, x, K, cuda_dev)
     Al = np.abs(ref.xin) @ np.abs(mw.router.astype(np.float64)).T
     assert (np.abs(logits - ref.logits) <= TOL * Al + 1e-6).all()
+    _check_topk(ref, idx, K, mw.router)
+    for e in sorted(set(idx.flatten().tolist())):
+        assert np.array_equal(mw.gate_up[e], gu[e].cpu().numpy()), e
+        assert np.array_equal(mw.down[e], dn[e].cpu().numpy()), e
+    assert np.allclose(w, ref.w, rtol=1e-4, atol=1e-6)
+    _stagewise(mw, x, K, idx, w, h, y, ref.xin)
+    _end_to_end(mw, x, ref, y)
+    assert epq_lib.epq_device_error() == 0
+    del gu, dn
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt,dfmt", [(oracle.Q2_K, None), (oracle.Q4_K, oracle.Q6_K)])
+def test_moe_full_size_decode_layer_k16(epq_lib, cuda_dev, fmt, dfmt):
+    """One layer of the MoE decode model at full size with 2-bit experts and
+    with the Q4_K + Q6_K-down recipe: hidden 2048, 256 experts of gate/up
+    2x512x2048 + down 2048x512, a shared expert, top-8, one token.  Top-K
+    against the oracle's, every selected expert stage-wise, and the GPU's
+    packing of each selected expert bit-exact with the oracle's."""
+    from synthetic import workloads as wl
+    c = wl.MoEDecode()
+    H, I, E, K = c.hidden, c.inter, c.n_experts, c.topk
+    d = fmt if dfmt is None else dfmt
+    gen_gu = lambda e: wl.weight("moe_decode", 0, 10, 2 * I, H, cuda_dev, expert=e)
+    gen_dn = lambda e: wl.weight("moe_decode", 0, 11, H, I, cuda_dev, expert=e)
+    gu = torch.empty((E, 2 * I, epq_lib.epq_row_bytes(fmt, H)), dtype=torch.uint8, device=cuda_dev)
+    dn = torch.empty((E, H, epq_lib.epq_row_bytes(d, I)), dtype=torch.uint8, device=cuda_dev)
+    for e in range(E):
+        epq_lib.epq_quantize(fmt, gen_gu(e), blocks=gu[e])
+        epq_lib.epq_quantize(d, gen_dn(e), blocks=dn[e])
+    R, _ = wl.moe_router("moe_decode", 0, E, H, cuda_dev, None)
+    sgu_f = wl.weight("moe_decode", 0, 12, 2 * I, H, cuda_dev)
+    sdn_f = wl.weight("moe_decode", 0, 13, H, I, cuda_dev)
+    layer = epq_lib.MoELayer(fmt, R, gu, dn, shared_gate_up=epq_lib.epq_quantize(fmt, sgu_f),
+                             shared_down=epq_lib.epq_quantize(d, sdn_f), down_fmt=dfmt)
+    mw = MoEWeights(fmt=fmt, hidden=H, inter=I, router=R.cpu().numpy(),
+                    gate_up=_OraclePackedExperts(fmt, gen_gu), down=_OraclePackedExperts(d, gen_dn),
+                    shared_gate_up=oracle.quantize(fmt, sgu_f.cpu().numpy()),
+                    shared_down=oracle.quantize(d, sdn_f.cpu().numpy()), down_fmt=dfmt)
+    assert np.array_equal(mw.shared_down, layer.shared_down.cpu().numpy())
+    draw = lambda a: wl.activations("moe_decode", 1, H, cuda_dev, stream_id=a).cpu().numpy()
+    x, ref, _ = _unambiguous_inputs(mw, draw, K, 1e-6)
+    y, idx, w, h, logits = _run(epq_lib, layer, x, K, cuda_dev, rms_eps=1e-6)
     _check_topk(ref, idx, K, mw.router)
     for e in sorted(set(idx.flatten().tolist())):
         assert np.array_equal(mw.gate_up[e], gu[e].cpu().numpy()), e
