@@ -164,8 +164,11 @@ def quantize_into(epq, fmt, W, out=None):
     return epq.epq_quantize(fmt, W, blocks=out)
 
 
+FMT_TAG = {0: "q8_0", 1: "q4_0", 2: "q4_1", 3: "q4k", 4: "q2k", 5: "q6k"}
+
+
 class Gemv4096Workload(Workload):
-    """The single Q4_K dequant-GEMV (W 4096x4096 Student-t(5)*0.02, x ~ N(0,1),
+    """The single dequant-GEMV (Q4_K unless another format is named) (W 4096x4096 Student-t(5)*0.02, x ~ N(0,1),
     batch 1), one launch per copy over ceil(4 L2 / row bytes) copies of the
     packed matrix, so every launch streams its 9.4 MB from HBM.  Launches are
     chained with programmatic dependent launch as in a decode step (the
@@ -193,7 +196,7 @@ class Gemv4096Workload(Workload):
         self.full_step_bytes = self.copies * self.matrix_bytes
 
     def config(self):
-        return {"workload": "gemv4096_q4k", "rows": 4096, "cols": 4096, "nvec": self.nvec, "batch": 1,
+        return {"workload": f"gemv4096_{FMT_TAG[self.fmt]}", "rows": 4096, "cols": 4096, "nvec": self.nvec, "batch": 1,
                 "packed_bytes": self.matrix_bytes, "copies_per_step": self.copies,
                 "l2": f"{self.copies} rotating copies ({self.copies * self.matrix_bytes / 1e6:.0f} MB > 4x L2)"}
 
@@ -214,13 +217,17 @@ class MoEDecodeWorkload(Workload):
     name = "moe_decode"
     unit = "tok/s"
 
-    def __init__(self, epq, dev, fmt, layers=None, attn_ctx=None):
+    def __init__(self, epq, dev, fmt, layers=None, attn_ctx=None, expert_fmt=None, down_fmt=None):
         from synthetic import workloads as wl
         self.cfg = c = wl.MoEDecode() if layers is None else wl.MoEDecode(layers=layers)
         self.attn_ctx = attn_ctx
         self.fmt, self.dev, self.epq = fmt, dev, epq
+        # expert formats: gate/up (and down unless down_fmt is given); attention projections stay in fmt
+        self.efmt = fmt if expert_fmt is None else expert_fmt
+        self.dfmt = self.efmt if down_fmt is None else down_fmt
         H, I, E = c.hidden, c.inter, c.n_experts
         rbH, rbI = epq.epq_row_bytes(fmt, H), epq.epq_row_bytes(fmt, I)
+        erbH, drbI = epq.epq_row_bytes(self.efmt, H), epq.epq_row_bytes(self.dfmt, I)
         import torch
         self.layers = []
         for l in range(c.layers):
@@ -229,18 +236,19 @@ class MoEDecodeWorkload(Workload):
                 epq.epq_quantize(fmt, wl.weight("moe_decode", l, t, H, H, dev), blocks=wqkv[t * H:(t + 1) * H])
             wo = epq.epq_quantize(fmt, wl.weight("moe_decode", l, 3, H, H, dev))
             R, bias = wl.moe_router("moe_decode", l, E, H, dev, c.zipf_s)
-            gu = torch.empty((E, 2 * I, rbH), dtype=torch.uint8, device=dev)
-            dn = torch.empty((E, H, rbI), dtype=torch.uint8, device=dev)
+            gu = torch.empty((E, 2 * I, erbH), dtype=torch.uint8, device=dev)
+            dn = torch.empty((E, H, drbI), dtype=torch.uint8, device=dev)
             for e0 in range(0, E, 64):
                 n = min(64, E - e0)
                 Wg = wl.weight("moe_decode", l, 10, n * 2 * I, H, dev, expert=e0)
-                epq.epq_quantize(fmt, Wg, blocks=gu[e0:e0 + n].view(n * 2 * I, rbH))
+                epq.epq_quantize(self.efmt, Wg, blocks=gu[e0:e0 + n].view(n * 2 * I, erbH))
                 Wd = wl.weight("moe_decode", l, 11, n * H, I, dev, expert=e0)
-                epq.epq_quantize(fmt, Wd, blocks=dn[e0:e0 + n].view(n * H, rbI))
+                epq.epq_quantize(self.dfmt, Wd, blocks=dn[e0:e0 + n].view(n * H, drbI))
                 del Wg, Wd
-            sgu = epq.epq_quantize(fmt, wl.weight("moe_decode", l, 12, 2 * I, H, dev))
-            sdn = epq.epq_quantize(fmt, wl.weight("moe_decode", l, 13, H, I, dev))
-            layer = epq.MoELayer(fmt, R, gu, dn, router_bias=bias, shared_gate_up=sgu, shared_down=sdn)
+            sgu = epq.epq_quantize(self.efmt, wl.weight("moe_decode", l, 12, 2 * I, H, dev))
+            sdn = epq.epq_quantize(self.dfmt, wl.weight("moe_decode", l, 13, H, I, dev))
+            layer = epq.MoELayer(self.efmt, R, gu, dn, router_bias=bias, shared_gate_up=sgu, shared_down=sdn,
+                                 down_fmt=self.dfmt)
             self.layers.append((wqkv, wo, layer))
         torch.cuda.synchronize()
         from moe_experts_gb300.decode import MoEDecoder
@@ -249,7 +257,7 @@ class MoEDecodeWorkload(Workload):
         self.x = wl.activations("moe_decode", self.T, H, dev)
         self.out = torch.empty((self.T, H), dtype=torch.float32, device=dev)
         self.units_per_step = float(self.T)
-        self.bytes_per_token = c.layers * (4 * H * rbH + E * H * 4 + (c.topk + 1) * (2 * I * rbH + H * rbI))
+        self.bytes_per_token = c.layers * (4 * H * rbH + E * H * 4 + (c.topk + 1) * (2 * I * erbH + H * drbI))
         self.kernels_per_step = self.T * c.layers * (5 if attn_ctx is None else 6)
         self.launches = {k: self.T * c.layers for k in ("gemv_qkv", "gemv_o", "moe_router", "moe_gateup",
                                                           "moe_down")}
@@ -260,8 +268,8 @@ class MoEDecodeWorkload(Workload):
             "gemv_qkv": 3 * H * rbH + 4 * (H + 3 * H),
             "gemv_o": H * rbH + 4 * (H + 2 * H),
             "moe_router": E * H * 4 + 4 * H,
-            "moe_gateup": (c.topk + 1) * 2 * I * rbH + 4 * (H + (c.topk + 1) * I),
-            "moe_down": (c.topk + 1) * H * rbI + 4 * ((c.topk + 1) * I + 2 * H),
+            "moe_gateup": (c.topk + 1) * 2 * I * erbH + 4 * (H + (c.topk + 1) * I),
+            "moe_down": (c.topk + 1) * H * drbI + 4 * ((c.topk + 1) * I + 2 * H),
         }
         if attn_ctx is not None:  # an upper bound: value rows of skipped positions are not read
             self.kernel_bytes["attention"] = 2 * c.heads * (attn_ctx + c.tokens // 2) * epq.epq_kv_row_bytes(
@@ -269,13 +277,17 @@ class MoEDecodeWorkload(Workload):
 
     def config(self):
         c = self.cfg
-        return {"workload": "moe_decode_q4k" + ("" if self.attn_ctx is None else f"_attn{self.attn_ctx}"),
+        tag = FMT_TAG[self.efmt] + ("" if self.dfmt == self.efmt else f"_{FMT_TAG[self.dfmt]}down")
+        return {"workload": f"moe_decode_{tag}" + ("" if self.attn_ctx is None else f"_attn{self.attn_ctx}"),
+                "expert_formats": {"gate_up": FMT_TAG[self.efmt], "down": FMT_TAG[self.dfmt],
+                                   "attention_projections": FMT_TAG[self.fmt]},
                 "attention": "one-token-context stand-in" if self.attn_ctx is None else
                 f"Q8_0 KV cache, {self.attn_ctx} cached positions + the 64-token run, ln(1e-4) skip threshold",
                 "layers": c.layers, "hidden": c.hidden, "experts": c.n_experts,
                 "inter": c.inter, "topk": c.topk, "shared_experts": 1, "tokens_per_step": c.tokens, "batch": 1,
                 "router": "fp32 zipf(1.1)", "weights_resident_gb": round(self.resident_gb(), 2),
-                "bytes_per_token": self.bytes_per_token, "l2": "inputs larger than L2 (1.1 GB/token)"}
+                "bytes_per_token": self.bytes_per_token,
+                "l2": f"inputs larger than L2 ({self.bytes_per_token / 1e9:.2f} GB/token)"}
 
     def resident_gb(self):
         tot = 0
@@ -373,10 +385,10 @@ class MoEDecodeWorkload(Workload):
             y = h.copy()
             gu_all, dn_all = layer.gate_up, layer.down
             for k, e in enumerate(idx[0]):
-                o = oracle.expert_forward_f64(self.fmt, gu_all[int(e)].cpu().numpy(), dn_all[int(e)].cpu().numpy(),
-                                              H, I, xin[0])[0]
+                o = oracle.expert_forward_f64(self.efmt, gu_all[int(e)].cpu().numpy(), dn_all[int(e)].cpu().numpy(),
+                                              H, I, xin[0], self.dfmt)[0]
                 y += w[0, k] * o
-            o = oracle.expert_forward_f64(self.fmt, mw.shared_gate_up, mw.shared_down, H, I, xin[0])[0]
+            o = oracle.expert_forward_f64(self.efmt, mw.shared_gate_up, mw.shared_down, H, I, xin[0], self.dfmt)[0]
             h = y + o
             done += 1
             if time.perf_counter() - t0 > budget_s:
@@ -772,12 +784,14 @@ def roofline(W, ktimes, step_ms, peak, peak_kind):
             "sum_of_kernels_over_step": round(total / step_ms, 3)}
 
 
-def make_workload(epq, dev, fmt, args, name=None, ntok=None, attn_ctx=-1):
+def make_workload(epq, dev, fmt, args, name=None, ntok=None, attn_ctx=-1, expert_fmt=None, down_fmt=None):
     name = name or args.workload
     if attn_ctx == -1:
         attn_ctx = args.attn_ctx
     if name == "moe_decode":
-        return MoEDecodeWorkload(epq, dev, fmt, layers=args.layers, attn_ctx=attn_ctx)
+        ef = expert_fmt if expert_fmt is not None else (epq.FORMATS[args.expert_fmt] if args.expert_fmt else None)
+        df = down_fmt if down_fmt is not None else (epq.FORMATS[args.down_fmt] if args.down_fmt else None)
+        return MoEDecodeWorkload(epq, dev, fmt, layers=args.layers, attn_ctx=attn_ctx, expert_fmt=ef, down_fmt=df)
     if name == "moe_layer":
         return MoELayerWorkload(epq, dev, fmt, ntok=ntok or args.ntok)
     if name == "gemv4096":
@@ -957,12 +971,20 @@ def run_epq(args):
         del g, replay, W
         torch.cuda.empty_cache()
         subs = {}
-        for key, name, ntok, ctx in (("gemv4096", "gemv4096", None, None), ("moe_layer_1tok", "moe_layer", 1, None),
-                                     ("moe_layer_8tok", "moe_layer", 8, None), ("moe_decode", "moe_decode", None, None),
-                                     ("dense8b_attn1024", "dense8b", None, 1024),
-                                     ("moe_decode_attn1024", "moe_decode", None, 1024)):
-            Wk = make_workload(epq, dev, fmt, argparse.Namespace(**{**vars(args), "layers": None, "nvec": 1}),
-                               name=name, ntok=ntok, attn_ctx=ctx)
+        Q2K, Q6K = epq.EPQ_Q2_K, epq.EPQ_Q6_K
+        for key, name, ntok, ctx, wfmt, ef, df in (
+                ("gemv4096", "gemv4096", None, None, fmt, None, None),
+                ("gemv4096_q2k", "gemv4096", None, None, Q2K, None, None),
+                ("gemv4096_q6k", "gemv4096", None, None, Q6K, None, None),
+                ("moe_layer_1tok", "moe_layer", 1, None, fmt, None, None),
+                ("moe_layer_8tok", "moe_layer", 8, None, fmt, None, None),
+                ("moe_decode", "moe_decode", None, None, fmt, None, None),
+                ("moe_decode_q2k_experts", "moe_decode", None, None, fmt, Q2K, None),
+                ("moe_decode_q6k_down", "moe_decode", None, None, fmt, None, Q6K),
+                ("dense8b_attn1024", "dense8b", None, 1024, fmt, None, None),
+                ("moe_decode_attn1024", "moe_decode", None, 1024, fmt, None, None)):
+            Wk = make_workload(epq, dev, wfmt, argparse.Namespace(**{**vars(args), "layers": None, "nvec": 1}),
+                               name=name, ntok=ntok, attn_ctx=ctx, expert_fmt=ef, down_fmt=df)
             subs[key] = sub_object(torch, epq, Wk, stream, args, peak, peak_kind)
             del Wk
             torch.cuda.empty_cache()
@@ -986,7 +1008,7 @@ def run_reference(args):
     import torch
     from oracle import cref
     from synthetic import workloads as wl
-    fmt = {"Q8_0": 0, "Q4_0": 1, "Q4_1": 2, "Q4_K": 3}[args.fmt]
+    fmt = {"Q8_0": 0, "Q4_0": 1, "Q4_1": 2, "Q4_K": 3, "Q2_K": 4, "Q6_K": 5}[args.fmt]
     nthreads = cref.hardware_threads()
     t_all = time.perf_counter()
     if args.workload in ("dense8b", "gemv4096"):
@@ -1013,7 +1035,7 @@ def run_reference(args):
             mats = [(packed, 4096)]
             step_bytes = packed.size
             unit, units = "GB/s", packed.size / 1e9
-            cfg = {"workload": "gemv4096_q4k", "rows": 4096, "cols": 4096, "nvec": args.nvec, "batch": 1}
+            cfg = {"workload": f"gemv4096_{FMT_TAG[fmt]}", "rows": 4096, "cols": 4096, "nvec": args.nvec, "batch": 1}
             desc = "the 4096x4096 matrix, one GEMV per step"
         sample_bytes = sum(p.size for p, _ in mats)
         xs = [np.random.default_rng(3).standard_normal((args.nvec, cols)).astype(np.float32) for _, cols in mats]
@@ -1038,7 +1060,9 @@ def run_reference(args):
         dev = torch.device(f"cuda:{local}")
         efmt = epq.FORMATS[args.fmt]
         if args.workload == "moe_decode":
-            W = MoEDecodeWorkload(epq, dev, efmt, layers=1)
+            W = MoEDecodeWorkload(epq, dev, efmt, layers=1,
+                                  expert_fmt=epq.FORMATS[args.expert_fmt] if args.expert_fmt else None,
+                                  down_fmt=epq.FORMATS[args.down_fmt] if args.down_fmt else None)
             W.cfg = wl.MoEDecode()
         else:
             W = MoELayerWorkload(epq, dev, efmt, ntok=args.ntok, replicas=1)
@@ -1076,7 +1100,11 @@ def main():
     ap.add_argument("--workload", default="dense8b", choices=["dense8b", "gemv4096", "moe_decode", "moe_layer"])
     ap.add_argument("--ntok", type=int, default=1, help="tokens per MoE layer forward (moe_layer)")
     ap.add_argument("--chain", action="store_true", help="dense step as one epq_gemv_chain launch")
-    ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K"])
+    ap.add_argument("--fmt", default="Q4_K", choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K", "Q2_K", "Q6_K"])
+    ap.add_argument("--expert-fmt", default=None, choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K", "Q2_K", "Q6_K"],
+                    help="moe_decode: format of the experts (default --fmt)")
+    ap.add_argument("--down-fmt", default=None, choices=["Q8_0", "Q4_0", "Q4_1", "Q4_K", "Q2_K", "Q6_K"],
+                    help="moe_decode: format of the experts' down projections (a mixed recipe)")
     ap.add_argument("--nvec", type=int, default=1)
     ap.add_argument("--attn-ctx", type=int, default=None,
                     help="decode with KV-cache attention over this many cached positions (dense8b, moe_decode)")

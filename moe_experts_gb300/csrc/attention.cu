@@ -15,10 +15,12 @@
 //
 // Organisation: one thread-block cluster of C CTAs per key/value head (the
 // positions split evenly over the C CTAs).
-//   phase 0  CTA rank 0 quantizes the new key and value rows into the cache;
-//            a cluster barrier publishes them;
-//   phase 1  each warp takes positions in turn: lane l holds 4 consecutive
-//            elements of the key row (one 32-bit load of codes plus its
+//   phase 0  the CTA whose positions include `pos` quantizes the step's key
+//            and value rows into the cache and keeps a shared-memory copy for
+//            its own scan (no other CTA reads them in this step);
+//   phase 1  each warp takes runs of 8 consecutive positions (all 8 rows
+//            loaded before any is reduced): lane l holds 4 consecutive
+//            elements of a key row (one 32-bit load of codes plus its
 //            block's fp16 factor) and multiplies them with the `group`
 //            query heads kept in shared memory; the warp sums the products;
 //            scores stay in shared memory (and optionally go to scores_out);
@@ -52,6 +54,7 @@ constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxGroup = 8;       // query heads per key/value head
 constexpr int kMaxCluster = 8;
 constexpr int kMaxPosPerCta = 2048;
+constexpr int kRunMax = 8;         // positions per warp step (rows in flight per warp)
 
 struct AttnParams {
   const float *q;               // [n_heads][D]
@@ -102,12 +105,45 @@ __device__ __forceinline__ void q8_block_lane(float x, uint16_t *d_out, int8_t *
   if ((threadIdx.x & 31) == 0) *d_out = __half_as_ushort(dh);
 }
 
-__device__ __forceinline__ float i8(uint32_t w, int b) {
-  return static_cast<float>(static_cast<int8_t>((w >> (8 * b)) & 0xFFu));
+// Sum over the warp of N values per lane (N a power of two <= 32): a
+// reduce-scatter that halves the set of values each lane carries at every
+// level (offsets 16, 8, ...), then plain butterflies once one value is left.
+// Lane l returns the warp total of value l / (32 / N) (the high bits of the
+// lane pick the value; the 32 / N lanes of a run hold the same total).
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+  int n = N;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    if (n > 1) {
+      const bool up = (lane & o) != 0;
+      const int half = n / 2;
+#pragma unroll
+      for (int j = 0; j < N / 2; ++j) {
+        if (j >= half) break;
+        const float send = up ? v[j] : v[j + half];
+        const float keep = up ? v[j + half] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+      n = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+  return v[0];
+}
+
+// Exact float of int8 code b of a word: with u = q + 128 (the code's byte
+// with its top bit flipped), the bit pattern 0x4B0000uu is the float 2^23 + u.
+__device__ __forceinline__ float i8(uint32_t wflip, int b) {
+  const uint32_t sel = static_cast<uint32_t>(b) | 0x7540u;  // byte b, then zero, zero, 0x4B
+  return __uint_as_float(__byte_perm(wflip, 0x4B000000u, sel)) - 8388736.0f;
 }
 
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  // kRun positions per warp step, so that a step's kRun x G dot products fit one reduce-scatter
+  constexpr int kRun = kRunMax * G <= 32 ? kRunMax : 32 / G;
   extern __shared__ __align__(16) float sm[];
   const int D = p.D;
   const int C = p.C;
@@ -127,66 +163,120 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   float *cmax = sc + G * kMaxPosPerCta;            // [C][G] maxima from every cluster CTA
   float *red = cmax + kMaxCluster * G;             // [warp][G][D + 1]: warp partials
   float *part = red + kAttnWarps * G * (D + 1);    // [C][G][D + 1]: rank 0 only
+  uint8_t *newrow = reinterpret_cast<uint8_t *>(part + C * G * (D + 1));  // [2][row_bytes]: the step's key, value
 
   pdl_launch_dependents();
   pdl_wait();  // q, k_new and v_new come from the preceding projection
 
   // ---------------------------------------------------------------- phase 0
-  uint8_t *krow_new = p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
-  uint8_t *vrow_new = p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
-  if (rank == 0) {
+  // Arrive on the cluster barrier now and wait on it only before the first
+  // store into another CTA's shared memory: every CTA of the cluster has
+  // then started.  The CTA whose range holds position `pos` quantizes the
+  // step's key and value rows, stores them into the cache (no other CTA
+  // reads them in this step) and keeps a shared-memory copy for its scan.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const bool owner = p0 <= p.pos && p.pos < p1;
+  if (owner) {
+    uint8_t *krow_new = p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
+    uint8_t *vrow_new = p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
     // warps 0..nblk-1 quantize the key blocks, the next nblk warps the value blocks
     for (int b = warp; b < 2 * nblk; b += kAttnWarps) {
       const bool isv = b >= nblk;
       const int bb = isv ? b - nblk : b;
       const float x = (isv ? p.v_new : p.k_new)[h * D + 32 * bb + lane];
       uint8_t *row = isv ? vrow_new : krow_new;
+      uint8_t *copy = newrow + (isv ? row_bytes : 0);
       uint16_t d;
       int8_t q;
       q8_block_lane(x, &d, &q);
-      row[2 * nblk + 32 * bb + lane] = static_cast<uint8_t>(q);
-      if (lane == 0) *reinterpret_cast<uint16_t *>(row + 2 * bb) = d;
+      row[2 * nblk + 32 * bb + lane] = copy[2 * nblk + 32 * bb + lane] = static_cast<uint8_t>(q);
+      if (lane == 0) {
+        *reinterpret_cast<uint16_t *>(row + 2 * bb) = d;
+        *reinterpret_cast<uint16_t *>(copy + 2 * bb) = d;
+      }
     }
-    __threadfence();  // the cache rows precede the release of the cluster barrier
   }
   for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = p.q[(h * G + i / D) * D + i % D];
-  cluster_sync();
+  __syncthreads();
+
+  // the lane's query elements stay in registers for the whole scan
+  float4 qr[G][2];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      qr[g][c] = c < D / 128 ? *reinterpret_cast<const float4 *>(qs + g * D + 128 * c + 4 * lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
 
   // ---------------------------------------------------------------- phase 1
-  // lane l: elements 4l..4l+3 of each 128-element chunk (D/128 chunks)
+  // Warp w takes runs of kRun consecutive positions (w*kRun + 8*kRun*j ...);
+  // all rows of a run are loaded before any is reduced, so kRun row loads are
+  // in flight per warp.  Lane l: elements 4l..4l+3 of each 128-element chunk.
   const int nch = D / 128;
   float wmax[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) wmax[g] = -INFINITY;
-  for (int i = warp; i < n; i += kAttnWarps) {
-    const uint8_t *row = p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i) * row_bytes;
-    float acc[G];
+  for (int i0 = warp * kRun; i0 < n; i0 += kAttnWarps * kRun) {
+    uint32_t wk[kRun][2];
+    float dk[kRun][2];
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
-    for (int c = 0; c < nch; ++c) {
-      const int e0 = 128 * c + 4 * lane;
-      const uint32_t w = __ldcg(reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0));
-      const float d = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32)))));
-      const float k0 = d * i8(w, 0), k1 = d * i8(w, 1), k2 = d * i8(w, 2), k3 = d * i8(w, 3);
+    for (int u = 0; u < kRun; ++u) {
+      const int i = min(i0 + u, n - 1);  // past the end: a repeat of the last row, not used
+      const uint8_t *row = p0 + i == p.pos ? newrow
+                                           : p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i) * row_bytes;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float4 qv = *reinterpret_cast<const float4 *>(qs + g * D + e0);
-        acc[g] = fmaf(k0, qv.x, fmaf(k1, qv.y, fmaf(k2, qv.z, fmaf(k3, qv.w, acc[g]))));
+      for (int c = 0; c < 2; ++c) {
+        if (c >= nch) break;
+        const int e0 = 128 * c + 4 * lane;
+        wk[u][c] = *reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0);
+        dk[u][c] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32))));
       }
     }
+    // partial dots of the run's kRun x G (position, head) pairs, then one
+    // reduce-scatter over the warp: lane l ends with the full sum of pair
+    // l % (kRun G) (index u G + g), instead of one butterfly per pair
+    float acc[kRun * G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float s = warp_sum(acc[g]) * p.scale;
-      wmax[g] = fmaxf(wmax[g], s);
-      if (lane == 0) sc[g * kMaxPosPerCta + i] = s;
+    for (int u = 0; u < kRun; ++u) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) acc[u * G + g] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (c >= nch) break;
+        // the lane's 4 elements share one Q8_0 block: the factor d multiplies their sum
+        const uint32_t w = wk[u][c] ^ 0x80808080u;
+        const float k0 = i8(w, 0), k1 = i8(w, 1), k2 = i8(w, 2), k3 = i8(w, 3);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float4 qv = qr[g][c];
+          acc[u * G + g] = fmaf(dk[u][c], fmaf(k0, qv.x, fmaf(k1, qv.y, fmaf(k2, qv.z, k3 * qv.w))), acc[u * G + g]);
+        }
+      }
+    }
+    const float sum = reduce_scatter<kRun * G>(acc, lane);
+    constexpr int kPairs = kRun * G;
+    constexpr int kCopies = 32 / kPairs;  // lanes holding the same pair
+    const int pr = lane / kCopies;        // pair held by this lane
+    const int u = pr / G, g = pr % G;
+    const float sv = sum * p.scale;
+    if (i0 + u < n) {
+      if (lane % kCopies == 0) sc[g * kMaxPosPerCta + i0 + u] = sv;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+        if (gg == g) wmax[gg] = fmaxf(wmax[gg], sv);  // constant indices keep wmax in registers
     }
   }
   // CTA maxima -> every cluster CTA's cmax[rank][g]
   __syncthreads();
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-    if (lane == 0) red[warp * G + g] = wmax[g];  // red holds the warp maxima until phase 2
+  for (int g = 0; g < G; ++g) {
+    float m = wmax[g];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp * G + g] = m;  // red holds the warp maxima until phase 2
+  }
   __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every cluster CTA has started
   if (tid < G) {
     float m = -INFINITY;
     for (int w = 0; w < kAttnWarps; ++w) m = fmaxf(m, red[w * G + tid]);
@@ -201,14 +291,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   cluster_sync();
 
   // ---------------------------------------------------------------- phase 2
-  float M[G], thr[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float m = -INFINITY;
+  // weights once per (head, position), in place of the scores: exp(s - M)
+  // for kept positions, 0 for skipped ones
+  for (int idx = tid; idx < G * n; idx += kAttnThreads) {
+    const int g = idx / n, i = idx - g * n;
+    float m = -INFINITY;  // the cluster maximum of head g (from shared memory: g is not a constant here)
     for (int r = 0; r < C; ++r) m = fmaxf(m, cmax[r * G + g]);
-    M[g] = m;
-    thr[g] = m + p.skip_log;
+    const float sv = sc[g * kMaxPosPerCta + i];
+    sc[g * kMaxPosPerCta + i] = sv >= m + p.skip_log ? expf(sv - m) : 0.0f;
   }
+  __syncthreads();
   float o[G][4 * 2];  // up to D = 256: two 128-element chunks of 4 per lane
   float ws[G];
 #pragma unroll
@@ -217,34 +309,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[g][j] = 0.0f;
   }
-  for (int i = warp; i < n; i += kAttnWarps) {
-    float w[G];
-    bool any = false;
+  // the same runs of positions; the value rows of a run that some query head
+  // keeps are all loaded before they are accumulated (in position order)
+  for (int i0 = warp * kRun; i0 < n; i0 += kAttnWarps * kRun) {
+    float w[kRun][G];
+    bool need[kRun];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float s = sc[g * kMaxPosPerCta + i];
-      w[g] = s >= thr[g] ? expf(s - M[g]) : 0.0f;
-      any = any || s >= thr[g];
-    }
-    if (!any) continue;  // warp-uniform: every lane read the same scores
-    const uint8_t *row = p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i) * row_bytes;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      if (c >= nch) break;
-      const int e0 = 128 * c + 4 * lane;
-      const uint32_t wv = __ldcg(reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0));
-      const float d = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32)))));
-      const float v0 = d * i8(wv, 0), v1 = d * i8(wv, 1), v2 = d * i8(wv, 2), v3 = d * i8(wv, 3);
+    for (int u = 0; u < kRun; ++u) {
+      need[u] = false;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        o[g][4 * c + 0] = fmaf(w[g], v0, o[g][4 * c + 0]);
-        o[g][4 * c + 1] = fmaf(w[g], v1, o[g][4 * c + 1]);
-        o[g][4 * c + 2] = fmaf(w[g], v2, o[g][4 * c + 2]);
-        o[g][4 * c + 3] = fmaf(w[g], v3, o[g][4 * c + 3]);
+        w[u][g] = i0 + u < n ? sc[g * kMaxPosPerCta + i0 + u] : 0.0f;
+        need[u] = need[u] || w[u][g] != 0.0f;
+      }
+    }
+    uint32_t wv[kRun][2];
+    float dv[kRun][2];
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) {
+      if (!need[u]) continue;  // warp-uniform: every lane read the same weights
+      const uint8_t *row = p0 + i0 + u == p.pos
+                               ? newrow + row_bytes
+                               : p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i0 + u) * row_bytes;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (c >= nch) break;
+        const int e0 = 128 * c + 4 * lane;
+        wv[u][c] = *reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0);
+        dv[u][c] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32))));
       }
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) ws[g] += w[g];
+    for (int u = 0; u < kRun; ++u) {
+      if (!need[u]) continue;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (c >= nch) break;
+        const uint32_t wq = wv[u][c] ^ 0x80808080u;
+        const float v0 = i8(wq, 0), v1 = i8(wq, 1), v2 = i8(wq, 2), v3 = i8(wq, 3);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float wd = w[u][g] * dv[u][c];  // weight times the block factor of the lane's elements
+          o[g][4 * c + 0] = fmaf(wd, v0, o[g][4 * c + 0]);
+          o[g][4 * c + 1] = fmaf(wd, v1, o[g][4 * c + 1]);
+          o[g][4 * c + 2] = fmaf(wd, v2, o[g][4 * c + 2]);
+          o[g][4 * c + 3] = fmaf(wd, v3, o[g][4 * c + 3]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) ws[g] += w[u][g];
+    }
   }
   // warp partials -> shared memory, then the CTA sum (warp order) -> rank 0
   __syncthreads();
@@ -281,7 +395,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
 
 size_t attn_smem(int G, int D, int C) {
   return sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * kMaxPosPerCta + kMaxCluster * G +
-                          static_cast<size_t>(kAttnWarps) * G * (D + 1) + static_cast<size_t>(C) * G * (D + 1));
+                          static_cast<size_t>(kAttnWarps) * G * (D + 1) + static_cast<size_t>(C) * G * (D + 1)) +
+         2 * static_cast<size_t>(D + D / 16);
 }
 
 template <int G>
@@ -331,9 +446,10 @@ extern "C" epq_status epq_attention_decode(const float *q, const float *k_new, c
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(out) || (scores_out && !aligned16(scores_out)))
     return EPQ_ERR_ALIGN;
-  // positions per CTA bounded by its shared-memory score buffer
+  // cluster size: enough CTAs that each has at most 64 positions (up to 8
+  // CTAs); positions per CTA bounded by its shared-memory score buffer
   int C = 1;
-  while (C < kMaxCluster && (pos + 1 + C - 1) / C > 256) C *= 2;
+  while (C < kMaxCluster && (pos + 1 + C - 1) / C > 64) C *= 2;
   if ((pos + 1 + C - 1) / C > kMaxPosPerCta) return EPQ_ERR_SHAPE;
   DeviceInfo dev;
   if (!current_device(&dev) || dev.major * 10 + dev.minor < 100) return EPQ_ERR_DEVICE;

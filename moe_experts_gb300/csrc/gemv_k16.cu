@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
   k16::RowOps<FMT> cur_lo, cur_hi, nxt_lo, nxt_hi;
   int sb = kq;
   const bool has_work = active && sb < p.nsb;
+  pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid before reading y
   if (has_work && p.early) {
     k16::load_ops<FMT, ALIGN>(cur_lo, row_lo, nsb, sb, t);
     k16::load_ops<FMT, ALIGN>(cur_hi, row_hi, nsb, sb, t);
@@ -180,7 +181,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
       cur_hi = nxt_hi;
     }
   }
-  pdl_launch_dependents();
 
   // ---------------------------------------------------------------- row totals
   float *red = reinterpret_cast<float *>(smem + L.red);

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
   const int I = a.I, nsb = a.H / 256;
   Meta m(smem + p.meta_off, a.ntok, a.topk);
 
+  pdl_launch_dependents();
   pdl_wait();  // logits, x statistics and cleared max |h| words come from the router kernel
   m.clear(tid, kKThreads);
   __syncthreads();
@@ -193,7 +194,6 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
     }
     __syncthreads();
   }
-  pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------ down + combine
@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
   const int I = a.I, H = a.H, nsbI = I / 256;
   Meta m(smem + p.meta_off, a.ntok, a.topk);
 
+  pdl_launch_dependents();
   pdl_wait();  // h and the routing come from the gate/up kernel
   load_meta(a, m, tid, kKThreads);
   __syncthreads();
@@ -299,7 +300,6 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
     }
     __syncthreads();
   }
-  pdl_launch_dependents();
 }
 
 template <typename K>
