@@ -8,10 +8,10 @@
 //     KP = 8 / RG warps (warp kq takes superblocks kq, kq + KP, ...);
 //   * the CTA first converts all of x into the shared-memory operand records
 //     (one warp per (vector, superblock)), together with the per-superblock
-//     scales, the sub-block sums of x (Q2_K) and the sums of squares (RMS
-//     pre-norm);
+//     scales, the sub-block sums of x and the sums of squares (RMS pre-norm);
 //   * each warp streams its rows' planes straight into registers (16-byte
-//     loads, no L1 allocation), one superblock ahead of the MMAs;
+//     loads, no L1 allocation) through a ring of 4 (Q2_K) or 2 (Q6_K)
+//     superblocks in flight ahead of the MMAs;
 //   * row totals: the 4 lanes of a row add their owners' parts with two
 //     butterflies, the KP warps' partials are added in k-part order through
 //     shared memory (deterministic), then the epilogue applies the RMS
@@ -51,7 +51,7 @@ struct K16Layout {
 
 __host__ __device__ inline uint32_t al16(uint32_t v) { return (v + 15u) & ~15u; }
 
-__host__ __device__ inline K16Layout k16_layout(int nv, int nsb, bool q2k) {
+__host__ __device__ inline K16Layout k16_layout(int nv, int nsb) {
   K16Layout L;
   uint32_t o = 0;
   L.frag = o;
@@ -59,7 +59,7 @@ __host__ __device__ inline K16Layout k16_layout(int nv, int nsb, bool q2k) {
   L.ps = o;
   o = al16(o + 4u * nv * nsb);
   L.xsum = o;
-  if (q2k) o = al16(o + 4u * nv * nsb * 16);
+  o = al16(o + 4u * nv * nsb * 16);
   L.red = o;  // [warp][16 rows][nv]
   o = al16(o + 4u * kWarps * 16 * nv);
   L.ssq = o;  // [warp][nv]
@@ -79,7 +79,7 @@ __device__ __forceinline__ int x_src(int j, int group, int head_dim) {
 template <int FMT, int NV, int ALIGN, bool SW>
 __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const K16Layout L = k16_layout(NV, p.nsb, FMT == EPQ_Q2_K);
+  const K16Layout L = k16_layout(NV, p.nsb);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int kq = warp % p.kp, rgl = warp / p.kp;
@@ -100,19 +100,23 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
   const uint8_t *row_hi = p.W + r_hi * p.row_bytes;
   const int64_t nsb = p.nsb;
 
-  k16::RowOps<FMT> cur_lo, cur_hi, nxt_lo, nxt_hi;
-  int sb = kq;
-  const bool has_work = active && sb < p.nsb;
+  // This warp's superblocks kq, kq + KP, ...: kDepth of them are in flight
+  // (a register ring indexed by compile-time slots).
+  constexpr int kDepth = FMT == EPQ_Q2_K ? 4 : 2;
+  k16::RowOps<FMT> ring_lo[kDepth], ring_hi[kDepth];
+  const int cnt = active && kq < p.nsb ? (p.nsb - kq + p.kp - 1) / p.kp : 0;
   pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid before reading y
-  if (has_work && p.early) {
-    k16::load_ops<FMT, ALIGN>(cur_lo, row_lo, nsb, sb, t);
-    k16::load_ops<FMT, ALIGN>(cur_hi, row_hi, nsb, sb, t);
-  }
+  auto fill = [&]() {
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d)
+      if (d < cnt) {
+        k16::load_ops<FMT, ALIGN>(ring_lo[d], row_lo, nsb, kq + d * p.kp, t);
+        k16::load_ops<FMT, ALIGN>(ring_hi[d], row_hi, nsb, kq + d * p.kp, t);
+      }
+  };
+  if (p.early) fill();
   pdl_wait();
-  if (has_work && !p.early) {
-    k16::load_ops<FMT, ALIGN>(cur_lo, row_lo, nsb, sb, t);
-    k16::load_ops<FMT, ALIGN>(cur_hi, row_hi, nsb, sb, t);
-  }
+  if (!p.early) fill();
 
   // ---------------------------------------------------------------- x staging
   float ssq[NV];
@@ -145,9 +149,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
     for (int w = 0; w < NV; ++w)
       if (w == v) ssq[w] += sq;
     uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
-    const float pv =
-        k16::stage_superblock(xv, frag_sb, lane, FMT == EPQ_Q2_K ? xsum_s + (v * p.nsb + b) * 16 : nullptr);
-    if (lane == 0) ps_s[v * p.nsb + b] = pv;
+    const int ex = k16::stage_superblock(xv, frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
+    if (lane == 0) ps_s[v * p.nsb + b] = k16::sum_scale<FMT>(ex);
   }
   float *ssq_s = reinterpret_cast<float *>(smem + L.ssq);
 #pragma unroll
@@ -163,22 +166,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
   for (int v = 0; v < NV; ++v) acc[0][v] = acc[1][v] = 0.0f;
   const uint32_t frag0 = smem_addr(smem + L.frag) + k16::lane_slot(lane);
   const uint32_t vstride = static_cast<uint32_t>(p.nsb) * k16::kSbFragBytes;
-  if (has_work) {
-    for (;;) {
-      const int nx = sb + p.kp;
-      if (nx < p.nsb) {
-        k16::load_ops<FMT, ALIGN>(nxt_lo, row_lo, nsb, nx, t);
-        k16::load_ops<FMT, ALIGN>(nxt_hi, row_hi, nsb, nx, t);
-      }
+  for (int j0 = 0; j0 < cnt; j0 += kDepth) {
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) {
+      const int j = j0 + d;
+      if (j >= cnt) break;
+      const int b = kq + j * p.kp;
       float ps[NV];
 #pragma unroll
-      for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsb + sb];
-      k16::superblock<FMT, NV>(cur_lo, cur_hi, frag0 + static_cast<uint32_t>(sb) * k16::kSbFragBytes, vstride, ps,
-                               xsum_s + sb * 16, p.nsb * 16, t, acc);
-      if (nx >= p.nsb) break;
-      sb = nx;
-      cur_lo = nxt_lo;
-      cur_hi = nxt_hi;
+      for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsb + b];
+      k16::superblock<FMT, NV>(ring_lo[d], ring_hi[d], frag0 + static_cast<uint32_t>(b) * k16::kSbFragBytes, vstride,
+                               ps, xsum_s + b * 16, p.nsb * 16, t, acc);
+      if (j + kDepth < cnt) {
+        k16::load_ops<FMT, ALIGN>(ring_lo[d], row_lo, nsb, b + kDepth * p.kp, t);
+        k16::load_ops<FMT, ALIGN>(ring_hi[d], row_hi, nsb, b + kDepth * p.kp, t);
+      }
     }
   }
 
@@ -250,7 +252,7 @@ epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, floa
   const int64_t rows_out = sw ? rows / 2 : rows;
   const int nsb = static_cast<int>(cols / 256);
   const int nvl = std::min(nvec, 2);
-  const K16Layout L = k16_layout(nvl, nsb, fmt == EPQ_Q2_K);
+  const K16Layout L = k16_layout(nvl, nsb);
   if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) return EPQ_ERR_SHAPE;
   const int64_t ngroups = (rows_out + (sw ? 7 : 15)) / (sw ? 8 : 16);
   int rg = 8;

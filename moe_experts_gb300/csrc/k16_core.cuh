@@ -21,13 +21,13 @@
 // (10, 14), (11, 15).  The low nibbles of positions (0, 4) are at bits 0-3
 // of the sub-block's first nibble word, (1, 5) at bits 4-7, and (2, 6),
 // (3, 7) the same after a shift by 8 (second word: positions 8..15).  So a
-// pair of codes becomes an fp16 pair with one or two logic ops and one
-// packed fp16 FMA, exactly:
-//   Q2_K  (W & m) read as fp16 = n * 2^-20 (mask A) or n * 2^-16 (mask B);
-//         times 2^10 or 2^6 gives n * 2^-10
+// pair of codes becomes an fp16 MMA operand pair with one or two logic
+// ops, exact (fp16 subnormals, which the tensor cores take as they are):
+//   Q2_K  (W & m) read as fp16 = n * 2^-20 (mask A) or n * 2^-16 (mask B)
 //   Q6_K  (N & nibble mask) | (W & field mask) read as fp16 = u * 2^-24
-//         (A) or u * 2^-20 (B); u * 2^14 - 2^-5 or u * 2^10 - 2^-5 gives
-//         (u - 32) * 2^-10
+//         (A) or u * 2^-20 (B), u = m + 32 (the offset is taken off with
+//         32 * sum(x) per sub-block)
+// and the x operands of class-B slots carry 2^4 less than those of class A.
 //
 // MMA layout (m16n8k16, A row-major, B column-major), one warp per 16 rows:
 //   * A rows are the 16 weight rows; lane (g, t) holds rows g and g + 8;
@@ -43,9 +43,10 @@
 //     exactly the two parts of its own sub-block for rows g and g + 8: the
 //     sub-block scale c (and for Q2_K the lift k * sum(x)) is applied in
 //     float32 right there, no data leaves the lane until the row reduction.
-// x is split per (vector, superblock) with a power-of-two scale 2^sigma that
-// maps its largest |x| into [2^14, 2^15); the superblock factor d is
-// multiplied by 2^(10 - sigma) to undo both scales.
+// x is split per (vector, superblock) into fp16 hi + lo parts after a
+// power-of-two scale that maps its largest |x| into [2^14, 2^15) for the
+// class-A slots; the superblock factor d is multiplied by the inverse
+// scale (sum_scale) to undo it.
 #pragma once
 
 #include "common.cuh"
@@ -60,26 +61,12 @@ constexpr int kSlotBytes = 8;
 constexpr int kMmaBytes = 9 * kSlotBytes;
 constexpr int kSbFragBytes = 16 * kMmaBytes;  // 1152
 
-// fp16 pair constants
-constexpr uint32_t kH2p14 = 0x74007400u;    // {2^14, 2^14}
-constexpr uint32_t kH2p10 = 0x64006400u;    // {2^10, 2^10}
-constexpr uint32_t kH2p6 = 0x54005400u;     // {2^6, 2^6}
-constexpr uint32_t kHm2m5 = 0xA800A800u;    // {-2^-5, -2^-5}
+// operand masks
 constexpr uint32_t kMaskA = 0x00300030u;    // 2-bit fields at bits 4-5 of each half
 constexpr uint32_t kMaskB = 0x03000300u;    // 2-bit fields at bits 8-9
 constexpr uint32_t kNibA = 0x000F000Fu;     // nibbles at bits 0-3
 constexpr uint32_t kNibB = 0x00F000F0u;     // nibbles at bits 4-7
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
 __device__ __forceinline__ uint32_t rotr(uint32_t w, int s) { return __funnelshift_r(w, w, s); }
 
 __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint2 b) {
@@ -186,30 +173,44 @@ __device__ __forceinline__ void load_ops(RowOps<FMT> &o, const uint8_t *row, int
 }
 
 // The 8 fp16 operand pairs of one sub-block of one row, in MMA order:
-// p[2i] and p[2i+1] feed MMA i (k-slots {2t, 2t+1} and {2t+8, 2t+9}).
+// p[2i] and p[2i+1] feed MMA i (k-slots {2t, 2t+1} and {2t+8, 2t+9}).  The
+// pairs are the masked code bits read as fp16 subnormals (the tensor cores
+// take subnormal fp16 operands exactly): even pairs ("class A") carry
+// code * 2^-20 (Q2_K) / u * 2^-24 (Q6_K), odd pairs ("class B") 16 times
+// that; the x operands of the two classes carry the compensating powers of
+// two (stage_superblock).
 __device__ __forceinline__ void pairs_q2k(uint32_t w, uint32_t (&p)[8]) {
   const uint32_t w2 = w >> 2, r = rotr(w, 24), r2 = r >> 2;
-  p[0] = hmul2(w & kMaskA, kH2p10);
-  p[1] = hmul2(w & kMaskB, kH2p6);
-  p[2] = hmul2(w2 & kMaskA, kH2p10);
-  p[3] = hmul2(w2 & kMaskB, kH2p6);
-  p[4] = hmul2(r & kMaskA, kH2p10);
-  p[5] = hmul2(r & kMaskB, kH2p6);
-  p[6] = hmul2(r2 & kMaskA, kH2p10);
-  p[7] = hmul2(r2 & kMaskB, kH2p6);
+  p[0] = w & kMaskA;
+  p[1] = w & kMaskB;
+  p[2] = w2 & kMaskA;
+  p[3] = w2 & kMaskB;
+  p[4] = r & kMaskA;
+  p[5] = r & kMaskB;
+  p[6] = r2 & kMaskA;
+  p[7] = r2 & kMaskB;
 }
 
 __device__ __forceinline__ void pairs_q6k(uint32_t n0, uint32_t n1, uint32_t w, uint32_t (&p)[8]) {
   const uint32_t w2 = w >> 2, r = rotr(w, 24), r2 = r >> 2;
   const uint32_t m0 = n0 >> 8, m1 = n1 >> 8;
-  p[0] = hfma2((n0 & kNibA) | (w & kMaskA), kH2p14, kHm2m5);
-  p[1] = hfma2((n0 & kNibB) | (w & kMaskB), kH2p10, kHm2m5);
-  p[2] = hfma2((m0 & kNibA) | (w2 & kMaskA), kH2p14, kHm2m5);
-  p[3] = hfma2((m0 & kNibB) | (w2 & kMaskB), kH2p10, kHm2m5);
-  p[4] = hfma2((n1 & kNibA) | (r & kMaskA), kH2p14, kHm2m5);
-  p[5] = hfma2((n1 & kNibB) | (r & kMaskB), kH2p10, kHm2m5);
-  p[6] = hfma2((m1 & kNibA) | (r2 & kMaskA), kH2p14, kHm2m5);
-  p[7] = hfma2((m1 & kNibB) | (r2 & kMaskB), kH2p10, kHm2m5);
+  p[0] = (n0 & kNibA) | (w & kMaskA);
+  p[1] = (n0 & kNibB) | (w & kMaskB);
+  p[2] = (m0 & kNibA) | (w2 & kMaskA);
+  p[3] = (m0 & kNibB) | (w2 & kMaskB);
+  p[4] = (n1 & kNibA) | (r & kMaskA);
+  p[5] = (n1 & kNibB) | (r & kMaskB);
+  p[6] = (m1 & kNibA) | (r2 & kMaskA);
+  p[7] = (m1 & kNibB) | (r2 & kMaskB);
+}
+
+// Power of two that brings a superblock's code sums back to code * x units:
+// the class-A product is code * 2^-20 * x * 2^(14 - e) (Q2_K) or
+// u * 2^-24 * x * 2^(14 - e) (Q6_K), e the exponent of the superblock's
+// largest |x| (stage_superblock).
+template <int FMT>
+__device__ __forceinline__ float sum_scale(int e) {
+  return exp2i((FMT == EPQ_Q2_K ? 6 : 10) + e);
 }
 
 // ------------------------------------------------------------------ one superblock
@@ -218,8 +219,9 @@ __device__ __forceinline__ void pairs_q6k(uint32_t n0, uint32_t n1, uint32_t w, 
 //   frag   shared address of this superblock's x operands for vector 0 plus
 //          the lane's slot offset; vector v adds v * vstride
 //   ps     2^(10 - sigma) of this superblock per vector
-//   xsum   Q2_K: shared float sums of x over the superblock's 16 sub-blocks
-//          for vector 0; vector v adds v * xstride floats
+//   xsum   shared float sums of x over the superblock's 16 sub-blocks for
+//          vector 0 (the Q2_K lift term, the Q6_K code offset); vector v adds
+//          v * xstride floats
 template <int FMT, int NV>
 __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<FMT> &hi, uint32_t frag,
                                            uint32_t vstride, const float (&ps)[NV], const float *xsum, int xstride,
@@ -259,12 +261,15 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
         ms[0][v] = fmaf(kl, X, ms[0][v]);
         ms[1][v] = fmaf(kh, X, ms[1][v]);
       }
-    } else {
+    } else {  // codes carry u = m + 32: the sub-block term is c (sum u x - 32 sum x)
       const float cl = s8_to_float((lo.sc >> (8 * q)) & 0xFFu), ch = s8_to_float((hi.sc >> (8 * q)) & 0xFFu);
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
+        const float X = xsum[v * xstride + 4 * t + q];
         cs[0][v] = fmaf(cl, c[v][0] + c[v][1], cs[0][v]);
         cs[1][v] = fmaf(ch, c[v][2] + c[v][3], cs[1][v]);
+        ms[0][v] = fmaf(cl, X, ms[0][v]);
+        ms[1][v] = fmaf(ch, X, ms[1][v]);
       }
     }
   }
@@ -280,8 +285,8 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
     const float dl = half_bits_to_float(lo.d), dh = half_bits_to_float(hi.d);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-      acc[0][v] = fmaf(dl * ps[v], cs[0][v], acc[0][v]);
-      acc[1][v] = fmaf(dh * ps[v], cs[1][v], acc[1][v]);
+      acc[0][v] = fmaf(dl * ps[v], cs[0][v], fmaf(-32.0f * dl, ms[0][v], acc[0][v]));
+      acc[1][v] = fmaf(dh * ps[v], cs[1][v], fmaf(-32.0f * dh, ms[1][v], acc[1][v]));
     }
   }
 }
@@ -289,25 +294,25 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
 // ------------------------------------------------------------------ x staging
 // One warp converts one (vector, superblock) of x: lane l holds positions
 // 8h..8h+7 (h = l & 1) of sub-block s = l >> 1, already gathered into xv.
-// Writes the operand slots of sub-block s, the zero slots (lanes of owner 0),
-// and returns 2^(10 - sigma) (same on every lane).  sum16 receives the
-// sub-block's sum of x (lanes with h = 0 hold it).
-__device__ __forceinline__ float stage_superblock(const float (&xv)[8], uint8_t *frag_sb, int lane, float *sum16) {
+// With e the exponent of the superblock's largest |x| (clamped to
+// [-100, 100]), the class-A slots get x * 2^(14 - e) and the class-B slots
+// x * 2^(10 - e), each split into fp16 hi + lo parts (the largest class-A
+// value lands in [2^14, 2^15)).  Writes the operand slots of sub-block s,
+// the zero slots (lanes of owner 0) and the sub-block's sum of x into
+// sum16[s]; returns e (same on every lane).
+__device__ __forceinline__ int stage_superblock(const float (&xv)[8], uint8_t *frag_sb, int lane, float *sum16) {
   float m = 0.0f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
   m = warp_max_all(m);
-  int sigma = 0;
-  if (m > 0.0f) {
-    const int e = static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127;  // floor(log2 m) for normal m
-    sigma = min(100, max(-100, 14 - e));
-  }
+  int ex = 0;
+  if (m > 0.0f) ex = min(100, max(-100, static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127));
   const int s = lane >> 1, h = lane & 1, q = s & 3, o = s >> 2;
-  uint32_t hi[4], lo[4];  // fp16 pairs (2i', 2i'+4), (2i'+1, 2i'+5) for i' = 0, 1
+  uint32_t hi[4], lo[4];  // fp16 pairs (k, k + 4) for k = 0..3; even k class A, odd k class B
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int a = (k >> 1) * 2 + (k & 1);  // k = 2 i' + r: pair of positions (a, a + 4)
-    const float xa = scale_pow2(xv[a], sigma), xb = scale_pow2(xv[a + 4], sigma);
+    const int sh = (k & 1 ? 10 : 14) - ex;
+    const float xa = scale_pow2(xv[k], sh), xb = scale_pow2(xv[k + 4], sh);
     const __half2 hh = __floats2half2_rn(xa, xb);
     const float2 hf = __half22float2(hh);
     const __half2 ll = __floats2half2_rn(xa - hf.x, xb - hf.y);
@@ -322,14 +327,12 @@ __device__ __forceinline__ float stage_superblock(const float (&xv)[8], uint8_t 
     *reinterpret_cast<uint2 *>(m0 + (2 * o + 1) * kSlotBytes) = make_uint2(lo[2 * ip], lo[2 * ip + 1]);
     if (o == 0) *reinterpret_cast<uint2 *>(m0 + 8 * kSlotBytes) = make_uint2(0u, 0u);
   }
-  if (sum16) {
-    float sx = 0.0f;
+  float sx = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sx += xv[e];
-    const float other = __shfl_xor_sync(0xffffffffu, sx, 1);
-    if (h == 0) sum16[s] = sx + other;
-  }
-  return exp2i(10 - sigma);
+  for (int e = 0; e < 8; ++e) sx += xv[e];
+  const float other = __shfl_xor_sync(0xffffffffu, sx, 1);
+  if (h == 0) sum16[s] = sx + other;
+  return ex;
 }
 
 // Lane's byte offset into a (group, mma) record: its own column's slot when

@@ -48,8 +48,8 @@ struct MkParams {
 __host__ __device__ inline uint32_t mk_al16(uint32_t v) { return (v + 15u) & ~15u; }
 
 // meta | operand records (gate/up: shared with the routing scratch) | scales
-// | sub-block sums of x (Q2_K) | partial sums
-inline void mk_layout(MkParams &p, int nv, bool gateup, bool q2k) {
+// | sub-block sums of x | partial sums
+inline void mk_layout(MkParams &p, int nv, bool gateup) {
   uint32_t o = 0;
   p.meta_off = o;
   o = mk_al16(o + 4u * meta_words(p.a.ntok, p.a.topk));
@@ -60,7 +60,7 @@ inline void mk_layout(MkParams &p, int nv, bool gateup, bool q2k) {
   p.ps_off = o;
   o = mk_al16(o + 4u * nv * p.nsbx);
   p.xsum_off = o;
-  if (q2k) o = mk_al16(o + 4u * nv * p.nsbx * 16);
+  o = mk_al16(o + 4u * nv * p.nsbx * 16);
   p.red_off = o;
   o = mk_al16(o + 4u * kKWarps * 16 * nv);
   p.total = o;
@@ -125,10 +125,9 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
 #pragma unroll
       for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
     }
-    const float pv = k16::stage_superblock(
-        xv, smem + p.frag_off + static_cast<uint32_t>(v * nsb + b) * k16::kSbFragBytes, lane,
-        FMT == EPQ_Q2_K ? xsum_s + (v * nsb + b) * 16 : nullptr);
-    if (lane == 0) ps_s[v * nsb + b] = pv;
+    const int ex = k16::stage_superblock(xv, smem + p.frag_off + static_cast<uint32_t>(v * nsb + b) * k16::kSbFragBytes,
+                                         lane, xsum_s + (v * nsb + b) * 16);
+    if (lane == 0) ps_s[v * nsb + b] = k16::sum_scale<FMT>(ex);
   }
   __syncthreads();
 
@@ -233,10 +232,10 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
 #pragma unroll
       for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
     }
-    const float pv = k16::stage_superblock(
+    const int ex = k16::stage_superblock(
         xv, smem + p.frag_off + static_cast<uint32_t>(v * p.nsbx + b) * k16::kSbFragBytes, lane,
-        FMT == EPQ_Q2_K ? xsum_s + (v * p.nsbx + b) * 16 : nullptr);
-    if (lane == 0) ps_s[v * p.nsbx + b] = pv;
+        xsum_s + (v * p.nsbx + b) * 16);
+    if (lane == 0) ps_s[v * p.nsbx + b] = k16::sum_scale<FMT>(ex);
   }
   __syncthreads();
 
@@ -343,17 +342,16 @@ int pick_rg(int64_t groups, int sm_count) {
 
 bool moe_k16_fits(const MoeArgs &a, int max_slots, bool gateup, bool down, const DeviceInfo &dev) {
   if (a.ntok < 1 || a.ntok > 2) return false;
-  // sized for Q2_K (its sub-block sums of x), the larger of the two
   MkParams p;
   p.a = a;
   if (gateup) {
     p.nsbx = a.H / 256;
-    mk_layout(p, a.ntok, true, true);
+    mk_layout(p, a.ntok, true);
     if (p.total > static_cast<uint32_t>(dev.max_smem_optin)) return false;
   }
   if (down) {
     p.nsbx = max_slots * (a.I / 256);
-    mk_layout(p, a.ntok, false, true);
+    mk_layout(p, a.ntok, false);
     if (p.total > static_cast<uint32_t>(dev.max_smem_optin)) return false;
   }
   return true;
@@ -365,7 +363,7 @@ cudaError_t moe_k16_gateup_launch(epq_fmt fmt, const MoeArgs &a, int max_slots, 
   p.a = a;
   p.nsbx = a.H / 256;
   p.want_hmax = want_hmax ? 1 : 0;
-  mk_layout(p, a.ntok, true, fmt == EPQ_Q2_K);
+  mk_layout(p, a.ntok, true);
   const int64_t groups = static_cast<int64_t>(max_slots) * (a.I / 8);
   p.rg = pick_rg(groups, dev.sm_count);
   p.kp = kKWarps / p.rg;
@@ -383,7 +381,7 @@ cudaError_t moe_k16_down_launch(epq_fmt fmt, const MoeArgs &a, int max_slots, co
   p.a = a;
   p.nsbx = max_slots * (a.I / 256);
   p.want_hmax = 0;
-  mk_layout(p, a.ntok, false, fmt == EPQ_Q2_K);
+  mk_layout(p, a.ntok, false);
   const int64_t groups = (a.H + 15) / 16;
   p.rg = pick_rg(groups, dev.sm_count);
   p.kp = kKWarps / p.rg;
