@@ -894,6 +894,8 @@ def run_epq(args):
     torch.cuda.set_device(dev)
     _build.build()
     epq.load()
+    if args.gemv_engine is not None:
+        epq.epq_set_tuning(epq.EPQ_TUNE_GEMV_ENGINE, args.gemv_engine)
     fmt = epq.FORMATS[args.fmt]
     W = make_workload(epq, dev, fmt, args)
     stream = torch.cuda.Stream(device=dev)
@@ -1113,6 +1115,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub", action="store_true", help="skip the other workloads' sub-objects")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly (no CUDA graph)")
+    ap.add_argument("--gemv-engine", type=int, default=None,
+                    help="EPQ_TUNE_GEMV_ENGINE for this run (0 automatic, 1 CUDA cores, 2 tensor cores, "
+                         "3 block-diagonal tensor-core engine for Q4_K)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -110,11 +110,14 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *                        engines (4096 .. 131072)
  *   EPQ_TUNE_RING_BYTES  shared-memory ring budget per CTA (32768 .. 200704)
  *   EPQ_TUNE_GEMV_ENGINE engine of the Q4_K GEMVs and MoE experts:
- *                        0 automatic (the tensor-core engine for two or more
- *                        vectors, for one vector over matrices of >= 2 MiB,
- *                        and for the MoE expert stages), 1 CUDA-core engines
- *                        only (also for the MoE experts), 2 tensor-core
- *                        engine wherever it applies
+ *                        0 automatic (the block-diagonal tensor-core engine
+ *                        of the Q2_K / Q6_K GEMV for one or two vectors, the
+ *                        ring tensor-core engine for three or more and for
+ *                        the MoE expert stages), 1 CUDA-core engines only
+ *                        (also for the MoE experts), 2 the ring tensor-core
+ *                        engine wherever it applies (one vector under 2 MiB:
+ *                        CUDA cores), 3 the block-diagonal engine for every
+ *                        Q4_K GEMV (the MoE experts as in 0)
  *   EPQ_TUNE_EARLY_STAGES pipeline stages the tensor-core GEMV issues before
  *                        its grid-dependency wait when weights_ready is set
  *                        (0 .. 16, default 4)

@@ -111,7 +111,7 @@ int epq_set_tuning(int key, int value) {
       if (value < 32768 || value > 200704) return -1;
       return epq::g_ring_bytes.exchange(value);
     case EPQ_TUNE_GEMV_ENGINE:
-      if (value < 0 || value > 2) return -1;
+      if (value < 0 || value > 3) return -1;
       return epq::g_gemv_engine.exchange(value);
     case EPQ_TUNE_EARLY_STAGES:
       if (value < 0 || value > 16) return -1;

@@ -688,13 +688,19 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   const int64_t rows_out = opts.swiglu ? rows / 2 : rows;
   const bool sw = opts.swiglu != 0;
   const int xs = opts.x_ld ? static_cast<int>(opts.x_ld) : static_cast<int>(cols / xg);
-  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K) return gemv_k16_launch(fmt, blocks, x, y, rows, cols, nvec, opts, xs, dev, s);
+  // Q2_K / Q6_K, and Q4_K with one or two vectors (or engine 3): the
+  // block-diagonal tensor-core engine (gemv_k16.cu), measured faster than the
+  // ring engine below on every matrix of the 8B-class decode step.  Three or
+  // more Q4_K vectors keep the ring engine's one-pass multi-vector form.
+  const int eng0 = tune_gemv_engine();
+  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K ||
+      (fmt == EPQ_Q4_K && (eng0 == 3 || (eng0 == 0 && nvec <= 2))))
+    return gemv_k16_launch(fmt, blocks, x, y, rows, cols, nvec, opts, xs, dev, s);
 
-  // Q4_K: the tensor-core engine (two vectors per weight pass, more in the
-  // multi-vector form).  With one vector it is chosen for matrices of >= 2
-  // MiB (a 2048x2048 projection and up), where its lower instruction count
-  // per weight pays; smaller one-vector launches keep the one-shot CUDA-core
-  // form, whose prologue is shorter.
+  // Q4_K (three or more vectors, or engine 2): the ring tensor-core engine
+  // (two vectors per weight pass, more in the multi-vector form).  Engine 2
+  // with one vector takes it for matrices of >= 2 MiB; smaller one-vector
+  // launches keep the one-shot CUDA-core form, whose prologue is shorter.
   const int eng = tune_gemv_engine();
   const bool tc_auto = nvec >= 2 || rows * row_bytes >= (int64_t(2) << 20);
   TcPlan tp;

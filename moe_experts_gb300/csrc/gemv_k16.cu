@@ -1,11 +1,14 @@
-// Tensor-core dequant-GEMV for Q2_K and Q6_K (epq_gemv / epq_gemv_ex).
+// Tensor-core dequant-GEMV for Q2_K and Q6_K (epq_gemv / epq_gemv_ex), and
+// the block-diagonal engine for Q4_K (EPQ_TUNE_GEMV_ENGINE 3).
 //
 // [H] "速度上限：带宽 ÷ 权重字节数": batch-1 decode streams every packed
 // weight once per token.  The operand decode and the MMA layout are those of
 // k16_core.cuh; this file adds the CTA organisation:
-//   * a CTA of 8 warps owns RG row groups (16 output rows each; 8 gate + 8
-//     up rows with SwiGLU) and splits the superblocks of every row between
-//     KP = 8 / RG warps (warp kq takes superblocks kq, kq + KP, ...);
+//   * a CTA of 8 warps works on RG row groups at a time (16 output rows
+//     each; 8 gate + 8 up rows with SwiGLU) and splits the superblocks of
+//     every row between KP = 8 / RG warps (warp kq takes superblocks kq,
+//     kq + KP, ...); the grid holds at most two CTAs per SM and a CTA loops
+//     over blocks of RG groups (k16_split picks RG and the grid);
 //   * the CTA first converts all of x into the shared-memory operand records
 //     (one warp per (vector, superblock)), together with the per-superblock
 //     scales, the sub-block sums of x and the sums of squares (RMS pre-norm);
@@ -83,30 +86,39 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int kq = warp % p.kp, rgl = warp / p.kp;
-  const int64_t rg = static_cast<int64_t>(blockIdx.x) * p.rg + rgl;
   constexpr int kOut = SW ? 8 : 16;  // outputs per row group
-  // rows of A held by this lane: g (lo) and g + 8 (hi)
-  int64_t r_lo, r_hi;
-  if (SW) {
-    const int64_t o = min(rg * 8 + g, p.rows_out - 1);
-    r_lo = o;
-    r_hi = p.up_rows + o;
-  } else {
-    r_lo = min(rg * 16 + g, p.rows_out - 1);
-    r_hi = min(rg * 16 + g + 8, p.rows_out - 1);
-  }
-  const bool active = rgl < p.rg && rg * kOut < p.rows_out;
-  const uint8_t *row_lo = p.W + r_lo * p.row_bytes;
-  const uint8_t *row_hi = p.W + r_hi * p.row_bytes;
+  // The CTA takes the row-group blocks blockIdx.x, blockIdx.x + gridDim.x,
+  // ... (RG groups each); x is staged once for all of them.
+  const int64_t ngroups = (p.rows_out + kOut - 1) / kOut;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * p.rg, stride = static_cast<int64_t>(gridDim.x) * p.rg;
+  const int iters = first < ngroups ? static_cast<int>((ngroups - first + stride - 1) / stride) : 0;
   const int64_t nsb = p.nsb;
+  // rows of A held by this lane in iteration it: g (lo) and g + 8 (hi),
+  // clamped to the matrix (rows past the end are read but not stored)
+  auto rows_of = [&](int it, const uint8_t *&lo, const uint8_t *&hi) {
+    const int64_t rg = first + it * stride + rgl;
+    int64_t r_lo, r_hi;
+    if (SW) {
+      r_lo = min(rg * 8 + g, p.rows_out - 1);
+      r_hi = p.up_rows + r_lo;
+    } else {
+      r_lo = min(rg * 16 + g, p.rows_out - 1);
+      r_hi = min(rg * 16 + g + 8, p.rows_out - 1);
+    }
+    lo = p.W + r_lo * p.row_bytes;
+    hi = p.W + r_hi * p.row_bytes;
+  };
 
-  // This warp's superblocks kq, kq + KP, ...: kDepth of them are in flight
-  // (a register ring indexed by compile-time slots).
+  // This warp's superblocks kq, kq + KP, ... of each row group: kDepth of
+  // them are in flight (a register ring indexed by compile-time slots); the
+  // first ones of the next row group are issued before the row totals.
   constexpr int kDepth = FMT == EPQ_Q2_K ? 4 : 2;
   k16::RowOps<FMT> ring_lo[kDepth], ring_hi[kDepth];
-  const int cnt = active && kq < p.nsb ? (p.nsb - kq + p.kp - 1) / p.kp : 0;
+  const int cnt = kq < p.nsb ? (p.nsb - kq + p.kp - 1) / p.kp : 0;
   pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid before reading y
-  auto fill = [&]() {
+  const uint8_t *row_lo = nullptr, *row_hi = nullptr;
+  auto fill = [&](int it) {
+    rows_of(it, row_lo, row_hi);
 #pragma unroll
     for (int d = 0; d < kDepth; ++d)
       if (d < cnt) {
@@ -114,9 +126,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
         k16::load_ops<FMT, ALIGN>(ring_hi[d], row_hi, nsb, kq + d * p.kp, t);
       }
   };
-  if (p.early) fill();
+  if (p.early && iters > 0) fill(0);
   pdl_wait();
-  if (!p.early) fill();
+  if (!p.early && iters > 0) fill(0);
 
   // ---------------------------------------------------------------- x staging
   float ssq[NV];
@@ -149,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
     for (int w = 0; w < NV; ++w)
       if (w == v) ssq[w] += sq;
     uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
-    const int ex = k16::stage_superblock(xv, frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
+    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, frag_sb, lane, xsum_s + (v * p.nsb + b) * 16)
+                                   : k16::stage_superblock(xv, frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
     if (lane == 0) ps_s[v * p.nsb + b] = k16::sum_scale<FMT>(ex);
   }
   float *ssq_s = reinterpret_cast<float *>(smem + L.ssq);
@@ -161,62 +174,72 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
   __syncthreads();
 
   // ---------------------------------------------------------------- main loop
-  float acc[2][NV];
-#pragma unroll
-  for (int v = 0; v < NV; ++v) acc[0][v] = acc[1][v] = 0.0f;
   const uint32_t frag0 = smem_addr(smem + L.frag) + k16::lane_slot(lane);
   const uint32_t vstride = static_cast<uint32_t>(p.nsb) * k16::kSbFragBytes;
-  for (int j0 = 0; j0 < cnt; j0 += kDepth) {
-#pragma unroll
-    for (int d = 0; d < kDepth; ++d) {
-      const int j = j0 + d;
-      if (j >= cnt) break;
-      const int b = kq + j * p.kp;
-      float ps[NV];
-#pragma unroll
-      for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsb + b];
-      k16::superblock<FMT, NV>(ring_lo[d], ring_hi[d], frag0 + static_cast<uint32_t>(b) * k16::kSbFragBytes, vstride,
-                               ps, xsum_s + b * 16, p.nsb * 16, t, acc);
-      if (j + kDepth < cnt) {
-        k16::load_ops<FMT, ALIGN>(ring_lo[d], row_lo, nsb, b + kDepth * p.kp, t);
-        k16::load_ops<FMT, ALIGN>(ring_hi[d], row_hi, nsb, b + kDepth * p.kp, t);
-      }
-    }
-  }
-
-  // ---------------------------------------------------------------- row totals
   float *red = reinterpret_cast<float *>(smem + L.red);
+  float rs[NV];  // RMS factors of the vectors
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      float s = acc[r][v];
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      if (t == 0) red[(warp * 16 + g + 8 * r) * NV + v] = s;
-    }
-  __syncthreads();
-  const int nout = p.rg * kOut * NV;
-  for (int idx = threadIdx.x; idx < nout; idx += kThreads) {
-    const int v = idx % NV, o = (idx / NV) % kOut, gl = idx / (NV * kOut);
-    const int64_t i = (static_cast<int64_t>(blockIdx.x) * p.rg + gl) * kOut + o;
-    if (v >= p.nv || i >= p.rows_out) continue;
-    float rs = 1.0f;
+  for (int v = 0; v < NV; ++v) {
+    rs[v] = 1.0f;
     if (p.rms) {
       float q = 0.0f;
       for (int w = 0; w < kWarps; ++w) q += ssq_s[w * NV + v];
-      rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.nsb * 256)), p.rms_eps)));
+      rs[v] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, static_cast<float>(p.nsb * 256)), p.rms_eps)));
     }
-    float a = 0.0f, b = 0.0f;
-    for (int k = 0; k < p.kp; ++k) {
-      const float *rr = red + ((gl * p.kp + k) * 16) * NV;
-      a += rr[o * NV + v];
-      if (SW) b += rr[(o + 8) * NV + v];
+  }
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    float acc[2][NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[0][v] = acc[1][v] = 0.0f;
+    for (int j0 = 0; j0 < cnt; j0 += kDepth) {
+#pragma unroll
+      for (int d = 0; d < kDepth; ++d) {
+        const int j = j0 + d;
+        if (j >= cnt) break;
+        const int b = kq + j * p.kp;
+        float ps[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsb + b];
+        k16::superblock<FMT, NV>(ring_lo[d], ring_hi[d], frag0 + static_cast<uint32_t>(b) * k16::kSbFragBytes,
+                                 vstride, ps, xsum_s + b * 16, p.nsb * 16, t, acc);
+        if (j + kDepth < cnt) {
+          k16::load_ops<FMT, ALIGN>(ring_lo[d], row_lo, nsb, b + kDepth * p.kp, t);
+          k16::load_ops<FMT, ALIGN>(ring_hi[d], row_hi, nsb, b + kDepth * p.kp, t);
+        }
+      }
     }
-    float val = a * rs;
-    if (SW) val = silu(val) * (b * rs);
-    if (p.residual) val += p.residual[v * p.y_stride + i];
-    p.y[v * p.y_stride + i] = val;
+    if (it + 1 < iters) fill(it + 1);
+
+    // ---------------------------------------------------------------- row totals
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float s = acc[r][v];
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (t == 0) red[(warp * 16 + g + 8 * r) * NV + v] = s;
+      }
+    __syncthreads();
+    const int nout = p.rg * kOut * NV;
+    for (int idx = threadIdx.x; idx < nout; idx += kThreads) {
+      const int v = idx % NV, o = (idx / NV) % kOut, gl = idx / (NV * kOut);
+      const int64_t i = (first + it * stride + gl) * kOut + o;
+      if (v >= p.nv || i >= p.rows_out) continue;
+      float a = 0.0f, b = 0.0f;
+      for (int k = 0; k < p.kp; ++k) {
+        const float *rr = red + ((gl * p.kp + k) * 16) * NV;
+        a += rr[o * NV + v];
+        if (SW) b += rr[(o + 8) * NV + v];
+      }
+      const float r = NV > 1 && v == NV - 1 ? rs[NV - 1] : rs[0];  // constant indices keep rs in registers
+      float val = a * r;
+      if (SW) val = silu(val) * (b * r);
+      if (p.residual) val += p.residual[v * p.y_stride + i];
+      p.y[v * p.y_stride + i] = val;
+    }
+    __syncthreads();  // red is rewritten by the next row group
   }
 }
 
@@ -241,6 +264,30 @@ cudaError_t dispatch_k16(const K16Params &p, int align, bool sw, unsigned grid, 
   return cudaErrorInvalidValue;
 }
 
+// Row groups per CTA (RG; the 8 warps split the superblocks KP = 8 / RG
+// ways) and grid.  Two CTAs per SM hide latency far better than one, so
+// among the RGs that still give every SM two CTAs (blocks >= 2 SMs) the one
+// with the fewest per-CTA iterations x (superblocks per warp + 1 for the
+// per-iteration reduction) wins, ties going to the larger RG; when no RG
+// fills the GPU twice, RG = 1 and one CTA per row group.
+void k16_split(int64_t ngroups, int nsb, int sms, int *rg_out, unsigned *grid_out) {
+  const int64_t cap = 2ll * sms;
+  int64_t best = -1;
+  *rg_out = 1;
+  *grid_out = static_cast<unsigned>(std::max<int64_t>(1, std::min(ngroups, cap)));
+  for (int rg = 8; rg >= 1; rg >>= 1) {
+    const int64_t units = (ngroups + rg - 1) / rg;
+    if (units < cap) continue;
+    const int kp = kWarps / rg;
+    const int64_t cost = (units + cap - 1) / cap * ((nsb + kp - 1) / kp + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      *rg_out = rg;
+      *grid_out = static_cast<unsigned>(cap);
+    }
+  }
+}
+
 }  // namespace
 
 // Called by gemv_launch (gemv.cu) after the common argument checks.
@@ -255,8 +302,9 @@ epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, floa
   const K16Layout L = k16_layout(nvl, nsb);
   if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) return EPQ_ERR_SHAPE;
   const int64_t ngroups = (rows_out + (sw ? 7 : 15)) / (sw ? 8 : 16);
-  int rg = 8;
-  while (rg > 1 && (ngroups + rg - 1) / rg < 2ll * dev.sm_count) rg >>= 1;
+  int rg = 1;
+  unsigned grid = 1;
+  k16_split(ngroups, nsb, dev.sm_count, &rg, &grid);
   K16Params p;
   p.W = static_cast<const uint8_t *>(blocks);
   p.rows_out = rows_out;
@@ -272,7 +320,6 @@ epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, floa
   p.x_group = o.x_group > 1 ? o.x_group : 1;
   p.x_head_dim = o.x_head_dim;
   p.early = o.weights_ready ? 1 : 0;
-  const unsigned grid = static_cast<unsigned>((ngroups + rg - 1) / rg);
   const int align = row_bytes % 16 == 0 ? 16 : (row_bytes % 4 == 0 ? 4 : 2);
   for (int v0 = 0; v0 < nvec; v0 += 2) {
     p.nv = std::min(2, nvec - v0);
@@ -280,7 +327,10 @@ epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, floa
     p.y = y + v0 * rows_out;
     p.residual = o.residual ? o.residual + v0 * rows_out : nullptr;
     cudaError_t e;
-    if (fmt == EPQ_Q2_K)
+    if (fmt == EPQ_Q4_K)  // 144-byte superblocks: every row starts on a 16-byte boundary
+      e = nvl == 1 ? dispatch_sw<EPQ_Q4_K, 1, 16>(p, sw, grid, L.total, s)
+                   : dispatch_sw<EPQ_Q4_K, 2, 16>(p, sw, grid, L.total, s);
+    else if (fmt == EPQ_Q2_K)
       e = nvl == 1 ? dispatch_k16<EPQ_Q2_K, 1>(p, align, sw, grid, L.total, s)
                    : dispatch_k16<EPQ_Q2_K, 2>(p, align, sw, grid, L.total, s);
     else

@@ -137,6 +137,12 @@ struct RowOps<EPQ_Q6_K> {
   uint32_t d;      // f16 d
 };
 
+template <>
+struct RowOps<EPQ_Q4_K> {
+  uint32_t qs[8];  // nibbles of sub-blocks 2t, 2t+1 (four words each; word i = weights 8i..8i+7)
+  uint4 hdr;       // f16 d | f16 dmin, then the 96-bit stream of scale and min codes
+};
+
 // ALIGN: the rows start on 16-byte boundaries (row bytes % 16 == 0: wide
 // planes read 16 bytes at a time), on 4-byte boundaries (word loads) or, for
 // Q6_K rows of an odd number of superblocks, on 2-byte boundaries.
@@ -153,6 +159,12 @@ __device__ __forceinline__ void load_ops(RowOps<FMT> &o, const uint8_t *row, int
     }
     o.sub = ldg_word<ALIGN>(row + 64 * nsb + 16 * static_cast<int64_t>(sb) + 4 * t);
     o.fac = ldg_word<ALIGN>(row + 80 * nsb + 4 * static_cast<int64_t>(sb));
+  } else if constexpr (FMT == EPQ_Q4_K) {  // 144-byte superblocks: rows are always 16-byte multiples
+    const uint8_t *b = row + 144 * static_cast<int64_t>(sb);
+    const uint4 h = ldg_stream16(b), a = ldg_stream16(b + 16 + 32 * t), c = ldg_stream16(b + 32 + 32 * t);
+    o.hdr = h;
+    o.qs[0] = a.x, o.qs[1] = a.y, o.qs[2] = a.z, o.qs[3] = a.w;
+    o.qs[4] = c.x, o.qs[5] = c.y, o.qs[6] = c.z, o.qs[7] = c.w;
   } else {
     const uint8_t *lp = row + 128 * static_cast<int64_t>(sb) + 32 * t;
     const uint8_t *hp = row + 128 * nsb + 64 * static_cast<int64_t>(sb) + 16 * t;
@@ -210,7 +222,66 @@ __device__ __forceinline__ void pairs_q6k(uint32_t n0, uint32_t n1, uint32_t w, 
 // largest |x| (stage_superblock).
 template <int FMT>
 __device__ __forceinline__ float sum_scale(int e) {
-  return exp2i((FMT == EPQ_Q2_K ? 6 : 10) + e);
+  return exp2i((FMT == EPQ_Q2_K ? 6 : 10) + e);  // Q4_K nibbles carry 2^-24 like the Q6_K codes
+}
+
+// Q4_K: the 6-bit scale / min codes of sub-blocks 2t, 2t+1 from a
+// superblock header (the 96-bit stream: c_0..c_7 at bits 0..47, k_0..k_7 at
+// bits 48..95, code j at bits 6j).
+__device__ __forceinline__ void q4k_codes(const uint4 &h, int t, float (&c)[2], float (&k)[2]) {
+  const uint64_t cf = static_cast<uint64_t>(h.y) | (static_cast<uint64_t>(h.z) << 32);
+  const uint64_t kf = static_cast<uint64_t>(h.z) | (static_cast<uint64_t>(h.w) << 32);
+  const uint32_t cc = static_cast<uint32_t>(cf >> (12 * t)), kk = static_cast<uint32_t>(kf >> (16 + 12 * t));
+  c[0] = u8_to_float(cc & 63u);
+  c[1] = u8_to_float((cc >> 6) & 63u);
+  k[0] = u8_to_float(kk & 63u);
+  k[1] = u8_to_float((kk >> 6) & 63u);
+}
+
+// Q4_K superblock: lane t owns sub-blocks 2t (group 0) and 2t+1 (group 1)
+// of 32 weights; MMA m of a group takes nibble word m/2, positions
+// (0,4)(1,5) for even m and (2,6)(3,7) for odd m (the word shifted by 8),
+// as fp16 subnormals n 2^-24 (class A) and 16 n 2^-24 (class B).
+template <int NV>
+__device__ __forceinline__ void superblock_q4k(const RowOps<EPQ_Q4_K> &lo, const RowOps<EPQ_Q4_K> &hi, uint32_t frag,
+                                               uint32_t vstride, const float (&ps)[NV], const float *xsum, int xstride,
+                                               int t, float (&acc)[2][NV]) {
+  float cl[2], kl[2], ch[2], kh[2];
+  q4k_codes(lo.hdr, t, cl, kl);
+  q4k_codes(hi.hdr, t, ch, kh);
+  float cs[2][NV], ms[2][NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) cs[0][v] = cs[1][v] = ms[0][v] = ms[1][v] = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    float c[NV][4];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) c[v][0] = c[v][1] = c[v][2] = c[v][3] = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint32_t wl = m & 1 ? lo.qs[4 * q + m / 2] >> 8 : lo.qs[4 * q + m / 2];
+      const uint32_t wh = m & 1 ? hi.qs[4 * q + m / 2] >> 8 : hi.qs[4 * q + m / 2];
+      const uint32_t a[4] = {wl & kNibA, wh & kNibA, wl & kNibB, wh & kNibB};
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+        mma(c[v], a, lds64(frag + v * vstride + static_cast<uint32_t>((q * 8 + m) * kMmaBytes)));
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const float X = xsum[v * xstride + 2 * t + q];
+      cs[0][v] = fmaf(cl[q], c[v][0] + c[v][1], cs[0][v]);
+      cs[1][v] = fmaf(ch[q], c[v][2] + c[v][3], cs[1][v]);
+      ms[0][v] = fmaf(kl[q], X, ms[0][v]);
+      ms[1][v] = fmaf(kh[q], X, ms[1][v]);
+    }
+  }
+  const float dl = half_bits_to_float(lo.hdr.x), ml = half_bits_to_float(lo.hdr.x >> 16);
+  const float dh = half_bits_to_float(hi.hdr.x), mh = half_bits_to_float(hi.hdr.x >> 16);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    acc[0][v] = fmaf(dl * ps[v], cs[0][v], fmaf(-ml, ms[0][v], acc[0][v]));
+    acc[1][v] = fmaf(dh * ps[v], cs[1][v], fmaf(-mh, ms[1][v], acc[1][v]));
+  }
 }
 
 // ------------------------------------------------------------------ one superblock
@@ -226,6 +297,10 @@ template <int FMT, int NV>
 __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<FMT> &hi, uint32_t frag,
                                            uint32_t vstride, const float (&ps)[NV], const float *xsum, int xstride,
                                            int t, float (&acc)[2][NV]) {
+  if constexpr (FMT == EPQ_Q4_K) {
+    superblock_q4k<NV>(lo, hi, frag, vstride, ps, xsum, xstride, t, acc);
+    return;
+  } else {
   float cs[2][NV], ms[2][NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) cs[0][v] = cs[1][v] = ms[0][v] = ms[1][v] = 0.0f;
@@ -289,6 +364,7 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
       acc[1][v] = fmaf(dh * ps[v], cs[1][v], fmaf(-32.0f * dh, ms[1][v], acc[1][v]));
     }
   }
+  }
 }
 
 // ------------------------------------------------------------------ x staging
@@ -332,6 +408,45 @@ __device__ __forceinline__ int stage_superblock(const float (&xv)[8], uint8_t *f
   for (int e = 0; e < 8; ++e) sx += xv[e];
   const float other = __shfl_xor_sync(0xffffffffu, sx, 1);
   if (h == 0) sum16[s] = sx + other;
+  return ex;
+}
+
+// Q4_K staging: lane l holds positions 8l..8l+7 of the superblock = word
+// i = l & 3 of sub-block s = l >> 2 (owner s >> 1, group s & 1), which feed
+// MMAs 2i (pairs (0,4), (1,5)) and 2i+1 (pairs (2,6), (3,7)) of the group.
+// Same scales as stage_superblock; sum8[s] receives the sub-block's sum of x.
+__device__ __forceinline__ int stage_superblock_q4k(const float (&xv)[8], uint8_t *frag_sb, int lane, float *sum8) {
+  float m = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
+  m = warp_max_all(m);
+  int ex = 0;
+  if (m > 0.0f) ex = min(100, max(-100, static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127));
+  const int s = lane >> 2, i = lane & 3, q = s & 1, o = s >> 1;
+  uint32_t hi[4], lo[4];  // fp16 pairs (k, k + 4); even k class A, odd k class B
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int sh = (k & 1 ? 10 : 14) - ex;
+    const float xa = scale_pow2(xv[k], sh), xb = scale_pow2(xv[k + 4], sh);
+    const __half2 hh = __floats2half2_rn(xa, xb);
+    const float2 hf = __half22float2(hh);
+    const __half2 ll = __floats2half2_rn(xa - hf.x, xb - hf.y);
+    hi[k] = *reinterpret_cast<const uint32_t *>(&hh);
+    lo[k] = *reinterpret_cast<const uint32_t *>(&ll);
+  }
+#pragma unroll
+  for (int mm = 0; mm < 2; ++mm) {
+    uint8_t *m0 = frag_sb + (q * 8 + 2 * i + mm) * kMmaBytes;
+    *reinterpret_cast<uint2 *>(m0 + (2 * o) * kSlotBytes) = make_uint2(hi[2 * mm], hi[2 * mm + 1]);
+    *reinterpret_cast<uint2 *>(m0 + (2 * o + 1) * kSlotBytes) = make_uint2(lo[2 * mm], lo[2 * mm + 1]);
+    if (o == 0) *reinterpret_cast<uint2 *>(m0 + 8 * kSlotBytes) = make_uint2(0u, 0u);
+  }
+  float sx = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sx += xv[e];
+  sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+  sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+  if (i == 0) sum8[s] = sx;
   return ex;
 }
 

@@ -1344,7 +1344,12 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   if (!workspace || workspace_bytes < L.total) return EPQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return EPQ_ERR_ALIGN;
   const epq_fmt gf = experts->fmt, df = experts->down_fmt_set ? experts->down_fmt : experts->fmt;
-  const bool k16g = gf == EPQ_Q2_K || gf == EPQ_Q6_K, k16d = df == EPQ_Q2_K || df == EPQ_Q6_K;
+  // the k16 expert kernels: Q2_K / Q6_K stages, and Q4_K ones under engine 3
+  // (measured in the chained layer: no faster than the ring kernels, which
+  // stay the automatic choice for Q4_K experts)
+  const int eng_t = tune_gemv_engine();
+  const bool k16g = gf == EPQ_Q2_K || gf == EPQ_Q6_K || (eng_t == 3 && gf == EPQ_Q4_K);
+  const bool k16d = df == EPQ_Q2_K || df == EPQ_Q6_K || (eng_t == 3 && df == EPQ_Q4_K);
   const bool whole = (o.stages & 7) == 0 || (o.stages & 7) == 7;
   // Tokens per pass of the Q2_K / Q6_K expert kernels: two when their
   // operands fit shared memory, else one.

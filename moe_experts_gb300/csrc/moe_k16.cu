@@ -1,6 +1,7 @@
 // Tensor-core expert kernels of the MoE layer for experts stored as Q2_K or
-// Q6_K (one or two tokens per launch), and for the Q2_K / Q6_K half of a
-// mixed recipe (gate/up in one format, down in another).
+// Q6_K (one or two tokens per launch), for the Q2_K / Q6_K half of a mixed
+// recipe (gate/up in one format, down in another), and for Q4_K experts
+// under EPQ_TUNE_GEMV_ENGINE 3.
 //
 // "Flash-MoE：在笔记本上运行 397B 参数大模型", section "每层流水线": the selected
 // experts' gate/up projections with SwiGLU, then the down projections and
@@ -125,8 +126,9 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
 #pragma unroll
       for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
     }
-    const int ex = k16::stage_superblock(xv, smem + p.frag_off + static_cast<uint32_t>(v * nsb + b) * k16::kSbFragBytes,
-                                         lane, xsum_s + (v * nsb + b) * 16);
+    uint8_t *fr = smem + p.frag_off + static_cast<uint32_t>(v * nsb + b) * k16::kSbFragBytes;
+    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, fr, lane, xsum_s + (v * nsb + b) * 16)
+                                   : k16::stage_superblock(xv, fr, lane, xsum_s + (v * nsb + b) * 16);
     if (lane == 0) ps_s[v * nsb + b] = k16::sum_scale<FMT>(ex);
   }
   __syncthreads();
@@ -232,9 +234,9 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
 #pragma unroll
       for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
     }
-    const int ex = k16::stage_superblock(
-        xv, smem + p.frag_off + static_cast<uint32_t>(v * p.nsbx + b) * k16::kSbFragBytes, lane,
-        xsum_s + (v * p.nsbx + b) * 16);
+    uint8_t *fr = smem + p.frag_off + static_cast<uint32_t>(v * p.nsbx + b) * k16::kSbFragBytes;
+    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, fr, lane, xsum_s + (v * p.nsbx + b) * 16)
+                                   : k16::stage_superblock(xv, fr, lane, xsum_s + (v * p.nsbx + b) * 16);
     if (lane == 0) ps_s[v * p.nsbx + b] = k16::sum_scale<FMT>(ex);
   }
   __syncthreads();
@@ -370,6 +372,9 @@ cudaError_t moe_k16_gateup_launch(epq_fmt fmt, const MoeArgs &a, int max_slots, 
   const unsigned grid = static_cast<unsigned>(
       std::max<int64_t>(1, std::min<int64_t>((groups + p.rg - 1) / p.rg, 2ll * dev.sm_count)));
   const int align = row_align(a.gu_row_bytes, a.gu_stride);
+  if (fmt == EPQ_Q4_K)  // 144-byte superblocks: rows and (16-byte) strides keep 16-byte alignment
+    return a.ntok == 1 ? mk_launch(moe_k16_gateup_kernel<EPQ_Q4_K, 1, 16>, p, grid, s)
+                       : mk_launch(moe_k16_gateup_kernel<EPQ_Q4_K, 2, 16>, p, grid, s);
   if (fmt == EPQ_Q2_K)
     return a.ntok == 1 ? gateup_by_align<EPQ_Q2_K, 1>(p, align, grid, s) : gateup_by_align<EPQ_Q2_K, 2>(p, align, grid, s);
   return a.ntok == 1 ? gateup_by_align<EPQ_Q6_K, 1>(p, align, grid, s) : gateup_by_align<EPQ_Q6_K, 2>(p, align, grid, s);
@@ -388,6 +393,9 @@ cudaError_t moe_k16_down_launch(epq_fmt fmt, const MoeArgs &a, int max_slots, co
   const unsigned grid = static_cast<unsigned>(
       std::max<int64_t>(1, std::min<int64_t>((groups + p.rg - 1) / p.rg, 2ll * dev.sm_count)));
   const int align = row_align(a.dn_row_bytes, a.dn_stride);
+  if (fmt == EPQ_Q4_K)
+    return a.ntok == 1 ? mk_launch(moe_k16_down_kernel<EPQ_Q4_K, 1, 16>, p, grid, s)
+                       : mk_launch(moe_k16_down_kernel<EPQ_Q4_K, 2, 16>, p, grid, s);
   if (fmt == EPQ_Q2_K)
     return a.ntok == 1 ? down_by_align<EPQ_Q2_K, 1>(p, align, grid, s) : down_by_align<EPQ_Q2_K, 2>(p, align, grid, s);
   return a.ntok == 1 ? down_by_align<EPQ_Q6_K, 1>(p, align, grid, s) : down_by_align<EPQ_Q6_K, 2>(p, align, grid, s);

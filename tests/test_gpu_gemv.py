@@ -161,3 +161,25 @@ def test_gemv_argument_errors(epq_lib, cuda_dev):
         epq_lib.epq_gemv(3, pk, x, 0, 256)                                       # rows < 1
     with pytest.raises(epq_lib.EpqError):
         epq_lib.epq_gemv(3, pk, x, 4, 32768)                                     # cols too large
+
+
+@pytest.fixture
+def engine3(epq_lib):
+    """The block-diagonal tensor-core engine for the Q4_K GEMVs."""
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, 3)
+    yield
+    epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_q4k_block_diagonal_engine_parity(epq_lib, cuda_dev, engine3, shape):
+    test_gemv_parity(epq_lib, cuda_dev, oracle.Q4_K, shape)
+
+
+def test_q4k_block_diagonal_engine_options(epq_lib, cuda_dev, engine3):
+    test_gemv_nvec8_and_scales(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_one_hot_is_exact_column(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_ex_residual_and_prenorm(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_ex_swiglu(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_ex_grouped_heads(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_full_size_layer_sampled(epq_lib, cuda_dev, oracle.Q4_K)

@@ -180,7 +180,7 @@ TC_CASES = [
 ]
 
 
-@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("engine", [0, 1, 3])
 @pytest.mark.parametrize("case", TC_CASES)
 def test_moe_q4k_engines(epq_lib, cuda_dev, case, engine):
     prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, engine)
