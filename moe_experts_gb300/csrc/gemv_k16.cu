@@ -136,34 +136,47 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
   for (int v = 0; v < NV; ++v) ssq[v] = 0.0f;
   float *ps_s = reinterpret_cast<float *>(smem + L.ps);
   float *xsum_s = reinterpret_cast<float *>(smem + L.xsum);
-  for (int u = warp; u < NV * p.nsb; u += kWarps) {
-    const int v = u / p.nsb, b = u % p.nsb;
-    float xv[8];
-    const int j0 = b * 256 + 16 * (lane >> 1) + 8 * (lane & 1);
-    if (v < p.nv) {
-      const float *xr = p.x + v * p.x_stride;
-      if (p.x_group <= 1) {
-        const float4 a = *reinterpret_cast<const float4 *>(xr + j0);
-        const float4 c = *reinterpret_cast<const float4 *>(xr + j0 + 4);
-        xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w, xv[4] = c.x, xv[5] = c.y, xv[6] = c.z, xv[7] = c.w;
+  // a warp stages units warp, warp + 8, ...; the x loads of kStageBatch
+  // units are issued before any of them is converted
+  constexpr int kStageBatch = 4;
+  const int nunits = NV * p.nsb;
+  for (int u0 = warp; u0 < nunits; u0 += kWarps * kStageBatch) {
+    float xv[kStageBatch][8];
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const int u = u0 + kWarps * k;
+      const int v = u / p.nsb, b = u - v * p.nsb;
+      const int j0 = b * 256 + 8 * lane;
+      if (u < nunits && v < p.nv) {
+        // the 8 columns lie in one head (head_dim % 32 == 0), so their
+        // sources are consecutive too: one index, two 16-byte loads
+        const float *xr = p.x + v * p.x_stride + x_src(j0, p.x_group, p.x_head_dim);
+        const float4 a = *reinterpret_cast<const float4 *>(xr);
+        const float4 c = *reinterpret_cast<const float4 *>(xr + 4);
+        xv[k][0] = a.x, xv[k][1] = a.y, xv[k][2] = a.z, xv[k][3] = a.w;
+        xv[k][4] = c.x, xv[k][5] = c.y, xv[k][6] = c.z, xv[k][7] = c.w;
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xv[e] = xr[x_src(j0 + e, p.x_group, p.x_head_dim)];
+        for (int e = 0; e < 8; ++e) xv[k][e] = 0.0f;
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
     }
-    float sq = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sq = fmaf(xv[e], xv[e], sq);
+    for (int k = 0; k < kStageBatch; ++k) {
+      const int u = u0 + kWarps * k;
+      if (u >= nunits) break;  // warp-uniform
+      const int v = u / p.nsb, b = u - v * p.nsb;
+      float sq = 0.0f;
 #pragma unroll
-    for (int w = 0; w < NV; ++w)
-      if (w == v) ssq[w] += sq;
-    uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
-    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, frag_sb, lane, xsum_s + (v * p.nsb + b) * 16)
-                                   : k16::stage_superblock(xv, frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
-    if (lane == 0) ps_s[v * p.nsb + b] = k16::sum_scale<FMT>(ex);
+      for (int e = 0; e < 8; ++e) sq = fmaf(xv[k][e], xv[k][e], sq);
+#pragma unroll
+      for (int w = 0; w < NV; ++w)
+        if (w == v) ssq[w] += sq;
+      uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
+      const int ex = FMT == EPQ_Q4_K
+                         ? k16::stage_superblock_q4k(xv[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16)
+                         : k16::stage_superblock(xv[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
+      if (lane == 0) ps_s[v * p.nsb + b] = k16::sum_scale<FMT>(ex);
+    }
   }
   float *ssq_s = reinterpret_cast<float *>(smem + L.ssq);
 #pragma unroll
