@@ -165,12 +165,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
       const int u = u0 + kWarps * k;
       if (u >= nunits) break;  // warp-uniform
       const int v = u / p.nsb, b = u - v * p.nsb;
-      float sq = 0.0f;
+      if (p.rms) {
+        float sq = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sq = fmaf(xv[k][e], xv[k][e], sq);
+        for (int e = 0; e < 8; ++e) sq = fmaf(xv[k][e], xv[k][e], sq);
 #pragma unroll
-      for (int w = 0; w < NV; ++w)
-        if (w == v) ssq[w] += sq;
+        for (int w = 0; w < NV; ++w)
+          if (w == v) ssq[w] += sq;
+      }
       uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
       const int ex = FMT == EPQ_Q4_K
                          ? k16::stage_superblock_q4k(xv[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16)

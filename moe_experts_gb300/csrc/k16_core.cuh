@@ -388,7 +388,8 @@ __device__ __forceinline__ int stage_superblock(const float (&xv)[8], uint8_t *f
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int sh = (k & 1 ? 10 : 14) - ex;
-    const float xa = scale_pow2(xv[k], sh), xb = scale_pow2(xv[k + 4], sh);
+    const float f = exp2i(sh);  // sh in [-90, 114]: a normal power of two
+    const float xa = xv[k] * f, xb = xv[k + 4] * f;
     const __half2 hh = __floats2half2_rn(xa, xb);
     const float2 hf = __half22float2(hh);
     const __half2 ll = __floats2half2_rn(xa - hf.x, xb - hf.y);
@@ -427,7 +428,8 @@ __device__ __forceinline__ int stage_superblock_q4k(const float (&xv)[8], uint8_
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int sh = (k & 1 ? 10 : 14) - ex;
-    const float xa = scale_pow2(xv[k], sh), xb = scale_pow2(xv[k + 4], sh);
+    const float f = exp2i(sh);  // sh in [-90, 114]: a normal power of two
+    const float xa = xv[k] * f, xb = xv[k + 4] * f;
     const __half2 hh = __floats2half2_rn(xa, xb);
     const float2 hf = __half22float2(hh);
     const __half2 ll = __floats2half2_rn(xa - hf.x, xb - hf.y);
