@@ -111,9 +111,9 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *   EPQ_TUNE_RING_BYTES  shared-memory ring budget per CTA (32768 .. 200704)
  *   EPQ_TUNE_GEMV_ENGINE engine of the Q4_K GEMVs and MoE experts:
  *                        0 automatic (the block-diagonal tensor-core engine
- *                        of the Q2_K / Q6_K GEMV for one or two vectors, the
- *                        ring tensor-core engine for three or more and for
- *                        the MoE expert stages), 1 CUDA-core engines only
+ *                        of the Q2_K / Q6_K GEMV for one vector, the ring
+ *                        tensor-core engine for two or more and for the MoE
+ *                        expert stages), 1 CUDA-core engines only
  *                        (also for the MoE experts), 2 the ring tensor-core
  *                        engine wherever it applies (one vector under 2 MiB:
  *                        CUDA cores), 3 the block-diagonal engine for every

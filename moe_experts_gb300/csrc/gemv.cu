@@ -688,13 +688,14 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   const int64_t rows_out = opts.swiglu ? rows / 2 : rows;
   const bool sw = opts.swiglu != 0;
   const int xs = opts.x_ld ? static_cast<int>(opts.x_ld) : static_cast<int>(cols / xg);
-  // Q2_K / Q6_K, and Q4_K with one or two vectors (or engine 3): the
-  // block-diagonal tensor-core engine (gemv_k16.cu), measured faster than the
-  // ring engine below on every matrix of the 8B-class decode step.  Three or
-  // more Q4_K vectors keep the ring engine's one-pass multi-vector form.
+  // Q2_K / Q6_K, and Q4_K with one vector (or engine 3): the block-diagonal
+  // tensor-core engine (gemv_k16.cu), measured faster than the ring engine
+  // below on every matrix of the 8B-class decode step with one vector
+  // (1.681 -> 1.459 ms per step) and slower with two (1.748 -> 2.046 ms),
+  // where the ring engine's two-vector operands pay.  Two or more Q4_K
+  // vectors keep the ring engine (one pass for up to eight).
   const int eng0 = tune_gemv_engine();
-  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K ||
-      (fmt == EPQ_Q4_K && (eng0 == 3 || (eng0 == 0 && nvec <= 2))))
+  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K || (fmt == EPQ_Q4_K && (eng0 == 3 || (eng0 == 0 && nvec == 1))))
     return gemv_k16_launch(fmt, blocks, x, y, rows, cols, nvec, opts, xs, dev, s);
 
   // Q4_K (three or more vectors, or engine 2): the ring tensor-core engine
