@@ -392,3 +392,43 @@ def test_moe_full_size_decode_layer_k16(epq_lib, cuda_dev, fmt, dfmt):
     assert epq_lib.epq_device_error() == 0
     del gu, dn
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt,dfmt", [(oracle.Q2_K, None), (oracle.Q4_K, oracle.Q6_K)])
+def test_moe_k16_stage_calls_equal_whole_call(epq_lib, cuda_dev, fmt, dfmt):
+    """The router, gate/up and down stages issued by separate calls (one
+    workspace) give the whole call's outputs bit for bit."""
+    E, H, I, topk, ntok = 12, 1024, 512, 3, 2
+    mw = _make(fmt, E, H, I, seed=606, shared=True, down_fmt=dfmt)
+    layer = _to_gpu(epq_lib, mw, cuda_dev)
+    x = torch.from_numpy(synthetic.normal((ntok, H), seed=607).numpy()).to(cuda_dev)
+    ws = torch.empty(layer.workspace_bytes(ntok, topk), dtype=torch.uint8, device=cuda_dev)
+    idx_a = torch.empty((ntok, topk), dtype=torch.int32, device=cuda_dev)
+    y_a, _, _ = epq_lib.epq_moe_forward(layer, x, topk, topk_idx=idx_a, workspace=ws, rms_prenorm=True,
+                                        rms_eps=1e-6)
+    y_b = torch.empty_like(x)
+    idx_b = torch.empty_like(idx_a)
+    for st in (epq_lib.EPQ_MOE_ROUTE, epq_lib.EPQ_MOE_GATE_UP, epq_lib.EPQ_MOE_DOWN):
+        epq_lib.epq_moe_forward(layer, x, topk, y=y_b, topk_idx=idx_b if st == epq_lib.EPQ_MOE_GATE_UP else None,
+                                workspace=ws, rms_prenorm=True, rms_eps=1e-6, stages=st)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_a, idx_b)
+    assert torch.equal(y_a, y_b)
+    assert epq_lib.epq_device_error() == 0
+
+
+def test_moe_k16_argument_errors(epq_lib, cuda_dev):
+    mw = _make(oracle.Q2_K, 8, 512, 256, seed=17, shared=False)
+    layer = _to_gpu(epq_lib, mw, cuda_dev)
+    x = torch.zeros((3, 512), device=cuda_dev)
+    with pytest.raises(epq_lib.EpqError) as e:   # stage calls are not split into token chunks
+        epq_lib.epq_moe_forward(layer, x, 2, stages=epq_lib.EPQ_MOE_GATE_UP)
+    assert e.value.status == 3
+    layer._x.down_fmt_set = 2                       # not 0 or 1
+    with pytest.raises(epq_lib.EpqError) as e:
+        epq_lib.epq_moe_forward(layer, x[:1], 2)
+    assert e.value.status == 1
+    layer._x.down_fmt_set, layer._x.down_fmt = 1, 9  # unknown format
+    with pytest.raises(epq_lib.EpqError) as e:
+        epq_lib.epq_moe_forward(layer, x[:1], 2)
+    assert e.value.status == 2

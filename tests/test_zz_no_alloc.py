@@ -54,6 +54,8 @@ CASES = [
     (oracle.Q4_K, 16, 1024, 512, 4, 3, 1),    # the same on the CUDA-core kernels, one pass
     (oracle.Q4_0, 16, 1024, 512, 4, 3, 0),    # another format: CUDA-core kernels
     (oracle.Q4_0, 32, 1024, 1792, 8, 16, 0),  # workspace 1,046,784 B: all but 1.8 KB of the array
+    (oracle.Q2_K, 16, 1024, 512, 4, 3, 0),    # 2-bit experts: the 16-weight sub-block kernels, chunks of two
+    (oracle.Q6_K, 12, 1280, 768, 3, 2, 0),    # Q6_K rows of an odd number of superblocks
 ]
 
 
