@@ -112,6 +112,28 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
   route_tokens(a, m, reinterpret_cast<uint32_t *>(smem + p.frag_off), blockIdx.x == 0);
   __syncthreads();  // the routing scratch becomes the operand records
 
+  const int nact = *m.nact, nslots = *m.nslots;
+  const int gps = I / 8;  // row groups (8 outputs) per slot
+  const int total = nslots * gps;
+  // a row group's rows and its first superblock's loads (issued for the
+  // first group before x is converted, so that they overlap)
+  k16::RowOps<FMT> cl, ch, nl, nh;
+  const uint8_t *row_lo = nullptr, *row_hi = nullptr;
+  bool work = false;
+  auto start = [&](int b0) {
+    const int vg = b0 + rgl;
+    work = vg < total && kq < nsb;
+    if (!work) return;
+    const int s = vg / gps, i = (vg - s * gps) * 8 + g;
+    const int e = s < nact ? m.active[s] : -1;
+    const uint8_t *Wm = e >= 0 ? a.gate_up + static_cast<int64_t>(e) * a.gu_stride : a.sh_gate_up;
+    row_lo = Wm + static_cast<int64_t>(i) * a.gu_row_bytes;
+    row_hi = Wm + static_cast<int64_t>(I + i) * a.gu_row_bytes;
+    k16::load_ops<FMT, ALIGN>(cl, row_lo, nsb, kq, t);
+    k16::load_ops<FMT, ALIGN>(ch, row_hi, nsb, kq, t);
+  };
+  start(blockIdx.x * p.rg);
+
   // x of the tokens (vector v = token v) into operand records
   float *ps_s = reinterpret_cast<float *>(smem + p.ps_off);
   float *xsum_s = reinterpret_cast<float *>(smem + p.xsum_off);
@@ -119,7 +141,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
     const int v = u / nsb, b = u - v * nsb;
     float xv[8];
     if (v < a.ntok) {
-      const float *xr = a.x + static_cast<int64_t>(v) * a.H + b * 256 + 16 * (lane >> 1) + 8 * (lane & 1);
+      const float *xr = a.x + static_cast<int64_t>(v) * a.H + b * 256 + 8 * lane;
       const float4 x0 = *reinterpret_cast<const float4 *>(xr), x1 = *reinterpret_cast<const float4 *>(xr + 4);
       xv[0] = x0.x, xv[1] = x0.y, xv[2] = x0.z, xv[3] = x0.w, xv[4] = x1.x, xv[5] = x1.y, xv[6] = x1.z, xv[7] = x1.w;
     } else {
@@ -133,28 +155,17 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
   }
   __syncthreads();
 
-  const int nact = *m.nact, nslots = *m.nslots;
-  const int gps = I / 8;  // row groups (8 outputs) per slot
-  const int total = nslots * gps;
   const uint32_t frag0 = smem_addr(smem + p.frag_off) + k16::lane_slot(lane);
   const uint32_t vstride = static_cast<uint32_t>(nsb) * k16::kSbFragBytes;
   float *red = reinterpret_cast<float *>(smem + p.red_off);
 #pragma unroll 1
   for (int base = blockIdx.x * p.rg; base < total; base += gridDim.x * p.rg) {
-    const int vg = base + rgl;
+    if (base != static_cast<int>(blockIdx.x) * p.rg) start(base);
     float acc[2][NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) acc[0][v] = acc[1][v] = 0.0f;
-    if (vg < total && kq < nsb) {
-      const int s = vg / gps, i = (vg - s * gps) * 8 + g;
-      const int e = s < nact ? m.active[s] : -1;
-      const uint8_t *Wm = e >= 0 ? a.gate_up + static_cast<int64_t>(e) * a.gu_stride : a.sh_gate_up;
-      const uint8_t *row_lo = Wm + static_cast<int64_t>(i) * a.gu_row_bytes;
-      const uint8_t *row_hi = Wm + static_cast<int64_t>(I + i) * a.gu_row_bytes;
-      k16::RowOps<FMT> cl, ch, nl, nh;
+    if (work) {
       int sb = kq;
-      k16::load_ops<FMT, ALIGN>(cl, row_lo, nsb, sb, t);
-      k16::load_ops<FMT, ALIGN>(ch, row_hi, nsb, sb, t);
       for (;;) {
         const int nx = sb + p.kp;
         if (nx < nsb) {
@@ -214,55 +225,80 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
   __syncthreads();
   const int nact = *m.nact, nslots = *m.nslots;
   const int nvsb = nslots * nsbI;  // <= p.nsbx
-
-  // x operand of token v: coef * h over the slots, zero where v is absent
-  float *ps_s = reinterpret_cast<float *>(smem + p.ps_off);
-  float *xsum_s = reinterpret_cast<float *>(smem + p.xsum_off);
-  for (int u = warp; u < NV * nvsb; u += kKWarps) {
-    const int v = u / nvsb, b = u - v * nvsb;
-    const int s = b / nsbI, lsb = b - s * nsbI;
-    float xv[8];
-    const int k = v < a.ntok ? entry_of(m, a.ntok, s, v) : -1;
-    if (k >= 0) {
-      const float coef = k == a.topk ? m.gs[v] : m.w[v * a.topk + k];
-      const float *hr = a.h + static_cast<int64_t>(v * (a.topk + 1) + k) * I + lsb * 256 + 16 * (lane >> 1) +
-                        8 * (lane & 1);
-      const float4 h0 = __ldcg(reinterpret_cast<const float4 *>(hr)), h1 = __ldcg(reinterpret_cast<const float4 *>(hr + 4));
-      xv[0] = coef * h0.x, xv[1] = coef * h0.y, xv[2] = coef * h0.z, xv[3] = coef * h0.w;
-      xv[4] = coef * h1.x, xv[5] = coef * h1.y, xv[6] = coef * h1.z, xv[7] = coef * h1.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
-    }
-    uint8_t *fr = smem + p.frag_off + static_cast<uint32_t>(v * p.nsbx + b) * k16::kSbFragBytes;
-    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, fr, lane, xsum_s + (v * p.nsbx + b) * 16)
-                                   : k16::stage_superblock(xv, fr, lane, xsum_s + (v * p.nsbx + b) * 16);
-    if (lane == 0) ps_s[v * p.nsbx + b] = k16::sum_scale<FMT>(ex);
-  }
-  __syncthreads();
-
   const int total = (H + 15) / 16;
-  const uint32_t frag0 = smem_addr(smem + p.frag_off) + k16::lane_slot(lane);
-  const uint32_t vstride = static_cast<uint32_t>(p.nsbx) * k16::kSbFragBytes;
-  float *red = reinterpret_cast<float *>(smem + p.red_off);
   auto row_base = [&](int s) -> const uint8_t * {
     const int e = s < nact ? m.active[s] : -1;
     return e >= 0 ? a.down + static_cast<int64_t>(e) * a.dn_stride : a.sh_down;
   };
+  // a row group's rows and its first superblock's loads (issued for the
+  // first group before h is staged, so that they overlap)
+  k16::RowOps<FMT> cl, ch, nl, nh;
+  int64_t r_lo = 0, r_hi = 0;
+  bool work = false;
+  auto start = [&](int b0) {
+    const int vg = b0 + rgl;
+    work = vg < total && kq < nvsb;
+    if (!work) return;
+    r_lo = min(vg * 16 + g, H - 1);
+    r_hi = min(vg * 16 + g + 8, H - 1);
+    const int s0 = kq / nsbI;
+    const uint8_t *Wm = row_base(s0);
+    k16::load_ops<FMT, ALIGN>(cl, Wm + r_lo * a.dn_row_bytes, nsbI, kq - s0 * nsbI, t);
+    k16::load_ops<FMT, ALIGN>(ch, Wm + r_hi * a.dn_row_bytes, nsbI, kq - s0 * nsbI, t);
+  };
+  start(blockIdx.x * p.rg);
+
+  // x operand of token v: coef * h over the slots, zero where v is absent;
+  // the h loads of kBatch units are issued before any is converted
+  float *ps_s = reinterpret_cast<float *>(smem + p.ps_off);
+  float *xsum_s = reinterpret_cast<float *>(smem + p.xsum_off);
+  constexpr int kBatch = 3;
+  const int nunits = NV * nvsb;
+  for (int u0 = warp; u0 < nunits; u0 += kKWarps * kBatch) {
+    float xv[kBatch][8];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int u = u0 + kKWarps * j;
+      const int v = u / nvsb, b = u - v * nvsb;
+      const int s = b / nsbI, lsb = b - s * nsbI;
+      const int k = u < nunits && v < a.ntok ? entry_of(m, a.ntok, s, v) : -1;
+      if (k >= 0) {
+        const float coef = k == a.topk ? m.gs[v] : m.w[v * a.topk + k];
+        const float *hr = a.h + static_cast<int64_t>(v * (a.topk + 1) + k) * I + lsb * 256 + 8 * lane;
+        const float4 h0 = __ldcg(reinterpret_cast<const float4 *>(hr));
+        const float4 h1 = __ldcg(reinterpret_cast<const float4 *>(hr + 4));
+        xv[j][0] = coef * h0.x, xv[j][1] = coef * h0.y, xv[j][2] = coef * h0.z, xv[j][3] = coef * h0.w;
+        xv[j][4] = coef * h1.x, xv[j][5] = coef * h1.y, xv[j][6] = coef * h1.z, xv[j][7] = coef * h1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[j][e] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int u = u0 + kKWarps * j;
+      if (u >= nunits) break;  // warp-uniform
+      const int v = u / nvsb, b = u - v * nvsb;
+      uint8_t *fr = smem + p.frag_off + static_cast<uint32_t>(v * p.nsbx + b) * k16::kSbFragBytes;
+      const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv[j], fr, lane, xsum_s + (v * p.nsbx + b) * 16)
+                                     : k16::stage_superblock(xv[j], fr, lane, xsum_s + (v * p.nsbx + b) * 16);
+      if (lane == 0) ps_s[v * p.nsbx + b] = k16::sum_scale<FMT>(ex);
+    }
+  }
+  __syncthreads();
+
+  const uint32_t frag0 = smem_addr(smem + p.frag_off) + k16::lane_slot(lane);
+  const uint32_t vstride = static_cast<uint32_t>(p.nsbx) * k16::kSbFragBytes;
+  float *red = reinterpret_cast<float *>(smem + p.red_off);
 #pragma unroll 1
   for (int base = blockIdx.x * p.rg; base < total; base += gridDim.x * p.rg) {
-    const int vg = base + rgl;
+    if (base != static_cast<int>(blockIdx.x) * p.rg) start(base);
     float acc[2][NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) acc[0][v] = acc[1][v] = 0.0f;
-    if (vg < total && kq < nvsb) {
-      const int64_t r_lo = min(vg * 16 + g, H - 1), r_hi = min(vg * 16 + g + 8, H - 1);
+    if (work) {
       int sb = kq;
       int s = sb / nsbI, lsb = sb - s * nsbI;
-      const uint8_t *Wm = row_base(s);
-      k16::RowOps<FMT> cl, ch, nl, nh;
-      k16::load_ops<FMT, ALIGN>(cl, Wm + r_lo * a.dn_row_bytes, nsbI, lsb, t);
-      k16::load_ops<FMT, ALIGN>(ch, Wm + r_hi * a.dn_row_bytes, nsbI, lsb, t);
       for (;;) {
         const int nx = sb + p.kp;
         int ns = s, nlsb = lsb + p.kp;
