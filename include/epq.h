@@ -124,10 +124,15 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *   EPQ_TUNE_TC_SPLIT    warps that share one 8-row block of the tensor-core
  *                        GEMV (1, 2, 4, 8 or 16; 0 = chosen by shape, the
  *                        default: 8 for rows of 8..32 superblocks)
+ *   EPQ_TUNE_ATTN_CHUNK  most cached key (value) rows epq_attention_decode
+ *                        copies into shared memory at a time: 0 = as many
+ *                        as fit (the default), else 8 .. 4096, a multiple
+ *                        of 8 (smaller chunks: more copy round trips, the
+ *                        same result)
  * Returns the previous value, or -1 for an unknown key or a value out of
  * range (nothing changes then).  Affects launches issued afterwards. */
 enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2, EPQ_TUNE_GEMV_ENGINE = 3, EPQ_TUNE_EARLY_STAGES = 4,
-       EPQ_TUNE_TC_SPLIT = 5 };
+       EPQ_TUNE_TC_SPLIT = 5, EPQ_TUNE_ATTN_CHUNK = 6 };
 int epq_set_tuning(int key, int value);
 
 /* ---------------------------------------------------------------- packing

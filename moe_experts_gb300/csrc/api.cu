@@ -69,6 +69,7 @@ std::atomic<int> g_ring_bytes{180 * 1024};
 std::atomic<int> g_gemv_engine{0};
 std::atomic<int> g_early_stages{4};
 std::atomic<int> g_tc_split{0};
+std::atomic<int> g_attn_chunk{0};
 }  // namespace
 
 int tune_tile_bytes() { return g_tile_bytes.load(std::memory_order_relaxed); }
@@ -76,6 +77,7 @@ int tune_ring_bytes() { return g_ring_bytes.load(std::memory_order_relaxed); }
 int tune_gemv_engine() { return g_gemv_engine.load(std::memory_order_relaxed); }
 int tune_early_stages() { return g_early_stages.load(std::memory_order_relaxed); }
 int tune_tc_split() { return g_tc_split.load(std::memory_order_relaxed); }
+int tune_attn_chunk() { return g_attn_chunk.load(std::memory_order_relaxed); }
 
 epq_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -119,6 +121,9 @@ int epq_set_tuning(int key, int value) {
     case EPQ_TUNE_TC_SPLIT:
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8 && value != 16) return -1;
       return epq::g_tc_split.exchange(value);
+    case EPQ_TUNE_ATTN_CHUNK:
+      if (value != 0 && (value < 8 || value > 4096 || value % 8)) return -1;
+      return epq::g_attn_chunk.exchange(value);
   }
   return -1;
 }

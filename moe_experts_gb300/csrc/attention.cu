@@ -15,33 +15,43 @@
 //
 // Organisation: one thread-block cluster of C CTAs per key/value head (the
 // positions split evenly over the C CTAs).
-//   phase 0  the CTA whose positions include `pos` quantizes the step's key
-//            and value rows into the cache and keeps a shared-memory copy for
-//            its own scan (no other CTA reads them in this step);
-//   phase 1  each warp takes runs of 8 consecutive positions (all 8 rows
-//            loaded before any is reduced): lane l holds 4 consecutive
-//            elements of a key row (one 32-bit load of codes plus its
-//            block's fp16 factor) and multiplies them with the `group`
-//            query heads kept in shared memory; the warp sums the products;
-//            scores stay in shared memory (and optionally go to scores_out);
-//            each CTA writes its per-head maximum into every cluster CTA's
-//            shared memory (distributed shared memory), one cluster barrier;
+//   entry    before the grid-dependency wait the CTA asks L2 for its cached
+//            key and value rows (written by earlier steps; a prefetch hint
+//            only); after it, every thread issues asynchronous 8-byte copies
+//            of those rows into shared memory (keys and values as two copy
+//            groups, in chunks when the rows do not fit), so that one round
+//            trip brings every row the CTA reads;
+//   phase 0  the query elements a lane uses go straight into registers; the
+//            CTA whose positions include `pos` quantizes the step's key and
+//            value rows into the cache and keeps a shared-memory copy for its
+//            own scan (no other CTA reads them in this step);
+//   phase 1  each warp takes runs of 8 consecutive positions: lane l holds 4
+//            consecutive elements of a key row (one 32-bit word of codes plus
+//            its block's fp16 factor, from shared memory) and multiplies them
+//            with the `group` query heads; one reduce-scatter gives the run's
+//            dot products; scores stay in shared memory (and optionally go to
+//            scores_out); each CTA writes its per-head maximum into every
+//            cluster CTA's shared memory (distributed shared memory), one
+//            cluster barrier;
 //   phase 2  each CTA forms the weights of its positions against the
 //            cluster-wide maximum, skips the positions below the threshold
-//            (for every query head of the group), accumulates the weighted
-//            value rows and the weight sums, reduces over its warps and
-//            writes the partial into cluster rank 0's shared memory; after a
-//            cluster barrier rank 0 adds the C partials in rank order and
-//            writes out = sum w v / sum w.
+//            (for every query head of the group: no exponential, no value
+//            arithmetic), accumulates the weighted value rows and the weight
+//            sums, reduces over its warps and writes the partial into cluster
+//            rank 0's shared memory; after a cluster barrier rank 0 adds the C
+//            partials in rank order and writes out = sum w v / sum w.
+// The value rows of skipped positions are copied with the others: the copy
+// is one round trip either way, and the page's saving is the arithmetic.
 // Every sum runs in a fixed order, so the result is bitwise reproducible.
-// There is no pipeline wait in this kernel (plain loads, cluster barriers
-// that every thread reaches).
+// There is no spin wait in this kernel (asynchronous copies waited with
+// cp.async.wait_group, cluster barriers that every thread reaches).
 //
 // Cache row layout (this library's own byte order; the values are Q8_0
 // blocks of 32 elements, fp16 factor d and int8 codes q, element = d * q):
 // position p of key/value head h is the D + D/16 byte row at
 // (h * max_pos + p) * (D + D/16): the D/32 fp16 factors first, then the D
 // int8 codes, so that a lane's 4 codes are one aligned 32-bit word.
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -54,7 +64,7 @@ constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxGroup = 8;       // query heads per key/value head
 constexpr int kMaxCluster = 8;
 constexpr int kMaxPosPerCta = 2048;
-constexpr int kRunMax = 8;         // positions per warp step (rows in flight per warp)
+constexpr int kRunMax = 8;         // positions per warp step
 
 struct AttnParams {
   const float *q;               // [n_heads][D]
@@ -63,8 +73,37 @@ struct AttnParams {
   float *out;                   // [n_heads][D]
   float *scores;                // NULL or [n_heads][max_pos]
   int n_kv, D, group, pos, max_pos, C;
+  int nsp;    // score stride per query head (>= positions of a CTA)
+  int chunk;  // rows of one shared-memory copy chunk
   float scale, skip_log;
 };
+
+__host__ __device__ inline uint32_t al16b(uint32_t v) { return (v + 15u) & ~15u; }
+
+// Shared-memory plan of one CTA (byte offsets, 16-byte aligned).
+struct AttnSmem {
+  uint32_t sc, cmax, red, part, newrow, stage, total;
+};
+
+__host__ __device__ inline AttnSmem attn_smem(int G, int D, int C, int nsp, int chunk) {
+  AttnSmem L;
+  const uint32_t rb = static_cast<uint32_t>(D + D / 16);
+  uint32_t o = 0;
+  L.sc = o;  // [G][nsp] scores, then weights
+  o = al16b(o + 4u * G * nsp);
+  L.cmax = o;  // [kMaxCluster][G] maxima from every cluster CTA
+  o = al16b(o + 4u * kMaxCluster * G);
+  L.red = o;  // [warp][G][D + 1] warp partials (warp maxima first)
+  o = al16b(o + 4u * kAttnWarps * G * (D + 1));
+  L.part = o;  // [C][G][D + 1] partials of every CTA (rank 0 only)
+  o = al16b(o + 4u * C * G * (D + 1));
+  L.newrow = o;  // [2][row] the step's key and value rows
+  o = al16b(o + 2u * rb);
+  L.stage = o;  // [2][chunk][row] copied key rows, value rows
+  o = al16b(o + 2u * static_cast<uint32_t>(chunk) * rb);
+  L.total = o;
+  return L;
+}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -83,12 +122,6 @@ __device__ __forceinline__ void st_cluster(const float *local, uint32_t rank, fl
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // Q8_0 of one 32-element run held one element per lane (the packer's
 // arithmetic: factor fp16(max|x| / 127), codes rint(x / factor) clamped to
 // +-127, zero codes for a zero factor).
@@ -103,6 +136,19 @@ __device__ __forceinline__ void q8_block_lane(float x, uint16_t *d_out, int8_t *
   if (d != 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(x, d)), -127.0f), 127.0f);
   *q_out = static_cast<int8_t>(q);
   if ((threadIdx.x & 31) == 0) *d_out = __half_as_ushort(dh);
+}
+
+// 8-byte asynchronous copy global -> shared (L1-allocating form), and the
+// per-thread copy groups.
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)),
+               "l"(static_cast<uint64_t>(__cvta_generic_to_global(src)))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Sum over the warp of N values per lane (N a power of two <= 32): a
@@ -144,7 +190,7 @@ template <int G>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
   // kRun positions per warp step, so that a step's kRun x G dot products fit one reduce-scatter
   constexpr int kRun = kRunMax * G <= 32 ? kRunMax : 32 / G;
-  extern __shared__ __align__(16) float sm[];
+  extern __shared__ __align__(16) uint8_t smem[];
   const int D = p.D;
   const int C = p.C;
   const uint32_t rank = cluster_rank();
@@ -152,29 +198,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row_bytes = D + D / 16;
   const int nblk = D / 32;
-  // positions of this CTA
+  // positions of this CTA; those below `pos` come from the cache
   const int npos = p.pos + 1;
   const int p0 = static_cast<int>((static_cast<int64_t>(rank) * npos) / C);
   const int p1 = static_cast<int>((static_cast<int64_t>(rank + 1) * npos) / C);
   const int n = p1 - p0;
+  const int ncached = min(p1, p.pos) - p0;
+  const int chunk = p.chunk;
+  const int nsp = p.nsp;
 
-  float *qs = sm;                                  // [G][D]
-  float *sc = qs + G * D;                          // [G][kMaxPosPerCta]
-  float *cmax = sc + G * kMaxPosPerCta;            // [C][G] maxima from every cluster CTA
-  float *red = cmax + kMaxCluster * G;             // [warp][G][D + 1]: warp partials
-  float *part = red + kAttnWarps * G * (D + 1);    // [C][G][D + 1]: rank 0 only
-  uint8_t *newrow = reinterpret_cast<uint8_t *>(part + C * G * (D + 1));  // [2][row_bytes]: the step's key, value
+  const AttnSmem L = attn_smem(G, D, C, nsp, chunk);
+  float *sc = reinterpret_cast<float *>(smem + L.sc);
+  float *cmax = reinterpret_cast<float *>(smem + L.cmax);
+  float *red = reinterpret_cast<float *>(smem + L.red);
+  float *part = reinterpret_cast<float *>(smem + L.part);
+  uint8_t *newrow = smem + L.newrow;
+  uint8_t *stk = smem + L.stage;                // [chunk][row] key rows
+  uint8_t *stv = stk + chunk * row_bytes;       // [chunk][row] value rows
+  const int64_t head_row0 = static_cast<int64_t>(h) * p.max_pos + p0;
+  const uint8_t *kc = p.k_cache + head_row0 * row_bytes;
+  const uint8_t *vc = p.v_cache + head_row0 * row_bytes;
 
+  // L2 hint for the cached rows (a prefetch cannot expose stale data: the
+  // rows are read only after the grid-dependency wait)
+  {
+    const int lines = (ncached * row_bytes + 127) / 128;
+    for (int i = tid; i < 2 * lines; i += kAttnThreads) {
+      const uint8_t *a = (i < lines ? kc : vc) + 128 * static_cast<int64_t>(i < lines ? i : i - lines);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<uint64_t>(__cvta_generic_to_global(a))));
+    }
+  }
   pdl_launch_dependents();
   pdl_wait();  // q, k_new and v_new come from the preceding projection
+
+  // rows [c0, c0 + cn) of this CTA's positions -> dst, 8-byte copies (rows
+  // are 8-byte multiples; the step's own position is never copied)
+  auto stage_rows = [&](const uint8_t *src_rows, uint8_t *dst, int c0, int cn) {
+    const int pieces = max(0, min(cn, ncached - c0)) * row_bytes / 8;
+    const uint8_t *src = src_rows + static_cast<int64_t>(c0) * row_bytes;
+    for (int i = tid; i < pieces; i += kAttnThreads) cp_async8(dst + 8 * i, src + 8 * i);
+  };
+  const bool one_chunk = n <= chunk;
+  stage_rows(kc, stk, 0, chunk);
+  cp_async_commit();
+  if (one_chunk) stage_rows(vc, stv, 0, chunk);
+  cp_async_commit();
 
   // ---------------------------------------------------------------- phase 0
   // Arrive on the cluster barrier now and wait on it only before the first
   // store into another CTA's shared memory: every CTA of the cluster has
-  // then started.  The CTA whose range holds position `pos` quantizes the
-  // step's key and value rows, stores them into the cache (no other CTA
-  // reads them in this step) and keeps a shared-memory copy for its scan.
+  // then started.  The lane's query elements go into registers for the whole
+  // scan.  The CTA whose range holds position `pos` quantizes the step's key
+  // and value rows, stores them into the cache and keeps a shared-memory
+  // copy for its scan.
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const int nch = D / 128;
+  float4 qr[G][2];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      qr[g][c] = c < nch ? *reinterpret_cast<const float4 *>(p.q + (h * G + g) * D + 128 * c + 4 * lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
   const bool owner = p0 <= p.pos && p.pos < p1;
   if (owner) {
     uint8_t *krow_new = p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p.pos) * row_bytes;
@@ -196,78 +281,77 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       }
     }
   }
-  for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = p.q[(h * G + i / D) * D + i % D];
+  cp_async_wait<1>();  // this thread's key copies (the value group may still be in flight)
   __syncthreads();
 
-  // the lane's query elements stay in registers for the whole scan
-  float4 qr[G][2];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-      qr[g][c] = c < D / 128 ? *reinterpret_cast<const float4 *>(qs + g * D + 128 * c + 4 * lane)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-
   // ---------------------------------------------------------------- phase 1
-  // Warp w takes runs of kRun consecutive positions (w*kRun + 8*kRun*j ...);
-  // all rows of a run are loaded before any is reduced, so kRun row loads are
-  // in flight per warp.  Lane l: elements 4l..4l+3 of each 128-element chunk.
-  const int nch = D / 128;
+  // Warp w takes runs of kRun consecutive positions (w*kRun + 8*kRun*j ...)
+  // of each chunk.  Lane l: elements 4l..4l+3 of each 128-element chunk.
   float wmax[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) wmax[g] = -INFINITY;
-  for (int i0 = warp * kRun; i0 < n; i0 += kAttnWarps * kRun) {
-    uint32_t wk[kRun][2];
-    float dk[kRun][2];
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) {
-      const int i = min(i0 + u, n - 1);  // past the end: a repeat of the last row, not used
-      const uint8_t *row = p0 + i == p.pos ? newrow
-                                           : p.k_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i) * row_bytes;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        if (c >= nch) break;
-        const int e0 = 128 * c + 4 * lane;
-        wk[u][c] = *reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0);
-        dk[u][c] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32))));
-      }
+#pragma unroll 1
+  for (int c0 = 0; c0 < n; c0 += chunk) {
+    const int cend = min(n, c0 + chunk);
+    if (c0 > 0) {  // a later chunk (long contexts): the previous one is no longer read
+      __syncthreads();
+      stage_rows(kc, stk, c0, chunk);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
     }
-    // partial dots of the run's kRun x G (position, head) pairs, then one
-    // reduce-scatter over the warp: lane l ends with the full sum of pair
-    // l % (kRun G) (index u G + g), instead of one butterfly per pair
-    float acc[kRun * G];
+#pragma unroll 1
+    for (int i0 = c0 + warp * kRun; i0 < cend; i0 += kAttnWarps * kRun) {
+      uint32_t wk[kRun][2];
+      float dk[kRun][2];
 #pragma unroll
-    for (int u = 0; u < kRun; ++u) {
+      for (int u = 0; u < kRun; ++u) {
+        const int i = min(i0 + u, cend - 1);  // past the end: a repeat of the last row, not used
+        const uint8_t *row = p0 + i == p.pos ? newrow : stk + (i - c0) * row_bytes;
 #pragma unroll
-      for (int g = 0; g < G; ++g) acc[u * G + g] = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        if (c >= nch) break;
-        // the lane's 4 elements share one Q8_0 block: the factor d multiplies their sum
-        const uint32_t w = wk[u][c] ^ 0x80808080u;
-        const float k0 = i8(w, 0), k1 = i8(w, 1), k2 = i8(w, 2), k3 = i8(w, 3);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qv = qr[g][c];
-          acc[u * G + g] = fmaf(dk[u][c], fmaf(k0, qv.x, fmaf(k1, qv.y, fmaf(k2, qv.z, k3 * qv.w))), acc[u * G + g]);
+        for (int c = 0; c < 2; ++c) {
+          if (c >= nch) break;
+          const int e0 = 128 * c + 4 * lane;
+          wk[u][c] = *reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0);
+          dk[u][c] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32))));
         }
       }
-    }
-    const float sum = reduce_scatter<kRun * G>(acc, lane);
-    constexpr int kPairs = kRun * G;
-    constexpr int kCopies = 32 / kPairs;  // lanes holding the same pair
-    const int pr = lane / kCopies;        // pair held by this lane
-    const int u = pr / G, g = pr % G;
-    const float sv = sum * p.scale;
-    if (i0 + u < n) {
-      if (lane % kCopies == 0) sc[g * kMaxPosPerCta + i0 + u] = sv;
+      // partial dots of the run's kRun x G (position, head) pairs, then one
+      // reduce-scatter over the warp: lane l ends with the full sum of pair
+      // l / (32 / (kRun G)) (index u G + g), instead of one butterfly per pair
+      float acc[kRun * G];
 #pragma unroll
-      for (int gg = 0; gg < G; ++gg)
-        if (gg == g) wmax[gg] = fmaxf(wmax[gg], sv);  // constant indices keep wmax in registers
+      for (int u = 0; u < kRun; ++u) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[u * G + g] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c >= nch) break;
+          // the lane's 4 elements share one Q8_0 block: the factor d multiplies their sum
+          const uint32_t w = wk[u][c] ^ 0x80808080u;
+          const float k0 = i8(w, 0), k1 = i8(w, 1), k2 = i8(w, 2), k3 = i8(w, 3);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float4 qv = qr[g][c];
+            acc[u * G + g] = fmaf(dk[u][c], fmaf(k0, qv.x, fmaf(k1, qv.y, fmaf(k2, qv.z, k3 * qv.w))), acc[u * G + g]);
+          }
+        }
+      }
+      const float sum = reduce_scatter<kRun * G>(acc, lane);
+      constexpr int kPairs = kRun * G;
+      constexpr int kCopies = 32 / kPairs;  // lanes holding the same pair
+      const int pr = lane / kCopies;        // pair held by this lane
+      const int u = pr / G, g = pr % G;
+      const float sv = sum * p.scale;
+      if (i0 + u < cend) {
+        if (lane % kCopies == 0) sc[g * nsp + i0 + u] = sv;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg)
+          if (gg == g) wmax[gg] = fmaxf(wmax[gg], sv);  // constant indices keep wmax in registers
+      }
     }
   }
   // CTA maxima -> every cluster CTA's cmax[rank][g]
-  __syncthreads();
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float m = wmax[g];
@@ -285,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   if (p.scores) {
     for (int idx = tid; idx < G * n; idx += kAttnThreads) {
       const int g = idx / n, i = idx % n;
-      p.scores[static_cast<int64_t>(h * G + g) * p.max_pos + p0 + i] = sc[g * kMaxPosPerCta + i];
+      p.scores[static_cast<int64_t>(h * G + g) * p.max_pos + p0 + i] = sc[g * nsp + i];
     }
   }
   cluster_sync();
@@ -297,9 +381,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     const int g = idx / n, i = idx - g * n;
     float m = -INFINITY;  // the cluster maximum of head g (from shared memory: g is not a constant here)
     for (int r = 0; r < C; ++r) m = fmaxf(m, cmax[r * G + g]);
-    const float sv = sc[g * kMaxPosPerCta + i];
-    sc[g * kMaxPosPerCta + i] = sv >= m + p.skip_log ? expf(sv - m) : 0.0f;
+    const float sv = sc[g * nsp + i];
+    sc[g * nsp + i] = sv >= m + p.skip_log ? expf(sv - m) : 0.0f;
   }
+  if (one_chunk) cp_async_wait<0>();  // this thread's value copies
   __syncthreads();
   float o[G][4 * 2];  // up to D = 256: two 128-element chunks of 4 per lane
   float ws[G];
@@ -309,55 +394,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[g][j] = 0.0f;
   }
-  // the same runs of positions; the value rows of a run that some query head
-  // keeps are all loaded before they are accumulated (in position order)
-  for (int i0 = warp * kRun; i0 < n; i0 += kAttnWarps * kRun) {
-    float w[kRun][G];
-    bool need[kRun];
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) {
-      need[u] = false;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        w[u][g] = i0 + u < n ? sc[g * kMaxPosPerCta + i0 + u] : 0.0f;
-        need[u] = need[u] || w[u][g] != 0.0f;
-      }
+  // the same runs of positions; a position that no query head keeps costs
+  // no value arithmetic
+#pragma unroll 1
+  for (int c0 = 0; c0 < n; c0 += chunk) {
+    const int cend = min(n, c0 + chunk);
+    if (!one_chunk) {
+      __syncthreads();
+      stage_rows(vc, stv, c0, chunk);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
     }
-    uint32_t wv[kRun][2];
-    float dv[kRun][2];
+#pragma unroll 1
+    for (int i0 = c0 + warp * kRun; i0 < cend; i0 += kAttnWarps * kRun) {
+      float w[kRun][G];
+      bool need[kRun];
 #pragma unroll
-    for (int u = 0; u < kRun; ++u) {
-      if (!need[u]) continue;  // warp-uniform: every lane read the same weights
-      const uint8_t *row = p0 + i0 + u == p.pos
-                               ? newrow + row_bytes
-                               : p.v_cache + (static_cast<int64_t>(h) * p.max_pos + p0 + i0 + u) * row_bytes;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        if (c >= nch) break;
-        const int e0 = 128 * c + 4 * lane;
-        wv[u][c] = *reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0);
-        dv[u][c] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32))));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) {
-      if (!need[u]) continue;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        if (c >= nch) break;
-        const uint32_t wq = wv[u][c] ^ 0x80808080u;
-        const float v0 = i8(wq, 0), v1 = i8(wq, 1), v2 = i8(wq, 2), v3 = i8(wq, 3);
+      for (int u = 0; u < kRun; ++u) {
+        need[u] = false;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float wd = w[u][g] * dv[u][c];  // weight times the block factor of the lane's elements
-          o[g][4 * c + 0] = fmaf(wd, v0, o[g][4 * c + 0]);
-          o[g][4 * c + 1] = fmaf(wd, v1, o[g][4 * c + 1]);
-          o[g][4 * c + 2] = fmaf(wd, v2, o[g][4 * c + 2]);
-          o[g][4 * c + 3] = fmaf(wd, v3, o[g][4 * c + 3]);
+          w[u][g] = i0 + u < cend ? sc[g * nsp + i0 + u] : 0.0f;
+          need[u] = need[u] || w[u][g] != 0.0f;
         }
       }
 #pragma unroll
-      for (int g = 0; g < G; ++g) ws[g] += w[u][g];
+      for (int u = 0; u < kRun; ++u) {
+        if (!need[u]) continue;  // warp-uniform: every lane read the same weights
+        const uint8_t *row = p0 + i0 + u == p.pos ? newrow + row_bytes : stv + (i0 + u - c0) * row_bytes;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c >= nch) break;
+          const int e0 = 128 * c + 4 * lane;
+          const uint32_t wq = *reinterpret_cast<const unsigned int *>(row + 2 * nblk + e0) ^ 0x80808080u;
+          const float dv = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(row + 2 * (e0 / 32))));
+          const float v0 = i8(wq, 0), v1 = i8(wq, 1), v2 = i8(wq, 2), v3 = i8(wq, 3);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float wd = w[u][g] * dv;  // weight times the block factor of the lane's elements
+            o[g][4 * c + 0] = fmaf(wd, v0, o[g][4 * c + 0]);
+            o[g][4 * c + 1] = fmaf(wd, v1, o[g][4 * c + 1]);
+            o[g][4 * c + 2] = fmaf(wd, v2, o[g][4 * c + 2]);
+            o[g][4 * c + 3] = fmaf(wd, v3, o[g][4 * c + 3]);
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) ws[g] += w[u][g];
+      }
     }
   }
   // warp partials -> shared memory, then the CTA sum (warp order) -> rank 0
@@ -393,16 +477,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   }
 }
 
-size_t attn_smem(int G, int D, int C) {
-  return sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * kMaxPosPerCta + kMaxCluster * G +
-                          static_cast<size_t>(kAttnWarps) * G * (D + 1) + static_cast<size_t>(C) * G * (D + 1)) +
-         2 * static_cast<size_t>(D + D / 16);
-}
-
 template <int G>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t s) {
   auto k = attn_decode_kernel<G>;
-  const size_t smem = attn_smem(G, p.D, p.C);
+  const size_t smem = attn_smem(G, p.D, p.C, p.nsp, p.chunk).total;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -467,6 +545,17 @@ extern "C" epq_status epq_attention_decode(const float *q, const float *k_new, c
   p.pos = pos;
   p.max_pos = max_pos;
   p.C = C;
+  // scores: positions of the largest CTA range, rounded to 4; key/value
+  // rows copied in chunks that fit the rest of the shared memory (the whole
+  // range in one chunk whenever it fits)
+  const int nmax = (pos + 1 + C - 1) / C;
+  p.nsp = (nmax + 3) & ~3;
+  const int64_t fixed = attn_smem(G, head_dim, C, p.nsp, 0).total;
+  const int64_t fit = (static_cast<int64_t>(dev.max_smem_optin) - fixed) / (2 * epq_kv_row_bytes(head_dim));
+  int64_t chunk = std::min<int64_t>((nmax + 7) & ~7, fit & ~int64_t(7));
+  if (tune_attn_chunk() > 0) chunk = std::min<int64_t>(chunk, tune_attn_chunk());
+  p.chunk = static_cast<int>(chunk);
+  if (p.chunk < 8) return EPQ_ERR_SHAPE;
   p.scale = scale;
   p.skip_log = skip_log;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -254,6 +254,8 @@ int tune_gemv_engine();
 int tune_early_stages();
 // k-parts (warps per 8-row block) of the tensor-core GEMV, 0 = chosen by shape
 int tune_tc_split();
+// most key/value rows of one attention copy chunk, 0 = as many as fit
+int tune_attn_chunk();
 
 // Record a CUDA error for epq_last_cuda_error() and return EPQ_ERR_CUDA.
 epq_status cuda_fail(cudaError_t e);

@@ -33,7 +33,7 @@ def test_tuning_keys(epq_lib):
     e = epq_lib
     cases = [(e.EPQ_TUNE_GEMV_ENGINE, 3, (-1, 4)), (e.EPQ_TUNE_TILE_BYTES, 65536, (4095, 131073)),
              (e.EPQ_TUNE_RING_BYTES, 65536, (32767, 200705)), (e.EPQ_TUNE_EARLY_STAGES, 3, (-1, 17)),
-             (e.EPQ_TUNE_TC_SPLIT, 8, (3, 32))]
+             (e.EPQ_TUNE_TC_SPLIT, 8, (3, 32)), (e.EPQ_TUNE_ATTN_CHUNK, 64, (-8, 4, 12, 4104))]
     for key, value, bad in cases:
         prev = e.epq_set_tuning(key, value)
         assert prev >= 0

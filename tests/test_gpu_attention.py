@@ -10,7 +10,12 @@ the float64 oracle.
   skip decision is then the same on both sides): within 1e-5 of
   sum_p w_p |v_p| / sum_p w_p per element;
 * bitwise reproducible; cluster sizes 1 to 8, grouped heads 1 to 8, head
-  sizes 128 and 256; score spreads with and without skipped positions.
+  sizes 128 and 256; score spreads with and without skipped positions;
+* key/value rows copied in several shared-memory chunks (forced small
+  chunks, and a long context of 8-head groups with 256-element heads whose
+  scores leave room for chunks of ~90 rows only): the same bounds, and with
+  chunks of 64 rows the output equals the one-chunk output bit for bit (the
+  positions then fall to the same warps).
 """
 import math
 
@@ -49,11 +54,28 @@ CASES = [
     (4, 2, 128, 1, 1.0),
     (16, 8, 128, 4000, 4.0),
     (8, 4, 256, 700, 5.0),
+    (64, 8, 256, 12001, 3.0),
 ]
 
 
 @pytest.mark.parametrize("case", CASES)
 def test_attention_parity(epq_lib, cuda_dev, case):
+    _check_case(epq_lib, cuda_dev, case)
+
+
+@pytest.mark.parametrize("chunk", [8, 24, 64])
+@pytest.mark.parametrize("case", [(32, 8, 128, 1025, 4.0), (8, 4, 256, 700, 5.0), (16, 16, 128, 300, 3.0)])
+def test_attention_chunked_copies(epq_lib, cuda_dev, case, chunk):
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_ATTN_CHUNK, chunk)
+    try:
+        out = _check_case(epq_lib, cuda_dev, case)
+    finally:
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_ATTN_CHUNK, prev)
+    if chunk == 64:
+        assert torch.equal(out, _check_case(epq_lib, cuda_dev, case))
+
+
+def _check_case(epq_lib, cuda_dev, case):
     n_heads, n_kv, D, T, spread = case
     rng = np.random.default_rng(T * 7 + D + n_heads)
     max_pos = T + 3
@@ -109,6 +131,7 @@ def test_attention_parity(epq_lib, cuda_dev, case):
     torch.cuda.synchronize()
     assert torch.equal(out, out2)
     assert epq_lib.epq_device_error() == 0
+    return out
 
 
 def test_attention_step_by_step_append(epq_lib, cuda_dev):
