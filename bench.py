@@ -896,6 +896,10 @@ def run_epq(args):
     epq.load()
     if args.gemv_engine is not None:
         epq.epq_set_tuning(epq.EPQ_TUNE_GEMV_ENGINE, args.gemv_engine)
+    for kv in args.tune:
+        name, value = kv.split("=")
+        if epq.epq_set_tuning(getattr(epq, "EPQ_TUNE_" + name.upper()), int(value)) < 0:
+            raise SystemExit(f"--tune {kv}: value out of range")
     fmt = epq.FORMATS[args.fmt]
     W = make_workload(epq, dev, fmt, args)
     stream = torch.cuda.Stream(device=dev)
@@ -1117,7 +1121,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly (no CUDA graph)")
     ap.add_argument("--gemv-engine", type=int, default=None,
                     help="EPQ_TUNE_GEMV_ENGINE for this run (0 automatic, 1 CUDA cores, 2 tensor cores, "
-                         "3 block-diagonal tensor-core engine for Q4_K)")
+                         "3 block-diagonal tensor-core engine for Q4_K, 4 vector-column engine for 2+ vectors)")
+    ap.add_argument("--tune", action="append", default=[], metavar="NAME=VALUE",
+                    help="an epq_set_tuning key for this run, e.g. VN_CLUSTER=4 (EPQ_TUNE_ prefix dropped)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

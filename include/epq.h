@@ -111,13 +111,16 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *   EPQ_TUNE_RING_BYTES  shared-memory ring budget per CTA (32768 .. 200704)
  *   EPQ_TUNE_GEMV_ENGINE engine of the Q4_K GEMVs and MoE experts:
  *                        0 automatic (the block-diagonal tensor-core engine
- *                        of the Q2_K / Q6_K GEMV for one vector, the ring
- *                        tensor-core engine for two or more and for the MoE
- *                        expert stages), 1 CUDA-core engines only
+ *                        of the Q2_K / Q6_K GEMV for one vector; for two or
+ *                        more the vector-column engine from 5 vectors, else
+ *                        the ring tensor-core engine; the ring engine for
+ *                        the MoE expert stages), 1 CUDA-core engines only
  *                        (also for the MoE experts), 2 the ring tensor-core
  *                        engine wherever it applies (one vector under 2 MiB:
  *                        CUDA cores), 3 the block-diagonal engine for every
- *                        Q4_K GEMV (the MoE experts as in 0)
+ *                        Q4_K GEMV (the MoE experts as in 0), 4 the
+ *                        vector-column engine for two or more Q4_K vectors
+ *                        (one weight pass for up to 8; MoE as in 0)
  *   EPQ_TUNE_EARLY_STAGES pipeline stages the tensor-core GEMV issues before
  *                        its grid-dependency wait when weights_ready is set
  *                        (0 .. 16, default 4)
@@ -129,10 +132,18 @@ int64_t epq_row_bytes(epq_fmt fmt, int64_t cols);
  *                        as fit (the default), else 8 .. 4096, a multiple
  *                        of 8 (smaller chunks: more copy round trips, the
  *                        same result)
+ *   EPQ_TUNE_VN_CHUNK    most superblocks of x operands the vector-column
+ *                        engine holds at a time: 0 = as many as fit (the
+ *                        default), else 1 .. 64 (longer rows run in chunks
+ *                        with partial sums in shared memory)
+ *   EPQ_TUNE_VN_CLUSTER  CTAs per thread-block cluster of the vector-column
+ *                        engine, which share the conversion of x: 0 =
+ *                        automatic (the default), 1, 2 or 4
  * Returns the previous value, or -1 for an unknown key or a value out of
  * range (nothing changes then).  Affects launches issued afterwards. */
 enum { EPQ_TUNE_TILE_BYTES = 1, EPQ_TUNE_RING_BYTES = 2, EPQ_TUNE_GEMV_ENGINE = 3, EPQ_TUNE_EARLY_STAGES = 4,
-       EPQ_TUNE_TC_SPLIT = 5, EPQ_TUNE_ATTN_CHUNK = 6 };
+       EPQ_TUNE_TC_SPLIT = 5, EPQ_TUNE_ATTN_CHUNK = 6, EPQ_TUNE_VN_CHUNK = 7,
+       EPQ_TUNE_VN_CLUSTER = 8 };
 int epq_set_tuning(int key, int value);
 
 /* ---------------------------------------------------------------- packing

@@ -145,7 +145,7 @@ def epq_block_bytes(fmt: int) -> int:
 
 
 EPQ_TUNE_TILE_BYTES, EPQ_TUNE_RING_BYTES, EPQ_TUNE_GEMV_ENGINE, EPQ_TUNE_EARLY_STAGES, EPQ_TUNE_TC_SPLIT = 1, 2, 3, 4, 5
-EPQ_TUNE_ATTN_CHUNK = 6
+EPQ_TUNE_ATTN_CHUNK, EPQ_TUNE_VN_CHUNK, EPQ_TUNE_VN_CLUSTER = 6, 7, 8
 
 
 def epq_set_tuning(key: int, value: int) -> int:

@@ -70,6 +70,8 @@ std::atomic<int> g_gemv_engine{0};
 std::atomic<int> g_early_stages{4};
 std::atomic<int> g_tc_split{0};
 std::atomic<int> g_attn_chunk{0};
+std::atomic<int> g_vn_chunk{0};
+std::atomic<int> g_vn_cluster{0};
 }  // namespace
 
 int tune_tile_bytes() { return g_tile_bytes.load(std::memory_order_relaxed); }
@@ -78,6 +80,8 @@ int tune_gemv_engine() { return g_gemv_engine.load(std::memory_order_relaxed); }
 int tune_early_stages() { return g_early_stages.load(std::memory_order_relaxed); }
 int tune_tc_split() { return g_tc_split.load(std::memory_order_relaxed); }
 int tune_attn_chunk() { return g_attn_chunk.load(std::memory_order_relaxed); }
+int tune_vn_chunk() { return g_vn_chunk.load(std::memory_order_relaxed); }
+int tune_vn_cluster() { return g_vn_cluster.load(std::memory_order_relaxed); }
 
 epq_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -113,7 +117,7 @@ int epq_set_tuning(int key, int value) {
       if (value < 32768 || value > 200704) return -1;
       return epq::g_ring_bytes.exchange(value);
     case EPQ_TUNE_GEMV_ENGINE:
-      if (value < 0 || value > 3) return -1;
+      if (value < 0 || value > 4) return -1;
       return epq::g_gemv_engine.exchange(value);
     case EPQ_TUNE_EARLY_STAGES:
       if (value < 0 || value > 16) return -1;
@@ -124,6 +128,12 @@ int epq_set_tuning(int key, int value) {
     case EPQ_TUNE_ATTN_CHUNK:
       if (value != 0 && (value < 8 || value > 4096 || value % 8)) return -1;
       return epq::g_attn_chunk.exchange(value);
+    case EPQ_TUNE_VN_CHUNK:
+      if (value < 0 || value > 64) return -1;
+      return epq::g_vn_chunk.exchange(value);
+    case EPQ_TUNE_VN_CLUSTER:
+      if (value != 0 && value != 1 && value != 2 && value != 4) return -1;
+      return epq::g_vn_cluster.exchange(value);
   }
   return -1;
 }

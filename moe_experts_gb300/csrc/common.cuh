@@ -256,6 +256,10 @@ int tune_early_stages();
 int tune_tc_split();
 // most key/value rows of one attention copy chunk, 0 = as many as fit
 int tune_attn_chunk();
+// most superblocks of x operands per chunk of the vector-column GEMV, 0 = as many as fit
+int tune_vn_chunk();
+// CTAs per cluster of the vector-column GEMV (1, 2, 4), 0 = automatic
+int tune_vn_cluster();
 
 // Record a CUDA error for epq_last_cuda_error() and return EPQ_ERR_CUDA.
 epq_status cuda_fail(cudaError_t e);

@@ -695,7 +695,20 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   // where the ring engine's two-vector operands pay.  Two or more Q4_K
   // vectors keep the ring engine (one pass for up to eight).
   const int eng0 = tune_gemv_engine();
-  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K || (fmt == EPQ_Q4_K && (eng0 == 3 || (eng0 == 0 && nvec == 1))))
+  // Q4_K with several vectors: the vector-column engine (gemv_vn.cu, one
+  // weight pass for up to 8 vectors on every shape) from 5 vectors on, where
+  // it was measured faster than the ring engine on the 8B-class step (8
+  // vectors: 3.13 against 4.48 ms per step).  With 3 or 4 vectors it wins
+  // only on gate/up and the LM head, and a step that alternates the two
+  // engines lost 0.5 ms at the switches (neither overlaps the other's
+  // tail: each needs a whole SM), so below 5 vectors every matrix keeps the
+  // ring engine.  Engine 4 takes it for every Q4_K launch of 2+ vectors.
+  const bool vn_auto = eng0 == 0 && nvec >= 5;
+  if (fmt == EPQ_Q4_K && nvec >= 2 && (eng0 == 4 || vn_auto)) {
+    const epq_status st = gemv_vn_launch(blocks, x, y, rows, cols, nvec, opts, xs, dev, s);
+    if (st != EPQ_ERR_SHAPE) return st;  // rows too many for its chunked partial sums: the ring engine below
+  }
+  if (fmt == EPQ_Q2_K || fmt == EPQ_Q6_K || (fmt == EPQ_Q4_K && (eng0 == 3 || (eng0 != 1 && eng0 != 2 && nvec == 1))))
     return gemv_k16_launch(fmt, blocks, x, y, rows, cols, nvec, opts, xs, dev, s);
 
   // Q4_K (three or more vectors, or engine 2): the ring tensor-core engine

@@ -80,7 +80,7 @@ __device__ __forceinline__ int x_src(int j, int group, int head_dim) {
 }
 
 template <int FMT, int NV, int ALIGN, bool SW>
-__global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p) {
+__global__ void __launch_bounds__(kThreads, NV <= 2 ? 2 : 1) gemv_k16_kernel(const K16Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const K16Layout L = k16_layout(NV, p.nsb);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -248,7 +248,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_k16_kernel(const K16Params p
         a += rr[o * NV + v];
         if (SW) b += rr[(o + 8) * NV + v];
       }
-      const float r = NV > 1 && v == NV - 1 ? rs[NV - 1] : rs[0];  // constant indices keep rs in registers
+      float r = rs[0];
+#pragma unroll
+      for (int w = 1; w < NV; ++w)
+        if (w == v) r = rs[w];  // constant indices keep rs in registers
       float val = a * r;
       if (SW) val = silu(val) * (b * r);
       if (p.residual) val += p.residual[v * p.y_stride + i];
@@ -285,8 +288,8 @@ cudaError_t dispatch_k16(const K16Params &p, int align, bool sw, unsigned grid, 
 // with the fewest per-CTA iterations x (superblocks per warp + 1 for the
 // per-iteration reduction) wins, ties going to the larger RG; when no RG
 // fills the GPU twice, RG = 1 and one CTA per row group.
-void k16_split(int64_t ngroups, int nsb, int sms, int *rg_out, unsigned *grid_out) {
-  const int64_t cap = 2ll * sms;
+void k16_split(int64_t ngroups, int nsb, int sms, int per_sm, int *rg_out, unsigned *grid_out) {
+  const int64_t cap = static_cast<int64_t>(per_sm) * sms;
   int64_t best = -1;
   *rg_out = 1;
   *grid_out = static_cast<unsigned>(std::max<int64_t>(1, std::min(ngroups, cap)));
@@ -313,13 +316,21 @@ epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, floa
   const bool sw = o.swiglu != 0;
   const int64_t rows_out = sw ? rows / 2 : rows;
   const int nsb = static_cast<int>(cols / 256);
-  const int nvl = std::min(nvec, 2);
+  // vectors per weight pass: Q4_K takes up to 8 in one pass when their x
+  // operands fit shared memory (one CTA per SM from 4 vectors on), else
+  // passes of two
+  int nvl = nvec <= 1 ? 1 : nvec <= 2 ? 2 : nvec <= 4 ? 4 : 8;
+  if (fmt != EPQ_Q4_K) nvl = std::min(nvl, 2);
+  while (nvl > 2 && k16_layout(nvl, nsb).total > static_cast<uint32_t>(dev.max_smem_optin)) nvl /= 2;
   const K16Layout L = k16_layout(nvl, nsb);
   if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) return EPQ_ERR_SHAPE;
+  // resident CTAs per SM: two when the launch bounds and 2 x (smem + the
+  // 1 KB the runtime reserves per CTA) fit the SM's 228 KB
+  const int per_sm = nvl <= 2 && 2 * (L.total + 1024u) <= 233472u ? 2 : 1;
   const int64_t ngroups = (rows_out + (sw ? 7 : 15)) / (sw ? 8 : 16);
   int rg = 1;
   unsigned grid = 1;
-  k16_split(ngroups, nsb, dev.sm_count, &rg, &grid);
+  k16_split(ngroups, nsb, dev.sm_count, per_sm, &rg, &grid);
   K16Params p;
   p.W = static_cast<const uint8_t *>(blocks);
   p.rows_out = rows_out;
@@ -336,15 +347,17 @@ epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, floa
   p.x_head_dim = o.x_head_dim;
   p.early = o.weights_ready ? 1 : 0;
   const int align = row_bytes % 16 == 0 ? 16 : (row_bytes % 4 == 0 ? 4 : 2);
-  for (int v0 = 0; v0 < nvec; v0 += 2) {
-    p.nv = std::min(2, nvec - v0);
+  for (int v0 = 0; v0 < nvec; v0 += nvl) {
+    p.nv = std::min(nvl, nvec - v0);
     p.x = x + v0 * x_stride;
     p.y = y + v0 * rows_out;
     p.residual = o.residual ? o.residual + v0 * rows_out : nullptr;
     cudaError_t e;
     if (fmt == EPQ_Q4_K)  // 144-byte superblocks: every row starts on a 16-byte boundary
-      e = nvl == 1 ? dispatch_sw<EPQ_Q4_K, 1, 16>(p, sw, grid, L.total, s)
-                   : dispatch_sw<EPQ_Q4_K, 2, 16>(p, sw, grid, L.total, s);
+      e = nvl == 1   ? dispatch_sw<EPQ_Q4_K, 1, 16>(p, sw, grid, L.total, s)
+          : nvl == 2 ? dispatch_sw<EPQ_Q4_K, 2, 16>(p, sw, grid, L.total, s)
+          : nvl == 4 ? dispatch_sw<EPQ_Q4_K, 4, 16>(p, sw, grid, L.total, s)
+                     : dispatch_sw<EPQ_Q4_K, 8, 16>(p, sw, grid, L.total, s);
     else if (fmt == EPQ_Q2_K)
       e = nvl == 1 ? dispatch_k16<EPQ_Q2_K, 1>(p, align, sw, grid, L.total, s)
                    : dispatch_k16<EPQ_Q2_K, 2>(p, align, sw, grid, L.total, s);

@@ -41,6 +41,11 @@ cudaError_t gemv_tc_launch(const TcPlan &pl, const TcArgs &a, cudaStream_t s);
 // shape is not covered (the caller then runs one pass per vector pair).
 bool gemv_tc_multi_launch(const TcArgs &a, int nvec, const DeviceInfo &dev, cudaStream_t s, cudaError_t *err);
 
+// Q4_K with 2..8 vectors in one weight pass, the vectors in the MMA's n
+// dimension (gemv_vn.cu): the whole epq_gemv_ex call after the common checks.
+epq_status gemv_vn_launch(const void *blocks, const float *x, float *y, int64_t rows, int64_t cols, int nvec,
+                          const epq_gemv_opts &o, int64_t x_stride, const DeviceInfo &dev, cudaStream_t s);
+
 // Q2_K / Q6_K (gemv_k16.cu): the whole epq_gemv_ex call after the common
 // argument checks (x_stride = floats between x vectors).
 epq_status gemv_k16_launch(epq_fmt fmt, const void *blocks, const float *x, float *y, int64_t rows, int64_t cols,

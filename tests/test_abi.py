@@ -31,7 +31,7 @@ def test_tuning_keys(epq_lib):
     """epq_set_tuning returns the previous value, and leaves the setting
     unchanged (returning -1) for an unknown key or a value out of range."""
     e = epq_lib
-    cases = [(e.EPQ_TUNE_GEMV_ENGINE, 3, (-1, 4)), (e.EPQ_TUNE_TILE_BYTES, 65536, (4095, 131073)),
+    cases = [(e.EPQ_TUNE_GEMV_ENGINE, 4, (-1, 5)), (e.EPQ_TUNE_VN_CHUNK, 5, (-1, 65)), (e.EPQ_TUNE_VN_CLUSTER, 4, (-1, 3, 8)), (e.EPQ_TUNE_TILE_BYTES, 65536, (4095, 131073)),
              (e.EPQ_TUNE_RING_BYTES, 65536, (32767, 200705)), (e.EPQ_TUNE_EARLY_STAGES, 3, (-1, 17)),
              (e.EPQ_TUNE_TC_SPLIT, 8, (3, 32)), (e.EPQ_TUNE_ATTN_CHUNK, 64, (-8, 4, 12, 4104))]
     for key, value, bad in cases:

@@ -87,7 +87,7 @@ def _decoder_matches(m, ref_logits, ref_h):
     assert m.epq.epq_device_error() == 0
 
 
-@pytest.mark.parametrize("nvec", [1, 2])
+@pytest.mark.parametrize("nvec", [1, 2, 4, 8])
 def test_dense_step_equals_isolated_calls(epq_lib, cuda_dev, nvec):
     m = _Model(epq_lib, cuda_dev, nvec, L=3, seed=11)
     logits, h = _isolated(m, Q4K)

@@ -183,3 +183,106 @@ def test_q4k_block_diagonal_engine_options(epq_lib, cuda_dev, engine3):
     test_gemv_ex_swiglu(epq_lib, cuda_dev, oracle.Q4_K)
     test_gemv_ex_grouped_heads(epq_lib, cuda_dev, oracle.Q4_K)
     test_gemv_full_size_layer_sampled(epq_lib, cuda_dev, oracle.Q4_K)
+
+
+@pytest.fixture
+def engine4(epq_lib):
+    """The vector-column tensor-core engine for the Q4_K GEMVs of 2+ vectors."""
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, 4)
+    yield
+    epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_GEMV_ENGINE, prev)
+
+
+MULTI_SHAPES = [(130, 4096, 4), (257, 2048, 5), (300, 4096, 8), (20, 14336, 6), (1000, 768, 7), (64, 256, 3),
+                (48, 1024, 2)]
+
+
+@pytest.mark.parametrize("rows,cols,nvec", MULTI_SHAPES)
+def test_q4k_block_diagonal_vectors_in_one_pass(epq_lib, cuda_dev, engine3, rows, cols, nvec):
+    """Up to 8 vectors per weight pass (4 or 8 x-operand sets in shared
+    memory; rows of 14336 take passes of two)."""
+    _multi_vector_case(epq_lib, cuda_dev, rows, cols, nvec)
+
+
+@pytest.mark.parametrize("cluster", [0, 1, 4])
+@pytest.mark.parametrize("chunk", [0, 3, 7])
+@pytest.mark.parametrize("rows,cols,nvec", MULTI_SHAPES)
+def test_q4k_vector_column_engine(epq_lib, cuda_dev, engine4, rows, cols, nvec, chunk, cluster):
+    """The vector-column engine (8 vector columns per MMA): the whole row's x
+    operands in shared memory, or chunks of 3 / 7 superblocks with partial
+    sums kept between chunks (rows of 14336 are chunked by default); the x
+    conversion shared by clusters of 2 (automatic) or 4 CTAs, or not."""
+    prev = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_VN_CHUNK, chunk)
+    prev_cl = epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_VN_CLUSTER, cluster)
+    try:
+        _multi_vector_case(epq_lib, cuda_dev, rows, cols, nvec)
+    finally:
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_VN_CHUNK, prev)
+        epq_lib.epq_set_tuning(epq_lib.EPQ_TUNE_VN_CLUSTER, prev_cl)
+
+
+def test_q4k_vector_column_engine_options(epq_lib, cuda_dev, engine4):
+    test_gemv_nvec8_and_scales(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_one_hot_is_exact_column(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_ex_residual_and_prenorm(epq_lib, cuda_dev, oracle.Q4_K)
+    test_gemv_ex_swiglu(epq_lib, cuda_dev, oracle.Q4_K)
+    for shape in SHAPES:
+        test_gemv_parity(epq_lib, cuda_dev, oracle.Q4_K, shape)
+
+
+def test_q4k_vector_column_engine_grouped_heads(epq_lib, cuda_dev, engine4):
+    """x_group with 4 vectors: each 128-float head of a vector feeds 4
+    consecutive heads of the product."""
+    fmt, rows, cols, hd, grp, nvec = oracle.Q4_K, 64, 4096, 128, 4, 4
+    W, packed, _ = _case(fmt, rows, cols, 1, seed=41)
+    v = synthetic.normal((nvec, cols // grp), seed=42).numpy()
+    xe = np.stack([np.concatenate([np.tile(v[k, h * hd:(h + 1) * hd], grp) for h in range(cols // grp // hd)])
+                   for k in range(nvec)])
+    y = epq_lib.epq_gemv_ex(fmt, torch.from_numpy(packed).to(cuda_dev), torch.from_numpy(v).to(cuda_dev),
+                            rows, cols, x_group=grp, x_head_dim=hd).cpu().numpy()
+    _check(y, oracle.gemv_f64(fmt, packed, xe, cols), oracle.gemv_bound(fmt, packed, xe, cols), what="grouped")
+
+
+def test_q4k_vector_column_engine_full_size_sampled(epq_lib, cuda_dev, engine4):
+    """8 vectors on the full 8B-layer shapes (the down projection chunked)."""
+    fmt = oracle.Q4_K
+    for rows, cols in ((14336, 4096), (4096, 14336)):
+        W = synthetic.student_t((rows, cols), seed=rows + 3 * cols, device=cuda_dev)
+        pk = epq_lib.epq_quantize(fmt, W)
+        x = synthetic.normal((8, cols), seed=cols + 9).to(cuda_dev)
+        y = epq_lib.epq_gemv(fmt, pk, x, rows, cols).cpu().numpy()
+        idx = np.sort(np.random.default_rng(rows).choice(rows, 128, replace=False))
+        pks = oracle.quantize(fmt, W.cpu().numpy()[idx])   # the oracle packs its own rows ...
+        assert np.array_equal(pks, pk.cpu().numpy()[idx])   # ... which the GPU packer matches byte for byte
+        xs = x.cpu().numpy()
+        _check(y[:, idx], oracle.gemv_f64(fmt, pks, xs, cols), oracle.gemv_bound(fmt, pks, xs, cols), what="full")
+    assert epq_lib.epq_device_error() == 0
+
+
+def _multi_vector_case(epq_lib, cuda_dev, rows, cols, nvec):
+    """Plain, SwiGLU and residual + RMS pre-norm with nvec vectors, each
+    vector with its own magnitude so that a vector reading another's
+    operands or RMS factor fails."""
+    fmt, eps = oracle.Q4_K, 1e-6
+    W, packed, x = _case(fmt, rows, cols, nvec, seed=rows * 7 + cols + nvec)
+    x = (x * np.float32(10.0) ** np.arange(-3, nvec - 3, dtype=np.float32)[:, None]).astype(np.float32)
+    pk = torch.from_numpy(packed).to(cuda_dev)
+    xd = torch.from_numpy(x).to(cuda_dev)
+    y = epq_lib.epq_gemv(fmt, pk, xd, rows, cols).cpu().numpy()
+    _check(y, oracle.gemv_f64(fmt, packed, x, cols), oracle.gemv_bound(fmt, packed, x, cols), what="plain")
+    res = synthetic.normal((nvec, rows), seed=rows + 5).numpy()
+    yr = torch.from_numpy(res).to(cuda_dev).clone()
+    epq_lib.epq_gemv_ex(fmt, pk, xd, rows, cols, y=yr, residual=yr, rms_prenorm=True, rms_eps=eps)
+    xn = oracle.rmsnorm_f64(x, eps)
+    _check(yr.cpu().numpy(), res + oracle.gemv_f64(fmt, packed, xn, cols),
+           oracle.gemv_bound(fmt, packed, xn, cols) + np.abs(res), what="residual+prenorm")
+    I = rows // 2
+    h = epq_lib.epq_gemv_ex(fmt, pk[:2 * I], xd, 2 * I, cols, swiglu=True).cpu().numpy()
+    yy = oracle.gemv_f64(fmt, packed[:2 * I], x, cols)
+    A = oracle.gemv_bound(fmt, packed[:2 * I], x, cols)
+    g, u, Ag, Au = yy[:, :I], yy[:, I:], A[:, :I], A[:, I:]
+    silu = g / (1 + np.exp(-g))
+    ref = silu * u
+    bound = TOL * (1.1 * Ag * np.abs(u) + np.abs(silu) * Au) + 1e-6 * np.abs(ref)
+    assert (np.abs(h - ref) <= bound + 1e-30).all(), (np.abs(h - ref) / (bound + 1e-30)).max()
+    assert epq_lib.epq_device_error() == 0
