@@ -978,18 +978,20 @@ def run_epq(args):
         torch.cuda.empty_cache()
         subs = {}
         Q2K, Q6K = epq.EPQ_Q2_K, epq.EPQ_Q6_K
-        for key, name, ntok, ctx, wfmt, ef, df in (
-                ("gemv4096", "gemv4096", None, None, fmt, None, None),
-                ("gemv4096_q2k", "gemv4096", None, None, Q2K, None, None),
-                ("gemv4096_q6k", "gemv4096", None, None, Q6K, None, None),
-                ("moe_layer_1tok", "moe_layer", 1, None, fmt, None, None),
-                ("moe_layer_8tok", "moe_layer", 8, None, fmt, None, None),
-                ("moe_decode", "moe_decode", None, None, fmt, None, None),
-                ("moe_decode_q2k_experts", "moe_decode", None, None, fmt, Q2K, None),
-                ("moe_decode_q6k_down", "moe_decode", None, None, fmt, None, Q6K),
-                ("dense8b_attn1024", "dense8b", None, 1024, fmt, None, None),
-                ("moe_decode_attn1024", "moe_decode", None, 1024, fmt, None, None)):
-            Wk = make_workload(epq, dev, wfmt, argparse.Namespace(**{**vars(args), "layers": None, "nvec": 1}),
+        for key, name, ntok, ctx, wfmt, ef, df, nv in (
+                ("gemv4096", "gemv4096", None, None, fmt, None, None, 1),
+                ("gemv4096_q2k", "gemv4096", None, None, Q2K, None, None, 1),
+                ("gemv4096_q6k", "gemv4096", None, None, Q6K, None, None, 1),
+                ("moe_layer_1tok", "moe_layer", 1, None, fmt, None, None, 1),
+                ("moe_layer_8tok", "moe_layer", 8, None, fmt, None, None, 1),
+                ("moe_decode", "moe_decode", None, None, fmt, None, None, 1),
+                ("moe_decode_q2k_experts", "moe_decode", None, None, fmt, Q2K, None, 1),
+                ("moe_decode_q6k_down", "moe_decode", None, None, fmt, None, Q6K, 1),
+                ("dense8b_attn1024", "dense8b", None, 1024, fmt, None, None, 1),
+                ("moe_decode_attn1024", "moe_decode", None, 1024, fmt, None, None, 1),
+                ("dense8b_verify2", "dense8b", None, None, fmt, None, None, 2),
+                ("dense8b_verify8", "dense8b", None, None, fmt, None, None, 8)):
+            Wk = make_workload(epq, dev, wfmt, argparse.Namespace(**{**vars(args), "layers": None, "nvec": nv}),
                                name=name, ntok=ntok, attn_ctx=ctx, expert_fmt=ef, down_fmt=df)
             subs[key] = sub_object(torch, epq, Wk, stream, args, peak, peak_kind)
             del Wk

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 2 : 1) gemv_k16_kernel(con
   __syncthreads();
 
   // ---------------------------------------------------------------- main loop
-  const uint32_t frag0 = smem_addr(smem + L.frag) + k16::lane_slot(lane);
+  const uint8_t *frag0 = smem + L.frag + k16::lane_slot(lane);
   const uint32_t vstride = static_cast<uint32_t>(p.nsb) * k16::kSbFragBytes;
   float *red = reinterpret_cast<float *>(smem + L.red);
   float rs[NV];  // RMS factors of the vectors
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 2 : 1) gemv_k16_kernel(con
         float ps[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsb + b];
-        k16::superblock<FMT, NV>(ring_lo[d], ring_hi[d], frag0 + static_cast<uint32_t>(b) * k16::kSbFragBytes,
+        k16::superblock<FMT, NV>(ring_lo[d], ring_hi[d], frag0 + b * k16::kSbFragBytes,
                                  vstride, ps, xsum_s + b * 16, p.nsb * 16, t, acc);
         if (j + kDepth < cnt) {
           k16::load_ops<FMT, ALIGN>(ring_lo[d], row_lo, nsb, b + kDepth * p.kp, t);

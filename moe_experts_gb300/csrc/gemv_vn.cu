@@ -104,12 +104,6 @@ __device__ __forceinline__ int vn_x_src(int j, int group, int head_dim) {
   return (j / span) * head_dim + (j % head_dim);
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t s) {
   __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&s));
   return *reinterpret_cast<uint32_t *>(&r);
@@ -343,8 +337,10 @@ __global__ void __launch_bounds__(kVnThreads, 1) gemv_vn_kernel(const VnParams p
     }
   };
 
-  const uint32_t main0 = smem_addr(smem + L.main) + static_cast<uint32_t>(lane) * 16u;
-  const uint32_t min0 = smem_addr(smem + L.minb) + static_cast<uint32_t>(lane) * 8u;
+  // B operands: plain loads from the __shared__ array, which the compiler may
+  // issue ahead of the preceding MMAs
+  const uint8_t *main0 = smem + L.main + lane * 16;
+  const uint8_t *min0 = smem + L.minb + lane * 8;
   if constexpr (CL > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   // Every CTA of a cluster runs the same barrier sequence, whatever its rows:
   // per chunk one barrier before the staging (c > 0: every CTA has finished
@@ -397,7 +393,7 @@ __global__ void __launch_bounds__(kVnThreads, 1) gemv_vn_kernel(const VnParams p
         float cm[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) cm[q][0] = cm[q][1] = cm[q][2] = cm[q][3] = 0.0f;
-        const uint32_t mb = main0 + static_cast<uint32_t>(bl) * kVnSbMain;
+        const uint8_t *mb = main0 + bl * kVnSbMain;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t sAl = j < 4 ? sAl0 : sAl1, sBl = j < 4 ? sBl0 : sBl1;
@@ -408,7 +404,7 @@ __global__ void __launch_bounds__(kVnThreads, 1) gemv_vn_kernel(const VnParams p
             const uint32_t wh = h ? hi.qs[j] >> 8 : hi.qs[j];
             const uint32_t a[4] = {hmul2u(wl & k16::kNibA, sAl), hmul2u(wh & k16::kNibA, sAh),
                                    hmul2u(wl & k16::kNibB, sBl), hmul2u(wh & k16::kNibB, sBh)};
-            const uint4 bb = lds128(mb + static_cast<uint32_t>(j) * kVnPair + static_cast<uint32_t>(h) * kVnMma);
+            const uint4 bb = *reinterpret_cast<const uint4 *>(mb + j * kVnPair + h * kVnMma);
             k16::mma(cm[2 * h], a, make_uint2(bb.x, bb.y));
             k16::mma(cm[2 * h + 1], a, make_uint2(bb.z, bb.w));
           }
@@ -417,7 +413,7 @@ __global__ void __launch_bounds__(kVnThreads, 1) gemv_vn_kernel(const VnParams p
         float cn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         {
           const uint32_t am[4] = {half2_bits(kl[0], kl[1]), half2_bits(kh[0], kh[1]), 0u, 0u};
-          const uint2 xb = k16::lds64(min0 + static_cast<uint32_t>(bl) * kVnSbMin);
+          const uint2 xb = *reinterpret_cast<const uint2 *>(min0 + bl * kVnSbMin);
           k16::mma(cn, am, make_uint2(xb.x, 0u));
           k16::mma(cn, am, make_uint2(xb.y, 0u));
         }

@@ -77,11 +77,10 @@ __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint2
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
 }
 
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
+// B operands are read with plain loads from the __shared__ array (not
+// volatile asm): the compiler may then issue them ahead of the preceding
+// MMAs, and the CTA barriers still order them after the staging stores.
+__device__ __forceinline__ uint2 lds64(const uint8_t *p) { return *reinterpret_cast<const uint2 *>(p); }
 
 // Streaming loads of packed weights (read once, not kept in L1).
 __device__ __forceinline__ uint4 ldg_stream16(const uint8_t *p) {
@@ -243,7 +242,7 @@ __device__ __forceinline__ void q4k_codes(const uint4 &h, int t, float (&c)[2], 
 // (0,4)(1,5) for even m and (2,6)(3,7) for odd m (the word shifted by 8),
 // as fp16 subnormals n 2^-24 (class A) and 16 n 2^-24 (class B).
 template <int NV>
-__device__ __forceinline__ void superblock_q4k(const RowOps<EPQ_Q4_K> &lo, const RowOps<EPQ_Q4_K> &hi, uint32_t frag,
+__device__ __forceinline__ void superblock_q4k(const RowOps<EPQ_Q4_K> &lo, const RowOps<EPQ_Q4_K> &hi, const uint8_t *frag,
                                                uint32_t vstride, const float (&ps)[NV], const float *xsum, int xstride,
                                                int t, float (&acc)[2][NV]) {
   float cl[2], kl[2], ch[2], kh[2];
@@ -264,7 +263,7 @@ __device__ __forceinline__ void superblock_q4k(const RowOps<EPQ_Q4_K> &lo, const
       const uint32_t a[4] = {wl & kNibA, wh & kNibA, wl & kNibB, wh & kNibB};
 #pragma unroll
       for (int v = 0; v < NV; ++v)
-        mma(c[v], a, lds64(frag + v * vstride + static_cast<uint32_t>((q * 8 + m) * kMmaBytes)));
+        mma(c[v], a, lds64(frag + v * vstride + (q * 8 + m) * kMmaBytes));
     }
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -287,14 +286,14 @@ __device__ __forceinline__ void superblock_q4k(const RowOps<EPQ_Q4_K> &lo, const
 // ------------------------------------------------------------------ one superblock
 // Adds one superblock's contribution to acc[row 0 = g, 1 = g + 8][vector]
 // (partial: only lane t's owner sub-blocks; the 4 lanes of a row sum later).
-//   frag   shared address of this superblock's x operands for vector 0 plus
-//          the lane's slot offset; vector v adds v * vstride
+//   frag   this superblock's x operands for vector 0 (in the __shared__
+//          array) plus the lane's slot offset; vector v adds v * vstride
 //   ps     2^(10 - sigma) of this superblock per vector
 //   xsum   shared float sums of x over the superblock's 16 sub-blocks for
 //          vector 0 (the Q2_K lift term, the Q6_K code offset); vector v adds
 //          v * xstride floats
 template <int FMT, int NV>
-__device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<FMT> &hi, uint32_t frag,
+__device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<FMT> &hi, const uint8_t *frag,
                                            uint32_t vstride, const float (&ps)[NV], const float *xsum, int xstride,
                                            int t, float (&acc)[2][NV]) {
   if constexpr (FMT == EPQ_Q4_K) {
@@ -322,7 +321,7 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
       const uint32_t a[4] = {pl[2 * i], ph[2 * i], pl[2 * i + 1], ph[2 * i + 1]};
 #pragma unroll
       for (int v = 0; v < NV; ++v)
-        mma(c[v], a, lds64(frag + v * vstride + static_cast<uint32_t>((q * 4 + i) * kMmaBytes)));
+        mma(c[v], a, lds64(frag + v * vstride + (q * 4 + i) * kMmaBytes));
     }
     if constexpr (FMT == EPQ_Q2_K) {
       const uint32_t bl = (lo.sub >> (8 * q)) & 0xFFu, bh = (hi.sub >> (8 * q)) & 0xFFu;

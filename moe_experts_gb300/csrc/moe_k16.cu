@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
   }
   __syncthreads();
 
-  const uint32_t frag0 = smem_addr(smem + p.frag_off) + k16::lane_slot(lane);
+  const uint8_t *frag0 = smem + p.frag_off + k16::lane_slot(lane);
   const uint32_t vstride = static_cast<uint32_t>(nsb) * k16::kSbFragBytes;
   float *red = reinterpret_cast<float *>(smem + p.red_off);
 #pragma unroll 1
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
         float ps[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * nsb + sb];
-        k16::superblock<FMT, NV>(cl, ch, frag0 + static_cast<uint32_t>(sb) * k16::kSbFragBytes, vstride, ps,
+        k16::superblock<FMT, NV>(cl, ch, frag0 + sb * k16::kSbFragBytes, vstride, ps,
                                  xsum_s + sb * 16, nsb * 16, t, acc);
         if (nx >= nsb) break;
         sb = nx;
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
   }
   __syncthreads();
 
-  const uint32_t frag0 = smem_addr(smem + p.frag_off) + k16::lane_slot(lane);
+  const uint8_t *frag0 = smem + p.frag_off + k16::lane_slot(lane);
   const uint32_t vstride = static_cast<uint32_t>(p.nsbx) * k16::kSbFragBytes;
   float *red = reinterpret_cast<float *>(smem + p.red_off);
 #pragma unroll 1
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
         float ps[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) ps[v] = ps_s[v * p.nsbx + sb];
-        k16::superblock<FMT, NV>(cl, ch, frag0 + static_cast<uint32_t>(sb) * k16::kSbFragBytes, vstride, ps,
+        k16::superblock<FMT, NV>(cl, ch, frag0 + sb * k16::kSbFragBytes, vstride, ps,
                                  xsum_s + sb * 16, p.nsbx * 16, t, acc);
         if (nx >= nvsb) break;
         sb = nx;
