@@ -1328,9 +1328,37 @@ extern "C" size_t epq_moe_workspace_bytes(const epq_router *router, const epq_ex
   return ws_layout(ntok, topk, router->n_experts, experts->inter).total;
 }
 
+namespace {
+
+// The routing buffers of a whole call, for the token chunks of its expert
+// stages: the router ran once for every token; chunk t0.. reads its tokens'
+// rows of the per-token buffers and reuses the per-call scratch (meta,
+// active, cnt, list), which each chunk's gate/up kernel rewrites after its
+// grid-dependency wait on the previous chunk's down kernel.
+struct MoePre {
+  float *logits, *xstat, *gshared, *w, *h;
+  int32_t *idx, *meta, *active, *cnt, *list;
+  uint32_t *hmax;
+};
+
+epq_status moe_forward_impl(const epq_router *router, const epq_experts *experts, const float *x, int ntok, int topk,
+                            const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w, void *workspace,
+                            size_t workspace_bytes, epq_stream_t stream, const MoePre *pre);
+
+}  // namespace
+
 extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_experts *experts, const float *x, int ntok,
                                       int topk, const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w,
                                       void *workspace, size_t workspace_bytes, epq_stream_t stream) {
+  return moe_forward_impl(router, experts, x, ntok, topk, opts, y, topk_idx, topk_w, workspace, workspace_bytes,
+                          stream, nullptr);
+}
+
+namespace {
+
+epq_status moe_forward_impl(const epq_router *router, const epq_experts *experts, const float *x, int ntok, int topk,
+                            const epq_moe_opts *opts, float *y, int32_t *topk_idx, float *topk_w, void *workspace,
+                            size_t workspace_bytes, epq_stream_t stream, const MoePre *pre) {
   epq_status st = check_moe(router, experts, ntok, topk);
   if (st != EPQ_OK) return st;
   if (!x || !y) return EPQ_ERR_ARG;
@@ -1367,25 +1395,53 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
       if (moe_k16_fits(q, std::min(E, c * topk) + shared, k16g, k16d, dv)) k16_chunk = c;
     }
     if (!k16_chunk) return EPQ_ERR_SHAPE;
-    if (ntok > k16_chunk && !whole) return EPQ_ERR_SHAPE;  // stage calls are not split into token chunks
+    // stage calls with expert stages are not split into token chunks
+    if (ntok > k16_chunk && !whole && (o.stages & (EPQ_MOE_GATE_UP | EPQ_MOE_DOWN))) return EPQ_ERR_SHAPE;
   }
   // Q4_K with three or more tokens, all stages in this call: the tensor-core
-  // expert kernels take two tokens per pass, so the call runs as chunks of
-  // two tokens (router, gate/up, down each; an expert chosen in two chunks
-  // is read once per chunk).  Measured faster than the CUDA-core engines,
-  // which read every chosen expert once for all tokens.  Calls with a
-  // Q2_K / Q6_K stage run as chunks of k16_chunk tokens.
+  // expert kernels take two tokens per pass, so the expert stages run as
+  // chunks of two tokens (an expert chosen in two chunks is read once per
+  // chunk) after ONE router launch for every token.  Measured faster than
+  // the CUDA-core engines, which read every chosen expert once for all
+  // tokens.  Calls with a Q2_K / Q6_K stage run as chunks of k16_chunk
+  // tokens.
   const int chunk = k16_chunk ? k16_chunk : 2;
-  if (ntok > chunk && whole &&
+  if (!pre && ntok > chunk && whole &&
       (k16_chunk || (gf == EPQ_Q4_K && df == EPQ_Q4_K && tune_gemv_engine() != 1))) {
+    epq_moe_opts orr = o;
+    orr.stages = EPQ_MOE_ROUTE;
+    st = moe_forward_impl(router, experts, x, ntok, topk, &orr, y, nullptr, nullptr, workspace, workspace_bytes,
+                          stream, nullptr);
+    if (st != EPQ_OK) return st;
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    const MoePre all{o.logits_out ? o.logits_out : reinterpret_cast<float *>(wsb + L.logits),
+                     reinterpret_cast<float *>(wsb + L.xstat),
+                     reinterpret_cast<float *>(wsb + L.gshared),
+                     reinterpret_cast<float *>(wsb + L.w),
+                     o.h_out ? o.h_out : reinterpret_cast<float *>(wsb + L.h),
+                     reinterpret_cast<int32_t *>(wsb + L.idx),
+                     reinterpret_cast<int32_t *>(wsb + L.meta),
+                     reinterpret_cast<int32_t *>(wsb + L.active),
+                     reinterpret_cast<int32_t *>(wsb + L.cnt),
+                     reinterpret_cast<int32_t *>(wsb + L.list),
+                     reinterpret_cast<uint32_t *>(wsb + L.hmax)};
     for (int t0 = 0; t0 < ntok; t0 += chunk) {
       const int nt = std::min(chunk, ntok - t0);
       epq_moe_opts oc = o;
-      if (o.logits_out) oc.logits_out = o.logits_out + static_cast<int64_t>(t0) * E;
-      if (o.h_out) oc.h_out = o.h_out + static_cast<int64_t>(t0) * (topk + 1) * I;
-      st = epq_moe_forward(router, experts, x + static_cast<int64_t>(t0) * H, nt, topk, &oc,
-                           y + static_cast<int64_t>(t0) * H, topk_idx ? topk_idx + t0 * topk : nullptr,
-                           topk_w ? topk_w + t0 * topk : nullptr, workspace, workspace_bytes, stream);
+      oc.stages = EPQ_MOE_GATE_UP | EPQ_MOE_DOWN;
+      oc.logits_out = nullptr;
+      oc.h_out = nullptr;
+      MoePre pc = all;
+      pc.logits += static_cast<int64_t>(t0) * E;
+      pc.xstat += 2 * t0;
+      pc.gshared += t0;
+      pc.w += t0 * topk;
+      pc.idx += t0 * topk;
+      pc.h += static_cast<int64_t>(t0) * (topk + 1) * I;
+      pc.hmax += t0 * (topk + 1);
+      st = moe_forward_impl(router, experts, x + static_cast<int64_t>(t0) * H, nt, topk, &oc,
+                            y + static_cast<int64_t>(t0) * H, topk_idx ? topk_idx + t0 * topk : nullptr,
+                            topk_w ? topk_w + t0 * topk : nullptr, workspace, workspace_bytes, stream, &pc);
       if (st != EPQ_OK) return st;
     }
     return EPQ_OK;
@@ -1433,6 +1489,19 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   a.list = reinterpret_cast<int32_t *>(ws + L.list);
   a.hmax = reinterpret_cast<uint32_t *>(ws + L.hmax);
   a.h = o.h_out ? o.h_out : reinterpret_cast<float *>(ws + L.h);
+  if (pre) {  // a token chunk of a routed call: the whole call's buffers
+    a.logits = pre->logits;
+    a.xstat = pre->xstat;
+    a.gshared = pre->gshared;
+    a.idx = pre->idx;
+    a.w = pre->w;
+    a.meta = pre->meta;
+    a.active = pre->active;
+    a.cnt = pre->cnt;
+    a.list = pre->list;
+    a.hmax = pre->hmax;
+    a.h = pre->h;
+  }
   a.err = err;
 
   const int stages = (o.stages & 7) ? (o.stages & 7) : 7;
@@ -1485,7 +1554,8 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   const int d_eng = k16d ? kK16 : (df == EPQ_Q4_K && tc_ok ? kTC : kCC);
   int g_eng = k16g ? kK16 : (gf == EPQ_Q4_K && tc_ok ? kTC : kCC);
   if (g_eng == kTC && d_eng == kCC) g_eng = kCC;
-  if ((g_eng == kK16 || d_eng == kK16) && ntok > 2) return EPQ_ERR_SHAPE;
+  if ((g_eng == kK16 || d_eng == kK16) && ntok > 2 && (stages & (EPQ_MOE_GATE_UP | EPQ_MOE_DOWN)))
+    return EPQ_ERR_SHAPE;
 
   if (stages & EPQ_MOE_GATE_UP) {
     if (g_eng == kK16) {
@@ -1558,6 +1628,8 @@ extern "C" epq_status epq_moe_forward(const epq_router *router, const epq_expert
   }
   return EPQ_OK;
 }
+
+}  // namespace
 
 // ------------------------------------------------------------------ fixed-scratch variant
 // A copy of the MoE workspace that lives in a file-scope device array instead

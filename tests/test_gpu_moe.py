@@ -169,7 +169,9 @@ def test_moe_parity(epq_lib, cuda_dev, case):
 
 
 # Q4_K with one or two tokens runs on the tensor-core expert kernels unless
-# the CUDA-core engines are forced: both against the oracle.
+# the CUDA-core engines are forced: both against the oracle.  Calls of more
+# tokens route every token once, then run the expert stages in chunks of
+# two (the logits, h and top-K outputs of every chunk checked).
 TC_CASES = [
     # fmt, E, H, I, topk, ntok, shared, gate_vec, bias, norm, rms
     (oracle.Q4_K, 16, 1024, 512, 4, 1, True, True, True, True, 1e-6),
@@ -177,6 +179,9 @@ TC_CASES = [
     (oracle.Q4_K, 12, 1280, 768, 3, 2, True, False, False, False, 1e-5),  # 5 superblocks of x, 3 per h
     (oracle.Q4_K, 6, 256, 256, 6, 2, False, False, False, True, None),    # every expert chosen, no shared
     (oracle.Q4_K, 40, 4096, 256, 2, 1, True, False, False, True, None),   # slot boundaries inside stages
+    # token chunks after one router launch for every token
+    (oracle.Q4_K, 16, 1024, 512, 4, 5, True, True, True, True, 1e-6),
+    (oracle.Q4_K, 40, 4096, 256, 2, 8, True, False, False, True, None),
 ]
 
 
