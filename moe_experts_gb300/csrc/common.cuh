@@ -218,6 +218,12 @@ __device__ __forceinline__ float warp_max_all(float v) {
   return v;
 }
 
+// Largest of the warp's non-negative values (NaN counts as 0) in one
+// redux.sync: non-negative floats order like their bit patterns.
+__device__ __forceinline__ float warp_absmax(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(v, 0.0f))));
+}
+
 __device__ __forceinline__ float warp_min_all(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 2 : 1) gemv_k16_kernel(con
   float *ps_s = reinterpret_cast<float *>(smem + L.ps);
   float *xsum_s = reinterpret_cast<float *>(smem + L.xsum);
   // a warp stages units warp, warp + 8, ...; the x loads of kStageBatch
-  // units are issued before any of them is converted
+  // units are issued before any of them is converted, and their warp
+  // maxima are reduced back to back before the conversions
   constexpr int kStageBatch = 4;
   const int nunits = NV * p.nsb;
   for (int u0 = warp; u0 < nunits; u0 += kWarps * kStageBatch) {
@@ -160,6 +161,9 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 2 : 1) gemv_k16_kernel(con
         for (int e = 0; e < 8; ++e) xv[k][e] = 0.0f;
       }
     }
+    float mx[kStageBatch];
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) mx[k] = warp_absmax(k16::lane_absmax(xv[k]));
 #pragma unroll
     for (int k = 0; k < kStageBatch; ++k) {
       const int u = u0 + kWarps * k;
@@ -175,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, NV <= 2 ? 2 : 1) gemv_k16_kernel(con
       }
       uint8_t *frag_sb = smem + L.frag + static_cast<uint32_t>(v * p.nsb + b) * k16::kSbFragBytes;
       const int ex = FMT == EPQ_Q4_K
-                         ? k16::stage_superblock_q4k(xv[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16)
-                         : k16::stage_superblock(xv[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
+                         ? k16::stage_superblock_q4k(xv[k], mx[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16)
+                         : k16::stage_superblock(xv[k], mx[k], frag_sb, lane, xsum_s + (v * p.nsb + b) * 16);
       if (lane == 0) ps_s[v * p.nsb + b] = k16::sum_scale<FMT>(ex);
     }
   }

@@ -181,18 +181,15 @@ __device__ __forceinline__ void cl_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// One (vector column v, superblock) of x by one warp: lane l holds
-// positions 8l..8l+7 (word j = l % 8 of owner t' = l / 8).  Writes the B
+// One (vector column v, superblock) of x by one warp (m: the warp's largest
+// |x| of it): lane l holds positions 8l..8l+7 (word j = l % 8 of owner
+// t' = l / 8).  Writes the B
 // operands of MMAs 2j and 2j+1 for column v, the min-term operands and
 // 2^(e - 9) (offsets into the shared window, to every target of st);
 // returns the lane's sum of squares.
 template <int CL>
-__device__ __forceinline__ float vn_stage(const float (&xv)[8], const VnStore<CL> &st, uint32_t main_sb,
+__device__ __forceinline__ float vn_stage(const float (&xv)[8], float m, const VnStore<CL> &st, uint32_t main_sb,
                                           uint32_t min_sb, uint32_t ps_sb, int v, int lane) {
-  float m = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
-  m = warp_max_all(m);
   int ex = 0;
   if (m > 0.0f) ex = min(100, max(-100, static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127));
   const float f = exp2i(14 - ex);
@@ -322,12 +319,15 @@ __global__ void __launch_bounds__(kVnThreads, 1) gemv_vn_kernel(const VnParams p
           for (int e = 0; e < 8; ++e) xv[k][e] = 0.0f;
         }
       }
+      float mx[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) mx[k] = warp_absmax(k16::lane_absmax(xv[k]));
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int u = static_cast<int>(rank) + CL * (l0 + kVnWarps * k);
         if (u >= nunits) break;  // warp-uniform
         const int v = u / nb, bl = u - v * nb;
-        const float sq = vn_stage<CL>(xv[k], st, L.main + bl * kVnSbMain, L.minb + bl * kVnSbMin,
+        const float sq = vn_stage<CL>(xv[k], mx[k], st, L.main + bl * kVnSbMain, L.minb + bl * kVnSbMin,
                                       L.ps + bl * 32, v, lane);
         if (p.rms) {
           const float s = warp_sum_xor<32>(sq);

@@ -367,7 +367,18 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
 }
 
 // ------------------------------------------------------------------ x staging
-// One warp converts one (vector, superblock) of x: lane l holds positions
+// Largest |x| of a lane's 8 values, and of the warp's 256 (one redux.sync;
+// callers reduce several units' maxima back to back so that their latencies
+// overlap).
+__device__ __forceinline__ float lane_absmax(const float (&xv)[8]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
+  return m;
+}
+
+// One warp converts one (vector, superblock) of x (m: the warp's largest
+// |x| of it, the same on every lane): lane l holds positions
 // 8h..8h+7 (h = l & 1) of sub-block s = l >> 1, already gathered into xv.
 // With e the exponent of the superblock's largest |x| (clamped to
 // [-100, 100]), the class-A slots get x * 2^(14 - e) and the class-B slots
@@ -375,11 +386,8 @@ __device__ __forceinline__ void superblock(const RowOps<FMT> &lo, const RowOps<F
 // value lands in [2^14, 2^15)).  Writes the operand slots of sub-block s,
 // the zero slots (lanes of owner 0) and the sub-block's sum of x into
 // sum16[s]; returns e (same on every lane).
-__device__ __forceinline__ int stage_superblock(const float (&xv)[8], uint8_t *frag_sb, int lane, float *sum16) {
-  float m = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
-  m = warp_max_all(m);
+__device__ __forceinline__ int stage_superblock(const float (&xv)[8], float m, uint8_t *frag_sb, int lane,
+                                                float *sum16) {
   int ex = 0;
   if (m > 0.0f) ex = min(100, max(-100, static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127));
   const int s = lane >> 1, h = lane & 1, q = s & 3, o = s >> 2;
@@ -415,11 +423,8 @@ __device__ __forceinline__ int stage_superblock(const float (&xv)[8], uint8_t *f
 // i = l & 3 of sub-block s = l >> 2 (owner s >> 1, group s & 1), which feed
 // MMAs 2i (pairs (0,4), (1,5)) and 2i+1 (pairs (2,6), (3,7)) of the group.
 // Same scales as stage_superblock; sum8[s] receives the sub-block's sum of x.
-__device__ __forceinline__ int stage_superblock_q4k(const float (&xv)[8], uint8_t *frag_sb, int lane, float *sum8) {
-  float m = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[e]));
-  m = warp_max_all(m);
+__device__ __forceinline__ int stage_superblock_q4k(const float (&xv)[8], float m, uint8_t *frag_sb, int lane,
+                                                    float *sum8) {
   int ex = 0;
   if (m > 0.0f) ex = min(100, max(-100, static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127));
   const int s = lane >> 2, i = lane & 3, q = s & 1, o = s >> 1;

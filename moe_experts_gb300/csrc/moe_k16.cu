@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_gateup_kernel(const MkPa
       for (int e = 0; e < 8; ++e) xv[e] = 0.0f;
     }
     uint8_t *fr = smem + p.frag_off + static_cast<uint32_t>(v * nsb + b) * k16::kSbFragBytes;
-    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, fr, lane, xsum_s + (v * nsb + b) * 16)
-                                   : k16::stage_superblock(xv, fr, lane, xsum_s + (v * nsb + b) * 16);
+    const float mx = warp_absmax(k16::lane_absmax(xv));
+    const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv, mx, fr, lane, xsum_s + (v * nsb + b) * 16)
+                                   : k16::stage_superblock(xv, mx, fr, lane, xsum_s + (v * nsb + b) * 16);
     if (lane == 0) ps_s[v * nsb + b] = k16::sum_scale<FMT>(ex);
   }
   __syncthreads();
@@ -274,14 +275,18 @@ __global__ void __launch_bounds__(kKThreads, 1) moe_k16_down_kernel(const MkPara
         for (int e = 0; e < 8; ++e) xv[j][e] = 0.0f;
       }
     }
+    float mx[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) mx[j] = warp_absmax(k16::lane_absmax(xv[j]));
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int u = u0 + kKWarps * j;
       if (u >= nunits) break;  // warp-uniform
       const int v = u / nvsb, b = u - v * nvsb;
       uint8_t *fr = smem + p.frag_off + static_cast<uint32_t>(v * p.nsbx + b) * k16::kSbFragBytes;
-      const int ex = FMT == EPQ_Q4_K ? k16::stage_superblock_q4k(xv[j], fr, lane, xsum_s + (v * p.nsbx + b) * 16)
-                                     : k16::stage_superblock(xv[j], fr, lane, xsum_s + (v * p.nsbx + b) * 16);
+      const int ex = FMT == EPQ_Q4_K
+                         ? k16::stage_superblock_q4k(xv[j], mx[j], fr, lane, xsum_s + (v * p.nsbx + b) * 16)
+                         : k16::stage_superblock(xv[j], mx[j], fr, lane, xsum_s + (v * p.nsbx + b) * 16);
       if (lane == 0) ps_s[v * p.nsbx + b] = k16::sum_scale<FMT>(ex);
     }
   }
