@@ -249,6 +249,93 @@ __device__ void select_topk(const MoeArgs &a, Meta &m, uint32_t *scratch, bool p
   }
 }
 
+// Softmax + top-K of a single token by one warp (the calling warp; ntok ==
+// 1), the same rule as select_topk -- larger logit first, equal logits to
+// the lower expert, weights exp(l - max) / sum_e exp(l_e - max), renormalised
+// over the chosen when norm_topk -- in one pass: lane l holds the logits of
+// experts l, l + 32, ...; round r takes the warp's largest key with one
+// redux.sync max and the lowest expert holding it with one redux.sync min.
+// Writes m.idx, m.w (and the caller's outputs when `publish`).
+template <int kPer>
+__device__ void select_single_n(const MoeArgs &a, Meta &m, bool publish, int lane) {
+  const int E = a.E, K = a.topk;
+  unsigned key[kPer];  // 0: absent or taken
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = j * 32 + lane;
+    key[j] = 0u;
+    if (j * 32 < E && e < E) key[j] = max(order_key(__ldcg(a.logits + e)), 1u);
+  }
+  unsigned kl = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) kl = max(kl, key[j]);
+  const float mx = key_value(__reduce_max_sync(0xffffffffu, kl));
+  float den = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) den += key[j] != 0u ? expf(key_value(key[j]) - mx) : 0.0f;
+  den = warp_sum_xor<32>(den);
+  int sel_e = 0;
+  unsigned sel_k = 0u;
+#pragma unroll 1
+  for (int r = 0; r < K; ++r) {
+    // the lane's largest key by a tree of adjacent pairs (log2 kPer levels
+    // instead of a chain of kPer compares): slot j of level w holds the best
+    // of keys [j, j + 2w), and on equal keys the left, lower expert wins
+    unsigned tk[kPer];
+    int tj[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      tk[j] = key[j];
+      tj[j] = j;
+    }
+#pragma unroll
+    for (int w = 1; w < kPer; w <<= 1)
+#pragma unroll
+      for (int j = 0; j + w < kPer; j += 2 * w) {
+        const bool right = tk[j + w] > tk[j];
+        tk[j] = right ? tk[j + w] : tk[j];
+        tj[j] = right ? tj[j + w] : tj[j];
+      }
+    const unsigned lb = tk[0];
+    const int lj = tj[0];
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, lb);
+    const unsigned cand = kmax != 0u && lb == kmax ? static_cast<unsigned>(lj * 32 + lane) : 0xffffffffu;
+    const unsigned emin = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == static_cast<int>(emin & 31u)) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (j == static_cast<int>(emin >> 5)) key[j] = 0u;  // constant indices keep key in registers
+    }
+    if (lane == r) {
+      sel_e = static_cast<int>(emin);
+      sel_k = kmax;
+    }
+  }
+  const float p = lane < K ? __fdiv_rn(expf(key_value(sel_k) - mx), den) : 0.0f;
+  const float sel_sum = warp_sum_xor<32>(p);
+  if (lane < K) {
+    const float wk = a.norm_topk ? __fdiv_rn(p, sel_sum) : p;
+    m.idx[lane] = sel_e;
+    m.w[lane] = wk;
+    if (publish) {
+      a.idx[lane] = sel_e;
+      a.w[lane] = wk;
+      if (a.out_idx) a.out_idx[lane] = sel_e;
+      if (a.out_w) a.out_w[lane] = wk;
+    }
+  }
+}
+
+// The per-lane key count fixed by E (up to 64, 128, ... 1024 experts), so
+// that every loop over a lane's keys unrolls and the keys stay in registers.
+__device__ void select_single(const MoeArgs &a, Meta &m, bool publish, int lane) {
+  if (a.E <= 64) select_single_n<2>(a, m, publish, lane);
+  else if (a.E <= 128) select_single_n<4>(a, m, publish, lane);
+  else if (a.E <= 256) select_single_n<8>(a, m, publish, lane);
+  else if (a.E <= 512) select_single_n<16>(a, m, publish, lane);
+  else select_single_n<32>(a, m, publish, lane);
+}
+
 // What the down kernel reads of the routing, from the CTA's copy.
 __device__ void publish_routing(const MoeArgs &a, const Meta &m, int tid, int nthr) {
   const int nact = *m.nact, nslots = *m.nslots;
@@ -284,8 +371,12 @@ __device__ void route_tokens(const MoeArgs &a, Meta &m, uint32_t *scratch, bool 
     tr = __ldcg(a.xstat + 2 * tid + 1);
     tx = __ldcg(a.xstat + 2 * tid);
   }
-  select_topk(a, m, scratch, publish);
-  const int rwarp = nwarps - 1 - warp;  // rwarp 0 ran token 0's softmax
+  const int rwarp = nwarps - 1 - warp;  // rwarp 0 runs token 0's softmax
+  if (a.ntok == 1) {
+    if (rwarp == 0) select_single(a, m, publish, lane);  // the other warps go straight to the barrier below
+  } else {
+    select_topk(a, m, scratch, publish);
+  }
   if (tid < a.ntok) {
     m.gs[tid] = tg;
     m.rms[tid] = tr;
@@ -294,7 +385,8 @@ __device__ void route_tokens(const MoeArgs &a, Meta &m, uint32_t *scratch, bool 
   if (a.ntok == 1) {
     // one token: its topk distinct experts are the slots, in ascending
     // order (rank among the chosen), one entry each
-    if (rwarp == 0) {  // m.w of token 0 is this warp's own write
+    if (rwarp == 0) {  // m.idx / m.w of token 0 are this warp's own writes
+      __syncwarp();
       const int e = lane < a.topk ? m.idx[lane] : 0x7fffffff;
       int rank = 0;
 #pragma unroll 1

@@ -311,9 +311,15 @@ __global__ void __launch_bounds__(kMtThreads, 1) moe_gateup_tc_kernel(const MtPa
       d += n;
     }
   };
-  if (tid == 0 && nst > 0) {
+  // The first stage's copies go out at once; the other free slots are
+  // filled by warps 1, 2, ... right after their own x conversion: issuing
+  // ~100 KB of copies stalls the issuing thread for microseconds while
+  // every SM's requests drain, and one thread issuing them all delayed its
+  // warp's conversion, which the staging release below waits for.
+  const int first_n = min(p.stages - L.held, nst);
+  if (tid == 0 && first_n > 0) {
     fence_proxy_async();  // the routing scratch writes precede the copies into the ring
-    for (int i = 0; i < min(p.stages - L.held, nst); ++i) issue(i);
+    issue(0);
   }
 
   float *gxsum = xsum + grp * nsb * 16;
@@ -327,6 +333,14 @@ __global__ void __launch_bounds__(kMtThreads, 1) moe_gateup_tc_kernel(const MtPa
         if (kq + i * KP >= nsb) xr[i][0][0] = xr[i][0][1] = xr[i][1][0] = xr[i][1][1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     convert_x<KP, NSB, FULL>(xr, a.ntok, kq, nsb, lane, cv, frag, gxsum, bq, fsc);
+  }
+  if (lane == 0) {
+    bool fenced = false;
+    for (int i = warp == 0 ? kMtWarps : warp; i < first_n; i += kMtWarps) {
+      if (!fenced) fence_proxy_async();
+      fenced = true;
+      issue(i);
+    }
   }
   release_held(L, p.stages, nst, cnt, lane, tid, a.err, issue);
 
@@ -449,8 +463,10 @@ __global__ void __launch_bounds__(kMtThreads, 1) moe_down_tc_kernel(const MtPara
       bulk_g2s(dst + static_cast<uint32_t>(sl) * seg, base + r0 * rbytes, bytes, &full[s]);
     }
   };
-  if (tid == 0)
-    for (int i = 0; i < min(p.stages - L.held, nst); ++i) issue(i);
+  // first stage now, the other free slots by warps 1, 2, ... after their
+  // conversion (as in the gate/up kernel)
+  const int first_n = min(p.stages - L.held, nst);
+  if (tid == 0 && first_n > 0) issue(0);
 
   const int g = lane >> 2, t = lane & 3, cv = t & 1;
   const int kq = warp % KP, grp = warp / KP;
@@ -494,6 +510,8 @@ __global__ void __launch_bounds__(kMtThreads, 1) moe_down_tc_kernel(const MtPara
     uint2 *frag = reinterpret_cast<uint2 *>(smem + L.frag) + warp * (kFragWarpBytes / 8);
     convert_x<KP, NSB, false>(xr, a.ntok, kq, nsb, lane, cv, frag, gxsum, bq, fsc);
   }
+  if (lane == 0)
+    for (int i = warp == 0 ? kMtWarps : warp; i < first_n; i += kMtWarps) issue(i);
   release_held(L, p.stages, nst, cnt, lane, tid, a.err, issue);
 
   const uint32_t csel = t == 0 ? 0x10u : (t == 1 ? 0x21u : (t == 2 ? 0x43u : 0x54u));
