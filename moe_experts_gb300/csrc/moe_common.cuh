@@ -326,14 +326,17 @@ __device__ void select_single_n(const MoeArgs &a, Meta &m, bool publish, int lan
   }
 }
 
-// The per-lane key count fixed by E (up to 64, 128, ... 1024 experts), so
+// The per-lane key count fixed by E (up to 64, 128 or 256 experts), so
 // that every loop over a lane's keys unrolls and the keys stay in registers.
+// Routers of more experts take select_topk: with 16+ keys per lane the
+// single warp's serial exponentials and scans were slower than the CTA-wide
+// selection (512 experts, top-4: 3.8 against 3.2 us per gate/up launch;
+// 256 experts, top-8: 3.3 against 3.8 us).
+constexpr int kSingleMaxExperts = 256;
 __device__ void select_single(const MoeArgs &a, Meta &m, bool publish, int lane) {
   if (a.E <= 64) select_single_n<2>(a, m, publish, lane);
   else if (a.E <= 128) select_single_n<4>(a, m, publish, lane);
-  else if (a.E <= 256) select_single_n<8>(a, m, publish, lane);
-  else if (a.E <= 512) select_single_n<16>(a, m, publish, lane);
-  else select_single_n<32>(a, m, publish, lane);
+  else select_single_n<8>(a, m, publish, lane);
 }
 
 // What the down kernel reads of the routing, from the CTA's copy.
@@ -372,7 +375,7 @@ __device__ void route_tokens(const MoeArgs &a, Meta &m, uint32_t *scratch, bool 
     tx = __ldcg(a.xstat + 2 * tid);
   }
   const int rwarp = nwarps - 1 - warp;  // rwarp 0 runs token 0's softmax
-  if (a.ntok == 1) {
+  if (a.ntok == 1 && a.E <= kSingleMaxExperts) {
     if (rwarp == 0) select_single(a, m, publish, lane);  // the other warps go straight to the barrier below
   } else {
     select_topk(a, m, scratch, publish);

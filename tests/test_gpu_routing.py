@@ -150,3 +150,28 @@ def _stage_split(epq_lib, cuda_dev, ntok):
     torch.cuda.synchronize()
     assert torch.equal(y0, y1)
     assert (idx >= 0).all() and (idx < E).all()
+
+
+@pytest.mark.parametrize("E,ties", [(200, (11, 40, 77, 190, 199)), (64, (0, 31, 32, 63)), (256, (5, 37, 69, 255))])
+def test_one_token_ties_go_to_lower_expert(epq_lib, cuda_dev, E, ties):
+    """One token (the single-warp selection for routers of up to 256
+    experts): bitwise-equal logits in different lanes and in the same lane
+    of the warp go to the lower expert, and an all-zero router selects
+    experts 0..K-1."""
+    H, topk = 512, len(ties)
+    R = synthetic.student_t((E, H), seed=E + 9).numpy()
+    for e in ties[1:]:
+        R[e] = R[ties[0]]
+    bias = np.zeros(E, np.float32)
+    bias[list(ties)] = 1e4
+    x = synthetic.normal((1, H), seed=E + 10).numpy()
+    layer = _layer(epq_lib, cuda_dev, E, H, 256, R, bias=bias)
+    for stages in (1, 0):
+        idx, w, logits, _ = _route(epq_lib, cuda_dev, layer, x, topk, stages)
+        assert idx.tolist() == [sorted(ties)]
+        assert np.allclose(w, 1.0 / topk, rtol=1e-6)
+    zero = _layer(epq_lib, cuda_dev, E, H, 256, np.zeros((E, H), np.float32), norm=False)
+    idx, w, _, _ = _route(epq_lib, cuda_dev, zero, x, 7, 0)
+    assert idx.tolist() == [list(range(7))]
+    assert np.allclose(w, 1.0 / E, rtol=1e-6)
+    assert epq_lib.epq_device_error() == 0
