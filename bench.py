@@ -26,7 +26,8 @@ the mean over the K bracketed steps plus the median and minimum of K
 individually timed replays, the roofline of the dominant kernel (its time
 per launch from a graph of back-to-back launches of that kernel alone on
 distinct weights, programmatic dependent launch as in the step), e2e (host
-buffers, H2D + D2H inside the timed region), clocks sampled during the timed
+buffers, H2D + D2H inside the timed region), clocks sampled every 100 ms
+while the step replays back to back before, during and after the timed
 region, gpu_launches, and the CPU baseline: the plain C++ oracle's float32
 dequant-GEMV at 1 thread and at all host threads (guided row split) on a
 bounded sample.  --impl reference times that oracle itself, one bounded
@@ -35,6 +36,7 @@ sample per step.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -70,16 +72,21 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms.  The
+    summary keeps the samples stamped inside the window between mark_start()
+    and mark_end() (all of them if the stamps cannot be read)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
+    INTERVAL_MS = 100
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t_start = None
+        self.t_end = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -87,7 +94,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.INTERVAL_MS)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
@@ -101,28 +108,56 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    @staticmethod
+    def _stamp(text):
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
+    def parse(self, lines):
+        """(sm MHz, max MHz, reasons, stamp or None) for each sample line."""
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        out = []
+        for line in lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, smax = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(names, f[5:9]) if v.lower() == "active"}
+            out.append((sm, smax, reasons, self._stamp(f[9]) if len(f) > 9 else None))
+        return out
+
     def summary(self):
-        sm, smax, reasons = [], [], set()
         try:
-            for line in open(self.path):
-                f = [v.strip() for v in line.split(",")]
-                if len(f) < 9:
-                    continue
-                try:
-                    sm.append(float(f[1]))
-                    smax.append(float(f[2]))
-                except ValueError:
-                    continue
-                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-                for n, v in zip(names, f[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+            rows = self.parse(open(self.path))
         except Exception:
-            pass
-        if not sm:
+            rows = []
+        window = None
+        if self.t_start is not None and self.t_end is not None and rows and all(r[3] is not None for r in rows):
+            inside = [r for r in rows if self.t_start <= r[3] <= self.t_end]
+            if inside:
+                rows, window = inside, round(self.t_end - self.t_start, 3)
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+               "reasons": sorted(set().union(*(r[2] for r in rows))), "samples": len(rows)}
+        if window is not None:
+            out["window_s"] = window
+            out["sampled"] = (f"every {self.INTERVAL_MS} ms while the GPU replayed the step back to back "
+                              "before, during and after the timed region")
+        return out
 
 
 def dist_env():
@@ -919,13 +954,23 @@ def run_epq(args):
     else:
         g = graph_of(torch, stream, W.step)
         replay = g.replay
+    t_warm = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             replay()
     torch.cuda.synchronize()
+    t_warm = (time.perf_counter() - t_warm) / max(3, args.warmup)
+    # the clock record spans ~0.6 s of untimed back-to-back replays on each
+    # side of the timed ones, so that its samples see the GPU under the load
+    # of the timed region
+    n_load = int(min(5000, max(1, 0.6 / max(t_warm, 1e-6))))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        clk.mark_start()
+        with torch.cuda.stream(stream):
+            for _ in range(n_load):
+                replay()
         barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):  # replays and events on one stream
@@ -935,6 +980,11 @@ def run_epq(args):
             e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(n_load):
+                replay()
+        torch.cuda.synchronize()
+        clk.mark_end()
         barrier()
         clocks = clk.summary()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
