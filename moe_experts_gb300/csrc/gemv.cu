@@ -692,8 +692,9 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
   // tensor-core engine (gemv_k16.cu), measured faster than the ring engine
   // below on every matrix of the 8B-class decode step with one vector
   // (1.681 -> 1.459 ms per step) and slower with two (1.748 -> 2.046 ms),
-  // where the ring engine's two-vector operands pay.  Two or more Q4_K
-  // vectors keep the ring engine (one pass for up to eight).
+  // where the ring engine's two-vector operands pay.  Two to four Q4_K
+  // vectors keep the ring engine (one pass for 3..8 vectors on 4096-column
+  // rows, else two vectors per pass).
   const int eng0 = tune_gemv_engine();
   // Q4_K with several vectors: the vector-column engine (gemv_vn.cu, one
   // weight pass for up to 8 vectors on every shape) from 5 vectors on, where
