@@ -25,9 +25,13 @@ reference values are float64.
 Pins (tests/test_oracle_*.py): the page's printed relative errors, closed-form
 bits/weight, the EPM expert byte sizes, hand-built blocks with exact expected
 bytes, brute-force nearest-code checks, brute-force float64 matvec and
-top-K-by-sort on tiny shapes, and MoE special cases.  Parity unpinned: the
-renormalisation of the top-K weights and the magnitude of MoE outputs have no
-printed value; both follow the definitions in ``oracle.moe``.
+top-K-by-sort on tiny shapes, and closed forms for every MoE and attention
+step (router logits with a bias, softmax, the combine with and without
+renormalising the top-K weights, the sigmoid shared gate, an expert built
+from diagonal matrices, the pre-norm).  The pages print no numeric MoE
+output, so those pins are closed forms rather than printed values; whether
+the top-K weights are renormalised is a reading of the pages (both variants
+are pinned and the library takes either).
 """
 from .formats import (  # noqa: F401
     Q8_0, Q4_0, Q4_1, Q4_K, Q2_K, Q6_K, FORMATS, BLOCK_WEIGHTS, BLOCK_BYTES,

@@ -100,6 +100,20 @@ def test_softmax_and_combine_weights():
     assert np.allclose(w4, np.sort(p, 1)[:, ::-1][:, :4])
 
 
+def test_router_logits_closed_form():
+    """R is a non-square shifted identity (row e picks column e + 1), so the
+    logits are x[e + 1] + bias[e]: a transposed R, a dropped or negated bias
+    or a wrong shift gives other numbers."""
+    E, H = 3, 5
+    R = np.zeros((E, H), np.float32)
+    for e in range(E):
+        R[e, e + 1] = 1.0
+    x = np.array([[1.0, 2.0, 3.0, 4.0, 5.0], [-1.0, 0.5, -0.25, 8.0, 0.0]], np.float32)
+    bias = np.array([10.0, -1.0, 0.5], np.float32)
+    assert oracle.router_logits_f64(R, x).tolist() == [[2.0, 3.0, 4.0], [0.5, -0.25, 8.0]]
+    assert oracle.router_logits_f64(R, x, bias).tolist() == [[12.0, 2.0, 4.5], [10.5, -1.25, 8.5]]
+
+
 def test_rmsnorm_closed_form():
     x = np.array([[3.0, 4.0]])
     # mean of squares 12.5
@@ -260,3 +274,15 @@ def test_moe_combine_and_sigmoid_gate_closed_form():
         y = x.astype(np.float64) + sum(wk * expert(k) for k, wk in enumerate(w)) + 0.5 * expert("s")
         assert np.allclose(r.y[0], y, rtol=1e-13, atol=1e-15)
     assert abs(p0 - 0.75) < 1e-7
+    # a router bias of (0, ln 9) lifts expert 1 over expert 0: logits
+    # (ln 3, ln 9), order [1, 0], weights 9/12 and 3/12
+    mw.router_bias = np.array([0.0, np.log(9.0)], np.float32)
+    mw.norm_topk = True
+    lb = float(np.float32(np.log(9.0)))
+    q1 = np.exp(lb) / (np.exp(lb) + np.exp(lnw))
+    r = oracle.moe_forward_f64(mw, x[None], 2)
+    assert r.idx[0].tolist() == [1, 0]
+    assert np.allclose(r.w[0], (q1, 1 - q1), rtol=1e-15, atol=0)
+    assert abs(q1 - 0.75) < 1e-7
+    y = x.astype(np.float64) + q1 * expert(1) + (1 - q1) * expert(0) + 0.5 * expert("s")
+    assert np.allclose(r.y[0], y, rtol=1e-13, atol=1e-15)
