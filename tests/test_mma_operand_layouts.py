@@ -21,6 +21,13 @@ fails by orders of magnitude.
   HMUL2 folds the sub-block scale into the code operand (c n 2^-14 for both
   code classes); the min term is one more MMA pair with the min codes as A
   and the sub-block sums of x as B.
+* ring engine (one or two vectors; also the MoE expert kernels): the 16 A
+  rows are 8 weight rows x two halves of each code word (nibble positions
+  0, 4, 2, 6 and 1, 5, 3, 7), lane (g, t) owns sub-blocks 2t, 2t+1 with the
+  scale folded in by HMUL2; the 8 B columns are (half, vector, hi/lo), the
+  x of a superblock scaled by 2^(15 - E) for |x| < 2^E; lanes t < 2 keep
+  half 0 and t >= 2 half 1 of vector t & 1, and the min term is added per
+  lane in float32 from the sub-block sums of x.
 """
 import numpy as np
 
@@ -192,6 +199,59 @@ def _vector_column(packed, x, nsb):
     return out[:, :nv]
 
 
+def _bound_exponent(amax):
+    """E with |x| < 2^E from the float32 exponent field (zero reads as the
+    smallest normal binade)."""
+    eb = int(np.array([amax], np.float32).view(np.uint32)[0] >> 23) & 0xFF
+    return max(eb, 1) - 126
+
+
+def _ring(packed, x, nsb):
+    """One or two vectors through the ring engine's layout, 8 rows -> [8][nv]."""
+    nv = x.shape[0]
+    out = np.zeros((8, nv))
+    for sb in range(nsb):
+        xs = x[:, 256 * sb:256 * (sb + 1)].astype(np.float32)
+        q, fs, X = [], [], []
+        for v in range(nv):
+            sig = min(126, max(-112, 15 - _bound_exponent(float(np.max(np.abs(xs[v]))))))
+            q.append(xs[v] * np.float32(2.0 ** sig))
+            fs.append(2.0 ** (14 - sig))
+            X.append([float(np.sum(xs[v, 32 * s_:32 * s_ + 32], dtype=np.float32)) for s_ in range(8)])
+        fields = [_superblock_fields(packed[r], sb) for r in range(8)]
+        C = np.zeros((16, 8))
+        for j in range(8):
+            a_regs, b_regs = [], []
+            for lane in range(32):
+                g, t = lane >> 2, lane & 3
+                _, _, c, _, words = fields[g]
+                code = c[2 * t + (j >> 2)]
+                mlo, mhi = _pack(code * 1024.0, code * 1024.0), _pack(code * 64.0, code * 64.0)
+                w = words[t][j]
+                a_regs.append((_hmul2(w & NIB_A, mlo), _hmul2(w & NIB_B, mhi),
+                               _hmul2((w >> 8) & NIB_A, mlo), _hmul2((w >> 8) & NIB_B, mhi)))
+                # B column g = (half h, vector v, lo): x of sub-block 2t + j/4,
+                # word j % 4, at the positions of half h
+                h, v, lo = g >> 2, (g >> 1) & 1, g & 1
+                if v >= nv:
+                    b_regs.append((0, 0))
+                    continue
+                base = 32 * (2 * t + (j >> 2)) + 8 * (j & 3)
+                qv = q[v][base:base + 8]
+                b_regs.append((_split(qv[h], qv[h + 4])[lo], _split(qv[h + 2], qv[h + 6])[lo]))
+            C += _mma(a_regs, b_regs)
+        for lane in range(32):
+            g, t = lane >> 2, lane & 3
+            d, dmin, _, m, _ = fields[g]
+            cv = t & 1
+            s_ = C[g, 2 * t] + C[g, 2 * t + 1] if t < 2 else C[g + 8, 2 * t] + C[g + 8, 2 * t + 1]
+            if cv < nv:
+                out[g, cv] += d * s_ * fs[cv]
+            for v in range(nv):
+                out[g, v] -= dmin * (m[2 * t] * X[v][2 * t] + m[2 * t + 1] * X[v][2 * t + 1])
+    return out
+
+
 def _case(seed, nsb, nv, spread):
     W = synthetic.student_t((16, 256 * nsb), seed=seed).numpy()
     packed = oracle.quantize(oracle.Q4_K, W)
@@ -219,6 +279,32 @@ def test_vector_column_layout_matches_oracle():
         packed, x = _case(seed, nsb, nv, spread)
         got = _vector_column(packed, x, nsb)
         _assert_close(got.T, packed, x, 256 * nsb)
+
+
+def test_ring_layout_matches_oracle():
+    for seed, nsb, nv, spread in ((15, 1, 1, 0.0), (17, 2, 2, 3.0), (19, 3, 2, 0.0)):
+        packed, x = _case(seed, nsb, nv, spread)
+        packed = packed[:8]
+        got = _ring(packed, x, nsb)
+        _assert_close(got.T, packed, x, 256 * nsb)
+
+
+def test_ring_layout_model_catches_a_wrong_nibble_mask():
+    """The odd nibble positions (A registers 1 and 3) read through the even
+    positions' mask, a plausible slip, breaks the match by far more than
+    the bound."""
+    packed, x = _case(21, 1, 2, 0.0)
+    packed = packed[:8]
+    ref = oracle.gemv_f64(oracle.Q4_K, packed, x, 256)
+    bound = oracle.gemv_bound(oracle.Q4_K, packed, x, 256)
+    global NIB_B
+    saved = NIB_B
+    try:
+        NIB_B = NIB_A  # odd nibble positions read the even ones
+        bad = _ring(packed, x, 1).T
+    finally:
+        NIB_B = saved
+    assert (np.abs(bad - ref) > 1e-3 * bound).any()
 
 
 def test_layout_models_catch_a_wrong_slot():
