@@ -38,6 +38,33 @@ def test_gemv_brute_force(fmt):
             assert A[v, i] == pytest.approx(a, rel=1e-12)
 
 
+@pytest.mark.parametrize("fmt", oracle.FORMATS)
+def test_gemv_against_exact_rational_sum(fmt):
+    """Both float64 GEMV oracles (numpy and C++) against the exact sum in
+    rational arithmetic: the dequantized float32 weights and a dyadic x are
+    exact as fractions, so the float64 results may differ from the exact
+    value only by float64 summation error (n * 2^-53 of sum |w x|)."""
+    from fractions import Fraction
+
+    from oracle import cref
+    rng = np.random.default_rng(40 + fmt)
+    cols = 512
+    W = _rand_w(rng, 3, cols)
+    x = (rng.integers(-64, 65, (2, cols)) * 2.0 ** -5).astype(np.float32)
+    p = oracle.quantize(fmt, W)
+    deq = oracle.dequantize(fmt, p, cols)
+    y_np = oracle.gemv_f64(fmt, p, x, cols)
+    y_c, _ = cref.gemv_f64(fmt, p, x, cols)
+    for v in range(2):
+        for i in range(3):
+            terms = [Fraction(float(deq[i, j])) * Fraction(float(x[v, j])) for j in range(cols)]
+            exact = sum(terms, Fraction(0))
+            A = float(sum(abs(t) for t in terms))
+            tol = cols * 2.0 ** -53 * A
+            assert abs(Fraction(float(y_np[v, i])) - exact) <= Fraction(tol), (fmt, v, i)
+            assert abs(Fraction(float(y_c[v, i])) - exact) <= Fraction(tol), (fmt, v, i)
+
+
 def test_gemv_one_hot_gives_column():
     rng = np.random.default_rng(1)
     W = _rand_w(rng, 5, 512)
