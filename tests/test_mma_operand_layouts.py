@@ -21,6 +21,13 @@ fails by orders of magnitude.
   HMUL2 folds the sub-block scale into the code operand (c n 2^-14 for both
   code classes); the min term is one more MMA pair with the min codes as A
   and the sub-block sums of x as B.
+* block-diagonal engine for the 16-weight sub-block K-quants (Q2_K, Q6_K),
+  read from their planar rows: a sub-block's 2-bit fields (Q2_K codes,
+  Q6_K high parts) sit at bit kField[i] of one word, and W, W >> 2,
+  rotr(W, 24), rotr(W, 24) >> 2 masked with 0x00300030 / 0x03000300 give
+  positions (0,4)(1,5) | (2,6)(3,7) | (8,12)(9,13) | (10,14)(11,15) as fp16
+  subnormals (Q6_K ORs in its low nibbles); lane t owns sub-block 4t + q of
+  group q.
 * ring engine (one or two vectors; also the MoE expert kernels): the 16 A
   rows are 8 weight rows x two halves of each code word (nibble positions
   0, 4, 2, 6 and 1, 5, 3, 7), lane (g, t) owns sub-blocks 2t, 2t+1 with the
@@ -30,6 +37,7 @@ fails by orders of magnitude.
   lane in float32 from the sub-block sums of x.
 """
 import numpy as np
+import pytest
 
 import oracle
 import synthetic
@@ -199,6 +207,86 @@ def _vector_column(packed, x, nsb):
     return out[:, :nv]
 
 
+KFIELD = [4, 8, 6, 10, 20, 24, 22, 26, 28, 0, 30, 2, 12, 16, 14, 18]
+MASK_A, MASK_B = 0x00300030, 0x03000300
+# x positions of MMA i in k-slots (2t, 2t+1) (class A) and (2t+8, 2t+9) (class B)
+K16_POS = [(0, 4, 1, 5), (2, 6, 3, 7), (8, 12, 9, 13), (10, 14, 11, 15)]
+
+
+def _rotr(w, s_):
+    return ((w >> s_) | (w << (32 - s_))) & 0xFFFFFFFF
+
+
+def _u32(b, off):
+    return int.from_bytes(bytes(b[off:off + 4]), "little")
+
+
+def _k16_subblock(fmt, row, nsb, sb, s_):
+    """Planar row -> (code word W, nibble words (Q6_K) or None, scale code,
+    min-term code, d, min-term factor) of sub-block s_ of superblock sb."""
+    if fmt == oracle.Q2_K:
+        W = _u32(row, 64 * sb + 4 * s_)
+        sub = int(row[64 * nsb + 16 * sb + s_])
+        fac = row[80 * nsb + 4 * sb:80 * nsb + 4 * sb + 4]
+        d, dmin = (float(v) for v in np.frombuffer(bytes(fac), np.float16))
+        return W, None, sub & 15, sub >> 4, d, dmin
+    W = _u32(row, 128 * nsb + 64 * sb + 4 * s_)
+    nib = (_u32(row, 128 * sb + 8 * s_), _u32(row, 128 * sb + 8 * s_ + 4))
+    c = int(np.frombuffer(bytes(row[192 * nsb + 16 * sb + s_:192 * nsb + 16 * sb + s_ + 1]), np.int8)[0])
+    d = float(np.frombuffer(bytes(row[208 * nsb + 2 * sb:208 * nsb + 2 * sb + 2]), np.float16)[0])
+    # w = d c (u - 32): the offset term is 32 d times c sum(x)
+    return W, nib, c, c, d, 32.0 * d
+
+
+def _k16_pairs(fmt, W, nib, i):
+    """Class-A and class-B fp16 pairs of MMA i from the masked words."""
+    base = [W, W >> 2, _rotr(W, 24), _rotr(W, 24) >> 2][i]
+    if fmt == oracle.Q2_K:
+        return base & MASK_A, base & MASK_B
+    n = [nib[0], nib[0] >> 8, nib[1], nib[1] >> 8][i]
+    return (n & NIB_A) | (base & MASK_A), (n & NIB_B) | (base & MASK_B)
+
+
+def _block_diagonal_k16(fmt, packed, x, nsb):
+    """One vector of a Q2_K / Q6_K matrix through the block-diagonal layout,
+    16 rows."""
+    out = np.zeros(16)
+    for sb in range(nsb):
+        xs = x[256 * sb:256 * (sb + 1)].astype(np.float32)
+        e = _exponent(xs)
+        fA, fB = np.float32(2.0 ** (14 - e)), np.float32(2.0 ** (10 - e))
+        ps = 2.0 ** ((6 if fmt == oracle.Q2_K else 10) + e)
+        cs, ms = np.zeros(16), np.zeros(16)
+        for q in range(4):
+            fields = {(r, t): _k16_subblock(fmt, packed[r], nsb, sb, 4 * t + q) for r in range(16) for t in range(4)}
+            C = np.zeros((16, 8))
+            for i in range(4):
+                pa0, pa1, pb0, pb1 = K16_POS[i]
+                a_regs, b_regs = [], []
+                for lane in range(32):
+                    g, t = lane >> 2, lane & 3
+                    lo, hi = _k16_pairs(fmt, *fields[(g, t)][:2], i), _k16_pairs(fmt, *fields[(g + 8, t)][:2], i)
+                    a_regs.append((lo[0], hi[0], lo[1], hi[1]))
+                    if (g >> 1) != t:  # column of another owner: the zero slot
+                        b_regs.append((0, 0))
+                        continue
+                    v = xs[16 * (4 * t + q):16 * (4 * t + q) + 16]
+                    part = g & 1
+                    b_regs.append((_split(v[pa0] * fA, v[pa1] * fA)[part], _split(v[pb0] * fB, v[pb1] * fB)[part]))
+                C += _mma(a_regs, b_regs)
+            for lane in range(32):
+                g, t = lane >> 2, lane & 3
+                X = float(np.sum(xs[16 * (4 * t + q):16 * (4 * t + q) + 16], dtype=np.float32))
+                for r in (g, g + 8):
+                    _, _, c, k, _, _ = fields[(r, t)]
+                    cs[r] += c * (C[r, 2 * t] + C[r, 2 * t + 1])
+                    ms[r] += k * X
+        for r in range(16):
+            _, _, _, _, d, dmin = _k16_subblock(fmt, packed[r], nsb, sb, 0)
+            out[r] += d * ps * cs[r] - dmin * ms[r]
+    return out
+
+
 def _bound_exponent(amax):
     """E with |x| < 2^E from the float32 exponent field (zero reads as the
     smallest normal binade)."""
@@ -260,9 +348,9 @@ def _case(seed, nsb, nv, spread):
     return packed, x
 
 
-def _assert_close(got, packed, x, cols):
-    ref = oracle.gemv_f64(oracle.Q4_K, packed, x, cols)       # [nv][rows]
-    bound = oracle.gemv_bound(oracle.Q4_K, packed, x, cols)
+def _assert_close(got, packed, x, cols, fmt=oracle.Q4_K):
+    ref = oracle.gemv_f64(fmt, packed, x, cols)       # [nv][rows]
+    bound = oracle.gemv_bound(fmt, packed, x, cols)
     err = np.abs(got - ref)
     assert (err <= 1e-6 * bound + 1e-30).all(), (err / (bound + 1e-30)).max()
 
@@ -279,6 +367,47 @@ def test_vector_column_layout_matches_oracle():
         packed, x = _case(seed, nsb, nv, spread)
         got = _vector_column(packed, x, nsb)
         _assert_close(got.T, packed, x, 256 * nsb)
+
+
+@pytest.mark.parametrize("fmt", [oracle.Q2_K, oracle.Q6_K])
+def test_block_diagonal_k16_layout_matches_oracle(fmt):
+    for seed, nsb in ((23, 1), (25, 3)):
+        W = synthetic.student_t((16, 256 * nsb), seed=seed).numpy()
+        packed = oracle.quantize(fmt, W)
+        x = synthetic.normal((1, 256 * nsb), seed=seed + 1).numpy()
+        got = _block_diagonal_k16(fmt, packed, x[0], nsb)
+        _assert_close(got[None, :], packed, x, 256 * nsb, fmt)
+
+
+def test_k16_field_table_gives_the_mma_positions():
+    """W, W >> 2, rotr(W, 24) and rotr(W, 24) >> 2 bring exactly the fields
+    of MMA i's positions (kField of K16_POS[i]) to the mask bits: bit 4 / 20
+    (class A, low / high fp16 half) and 8 / 24 (class B)."""
+    forms = [lambda w: w, lambda w: w >> 2, lambda w: _rotr(w, 24), lambda w: _rotr(w, 24) >> 2]
+    for i, f in enumerate(forms):
+        for slot, target in enumerate((4, 20, 8, 24)):
+            src = [b for b in range(32) if f(1 << b) & (1 << target)]
+            assert src == [KFIELD[K16_POS[i][slot]]], (i, slot, src)
+    assert sorted(KFIELD) == list(range(0, 32, 2))   # 16 disjoint 2-bit fields
+
+
+def test_block_diagonal_k16_model_catches_moved_fields():
+    """The model reads field positions from the bits: exchanging the codes
+    of positions 8 and 9 (bits 28 and 0) in every word breaks the match."""
+    W = synthetic.student_t((16, 256), seed=27).numpy()
+    packed = oracle.quantize(oracle.Q2_K, W)
+    x = synthetic.normal((1, 256), seed=28).numpy()
+    ref = oracle.gemv_f64(oracle.Q2_K, packed, x, 256)
+    bound = oracle.gemv_bound(oracle.Q2_K, packed, x, 256)
+    bad_packed = packed.copy()
+    for r in range(16):
+        for s_ in range(16):
+            w = _u32(bad_packed[r], 4 * s_)
+            a, b = (w >> 28) & 3, w & 3
+            w = (w & ~((3 << 28) | 3) & 0xFFFFFFFF) | (b << 28) | a
+            bad_packed[r, 4 * s_:4 * s_ + 4] = np.frombuffer(w.to_bytes(4, "little"), np.uint8)
+    bad = _block_diagonal_k16(oracle.Q2_K, bad_packed, x[0], 1)
+    assert (np.abs(bad[None, :] - ref) > 1e-3 * bound).any()
 
 
 def test_ring_layout_matches_oracle():
