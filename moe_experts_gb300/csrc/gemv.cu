@@ -796,6 +796,7 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
         case EPQ_Q4_0: e = sw ? launch_flat<EPQ_Q4_0, true>(p, pl, s) : launch_flat<EPQ_Q4_0, false>(p, pl, s); break;
         case EPQ_Q4_1: e = sw ? launch_flat<EPQ_Q4_1, true>(p, pl, s) : launch_flat<EPQ_Q4_1, false>(p, pl, s); break;
         case EPQ_Q4_K: e = sw ? launch_flat<EPQ_Q4_K, true>(p, pl, s) : launch_flat<EPQ_Q4_K, false>(p, pl, s); break;
+        default: return EPQ_ERR_FORMAT;  // Q2_K / Q6_K took the block-diagonal engine above
       }
       if (e != cudaSuccess) return cuda_fail(e);
       continue;
@@ -805,6 +806,7 @@ epq_status gemv_launch(epq_fmt fmt, const void *blocks, const float *x, float *y
       case EPQ_Q4_0: e = dispatch_fmt<EPQ_Q4_0>(p, pl, s, true, sw); break;
       case EPQ_Q4_1: e = dispatch_fmt<EPQ_Q4_1>(p, pl, s, true, sw); break;
       case EPQ_Q4_K: e = dispatch_fmt<EPQ_Q4_K>(p, pl, s, true, sw); break;
+      default: return EPQ_ERR_FORMAT;  // as above
     }
     if (e != cudaSuccess) return cuda_fail(e);
   }
